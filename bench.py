@@ -1,0 +1,359 @@
+#!/usr/bin/env python
+"""Benchmark: compressed-KV decode attention on one GB300 (and N replicas).
+
+One step = the whole hot path once on the Llama-2-7B-shaped decode workload
+(batch 16, 32 heads, head_dim 128, context 8192, bf16, KQV at a 4-bit
+budget): append-quantise one new K/V token per sequence into slot 8191, then
+decode attention of one query per head over the 8192 compressed tokens
+(query prep, split-K decode, combine). `value` is the step's algorithmic bytes
+(packed records + norms + signs read, new records written, q, output) per
+second of device time; `append_quantize` reports the bulk append-quantise
+throughput of refilling the whole cache. Inputs are synthetic, drawn on the
+device from a seeded generator; the 587 MB cache is larger than the 129 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica (the path has no
+exchange step); rank 0 prints one JSON line.
+"""
+
+import argparse
+import json
+import math
+import os
+import signal
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compressed-KV decode attention GB/s and % of HBM peak; append-quantise tokens/s"
+CAP = 8192
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        busy = [r for r in rows if num(r[4]) > 0] or rows
+        sm = sorted(num(r[1]) for r in busy)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": num(rows[0][2]), "reasons": reasons,
+                "samples": len(busy), "power_w_max": max(num(r[3]) for r in busy)}
+
+
+class OracleDecode:
+    """The CPU oracle's decode attention on one (batch, head) unit of the workload.
+
+    Setup (untimed): the oracle encodes one head's K/V (8192 tokens) into the
+    stored-record format. Timed: unpack the records, reconstruct K and V in
+    fp64, dense softmax attention of one query."""
+
+    def __init__(self, N, bits, seed):
+        import numpy as np
+        from oracle import turboquant as otq
+        self.otq = otq
+        self.params = otq.make_params(128, bits, "KQV", seed)
+        self.rk, self.rv = self.params.roles()
+        g = np.random.default_rng(seed)
+        K = g.standard_normal((N, 128)) * np.exp(g.standard_normal(128))[None, :]
+        V = g.standard_normal((N, 128))
+        self.ek = otq.encode(K, self.rk, self.params)
+        self.ev = otq.encode(V, self.rv, self.params)
+        self.kc = otq.pack_codes(self.ek.idx, self.rk.bits)
+        self.vc, self.vs = otq.pack_codes(self.ev.idx, self.rv.bits), otq.pack_signs(self.ev.signs)
+        self.q = g.standard_normal(128)
+
+    def one_head(self):
+        from oracle import attention as oatt
+        otq = self.otq
+        ekk = otq.encoded_from_storage(self.rk, self.ek.norm, self.kc, 128)
+        evv = otq.encoded_from_storage(self.rv, self.ev.norm, self.vc, 128, self.vs, self.ev.rnorm)
+        return oatt.attend(self.q, otq.decode(ekk, self.params), otq.decode(evv, self.params))
+
+    def run(self, target_s):
+        """Decode heads until target_s seconds have passed (at least one). Returns (heads, seconds)."""
+        heads, t0 = 0, time.perf_counter()
+        while True:
+            self.one_head()
+            heads += 1
+            el = time.perf_counter() - t0
+            if el >= target_s:
+                return heads, el
+
+
+def host_threads():
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [threads])
+    except Exception:
+        pass
+    return threads
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm, on this host's cores (rank 0 only)."""
+    if rank != 0:
+        return
+    N, bits = CAP, 4
+    rec = 140  # bytes per token-head, KQV n=4
+    per_head_bytes = N * rec
+    od = OracleDecode(N, bits, 42)
+    for _ in range(args.warmup):
+        od.one_head()
+    total_heads, total_s = 0, 0.0
+    threads = host_threads()
+    for _ in range(args.steps):
+        h, s = od.run(0.0)
+        total_heads += h
+        total_s += s
+    gbs = total_heads * per_head_bytes / total_s / 1e9
+    sample = f"{total_heads} of the 512 (batch, head) decode units over {N} tokens, one per step"
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config():
+    return {"workload": "Llama-2-7B-shaped decode step: append 1 token/sequence + decode attention, "
+                        "B16 H32 d128 context 8192 bf16, KQV n=4",
+            "batch": 16, "heads_q": 32, "heads_kv": 32, "head_dim": 128, "context": CAP, "scheme": "KQV",
+            "bits": 4, "input_dtype": "bf16", "l2": "inputs larger than L2 (587 MB compressed cache > 129 MB)",
+            "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import numpy as np
+    import torch
+    from quantised_kv_cache_gb300 import build
+    from quantised_kv_cache_gb300 import tq
+    from quantised_kv_cache_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(tq.LIB_PATH):
+        build.build()
+    if dist is not None:
+        dist.barrier()
+
+    w = wl.WORKLOADS[2]
+    B, H, d = w.batch, w.heads_kv, w.d
+    ctx = tq.Context(d, w.bits, "KQV", 42)
+    cache = tq.Cache(ctx, B, H, CAP, device=dev)
+    rec = cache.record_bytes  # 140 B per token-head
+    q0, k_all, v_all = wl.generate(w, dev, seed=1002 + rank)
+    zeros = torch.zeros((B,), dtype=torch.int32, device=dev)
+
+    # ---------------- bulk append-quantise: refill the whole cache
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tq.tq_append_quantize(ctx.handle, cache, k_all, v_all, zeros)
+    torch.cuda.synchronize()
+    reps = 5
+    e0.record()
+    for _ in range(reps):
+        tq.tq_append_quantize(ctx.handle, cache, k_all, v_all, zeros)
+    e1.record()
+    torch.cuda.synchronize()
+    append_ms = e0.elapsed_time(e1) / reps
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    token_heads = B * H * CAP
+    append_bytes = token_heads * (2 * d * 2 + rec)
+    hbm_peak, peak_kind = peaks()
+
+    # ---------------- decode step
+    pool = [wl.step_token(w, s, dev) for s in range(8)]
+    lens_append = torch.full((B,), CAP - 1, dtype=torch.int32, device=dev)
+    lens_decode = torch.full((B,), CAP, dtype=torch.int32, device=dev)
+    ws = torch.empty(tq.tq_workspace_size(ctx.handle, B, w.heads_q, H, CAP, 0), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, w.heads_q, d), dtype=torch.float32, device=dev)
+
+    def step(i):
+        q, kn, vn = pool[i % len(pool)]
+        tq.tq_append_quantize(ctx.handle, cache, kn, vn, lens_append)
+        tq.tq_decode_attention(ctx.handle, cache, q, lens_decode, CAP, 0, ws, out)
+
+    step_bytes = (B * H * CAP * rec            # compressed cache read by the decode kernel
+                  + B * H * (2 * d * 2 + rec)  # new K/V token read, new records written
+                  + B * w.heads_q * d * 2      # q (bf16)
+                  + B * w.heads_q * d * 4)     # output (fp32)
+    decode_kernel_bytes = B * H * CAP * rec + B * w.heads_q * d * (2 + 4)
+
+    clocks = Clocks(local)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    K = args.steps
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        tq.tq_set_profile_events(ctx.handle, dec_ev[i][0], dec_ev[i][1])
+        step(i)
+    t_stop.record()
+    torch.cuda.synchronize()
+    tq.tq_set_profile_events(ctx.handle)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_stop)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / K
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
+    value = world * step_bytes * K / (elapsed_ms / 1e3) / 1e9
+    assert tq.tq_get_device_error(ctx.handle) == 0
+
+    # ---------------- end to end through the ABI with host buffers
+    pin = [(q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()) for q, kn, vn in pool]
+    dq = torch.empty_like(pool[0][0])
+    dk = torch.empty_like(pool[0][1])
+    dv = torch.empty_like(pool[0][2])
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = dq.numel() * dq.element_size() + dk.numel() * dk.element_size() + dv.numel() * dv.element_size()
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step(i):
+        hq, hk, hv = pin[i % len(pin)]
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        tq.tq_append_quantize(ctx.handle, cache, dk, dv, lens_append)
+        tq.tq_decode_attention(ctx.handle, cache, dq, lens_decode, CAP, 0, ws, out)
+        host_out.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(K):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * step_bytes * K / e2e_s / 1e9
+
+    line = None
+    if rank == 0:
+        achieved = decode_kernel_bytes / (dec_ms / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": workload_config(),
+            "pct_of_hbm_peak": 100.0 * (value / world) / hbm_peak,
+            "roofline": {"bound": "hbm", "kernel": "decode_tq_kernel (split-K decode attention)",
+                         "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "ms_per_launch": dec_ms,
+                         "bytes_per_launch": decode_kernel_bytes},
+            "append_quantize": {"tokens_per_s": B * CAP / (append_ms / 1e3),
+                                "token_heads_per_s": token_heads / (append_ms / 1e3),
+                                "GB_per_s": append_bytes / (append_ms / 1e3) / 1e9,
+                                "frac": append_bytes / (append_ms / 1e3) / 1e9 / hbm_peak,
+                                "ms": append_ms, "bytes": append_bytes,
+                                "what": "bulk re-quantise of all 8192 tokens x 512 heads from bf16 K/V"},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": 1e3 * e2e_s / K},
+            "gpu_launches": 5 * K,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            heads, secs = OracleDecode(CAP, w.bits, 42).run(15.0)
+            threads = host_threads()
+            line["cpu_baseline"] = {"value": heads * CAP * rec / secs / 1e9, "unit": "GB/s", "cores": threads,
+                                    "kind": "oracle",
+                                    "sample": f"{heads} (batch, head) decode units of this workload "
+                                              f"(8192 tokens each) in {secs:.1f} s"}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

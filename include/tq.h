@@ -1,0 +1,267 @@
+/*
+ * tq.h -- C ABI of libtq: TurboQuant-style KV-cache compression and decode
+ * attention read directly from the compressed cache, for one NVIDIA GB300
+ * (sm_103a). Plain pointers and sizes only; no framework types.
+ *
+ * Sources, cited by page title and section:
+ *   [TQ-stats]  "Statistical Inference and Quality Measures of KV Cache
+ *               Quantisations Inspired by TurboQuant" (technical summary:
+ *               "Theoretical framework", "Quantisation schemes",
+ *               "Main contribution 1").
+ *   [HeadQ]     "HeadQ: Model-Visible Distortion and Score-Space Correction
+ *               for KV-Cache Quantization", sections 2.1-2.2 and 3 (keys are
+ *               read through logits, values through the p-weighted sum; the
+ *               cache-write / cache-read split).
+ *   [KIVI-geom] "Your KV cache is not a bit problem but a geometry problem"
+ *               ("What quantisation error is made of", "Keys", "Values",
+ *               "The systems tax").
+ *   [KVQuant++] "KVQuant++" forum post ("Codebook design", "Fast codebook
+ *               lookup", "Deployment and use": a quantiser built from
+ *               head_dim and num_bits with compress / decompress calls).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions for every call
+ * ---------------------------------------------------------------------------
+ *  - Every function returns tq_status; nothing throws across the ABI.
+ *  - "d_" pointers are device pointers on the device that was current when
+ *    the context was created; "h_" pointers are host pointers.
+ *  - The caller owns every buffer it passes (cache planes, inputs, outputs,
+ *    workspace). The library allocates only the context's small parameter
+ *    block (codebooks, D, S, the device error word) in tq_init and frees it
+ *    in tq_destroy. The library never frees caller memory.
+ *  - Launches are asynchronous on the given stream (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream). No call synchronises except
+ *    tq_get_device_error.
+ *  - Argument errors are found on the host before any launch (TQ_ERR_ARG,
+ *    TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGN). Conditions only the device can see
+ *    (a write past a cache's capacity) set a sticky device error word and
+ *    skip the offending writes; read it with tq_get_device_error.
+ *  - A failed CUDA launch returns TQ_ERR_CUDA.
+ *
+ * ---------------------------------------------------------------------------
+ * Storage format (both the library and the independent CPU checker implement
+ * this text)
+ * ---------------------------------------------------------------------------
+ *  Cache geometry: each plane is an array over [batch][heads_kv][capacity]
+ *  token slots (row-major); a token's slot holds one fixed-size record.
+ *
+ *  Code records: a vector's d coordinates each get a b-bit index into the
+ *  Lloyd-Max codebook. Coordinate i's index occupies bits [b*i, b*i + b) of
+ *  a d*b-bit little-endian bit string (string bit k = bit k % 8 of byte
+ *  k / 8); the record is d*b/8 bytes. Index 0 is the most negative centroid.
+ *  Sign records (QJL): bit i of a d-bit string in the same order is 1 when
+ *  (S r)_i >= 0. Norm records: float32.
+ *
+ *  Per scheme, for a budget of n bits per coordinate ([TQ-stats]
+ *  "Quantisation schemes"):
+ *    TQ_SCHEME_KV   K: n-bit codes of the unrotated unit vector + norm.
+ *                   V: the same.
+ *    TQ_SCHEME_KQV  K: n-bit codes of the rotated unit vector + norm.
+ *                   V: (n-1)-bit codes of the rotated unit vector + norm
+ *                      + d sign bits + residual norm.
+ *    TQ_SCHEME_QKQV K and V: (n-1)-bit codes + norm + signs + residual norm.
+ *  Unused planes are NULL with size 0.
+ *
+ *  Quantisation of one vector x (fp32 arithmetic on the device; the CPU
+ *  checker repeats it in fp64 and codes must agree except where the exact
+ *  value lies within 1e-6 of a decision boundary):
+ *    nu = ||x||_2;   u = x / nu   (nu == 0: stored nu = 0, codes of u = 0,
+ *                                  all sign bits 1, rho = 0)
+ *    y  = H_d D u  for rotated schemes (D = seeded +/-1 diagonal, H_d the
+ *                  orthonormal Sylvester Hadamard in natural order); y = u
+ *                  for TQ_SCHEME_KV
+ *    idx_i = number of codebook boundaries b_j with y_i >= b_j
+ *    QJL:  r = y - c[idx] (unit domain), sign_i = [(S r)_i >= 0],
+ *          rho = nu * ||r||   (stored float32)
+ *  Codebook: the Lloyd-Max quantiser of the density (1 - t^2)^((d-3)/2) on
+ *  [-1, 1] ([KVQuant++] "Codebook design"; [TQ-stats] "Theoretical
+ *  framework"), fitted in fp64 and stored as float32 (centroids and midpoint
+ *  boundaries, each rounded to nearest).
+ *  Method randomness: SplitMix64 (Steele, Lea & Flood 2014) evaluated at
+ *  counter c: w(seed, c) = mix64(seed + c * 0x9E3779B97F4A7C15 mod 2^64),
+ *  c = stream * 2^32 + i + 1.  D_i = (w(seed, 1<<32 | i) >> 63) ? -1 : +1.
+ *  S (d x d, row-major entry k = row*d + col) uses stream 2:
+ *  u1 = ((w_{2k} >> 11) + 1) 2^-53, u2 = (w_{2k+1} >> 11) 2^-53,
+ *  S_k = (float)(sqrt(-2 log u1) * cos(2 pi u2)) in double precision.
+ *
+ *  Reconstruction ("dequantise"): x_hat = nu D H c[idx]
+ *    (+ rho sqrt(pi/2)/d D H S^T sigma, sigma_i = +/-1, for sketched vectors;
+ *     D and H dropped for TQ_SCHEME_KV).
+ *
+ *  KIVI records (TQ_SCHEME_KIVI, [KIVI-geom]): 2-bit codes per element in the
+ *  same bit-string layout (d/4 bytes per token) for both K and V; float16
+ *  (zero, step) pairs per group, zero = fp16(group min), step =
+ *  fp16((max - min) / 3) with the quotient in fp64, code =
+ *  clamp(round_half_even((x - zero) / step), 0, 3) (0 when step == 0).
+ *  A per-channel tensor groups `group` consecutive quantised tokens of one
+ *  channel: stats plane [batch][heads_kv][capacity/group][d][2] halves.
+ *  A per-token tensor groups `group` consecutive channels of one token:
+ *  stats plane [batch][heads_kv][capacity][d/group][2] halves.
+ *  The most recent tokens stay in a bfloat16 window: ring buffer
+ *  [batch][heads_kv][window + group][d], token t in slot t % (window+group).
+ *  After a sequence holds N tokens, its first nq = group*floor((N-window)/
+ *  group) tokens (0 while N < window + group) are quantised and tokens
+ *  [nq, N) are in the window.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_ABI_VERSION 1
+
+typedef struct tq_ctx tq_ctx; /* opaque, host-owned */
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_ARG = 1,         /* a null pointer, a negative size, a bad enum value */
+  TQ_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement   */
+  TQ_ERR_CAPACITY = 3,    /* (device) an append ran past a cache's capacity  */
+  TQ_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed            */
+  TQ_ERR_TIMEOUT = 5,     /* (device) a bounded wait gave up                 */
+  TQ_ERR_STATE = 6,       /* the call does not fit the context's scheme      */
+  TQ_ERR_ALIGN = 7,       /* a pointer is not 16-byte aligned                */
+  TQ_ERR_WORKSPACE = 8    /* the workspace is smaller than tq_workspace_size */
+} tq_status;
+
+typedef enum {
+  TQ_SCHEME_KV = 0,
+  TQ_SCHEME_KQV = 1,
+  TQ_SCHEME_QKQV = 2,
+  TQ_SCHEME_KIVI = 3
+} tq_scheme;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
+
+/* Device pointers to the planes of one cache. Sizes come from
+ * tq_cache_sizes; a plane whose size is 0 is unused and may be NULL. Every
+ * non-NULL plane must be 16-byte aligned. */
+typedef struct tq_cache {
+  int batch, heads_kv, capacity;
+  uint8_t *k_codes;  float *k_norm;  uint8_t *k_signs;  float *k_rnorm;
+  uint8_t *v_codes;  float *v_norm;  uint8_t *v_signs;  float *v_rnorm;
+  uint16_t *k_stats; uint16_t *v_stats;      /* KIVI: fp16 (zero, step) */
+  uint16_t *k_window; uint16_t *v_window;    /* KIVI: bf16 ring buffers */
+} tq_cache;
+
+typedef struct tq_cache_sizes {
+  size_t k_codes, k_norm, k_signs, k_rnorm;
+  size_t v_codes, v_norm, v_signs, v_rnorm;
+  size_t k_stats, v_stats, k_window, v_window;
+  size_t record_bytes; /* algorithmic bytes of one token-head (K + V records) */
+} tq_cache_sizes;
+
+/* ABI version of the loaded library (TQ_ABI_VERSION it was built with). */
+int tq_abi_version(void);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char *tq_status_str(int status);
+
+/* Create a context ([KVQuant++] "Deployment and use": a quantiser from
+ * head_dim and num_bits; [TQ-stats] "Quantisation schemes": the scheme and
+ * its budget). d: head dimension (this build: 128). bits: the budget n in
+ * bits per coordinate, 2..4 (TQ_SCHEME_KIVI: must be 2). scheme: a
+ * tq_scheme. seed: selects D and S. Fits the needed codebooks on the host
+ * (fp64), draws D and S, copies them to the current device.
+ * *out receives the handle (NULL on failure). */
+tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out);
+
+/* Free the context's device parameter block and the handle. NULL is a no-op. */
+void tq_destroy(tq_ctx *ctx);
+
+/* KIVI options ([KIVI-geom]): group size (32), full-precision window length
+ * (128, a multiple of group), and the grouping axes: k_per_channel = 1 groups
+ * keys along tokens per channel, 0 along channels per token; v_per_token = 1
+ * groups values along channels per token, 0 along tokens per channel. Call
+ * before sizing or using a cache; TQ_ERR_STATE for other schemes. */
+tq_status tq_set_kivi(tq_ctx *ctx, int group, int window, int k_per_channel, int v_per_token);
+
+/* Byte sizes of every plane of a cache of `capacity` token slots for
+ * [batch][heads_kv] sequences-heads. KIVI: capacity must be a multiple of
+ * the group. */
+tq_status tq_cache_sizes_get(const tq_ctx *ctx, int batch, int heads_kv, int capacity,
+                             tq_cache_sizes *out);
+
+/* Quantise and write n_new tokens per sequence ([HeadQ] 3, "cache write";
+ * [KIVI-geom] "The systems tax": per-token append).
+ *   d_k, d_v : [batch][heads_kv][n_new][d] contiguous, dtype TQ_F32 or TQ_BF16
+ *   d_seq_lens : int32 [batch], the current length of each sequence; token t
+ *                of sequence b goes to slot d_seq_lens[b] + t. The library
+ *                does not advance it: the caller adds n_new afterwards, in
+ *                stream order.
+ * A sequence whose slots would exceed the capacity is skipped and the
+ * device error word is set to TQ_ERR_CAPACITY. KIVI: keeps the window rule
+ * stated above (groups leave the window when it reaches window + group). */
+tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const void *d_k,
+                             const void *d_v, int dtype, int batch, int heads_kv, int n_new,
+                             const int32_t *d_seq_lens, void *stream);
+
+/* Workspace bytes tq_decode_attention needs for these sizes (split-K
+ * partials and the prepared queries). splits = 0 asks for the library's
+ * choice for max_len. */
+tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len,
+                            int splits, size_t *out);
+
+/* Decode attention read straight from the compressed cache ([HeadQ] 2.1-2.2;
+ * [TQ-stats] "Theoretical framework": keys through the logits, values
+ * linearly):  out[b][h] = softmax(q[b][h] . K_hat^T / sqrt(d)) V_hat over the
+ * first d_seq_lens[b] tokens of KV head h / (heads_q / heads_kv).
+ *   d_q   : [batch][heads_q][d], dtype TQ_F32 or TQ_BF16
+ *   d_seq_lens : int32 [batch], each in [1, max_len], max_len <= capacity
+ *   splits: token chunks per (batch, kv head); 0 = library's choice
+ *   d_workspace : >= tq_workspace_size(...) bytes, 16-byte aligned, no
+ *                 initial contents required
+ *   d_out : float32 [batch][heads_q][d]
+ * heads_q must be a multiple of heads_kv with heads_q / heads_kv <= 8. */
+tq_status tq_decode_attention(const tq_ctx *ctx, const tq_cache *cache, const void *d_q, int q_dtype,
+                              int batch, int heads_q, int heads_kv, const int32_t *d_seq_lens,
+                              int max_len, int splits, void *d_workspace, size_t workspace_bytes,
+                              float *d_out, void *stream);
+
+/* Reconstruct tokens [t0, t1) of every (batch, kv head) into fp32
+ * ([KVQuant++] "Deployment and use": decompress). d_k_hat / d_v_hat:
+ * [batch][heads_kv][t1 - t0][d] (either may be NULL to skip). For KIVI the
+ * window tokens are returned as stored (bf16 values). d_seq_lens (KIVI only,
+ * may be NULL otherwise) gives each sequence's length so the quantised/window
+ * split is known. */
+tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int heads_kv, int t0,
+                        int t1, const int32_t *d_seq_lens, float *d_k_hat, float *d_v_hat,
+                        void *stream);
+
+/* Copy the context's float32 parameters to host buffers (any may be NULL):
+ * the codebook used for K and for V (centroids: 2^bits floats, boundaries:
+ * 2^bits - 1 floats, for the widths *h_k_bits / *h_v_bits), D (d int8) and
+ * S (d*d floats, row-major). */
+tq_status tq_export_params(const tq_ctx *ctx, int *h_k_bits, float *h_k_centroids, float *h_k_bounds,
+                           int *h_v_bits, float *h_v_centroids, float *h_v_bounds, int8_t *h_diag,
+                           float *h_sketch);
+
+/* Host utility: the fp64 Lloyd-Max codebook for dimension d and width bits
+ * (1..4): 2^bits centroids ascending and 2^bits - 1 midpoint boundaries. */
+tq_status tq_codebook_f64(int d, int bits, double *h_centroids, double *h_bounds);
+
+/* Host utility: the method randomness a context created with `seed` uses,
+ * drawn by the SplitMix64 / Box-Muller recipe above: D (d int8, +/-1) and S
+ * (d*d floats, row-major). Either output may be NULL. */
+tq_status tq_draw_params(uint64_t seed, int d, int8_t *h_diag, float *h_sketch);
+
+/* Instrumentation: when set (non-NULL cudaEvent_t handles passed as void*),
+ * every later tq_decode_attention records `start` just before its split-K
+ * decode kernel and `stop` just after it, on the call's stream, and every
+ * tq_append_quantize records `append_start` / `append_stop` around its
+ * quantise kernels. Pass NULLs to stop. The caller owns the events. */
+tq_status tq_set_profile_events(tq_ctx *ctx, void *start, void *stop, void *append_start, void *append_stop);
+
+/* Synchronise `stream`, then read and clear the context's sticky device
+ * error word into *code (TQ_OK when nothing was recorded). */
+tq_status tq_get_device_error(const tq_ctx *ctx, void *stream, int *code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

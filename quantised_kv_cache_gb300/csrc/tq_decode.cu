@@ -1,0 +1,644 @@
+// Decode attention read straight from the compressed cache.
+//
+//   o = softmax(q K_hat^T / sqrt(d)) V_hat
+// with K_hat and V_hat never materialised: keys are read through logits
+// ("HeadQ", 2.1: a key enters attention only through q^T k / sqrt(d)) and
+// values through the p-weighted sum, which is linear ("HeadQ", 2.2; "Statistical
+// Inference ... Inspired by TurboQuant", technical summary, "K-V asymmetry").
+// Linearity lets the value side stay in the rotated, unit-codebook domain:
+//   sum_j p_j v_hat_j = D H ( sum_j p_j nu_j c[idx_j]
+//                             + sqrt(pi/2)/m S^T sum_j p_j rho_j sigma_j ),
+// so each head needs one S^T matvec and one inverse WHT after the token loop.
+// For sketched keys (QKQV) the score adds the QJL correction
+//   rho_j sqrt(pi/2)/m <S q_rot, sigma_j>  ("Main contribution 1").
+//
+// Three launches, stream-ordered:
+//   qprep   -- q_rot = H D q / sqrt(d) (and S q_rot for sketched keys)
+//   decode  -- one CTA per (batch, kv head, token chunk): online softmax over
+//              the chunk, partial (m, l, sum p nu c, sum p rho sigma)
+//   combine -- merge the chunks of each query head, S^T, inverse WHT.
+
+#include <cuda_fp16.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kDecodeWarps = 4;
+constexpr int kTile = 8;  // tokens per warp step
+
+struct PrepArgs {
+  const void *q;
+  int bf16, batch, heads_q, rotate, sketch_k;
+  const float *diag;
+  const float *sketch;
+  float *qprep;  // [batch*heads_q][2][128]
+};
+
+// one warp per (batch, query head)
+__global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
+  __shared__ float s_q[4][kD];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  const bool live = row < a.batch * a.heads_q;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (live) load4(a.q, (size_t)row * kD + 4 * lane, a.bf16 != 0, v);
+  if (a.rotate) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] *= __ldg(a.diag + 4 * lane + j);
+    wht128(v, lane);
+  }
+  if (live) {
+    float4 o = make_float4(v[0] * kInvSqrtD, v[1] * kInvSqrtD, v[2] * kInvSqrtD, v[3] * kInvSqrtD);
+    reinterpret_cast<float4 *>(a.qprep + (size_t)row * 2 * kD)[lane] = o;
+  }
+  if (!a.sketch_k) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) s_q[warp][4 * lane + j] = v[j];
+  __syncwarp();
+  // (S q_rot)_k for k = lane + 32 m
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = 0; i < kD; ++i) {
+    const float qi = s_q[warp][i];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) acc[m] = fmaf(__ldg(a.sketch + (lane + 32 * m) * kD + i), qi, acc[m]);
+  }
+  if (live) {
+    const float c = kSqrtHalfPi / kD * kInvSqrtD;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) a.qprep[(size_t)row * 2 * kD + kD + lane + 32 * m] = acc[m] * c;
+  }
+}
+
+struct DecodeKernelArgs {
+  const uint8_t *k_codes;
+  const float *k_norm;
+  const uint8_t *k_signs;
+  const float *k_rnorm;
+  const uint8_t *v_codes;
+  const float *v_norm;
+  const uint8_t *v_signs;
+  const float *v_rnorm;
+  int capacity, heads_kv, heads_q, chunk, splits;
+  const int32_t *seq_lens;
+  const float *qprep;
+  float *partials;
+  const float *k_centroids;
+  const float *v_centroids;
+};
+
+// lane -> token (0..7) after the 8-way reduce-scatter below, and back
+__device__ __forceinline__ int tile_token_of_lane(int lane) {
+  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
+__device__ __forceinline__ int lane_of_tile_token(int jj) {
+  return ((jj >> 2) & 1) * 16 + ((jj >> 1) & 1) * 8 + (jj & 1) * 4;
+}
+
+// Sum eight per-lane partials over the warp; lane ends with the sum for token
+// tile_token_of_lane(lane). 9 shuffles instead of 40 for eight full reductions.
+__device__ __forceinline__ float reduce8(const float (&p)[kTile], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float k1[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float send = b4 ? p[k] : p[k + 4];
+    const float keep = b4 ? p[k + 4] : p[k];
+    k1[k] = keep + __shfl_xor_sync(kFull, send, 16);
+  }
+  float k2[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float send = b3 ? k1[k] : k1[k + 2];
+    const float keep = b3 ? k1[k + 2] : k1[k];
+    k2[k] = keep + __shfl_xor_sync(kFull, send, 8);
+  }
+  const float send = b2 ? k2[0] : k2[1];
+  float s = (b2 ? k2[1] : k2[0]) + __shfl_xor_sync(kFull, send, 4);
+  s += __shfl_xor_sync(kFull, s, 2);
+  s += __shfl_xor_sync(kFull, s, 1);
+  return s;
+}
+
+template <int KB, int VB, bool KQJL, bool VQJL, int G>
+__global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKernelArgs a) {
+  __shared__ float s_cb[32];  // [0,16) K centroids, [16,32) V centroids
+  __shared__ float s_m[kDecodeWarps][G], s_l[kDecodeWarps][G];
+  __shared__ float s_acc[kDecodeWarps][G][kD];
+  __shared__ float s_sacc[VQJL ? kDecodeWarps : 1][G][VQJL ? kD : 1];
+
+  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < 16) s_cb[tid] = a.k_centroids[tid];
+  else if (tid < 32) s_cb[tid] = a.v_centroids[tid - 16];
+
+  const int len = min(max(__ldg(a.seq_lens + b), 0), a.capacity);
+  const int t_begin = split * a.chunk;
+  const int t_end = min(t_begin + a.chunk, len);
+
+  float qv[G][4], sq[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float *qp = a.qprep + ((size_t)b * a.heads_q + hk * G + g) * 2 * kD;
+    const float4 q4 = __ldg(reinterpret_cast<const float4 *>(qp) + lane);
+    qv[g][0] = q4.x; qv[g][1] = q4.y; qv[g][2] = q4.z; qv[g][3] = q4.w;
+    if (KQJL) {
+      const float4 s4 = __ldg(reinterpret_cast<const float4 *>(qp + kD) + lane);
+      sq[g][0] = s4.x; sq[g][1] = s4.y; sq[g][2] = s4.z; sq[g][3] = s4.w;
+    }
+  }
+  __syncthreads();
+
+  float m[G], l[G], acc[G][4], sacc[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[g][j] = sacc[g][j] = 0.f;
+  }
+
+  const size_t slot0 = ((size_t)b * a.heads_kv + hk) * a.capacity;
+  const uint32_t *kc = reinterpret_cast<const uint32_t *>(a.k_codes) + slot0 * (KB * 4);
+  const uint32_t *vc = reinterpret_cast<const uint32_t *>(a.v_codes) + slot0 * (VB * 4);
+  const uint32_t *ks = KQJL ? reinterpret_cast<const uint32_t *>(a.k_signs) + slot0 * 4 : nullptr;
+  const uint32_t *vs = VQJL ? reinterpret_cast<const uint32_t *>(a.v_signs) + slot0 * 4 : nullptr;
+  const float *kn = a.k_norm + slot0, *vn = a.v_norm + slot0;
+  const float *kr = KQJL ? a.k_rnorm + slot0 : nullptr;
+  const float *vr = VQJL ? a.v_rnorm + slot0 : nullptr;
+  const int my_tok = tile_token_of_lane(lane);
+  constexpr uint32_t kMaskK = (1u << KB) - 1, kMaskV = (1u << VB) - 1;
+  const int sign_shift = (4 * lane) & 31, sign_word = lane >> 3;
+
+  for (int tile = t_begin + warp * kTile; tile < t_end; tile += kDecodeWarps * kTile) {
+    // ---- scores for 8 tokens
+    float part[G][kTile];
+#pragma unroll
+    for (int jj = 0; jj < kTile; ++jj) {
+      const int t = min(tile + jj, t_end - 1);
+      const uint32_t f = lane_code_field<KB>(kc + (size_t)t * (KB * 4), lane);
+      float c[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[j] = s_cb[(f >> (KB * j)) & kMaskK];
+      const float nu = __ldg(kn + t);
+      float sg[4];
+      float rk = 0.f;
+      if (KQJL) {
+        const uint32_t sw = __ldg(ks + (size_t)t * 4 + sign_word) >> sign_shift;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sg[j] = ((sw >> j) & 1u) ? 1.f : -1.f;
+        rk = __ldg(kr + t);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float s = qv[g][0] * c[0] + qv[g][1] * c[1] + qv[g][2] * c[2] + qv[g][3] * c[3];
+        s *= nu;
+        if (KQJL) s += rk * (sq[g][0] * sg[0] + sq[g][1] * sg[1] + sq[g][2] * sg[2] + sq[g][3] * sg[3]);
+        part[g][jj] = s;
+      }
+    }
+    // ---- online softmax over the 8 tokens
+    const bool valid = tile + my_tok < t_end;
+    float p[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float s = reduce8(part[g], lane);
+      s = valid ? s : -INFINITY;
+      float tmax = fmaxf(s, __shfl_xor_sync(kFull, s, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+      const float mnew = fmaxf(m[g], tmax);  // finite: token `tile` is valid
+      const float scale = __expf(m[g] - mnew);
+      p[g] = valid ? __expf(s - mnew) : 0.f;
+      float psum = p[g] + __shfl_xor_sync(kFull, p[g], 4);
+      psum += __shfl_xor_sync(kFull, psum, 8);
+      psum += __shfl_xor_sync(kFull, psum, 16);
+      l[g] = l[g] * scale + psum;
+      m[g] = mnew;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[g][j] *= scale;
+        if (VQJL) sacc[g][j] *= scale;
+      }
+    }
+    // ---- values, in the rotated unit domain
+#pragma unroll
+    for (int jj = 0; jj < kTile; ++jj) {
+      const int t = tile + jj;
+      if (t >= t_end) break;
+      const int src = lane_of_tile_token(jj);
+      const uint32_t f = lane_code_field<VB>(vc + (size_t)t * (VB * 4), lane);
+      float c[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[j] = s_cb[16 + ((f >> (VB * j)) & kMaskV)];
+      const float nu = __ldg(vn + t);
+      uint32_t sw = 0;
+      float rv = 0.f;
+      if (VQJL) {
+        sw = __ldg(vs + (size_t)t * 4 + sign_word) >> sign_shift;
+        rv = __ldg(vr + t);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float pj = __shfl_sync(kFull, p[g], src);
+        const float w = pj * nu;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w, c[j], acc[g][j]);
+        if (VQJL) {
+          const float wr = pj * rv;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sacc[g][j] += ((sw >> j) & 1u) ? wr : -wr;
+        }
+      }
+    }
+  }
+
+  // ---- merge the four warps of the CTA
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      s_m[warp][g] = m[g];
+      s_l[warp][g] = l[g];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      s_acc[warp][g][4 * lane + j] = acc[g][j];
+      if (VQJL) s_sacc[warp][g][4 * lane + j] = sacc[g][j];
+    }
+  }
+  __syncthreads();
+  const int i = tid;  // coordinate
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, s_m[w][g]);
+    float L = 0.f, A = 0.f, Sg = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float e = (s_m[w][g] == -INFINITY) ? 0.f : __expf(s_m[w][g] - M);
+      L += s_l[w][g] * e;
+      A += s_acc[w][g][i] * e;
+      if (VQJL) Sg += s_sacc[w][g][i] * e;
+    }
+    float *rec = a.partials + (((size_t)b * a.heads_q + hk * G + g) * a.splits + split) * kPartialFloats;
+    if (i == 0) {
+      rec[0] = M;
+      rec[1] = L;
+    }
+    rec[2 + i] = A;
+    rec[2 + kD + i] = Sg;
+  }
+}
+
+struct CombineArgs {
+  int batch, heads_q, splits, rotate, sketch_v;
+  const float *partials;
+  const float *diag;
+  const float *sketch;
+  float *out;
+};
+
+// one CTA (128 threads, thread = coordinate) per (batch, query head)
+__global__ void __launch_bounds__(128) combine_tq_kernel(CombineArgs a) {
+  __shared__ float s_sig[kD];
+  __shared__ float s_o[kD];
+  const int row = blockIdx.x, i = threadIdx.x;
+  const float *base = a.partials + (size_t)row * a.splits * kPartialFloats;
+  float M = -INFINITY;
+  for (int s = 0; s < a.splits; ++s) M = fmaxf(M, __ldg(base + (size_t)s * kPartialFloats));
+  float L = 0.f, A = 0.f, Sg = 0.f;
+  for (int s = 0; s < a.splits; ++s) {
+    const float *rec = base + (size_t)s * kPartialFloats;
+    const float ms = __ldg(rec);
+    const float e = (ms == -INFINITY) ? 0.f : __expf(ms - M);
+    L += __ldg(rec + 1) * e;
+    A += __ldg(rec + 2 + i) * e;
+    if (a.sketch_v) Sg += __ldg(rec + 2 + kD + i) * e;
+  }
+  float o = A;
+  if (a.sketch_v) {
+    s_sig[i] = Sg;
+    __syncthreads();
+    float t = 0.f;
+    for (int k = 0; k < kD; ++k) t = fmaf(__ldg(a.sketch + k * kD + i), s_sig[k], t);
+    o += (kSqrtHalfPi / kD) * t;
+  }
+  o = (L > 0.f) ? o / L : 0.f;
+  if (!a.rotate) {
+    a.out[(size_t)row * kD + i] = o;
+    return;
+  }
+  s_o[i] = o;
+  __syncthreads();
+  if (i < 32) {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = s_o[4 * i + j];
+    wht128(v, i);
+    float4 r;
+    r.x = v[0] * __ldg(a.diag + 4 * i + 0);
+    r.y = v[1] * __ldg(a.diag + 4 * i + 1);
+    r.z = v[2] * __ldg(a.diag + 4 * i + 2);
+    r.w = v[3] * __ldg(a.diag + 4 * i + 3);
+    reinterpret_cast<float4 *>(a.out + (size_t)row * kD)[i] = r;
+  }
+}
+
+// ---------------------------------------------------------------- KIVI decode
+// Scores and values from 2-bit grouped codes ("Your KV cache is not a bit
+// problem but a geometry problem", "What quantisation error is made of":
+// x_hat = zero + step * code) for tokens [0, nq) and from the bfloat16 window
+// for [nq, len); same online softmax and split-K partials as above, with no
+// rotation and no sketch.
+
+struct KiviDecodeKernelArgs {
+  const uint8_t *k_codes;
+  const uint8_t *v_codes;
+  const uint16_t *k_stats;
+  const uint16_t *v_stats;
+  const uint16_t *k_ring;
+  const uint16_t *v_ring;
+  int capacity, heads_kv, heads_q, chunk, splits, window;
+  const int32_t *seq_lens;
+  const float *qprep;
+  float *partials;
+};
+
+__device__ __forceinline__ void half2_pair(uint32_t st, float &z, float &s) {
+  z = __half2float(__ushort_as_half((unsigned short)(st & 0xffffu)));
+  s = __half2float(__ushort_as_half((unsigned short)(st >> 16)));
+}
+
+// four channels 4L..4L+3 of token t: per-channel stats preloaded in (pz, ps)
+template <bool PER_CHANNEL>
+__device__ __forceinline__ void kivi_token(const uint32_t *codes, const uint32_t *stats_tok, const uint16_t *ring,
+                                           bool quantised, int t, int R, int lane, const float (&pz)[4],
+                                           const float (&ps)[4], float (&x)[4]) {
+  if (quantised) {
+    const uint32_t f = lane_code_field<2>(codes + (size_t)t * 8, lane);
+    if (PER_CHANNEL) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) x[c] = fmaf(ps[c], (float)((f >> (2 * c)) & 3u), pz[c]);
+    } else {
+      float z, s;
+      half2_pair(__ldg(stats_tok + (size_t)t * 4 + (lane >> 3)), z, s);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) x[c] = fmaf(s, (float)((f >> (2 * c)) & 3u), z);
+    }
+  } else {
+    load4(ring + (size_t)(t % R) * kD, 4 * lane, true, x);
+  }
+}
+
+template <bool KPC, bool VPT, int G>
+__global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDecodeKernelArgs a) {
+  __shared__ float s_m[kDecodeWarps][G], s_l[kDecodeWarps][G];
+  __shared__ float s_acc[kDecodeWarps][G][kD];
+  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int len = min(max(__ldg(a.seq_lens + b), 0), a.capacity);
+  const int nq = (len < a.window + 32) ? 0 : 32 * ((len - a.window) / 32);
+  const int t_begin = split * a.chunk;
+  const int t_end = min(t_begin + a.chunk, len);
+  const int R = a.window + 32;
+
+  float qv[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float4 q4 = __ldg(reinterpret_cast<const float4 *>(a.qprep + ((size_t)b * a.heads_q + hk * G + g) * 2 * kD) + lane);
+    qv[g][0] = q4.x; qv[g][1] = q4.y; qv[g][2] = q4.z; qv[g][3] = q4.w;
+  }
+  float m[G], l[G], acc[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[g][j] = 0.f;
+  }
+  const size_t bh = (size_t)b * a.heads_kv + hk;
+  const uint32_t *kc = reinterpret_cast<const uint32_t *>(a.k_codes) + bh * a.capacity * 8;
+  const uint32_t *vc = reinterpret_cast<const uint32_t *>(a.v_codes) + bh * a.capacity * 8;
+  // per-token stats: [slot][4 groups]; per-channel stats: [group][128 channels]
+  const uint32_t *ks_tok = reinterpret_cast<const uint32_t *>(a.k_stats) + bh * a.capacity * 4;
+  const uint32_t *vs_tok = reinterpret_cast<const uint32_t *>(a.v_stats) + bh * a.capacity * 4;
+  const uint32_t *ks_ch = reinterpret_cast<const uint32_t *>(a.k_stats) + bh * (a.capacity / 32) * kD;
+  const uint32_t *vs_ch = reinterpret_cast<const uint32_t *>(a.v_stats) + bh * (a.capacity / 32) * kD;
+  const uint16_t *kring = a.k_ring + bh * R * kD;
+  const uint16_t *vring = a.v_ring + bh * R * kD;
+  const int my_tok = tile_token_of_lane(lane);
+
+  for (int tile = t_begin + warp * kTile; tile < t_end; tile += kDecodeWarps * kTile) {
+    const bool quant = tile < nq;
+    float kz[4] = {0.f, 0.f, 0.f, 0.f}, kscl[4] = {0.f, 0.f, 0.f, 0.f};
+    float vz[4] = {0.f, 0.f, 0.f, 0.f}, vscl[4] = {0.f, 0.f, 0.f, 0.f};
+    if (quant && KPC) {
+      const uint4 s4 = __ldg(reinterpret_cast<const uint4 *>(ks_ch + (size_t)(tile / 32) * kD) + lane);
+      half2_pair(s4.x, kz[0], kscl[0]); half2_pair(s4.y, kz[1], kscl[1]);
+      half2_pair(s4.z, kz[2], kscl[2]); half2_pair(s4.w, kz[3], kscl[3]);
+    }
+    if (quant && !VPT) {
+      const uint4 s4 = __ldg(reinterpret_cast<const uint4 *>(vs_ch + (size_t)(tile / 32) * kD) + lane);
+      half2_pair(s4.x, vz[0], vscl[0]); half2_pair(s4.y, vz[1], vscl[1]);
+      half2_pair(s4.z, vz[2], vscl[2]); half2_pair(s4.w, vz[3], vscl[3]);
+    }
+    float part[G][kTile];
+#pragma unroll
+    for (int jj = 0; jj < kTile; ++jj) {
+      const int t = min(tile + jj, t_end - 1);
+      float x[4];
+      kivi_token<KPC>(kc, ks_tok, kring, quant, t, R, lane, kz, kscl, x);
+#pragma unroll
+      for (int g = 0; g < G; ++g) part[g][jj] = qv[g][0] * x[0] + qv[g][1] * x[1] + qv[g][2] * x[2] + qv[g][3] * x[3];
+    }
+    const bool valid = tile + my_tok < t_end;
+    float p[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float s = reduce8(part[g], lane);
+      s = valid ? s : -INFINITY;
+      float tmax = fmaxf(s, __shfl_xor_sync(kFull, s, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+      const float mnew = fmaxf(m[g], tmax);
+      const float scale = __expf(m[g] - mnew);
+      p[g] = valid ? __expf(s - mnew) : 0.f;
+      float psum = p[g] + __shfl_xor_sync(kFull, p[g], 4);
+      psum += __shfl_xor_sync(kFull, psum, 8);
+      psum += __shfl_xor_sync(kFull, psum, 16);
+      l[g] = l[g] * scale + psum;
+      m[g] = mnew;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[g][j] *= scale;
+    }
+#pragma unroll
+    for (int jj = 0; jj < kTile; ++jj) {
+      const int t = tile + jj;
+      if (t >= t_end) break;
+      float x[4];
+      kivi_token<!VPT>(vc, vs_tok, vring, quant, t, R, lane, vz, vscl, x);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float w = __shfl_sync(kFull, p[g], lane_of_tile_token(jj));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w, x[j], acc[g][j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      s_m[warp][g] = m[g];
+      s_l[warp][g] = l[g];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s_acc[warp][g][4 * lane + j] = acc[g][j];
+  }
+  __syncthreads();
+  const int i = tid;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, s_m[w][g]);
+    float L = 0.f, A = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float e = (s_m[w][g] == -INFINITY) ? 0.f : __expf(s_m[w][g] - M);
+      L += s_l[w][g] * e;
+      A += s_acc[w][g][i] * e;
+    }
+    float *rec = a.partials + (((size_t)b * a.heads_q + hk * G + g) * a.splits + split) * kPartialFloats;
+    if (i == 0) {
+      rec[0] = M;
+      rec[1] = L;
+    }
+    rec[2 + i] = A;
+    rec[2 + kD + i] = 0.f;
+  }
+}
+
+template <bool KPC, bool VPT>
+int launch_kivi_g(const KiviDecodeKernelArgs &k, int G, dim3 grid, cudaStream_t st) {
+  switch (G) {
+    case 1: decode_kivi_kernel<KPC, VPT, 1><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    case 2: decode_kivi_kernel<KPC, VPT, 2><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    case 4: decode_kivi_kernel<KPC, VPT, 4><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    case 8: decode_kivi_kernel<KPC, VPT, 8><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+  return TQ_OK;
+}
+
+template <int KB, int VB, bool KQJL, bool VQJL>
+int launch_decode_g(const DecodeKernelArgs &k, int G, dim3 grid, cudaStream_t st) {
+  switch (G) {
+    case 1: decode_tq_kernel<KB, VB, KQJL, VQJL, 1><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    case 2: decode_tq_kernel<KB, VB, KQJL, VQJL, 2><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    case 4: decode_tq_kernel<KB, VB, KQJL, VQJL, 4><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    case 8: decode_tq_kernel<KB, VB, KQJL, VQJL, 8><<<grid, kDecodeWarps * 32, 0, st>>>(k); break;
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+  return TQ_OK;
+}
+
+}  // namespace
+
+int launch_decode_tq(const DecodeArgs &a, void *stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const tq_ctx *ctx = a.ctx;
+  const int G = a.heads_q / a.heads_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return TQ_ERR_UNSUPPORTED;
+
+  PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, ctx->k.rotate, ctx->k.qjl,
+             ctx->dparams->diag, ctx->dparams->sketch, a.qprep};
+  const int rows = a.batch * a.heads_q;
+  qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
+
+  DecodeKernelArgs k{};
+  const tq_cache *c = a.cache;
+  k.k_codes = c->k_codes; k.k_norm = c->k_norm; k.k_signs = c->k_signs; k.k_rnorm = c->k_rnorm;
+  k.v_codes = c->v_codes; k.v_norm = c->v_norm; k.v_signs = c->v_signs; k.v_rnorm = c->v_rnorm;
+  k.capacity = c->capacity;
+  k.heads_kv = a.heads_kv;
+  k.heads_q = a.heads_q;
+  k.chunk = a.chunk;
+  k.splits = a.splits;
+  k.seq_lens = a.seq_lens;
+  k.qprep = a.qprep;
+  k.partials = a.partials;
+  k.k_centroids = ctx->dparams->k_centroids;
+  k.v_centroids = ctx->dparams->v_centroids;
+  dim3 grid(a.splits, a.heads_kv, a.batch);
+  const int kb = ctx->k.bits, vb = ctx->v.bits;
+  int r = TQ_ERR_UNSUPPORTED;
+  if (ctx->prof_decode_start) cudaEventRecord((cudaEvent_t)ctx->prof_decode_start, st);
+  switch (ctx->scheme) {
+    case TQ_SCHEME_KV:
+      if (kb == 2) r = launch_decode_g<2, 2, false, false>(k, G, grid, st);
+      else if (kb == 3) r = launch_decode_g<3, 3, false, false>(k, G, grid, st);
+      else if (kb == 4) r = launch_decode_g<4, 4, false, false>(k, G, grid, st);
+      break;
+    case TQ_SCHEME_KQV:
+      if (kb == 2) r = launch_decode_g<2, 1, false, true>(k, G, grid, st);
+      else if (kb == 3) r = launch_decode_g<3, 2, false, true>(k, G, grid, st);
+      else if (kb == 4) r = launch_decode_g<4, 3, false, true>(k, G, grid, st);
+      break;
+    case TQ_SCHEME_QKQV:
+      if (kb == 1) r = launch_decode_g<1, 1, true, true>(k, G, grid, st);
+      else if (kb == 2) r = launch_decode_g<2, 2, true, true>(k, G, grid, st);
+      else if (kb == 3) r = launch_decode_g<3, 3, true, true>(k, G, grid, st);
+      break;
+    default: break;
+  }
+  (void)vb;
+  if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
+  if (r != TQ_OK) return r;
+
+  CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
+                  ctx->dparams->diag, ctx->dparams->sketch, a.out};
+  combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+int launch_decode_kivi(const DecodeArgs &a, void *stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const tq_ctx *ctx = a.ctx;
+  const int G = a.heads_q / a.heads_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return TQ_ERR_UNSUPPORTED;
+  if (ctx->kivi_group != 32) return TQ_ERR_UNSUPPORTED;
+  PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, 0, 0, ctx->dparams->diag, ctx->dparams->sketch, a.qprep};
+  const int rows = a.batch * a.heads_q;
+  qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
+  const tq_cache *c = a.cache;
+  KiviDecodeKernelArgs k{};
+  k.k_codes = c->k_codes; k.v_codes = c->v_codes;
+  k.k_stats = c->k_stats; k.v_stats = c->v_stats;
+  k.k_ring = c->k_window; k.v_ring = c->v_window;
+  k.capacity = c->capacity;
+  k.heads_kv = a.heads_kv;
+  k.heads_q = a.heads_q;
+  k.chunk = a.chunk;
+  k.splits = a.splits;
+  k.window = ctx->kivi_window;
+  k.seq_lens = a.seq_lens;
+  k.qprep = a.qprep;
+  k.partials = a.partials;
+  dim3 grid(a.splits, a.heads_kv, a.batch);
+  const bool kpc = ctx->kivi_k_per_channel != 0, vpt = ctx->kivi_v_per_token != 0;
+  int r;
+  if (ctx->prof_decode_start) cudaEventRecord((cudaEvent_t)ctx->prof_decode_start, st);
+  if (kpc && vpt) r = launch_kivi_g<true, true>(k, G, grid, st);
+  else if (kpc) r = launch_kivi_g<true, false>(k, G, grid, st);
+  else if (vpt) r = launch_kivi_g<false, true>(k, G, grid, st);
+  else r = launch_kivi_g<false, false>(k, G, grid, st);
+  if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
+  if (r != TQ_OK) return r;
+  CombineArgs cmb{a.batch, a.heads_q, a.splits, 0, 0, a.partials, ctx->dparams->diag, ctx->dparams->sketch, a.out};
+  combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace tq

@@ -1,0 +1,93 @@
+// Dequantise ("decompress", "KVQuant++" forum post, "Deployment and use"):
+//   x_hat = nu D H c[idx]  (+ rho sqrt(pi/2)/m D H S^T sigma for sketched vectors)
+// The sketch term is the QJL reconstruction of the residual ("Statistical
+// Inference ... Inspired by TurboQuant", technical summary, "Main contribution
+// 1"). One warp per vector, lane L owning coordinates 4L..4L+3. Used for
+// reconstruction-quality measurements and tests, not on the decode path.
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace {
+
+struct DequantKernelArgs {
+  const uint8_t *codes;
+  const float *norms;
+  const uint8_t *signs;
+  const float *rnorms;
+  int batch, heads, capacity, t0, t1;
+  const float *centroids;
+  const float *diag;
+  const float *sketch;
+  float *out;
+};
+
+template <int BITS, bool ROT, bool QJL>
+__global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
+  __shared__ float s_c[16];
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < (1 << BITS)) s_c[threadIdx.x] = a.centroids[threadIdx.x];
+  __syncthreads();
+  const int n = a.t1 - a.t0;
+  const long long total = (long long)a.batch * a.heads * n;
+  const long long vec = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (vec >= total) return;
+  const long long bh = vec / n;
+  const int t = a.t0 + (int)(vec % n);
+  const size_t slot = (size_t)bh * a.capacity + t;
+  const uint32_t f = lane_code_field<BITS>(reinterpret_cast<const uint32_t *>(a.codes) + slot * (BITS * 4), lane);
+  const float nu = __ldg(a.norms + slot);
+  float y[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) y[j] = nu * s_c[(f >> (BITS * j)) & ((1u << BITS) - 1)];
+  if (QJL) {
+    const uint32_t *srec = reinterpret_cast<const uint32_t *>(a.signs) + slot * 4;
+    uint32_t sw[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) sw[w] = __ldg(srec + w);
+    float r[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < kD; ++k) {
+      const float sg = ((sw[k >> 5] >> (k & 31)) & 1u) ? 1.f : -1.f;
+      const float4 s = __ldg(reinterpret_cast<const float4 *>(a.sketch + k * kD) + lane);
+      r[0] = fmaf(s.x, sg, r[0]);
+      r[1] = fmaf(s.y, sg, r[1]);
+      r[2] = fmaf(s.z, sg, r[2]);
+      r[3] = fmaf(s.w, sg, r[3]);
+    }
+    const float rho = __ldg(a.rnorms + slot) * (kSqrtHalfPi / kD);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) y[j] = fmaf(rho, r[j], y[j]);
+  }
+  if (ROT) {
+    wht128(y, lane);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) y[j] *= __ldg(a.diag + 4 * lane + j);
+  }
+  reinterpret_cast<float4 *>(a.out + (size_t)vec * kD)[lane] = make_float4(y[0], y[1], y[2], y[3]);
+}
+
+template <bool ROT, bool QJL>
+int go(int bits, const DequantKernelArgs &k, unsigned blocks, cudaStream_t st) {
+  switch (bits) {
+    case 1: dequant_tq_kernel<1, ROT, QJL><<<blocks, 256, 0, st>>>(k); break;
+    case 2: dequant_tq_kernel<2, ROT, QJL><<<blocks, 256, 0, st>>>(k); break;
+    case 3: dequant_tq_kernel<3, ROT, QJL><<<blocks, 256, 0, st>>>(k); break;
+    case 4: dequant_tq_kernel<4, ROT, QJL><<<blocks, 256, 0, st>>>(k); break;
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_dequant_tq(const DequantArgs &a, void *stream) {
+  DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.batch, a.heads, a.capacity, a.t0, a.t1,
+                      a.centroids, a.params->diag, a.params->sketch, a.out};
+  const long long total = (long long)a.batch * a.heads * (a.t1 - a.t0);
+  const unsigned blocks = (unsigned)((total + 7) / 8);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (a.role.qjl) return a.role.rotate ? go<true, true>(a.role.bits, k, blocks, st) : TQ_ERR_UNSUPPORTED;
+  return a.role.rotate ? go<true, false>(a.role.bits, k, blocks, st) : go<false, false>(a.role.bits, k, blocks, st);
+}
+
+}  // namespace tq

@@ -1,0 +1,563 @@
+// Host side of libtq: context creation (codebook fit, method randomness),
+// cache sizing, argument validation and dispatch to the CUDA launchers.
+//
+// Codebook: Lloyd-Max quantiser of the unit-sphere coordinate marginal
+// f(t) ~ (1 - t^2)^((d-3)/2) ("KVQuant++" forum post, "Codebook design";
+// "Statistical Inference and Quality Measures of KV Cache Quantisations
+// Inspired by TurboQuant", technical summary, "Theoretical framework" and
+// "Quantisation schemes"). Cell masses and first moments are integrated with
+// composite Gauss-Legendre quadrature in fp64; the Lloyd iteration alternates
+// midpoint boundaries and conditional-mean centroids until no centroid moves
+// by more than 1e-15 (or the step stalls at the fp64 noise floor).
+//
+// Method randomness: SplitMix64 (Steele, Lea & Flood, OOPSLA 2014) at counter
+// stream*2^32 + i + 1; D from the top bit of stream 1, S by the cosine branch
+// of Box-Muller on stream 2, evaluated in double with libm, rounded to float.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <utility>
+#include <vector>
+
+#include "tq_internal.h"
+
+namespace {
+
+// ---------------------------------------------------------------- SplitMix64
+
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+
+uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+uint64_t draw(uint64_t seed, uint64_t stream, uint64_t i) {
+  uint64_t counter = (stream << 32) + i + 1;
+  return mix64(seed + counter * kGamma);
+}
+
+void make_diag(uint64_t seed, int d, int8_t *out) {
+  for (int i = 0; i < d; ++i) out[i] = (draw(seed, 1, i) >> 63) ? -1 : 1;
+}
+
+void make_sketch(uint64_t seed, int d, float *out) {
+  const double scale = std::ldexp(1.0, -53);
+  const double two_pi = 2.0 * M_PI;
+  for (int k = 0; k < d * d; ++k) {
+    uint64_t w1 = draw(seed, 2, 2 * (uint64_t)k);
+    uint64_t w2 = draw(seed, 2, 2 * (uint64_t)k + 1);
+    double u1 = (double)((w1 >> 11) + 1) * scale;
+    double u2 = (double)(w2 >> 11) * scale;
+    out[k] = (float)(std::sqrt(-2.0 * std::log(u1)) * std::cos(two_pi * u2));
+  }
+}
+
+// ---------------------------------------------------------------- codebook
+
+struct GaussLegendre {
+  std::vector<double> x, w;  // nodes/weights on [-1, 1]
+  explicit GaussLegendre(int n) : x(n), w(n) {
+    for (int i = 0; i < n; ++i) {
+      double z = std::cos(M_PI * (i + 0.75) / (n + 0.5));
+      for (int it = 0; it < 100; ++it) {
+        double p0 = 1.0, p1 = z;
+        for (int k = 2; k <= n; ++k) {
+          double p2 = ((2.0 * k - 1.0) * z * p1 - (k - 1.0) * p0) / k;
+          p0 = p1;
+          p1 = p2;
+        }
+        double dp = n * (z * p1 - p0) / (z * z - 1.0);
+        double dz = p1 / dp;
+        z -= dz;
+        if (std::fabs(dz) < 1e-16) {
+          // recompute the derivative at the converged node for the weight
+          double q0 = 1.0, q1 = z;
+          for (int k = 2; k <= n; ++k) {
+            double q2 = ((2.0 * k - 1.0) * z * q1 - (k - 1.0) * q0) / k;
+            q0 = q1;
+            q1 = q2;
+          }
+          dp = n * (z * q1 - q0) / (z * z - 1.0);
+          x[i] = z;
+          w[i] = 2.0 / ((1.0 - z * z) * dp * dp);
+          break;
+        }
+      }
+    }
+  }
+};
+
+// (mass, first moment) of the unnormalised density g(t) = (1 - t^2)^e on [lo, hi]
+std::pair<double, double> cell_integrals(double lo, double hi, double e, const GaussLegendre &gl) {
+  if (hi <= lo) return {0.0, 0.0};
+  const double panel = 1.0 / 32.0;
+  int panels = std::max(1, (int)std::ceil((hi - lo) / panel));
+  double h = (hi - lo) / panels;
+  double mass = 0.0, mom = 0.0;
+  for (int p = 0; p < panels; ++p) {
+    double a = lo + p * h;
+    double mid = a + 0.5 * h, half = 0.5 * h;
+    for (size_t i = 0; i < gl.x.size(); ++i) {
+      double t = mid + half * gl.x[i];
+      double g = std::exp(e * std::log1p(-t * t));
+      mass += gl.w[i] * half * g;
+      mom += gl.w[i] * half * g * t;
+    }
+  }
+  return {mass, mom};
+}
+
+struct Codebook64 {
+  std::vector<double> c, b;
+};
+
+Codebook64 fit_lloyd_max(int d, int bits) {
+  static const GaussLegendre gl(24);
+  const int L = 1 << bits;
+  const double e = 0.5 * (d - 3);
+  const double sigma = 1.0 / std::sqrt((double)d);
+  std::vector<double> c(L), cn(L), edges(L + 1);
+  for (int i = 0; i < L; ++i) c[i] = sigma * 2.5 * ((2.0 * (i + 0.5) / L) - 1.0);
+  double best = INFINITY;
+  int since_best = 0;
+  for (int it = 0; it < 400000; ++it) {
+    edges[0] = -1.0;
+    edges[L] = 1.0;
+    for (int i = 1; i < L; ++i) edges[i] = 0.5 * (c[i - 1] + c[i]);
+    double step = 0.0;
+    for (int i = 0; i < L; ++i) {
+      auto mm = cell_integrals(edges[i], edges[i + 1], e, gl);
+      cn[i] = mm.second / mm.first;
+      step = std::max(step, std::fabs(cn[i] - c[i]));
+    }
+    c.swap(cn);
+    if (step < 1e-15) break;
+    if (step < best) {
+      best = step;
+      since_best = 0;
+    } else if (++since_best > 2000) {
+      break;
+    }
+  }
+  Codebook64 out;
+  out.c.resize(L);
+  for (int i = 0; i < L; ++i) out.c[i] = 0.5 * (c[i] - c[L - 1 - i]);
+  out.b.resize(L - 1);
+  for (int i = 0; i + 1 < L; ++i) out.b[i] = 0.5 * (out.c[i] + out.c[i + 1]);
+  out.b[L / 2 - 1] = 0.0;
+  return out;
+}
+
+const Codebook64 &cached_codebook(int d, int bits) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, Codebook64> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(d, bits);
+  auto it = cache.find(key);
+  if (it == cache.end()) it = cache.emplace(key, fit_lloyd_max(d, bits)).first;
+  return it->second;
+}
+
+// ---------------------------------------------------------------- helpers
+
+bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+tq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+bool is_tq_scheme(int s) { return s == TQ_SCHEME_KV || s == TQ_SCHEME_KQV || s == TQ_SCHEME_QKQV; }
+
+void roles_for(int scheme, int n, tq::Role *k, tq::Role *v) {
+  switch (scheme) {
+    case TQ_SCHEME_KV: *k = {n, false, false}; *v = {n, false, false}; break;
+    case TQ_SCHEME_KQV: *k = {n, true, false}; *v = {n - 1, true, true}; break;
+    case TQ_SCHEME_QKQV: *k = {n - 1, true, true}; *v = {n - 1, true, true}; break;
+    default: *k = {2, false, false}; *v = {2, false, false}; break;  // KIVI
+  }
+}
+
+size_t code_bytes(int bits, int d) { return (size_t)bits * d / 8; }
+
+}  // namespace
+
+namespace tq {
+
+void choose_splits(int batch, int heads_kv, int max_len, int requested, int *splits, int *chunk) {
+  int s = requested;
+  if (s <= 0) {
+    // enough CTAs for several waves on 152 SMs, but chunks of >= 256 tokens
+    const int target_ctas = 152 * 8;
+    int units = std::max(1, batch * heads_kv);
+    s = (target_ctas + units - 1) / units;
+    s = std::min(s, std::max(1, max_len / 256));
+    s = std::max(1, std::min(s, 1024));
+  }
+  s = std::max(1, std::min(s, std::max(1, max_len)));
+  int c = (max_len + s - 1) / s;
+  c = (c + 31) / 32 * 32;  // whole 32-token tiles
+  *splits = s;
+  *chunk = c;
+}
+
+}  // namespace tq
+
+extern "C" {
+
+int tq_abi_version(void) { return TQ_ABI_VERSION; }
+
+const char *tq_status_str(int s) {
+  switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_ARG: return "invalid argument";
+    case TQ_ERR_UNSUPPORTED: return "unsupported by this build";
+    case TQ_ERR_CAPACITY: return "append past cache capacity";
+    case TQ_ERR_CUDA: return "CUDA error";
+    case TQ_ERR_TIMEOUT: return "bounded device wait timed out";
+    case TQ_ERR_STATE: return "call does not fit the context's scheme";
+    case TQ_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case TQ_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+tq_status tq_codebook_f64(int d, int bits, double *h_c, double *h_b) {
+  if (d < 4 || (d & (d - 1)) || d > 4096 || bits < 1 || bits > 4) return TQ_ERR_ARG;
+  const Codebook64 &cb = cached_codebook(d, bits);
+  if (h_c) std::memcpy(h_c, cb.c.data(), cb.c.size() * sizeof(double));
+  if (h_b) std::memcpy(h_b, cb.b.data(), cb.b.size() * sizeof(double));
+  return TQ_OK;
+}
+
+tq_status tq_draw_params(uint64_t seed, int d, int8_t *h_diag, float *h_sketch) {
+  if (d < 4 || (d & (d - 1)) || d > 4096) return TQ_ERR_ARG;
+  if (h_diag) make_diag(seed, d, h_diag);
+  if (h_sketch) make_sketch(seed, d, h_sketch);
+  return TQ_OK;
+}
+
+tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
+  if (!out) return TQ_ERR_ARG;
+  *out = nullptr;
+  if (scheme < TQ_SCHEME_KV || scheme > TQ_SCHEME_KIVI) return TQ_ERR_ARG;
+  if (d < 4 || (d & (d - 1))) return TQ_ERR_ARG;
+  if (bits < 2 || bits > 4) return TQ_ERR_ARG;
+  if (d != tq::kD) return TQ_ERR_UNSUPPORTED;
+  if (scheme == TQ_SCHEME_KIVI && bits != 2) return TQ_ERR_UNSUPPORTED;
+
+  tq_ctx *c = new (std::nothrow) tq_ctx();
+  if (!c) return TQ_ERR_ARG;
+  c->d = d;
+  c->bits = bits;
+  c->scheme = scheme;
+  c->seed = seed;
+  roles_for(scheme, bits, &c->k, &c->v);
+  if (is_tq_scheme(scheme)) {
+    const Codebook64 &ck = cached_codebook(d, c->k.bits);
+    const Codebook64 &cv = cached_codebook(d, c->v.bits);
+    for (size_t i = 0; i < ck.c.size(); ++i) c->k_centroids[i] = (float)ck.c[i];
+    for (size_t i = 0; i < ck.b.size(); ++i) c->k_bounds[i] = (float)ck.b[i];
+    for (size_t i = 0; i < cv.c.size(); ++i) c->v_centroids[i] = (float)cv.c[i];
+    for (size_t i = 0; i < cv.b.size(); ++i) c->v_bounds[i] = (float)cv.b[i];
+  }
+  make_diag(seed, d, c->diag);
+  c->sketch = (float *)std::malloc(sizeof(float) * d * d);
+  if (!c->sketch) {
+    delete c;
+    return TQ_ERR_ARG;
+  }
+  make_sketch(seed, d, c->sketch);
+
+  tq::DevParams *hp = (tq::DevParams *)std::calloc(1, sizeof(tq::DevParams));
+  if (!hp) {
+    std::free(c->sketch);
+    delete c;
+    return TQ_ERR_ARG;
+  }
+  std::memcpy(hp->k_centroids, c->k_centroids, sizeof(hp->k_centroids));
+  std::memcpy(hp->k_bounds, c->k_bounds, sizeof(hp->k_bounds));
+  std::memcpy(hp->v_centroids, c->v_centroids, sizeof(hp->v_centroids));
+  std::memcpy(hp->v_bounds, c->v_bounds, sizeof(hp->v_bounds));
+  for (int i = 0; i < d; ++i) hp->diag[i] = (float)c->diag[i];
+  std::memcpy(hp->sketch, c->sketch, sizeof(float) * d * d);
+  hp->error = 0;
+
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaMalloc((void **)&c->dparams, sizeof(tq::DevParams));
+  if (e == cudaSuccess) e = cudaMemcpy(c->dparams, hp, sizeof(tq::DevParams), cudaMemcpyHostToDevice);
+  std::free(hp);
+  if (e != cudaSuccess) {
+    if (c->dparams) cudaFree(c->dparams);
+    std::free(c->sketch);
+    delete c;
+    return TQ_ERR_CUDA;
+  }
+  *out = c;
+  return TQ_OK;
+}
+
+void tq_destroy(tq_ctx *ctx) {
+  if (!ctx) return;
+  if (ctx->dparams) cudaFree(ctx->dparams);
+  std::free(ctx->sketch);
+  delete ctx;
+}
+
+tq_status tq_set_kivi(tq_ctx *ctx, int group, int window, int k_per_channel, int v_per_token) {
+  if (!ctx) return TQ_ERR_ARG;
+  if (ctx->scheme != TQ_SCHEME_KIVI) return TQ_ERR_STATE;
+  if (group <= 0 || window < 0 || window % (group > 0 ? group : 1)) return TQ_ERR_ARG;
+  if (group != 32 || window > 4096) return TQ_ERR_UNSUPPORTED;
+  ctx->kivi_group = group;
+  ctx->kivi_window = window;
+  ctx->kivi_k_per_channel = k_per_channel ? 1 : 0;
+  ctx->kivi_v_per_token = v_per_token ? 1 : 0;
+  return TQ_OK;
+}
+
+tq_status tq_cache_sizes_get(const tq_ctx *ctx, int batch, int heads_kv, int capacity, tq_cache_sizes *out) {
+  if (!ctx || !out || batch <= 0 || heads_kv <= 0 || capacity <= 0) return TQ_ERR_ARG;
+  std::memset(out, 0, sizeof(*out));
+  const size_t slots = (size_t)batch * heads_kv * capacity;
+  const int d = ctx->d;
+  if (ctx->scheme == TQ_SCHEME_KIVI) {
+    const int G = ctx->kivi_group;
+    if (capacity % G) return TQ_ERR_ARG;
+    out->k_codes = slots * (d / 4);
+    out->v_codes = slots * (d / 4);
+    const size_t per_channel = (size_t)batch * heads_kv * (capacity / G) * d * 2 * sizeof(uint16_t);
+    const size_t per_token = slots * (d / G) * 2 * sizeof(uint16_t);
+    out->k_stats = ctx->kivi_k_per_channel ? per_channel : per_token;
+    out->v_stats = ctx->kivi_v_per_token ? per_token : per_channel;
+    const size_t win = (size_t)batch * heads_kv * (ctx->kivi_window + G) * d * sizeof(uint16_t);
+    out->k_window = win;
+    out->v_window = win;
+    out->record_bytes = 2 * (d / 4 + (size_t)(d / G) * 4);
+    return TQ_OK;
+  }
+  out->k_codes = slots * code_bytes(ctx->k.bits, d);
+  out->k_norm = slots * sizeof(float);
+  out->v_codes = slots * code_bytes(ctx->v.bits, d);
+  out->v_norm = slots * sizeof(float);
+  size_t rec = code_bytes(ctx->k.bits, d) + 4 + code_bytes(ctx->v.bits, d) + 4;
+  if (ctx->k.qjl) {
+    out->k_signs = slots * (d / 8);
+    out->k_rnorm = slots * sizeof(float);
+    rec += d / 8 + 4;
+  }
+  if (ctx->v.qjl) {
+    out->v_signs = slots * (d / 8);
+    out->v_rnorm = slots * sizeof(float);
+    rec += d / 8 + 4;
+  }
+  out->record_bytes = rec;
+  return TQ_OK;
+}
+
+static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const void *d_k, const void *d_v,
+                                int dtype, int batch, int heads_kv, int n_new, const int32_t *d_seq_lens,
+                                void *stream);
+
+static tq_status check_cache(const tq_ctx *ctx, const tq_cache *c, int batch, int heads_kv) {
+  if (!c) return TQ_ERR_ARG;
+  if (c->batch != batch || c->heads_kv != heads_kv || c->capacity <= 0) return TQ_ERR_ARG;
+  const void *planes[] = {c->k_codes, c->k_norm, c->k_signs, c->k_rnorm, c->v_codes, c->v_norm,
+                          c->v_signs, c->v_rnorm, c->k_stats, c->v_stats, c->k_window, c->v_window};
+  for (const void *p : planes)
+    if (!aligned16(p)) return TQ_ERR_ALIGN;
+  if (ctx->scheme == TQ_SCHEME_KIVI) {
+    if (!c->k_codes || !c->v_codes || !c->k_stats || !c->v_stats || !c->k_window || !c->v_window)
+      return TQ_ERR_ARG;
+    if (c->capacity % ctx->kivi_group) return TQ_ERR_ARG;
+    return TQ_OK;
+  }
+  if (!c->k_codes || !c->k_norm || !c->v_codes || !c->v_norm) return TQ_ERR_ARG;
+  if (ctx->k.qjl && (!c->k_signs || !c->k_rnorm)) return TQ_ERR_ARG;
+  if (ctx->v.qjl && (!c->v_signs || !c->v_rnorm)) return TQ_ERR_ARG;
+  return TQ_OK;
+}
+
+tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const void *d_k, const void *d_v,
+                             int dtype, int batch, int heads_kv, int n_new, const int32_t *d_seq_lens,
+                             void *stream) {
+  if (!ctx || !d_k || !d_v || !d_seq_lens) return TQ_ERR_ARG;
+  if (dtype != TQ_F32 && dtype != TQ_BF16) return TQ_ERR_ARG;
+  if (batch <= 0 || heads_kv <= 0 || n_new < 0) return TQ_ERR_ARG;
+  tq_status s = check_cache(ctx, cache, batch, heads_kv);
+  if (s != TQ_OK) return s;
+  if (!aligned16(d_k) || !aligned16(d_v)) return TQ_ERR_ALIGN;
+  if (n_new == 0) return TQ_OK;
+  if (ctx->scheme == TQ_SCHEME_KIVI) {
+    tq::KiviAppendArgs a{ctx, cache, d_k, d_v, dtype, batch, heads_kv, n_new, d_seq_lens, &ctx->dparams->error};
+    if (ctx->prof_append_start) cudaEventRecord((cudaEvent_t)ctx->prof_append_start, (cudaStream_t)stream);
+    s = (tq_status)tq::launch_append_kivi(a, stream);
+    if (ctx->prof_append_stop) cudaEventRecord((cudaEvent_t)ctx->prof_append_stop, (cudaStream_t)stream);
+    return s;
+  }
+  if (ctx->prof_append_start) cudaEventRecord((cudaEvent_t)ctx->prof_append_start, (cudaStream_t)stream);
+  s = append_tq_both(ctx, cache, d_k, d_v, dtype, batch, heads_kv, n_new, d_seq_lens, stream);
+  if (ctx->prof_append_stop) cudaEventRecord((cudaEvent_t)ctx->prof_append_stop, (cudaStream_t)stream);
+  return s;
+}
+
+static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const void *d_k, const void *d_v,
+                                int dtype, int batch, int heads_kv, int n_new, const int32_t *d_seq_lens,
+                                void *stream) {
+  tq_status s;
+  tq::AppendArgs a{};
+  a.dtype = dtype;
+  a.batch = batch;
+  a.heads = heads_kv;
+  a.n_new = n_new;
+  a.capacity = cache->capacity;
+  a.seq_lens = d_seq_lens;
+  a.params = ctx->dparams;
+  a.error = &ctx->dparams->error;
+  // K
+  a.x = d_k;
+  a.codes = cache->k_codes;
+  a.norms = cache->k_norm;
+  a.signs = cache->k_signs;
+  a.rnorms = cache->k_rnorm;
+  a.role = ctx->k;
+  a.centroids = ctx->dparams->k_centroids;
+  a.bounds = ctx->dparams->k_bounds;
+  s = (tq_status)tq::launch_append_tq(a, stream);
+  if (s != TQ_OK) return s;
+  // V
+  a.x = d_v;
+  a.codes = cache->v_codes;
+  a.norms = cache->v_norm;
+  a.signs = cache->v_signs;
+  a.rnorms = cache->v_rnorm;
+  a.role = ctx->v;
+  a.centroids = ctx->dparams->v_centroids;
+  a.bounds = ctx->dparams->v_bounds;
+  return (tq_status)tq::launch_append_tq(a, stream);
+}
+
+tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len, int splits,
+                            size_t *out) {
+  if (!ctx || !out || batch <= 0 || heads_q <= 0 || heads_kv <= 0 || max_len <= 0 || splits < 0)
+    return TQ_ERR_ARG;
+  int s, chunk;
+  tq::choose_splits(batch, heads_kv, max_len, splits, &s, &chunk);
+  size_t qprep = (size_t)batch * heads_q * 2 * ctx->d * sizeof(float);
+  size_t parts = (size_t)batch * heads_q * s * tq::kPartialFloats * sizeof(float);
+  *out = qprep + parts;
+  return TQ_OK;
+}
+
+tq_status tq_decode_attention(const tq_ctx *ctx, const tq_cache *cache, const void *d_q, int q_dtype, int batch,
+                              int heads_q, int heads_kv, const int32_t *d_seq_lens, int max_len, int splits,
+                              void *d_workspace, size_t ws_bytes, float *d_out, void *stream) {
+  if (!ctx || !d_q || !d_seq_lens || !d_workspace || !d_out) return TQ_ERR_ARG;
+  if (q_dtype != TQ_F32 && q_dtype != TQ_BF16) return TQ_ERR_ARG;
+  if (batch <= 0 || heads_q <= 0 || heads_kv <= 0 || max_len <= 0 || splits < 0) return TQ_ERR_ARG;
+  if (heads_q % heads_kv) return TQ_ERR_ARG;
+  if (heads_q / heads_kv > tq::kMaxGroup) return TQ_ERR_UNSUPPORTED;
+  tq_status s = check_cache(ctx, cache, batch, heads_kv);
+  if (s != TQ_OK) return s;
+  if (max_len > cache->capacity) return TQ_ERR_ARG;
+  if (!aligned16(d_q) || !aligned16(d_workspace) || !aligned16(d_out)) return TQ_ERR_ALIGN;
+  size_t need = 0;
+  tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, splits, &need);
+  if (ws_bytes < need) return TQ_ERR_WORKSPACE;
+  tq::DecodeArgs a{};
+  a.ctx = ctx;
+  a.cache = cache;
+  a.q = d_q;
+  a.q_dtype = q_dtype;
+  a.batch = batch;
+  a.heads_q = heads_q;
+  a.heads_kv = heads_kv;
+  a.max_len = max_len;
+  tq::choose_splits(batch, heads_kv, max_len, splits, &a.splits, &a.chunk);
+  a.seq_lens = d_seq_lens;
+  a.qprep = (float *)d_workspace;
+  a.partials = a.qprep + (size_t)batch * heads_q * 2 * ctx->d;
+  a.out = d_out;
+  if (ctx->scheme == TQ_SCHEME_KIVI) return (tq_status)tq::launch_decode_kivi(a, stream);
+  return (tq_status)tq::launch_decode_tq(a, stream);
+}
+
+tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int heads_kv, int t0, int t1,
+                        const int32_t *d_seq_lens, float *d_k, float *d_v, void *stream) {
+  if (!ctx || batch <= 0 || heads_kv <= 0 || t0 < 0 || t1 < t0) return TQ_ERR_ARG;
+  tq_status s = check_cache(ctx, cache, batch, heads_kv);
+  if (s != TQ_OK) return s;
+  if (t1 > cache->capacity) return TQ_ERR_ARG;
+  if (t1 == t0) return TQ_OK;
+  if (ctx->scheme == TQ_SCHEME_KIVI) {
+    if (!d_seq_lens) return TQ_ERR_ARG;
+    tq::KiviDequantArgs a{ctx, cache, batch, heads_kv, t0, t1, d_seq_lens, d_k, d_v};
+    return (tq_status)tq::launch_dequant_kivi(a, stream);
+  }
+  for (int which = 0; which < 2; ++which) {
+    float *out = which ? d_v : d_k;
+    if (!out) continue;
+    tq::DequantArgs a{};
+    a.batch = batch;
+    a.heads = heads_kv;
+    a.capacity = cache->capacity;
+    a.t0 = t0;
+    a.t1 = t1;
+    a.params = ctx->dparams;
+    a.out = out;
+    if (which == 0) {
+      a.codes = cache->k_codes; a.norms = cache->k_norm; a.signs = cache->k_signs; a.rnorms = cache->k_rnorm;
+      a.role = ctx->k; a.centroids = ctx->dparams->k_centroids;
+    } else {
+      a.codes = cache->v_codes; a.norms = cache->v_norm; a.signs = cache->v_signs; a.rnorms = cache->v_rnorm;
+      a.role = ctx->v; a.centroids = ctx->dparams->v_centroids;
+    }
+    s = (tq_status)tq::launch_dequant_tq(a, stream);
+    if (s != TQ_OK) return s;
+  }
+  return TQ_OK;
+}
+
+tq_status tq_export_params(const tq_ctx *ctx, int *k_bits, float *k_c, float *k_b, int *v_bits, float *v_c,
+                           float *v_b, int8_t *diag, float *sketch) {
+  if (!ctx) return TQ_ERR_ARG;
+  const int Lk = 1 << ctx->k.bits, Lv = 1 << ctx->v.bits;
+  if (k_bits) *k_bits = ctx->k.bits;
+  if (v_bits) *v_bits = ctx->v.bits;
+  if (k_c) std::memcpy(k_c, ctx->k_centroids, sizeof(float) * Lk);
+  if (k_b) std::memcpy(k_b, ctx->k_bounds, sizeof(float) * (Lk - 1));
+  if (v_c) std::memcpy(v_c, ctx->v_centroids, sizeof(float) * Lv);
+  if (v_b) std::memcpy(v_b, ctx->v_bounds, sizeof(float) * (Lv - 1));
+  if (diag) std::memcpy(diag, ctx->diag, ctx->d);
+  if (sketch) std::memcpy(sketch, ctx->sketch, sizeof(float) * ctx->d * ctx->d);
+  return TQ_OK;
+}
+
+tq_status tq_set_profile_events(tq_ctx *ctx, void *start, void *stop, void *append_start, void *append_stop) {
+  if (!ctx) return TQ_ERR_ARG;
+  ctx->prof_decode_start = start;
+  ctx->prof_decode_stop = stop;
+  ctx->prof_append_start = append_start;
+  ctx->prof_append_stop = append_stop;
+  return TQ_OK;
+}
+
+tq_status tq_get_device_error(const tq_ctx *ctx, void *stream, int *code) {
+  if (!ctx || !code) return TQ_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaStreamSynchronize(st);
+  int v = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&v, &ctx->dparams->error, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(&ctx->dparams->error, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  *code = v;
+  return cuda_status(e);
+}
+
+}  // extern "C"

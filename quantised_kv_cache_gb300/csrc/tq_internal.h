@@ -1,0 +1,131 @@
+// Internal declarations shared by the host code and the CUDA translation units
+// of libtq. Not part of the ABI (include/tq.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+constexpr int kD = 128;          // the head dimension this build implements
+constexpr int kMaxLevels = 16;   // 4-bit codebooks at most
+constexpr int kMaxGroup = 8;     // query heads per KV head handled by one CTA
+constexpr int kPartialFloats = 260;  // m, l, acc[128], sign_acc[128], 2 pad
+
+// Device-resident parameter block of a context (one cudaMalloc).
+struct DevParams {
+  float k_centroids[kMaxLevels];
+  float k_bounds[kMaxLevels];  // 2^b - 1 used
+  float v_centroids[kMaxLevels];
+  float v_bounds[kMaxLevels];
+  float diag[kD];              // D as +/-1.0f
+  float sketch[kD * kD];       // S, row-major [row][col]
+  int error;                   // sticky device error word (a tq_status)
+  int pad[3];
+};
+
+struct Role {
+  int bits = 0;
+  bool rotate = false;
+  bool qjl = false;
+};
+
+}  // namespace tq
+
+struct tq_ctx {
+  int d = 0;
+  int bits = 0;
+  int scheme = 0;
+  uint64_t seed = 0;
+  int device = 0;
+  tq::Role k, v;
+  // KIVI options
+  int kivi_group = 32;
+  int kivi_window = 128;
+  int kivi_k_per_channel = 1;
+  int kivi_v_per_token = 1;
+  // host copies of the float32 parameters
+  float k_centroids[tq::kMaxLevels] = {};
+  float k_bounds[tq::kMaxLevels] = {};
+  float v_centroids[tq::kMaxLevels] = {};
+  float v_bounds[tq::kMaxLevels] = {};
+  int8_t diag[tq::kD] = {};
+  float *sketch = nullptr;  // host, d*d
+  tq::DevParams *dparams = nullptr;
+  // optional CUDA events recorded around the decode / append kernels
+  void *prof_decode_start = nullptr, *prof_decode_stop = nullptr;
+  void *prof_append_start = nullptr, *prof_append_stop = nullptr;
+};
+
+namespace tq {
+
+// Launchers implemented in the .cu translation units. All return a tq_status.
+struct AppendArgs {
+  const void *x;         // [batch][heads][n_new][d]
+  int dtype;             // TQ_F32 / TQ_BF16
+  int batch, heads, n_new, capacity;
+  const int32_t *seq_lens;
+  uint8_t *codes;
+  float *norms;
+  uint8_t *signs;
+  float *rnorms;
+  Role role;
+  const float *centroids;  // device pointers into DevParams
+  const float *bounds;
+  const DevParams *params;
+  int *error;
+};
+int launch_append_tq(const AppendArgs &a, void *stream);
+
+struct DecodeArgs {
+  const tq_ctx *ctx;
+  const tq_cache *cache;
+  const void *q;
+  int q_dtype;
+  int batch, heads_q, heads_kv, max_len, splits, chunk;
+  const int32_t *seq_lens;
+  float *qprep;     // [batch][heads_q][2][d]
+  float *partials;  // [batch][heads_q][splits][kPartialFloats]
+  float *out;
+};
+int launch_decode_tq(const DecodeArgs &a, void *stream);
+int launch_decode_kivi(const DecodeArgs &a, void *stream);
+
+struct DequantArgs {
+  const uint8_t *codes;
+  const float *norms;
+  const uint8_t *signs;
+  const float *rnorms;
+  int batch, heads, capacity, t0, t1;
+  Role role;
+  const float *centroids;
+  const DevParams *params;
+  float *out;
+};
+int launch_dequant_tq(const DequantArgs &a, void *stream);
+
+struct KiviAppendArgs {
+  const tq_ctx *ctx;
+  const tq_cache *cache;
+  const void *k, *v;
+  int dtype, batch, heads, n_new;
+  const int32_t *seq_lens;
+  int *error;
+};
+int launch_append_kivi(const KiviAppendArgs &a, void *stream);
+
+struct KiviDequantArgs {
+  const tq_ctx *ctx;
+  const tq_cache *cache;
+  int batch, heads, t0, t1;
+  const int32_t *seq_lens;
+  float *k_out, *v_out;
+};
+int launch_dequant_kivi(const KiviDequantArgs &a, void *stream);
+
+// split count / chunk policy shared by sizing and launch
+void choose_splits(int batch, int heads_kv, int max_len, int requested, int *splits, int *chunk);
+
+}  // namespace tq

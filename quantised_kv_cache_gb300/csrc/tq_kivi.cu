@@ -1,0 +1,294 @@
+// KIVI-style asymmetric 2-bit grouped quantisation with a bfloat16 window of
+// recent tokens ("Your KV cache is not a bit problem but a geometry problem":
+// "What quantisation error is made of" -- zero point = group minimum, step =
+// range / (2^B - 1), round to nearest; "Keys" / "Values" -- group keys per
+// channel along tokens and values per token along channels, or the flips;
+// "The systems tax" -- keep the most recent tokens in full precision and
+// quantise them in groups once enough have accumulated).
+//
+// Append of n_new tokens to a sequence holding N0 tokens, N = N0 + n_new:
+// the window rule leaves tokens [0, nq(N)) quantised and [nq(N), N) in the
+// window, nq(N) = G floor((N - W) / G) once N >= W + G. Two stream-ordered
+// launches per tensor keep the ring consistent:
+//   flush  -- quantise every group in [nq(N0), nq(N)), reading tokens < N0
+//             from the ring and later ones from the input;
+//   window -- copy tokens [max(nq(N), N0), N) from the input into the ring.
+
+#include <cuda_fp16.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kG = 32;  // group size this build implements
+
+__device__ __forceinline__ int kivi_nq(int n, int window) {
+  return (n < window + kG) ? 0 : kG * ((n - window) / kG);
+}
+
+struct KiviTensorArgs {
+  const void *x;  // [batch][heads][n_new][d] input
+  int bf16;
+  int batch, heads, n_new, capacity, window;
+  const int32_t *seq_lens;
+  uint8_t *codes;      // [batch][heads][capacity][d/4]
+  uint16_t *stats;     // fp16 (zero, step) pairs
+  uint16_t *ring;      // bf16 [batch][heads][window + G][d]
+  int *error;
+};
+
+// token j's four channels 4L..4L+3 from the ring (j < n0) or the input
+__device__ __forceinline__ void kivi_load(const KiviTensorArgs &a, long long bh, int n0, int j, int lane,
+                                          float (&x)[4]) {
+  if (j < n0) {
+    const int R = a.window + kG;
+    const uint16_t *src = a.ring + ((size_t)bh * R + (j % R)) * kD + 4 * lane;
+    load4(src, 0, true, x);
+  } else {
+    load4(a.x, ((size_t)bh * a.n_new + (j - n0)) * kD + 4 * lane, a.bf16 != 0, x);
+  }
+}
+
+__device__ __forceinline__ void group_stats(float mn, float mx, __half &z, __half &s) {
+  z = __float2half_rn(mn);
+  s = __double2half(((double)mx - (double)mn) / 3.0);
+}
+
+__device__ __forceinline__ uint32_t kivi_code(float x, float z, float s) {
+  if (!(s > 0.f)) return 0u;
+  float t = rintf((x - z) / s);
+  t = fminf(fmaxf(t, 0.f), 3.f);
+  return (uint32_t)t;
+}
+
+// one warp per (batch, head, group of 32 tokens); lane owns channels 4L..4L+3
+__global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, int units_per_bh) {
+  const int lane = threadIdx.x & 31;
+  const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long bh = unit / units_per_bh;
+  if (bh >= (long long)a.batch * a.heads) return;
+  const int b = (int)(bh / a.heads);
+  const int n0 = __ldg(a.seq_lens + b);
+  const int n1 = n0 + a.n_new;
+  if (n1 > a.capacity) {
+    if (lane == 0 && unit % units_per_bh == 0) set_error(a.error, TQ_ERR_CAPACITY);
+    return;
+  }
+  const int g = kivi_nq(n0, a.window) / kG + (int)(unit % units_per_bh);
+  if (g * kG >= kivi_nq(n1, a.window)) return;
+  float mn[4], mx[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    mn[c] = INFINITY;
+    mx[c] = -INFINITY;
+  }
+  for (int k = 0; k < kG; ++k) {
+    float x[4];
+    kivi_load(a, bh, n0, g * kG + k, lane, x);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      mn[c] = fminf(mn[c], x[c]);
+      mx[c] = fmaxf(mx[c], x[c]);
+    }
+  }
+  float zf[4], sf[4];
+  uint32_t st[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    __half z, s;
+    group_stats(mn[c], mx[c], z, s);
+    zf[c] = __half2float(z);
+    sf[c] = __half2float(s);
+    st[c] = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
+  }
+  uint4 *srec = reinterpret_cast<uint4 *>(a.stats + (((size_t)bh * (a.capacity / kG) + g) * kD) * 2);
+  srec[lane] = make_uint4(st[0], st[1], st[2], st[3]);
+  for (int k = 0; k < kG; ++k) {
+    const int j = g * kG + k;
+    float x[4];
+    kivi_load(a, bh, n0, j, lane, x);
+    uint32_t field = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf[c], sf[c]) << (2 * c);
+    const uint32_t word = pack_record_word<2>(field, lane);
+    if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + ((size_t)bh * a.capacity + j) * (kD / 4))[lane] = word;
+  }
+}
+
+// one warp per (batch, head, token); groups are 32 channels = 8 lanes
+__global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, int units_per_bh) {
+  const int lane = threadIdx.x & 31;
+  const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long bh = unit / units_per_bh;
+  if (bh >= (long long)a.batch * a.heads) return;
+  const int b = (int)(bh / a.heads);
+  const int n0 = __ldg(a.seq_lens + b);
+  const int n1 = n0 + a.n_new;
+  if (n1 > a.capacity) {
+    if (lane == 0 && unit % units_per_bh == 0) set_error(a.error, TQ_ERR_CAPACITY);
+    return;
+  }
+  const int j = kivi_nq(n0, a.window) + (int)(unit % units_per_bh);
+  if (j >= kivi_nq(n1, a.window)) return;
+  float x[4];
+  kivi_load(a, bh, n0, j, lane, x);
+  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  }
+  __half z, s;
+  group_stats(mn, mx, z, s);
+  const float zf = __half2float(z), sf = __half2float(s);
+  uint32_t field = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf, sf) << (2 * c);
+  const uint32_t word = pack_record_word<2>(field, lane);
+  const size_t slot = (size_t)bh * a.capacity + j;
+  if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + slot * (kD / 4))[lane] = word;
+  if ((lane & 7) == 0) {
+    const uint32_t st = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
+    reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[lane >> 3] = st;
+  }
+}
+
+// one warp per (batch, head, new token): window tokens go to the bf16 ring
+__global__ void __launch_bounds__(256) kivi_window_write(KiviTensorArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long bh = unit / a.n_new;
+  if (bh >= (long long)a.batch * a.heads) return;
+  const int t = (int)(unit % a.n_new);
+  const int b = (int)(bh / a.heads);
+  const int n0 = __ldg(a.seq_lens + b);
+  const int n1 = n0 + a.n_new;
+  if (n1 > a.capacity) return;
+  const int j = n0 + t;
+  if (j < kivi_nq(n1, a.window)) return;
+  float x[4];
+  load4(a.x, ((size_t)bh * a.n_new + t) * kD + 4 * lane, a.bf16 != 0, x);
+  const int R = a.window + kG;
+  uint16_t h[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) h[c] = __bfloat16_as_ushort(__float2bfloat16_rn(x[c]));
+  uint2 w;
+  w.x = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
+  w.y = (uint32_t)h[2] | ((uint32_t)h[3] << 16);
+  reinterpret_cast<uint2 *>(a.ring + ((size_t)bh * R + (j % R)) * kD)[lane] = w;
+}
+
+struct KiviDequantKernelArgs {
+  const uint8_t *codes;
+  const uint16_t *stats;
+  const uint16_t *ring;
+  int per_channel, batch, heads, capacity, window, t0, t1;
+  const int32_t *seq_lens;
+  float *out;
+};
+
+__global__ void __launch_bounds__(256) kivi_dequant_kernel(KiviDequantKernelArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int n = a.t1 - a.t0;
+  const long long vec = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (vec >= (long long)a.batch * a.heads * n) return;
+  const long long bh = vec / n;
+  const int j = a.t0 + (int)(vec % n);
+  const int len = min(max(__ldg(a.seq_lens + bh / a.heads), 0), a.capacity);
+  const int nq = kivi_nq(len, a.window);
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+  const size_t slot = (size_t)bh * a.capacity + j;
+  if (j < nq) {
+    const uint32_t f = lane_code_field<2>(reinterpret_cast<const uint32_t *>(a.codes) + slot * (kD / 16), lane);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t st;
+      if (a.per_channel)
+        st = __ldg(reinterpret_cast<const uint32_t *>(a.stats) + ((size_t)bh * (a.capacity / kG) + j / kG) * kD +
+                   4 * lane + c);
+      else
+        st = __ldg(reinterpret_cast<const uint32_t *>(a.stats) + slot * (kD / kG) + (lane >> 3));
+      const float z = __half2float(__ushort_as_half((unsigned short)(st & 0xffffu)));
+      const float s = __half2float(__ushort_as_half((unsigned short)(st >> 16)));
+      y[c] = fmaf(s, (float)((f >> (2 * c)) & 3u), z);
+    }
+  } else if (j < len) {
+    const int R = a.window + kG;
+    load4(a.ring + ((size_t)bh * R + (j % R)) * kD, 4 * lane, true, y);
+  }
+  reinterpret_cast<float4 *>(a.out + (size_t)vec * kD)[lane] = make_float4(y[0], y[1], y[2], y[3]);
+}
+
+int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
+  const long long bh = (long long)t.batch * t.heads;
+  // groups (or tokens) newly quantised by one append: at most (n_new + G - 1) tokens
+  const int max_tokens = t.n_new + kG - 1;
+  const int units = per_channel ? (max_tokens + kG - 1) / kG + 1 : max_tokens;
+  const long long warps = bh * units;
+  const unsigned blocks = (unsigned)((warps + 7) / 8);
+  if (per_channel) kivi_flush_per_channel<<<blocks, 256, 0, st>>>(t, units);
+  else kivi_flush_per_token<<<blocks, 256, 0, st>>>(t, units);
+  const long long wwarps = bh * t.n_new;
+  kivi_window_write<<<(unsigned)((wwarps + 7) / 8), 256, 0, st>>>(t);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_append_kivi(const KiviAppendArgs &a, void *stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const tq_ctx *ctx = a.ctx;
+  const tq_cache *c = a.cache;
+  if (ctx->kivi_group != kG) return TQ_ERR_UNSUPPORTED;
+  KiviTensorArgs t{};
+  t.bf16 = a.dtype == TQ_BF16;
+  t.batch = a.batch;
+  t.heads = a.heads;
+  t.n_new = a.n_new;
+  t.capacity = c->capacity;
+  t.window = ctx->kivi_window;
+  t.seq_lens = a.seq_lens;
+  t.error = a.error;
+  t.x = a.k;
+  t.codes = c->k_codes;
+  t.stats = c->k_stats;
+  t.ring = c->k_window;
+  int r = flush_and_window(t, ctx->kivi_k_per_channel != 0, st);
+  if (r != TQ_OK) return r;
+  t.x = a.v;
+  t.codes = c->v_codes;
+  t.stats = c->v_stats;
+  t.ring = c->v_window;
+  return flush_and_window(t, ctx->kivi_v_per_token == 0, st);
+}
+
+int launch_dequant_kivi(const KiviDequantArgs &a, void *stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const tq_ctx *ctx = a.ctx;
+  const tq_cache *c = a.cache;
+  const long long total = (long long)a.batch * a.heads * (a.t1 - a.t0);
+  const unsigned blocks = (unsigned)((total + 7) / 8);
+  for (int which = 0; which < 2; ++which) {
+    float *out = which ? a.v_out : a.k_out;
+    if (!out) continue;
+    KiviDequantKernelArgs k{};
+    k.codes = which ? c->v_codes : c->k_codes;
+    k.stats = which ? c->v_stats : c->k_stats;
+    k.ring = which ? c->v_window : c->k_window;
+    k.per_channel = which ? (ctx->kivi_v_per_token == 0) : (ctx->kivi_k_per_channel != 0);
+    k.batch = a.batch;
+    k.heads = a.heads;
+    k.capacity = c->capacity;
+    k.window = ctx->kivi_window;
+    k.t0 = a.t0;
+    k.t1 = a.t1;
+    k.seq_lens = a.seq_lens;
+    k.out = out;
+    kivi_dequant_kernel<<<blocks, 256, 0, st>>>(k);
+  }
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace tq

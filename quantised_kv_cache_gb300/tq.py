@@ -1,0 +1,321 @@
+"""Thin ctypes binding of libtq's C ABI (include/tq.h), same names as the C calls.
+
+Argument marshalling only: every step of quantisation and attention runs in
+the CUDA kernels behind the ABI. PyTorch is used for device memory and
+streams. If ``_lib/libtq.so`` is missing this module raises at first use --
+there is no fallback implementation.
+"""
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtq.so")
+
+TQ_OK = 0
+TQ_ERR_ARG = 1
+TQ_ERR_UNSUPPORTED = 2
+TQ_ERR_CAPACITY = 3
+TQ_ERR_CUDA = 4
+TQ_ERR_TIMEOUT = 5
+TQ_ERR_STATE = 6
+TQ_ERR_ALIGN = 7
+TQ_ERR_WORKSPACE = 8
+
+TQ_SCHEME_KV = 0
+TQ_SCHEME_KQV = 1
+TQ_SCHEME_QKQV = 2
+TQ_SCHEME_KIVI = 3
+SCHEMES = {"KV": TQ_SCHEME_KV, "KQV": TQ_SCHEME_KQV, "QKQV": TQ_SCHEME_QKQV, "KIVI": TQ_SCHEME_KIVI}
+
+TQ_F32 = 0
+TQ_BF16 = 1
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+
+class tq_cache(ctypes.Structure):
+    _fields_ = [("batch", _i), ("heads_kv", _i), ("capacity", _i),
+                ("k_codes", _vp), ("k_norm", _vp), ("k_signs", _vp), ("k_rnorm", _vp),
+                ("v_codes", _vp), ("v_norm", _vp), ("v_signs", _vp), ("v_rnorm", _vp),
+                ("k_stats", _vp), ("v_stats", _vp), ("k_window", _vp), ("v_window", _vp)]
+
+
+PLANES = ["k_codes", "k_norm", "k_signs", "k_rnorm", "v_codes", "v_norm", "v_signs", "v_rnorm",
+          "k_stats", "v_stats", "k_window", "v_window"]
+
+
+class tq_cache_sizes(ctypes.Structure):
+    _fields_ = [(p, _sz) for p in PLANES] + [("record_bytes", _sz)]
+
+
+_SIGNATURES = {
+    "tq_abi_version": (_i, []),
+    "tq_status_str": (ctypes.c_char_p, [_i]),
+    "tq_init": (_i, [_i, _i, _i, ctypes.c_uint64, ctypes.POINTER(_vp)]),
+    "tq_destroy": (None, [_vp]),
+    "tq_set_kivi": (_i, [_vp, _i, _i, _i, _i]),
+    "tq_cache_sizes_get": (_i, [_vp, _i, _i, _i, ctypes.POINTER(tq_cache_sizes)]),
+    "tq_append_quantize": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
+    "tq_workspace_size": (_i, [_vp, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "tq_decode_attention": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _i, _i, _i, _i, _vp, _i, _i, _vp, _sz,
+                                 _vp, _vp]),
+    "tq_dequantize": (_i, [_vp, ctypes.POINTER(tq_cache), _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "tq_export_params": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "tq_codebook_f64": (_i, [_i, _i, _vp, _vp]),
+    "tq_draw_params": (_i, [ctypes.c_uint64, _i, _vp, _vp]),
+    "tq_get_device_error": (_i, [_vp, _vp, ctypes.POINTER(_i)]),
+    "tq_set_profile_events": (_i, [_vp, _vp, _vp, _vp, _vp]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtq.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libtq.so not built at {LIB_PATH}: run "
+                               "`python -m quantised_kv_cache_gb300.build` (no CPU fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+class TQError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = lib().tq_status_str(status).decode()
+        super().__init__(f"{what}: {msg} (status {status})" if what else f"{msg} (status {status})")
+
+
+def check(status: int, what: str = "") -> None:
+    if status != TQ_OK:
+        raise TQError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return TQ_F32
+    if t.dtype == torch.bfloat16:
+        return TQ_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# ----------------------------------------------------------------------------
+# same-name wrappers of the C calls
+# ----------------------------------------------------------------------------
+
+def tq_abi_version() -> int:
+    return lib().tq_abi_version()
+
+
+def tq_status_str(status: int) -> str:
+    return lib().tq_status_str(status).decode()
+
+
+def tq_init(d: int, bits: int, scheme, seed: int) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    s = SCHEMES[scheme] if isinstance(scheme, str) else int(scheme)
+    check(lib().tq_init(d, bits, s, ctypes.c_uint64(seed), ctypes.byref(h)), "tq_init")
+    return h
+
+
+def tq_destroy(ctx) -> None:
+    lib().tq_destroy(ctx)
+
+
+def tq_set_kivi(ctx, group=32, window=128, k_per_channel=True, v_per_token=True) -> None:
+    check(lib().tq_set_kivi(ctx, group, window, int(k_per_channel), int(v_per_token)), "tq_set_kivi")
+
+
+def tq_cache_sizes_get(ctx, batch: int, heads_kv: int, capacity: int) -> tq_cache_sizes:
+    out = tq_cache_sizes()
+    check(lib().tq_cache_sizes_get(ctx, batch, heads_kv, capacity, ctypes.byref(out)), "tq_cache_sizes_get")
+    return out
+
+
+def tq_append_quantize(ctx, cache: "Cache", k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                       stream=None) -> None:
+    B, H, n, d = k.shape
+    assert v.shape == k.shape and k.dtype == v.dtype and k.is_contiguous() and v.is_contiguous()
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_cuda
+    check(lib().tq_append_quantize(ctx, ctypes.byref(cache.struct), _ptr(k), _ptr(v), _dtype_code(k), B, H, n,
+                                   _ptr(seq_lens), _stream(stream)), "tq_append_quantize")
+
+
+def tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, splits=0) -> int:
+    out = _sz()
+    check(lib().tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, splits, ctypes.byref(out)),
+          "tq_workspace_size")
+    return out.value
+
+
+def tq_decode_attention(ctx, cache: "Cache", q: torch.Tensor, seq_lens: torch.Tensor, max_len: int,
+                        splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    B, Hq, d = q.shape
+    assert q.is_contiguous() and seq_lens.dtype == torch.int32
+    Hkv = cache.struct.heads_kv
+    need = tq_workspace_size(ctx, B, Hq, Hkv, max_len, splits)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    check(lib().tq_decode_attention(ctx, ctypes.byref(cache.struct), _ptr(q), _dtype_code(q), B, Hq, Hkv,
+                                    _ptr(seq_lens), max_len, splits, _ptr(workspace), workspace.numel(),
+                                    _ptr(out), _stream(stream)), "tq_decode_attention")
+    return out
+
+
+def tq_dequantize(ctx, cache: "Cache", t0: int, t1: int, seq_lens: Optional[torch.Tensor] = None,
+                  k_out: Optional[torch.Tensor] = None, v_out: Optional[torch.Tensor] = None, stream=None):
+    B, H = cache.struct.batch, cache.struct.heads_kv
+    dev = cache.device
+    if k_out is None:
+        k_out = torch.empty((B, H, t1 - t0, 128), dtype=torch.float32, device=dev)
+    if v_out is None:
+        v_out = torch.empty((B, H, t1 - t0, 128), dtype=torch.float32, device=dev)
+    check(lib().tq_dequantize(ctx, ctypes.byref(cache.struct), B, H, t0, t1, _ptr(seq_lens), _ptr(k_out),
+                              _ptr(v_out), _stream(stream)), "tq_dequantize")
+    return k_out, v_out
+
+
+@dataclass
+class Params:
+    k_bits: int
+    k_centroids: "np.ndarray"
+    k_bounds: "np.ndarray"
+    v_bits: int
+    v_centroids: "np.ndarray"
+    v_bounds: "np.ndarray"
+    diag: "np.ndarray"
+    sketch: "np.ndarray"
+
+
+def tq_export_params(ctx, d: int = 128) -> Params:
+    import numpy as np
+    kb, vb = _i(), _i()
+    kc, kbd, vc, vbd = (np.zeros(16, np.float32) for _ in range(4))
+    diag = np.zeros(d, np.int8)
+    S = np.zeros((d, d), np.float32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    check(lib().tq_export_params(ctx, ctypes.byref(kb), p(kc), p(kbd), ctypes.byref(vb), p(vc), p(vbd), p(diag),
+                                 p(S)), "tq_export_params")
+    Lk, Lv = 1 << kb.value, 1 << vb.value
+    return Params(kb.value, kc[:Lk], kbd[:Lk - 1], vb.value, vc[:Lv], vbd[:Lv - 1], diag, S)
+
+
+def tq_codebook_f64(d: int, bits: int):
+    import numpy as np
+    c = np.zeros(1 << bits)
+    b = np.zeros((1 << bits) - 1)
+    check(lib().tq_codebook_f64(d, bits, c.ctypes.data_as(ctypes.c_void_p), b.ctypes.data_as(ctypes.c_void_p)),
+          "tq_codebook_f64")
+    return c, b
+
+
+def tq_draw_params(seed: int, d: int):
+    import numpy as np
+    diag = np.zeros(d, np.int8)
+    S = np.zeros((d, d), np.float32)
+    check(lib().tq_draw_params(ctypes.c_uint64(seed), d, diag.ctypes.data_as(ctypes.c_void_p),
+                               S.ctypes.data_as(ctypes.c_void_p)), "tq_draw_params")
+    return diag, S
+
+
+def tq_set_profile_events(ctx, start=None, stop=None, append_start=None, append_stop=None) -> None:
+    """Pass torch.cuda.Event objects (created with enable_timing=True) or None."""
+    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    check(lib().tq_set_profile_events(ctx, h(start), h(stop), h(append_start), h(append_stop)),
+          "tq_set_profile_events")
+
+
+def tq_get_device_error(ctx, stream=None) -> int:
+    code = _i()
+    check(lib().tq_get_device_error(ctx, _stream(stream), ctypes.byref(code)), "tq_get_device_error")
+    return code.value
+
+
+# ----------------------------------------------------------------------------
+# device-memory plumbing: a context handle and a cache whose planes torch owns
+# ----------------------------------------------------------------------------
+
+class Context:
+    """Owns one tq_ctx (created on the current CUDA device)."""
+
+    def __init__(self, d: int = 128, bits: int = 4, scheme="KQV", seed: int = 42, *, kivi_group=32,
+                 kivi_window=128, k_per_channel=True, v_per_token=True):
+        self.d, self.bits, self.seed = d, bits, seed
+        self.scheme = scheme if isinstance(scheme, str) else [k for k, v in SCHEMES.items() if v == scheme][0]
+        self.handle = tq_init(d, bits, self.scheme, seed)
+        if self.scheme == "KIVI":
+            tq_set_kivi(self.handle, kivi_group, kivi_window, k_per_channel, v_per_token)
+            self.kivi = dict(group=kivi_group, window=kivi_window, k_per_channel=k_per_channel,
+                             v_per_token=v_per_token)
+
+    def close(self):
+        if self.handle is not None:
+            tq_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+
+class Cache:
+    """Cache planes allocated as torch uint8 tensors on `device` (16-byte aligned)."""
+
+    def __init__(self, ctx: Context, batch: int, heads_kv: int, capacity: int, device="cuda"):
+        self.sizes = tq_cache_sizes_get(ctx.handle, batch, heads_kv, capacity)
+        self.device = torch.device(device)
+        self.tensors = {}
+        self.struct = tq_cache()
+        self.struct.batch, self.struct.heads_kv, self.struct.capacity = batch, heads_kv, capacity
+        for p in PLANES:
+            n = getattr(self.sizes, p)
+            if n:
+                t = torch.zeros(n, dtype=torch.uint8, device=self.device)
+                assert t.data_ptr() % 16 == 0
+                self.tensors[p] = t
+                setattr(self.struct, p, t.data_ptr())
+            else:
+                setattr(self.struct, p, None)
+
+    def plane(self, name: str) -> torch.Tensor:
+        return self.tensors[name]
+
+    @property
+    def record_bytes(self) -> int:
+        return self.sizes.record_bytes
+
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in self.tensors.values())
