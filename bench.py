@@ -44,7 +44,7 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 100 ms from the warm-up through the timed loops."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -59,7 +59,7 @@ class Clocks:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -173,6 +173,21 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest replica's)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput of `world` replicas: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
 def workload_config():
     return {"workload": "Llama-2-7B-shaped decode step: append 1 token/sequence + decode attention, "
                         "B16 H32 d128 context 8192 bf16, KQV n=4",
@@ -181,13 +196,41 @@ def workload_config():
             "parallelism": "replicas"}
 
 
+def run_small_case(args, dev):
+    """A smaller instance of the Llama-2-7B-shaped workload for profiler captures:
+    B16 H32 context 4096 (294 MB of compressed records, 537 MB of bf16 K/V)."""
+    import torch
+    from quantised_kv_cache_gb300 import tq
+    from quantised_kv_cache_gb300 import workloads as wl
+    w = wl.WORKLOADS[2]
+    N = 4096
+    B, H = w.batch, w.heads_kv
+    ctx = tq.Context(128, w.bits, "KQV", 42)
+    cache = tq.Cache(ctx, B, H, N, device=dev)
+    q, k, v = wl.generate(w, dev, seq=N)
+    zeros = torch.zeros((B,), dtype=torch.int32, device=dev)
+    tq.tq_append_quantize(ctx.handle, cache, k, v, zeros)
+    lens = torch.full((B,), N, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        if args.case == "append-small":
+            tq.tq_append_quantize(ctx.handle, cache, k, v, zeros)
+        else:
+            tq.tq_decode_attention(ctx.handle, cache, q, lens, N)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    print(json.dumps({"case": args.case, "ok": True}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["step", "decode-small", "append-small"], default="step",
+                    help="step: the benchmark; *-small: one kernel family on B16 H32 N4096 (294 MB of records, "
+                         "above L2) for profiler captures")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -212,6 +255,10 @@ def main():
         build.build()
     if dist is not None:
         dist.barrier()
+
+    if args.case != "step":
+        run_small_case(args, dev)
+        return
 
     w = wl.WORKLOADS[2]
     B, H, d = w.batch, w.heads_kv, w.d
@@ -265,6 +312,10 @@ def main():
         dist.barrier()
     K = args.steps
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in dec_ev:  # torch creates the CUDA event on first record; the library needs the handle
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record()
     for i in range(K):
@@ -273,15 +324,10 @@ def main():
     t_stop.record()
     torch.cuda.synchronize()
     tq.tq_set_profile_events(ctx.handle)
-    clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_stop)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_stop), dist, dev)
     ms_step = elapsed_ms / K
     dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
-    value = world * step_bytes * K / (elapsed_ms / 1e3) / 1e9
+    value = job_throughput(step_bytes * K, world, elapsed_ms / 1e3) / 1e9
     assert tq.tq_get_device_error(ctx.handle) == 0
 
     # ---------------- end to end through the ABI with host buffers
@@ -311,12 +357,9 @@ def main():
     for i in range(K):
         e2e_step(i)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * step_bytes * K / e2e_s / 1e9
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    clk = clocks.stop()
+    e2e_value = job_throughput(step_bytes * K, world, e2e_s) / 1e9
 
     line = None
     if rank == 0:

@@ -246,8 +246,14 @@ def tq_draw_params(seed: int, d: int):
 
 
 def tq_set_profile_events(ctx, start=None, stop=None, append_start=None, append_stop=None) -> None:
-    """Pass torch.cuda.Event objects (created with enable_timing=True) or None."""
-    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    """Pass torch.cuda.Event objects (created with enable_timing=True, and recorded at
+    least once so that torch has created the CUDA event) or None."""
+    def h(e):
+        if e is None:
+            return None
+        if not e.cuda_event:
+            raise ValueError("event not yet created: record it once before passing it")
+        return ctypes.c_void_p(e.cuda_event)
     check(lib().tq_set_profile_events(ctx, h(start), h(stop), h(append_start), h(append_stop)),
           "tq_set_profile_events")
 

@@ -33,8 +33,13 @@ def _fill(ctx, w, cache, k, v):
     tq.tq_append_quantize(ctx.handle, cache, k, v, z)
 
 
-def _check_sampled_codes(cache, params, k, v, B, H, N, n_sample, seed):
-    """Compare n_sample random token-heads of K and V with the oracle's encoding."""
+def _check_sampled_codes(cache, params, k, v, B, H, N, n_sample, seed, rep=None, srep=None):
+    """Compare n_sample random token-heads of K and V with the oracle's encoding.
+
+    Out-of-band mismatches fail at once; the in-band fraction is checked by the
+    caller on the reports accumulated over the whole workload."""
+    rep = P.BandReport() if rep is None else rep
+    srep = P.BandReport() if srep is None else srep
     g = np.random.default_rng(seed)
     sel = g.choice(B * H * N, size=min(n_sample, B * H * N), replace=False)
     b, h, t = sel // (H * N), (sel // N) % H, sel % N
@@ -46,9 +51,8 @@ def _check_sampled_codes(cache, params, k, v, B, H, N, n_sample, seed):
         codes = cache.plane(f"{which}_codes").view(B, H, cap, cb)[torch.as_tensor(b), torch.as_tensor(h),
                                                                    torch.as_tensor(t)].cpu().numpy()
         gidx = otq.unpack_codes(codes, role.bits, 128)
-        rep = P.BandReport()
         mism = P.compare_codes(gidx, ora, ocb.lloyd_max(128, role.bits).bounds32, rep)
-        assert rep.ok(), f"{which}: {rep}"
+        assert rep.ok_out_of_band(), f"{which}: {rep}"
         norms = cache.plane(f"{which}_norm").view(torch.float32).view(B, H, cap)[torch.as_tensor(b),
                                                                              torch.as_tensor(h),
                                                                              torch.as_tensor(t)].cpu().numpy()
@@ -56,9 +60,9 @@ def _check_sampled_codes(cache, params, k, v, B, H, N, n_sample, seed):
         if role.qjl:
             sg = cache.plane(f"{which}_signs").view(B, H, cap, 16)[torch.as_tensor(b), torch.as_tensor(h),
                                                                   torch.as_tensor(t)].cpu().numpy()
-            srep = P.BandReport()
             P.compare_signs(otq.unpack_signs(sg, 128), ora, srep, skip_rows=mism.any(axis=1))
-            assert srep.ok(), f"{which} signs: {srep}"
+            assert srep.ok_out_of_band(), f"{which} signs: {srep}"
+    return rep, srep
 
 
 def _check_sampled_decode(cache, params, q, out, lens, B, Hkv, Hq, units, tol=1e-3):
@@ -95,7 +99,8 @@ def test_config1_single_head_all_codes_and_output():
     cache = tq.Cache(ctx, 1, 1, w.seq)
     _fill(ctx, w, cache, k, v)
     params = otq.make_params(128, w.bits, w.scheme, 42)
-    _check_sampled_codes(cache, params, k, v, 1, 1, w.seq, w.seq, 0)  # every token
+    rep, srep = _check_sampled_codes(cache, params, k, v, 1, 1, w.seq, w.seq, 0)  # every token
+    assert rep.ok() and srep.ok(), (rep, srep)
     lens = torch.full((1,), w.seq, dtype=torch.int32, device=DEV)
     out = tq.tq_decode_attention(ctx.handle, cache, q, lens, w.seq)
     _check_sampled_decode(cache, params, q, out, [w.seq], 1, 1, 1, [(0, 0)])
@@ -116,23 +121,23 @@ def test_config2_llama7b_shaped_decode_step():
     torch.cuda.synchronize()
     assert tq.tq_get_device_error(ctx.handle) == 0
     params = otq.make_params(128, w.bits, w.scheme, 42)
-    _check_sampled_codes(cache, params, k, v, w.batch, w.heads_kv, w.seq, 20000, 1)
+    rep, srep = _check_sampled_codes(cache, params, k, v, w.batch, w.heads_kv, w.seq, 20000, 1)
     # the appended slot of every head
-    _check_sampled_codes_slot(cache, params, k, v, w)
+    _check_sampled_codes_slot(cache, params, k, v, w, rep)
+    assert rep.ok() and srep.ok(), (rep, srep)
     _check_sampled_decode(cache, params, q, out, [w.seq] * w.batch, w.batch, w.heads_kv, w.heads_q,
                           [(0, 0), (3, 17), (15, 31)])
 
 
-def _check_sampled_codes_slot(cache, params, k, v, w):
+def _check_sampled_codes_slot(cache, params, k, v, w, rep):
     B, H, N = w.batch, w.heads_kv, w.seq
     for which, x, role in (("k", k, params.roles()[0]), ("v", v, params.roles()[1])):
         xs = x[:, :, -1].float().cpu().numpy().reshape(-1, 128)
         ora = otq.encode(xs, role, params)
         codes = cache.plane(f"{which}_codes").view(B, H, N, role.bits * 16)[:, :, -1].cpu().numpy()
-        rep = P.BandReport()
         P.compare_codes(otq.unpack_codes(codes.reshape(-1, role.bits * 16), role.bits, 128), ora,
                         ocb.lloyd_max(128, role.bits).bounds32, rep)
-        assert rep.ok(), rep
+        assert rep.ok_out_of_band(), rep
 
 
 @pytest.mark.parametrize("dist", ["gauss", "lowrank", "student3"])
@@ -148,7 +153,8 @@ def test_config3_scheme_sweep(dist, scheme, n):
     out = tq.tq_decode_attention(ctx.handle, cache, q, lens, w.seq)
     torch.cuda.synchronize()
     params = otq.make_params(128, n, scheme, 42)
-    _check_sampled_codes(cache, params, k, v, w.batch, w.heads_kv, w.seq, 3000, n)
+    rep, srep = _check_sampled_codes(cache, params, k, v, w.batch, w.heads_kv, w.seq, 3000, n)
+    assert rep.ok() and srep.ok(), (rep, srep)
     _check_sampled_decode(cache, params, q, out, [w.seq] * w.batch, w.batch, w.heads_kv, w.heads_q,
                           [(1, 5)])
 
@@ -163,7 +169,8 @@ def test_config4_gqa_long_context_64_splits():
     out = tq.tq_decode_attention(ctx.handle, cache, q, lens, w.seq, splits=w.splits)
     torch.cuda.synchronize()
     params = otq.make_params(128, w.bits, w.scheme, 42)
-    _check_sampled_codes(cache, params, k, v, w.batch, w.heads_kv, w.seq, 20000, 4)
+    rep, srep = _check_sampled_codes(cache, params, k, v, w.batch, w.heads_kv, w.seq, 20000, 4)
+    assert rep.ok() and srep.ok(), (rep, srep)
     _check_sampled_decode(cache, params, q, out, [w.seq], w.batch, w.heads_kv, w.heads_q, [(0, 2), (0, 7)])
 
 
