@@ -46,10 +46,14 @@
  *  token slots (row-major); a token's slot holds one fixed-size record.
  *
  *  Code records: a vector's d coordinates each get a b-bit index into the
- *  Lloyd-Max codebook. Coordinate i's index occupies bits [b*i, b*i + b) of
- *  a d*b-bit little-endian bit string (string bit k = bit k % 8 of byte
- *  k / 8); the record is d*b/8 bytes. Index 0 is the most negative centroid.
- *  Sign records (QJL): bit i of a d-bit string in the same order is 1 when
+ *  Lloyd-Max codebook (index 0 = the most negative centroid). The d/2
+ *  coordinate pairs (2p, 2p+1), p = 4n + t (t = p mod 4), are stored in slot
+ *  order: pair p occupies slot (d/8) t + n, so coordinate i = 8n + 2t + e
+ *  (e = i mod 2) has its index at bit offset b ((d/4) t + 2n + e) of the
+ *  record's d*b-bit little-endian string (string bit k = bit k % 8 of byte
+ *  k / 8); the record is d*b/8 bytes. (With d = 128 the 16 pairs a tensor-core
+ *  thread consumes -- fixed t, n = 0..15 -- are contiguous.)
+ *  Sign records (QJL): the same offsets with b = 1; the bit is 1 when
  *  (S r)_i >= 0. Norm records: float32.
  *
  *  Per scheme, for a budget of n bits per coordinate ([TQ-stats]
@@ -88,8 +92,9 @@
  *    (+ rho sqrt(pi/2)/d D H S^T sigma, sigma_i = +/-1, for sketched vectors;
  *     D and H dropped for TQ_SCHEME_KV).
  *
- *  KIVI records (TQ_SCHEME_KIVI, [KIVI-geom]): 2-bit codes per element in the
- *  same bit-string layout (d/4 bytes per token) for both K and V; float16
+ *  KIVI records (TQ_SCHEME_KIVI, [KIVI-geom]): 2-bit codes per element in
+ *  plain channel order, channel i at bits [2i, 2i+2) (d/4 bytes per token),
+ *  for both K and V; float16
  *  (zero, step) pairs per group, zero = fp16(group min), step =
  *  fp16((max - min) / 3) with the quotient in fp64, code =
  *  clamp(round_half_even((x - zero) / step), 0, 3) (0 when step == 0).

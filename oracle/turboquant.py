@@ -34,10 +34,12 @@ Readings where the pages are silent (each is listed in the design doc):
   (+ rho sqrt(pi/2)/m * D H S^T sigma for sketched vectors).
 * a zero vector stores nu = 0, the codes of y = 0, all sign bits 1, rho = 0.
 
-Storage format (the library's, stated in include/tq.h and restated here):
-coordinate i's b-bit code occupies bits [b*i, b*i + b) of the vector's
-little-endian bit string (bit k lives in byte k // 8 at position k % 8);
-sign bit i is bit i of a d-bit string in the same order.
+Storage format (the library's, stated in include/tq.h and restated here): the
+vector's d coordinates form d/2 pairs (2p, 2p+1); pair p = 4n + t (t = p mod 4)
+sits in slot (d/8) t + n, so coordinate i = 8n + 2t + e (e = i mod 2) has its
+b-bit code at bit offset b ((d/4) t + 2n + e) of the record's little-endian
+bit string (string bit k is bit k % 8 of byte k // 8). Sign bits use the same
+offsets with b = 1. For d = 8 this is the natural order.
 """
 
 from dataclasses import dataclass
@@ -175,27 +177,43 @@ def decode(enc: Encoded, params: Params) -> np.ndarray:
 # storage format
 # ----------------------------------------------------------------------------
 
+def slot_order(d: int) -> np.ndarray:
+    """Position (in units of one code) of coordinate i in the record: (d/4) t + 2n + e."""
+    if d % 8:
+        raise ValueError("d must be a multiple of 8")
+    i = np.arange(d)
+    n, t, e = i >> 3, (i >> 1) & 3, i & 1
+    return (d // 4) * t + 2 * n + e
+
+
 def pack_codes(idx: np.ndarray, bits: int) -> np.ndarray:
-    """[N, d] integer codes -> [N, bits*d/8] bytes, code i at stream bits [bits*i, bits*i+bits)."""
+    """[N, d] integer codes -> [N, bits*d/8] bytes in the slot order above."""
     idx = np.asarray(idx, dtype=np.int64)
     N, d = idx.shape
-    planes = (idx[:, :, None] >> np.arange(bits)[None, None, :]) & 1  # [N, d, bits], stream order
-    return np.packbits(planes.reshape(N, d * bits).astype(np.uint8), axis=1, bitorder="little")
+    pos = slot_order(d)
+    stream = np.zeros((N, d * bits), dtype=np.uint8)
+    for k in range(bits):
+        stream[:, bits * pos + k] = (idx >> k) & 1
+    return np.packbits(stream, axis=1, bitorder="little")
 
 
 def unpack_codes(packed: np.ndarray, bits: int, d: int) -> np.ndarray:
     packed = np.asarray(packed, dtype=np.uint8)
-    N = packed.shape[0]
-    stream = np.unpackbits(packed, axis=1, bitorder="little")[:, : d * bits].reshape(N, d, bits)
-    return np.sum(stream.astype(np.int64) << np.arange(bits)[None, None, :], axis=2)
+    stream = np.unpackbits(packed, axis=1, bitorder="little")[:, : d * bits].astype(np.int64)
+    pos = slot_order(d)
+    return sum(stream[:, bits * pos + k] << k for k in range(bits))
 
 
 def pack_signs(signs: np.ndarray) -> np.ndarray:
-    return np.packbits(np.asarray(signs, dtype=np.uint8), axis=1, bitorder="little")
+    signs = np.asarray(signs, dtype=np.uint8)
+    stream = np.zeros_like(signs)
+    stream[:, slot_order(signs.shape[1])] = signs
+    return np.packbits(stream, axis=1, bitorder="little")
 
 
 def unpack_signs(packed: np.ndarray, d: int) -> np.ndarray:
-    return np.unpackbits(np.asarray(packed, dtype=np.uint8), axis=1, bitorder="little")[:, :d].astype(bool)
+    stream = np.unpackbits(np.asarray(packed, dtype=np.uint8), axis=1, bitorder="little")[:, :d]
+    return stream[:, slot_order(d)].astype(bool)
 
 
 def encoded_from_storage(role: Role, norm, codes_packed, d, signs_packed=None, rnorm=None) -> Encoded:

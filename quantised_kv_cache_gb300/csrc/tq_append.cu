@@ -57,9 +57,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) append_tq_kernel(AppendKernelA
   if (tid < L) s_cent[tid] = a.centroids[tid];
   if (tid < L - 1) s_bound[tid] = a.bounds[tid];
   if (QJL) {
+    // entry (i, 4L + m) = S[row][i] for the coordinate row = 8(L/2) + 2m + (L&1) whose sign
+    // bit is bit L of sign word m, so one ballot per m yields the record's word m
     for (int e = tid; e < kD * kD; e += blockDim.x) {
-      const int i = e >> 7, col = e & 127, l = col >> 2, j = col & 3;
-      s_st[e] = __ldg(a.sketch + (l + 32 * j) * kD + i);
+      const int i = e >> 7, col = e & 127, l = col >> 2, m = col & 3;
+      const int row = 8 * (l >> 1) + 2 * m + (l & 1);
+      s_st[e] = __ldg(a.sketch + row * kD + i);
     }
   }
   float dg[4];
@@ -104,7 +107,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2) append_tq_kernel(AppendKernelA
 #pragma unroll
       for (int j = 0; j < 4; ++j) y[j] = (nu > 0.f) ? (x[j] / nu) * dg[j] : 0.f;
       if (ROT) wht128(y, lane);
-      uint32_t field = 0;
       int idx[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -112,9 +114,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) append_tq_kernel(AppendKernelA
 #pragma unroll
         for (int k = 0; k < L - 1; ++k) c += (y[j] >= bnd[k]) ? 1 : 0;
         idx[j] = c;
-        field |= (uint32_t)c << (BITS * j);
       }
-      const uint32_t word = pack_record_word<BITS>(field, lane);
+      const uint32_t fa = (uint32_t)idx[0] | ((uint32_t)idx[1] << BITS);
+      const uint32_t fb = (uint32_t)idx[2] | ((uint32_t)idx[3] << BITS);
+      const uint32_t word = pack_slot_word<BITS>(fa, fb, lane);
       if (ok) {
         if (lane < 4 * BITS) reinterpret_cast<uint32_t *>(a.codes + slot * (BITS * kD / 8))[lane] = word;
         if (!QJL && lane == 0) a.norms[slot] = nu;

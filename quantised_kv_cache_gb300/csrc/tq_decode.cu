@@ -168,8 +168,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
   const float *kr = KQJL ? a.k_rnorm + slot0 : nullptr;
   const float *vr = VQJL ? a.v_rnorm + slot0 : nullptr;
   const int my_tok = tile_token_of_lane(lane);
-  constexpr uint32_t kMaskK = (1u << KB) - 1, kMaskV = (1u << VB) - 1;
-  const int sign_shift = (4 * lane) & 31, sign_word = lane >> 3;
 
   for (int tile = t_begin + warp * kTile; tile < t_end; tile += kDecodeWarps * kTile) {
     // ---- scores for 8 tokens
@@ -177,17 +175,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
 #pragma unroll
     for (int jj = 0; jj < kTile; ++jj) {
       const int t = min(tile + jj, t_end - 1);
-      const uint32_t f = lane_code_field<KB>(kc + (size_t)t * (KB * 4), lane);
+      uint32_t code[4];
+      lane_codes<KB>(kc + (size_t)t * (KB * 4), lane, code);
       float c[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) c[j] = s_cb[(f >> (KB * j)) & kMaskK];
+      for (int j = 0; j < 4; ++j) c[j] = s_cb[code[j]];
       const float nu = __ldg(kn + t);
       float sg[4];
       float rk = 0.f;
       if (KQJL) {
-        const uint32_t sw = __ldg(ks + (size_t)t * 4 + sign_word) >> sign_shift;
+        uint32_t sb[4];
+        lane_signs(ks + (size_t)t * 4, lane, sb);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sg[j] = ((sw >> j) & 1u) ? 1.f : -1.f;
+        for (int j = 0; j < 4; ++j) sg[j] = sb[j] ? 1.f : -1.f;
         rk = __ldg(kr + t);
       }
 #pragma unroll
@@ -228,15 +228,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
       const int t = tile + jj;
       if (t >= t_end) break;
       const int src = lane_of_tile_token(jj);
-      const uint32_t f = lane_code_field<VB>(vc + (size_t)t * (VB * 4), lane);
+      uint32_t code[4];
+      lane_codes<VB>(vc + (size_t)t * (VB * 4), lane, code);
       float c[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) c[j] = s_cb[16 + ((f >> (VB * j)) & kMaskV)];
+      for (int j = 0; j < 4; ++j) c[j] = s_cb[16 + code[j]];
       const float nu = __ldg(vn + t);
-      uint32_t sw = 0;
+      uint32_t sb[4] = {0u, 0u, 0u, 0u};
       float rv = 0.f;
       if (VQJL) {
-        sw = __ldg(vs + (size_t)t * 4 + sign_word) >> sign_shift;
+        lane_signs(vs + (size_t)t * 4, lane, sb);
         rv = __ldg(vr + t);
       }
 #pragma unroll
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
         if (VQJL) {
           const float wr = pj * rv;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) sacc[g][j] += ((sw >> j) & 1u) ? wr : -wr;
+          for (int j = 0; j < 4; ++j) sacc[g][j] += sb[j] ? wr : -wr;
         }
       }
     }
@@ -377,7 +378,7 @@ __device__ __forceinline__ void kivi_token(const uint32_t *codes, const uint32_t
                                            bool quantised, int t, int R, int lane, const float (&pz)[4],
                                            const float (&ps)[4], float (&x)[4]) {
   if (quantised) {
-    const uint32_t f = lane_code_field<2>(codes + (size_t)t * 8, lane);
+    const uint32_t f = kivi_lane_field(codes + (size_t)t * 8, lane);
     if (PER_CHANNEL) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) x[c] = fmaf(ps[c], (float)((f >> (2 * c)) & 3u), pz[c]);

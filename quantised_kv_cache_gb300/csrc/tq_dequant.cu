@@ -35,11 +35,12 @@ __global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
   const long long bh = vec / n;
   const int t = a.t0 + (int)(vec % n);
   const size_t slot = (size_t)bh * a.capacity + t;
-  const uint32_t f = lane_code_field<BITS>(reinterpret_cast<const uint32_t *>(a.codes) + slot * (BITS * 4), lane);
+  uint32_t code[4];
+  lane_codes<BITS>(reinterpret_cast<const uint32_t *>(a.codes) + slot * (BITS * 4), lane, code);
   const float nu = __ldg(a.norms + slot);
   float y[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) y[j] = nu * s_c[(f >> (BITS * j)) & ((1u << BITS) - 1)];
+  for (int j = 0; j < 4; ++j) y[j] = nu * s_c[code[j]];
   if (QJL) {
     const uint32_t *srec = reinterpret_cast<const uint32_t *>(a.signs) + slot * 4;
     uint32_t sw[4];
@@ -47,7 +48,9 @@ __global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
     for (int w = 0; w < 4; ++w) sw[w] = __ldg(srec + w);
     float r[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k < kD; ++k) {
-      const float sg = ((sw[k >> 5] >> (k & 31)) & 1u) ? 1.f : -1.f;
+      // coordinate k = 8n + 2t + e sits at sign word t, bit 2n + e
+      const int word = (k >> 1) & 3, bit = 2 * (k >> 3) + (k & 1);
+      const float sg = ((sw[word] >> bit) & 1u) ? 1.f : -1.f;
       const float4 s = __ldg(reinterpret_cast<const float4 *>(a.sketch + k * kD) + lane);
       r[0] = fmaf(s.x, sg, r[0]);
       r[1] = fmaf(s.y, sg, r[1]);

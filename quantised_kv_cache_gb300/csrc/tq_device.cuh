@@ -71,35 +71,85 @@ __device__ __forceinline__ void set_error(int *err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-// The 4*BITS-bit field holding lane's four codes (coordinates 4L..4L+3) in a
-// record of 4*BITS 32-bit words.
+// Record layout of a d = 128 vector's codes (include/tq.h): pair p = (2p, 2p+1),
+// p = 4n + t, sits in slot 16t + n; slot s holds 2*BITS bits at bit offset
+// 2*BITS*s (low BITS bits: even coordinate). Lane L of a warp that owns
+// coordinates 4L..4L+3 owns pairs 2L (slot 32(L&1) + L/2) and 2L+1 (that + 16).
+__device__ __forceinline__ int lane_slot_a(int lane) { return 32 * (lane & 1) + (lane >> 1); }
+
 template <int BITS>
-__device__ __forceinline__ uint32_t lane_code_field(const uint32_t *rec, int lane) {
-  constexpr int W = 4 * BITS;
-  const int bit = 4 * BITS * lane;
+__device__ __forceinline__ uint32_t record_field(const uint32_t *rec, int slot) {
+  constexpr int F = 2 * BITS;
+  constexpr int W = 4 * BITS;  // words in the record
+  const int bit = F * slot;
   const int wi = bit >> 5, off = bit & 31;
   uint32_t lo = __ldg(rec + wi);
-  if (off + 4 * BITS <= 32) return lo >> off;
-  uint32_t hi = __ldg(rec + ((wi + 1 < W) ? wi + 1 : wi));
-  return __funnelshift_r(lo, hi, off);
+  uint32_t v;
+  if (off + F <= 32) {
+    v = lo >> off;
+  } else {
+    uint32_t hi = __ldg(rec + ((wi + 1 < W) ? wi + 1 : wi));
+    v = __funnelshift_r(lo, hi, off);
+  }
+  return v & ((1u << F) - 1u);
 }
 
-// Pack each lane's 4*BITS-bit field into the record's little-endian bit
-// string; lanes 0..4*BITS-1 return their 32-bit word.
+// Codes of this lane's coordinates 4L..4L+3 (warp-per-vector layout).
 template <int BITS>
-__device__ __forceinline__ uint32_t pack_record_word(uint32_t field, int lane) {
-  constexpr int F = 4 * BITS;                    // bits per lane
-  constexpr int K = (32 + F - 1) / F + 1;        // lanes touching one word
+__device__ __forceinline__ void lane_codes(const uint32_t *rec, int lane, uint32_t (&c)[4]) {
+  constexpr uint32_t M = (1u << BITS) - 1u;
+  const int sa = lane_slot_a(lane);
+  const uint32_t fa = record_field<BITS>(rec, sa);
+  const uint32_t fb = record_field<BITS>(rec, sa + 16);
+  c[0] = fa & M;
+  c[1] = fa >> BITS;
+  c[2] = fb & M;
+  c[3] = fb >> BITS;
+}
+
+// Sign bits of this lane's coordinates 4L..4L+3 from a 4-word sign record
+// (same slot layout with BITS = 1: word t holds slots 16t..16t+15).
+__device__ __forceinline__ void lane_signs(const uint32_t *srec, int lane, uint32_t (&sg)[4]) {
+  const int w = 2 * (lane & 1), sh = 2 * (lane >> 1);
+  const uint32_t a = __ldg(srec + w) >> sh, b = __ldg(srec + w + 1) >> sh;
+  sg[0] = a & 1u;
+  sg[1] = (a >> 1) & 1u;
+  sg[2] = b & 1u;
+  sg[3] = (b >> 1) & 1u;
+}
+
+// Assemble the record from every lane's two pair fields; lanes 0..4*BITS-1
+// return their 32-bit word of the record.
+template <int BITS>
+__device__ __forceinline__ uint32_t pack_slot_word(uint32_t field_a, uint32_t field_b, int lane) {
+  constexpr int F = 2 * BITS;                  // bits per slot
+  constexpr int K = (32 + F - 1) / F + 1;      // slots touching one word
+  const uint32_t both = field_a | (field_b << F);
   const int first = (32 * lane) / F;
   uint32_t word = 0;
 #pragma unroll
   for (int k = 0; k < K; ++k) {
-    const int src = first + k;
-    uint32_t c = __shfl_sync(kFull, field, src & 31);
-    const int shift = F * src - 32 * lane;
-    if (src < 32 && shift > -F && shift < 32) word |= (shift >= 0) ? (c << shift) : (c >> (-shift));
+    const int slot = first + k;
+    const int src = 2 * (slot & 15) + ((slot >> 5) & 1);
+    const uint32_t v = __shfl_sync(kFull, both, src & 31);
+    const uint32_t f = ((slot >> 4) & 1) ? (v >> F) : (v & ((1u << F) - 1u));
+    const int shift = F * slot - 32 * lane;
+    if (slot < 64 && shift > -F && shift < 32) word |= (shift >= 0) ? (f << shift) : (f >> (-shift));
   }
   return word;
+}
+
+// KIVI records keep the plain order: channel i's 2-bit code at bits [2i, 2i+2).
+__device__ __forceinline__ uint32_t kivi_lane_field(const uint32_t *rec, int lane) {
+  return __ldg(rec + (lane >> 2)) >> (8 * (lane & 3));  // 8 bits: channels 4L..4L+3
+}
+
+// lanes 0..7 return word w = the 8-bit fields of lanes 4w..4w+3
+__device__ __forceinline__ uint32_t kivi_pack_word(uint32_t field8, int lane) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w |= (__shfl_sync(kFull, field8 & 0xffu, (4 * lane + k) & 31)) << (8 * k);
+  return w;
 }
 
 }  // namespace tq

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
     uint32_t field = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf[c], sf[c]) << (2 * c);
-    const uint32_t word = pack_record_word<2>(field, lane);
+    const uint32_t word = kivi_pack_word(field, lane);
     if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + ((size_t)bh * a.capacity + j) * (kD / 4))[lane] = word;
   }
 }
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, in
   uint32_t field = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf, sf) << (2 * c);
-  const uint32_t word = pack_record_word<2>(field, lane);
+  const uint32_t word = kivi_pack_word(field, lane);
   const size_t slot = (size_t)bh * a.capacity + j;
   if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + slot * (kD / 4))[lane] = word;
   if ((lane & 7) == 0) {
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(256) kivi_dequant_kernel(KiviDequantKernelArgs
   float y[4] = {0.f, 0.f, 0.f, 0.f};
   const size_t slot = (size_t)bh * a.capacity + j;
   if (j < nq) {
-    const uint32_t f = lane_code_field<2>(reinterpret_cast<const uint32_t *>(a.codes) + slot * (kD / 16), lane);
+    const uint32_t f = kivi_lane_field(reinterpret_cast<const uint32_t *>(a.codes) + slot * (kD / 16), lane);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t st;

@@ -54,6 +54,7 @@ def test_packing_matches_hand_worked_examples(row):
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
 def test_pack_matches_brute_force_bit_setting(bits):
+    """Slot order written out per coordinate: i = 8n + 2t + e -> code offset 32t + 2n + e."""
     g = np.random.default_rng(bits)
     d = 128
     idx = g.integers(0, 1 << bits, size=(5, d))
@@ -61,11 +62,18 @@ def test_pack_matches_brute_force_bit_setting(bits):
     for n in range(5):
         stream = bytearray(bits * d // 8)
         for i in range(d):
+            nn, t, e = i // 8, (i // 2) % 4, i % 2
+            off = 32 * t + 2 * nn + e
             for k in range(bits):
                 if (idx[n, i] >> k) & 1:
-                    pos = bits * i + k
+                    pos = bits * off + k
                     stream[pos // 8] |= 1 << (pos % 8)
         assert bytes(got[n]) == bytes(stream)
+    # a tensor-core thread's 16 pairs (fixed t) are contiguous: 32*bits bits from 32*bits*t
+    t = 2
+    want = [(i, c) for i in range(d) if (i // 2) % 4 == t for c in [idx[0, i]]]
+    seg = tq.unpack_codes(got[:1], bits, d)[0]
+    assert [seg[i] for i, _ in want] == [c for _, c in want]
 
 
 # ---------------------------------------------------------------- quantiser
@@ -283,8 +291,12 @@ def test_kivi_two_bit_packing_roundtrip():
     g = np.random.default_rng(3)
     c = g.integers(0, 4, size=(7, 128)).astype(np.uint8)
     np.testing.assert_array_equal(kivi.unpack2(kivi.pack2(c), 128), c)
-    # same stream layout as the TurboQuant codes at 2 bits
-    np.testing.assert_array_equal(kivi.pack2(c), tq.pack_codes(c.astype(np.int64), 2))
+    # plain channel order: channel i at bits [2i, 2i+2)
+    for n in range(7):
+        want = bytearray(32)
+        for i in range(128):
+            want[(2 * i) // 8] |= int(c[n, i]) << ((2 * i) % 8)
+        assert bytes(kivi.pack2(c)[n]) == bytes(want)
 
 
 def test_bf16_rounding_is_nearest_even():
