@@ -262,6 +262,34 @@ tq_status tq_draw_params(uint64_t seed, int d, int8_t *h_diag, float *h_sketch);
  * quantise kernels. Pass NULLs to stop. The caller owns the events. */
 tq_status tq_set_profile_events(tq_ctx *ctx, void *start, void *stop, void *append_start, void *append_stop);
 
+/* Decode attention without a caller-provided workspace. The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory themselves (an application that owns the whole device-memory budget
+ * and hands this library only cache and output buffers, a latency-critical
+ * decode loop that must never enter the CUDA allocator, a runtime with no
+ * access to cudaMalloc). Arguments and results are those of
+ * tq_decode_attention without d_workspace / workspace_bytes; the workspace
+ * is a fixed array of tq_static_scratch_bytes() bytes (8 MiB) compiled into
+ * the library, which every GPU that loads the library holds until the
+ * process exits.
+ *  - The call allocates nothing: no cudaMalloc, cudaFree or allocating
+ *    library routine.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current, which must be the context's device) and caches it;
+ *    make that first call before any stream capture begins.
+ *  - Requests whose workspace (tq_workspace_size) exceeds the array return
+ *    TQ_ERR_WORKSPACE before any launch.
+ *  - Every call shares the one array and the array keeps the last call's
+ *    contents; nothing in it needs to start at zero. Calls that overlap on
+ *    the GPU (different streams, or devices sharing a context) race on the
+ *    array: serialise them. */
+tq_status tq_decode_attention_static(const tq_ctx *ctx, const tq_cache *cache, const void *d_q, int q_dtype,
+                                     int batch, int heads_q, int heads_kv, const int32_t *d_seq_lens,
+                                     int max_len, int splits, float *d_out, void *stream);
+
+/* Size in bytes of the array tq_decode_attention_static uses. */
+size_t tq_static_scratch_bytes(void);
+
 /* Synchronise `stream`, then read and clear the context's sticky device
  * error word into *code (TQ_OK when nothing was recorded). */
 tq_status tq_get_device_error(const tq_ctx *ctx, void *stream, int *code);

@@ -72,6 +72,9 @@ _SIGNATURES = {
     "tq_draw_params": (_i, [ctypes.c_uint64, _i, _vp, _vp]),
     "tq_get_device_error": (_i, [_vp, _vp, ctypes.POINTER(_i)]),
     "tq_set_profile_events": (_i, [_vp, _vp, _vp, _vp, _vp]),
+    "tq_decode_attention_static": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _i, _i, _i, _i, _vp, _i, _i, _vp,
+                                        _vp]),
+    "tq_static_scratch_bytes": (_sz, []),
 }
 
 _lib = None
@@ -187,6 +190,23 @@ def tq_decode_attention(ctx, cache: "Cache", q: torch.Tensor, seq_lens: torch.Te
                                     _ptr(seq_lens), max_len, splits, _ptr(workspace), workspace.numel(),
                                     _ptr(out), _stream(stream)), "tq_decode_attention")
     return out
+
+
+def tq_decode_attention_static(ctx, cache: "Cache", q: torch.Tensor, seq_lens: torch.Tensor, max_len: int,
+                               splits: int = 0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """tq_decode_attention with the library's built-in scratch array instead of a workspace."""
+    B, Hq, d = q.shape
+    assert q.is_contiguous() and seq_lens.dtype == torch.int32
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    check(lib().tq_decode_attention_static(ctx, ctypes.byref(cache.struct), _ptr(q), _dtype_code(q), B, Hq,
+                                           cache.struct.heads_kv, _ptr(seq_lens), max_len, splits, _ptr(out),
+                                           _stream(stream)), "tq_decode_attention_static")
+    return out
+
+
+def tq_static_scratch_bytes() -> int:
+    return lib().tq_static_scratch_bytes()
 
 
 def tq_dequantize(ctx, cache: "Cache", t0: int, t1: int, seq_lens: Optional[torch.Tensor] = None,
