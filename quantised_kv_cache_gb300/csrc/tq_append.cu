@@ -232,6 +232,10 @@ int dispatch_bits(int bits, const AppendKernelArgs &k, long long total, cudaStre
 }  // namespace
 
 int launch_append_tq(const AppendArgs &a, void *stream) {
+  if (a.ctx) {
+    const int r = launch_append2(a, a.ctx, stream);
+    if (r != TQ_ERR_UNSUPPORTED) return r;
+  }
   AppendKernelArgs k{};
   k.x = a.x;
   k.batch = a.batch;

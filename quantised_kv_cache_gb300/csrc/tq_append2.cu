@@ -1,0 +1,202 @@
+// Append-quantise with one thread per vector (vectors without a QJL sketch:
+// keys of KV / KQV, values of KV).
+//
+// "Statistical Inference ... Inspired by TurboQuant", technical summary,
+// "Quantisation schemes": normalise, rotate with the randomised WHT, code each
+// coordinate with the Lloyd-Max codebook; "KVQuant++", "Fast codebook lookup":
+// the code is a boundary count, found by binary search.
+//
+// A thread holds its whole 128-coordinate vector in registers, so the seven
+// butterfly stages of the Walsh-Hadamard transform need no shuffles. The
+// transform is left unnormalised (entries +/-1) and the vector is not divided
+// by its norm: instead each vector compares against its own scaled boundaries
+// nu * sqrt(128) * b_j (nu * b_j without rotation), which decides every code
+// exactly as y = H D x / (nu sqrt(128)) against b_j would. The +/-1 diagonal D
+// arrives as kernel parameters, so its multiplications read constant-bank
+// operands. The boundaries are symmetric about 0, so a code is the sign of y
+// plus a binary search of |y| over the positive boundaries.
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace {
+
+struct Append2Args {
+  const void *x;
+  int batch, heads, n_new, capacity;
+  const int32_t *seq_lens;
+  uint8_t *codes;
+  float *norms;
+  int *error;
+  float diag[kD];
+  float bounds[kMaxLevels];  // 2^BITS - 1 used
+};
+
+constexpr float kSqrtD = 11.313708498984761f;  // sqrt(128)
+
+// count of positive boundaries P[0..H-1] (ascending) at or below a >= 0
+template <int H>
+__device__ __forceinline__ int count_pos(float a, const float (&P)[H]) {
+  if (H == 1) {
+    return a >= P[0] ? 1 : 0;
+  } else if (H == 3) {
+    int m = a >= P[1] ? 2 : 0;
+    const float c = m ? P[2] : P[0];
+    return m + (a >= c ? 1 : 0);
+  } else {  // H == 7
+    int m = a >= P[3] ? 4 : 0;
+    const float c2 = m ? P[5] : P[1];
+    m += a >= c2 ? 2 : 0;
+    const float c1 = (m & 4) ? ((m & 2) ? P[6] : P[4]) : ((m & 2) ? P[2] : P[0]);
+    return m + (a >= c1 ? 1 : 0);
+  }
+}
+
+template <int BITS, bool ROT, bool BF16>
+__global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Append2Args a) {
+  constexpr int L = 1 << BITS, H = L / 2 - 1;
+  const long long total = (long long)a.batch * a.heads * a.n_new;
+  for (long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x; vec < total;
+       vec += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(vec % a.n_new);
+    const long long bh = vec / a.n_new;
+    const int b = (int)(bh / a.heads);
+    const int len = __ldg(a.seq_lens + b);
+    const bool ok = len >= 0 && len + a.n_new <= a.capacity;  // a sequence that would not fit is skipped whole
+    if (!ok) {
+      if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);
+      continue;
+    }
+    const long long slot = bh * a.capacity + len + t;
+
+    float x[kD];
+    if (BF16) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.x) + vec * kD);
+#pragma unroll
+      for (int k = 0; k < kD / 8; ++k) {
+        const uint4 w = __ldg(src + k);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[8 * k + 2 * j] = __uint_as_float(ww[j] << 16);
+          x[8 * k + 2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+        }
+      }
+    } else {
+      const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(a.x) + vec * kD);
+#pragma unroll
+      for (int k = 0; k < kD / 4; ++k) {
+        const float4 f = __ldg(src + k);
+        x[4 * k] = f.x;
+        x[4 * k + 1] = f.y;
+        x[4 * k + 2] = f.z;
+        x[4 * k + 3] = f.w;
+      }
+    }
+    // squared norm by a pairwise tree (matches the warp design's rounding order closely)
+    float sq[kD / 2];
+#pragma unroll
+    for (int i = 0; i < kD / 2; ++i) sq[i] = fmaf(x[2 * i], x[2 * i], x[2 * i + 1] * x[2 * i + 1]);
+#pragma unroll
+    for (int w = kD / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) sq[i] = sq[i] + sq[i + w];
+    const float nu = sqrtf(sq[0]);
+
+    if (ROT) {
+#pragma unroll
+      for (int i = 0; i < kD; ++i) x[i] *= a.diag[i];
+#pragma unroll
+      for (int hs = 1; hs < kD; hs <<= 1)
+#pragma unroll
+        for (int i = 0; i < kD; ++i)
+          if ((i & hs) == 0) {
+            const float u = x[i], v = x[i + hs];
+            x[i] = u + v;
+            x[i + hs] = u - v;
+          }
+    }
+    // positive boundaries scaled to this vector: b_{L/2 + k} * nu (* sqrt(128)); a zero
+    // vector keeps the unit boundaries so that y = 0 codes to L/2 as the format requires
+    const float s = (nu > 0.f) ? (ROT ? nu * kSqrtD : nu) : 1.f;
+    float P[H];
+#pragma unroll
+    for (int k = 0; k < H; ++k) P[k] = a.bounds[L / 2 + k] * s;
+
+    // code i: sign half plus the count of positive boundaries below |y|; nu = 0 gives y = 0 -> L/2
+    uint32_t word[4 * BITS];
+#pragma unroll
+    for (int w = 0; w < 4 * BITS; ++w) word[w] = 0u;
+#pragma unroll
+    for (int i = 0; i < kD; ++i) {
+      const float y = x[i];
+      const int m = count_pos<H>(fabsf(y), P);
+      const int code = (y >= 0.f) ? (L / 2 + m) : (L / 2 - 1 - m);
+      // slot order: coordinate i = 8n + 2t + e at code offset 32t + 2n + e
+      const int n = i >> 3, tt = (i >> 1) & 3, e = i & 1;
+      const int off = BITS * (32 * tt + 2 * n + e);
+      word[off >> 5] |= (uint32_t)code << (off & 31);
+      if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= (uint32_t)code >> (32 - (off & 31));
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(a.codes + slot * (BITS * kD / 8));
+#pragma unroll
+    for (int k = 0; k < BITS; ++k) dst[k] = make_uint4(word[4 * k], word[4 * k + 1], word[4 * k + 2], word[4 * k + 3]);
+    a.norms[slot] = nu;
+  }
+}
+
+int g_sms2 = 0;
+
+template <int BITS, bool ROT, bool BF16>
+int go(const Append2Args &k, long long total, cudaStream_t st) {
+  if (g_sms2 == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms2, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms2 <= 0) g_sms2 = 152;
+  }
+  long long blocks = (total + 127) / 128;
+  const long long cap = 4LL * g_sms2;  // enough resident threads to cover memory latency
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  append2_kernel<BITS, ROT, BF16><<<(unsigned)blocks, 128, 0, st>>>(k);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+template <bool ROT, bool BF16>
+int dispatch(int bits, const Append2Args &k, long long total, cudaStream_t st) {
+  switch (bits) {
+    case 2: return go<2, ROT, BF16>(k, total, st);
+    case 3: return go<3, ROT, BF16>(k, total, st);
+    case 4: return go<4, ROT, BF16>(k, total, st);
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+// Thread-per-vector append for vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise.
+int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
+  if (a.role.qjl || a.role.bits < 2) return TQ_ERR_UNSUPPORTED;
+  Append2Args k{};
+  k.x = a.x;
+  k.batch = a.batch;
+  k.heads = a.heads;
+  k.n_new = a.n_new;
+  k.capacity = a.capacity;
+  k.seq_lens = a.seq_lens;
+  k.codes = a.codes;
+  k.norms = a.norms;
+  k.error = a.error;
+  for (int i = 0; i < kD; ++i) k.diag[i] = (float)ctx->diag[i];
+  const float *src = (a.centroids == ctx->dparams->k_centroids) ? ctx->k_bounds : ctx->v_bounds;
+  for (int i = 0; i < (1 << a.role.bits) - 1; ++i) k.bounds[i] = src[i];
+  const long long total = (long long)a.batch * a.heads * a.n_new;
+  cudaStream_t st = (cudaStream_t)stream;
+  const bool bf16 = a.dtype == TQ_BF16;
+  if (a.role.rotate) return bf16 ? dispatch<true, true>(a.role.bits, k, total, st)
+                                 : dispatch<true, false>(a.role.bits, k, total, st);
+  return bf16 ? dispatch<false, true>(a.role.bits, k, total, st) : dispatch<false, false>(a.role.bits, k, total, st);
+}
+
+}  // namespace tq

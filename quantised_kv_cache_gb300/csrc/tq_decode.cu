@@ -558,6 +558,18 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   const int rows = a.batch * a.heads_q;
   qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
 
+  // the TMA / tensor-core kernel covers one query head per KV head
+  if (ctx->prof_decode_start) cudaEventRecord((cudaEvent_t)ctx->prof_decode_start, st);
+  int r2 = launch_decode2_g1(a, a.qprep, a.partials, stream);
+  if (r2 == TQ_OK) {
+    if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
+    CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
+                    ctx->dparams->diag, ctx->dparams->sketch, a.out};
+    combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  }
+  if (r2 != TQ_ERR_UNSUPPORTED) return r2;
+
   DecodeKernelArgs k{};
   const tq_cache *c = a.cache;
   k.k_codes = c->k_codes; k.k_norm = c->k_norm; k.k_signs = c->k_signs; k.k_rnorm = c->k_rnorm;

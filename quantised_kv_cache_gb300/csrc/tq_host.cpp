@@ -193,12 +193,23 @@ namespace tq {
 void choose_splits(int batch, int heads_kv, int max_len, int requested, int *splits, int *chunk) {
   int s = requested;
   if (s <= 0) {
-    // enough CTAs for several waves on 152 SMs, but chunks of >= 256 tokens
-    const int target_ctas = 152 * 8;
-    int units = std::max(1, batch * heads_kv);
-    s = (target_ctas + units - 1) / units;
-    s = std::min(s, std::max(1, max_len / 256));
-    s = std::max(1, std::min(s, 1024));
+    // Pick the split count that minimises (rounds of CTAs on 152 SMs x 2 CTAs)
+    // x (chunk tokens + a fixed per-CTA setup cost of about 64 tokens), with
+    // chunks of at least 256 tokens.
+    const long long slots = 152LL * 2;
+    const long long units = std::max(1, batch * heads_kv);
+    const int s_max = std::max(1, std::min(1024, max_len / 256));
+    double best = 1e300;
+    s = 1;
+    for (int c = 1; c <= s_max; ++c) {
+      const long long ctas = units * c;
+      const long long rounds = (ctas + slots - 1) / slots;
+      const double cost = (double)rounds * ((double)((max_len + c - 1) / c) + 64.0);
+      if (cost < best * 0.999) {
+        best = cost;
+        s = c;
+      }
+    }
   }
   s = std::max(1, std::min(s, std::max(1, max_len)));
   int c = (max_len + s - 1) / s;
@@ -420,6 +431,7 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.seq_lens = d_seq_lens;
   a.params = ctx->dparams;
   a.error = &ctx->dparams->error;
+  a.ctx = ctx;
   // K
   a.x = d_k;
   a.codes = cache->k_codes;

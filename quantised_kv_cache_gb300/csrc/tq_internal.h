@@ -76,8 +76,11 @@ struct AppendArgs {
   const float *bounds;
   const DevParams *params;
   int *error;
+  const tq_ctx *ctx;
 };
 int launch_append_tq(const AppendArgs &a, void *stream);
+// thread-per-vector append for vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise
+int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream);
 
 struct DecodeArgs {
   const tq_ctx *ctx;
@@ -91,6 +94,9 @@ struct DecodeArgs {
   float *out;
 };
 int launch_decode_tq(const DecodeArgs &a, void *stream);
+// TMA-staged, tensor-core decode for one query head per KV head; returns
+// TQ_ERR_UNSUPPORTED when the request falls outside what it covers.
+int launch_decode2_g1(const DecodeArgs &a, const float *qprep, float *partials, void *stream);
 int launch_decode_kivi(const DecodeArgs &a, void *stream);
 
 struct DequantArgs {

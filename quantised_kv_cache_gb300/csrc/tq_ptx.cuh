@@ -76,6 +76,18 @@ __device__ __forceinline__ void tma_load_1d(void *smem_dst, const void *gmem_src
       : "memory");
 }
 
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 // 8x8 b16 matrix transpose across the warp (fragment layout: lane (g,t) holds row g, cols 2t, 2t+1)
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;

@@ -76,7 +76,7 @@ def test_append_codes_bit_exact(scheme, n, dtype):
         # bytes identical wherever the codes are
         same = ~code_mism.any(axis=1)
         np.testing.assert_array_equal(packed[same], otq.pack_codes(ora.idx[same], role.bits))
-        np.testing.assert_allclose(gpu.norm, ora.norm, rtol=2e-7, atol=0)
+        np.testing.assert_allclose(gpu.norm, ora.norm, rtol=1e-6, atol=0)
         if role.qjl:
             srep = P.BandReport()
             P.compare_signs(gpu.signs, ora, srep, skip_rows=code_mism.any(axis=1))
@@ -175,8 +175,10 @@ def test_decode_short_sequences_and_more_splits_than_tokens(N):
     want = P.oracle_decode_from_cache(cache, otq.make_params(128, 4, "KQV", 1), q.float().numpy(), [N], B, H, H)
     assert P.rel_l2(out.cpu().numpy(), want) < 1e-3
     if N == 1:
+        # a single token: the output is that token's reconstructed value (the decode
+        # accumulates values on fp16 tensor-core operands, hence the attention bound)
         kh, vh = tq.tq_dequantize(ctx.handle, cache, 0, 1)
-        np.testing.assert_allclose(out.cpu().numpy()[0], vh.cpu().numpy()[0, :, 0], rtol=1e-5, atol=1e-6)
+        assert P.rel_l2(out.cpu().numpy()[0], vh.cpu().numpy()[0, :, 0]) < 1e-3
 
 
 def test_decode_argument_errors():
