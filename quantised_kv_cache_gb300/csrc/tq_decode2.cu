@@ -8,20 +8,25 @@
 //
 // * record tiles of 64 tokens stream into shared memory through 1-D TMA bulk
 //   copies, three stages deep, each completing on an mbarrier (bounded waits);
+//   the last warp done with a stage refills it, so warps never wait on one
+//   another inside the token loop;
 // * keys: per CTA a float32 table T[v][pos] = sum over the coordinates a code
 //   position covers of q_rot[i] c[code_i(v)] turns each token's score into one
 //   lookup per byte (or 6-bit slot) of its record -- fp32 throughout, so scores
-//   keep full precision whatever the key scale;
+//   keep full precision whatever the key scale. The table is built as an outer
+//   sum of two per-position half tables, one add per entry;
 // * values and QJL signs: the p-weighted sums over a warp's 16 tokens run on
-//   the tensor cores (mma.sync m16n8k16, fp32 accumulate): value codes are
-//   decoded to fp16 pairs through a per-lane replicated table and transposed
-//   with movmatrix; sign bits become {0, 2^-14} operands built from two
-//   tokens' sign words with a byte permute and one funnel shift. The token weights p nu are split into fp16
-//   hi + lo parts so the weights add no rounding of their own.
+//   the tensor cores (mma.sync m16n8k16, fp32 accumulate) into ONE accumulator:
+//   B column 0/1 carry the fp16 hi/lo parts of p nu (values), columns 2/3 the
+//   hi/lo parts of p rho (signs). Value codes are decoded to fp16 pairs through
+//   a per-lane replicated table and transposed with movmatrix; a sign bit
+//   becomes a power of two (its bit moved into the fp16 exponent field by one
+//   rotate, isolated by one AND), undone per accumulator row at the merge.
 //
 // CTA: 4 warps, one (batch, kv head, chunk). A warp owns 16 tokens of each
 // 64-token tile: it scores them (16 lanes per token, 2 tokens per step), takes
-// the online-softmax step, and issues the value / sign MMAs.
+// the online-softmax step (base-2 exponent; the log2(e) factor sits in the
+// key tables) and issues the value / sign MMAs.
 
 #include <cuda_fp16.h>
 
@@ -33,6 +38,8 @@ namespace {
 constexpr int kWarps2 = 4;
 constexpr int kTT = 64;     // tokens per tile
 constexpr int kStages = 3;  // TMA pipeline depth (two CTAs per SM fit in shared memory)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 template <int KB, int VB, bool KQJL, bool VQJL>
 struct Geo {
@@ -48,13 +55,24 @@ struct Geo {
   static constexpr int off_vs = off_vn + kTT * 4;
   static constexpr int off_vr = off_vs + (VQJL ? kTT * 16 : 0);
   static constexpr int stage = off_vr + (VQJL ? kTT * 4 : 0);
-  // key table: positions per record and values per position
-  static constexpr int kpos = (KB == 3) ? 64 : 16 * KB;   // 6-bit slots, or bytes
+  // key table: positions per record (bytes, or 6-bit pair slots) and values per position
+  static constexpr int kpos = (KB == 3) ? 64 : 16 * KB;
   static constexpr int kval = (KB == 3) ? 64 : 256;
-  static constexpr int ktab = kpos * kval;                 // floats
-  static constexpr int stab = KQJL ? 16 * 256 : 0;         // sign-byte table (floats)
-  static constexpr int vval = 1 << (2 * VB);               // values of one pair field
+  static constexpr int ktab = kpos * kval;                 // floats; row v holds kpos entries
+  static constexpr int stab = KQJL ? 16 * 256 : 0;         // sign-byte table [256][16] (floats)
+  static constexpr int vval = 1 << (2 * VB);               // values of one value pair field
   static constexpr int vlut = vval * 32;                   // half2 words, replicated per lane
+  // shared-memory offsets (bytes from the dynamic base): value table first
+  static constexpr int sm_ktab = vlut * 4;
+  static constexpr int sm_stab = sm_ktab + ktab * 4;
+  static constexpr int sm_stage = sm_stab + stab * 4;
+  static constexpr int sm_bar = sm_stage + kStages * stage;
+  static constexpr int sm_cnt = sm_bar + kStages * 8;
+  static constexpr int sm_q = sm_cnt + 16;                 // [2][128] floats
+  static constexpr int sm_m = sm_q + 2 * kD * 4;           // [warps] x 3 floats
+  static constexpr int sm_acc = sm_m + 3 * kWarps2 * 4;    // [warps][128] floats, values
+  static constexpr int sm_sacc = sm_acc + kWarps2 * kD * 4;  // [warps][128] floats, signs
+  static constexpr int total = sm_sacc + kWarps2 * kD * 4;
 };
 
 struct Decode2Args {
@@ -80,40 +98,76 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-__device__ __forceinline__ float half_lo_f(uint32_t h2) {
-  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
-}
-__device__ __forceinline__ float half_hi_f(uint32_t h2) {
-  return __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+__device__ __forceinline__ uint32_t rotr(uint32_t w, uint32_t r) { return __funnelshift_r(w, w, r); }
+
+// coordinate of code offset o in the pair-slot order (coordinate 8n + 2t + e at 32t + 2n + e)
+__device__ __forceinline__ int slot_coord(int o) {
+  const int ps = o >> 1, e = o & 1;
+  return 8 * (ps & 15) + 2 * (ps >> 4) + e;
 }
 
-// 2*VB-bit field n (n = 0..15) of a thread's contiguous 32*VB-bit span
-template <int VB>
-__device__ __forceinline__ uint32_t span_field(const uint32_t (&w)[VB], int n) {
-  constexpr int F = 2 * VB;
-  const int bit = F * n, wi = bit >> 5, off = bit & 31;
-  uint32_t v;
-  if (off + F <= 32 || wi + 1 >= VB) v = w[wi] >> off;
-  else v = __funnelshift_r(w[wi], w[wi + 1], off);
-  return v & ((1u << F) - 1u);
+// Lookup table T[v][pos] (row stride KPOS floats): the sum, over the CPP codes
+// that value v packs at position pos (code offsets pos*CPP + j, CB bits each),
+// of q[coord] * cb[code]. Built as lo[v & low bits] + hi[v >> LOB]: each
+// thread owns one position and a slice of the high values. SIGN: cb = {-1, +1}.
+template <int CB, int KPOS, int VBITS, bool SIGN>
+__device__ __forceinline__ void build_lookup(float *T, const float *q, const float *cb_g, float scale, int tid) {
+  constexpr int CPP = VBITS / CB;
+  constexpr int LOB = (VBITS >= 8) ? 4 : 3;  // low-part bits (a whole number of codes)
+  constexpr int HIB = VBITS - LOB;
+  constexpr int NLO = 1 << LOB, PARTS = 128 / KPOS, NH = (1 << HIB) / PARTS;
+  constexpr int M = (1 << CB) - 1;
+  const int pos = tid % KPOS, part = tid / KPOS;
+  float qv[CPP];
+#pragma unroll
+  for (int j = 0; j < CPP; ++j) qv[j] = q[slot_coord(pos * CPP + j)] * scale;
+  float cb[M + 1];
+#pragma unroll
+  for (int c = 0; c <= M; ++c) cb[c] = SIGN ? (c ? 1.f : -1.f) : __ldg(cb_g + c);
+  float lo[NLO];
+#pragma unroll
+  for (int x = 0; x < NLO; ++x) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < LOB / CB; ++j) acc = fmaf(qv[j], cb[(x >> (CB * j)) & M], acc);
+    lo[x] = acc;
+  }
+#pragma unroll 1
+  for (int yy = 0; yy < NH; ++yy) {
+    const int y = part * NH + yy;
+    float hi = 0.f;
+#pragma unroll
+    for (int j = 0; j < HIB / CB; ++j) {
+      const int c = (y >> (CB * j)) & M;
+      hi = fmaf(qv[LOB / CB + j], SIGN ? (c ? 1.f : -1.f) : __ldg(cb_g + c), hi);
+    }
+#pragma unroll
+    for (int x = 0; x < NLO; ++x) T[((y << LOB) | x) * KPOS + pos] = lo[x] + hi;
+  }
+}
+
+// landing bit (10..14) of sign bit k (0..15) of a half-word, and the rotation that takes it there
+__host__ __device__ constexpr int sign_land(int k) { return k <= 4 ? k + 10 : (k <= 9 ? k + 5 : (k <= 14 ? k : 10)); }
+__host__ __device__ constexpr int sign_rot(int k) { return k <= 4 ? 10 : (k <= 9 ? 5 : (k <= 14 ? 0 : 27)); }
+// 1 / (fp16 value whose only set bit is bit L, 10 <= L <= 14): 2^(15 - 2^(L-10))
+__device__ __forceinline__ float sign_unscale(int L) {
+  return L == 10 ? 16384.f : (L == 11 ? 8192.f : (L == 12 ? 2048.f : (L == 13 ? 128.f : 0.5f)));
 }
 
 template <int KB, int VB, bool KQJL, bool VQJL>
 __global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args a) {
   using Gm = Geo<KB, VB, KQJL, VQJL>;
   extern __shared__ __align__(1024) unsigned char smem[];
-  // the value table sits first so that (field << 7) | (lane << 2) needs no base add
-  uint32_t *s_vlut = reinterpret_cast<uint32_t *>(smem);                // [vval][32]
-  float *s_ktab = reinterpret_cast<float *>(s_vlut + Gm::vlut);         // [kval][kpos]
-  float *s_stab = s_ktab + Gm::ktab;                                    // [256][16]
-  unsigned char *s_stage = reinterpret_cast<unsigned char *>(s_stab + Gm::stab);
-  uint64_t *s_full = reinterpret_cast<uint64_t *>(s_stage + kStages * Gm::stage);
-  float *s_q = reinterpret_cast<float *>(s_full + kStages);       // [128] q_rot / sqrt(d), [128] S q
-  float *s_m = s_q + 2 * kD;                                       // [warps]
-  float *s_l = s_m + kWarps2;
-  float *s_wsum = s_l + kWarps2;
-  float *s_acc = s_wsum + kWarps2;                                 // [warps][128]
-  float *s_sacc = s_acc + kWarps2 * kD;                            // [warps][128]
+  unsigned char *s_vlut = smem;  // [vval][32] half2 words, at offset 0
+  float *s_ktab = reinterpret_cast<float *>(smem + Gm::sm_ktab);
+  float *s_stab = reinterpret_cast<float *>(smem + Gm::sm_stab);
+  unsigned char *s_stage = smem + Gm::sm_stage;
+  uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Gm::sm_bar);
+  unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + Gm::sm_cnt);
+  float *s_q = reinterpret_cast<float *>(smem + Gm::sm_q);  // [128] q_rot / sqrt(d), [128] scaled S q
+  float *s_m = reinterpret_cast<float *>(smem + Gm::sm_m);  // [warps] max, [warps] sum, [warps] sign weight sum
+  float *s_acc = reinterpret_cast<float *>(smem + Gm::sm_acc);
+  float *s_sacc = reinterpret_cast<float *>(smem + Gm::sm_sacc);
 
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -126,7 +180,10 @@ __global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args
 
   // ---------------- prologue: barriers, first TMA stages, tables
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&s_full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&s_full[s], 1);
+      s_cnt[s] = 0;
+    }
     mbar_fence_init();
   }
   __syncthreads();
@@ -164,65 +221,69 @@ __global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args
   if (KQJL) s_q[kD + tid] = __ldg(qp + kD + tid);
   __syncthreads();
 
-  // key table: position pos of a record covers codes of coordinates by the slot order
+  // key tables carry log2(e) so that scores come out in base-2 units
+  if constexpr (KB == 3) build_lookup<3, 64, 6, false>(s_ktab, s_q, a.k_centroids, kLog2e, tid);
+  else build_lookup<KB, 16 * KB, 8, false>(s_ktab, s_q, a.k_centroids, kLog2e, tid);
+  if constexpr (KQJL) build_lookup<1, 16, 8, true>(s_stab, s_q + kD, nullptr, kLog2e, tid);
   {
-    const float *kc = a.k_centroids;
-    for (int e = tid; e < Gm::ktab; e += blockDim.x) {
-      const int v = e / Gm::kpos, pos = e % Gm::kpos;
-      float acc = 0.f;
-      if (KB == 3) {
-        const int s = pos, t = s >> 4, n = s & 15, p = 4 * n + t;
-        acc = s_q[2 * p] * __ldg(kc + (v & 7)) + s_q[2 * p + 1] * __ldg(kc + (v >> 3));
-      } else {
-        constexpr int per = 8 / (2 * KB);  // slots per byte
-#pragma unroll
-        for (int u = 0; u < per; ++u) {
-          const int s = pos * per + u, t = s >> 4, n = s & 15, p = 4 * n + t;
-          const int f = (v >> (2 * KB * u)) & ((1 << (2 * KB)) - 1);
-          acc += s_q[2 * p] * __ldg(kc + (f & ((1 << KB) - 1))) + s_q[2 * p + 1] * __ldg(kc + (f >> KB));
-        }
-      }
-      s_ktab[e] = acc;
-    }
-    if (KQJL) {
-      // sign byte at position pos (0..15) covers slots 4pos..4pos+3 of the 1-bit layout
-      for (int e = tid; e < 16 * 256; e += blockDim.x) {
-        const int v = e >> 4, pos = e & 15;
-        float acc = 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int s = 4 * pos + u, t = s >> 4, n = s & 15, p = 4 * n + t;
-          acc += ((v >> (2 * u)) & 1 ? 1.f : -1.f) * s_q[kD + 2 * p] +
-                 ((v >> (2 * u + 1)) & 1 ? 1.f : -1.f) * s_q[kD + 2 * p + 1];
-        }
-        s_stab[e] = acc;
-      }
-    }
     // value pair table: field f -> half2(c[f & mask], c[f >> VB]), replicated for every lane
     const float *vcb = a.v_centroids;
+    uint32_t *vl = reinterpret_cast<uint32_t *>(s_vlut);
     for (int e = tid; e < Gm::vlut; e += blockDim.x) {
       const int f = e >> 5;
-      s_vlut[e] = pack_half2(__ldg(vcb + (f & ((1 << VB) - 1))), __ldg(vcb + (f >> VB)));
+      vl[e] = pack_half2(__ldg(vcb + (f & ((1 << VB) - 1))), __ldg(vcb + (f >> VB)));
     }
   }
   __syncthreads();
 
   // ---------------- per-lane constants
-  const uint32_t ktab_sa = smem_u32(s_ktab);
   const int half = lane >> 4, l = lane & 15;
   const int g = lane >> 2, t4 = lane & 3;
-  // reduce-scatter result: lane l (within its half) holds step sigma(l)
+  // key lookups: byte offset into T from (record word, constant, selector / rotation)
+  uint32_t kcon[4], ksel[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (KB == 4 || KB == 3) {
+      const int kk = (k + (lane >> 3)) & 3;  // staggered so that the 32 lanes hit 32 banks
+      kcon[k] = 4u * (4 * l + kk);
+      ksel[k] = (KB == 4) ? (0x5504u | ((uint32_t)kk << 4)) : (uint32_t)((6 * kk - 8) & 31);
+    } else if (KB == 2) {
+      const int jj = (k + half) & 1, bpos = 2 * l + jj;
+      kcon[k] = 4u * bpos;
+      ksel[k] = (uint32_t)((8 * (bpos & 3) - 7) & 31);
+    } else {
+      kcon[k] = 4u * l;
+      ksel[k] = (uint32_t)((8 * (l & 3) - 6) & 31);
+    }
+  }
+  const uint32_t ssel = (uint32_t)((8 * (l & 3) - 6) & 31);  // key sign byte l -> row offset (64-byte rows)
+  // reduce-scatter result: lane l (within its half) holds step sigma(l); token j = 2 sigma + half
   const int my_step = 4 * ((l >> 3) & 1) + 2 * ((l >> 2) & 1) + ((l >> 1) & 1);
-  float m_run = -INFINITY, l_run = 0.f, wsum = 0.f;
-  float dv[8][4], ds[8][4];
+  const int my_j = 2 * my_step + half;
+  // B gather: token j of the warp sits on lanes 16(j&1) + 8((j>>3)&1) + 4((j>>2)&1) + 2((j>>1)&1) (+1);
+  // the even lane carries p nu, the odd one p rho
+  int bsrc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int j = 2 * t4 + (c & 1) + 8 * (c >> 1);
+    bsrc[c] = 16 * (j & 1) + 8 * ((j >> 3) & 1) + 4 * ((j >> 2) & 1) + 2 * ((j >> 1) & 1) + ((g >> 1) & 1);
+  }
+  const uint32_t bsel = (g & 1) ? 0x7632u : 0x5410u;  // hi parts (even g) or lo parts (odd g)
+  const bool bv_live = g < 2, bs_live = (g >> 1) == 1;
+  const uint32_t lane4 = (uint32_t)lane << 2;
+  // sign operands: this thread's rows are half (g & 1) of sign word (g >> 1)
+  const uint32_t swsel = (g & 1) ? 0x7632u : 0x5410u;
+
+  float m_run = -INFINITY, l_run = 0.f, w_run = 0.f;
+  float acc[8][4];
 #pragma unroll
   for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dv[mb][j] = ds[mb][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc[mb][j] = 0.f;
 
   // A wait that runs out of time (it never should) records TQ_ERR_TIMEOUT; the
-  // CTA then stops waiting and computing but still reaches every barrier, so
-  // no thread is left behind. Its partial record is then meaningless, which the
+  // warp then stops waiting and computing but keeps releasing its stages, so
+  // no warp is left behind. The partial record is then meaningless, which the
   // error word reports.
   bool bad = false;
   for (int tile = 0; tile < ntiles; ++tile) {
@@ -230,218 +291,219 @@ __global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args
     const uint32_t parity = (tile / kStages) & 1;
     if (!bad && !mbar_wait_bounded(&s_full[stage], parity, a.error)) bad = true;
     bad = __any_sync(kFull, bad);  // whole warps skip together (the body shuffles)
-    if (bad) {
-      __syncthreads();
-      continue;
-    }
     const unsigned char *st = s_stage + stage * Gm::stage;
     const int t0 = t_begin + tile * kTT;
     const int wbase = warp * 16;  // this warp's first token within the tile
-    const float *kn = reinterpret_cast<const float *>(st + Gm::off_kn);
-    const float *vn = reinterpret_cast<const float *>(st + Gm::off_vn);
+    if (!bad) {
+      const float *kn = reinterpret_cast<const float *>(st + Gm::off_kn);
+      const float *kr = reinterpret_cast<const float *>(st + Gm::off_kr);
 
-    // ---- scores: 8 steps of 2 tokens, 16 lanes per token
-    float part[8];
+      // ---- scores: 8 steps of 2 tokens, 16 lanes per token
+      float part[8];
 #pragma unroll
-    for (int step = 0; step < 8; ++step) {
-      const int lt = wbase + 2 * step + half;
-      const float nu = kn[lt];
-      const unsigned char *rec = st + Gm::off_kc + lt * Gm::kc;
-      float acc = 0.f;
-      if (KB == 4) {
-        // lane l owns bytes 4l..4l+3; byte kk of word w indexes T[v][4l + kk]; the
-        // byte address (v << 8) | (4 pos) comes from one byte permute
-        const uint32_t w = reinterpret_cast<const uint32_t *>(rec)[l];
-        float t[4];
+      for (int step = 0; step < 8; ++step) {
+        const int lt = wbase + 2 * step + half;
+        const uint32_t *rec = reinterpret_cast<const uint32_t *>(st + Gm::off_kc + lt * Gm::kc);
+        const unsigned char *tb = reinterpret_cast<const unsigned char *>(s_ktab);
+        float sum;
+        if (KB == 4) {
+          const uint32_t w = rec[l];
+          float t[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) t[k] = *reinterpret_cast<const float *>(tb + __byte_perm(w, kcon[k], ksel[k]));
+          sum = (t[0] + t[1]) + (t[2] + t[3]);
+        } else if (KB == 3) {
+          // lane l owns pair slots 4l..4l+3 (24 bits at bit 24 l)
+          const int bit = 24 * l, wi = bit >> 5, off = bit & 31;
+          const uint32_t f24 = __funnelshift_r(rec[wi], rec[(wi + 1 < 12) ? wi + 1 : wi], off);
+          float t[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            t[k] = *reinterpret_cast<const float *>(tb + ((rotr(f24, ksel[k]) & 0x3F00u) | kcon[k]));
+          sum = (t[0] + t[1]) + (t[2] + t[3]);
+        } else if (KB == 2) {
+          const uint32_t w = rec[l >> 1];
+          float t[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            t[k] = *reinterpret_cast<const float *>(tb + ((rotr(w, ksel[k]) & 0x7F80u) | kcon[k]));
+          sum = t[0] + t[1];
+        } else {
+          const uint32_t w = rec[l >> 2];
+          sum = *reinterpret_cast<const float *>(tb + ((rotr(w, ksel[0]) & 0x3FC0u) | kcon[0]));
+        }
+        if (KQJL) {
+          const uint32_t *srec = reinterpret_cast<const uint32_t *>(st + Gm::off_ks + lt * 16);
+          const uint32_t w = srec[l >> 2];
+          const float ts = *reinterpret_cast<const float *>(reinterpret_cast<const unsigned char *>(s_stab) +
+                                                            ((rotr(w, ssel) & 0x3FC0u) | (4u * l)));
+          sum = fmaf(kr[lt], ts, kn[lt] * sum);
+        }
+        part[step] = sum;
+      }
+      // reduce-scatter 8 values over the 16 lanes of each half
+      float sc;
+      {
+        float r4[4], r2[2];
+        const bool hb = (l & 8) != 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int kk = (k + (lane >> 3)) & 3;
-          const uint32_t off = __byte_perm(w, (uint32_t)(4 * (4 * l + kk)), 0x4440u | (uint32_t)kk << 4);
-          t[k] = ld_shared_f32(ktab_sa + off);
+          const float send = hb ? part[k] : part[k + 4];
+          const float keep = hb ? part[k + 4] : part[k];
+          r4[k] = keep + __shfl_xor_sync(kFull, send, 8);
         }
-        acc = (t[0] + t[1]) + (t[2] + t[3]);
-      } else if (KB == 2) {
-        const uint32_t w = reinterpret_cast<const uint32_t *>(rec)[l >> 1] >> (16 * (l & 1));
-        float t[2];
+        const bool hb2 = (l & 4) != 0;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int kk = (k + half) & 1;
-          const int pos = 2 * l + kk;
-          const uint32_t v = (w >> (8 * kk)) & 0xffu;
-          t[k] = s_ktab[v * Gm::kpos + pos];
+          const float send = hb2 ? r4[k] : r4[k + 2];
+          const float keep = hb2 ? r4[k + 2] : r4[k];
+          r2[k] = keep + __shfl_xor_sync(kFull, send, 4);
         }
-        acc = t[0] + t[1];
-      } else if (KB == 1) {
-        const uint32_t v = rec[l];
-        acc = s_ktab[v * Gm::kpos + l];
-      } else {  // KB == 3: lane l owns slots 4l..4l+3 (24 bits at bit 24 l)
-        const uint32_t *rw = reinterpret_cast<const uint32_t *>(rec);
-        const int bit = 24 * l, wi = bit >> 5, off = bit & 31;
-        const uint32_t lo = rw[wi], hi = rw[(wi + 1 < 12) ? wi + 1 : wi];
-        const uint32_t f24 = __funnelshift_r(lo, hi, off);
-        float t[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int kk = (k + (lane >> 3)) & 3;
-          const uint32_t v = (f24 >> (6 * kk)) & 63u;
-          t[k] = s_ktab[v * Gm::kpos + 4 * l + kk];
-        }
-        acc = (t[0] + t[1]) + (t[2] + t[3]);
+        const bool hb1 = (l & 2) != 0;
+        sc = (hb1 ? r2[1] : r2[0]) + __shfl_xor_sync(kFull, hb1 ? r2[0] : r2[1], 2);
+        sc += __shfl_xor_sync(kFull, sc, 1);
       }
-      acc *= nu;
-      if (KQJL) {
-        const float rho = reinterpret_cast<const float *>(st + Gm::off_kr)[lt];
-        const uint32_t v = (st + Gm::off_ks + lt * 16)[l];
-        acc = fmaf(rho, s_stab[v * 16 + l], acc);
-      }
-      part[step] = acc;
-    }
-    // reduce-scatter 8 values over the 16 lanes of each half
-    float r4[4], r2[2];
-    {
-      const bool hb = (l & 8) != 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float send = hb ? part[k] : part[k + 4];
-        const float keep = hb ? part[k + 4] : part[k];
-        r4[k] = keep + __shfl_xor_sync(kFull, send, 8);
-      }
-      const bool hb2 = (l & 4) != 0;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float send = hb2 ? r4[k] : r4[k + 2];
-        const float keep = hb2 ? r4[k + 2] : r4[k];
-        r2[k] = keep + __shfl_xor_sync(kFull, send, 4);
-      }
-    }
-    const bool hb1 = (l & 2) != 0;
-    float sc = (hb1 ? r2[1] : r2[0]) + __shfl_xor_sync(kFull, hb1 ? r2[0] : r2[1], 2);
-    sc += __shfl_xor_sync(kFull, sc, 1);
-    const int my_tok = wbase + 2 * my_step + half;
-    const bool valid = t0 + my_tok < t_end;
-    sc = valid ? sc : -INFINITY;
+      const int tok = wbase + my_j;
+      const bool valid = t0 + tok < t_end;
+      if (!KQJL) sc *= kn[tok];
+      sc = valid ? sc : -INFINITY;
 
-    // ---- online softmax over the warp's 16 tokens
-    float tmax = sc;
+      // ---- online softmax over the warp's 16 tokens (base 2)
+      float tmax = sc;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
-    const float m_new = fmaxf(m_run, tmax);
-    const bool any = m_new != -INFINITY;  // at least one valid token seen by this warp
-    const float scale = any ? __expf(m_run - m_new) : 1.f;
-    const float p = valid ? __expf(sc - m_new) : 0.f;
-    float psum = p;
+      for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+      const float m_new = fmaxf(m_run, tmax);
+      const float p = valid ? ex2_approx(sc - m_new) : 0.f;
+      if (m_new != m_run) {  // warp-uniform: the running max moved (m_run = -inf scales zeros)
+        const float scale = ex2_approx(m_run - m_new);
+        l_run *= scale;
+        w_run *= scale;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) psum += __shfl_xor_sync(kFull, psum, o);
-    l_run = l_run * scale + 0.5f * psum;  // every token sits on two lanes
-    m_run = m_new;
-    if (scale != 1.f) {  // warp-uniform: the running max moved
-      wsum *= scale;
+        for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          dv[mb][j] *= scale;
-          if (VQJL) ds[mb][j] *= scale;
-        }
-    }
-
-    // ---- B operands: column 0 = this warp's 16 token weights, other columns 0
-    // token j (0..15) of the warp sits on lane 16(j&1) + 8((j>>3)&1) + 4((j>>2)&1) + 2((j>>1)&1)
-    uint32_t bh0, bh1, bl0, bl1, bs0 = 0, bs1 = 0;
-    {
-      float w[4], wr[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int j = 2 * t4 + (c & 1) + 8 * (c >> 1);
-        const int src = 16 * (j & 1) + 8 * ((j >> 3) & 1) + 4 * ((j >> 2) & 1) + 2 * ((j >> 1) & 1);
-        const float pj = __shfl_sync(kFull, p, src);
-        const bool live = (g == 0) && (t0 + wbase + j < t_end);
-        w[c] = live ? pj * vn[wbase + j] : 0.f;
-        wr[c] = (live && VQJL) ? pj * reinterpret_cast<const float *>(st + Gm::off_vr)[wbase + j] : 0.f;
+          for (int j = 0; j < 4; ++j) acc[mb][j] *= scale;
+        m_run = m_new;
       }
-      bh0 = pack_half2(w[0], w[1]);
-      bh1 = pack_half2(w[2], w[3]);
-      bl0 = pack_half2(w[0] - half_lo_f(bh0), w[1] - half_hi_f(bh0));
-      bl1 = pack_half2(w[2] - half_lo_f(bh1), w[3] - half_hi_f(bh1));
+      l_run += p;  // every token sits on two lanes: halved at the merge
+
+      // ---- B operands: this lane's token weight (p nu on even lanes, p rho on odd ones)
+      // as an fp16 hi/lo pair, gathered into column g of the MMA's B fragment
+      uint32_t bv0, bv1, bs0 = 0, bs1 = 0;
+      {
+        const bool odd = VQJL && (lane & 1);
+        const float *wsrc = reinterpret_cast<const float *>(st + (odd ? Gm::off_vr : Gm::off_vn));
+        const float wv = valid ? p * wsrc[tok] : 0.f;
+        w_run += wv;  // sum of p rho over the odd lanes (the even ones are ignored)
+        const __half hh = __float2half_rn(wv);
+        const float rem = wv - __half2float(hh);
+        const uint32_t hl = (uint32_t)__half_as_ushort(hh) | ((uint32_t)__half_as_ushort(__float2half_rn(rem)) << 16);
+        const uint32_t x0 = __shfl_sync(kFull, hl, bsrc[0]);
+        const uint32_t x1 = __shfl_sync(kFull, hl, bsrc[1]);
+        const uint32_t x2 = __shfl_sync(kFull, hl, bsrc[2]);
+        const uint32_t x3 = __shfl_sync(kFull, hl, bsrc[3]);
+        const uint32_t b0 = __byte_perm(x0, x1, bsel), b1 = __byte_perm(x2, x3, bsel);
+        bv0 = bv_live ? b0 : 0u;
+        bv1 = bv_live ? b1 : 0u;
+        if (VQJL) {
+          bs0 = bs_live ? b0 : 0u;
+          bs1 = bs_live ? b1 : 0u;
+        }
+      }
+
+      // ---- values: decode (token, coordinate-pair) fp16 pairs, transpose, MMA
+      {
+        uint32_t w0[VB], w1[VB];
+        const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + g) * Gm::vc);
+        const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + 8 + g) * Gm::vc);
+#pragma unroll
+        for (int k = 0; k < VB; ++k) {
+          w0[k] = r0[VB * t4 + k];
+          w1[k] = r1[VB * t4 + k];
+        }
+        // field n of a span -> byte offset (field << 7) | (lane << 2) of the value table
+        auto lut = [&](const uint32_t(&w)[VB], int n) -> uint32_t {
+          constexpr int F = 2 * VB;
+          constexpr uint32_t mask = ((1u << F) - 1u) << 7;
+          const int bit = F * n, wi = bit >> 5, off = bit & 31;
+          uint32_t x;
+          if (off < 7) x = w[wi] << (7 - off);
+          else x = __funnelshift_r(w[wi], w[(wi + 1 < VB) ? wi + 1 : wi], off - 7);
+          return *reinterpret_cast<const uint32_t *>(s_vlut + ((x & mask) | lane4));
+        };
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          const uint32_t x00 = movmatrix_t(lut(w0, 2 * mb));
+          const uint32_t x01 = movmatrix_t(lut(w0, 2 * mb + 1));
+          const uint32_t x10 = movmatrix_t(lut(w1, 2 * mb));
+          const uint32_t x11 = movmatrix_t(lut(w1, 2 * mb + 1));
+          mma_16816(acc[mb], x00, x01, x10, x11, bv0, bv1);
+        }
+      }
+
+      // ---- QJL signs: rows of this thread = bits of half (g & 1) of sign word (g >> 1)
       if (VQJL) {
-        bs0 = pack_half2(wr[0], wr[1]);
-        bs1 = pack_half2(wr[2], wr[3]);
-        // the sign MMA runs on bits b (as 2^-14 b); sum_j w'_j sigma_j = 2 sum_j w'_j b_j - sum_j w'_j
-        float ws = half_lo_f(bs0) + half_hi_f(bs0) + half_lo_f(bs1) + half_hi_f(bs1);
+        const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + Gm::off_vs);
+        const int wsel = g >> 1;
+        const uint32_t wa0 = sw[(wbase + 2 * t4) * 4 + wsel], wb0 = sw[(wbase + 2 * t4 + 1) * 4 + wsel];
+        const uint32_t wa1 = sw[(wbase + 2 * t4 + 8) * 4 + wsel], wb1 = sw[(wbase + 2 * t4 + 9) * 4 + wsel];
+        // token 2t (8 + 2t) in bits 0..15, token 2t + 1 (9 + 2t) in bits 16..31
+        const uint32_t s0 = __byte_perm(wa0, wb0, swsel), s1 = __byte_perm(wa1, wb1, swsel);
+        const uint32_t s0r10 = rotr(s0, 22), s0r5 = rotr(s0, 27), s0r27 = rotr(s0, 5);
+        const uint32_t s1r10 = rotr(s1, 22), s1r5 = rotr(s1, 27), s1r27 = rotr(s1, 5);
+        auto pick = [&](int k, uint32_t r0, uint32_t r5, uint32_t r10, uint32_t r27) -> uint32_t {
+          const uint32_t src = sign_rot(k) == 10 ? r10 : (sign_rot(k) == 5 ? r5 : (sign_rot(k) == 0 ? r0 : r27));
+          return src & (0x00010001u << sign_land(k));
+        };
 #pragma unroll
-        for (int o = 1; o < 4; o <<= 1) ws += __shfl_xor_sync(kFull, ws, o);  // over t4 (g = 0 lanes)
-        wsum += ws;
+        for (int mb = 0; mb < 8; ++mb) {
+          const uint32_t a0 = pick(2 * mb, s0, s0r5, s0r10, s0r27);
+          const uint32_t a1 = pick(2 * mb + 1, s0, s0r5, s0r10, s0r27);
+          const uint32_t a2 = pick(2 * mb, s1, s1r5, s1r10, s1r27);
+          const uint32_t a3 = pick(2 * mb + 1, s1, s1r5, s1r10, s1r27);
+          mma_16816(acc[mb], a0, a1, a2, a3, bs0, bs1);
+        }
       }
     }
 
-    // ---- values: decode (token, coordinate-pair) fp16 pairs, transpose, MMA
-    {
-      uint32_t w0[VB], w1[VB];
-      const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + g) * Gm::vc);
-      const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + 8 + g) * Gm::vc);
-#pragma unroll
-      for (int k = 0; k < VB; ++k) {
-        w0[k] = r0[VB * t4 + k];
-        w1[k] = r1[VB * t4 + k];
+    // release the stage: the last of the four warps refills it
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      const unsigned old = atomicAdd(&s_cnt[stage], 1u);
+      if ((old & (kWarps2 - 1)) == kWarps2 - 1 && tile + kStages < ntiles) {
+        __threadfence_block();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_tile(tile + kStages);
       }
-      const uint32_t lane_sa = smem_u32(s_vlut) | (uint32_t)(lane << 2);
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb) {
-        const uint32_t x00 = movmatrix_t(ld_shared_u32(lane_sa | (span_field<VB>(w0, 2 * mb) << 7)));
-        const uint32_t x01 = movmatrix_t(ld_shared_u32(lane_sa | (span_field<VB>(w0, 2 * mb + 1) << 7)));
-        const uint32_t x10 = movmatrix_t(ld_shared_u32(lane_sa | (span_field<VB>(w1, 2 * mb) << 7)));
-        const uint32_t x11 = movmatrix_t(ld_shared_u32(lane_sa | (span_field<VB>(w1, 2 * mb + 1) << 7)));
-        mma_16816(dv[mb], x00, x01, x10, x11, bh0, bh1);
-        mma_16816(dv[mb], x00, x01, x10, x11, bl0, bl1);
-      }
-    }
-
-    // ---- QJL signs: A(coords x tokens) as 0/1 fp16 pairs built from two tokens' sign words
-    if (VQJL) {
-      // coordinate 16mb + g (+8) of token j: sign word (g>>1)&3, bit 4mb + (g&1) (+2)
-      const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + Gm::off_vs);
-      const int wsel = (g >> 1) & 3, e = g & 1;
-      const uint32_t wa0 = sw[(wbase + 2 * t4) * 4 + wsel], wb0 = sw[(wbase + 2 * t4 + 1) * 4 + wsel];
-      const uint32_t wa1 = sw[(wbase + 2 * t4 + 8) * 4 + wsel], wb1 = sw[(wbase + 2 * t4 + 9) * 4 + wsel];
-      // low halves of the two tokens' words side by side (token 2t in bits 0..15, 2t+1 in 16..31)
-      const uint32_t lo0 = __byte_perm(wa0, wb0, 0x5410), hi0 = __byte_perm(wa0, wb0, 0x7632);
-      const uint32_t lo1 = __byte_perm(wa1, wb1, 0x5410), hi1 = __byte_perm(wa1, wb1, 0x7632);
-      // a set bit becomes the fp16 value 2^-14 (bit 10, the smallest normal): one
-      // shift lands bits k and 16 + k on bits 10 and 26; the merge rescales by 2^14
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb) {
-        const int sh0 = (4 * mb + e) & 15, sh1 = (4 * mb + 2 + e) & 15;
-        const uint32_t s0 = (mb < 4) ? lo0 : hi0, s1 = (mb < 4) ? lo1 : hi1;
-        const uint32_t a0 = __funnelshift_l(s0, s0, 10 - sh0 + 32) & 0x04000400u;
-        const uint32_t a2 = __funnelshift_l(s0, s0, 10 - sh1 + 32) & 0x04000400u;
-        const uint32_t a4 = __funnelshift_l(s1, s1, 10 - sh0 + 32) & 0x04000400u;
-        const uint32_t a6 = __funnelshift_l(s1, s1, 10 - sh1 + 32) & 0x04000400u;
-        mma_16816(ds[mb], a0, a2, a4, a6, bs0, bs1);
-      }
-    }
-
-    __syncthreads();  // every warp is done with this stage
-    if (tid == 0 && !bad && tile + kStages < ntiles) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue_tile(tile + kStages);
     }
   }
 
   // ---------------- merge the warps and write this chunk's partial record
-  if (lane == 0) {
-    s_m[warp] = m_run;
-    s_l[warp] = l_run;
-    s_wsum[warp] = wsum;
+  {
+    float lw = l_run, ww = (lane & 1) ? w_run : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lw += __shfl_xor_sync(kFull, lw, o);
+      ww += __shfl_xor_sync(kFull, ww, o);
+    }
+    if (lane == 0) {
+      s_m[warp] = m_run;
+      s_m[kWarps2 + warp] = 0.5f * lw;
+      s_m[2 * kWarps2 + warp] = ww;
+    }
   }
-  if (t4 == 0) {  // column 0 of the accumulators: coordinates 16mb + g and 16mb + 8 + g
+  if (t4 == 0) {  // columns 0/1: value sums of coordinates 16mb + g and 16mb + 8 + g
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
-      s_acc[warp * kD + 16 * mb + g] = dv[mb][0];
-      s_acc[warp * kD + 16 * mb + 8 + g] = dv[mb][2];
-      if (VQJL) {
-        s_sacc[warp * kD + 16 * mb + g] = ds[mb][0];
-        s_sacc[warp * kD + 16 * mb + 8 + g] = ds[mb][2];
-      }
+      s_acc[warp * kD + 16 * mb + g] = acc[mb][0] + acc[mb][1];
+      s_acc[warp * kD + 16 * mb + 8 + g] = acc[mb][2] + acc[mb][3];
+    }
+  } else if (VQJL && t4 == 1) {  // columns 2/3: sign sums; row (mb, r) is bit 2mb + r of half g&1 of word g>>1
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const int c0 = 64 * (g & 1) + 8 * mb + 2 * (g >> 1);
+      s_sacc[warp * kD + c0] = (acc[mb][0] + acc[mb][1]) * sign_unscale(sign_land(2 * mb));
+      s_sacc[warp * kD + c0 + 1] = (acc[mb][2] + acc[mb][3]) * sign_unscale(sign_land(2 * mb + 1));
     }
   }
   __syncthreads();
@@ -452,14 +514,15 @@ __global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args
   float L = 0.f, A = 0.f, Sg = 0.f;
 #pragma unroll
   for (int w = 0; w < kWarps2; ++w) {
-    const float e = (s_m[w] == -INFINITY) ? 0.f : __expf(s_m[w] - M);
-    L += s_l[w] * e;
+    const float e = (s_m[w] == -INFINITY) ? 0.f : ex2_approx(s_m[w] - M);
+    L += s_m[kWarps2 + w] * e;
     A += s_acc[w * kD + i] * e;
-    if (VQJL) Sg += (2.f * 16384.f * s_sacc[w * kD + i] - s_wsum[w]) * e;
+    // the sign MMA summed p rho b over bits b; sum p rho sigma = 2 sum p rho b - sum p rho
+    if (VQJL) Sg += (2.f * s_sacc[w * kD + i] - s_m[2 * kWarps2 + w]) * e;
   }
   float *rec = a.partials + (((size_t)b * a.heads_q + hq) * a.splits + split) * kPartialFloats;
   if (i == 0) {
-    rec[0] = M;
+    rec[0] = M * kLn2;  // natural-log units for the combine step
     rec[1] = L;
   }
   rec[2 + i] = A;
@@ -468,9 +531,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args
 
 template <int KB, int VB, bool KQJL, bool VQJL>
 size_t smem_bytes() {
-  using Gm = Geo<KB, VB, KQJL, VQJL>;
-  return sizeof(float) * (Gm::ktab + Gm::stab) + sizeof(uint32_t) * Gm::vlut + kStages * Gm::stage +
-         kStages * sizeof(uint64_t) + sizeof(float) * (2 * kD + 3 * kWarps2 + 2 * kWarps2 * kD);
+  return (size_t)Geo<KB, VB, KQJL, VQJL>::total;
 }
 
 template <int KB, int VB, bool KQJL, bool VQJL>
