@@ -5,7 +5,7 @@ One step = the whole hot path once on the Llama-2-7B-shaped decode workload
 (batch 16, 32 heads, head_dim 128, context 8192, bf16, KQV at a 4-bit
 budget): append-quantise one new K/V token per sequence into slot 8191, then
 decode attention of one query per head over the 8192 compressed tokens
-(query prep, split-K decode, combine). `value` is the step's algorithmic bytes
+(query prep, decode, combine). `value` is the step's algorithmic bytes
 (packed records + norms + signs read, new records written, q, output) per
 second of device time; `append_quantize` reports the bulk append-quantise
 throughput of refilling the whole cache. Inputs are synthetic, drawn on the
@@ -369,7 +369,7 @@ def main():
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": workload_config(),
             "pct_of_hbm_peak": 100.0 * (value / world) / hbm_peak,
-            "roofline": {"bound": "hbm", "kernel": "decode_tq_kernel (split-K decode attention)",
+            "roofline": {"bound": "hbm", "kernel": "decode_persist_kernel (persistent decode attention)",
                          "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": None, "ms_per_launch": dec_ms,
                          "bytes_per_launch": decode_kernel_bytes},

@@ -206,8 +206,10 @@ tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const voi
                              const void *d_v, int dtype, int batch, int heads_kv, int n_new,
                              const int32_t *d_seq_lens, void *stream);
 
-/* Workspace bytes tq_decode_attention needs for these sizes (split-K
- * partials and the prepared queries). splits = 0 asks for the library's
+/* Workspace bytes tq_decode_attention needs for these sizes: the prepared
+ * queries, a per-batch tile prefix, and the partial softmax records (per
+ * split for the split-K kernels, or two per (CTA + head) slot for the
+ * persistent kernel, whichever is larger). splits = 0 asks for the library's
  * choice for max_len. */
 tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len,
                             int splits, size_t *out);
@@ -217,8 +219,13 @@ tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads
  * linearly):  out[b][h] = softmax(q[b][h] . K_hat^T / sqrt(d)) V_hat over the
  * first d_seq_lens[b] tokens of KV head h / (heads_q / heads_kv).
  *   d_q   : [batch][heads_q][d], dtype TQ_F32 or TQ_BF16
- *   d_seq_lens : int32 [batch], each in [1, max_len], max_len <= capacity
- *   splits: token chunks per (batch, kv head); 0 = library's choice
+ *   d_seq_lens : int32 [batch], each in [0, max_len], max_len <= capacity;
+ *                a sequence of length 0 yields zeros
+ *   splits: token chunks per (batch, kv head) for the split-K kernels; 0 =
+ *           library's choice. With one query head per KV head, batch <= 256
+ *           and a capacity that is a multiple of 4, a persistent kernel
+ *           divides the (batch, head, 64-token tile) space evenly over the
+ *           SMs instead and splits does not change the work division.
  *   d_workspace : >= tq_workspace_size(...) bytes, 16-byte aligned, no
  *                 initial contents required
  *   d_out : float32 [batch][heads_q][d]

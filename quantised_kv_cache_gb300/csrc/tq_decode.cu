@@ -34,11 +34,45 @@ struct PrepArgs {
   const float *diag;
   const float *sketch;
   float *qprep;  // [batch*heads_q][2][128]
+  // optional: tiles of kDecodeTile tokens before each batch, [batch + 1]
+  const int32_t *seq_lens;
+  int capacity;
+  int32_t *tile_prefix;
 };
+
+// Exclusive prefix over batches of ceil(clamped length / kDecodeTile), by one
+// block of 128 threads (any batch count: chunks of 128 with a running carry).
+__device__ void tile_prefix_block(const PrepArgs &a) {
+  __shared__ int s_scan[128];
+  __shared__ int s_carry;
+  const int t = threadIdx.x;
+  if (t == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.batch; base += 128) {
+    const int b = base + t;
+    const int len = (b < a.batch) ? min(max(__ldg(a.seq_lens + b), 0), a.capacity) : 0;
+    const int n = (len + kDecodeTile - 1) / kDecodeTile;
+    s_scan[t] = n;
+    __syncthreads();
+    for (int o = 1; o < 128; o <<= 1) {  // inclusive Hillis-Steele scan
+      const int v = (t >= o) ? s_scan[t - o] : 0;
+      __syncthreads();
+      s_scan[t] += v;
+      __syncthreads();
+    }
+    const int carry = s_carry;
+    if (b < a.batch) a.tile_prefix[b] = carry + s_scan[t] - n;
+    __syncthreads();
+    if (t == 127) s_carry = carry + s_scan[127];
+    __syncthreads();
+  }
+  if (t == 0) a.tile_prefix[a.batch] = s_carry;
+}
 
 // one warp per (batch, query head)
 __global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
   __shared__ float s_q[4][kD];
+  if (a.tile_prefix && blockIdx.x == 0) tile_prefix_block(a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
   const bool live = row < a.batch * a.heads_q;
@@ -299,6 +333,10 @@ struct CombineArgs {
   const float *diag;
   const float *sketch;
   float *out;
+  // persistent layout (tile_prefix != nullptr): records [(cta + unit) * 2 + group],
+  // one query head per KV head
+  const int32_t *tile_prefix;
+  int persist_ctas, heads_kv;
 };
 
 // one CTA (128 threads, thread = coordinate) per (batch, query head)
@@ -306,12 +344,39 @@ __global__ void __launch_bounds__(128) combine_tq_kernel(CombineArgs a) {
   __shared__ float s_sig[kD];
   __shared__ float s_o[kD];
   const int row = blockIdx.x, i = threadIdx.x;
+  // the partial records of this row: split-K ones in a row, or the persistent
+  // kernel's (cta, group) records of every CTA whose slice touched this head
   const float *base = a.partials + (size_t)row * a.splits * kPartialFloats;
+  long long T = 0, C = 1, c_lo = 0, c_hi = -1;
+  int unit = 0;
+  if (a.tile_prefix) {
+    const int b = row / a.heads_q, h = row % a.heads_q;
+    const int p0 = __ldg(a.tile_prefix + b), nb = __ldg(a.tile_prefix + b + 1) - p0;
+    T = (long long)a.heads_kv * __ldg(a.tile_prefix + a.batch);
+    C = a.persist_ctas;
+    unit = b * a.heads_kv + h;
+    if (nb > 0) {
+      const long long us = (long long)a.heads_kv * p0 + (long long)h * nb, ue = us + nb;
+      c_lo = ((us + 1) * C - 1) / T;  // the CTA whose slice [T c / C, T (c+1) / C) holds tile us
+      c_hi = (ue * C - 1) / T;
+    }
+  }
+  const int nrec = a.tile_prefix ? (int)(2 * (c_hi - c_lo + 1)) : a.splits;
+  auto record = [&](int k) -> const float * {
+    if (!a.tile_prefix) return base + (size_t)k * kPartialFloats;
+    const long long c = c_lo + k / 2;
+    if (T * c / C == T * (c + 1) / C) return nullptr;  // an empty slice wrote nothing
+    return a.partials + ((size_t)(c + unit) * 2 + (k & 1)) * kPartialFloats;
+  };
   float M = -INFINITY;
-  for (int s = 0; s < a.splits; ++s) M = fmaxf(M, __ldg(base + (size_t)s * kPartialFloats));
+  for (int k = 0; k < nrec; ++k) {
+    const float *rec = record(k);
+    if (rec) M = fmaxf(M, __ldg(rec));
+  }
   float L = 0.f, A = 0.f, Sg = 0.f;
-  for (int s = 0; s < a.splits; ++s) {
-    const float *rec = base + (size_t)s * kPartialFloats;
+  for (int k = 0; k < nrec; ++k) {
+    const float *rec = record(k);
+    if (!rec) continue;
     const float ms = __ldg(rec);
     const float e = (ms == -INFINITY) ? 0.f : __expf(ms - M);
     L += __ldg(rec + 1) * e;
@@ -553,18 +618,24 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   const int G = a.heads_q / a.heads_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return TQ_ERR_UNSUPPORTED;
 
+  const bool g1 = a.heads_q == a.heads_kv;
   PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, ctx->k.rotate, ctx->k.qjl,
-             ctx->dparams->diag, ctx->dparams->sketch, a.qprep};
+             ctx->dparams->diag, ctx->dparams->sketch, a.qprep,
+             a.seq_lens, a.cache->capacity, g1 ? a.tile_prefix : nullptr};
   const int rows = a.batch * a.heads_q;
   qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
 
-  // the TMA / tensor-core kernel covers one query head per KV head
+  // the TMA / tensor-core kernels cover one query head per KV head
   if (ctx->prof_decode_start) cudaEventRecord((cudaEvent_t)ctx->prof_decode_start, st);
-  int r2 = launch_decode2_g1(a, a.qprep, a.partials, stream);
+  int persist_ctas = 0;
+  DecodeArgs a2 = a;
+  if (!g1) a2.tile_prefix = nullptr;
+  int r2 = launch_decode2_g1(a2, &persist_ctas, stream);
   if (r2 == TQ_OK) {
     if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
     CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
-                    ctx->dparams->diag, ctx->dparams->sketch, a.out};
+                    ctx->dparams->diag, ctx->dparams->sketch, a.out,
+                    persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv};
     combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
   }
@@ -611,7 +682,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   if (r != TQ_OK) return r;
 
   CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
-                  ctx->dparams->diag, ctx->dparams->sketch, a.out};
+                  ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv};
   combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
@@ -622,7 +693,8 @@ int launch_decode_kivi(const DecodeArgs &a, void *stream) {
   const int G = a.heads_q / a.heads_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return TQ_ERR_UNSUPPORTED;
   if (ctx->kivi_group != 32) return TQ_ERR_UNSUPPORTED;
-  PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, 0, 0, ctx->dparams->diag, ctx->dparams->sketch, a.qprep};
+  PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, 0, 0, ctx->dparams->diag, ctx->dparams->sketch, a.qprep,
+             a.seq_lens, a.cache->capacity, nullptr};
   const int rows = a.batch * a.heads_q;
   qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
   const tq_cache *c = a.cache;
@@ -649,7 +721,8 @@ int launch_decode_kivi(const DecodeArgs &a, void *stream) {
   else r = launch_kivi_g<false, false>(k, G, grid, st);
   if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
   if (r != TQ_OK) return r;
-  CombineArgs cmb{a.batch, a.heads_q, a.splits, 0, 0, a.partials, ctx->dparams->diag, ctx->dparams->sketch, a.out};
+  CombineArgs cmb{a.batch, a.heads_q, a.splits, 0, 0, a.partials, ctx->dparams->diag, ctx->dparams->sketch, a.out,
+                  nullptr, 0, a.heads_kv};
   combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

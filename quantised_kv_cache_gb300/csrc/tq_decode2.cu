@@ -1,16 +1,25 @@
-// Split-K decode attention over the packed cache, one query head per KV head.
+// Decode attention over the packed cache, one query head per KV head, as two
+// kernels that share one tile body:
 //
-// Same computation as decode_tq_kernel (softmax(q K_hat^T / sqrt(d)) V_hat
-// with keys read through logits and values through the p-weighted sum in the
-// rotated domain; "HeadQ", 2.1-2.2; "Statistical Inference ... Inspired by
-// TurboQuant", technical summary, "K-V asymmetry", "Main contribution 1"),
-// organised for sm_103a:
+// * decode_persist_kernel -- persistent: two CTAs of 8 warps per SM walk
+//   contiguous slices of the flattened (batch, kv head, 64-token tile) space,
+//   so every SM gets the same number of tiles whatever the sequence lengths;
+//   key tables are rebuilt only where a slice crosses into the next head, and
+//   the TMA ring keeps streaming across that boundary. Each 4-warp group
+//   writes one partial softmax record per (CTA, head) segment.
+// * decode2_g1_kernel -- split-K over a fixed (batch, head, chunk) grid, for
+//   batches too large for the persistent kernel's shared-memory prefix table.
+//
+// Both compute softmax(q K_hat^T / sqrt(d)) V_hat with keys read through
+// logits and values through the p-weighted sum in the rotated domain
+// ("HeadQ", 2.1-2.2; "Statistical Inference ... Inspired by TurboQuant",
+// technical summary, "K-V asymmetry", "Main contribution 1"):
 //
 // * record tiles of 64 tokens stream into shared memory through 1-D TMA bulk
-//   copies, three stages deep, each completing on an mbarrier (bounded waits);
-//   the last warp done with a stage refills it, so warps never wait on one
-//   another inside the token loop;
-// * keys: per CTA a float32 table T[v][pos] = sum over the coordinates a code
+//   copies, each completing on an mbarrier (bounded waits); the last warp
+//   done with a stage refills it, so warps never wait on one another inside
+//   the token loop;
+// * keys: a float32 table T[v][pos] = sum over the coordinates a code
 //   position covers of q_rot[i] c[code_i(v)] turns each token's score into one
 //   lookup per byte (or 6-bit slot) of its record -- fp32 throughout, so scores
 //   keep full precision whatever the key scale. The table is built as an outer
@@ -23,26 +32,27 @@
 //   becomes a power of two (its bit moved into the fp16 exponent field by one
 //   rotate, isolated by one AND), undone per accumulator row at the merge.
 //
-// CTA: 4 warps, one (batch, kv head, chunk). A warp owns 16 tokens of each
-// 64-token tile: it scores them (16 lanes per token, 2 tokens per step), takes
-// the online-softmax step (base-2 exponent; the log2(e) factor sits in the
-// key tables) and issues the value / sign MMAs.
+// A warp owns 16 tokens of each tile it takes: it scores them (16 lanes per
+// token, 2 tokens per step), takes the online-softmax step (base-2 exponent;
+// the log2(e) factor sits in the key tables) and issues the value / sign MMAs.
 
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "tq_ptx.cuh"
 
 namespace tq {
 namespace {
 
-constexpr int kWarps2 = 4;
-constexpr int kTT = 64;     // tokens per tile
-constexpr int kStages = 3;  // TMA pipeline depth (two CTAs per SM fit in shared memory)
+constexpr int kTT = kDecodeTile;  // tokens per tile (4 warps x 16)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxPersistBatch = 256;  // prefix table held in shared memory
 
-template <int KB, int VB, bool KQJL, bool VQJL>
+template <int KB, int VB, bool KQJL, bool VQJL, int NW, int S>
 struct Geo {
+  static constexpr int kStages = S;
   // per-token record bytes of each plane
   static constexpr int kc = 16 * KB, vc = 16 * VB;
   // stage layout (bytes), every plane 16-byte aligned
@@ -66,13 +76,12 @@ struct Geo {
   static constexpr int sm_ktab = vlut * 4;
   static constexpr int sm_stab = sm_ktab + ktab * 4;
   static constexpr int sm_stage = sm_stab + stab * 4;
-  static constexpr int sm_bar = sm_stage + kStages * stage;
-  static constexpr int sm_cnt = sm_bar + kStages * 8;
-  static constexpr int sm_q = sm_cnt + 16;                 // [2][128] floats
-  static constexpr int sm_m = sm_q + 2 * kD * 4;           // [warps] x 3 floats
-  static constexpr int sm_acc = sm_m + 3 * kWarps2 * 4;    // [warps][128] floats, values
-  static constexpr int sm_sacc = sm_acc + kWarps2 * kD * 4;  // [warps][128] floats, signs
-  static constexpr int total = sm_sacc + kWarps2 * kD * 4;
+  static constexpr int sm_bar = sm_stage + S * stage;
+  static constexpr int sm_cnt = sm_bar + S * 8;
+  static constexpr int sm_q = sm_cnt + 16 * ((S * 4 + 15) / 16);   // [2][128] floats
+  static constexpr int sm_misc = sm_q + 2 * kD * 4;
+  // per-warp partial states are parked in the key-table area at a flush
+  static_assert(NW * kPartialFloats <= ktab, "flush area must fit in the key table");
 };
 
 struct Decode2Args {
@@ -84,8 +93,9 @@ struct Decode2Args {
   const float *v_norm;
   const uint8_t *v_signs;
   const float *v_rnorm;
-  int capacity, heads_kv, heads_q, chunk, splits;
+  int capacity, batch, heads_kv, heads_q, chunk, splits;
   const int32_t *seq_lens;
+  const int32_t *tile_prefix;  // persistent kernel: [batch + 1] tiles before each batch
   const float *qprep;
   float *partials;
   const float *k_centroids;
@@ -108,14 +118,16 @@ __device__ __forceinline__ int slot_coord(int o) {
 
 // Lookup table T[v][pos] (row stride KPOS floats): the sum, over the CPP codes
 // that value v packs at position pos (code offsets pos*CPP + j, CB bits each),
-// of q[coord] * cb[code]. Built as lo[v & low bits] + hi[v >> LOB]: each
-// thread owns one position and a slice of the high values. SIGN: cb = {-1, +1}.
-template <int CB, int KPOS, int VBITS, bool SIGN>
+// of q[coord] * cb[code]. Built as lo[v & low bits] + hi[v >> LOB] by NT
+// threads: each owns one position and a slice of the high values.
+// SIGN: cb = {-1, +1}.
+template <int CB, int KPOS, int VBITS, bool SIGN, int NT>
 __device__ __forceinline__ void build_lookup(float *T, const float *q, const float *cb_g, float scale, int tid) {
   constexpr int CPP = VBITS / CB;
   constexpr int LOB = (VBITS >= 8) ? 4 : 3;  // low-part bits (a whole number of codes)
   constexpr int HIB = VBITS - LOB;
-  constexpr int NLO = 1 << LOB, PARTS = 128 / KPOS, NH = (1 << HIB) / PARTS;
+  constexpr int NLO = 1 << LOB, PARTS = NT / KPOS, NH = (1 << HIB) / PARTS;
+  static_assert(NH >= 1 && PARTS * KPOS == NT, "table build split");
   constexpr int M = (1 << CB) - 1;
   const int pos = tid % KPOS, part = tid / KPOS;
   float qv[CPP];
@@ -154,20 +166,354 @@ __device__ __forceinline__ float sign_unscale(int L) {
   return L == 10 ? 16384.f : (L == 11 ? 8192.f : (L == 12 ? 2048.f : (L == 13 ? 128.f : 0.5f)));
 }
 
+// Key tables (with log2(e)) and the value pair table for one query head.
+template <int KB, int VB, bool KQJL, int NT>
+__device__ __forceinline__ void build_tables(unsigned char *smem, int sm_ktab, int sm_stab, int vlut_words,
+                                             const float *s_q, const float *k_centroids, const float *v_centroids,
+                                             int tid) {
+  float *s_ktab = reinterpret_cast<float *>(smem + sm_ktab);
+  if constexpr (KB == 3) build_lookup<3, 64, 6, false, NT>(s_ktab, s_q, k_centroids, kLog2e, tid);
+  else build_lookup<KB, 16 * KB, 8, false, NT>(s_ktab, s_q, k_centroids, kLog2e, tid);
+  if constexpr (KQJL)
+    build_lookup<1, 16, 8, true, NT>(reinterpret_cast<float *>(smem + sm_stab), s_q + kD, nullptr, kLog2e, tid);
+  // value pair table: field f -> half2(c[f & mask], c[f >> VB]), replicated for every lane
+  uint32_t *vl = reinterpret_cast<uint32_t *>(smem);
+  for (int e = tid; e < vlut_words; e += NT) {
+    const int f = e >> 5;
+    vl[e] = pack_half2(__ldg(v_centroids + (f & ((1 << VB) - 1))), __ldg(v_centroids + (f >> VB)));
+  }
+}
+
+// Lane-invariant constants of the tile body.
+template <int KB>
+struct LaneConsts {
+  uint32_t kcon[4], ksel[4];  // key lookups: byte offset into T from (record word, constant, selector)
+  uint32_t ssel;              // key sign byte -> row offset (64-byte rows)
+  int my_j;                   // token (0..15 of the warp) this lane holds after the score reduction
+  int bsrc[4];                // lanes that hold the tokens of this lane's B fragment
+  uint32_t bsel, swsel, lane4;
+  bool bv_live, bs_live;
+
+  __device__ __forceinline__ explicit LaneConsts(int lane) {
+    const int half = lane >> 4, l = lane & 15, g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (KB == 4 || KB == 3) {
+        const int kk = (k + (lane >> 3)) & 3;  // staggered so that the 32 lanes hit 32 banks
+        kcon[k] = 4u * (4 * l + kk);
+        ksel[k] = (KB == 4) ? (0x5504u | ((uint32_t)kk << 4)) : (uint32_t)((6 * kk - 8) & 31);
+      } else if (KB == 2) {
+        const int jj = (k + half) & 1, bpos = 2 * l + jj;
+        kcon[k] = 4u * bpos;
+        ksel[k] = (uint32_t)((8 * (bpos & 3) - 7) & 31);
+      } else {
+        kcon[k] = 4u * l;
+        ksel[k] = (uint32_t)((8 * (l & 3) - 6) & 31);
+      }
+    }
+    ssel = (uint32_t)((8 * (l & 3) - 6) & 31);
+    // reduce-scatter result: lane l (within its half) holds step sigma(l); token j = 2 sigma + half
+    const int my_step = 4 * ((l >> 3) & 1) + 2 * ((l >> 2) & 1) + ((l >> 1) & 1);
+    my_j = 2 * my_step + half;
+    // token j of the warp sits on lanes 16(j&1) + 8((j>>3)&1) + 4((j>>2)&1) + 2((j>>1)&1) (+1);
+    // the even lane carries p nu, the odd one p rho
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = 2 * t4 + (c & 1) + 8 * (c >> 1);
+      bsrc[c] = 16 * (j & 1) + 8 * ((j >> 3) & 1) + 4 * ((j >> 2) & 1) + 2 * ((j >> 1) & 1) + ((g >> 1) & 1);
+    }
+    bsel = (g & 1) ? 0x7632u : 0x5410u;  // hi parts (even g) or lo parts (odd g)
+    bv_live = g < 2;
+    bs_live = (g >> 1) == 1;
+    lane4 = (uint32_t)lane << 2;
+    swsel = (g & 1) ? 0x7632u : 0x5410u;  // sign rows: half (g & 1) of sign word (g >> 1)
+  }
+};
+
+// Online-softmax state of one warp (base-2 logits).
+struct WarpState {
+  float m, l, w;
+  float acc[8][4];
+  __device__ __forceinline__ void reset() {
+    m = -INFINITY;
+    l = 0.f;
+    w = 0.f;
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[mb][j] = 0.f;
+  }
+};
+
+// One warp's 16 tokens (wbase .. wbase + 15 of the tile at `st`, tile start t0,
+// sequence end t_end): scores, online-softmax step, value and sign MMAs.
+template <typename Gm, int KB, int VB, bool KQJL, bool VQJL>
+__device__ __forceinline__ void tile_body(const unsigned char *st, const unsigned char *smem, int wbase, int t0,
+                                          int t_end, int lane, const LaneConsts<KB> &lc, WarpState &ws) {
+  const int half = lane >> 4, l = lane & 15, g = lane >> 2, t4 = lane & 3;
+  const float *kn = reinterpret_cast<const float *>(st + Gm::off_kn);
+  const float *kr = reinterpret_cast<const float *>(st + Gm::off_kr);
+  const unsigned char *tb = smem + Gm::sm_ktab;
+
+  // ---- scores: 8 steps of 2 tokens, 16 lanes per token
+  float part[8];
+#pragma unroll
+  for (int step = 0; step < 8; ++step) {
+    const int lt = wbase + 2 * step + half;
+    const uint32_t *rec = reinterpret_cast<const uint32_t *>(st + Gm::off_kc + lt * Gm::kc);
+    float sum;
+    if (KB == 4) {
+      const uint32_t w = rec[l];
+      float t[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        t[k] = *reinterpret_cast<const float *>(tb + __byte_perm(w, lc.kcon[k], lc.ksel[k]));
+      sum = (t[0] + t[1]) + (t[2] + t[3]);
+    } else if (KB == 3) {
+      // lane l owns pair slots 4l..4l+3 (24 bits at bit 24 l)
+      const int bit = 24 * l, wi = bit >> 5, off = bit & 31;
+      const uint32_t f24 = __funnelshift_r(rec[wi], rec[(wi + 1 < 12) ? wi + 1 : wi], off);
+      float t[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        t[k] = *reinterpret_cast<const float *>(tb + ((rotr(f24, lc.ksel[k]) & 0x3F00u) | lc.kcon[k]));
+      sum = (t[0] + t[1]) + (t[2] + t[3]);
+    } else if (KB == 2) {
+      const uint32_t w = rec[l >> 1];
+      float t[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        t[k] = *reinterpret_cast<const float *>(tb + ((rotr(w, lc.ksel[k]) & 0x7F80u) | lc.kcon[k]));
+      sum = t[0] + t[1];
+    } else {
+      const uint32_t w = rec[l >> 2];
+      sum = *reinterpret_cast<const float *>(tb + ((rotr(w, lc.ksel[0]) & 0x3FC0u) | lc.kcon[0]));
+    }
+    if (KQJL) {
+      const uint32_t *srec = reinterpret_cast<const uint32_t *>(st + Gm::off_ks + lt * 16);
+      const uint32_t w = srec[l >> 2];
+      const float ts =
+          *reinterpret_cast<const float *>(smem + Gm::sm_stab + ((rotr(w, lc.ssel) & 0x3FC0u) | (4u * l)));
+      sum = fmaf(kr[lt], ts, kn[lt] * sum);
+    }
+    part[step] = sum;
+  }
+  // reduce-scatter 8 values over the 16 lanes of each half
+  float sc;
+  {
+    float r4[4], r2[2];
+    const bool hb = (l & 8) != 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float send = hb ? part[k] : part[k + 4];
+      const float keep = hb ? part[k + 4] : part[k];
+      r4[k] = keep + __shfl_xor_sync(kFull, send, 8);
+    }
+    const bool hb2 = (l & 4) != 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = hb2 ? r4[k] : r4[k + 2];
+      const float keep = hb2 ? r4[k + 2] : r4[k];
+      r2[k] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+    const bool hb1 = (l & 2) != 0;
+    sc = (hb1 ? r2[1] : r2[0]) + __shfl_xor_sync(kFull, hb1 ? r2[0] : r2[1], 2);
+    sc += __shfl_xor_sync(kFull, sc, 1);
+  }
+  const int tok = wbase + lc.my_j;
+  const bool valid = t0 + tok < t_end;
+  if (!KQJL) sc *= kn[tok];
+  sc = valid ? sc : -INFINITY;
+
+  // ---- online softmax over the warp's 16 tokens (base 2)
+  float tmax = sc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+  const float m_new = fmaxf(ws.m, tmax);
+  const float p = valid ? ex2_approx(sc - m_new) : 0.f;
+  if (m_new != ws.m) {  // warp-uniform: the running max moved (m = -inf scales zeros)
+    const float scale = ex2_approx(ws.m - m_new);
+    ws.l *= scale;
+    ws.w *= scale;
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ws.acc[mb][j] *= scale;
+    ws.m = m_new;
+  }
+  ws.l += p;  // every token sits on two lanes: halved at the flush
+
+  // ---- B operands: this lane's token weight (p nu on even lanes, p rho on odd ones)
+  // as an fp16 hi/lo pair, gathered into column g of the MMA's B fragment
+  uint32_t bv0, bv1, bs0 = 0, bs1 = 0;
+  {
+    const bool odd = VQJL && (lane & 1);
+    const float *wsrc = reinterpret_cast<const float *>(st + (odd ? Gm::off_vr : Gm::off_vn));
+    const float wv = valid ? p * wsrc[tok] : 0.f;
+    ws.w += wv;  // sum of p rho over the odd lanes (the even ones are ignored)
+    const __half hh = __float2half_rn(wv);
+    const float rem = wv - __half2float(hh);
+    const uint32_t hl =
+        (uint32_t)__half_as_ushort(hh) | ((uint32_t)__half_as_ushort(__float2half_rn(rem)) << 16);
+    const uint32_t x0 = __shfl_sync(kFull, hl, lc.bsrc[0]);
+    const uint32_t x1 = __shfl_sync(kFull, hl, lc.bsrc[1]);
+    const uint32_t x2 = __shfl_sync(kFull, hl, lc.bsrc[2]);
+    const uint32_t x3 = __shfl_sync(kFull, hl, lc.bsrc[3]);
+    const uint32_t b0 = __byte_perm(x0, x1, lc.bsel), b1 = __byte_perm(x2, x3, lc.bsel);
+    bv0 = lc.bv_live ? b0 : 0u;
+    bv1 = lc.bv_live ? b1 : 0u;
+    if (VQJL) {
+      bs0 = lc.bs_live ? b0 : 0u;
+      bs1 = lc.bs_live ? b1 : 0u;
+    }
+  }
+
+  // ---- values: decode (token, coordinate-pair) fp16 pairs, transpose, MMA
+  {
+    uint32_t w0[VB], w1[VB];
+    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + g) * Gm::vc);
+    const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + 8 + g) * Gm::vc);
+#pragma unroll
+    for (int k = 0; k < VB; ++k) {
+      w0[k] = r0[VB * t4 + k];
+      w1[k] = r1[VB * t4 + k];
+    }
+    // field n of a span -> byte offset (field << 7) | (lane << 2) of the value table
+    auto lut = [&](const uint32_t(&w)[VB], int n) -> uint32_t {
+      constexpr int F = 2 * VB;
+      constexpr uint32_t mask = ((1u << F) - 1u) << 7;
+      const int bit = F * n, wi = bit >> 5, off = bit & 31;
+      uint32_t x;
+      if (off < 7) x = w[wi] << (7 - off);
+      else x = __funnelshift_r(w[wi], w[(wi + 1 < VB) ? wi + 1 : wi], off - 7);
+      return *reinterpret_cast<const uint32_t *>(smem + ((x & mask) | lc.lane4));
+    };
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const uint32_t x00 = movmatrix_t(lut(w0, 2 * mb));
+      const uint32_t x01 = movmatrix_t(lut(w0, 2 * mb + 1));
+      const uint32_t x10 = movmatrix_t(lut(w1, 2 * mb));
+      const uint32_t x11 = movmatrix_t(lut(w1, 2 * mb + 1));
+      mma_16816(ws.acc[mb], x00, x01, x10, x11, bv0, bv1);
+    }
+  }
+
+  // ---- QJL signs: rows of this thread = bits of half (g & 1) of sign word (g >> 1)
+  if (VQJL) {
+    const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + Gm::off_vs);
+    const int wsel = g >> 1;
+    const uint32_t wa0 = sw[(wbase + 2 * t4) * 4 + wsel], wb0 = sw[(wbase + 2 * t4 + 1) * 4 + wsel];
+    const uint32_t wa1 = sw[(wbase + 2 * t4 + 8) * 4 + wsel], wb1 = sw[(wbase + 2 * t4 + 9) * 4 + wsel];
+    // token 2t (8 + 2t) in bits 0..15, token 2t + 1 (9 + 2t) in bits 16..31
+    const uint32_t s0 = __byte_perm(wa0, wb0, lc.swsel), s1 = __byte_perm(wa1, wb1, lc.swsel);
+    const uint32_t s0r10 = rotr(s0, 22), s0r5 = rotr(s0, 27), s0r27 = rotr(s0, 5);
+    const uint32_t s1r10 = rotr(s1, 22), s1r5 = rotr(s1, 27), s1r27 = rotr(s1, 5);
+    auto pick = [&](int k, uint32_t r0, uint32_t r5, uint32_t r10, uint32_t r27) -> uint32_t {
+      const uint32_t src = sign_rot(k) == 10 ? r10 : (sign_rot(k) == 5 ? r5 : (sign_rot(k) == 0 ? r0 : r27));
+      return src & (0x00010001u << sign_land(k));
+    };
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const uint32_t a0 = pick(2 * mb, s0, s0r5, s0r10, s0r27);
+      const uint32_t a1 = pick(2 * mb + 1, s0, s0r5, s0r10, s0r27);
+      const uint32_t a2 = pick(2 * mb, s1, s1r5, s1r10, s1r27);
+      const uint32_t a3 = pick(2 * mb + 1, s1, s1r5, s1r10, s1r27);
+      mma_16816(ws.acc[mb], a0, a1, a2, a3, bs0, bs1);
+    }
+  }
+}
+
+// Park one warp's state as [m, l, w, pad, values[128], signs[128]] (signs
+// un-scaled, 2 sum p rho b - sum p rho not yet formed).
+template <bool VQJL>
+__device__ __forceinline__ void park_warp(float *dst, int lane, const WarpState &ws) {
+  const int g = lane >> 2, t4 = lane & 3;
+  float lw = ws.l, ww = (lane & 1) ? ws.w : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lw += __shfl_xor_sync(kFull, lw, o);
+    ww += __shfl_xor_sync(kFull, ww, o);
+  }
+  if (lane == 0) {
+    dst[0] = ws.m;
+    dst[1] = 0.5f * lw;
+    dst[2] = ww;
+  }
+  float *va = dst + 4, *sa = dst + 4 + kD;
+  if (t4 == 0) {  // columns 0/1: value sums of coordinates 16mb + g and 16mb + 8 + g
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      va[16 * mb + g] = ws.acc[mb][0] + ws.acc[mb][1];
+      va[16 * mb + 8 + g] = ws.acc[mb][2] + ws.acc[mb][3];
+    }
+  } else if (VQJL && t4 == 1) {  // columns 2/3: sign sums; row (mb, r) is bit 2mb + r of half g&1 of word g>>1
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const int c0 = 64 * (g & 1) + 8 * mb + 2 * (g >> 1);
+      sa[c0] = (ws.acc[mb][0] + ws.acc[mb][1]) * sign_unscale(sign_land(2 * mb));
+      sa[c0 + 1] = (ws.acc[mb][2] + ws.acc[mb][3]) * sign_unscale(sign_land(2 * mb + 1));
+    }
+  }
+}
+
+// Merge NWG parked warp states (stride kPartialFloats) into one partial record;
+// thread i of 128 handles coordinate i.
+template <int NWG, bool VQJL>
+__device__ __forceinline__ void merge_parked(const float *src, int i, float *rec) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NWG; ++w) M = fmaxf(M, src[w * kPartialFloats]);
+  float L = 0.f, A = 0.f, Sg = 0.f;
+#pragma unroll
+  for (int w = 0; w < NWG; ++w) {
+    const float *p = src + w * kPartialFloats;
+    const float e = (p[0] == -INFINITY) ? 0.f : ex2_approx(p[0] - M);
+    L += p[1] * e;
+    A += p[4 + i] * e;
+    // the sign MMA summed p rho b over bits b; sum p rho sigma = 2 sum p rho b - sum p rho
+    if (VQJL) Sg += (2.f * p[4 + kD + i] - p[2]) * e;
+  }
+  if (i == 0) {
+    rec[0] = M * kLn2;  // natural-log units for the combine step
+    rec[1] = L;
+  }
+  rec[2 + i] = A;
+  rec[2 + kD + i] = Sg;
+}
+
+template <typename Gm, bool KQJL, bool VQJL>
+__device__ __forceinline__ void issue_tile_to(unsigned char *st, uint64_t *bar, const Decode2Args &a, size_t s0, int n) {
+  const int n4 = (n + 3) & ~3;  // norms in 16-byte units
+  uint32_t bytes = n * Gm::kc + n4 * 4 + n * Gm::vc + n4 * 4;
+  if (KQJL) bytes += n * 16 + n4 * 4;
+  if (VQJL) bytes += n * 16 + n4 * 4;
+  mbar_arrive_expect_tx(bar, bytes);
+  tma_load_1d(st + Gm::off_kc, a.k_codes + s0 * Gm::kc, n * Gm::kc, bar);
+  tma_load_1d(st + Gm::off_kn, a.k_norm + s0, n4 * 4, bar);
+  if (KQJL) {
+    tma_load_1d(st + Gm::off_ks, a.k_signs + s0 * 16, n * 16, bar);
+    tma_load_1d(st + Gm::off_kr, a.k_rnorm + s0, n4 * 4, bar);
+  }
+  tma_load_1d(st + Gm::off_vc, a.v_codes + s0 * Gm::vc, n * Gm::vc, bar);
+  tma_load_1d(st + Gm::off_vn, a.v_norm + s0, n4 * 4, bar);
+  if (VQJL) {
+    tma_load_1d(st + Gm::off_vs, a.v_signs + s0 * 16, n * 16, bar);
+    tma_load_1d(st + Gm::off_vr, a.v_rnorm + s0, n4 * 4, bar);
+  }
+}
+
+// ============================================================================
+// split-K kernel: one CTA of 4 warps per (batch, kv head, chunk)
+// ============================================================================
 template <int KB, int VB, bool KQJL, bool VQJL>
-__global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args a) {
-  using Gm = Geo<KB, VB, KQJL, VQJL>;
+__global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
+  using Gm = Geo<KB, VB, KQJL, VQJL, 4, 3>;
+  constexpr int S = Gm::kStages;
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char *s_vlut = smem;  // [vval][32] half2 words, at offset 0
-  float *s_ktab = reinterpret_cast<float *>(smem + Gm::sm_ktab);
-  float *s_stab = reinterpret_cast<float *>(smem + Gm::sm_stab);
   unsigned char *s_stage = smem + Gm::sm_stage;
   uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Gm::sm_bar);
   unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + Gm::sm_cnt);
-  float *s_q = reinterpret_cast<float *>(smem + Gm::sm_q);  // [128] q_rot / sqrt(d), [128] scaled S q
-  float *s_m = reinterpret_cast<float *>(smem + Gm::sm_m);  // [warps] max, [warps] sum, [warps] sign weight sum
-  float *s_acc = reinterpret_cast<float *>(smem + Gm::sm_acc);
-  float *s_sacc = reinterpret_cast<float *>(smem + Gm::sm_sacc);
+  float *s_q = reinterpret_cast<float *>(smem + Gm::sm_q);
 
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -178,365 +524,186 @@ __global__ void __launch_bounds__(kWarps2 * 32, 2) decode2_g1_kernel(Decode2Args
   const size_t slot0 = ((size_t)b * a.heads_kv + hk) * a.capacity;
   const int hq = hk;  // one query head per KV head
 
-  // ---------------- prologue: barriers, first TMA stages, tables
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&s_full[s], 1);
       s_cnt[s] = 0;
     }
     mbar_fence_init();
   }
   __syncthreads();
-
-  auto issue_tile = [&](int tile) {
-    const int stage = tile % kStages;
-    unsigned char *st = s_stage + stage * Gm::stage;
+  auto issue = [&](int tile) {
     const int t0 = t_begin + tile * kTT;
-    const int n = min(kTT, t_end - t0);
-    const int n4 = (n + 3) & ~3;  // norms in 16-byte units
-    uint32_t bytes = n * Gm::kc + n4 * 4 + n * Gm::vc + n4 * 4;
-    if (KQJL) bytes += n * 16 + n4 * 4;
-    if (VQJL) bytes += n * 16 + n4 * 4;
-    mbar_arrive_expect_tx(&s_full[stage], bytes);
-    const size_t s0 = slot0 + t0;
-    tma_load_1d(st + Gm::off_kc, a.k_codes + s0 * Gm::kc, n * Gm::kc, &s_full[stage]);
-    tma_load_1d(st + Gm::off_kn, a.k_norm + s0, n4 * 4, &s_full[stage]);
-    if (KQJL) {
-      tma_load_1d(st + Gm::off_ks, a.k_signs + s0 * 16, n * 16, &s_full[stage]);
-      tma_load_1d(st + Gm::off_kr, a.k_rnorm + s0, n4 * 4, &s_full[stage]);
-    }
-    tma_load_1d(st + Gm::off_vc, a.v_codes + s0 * Gm::vc, n * Gm::vc, &s_full[stage]);
-    tma_load_1d(st + Gm::off_vn, a.v_norm + s0, n4 * 4, &s_full[stage]);
-    if (VQJL) {
-      tma_load_1d(st + Gm::off_vs, a.v_signs + s0 * 16, n * 16, &s_full[stage]);
-      tma_load_1d(st + Gm::off_vr, a.v_rnorm + s0, n4 * 4, &s_full[stage]);
-    }
+    issue_tile_to<Gm, KQJL, VQJL>(s_stage + (tile % S) * Gm::stage, &s_full[tile % S], a, slot0 + t0,
+                                  min(kTT, t_end - t0));
   };
   if (tid == 0)
-    for (int i = 0; i < kStages && i < ntiles; ++i) issue_tile(i);
+    for (int i = 0; i < S && i < ntiles; ++i) issue(i);
 
   // prepared query (already rotated and scaled by 1/sqrt(d); S q scaled by sqrt(pi/2)/m/sqrt(d))
   const float *qp = a.qprep + ((size_t)b * a.heads_q + hq) * 2 * kD;
   s_q[tid] = __ldg(qp + tid);
   if (KQJL) s_q[kD + tid] = __ldg(qp + kD + tid);
   __syncthreads();
-
-  // key tables carry log2(e) so that scores come out in base-2 units
-  if constexpr (KB == 3) build_lookup<3, 64, 6, false>(s_ktab, s_q, a.k_centroids, kLog2e, tid);
-  else build_lookup<KB, 16 * KB, 8, false>(s_ktab, s_q, a.k_centroids, kLog2e, tid);
-  if constexpr (KQJL) build_lookup<1, 16, 8, true>(s_stab, s_q + kD, nullptr, kLog2e, tid);
-  {
-    // value pair table: field f -> half2(c[f & mask], c[f >> VB]), replicated for every lane
-    const float *vcb = a.v_centroids;
-    uint32_t *vl = reinterpret_cast<uint32_t *>(s_vlut);
-    for (int e = tid; e < Gm::vlut; e += blockDim.x) {
-      const int f = e >> 5;
-      vl[e] = pack_half2(__ldg(vcb + (f & ((1 << VB) - 1))), __ldg(vcb + (f >> VB)));
-    }
-  }
+  build_tables<KB, VB, KQJL, 128>(smem, Gm::sm_ktab, Gm::sm_stab, Gm::vlut, s_q, a.k_centroids, a.v_centroids,
+                                  tid);
   __syncthreads();
 
-  // ---------------- per-lane constants
-  const int half = lane >> 4, l = lane & 15;
-  const int g = lane >> 2, t4 = lane & 3;
-  // key lookups: byte offset into T from (record word, constant, selector / rotation)
-  uint32_t kcon[4], ksel[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (KB == 4 || KB == 3) {
-      const int kk = (k + (lane >> 3)) & 3;  // staggered so that the 32 lanes hit 32 banks
-      kcon[k] = 4u * (4 * l + kk);
-      ksel[k] = (KB == 4) ? (0x5504u | ((uint32_t)kk << 4)) : (uint32_t)((6 * kk - 8) & 31);
-    } else if (KB == 2) {
-      const int jj = (k + half) & 1, bpos = 2 * l + jj;
-      kcon[k] = 4u * bpos;
-      ksel[k] = (uint32_t)((8 * (bpos & 3) - 7) & 31);
-    } else {
-      kcon[k] = 4u * l;
-      ksel[k] = (uint32_t)((8 * (l & 3) - 6) & 31);
-    }
-  }
-  const uint32_t ssel = (uint32_t)((8 * (l & 3) - 6) & 31);  // key sign byte l -> row offset (64-byte rows)
-  // reduce-scatter result: lane l (within its half) holds step sigma(l); token j = 2 sigma + half
-  const int my_step = 4 * ((l >> 3) & 1) + 2 * ((l >> 2) & 1) + ((l >> 1) & 1);
-  const int my_j = 2 * my_step + half;
-  // B gather: token j of the warp sits on lanes 16(j&1) + 8((j>>3)&1) + 4((j>>2)&1) + 2((j>>1)&1) (+1);
-  // the even lane carries p nu, the odd one p rho
-  int bsrc[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int j = 2 * t4 + (c & 1) + 8 * (c >> 1);
-    bsrc[c] = 16 * (j & 1) + 8 * ((j >> 3) & 1) + 4 * ((j >> 2) & 1) + 2 * ((j >> 1) & 1) + ((g >> 1) & 1);
-  }
-  const uint32_t bsel = (g & 1) ? 0x7632u : 0x5410u;  // hi parts (even g) or lo parts (odd g)
-  const bool bv_live = g < 2, bs_live = (g >> 1) == 1;
-  const uint32_t lane4 = (uint32_t)lane << 2;
-  // sign operands: this thread's rows are half (g & 1) of sign word (g >> 1)
-  const uint32_t swsel = (g & 1) ? 0x7632u : 0x5410u;
-
-  float m_run = -INFINITY, l_run = 0.f, w_run = 0.f;
-  float acc[8][4];
-#pragma unroll
-  for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[mb][j] = 0.f;
-
+  const LaneConsts<KB> lc(lane);
+  WarpState ws;
+  ws.reset();
   // A wait that runs out of time (it never should) records TQ_ERR_TIMEOUT; the
   // warp then stops waiting and computing but keeps releasing its stages, so
   // no warp is left behind. The partial record is then meaningless, which the
   // error word reports.
   bool bad = false;
   for (int tile = 0; tile < ntiles; ++tile) {
-    const int stage = tile % kStages;
-    const uint32_t parity = (tile / kStages) & 1;
-    if (!bad && !mbar_wait_bounded(&s_full[stage], parity, a.error)) bad = true;
+    const int stage = tile % S;
+    if (!bad && !mbar_wait_bounded(&s_full[stage], (tile / S) & 1, a.error)) bad = true;
     bad = __any_sync(kFull, bad);  // whole warps skip together (the body shuffles)
-    const unsigned char *st = s_stage + stage * Gm::stage;
-    const int t0 = t_begin + tile * kTT;
-    const int wbase = warp * 16;  // this warp's first token within the tile
-    if (!bad) {
-      const float *kn = reinterpret_cast<const float *>(st + Gm::off_kn);
-      const float *kr = reinterpret_cast<const float *>(st + Gm::off_kr);
-
-      // ---- scores: 8 steps of 2 tokens, 16 lanes per token
-      float part[8];
-#pragma unroll
-      for (int step = 0; step < 8; ++step) {
-        const int lt = wbase + 2 * step + half;
-        const uint32_t *rec = reinterpret_cast<const uint32_t *>(st + Gm::off_kc + lt * Gm::kc);
-        const unsigned char *tb = reinterpret_cast<const unsigned char *>(s_ktab);
-        float sum;
-        if (KB == 4) {
-          const uint32_t w = rec[l];
-          float t[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) t[k] = *reinterpret_cast<const float *>(tb + __byte_perm(w, kcon[k], ksel[k]));
-          sum = (t[0] + t[1]) + (t[2] + t[3]);
-        } else if (KB == 3) {
-          // lane l owns pair slots 4l..4l+3 (24 bits at bit 24 l)
-          const int bit = 24 * l, wi = bit >> 5, off = bit & 31;
-          const uint32_t f24 = __funnelshift_r(rec[wi], rec[(wi + 1 < 12) ? wi + 1 : wi], off);
-          float t[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            t[k] = *reinterpret_cast<const float *>(tb + ((rotr(f24, ksel[k]) & 0x3F00u) | kcon[k]));
-          sum = (t[0] + t[1]) + (t[2] + t[3]);
-        } else if (KB == 2) {
-          const uint32_t w = rec[l >> 1];
-          float t[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            t[k] = *reinterpret_cast<const float *>(tb + ((rotr(w, ksel[k]) & 0x7F80u) | kcon[k]));
-          sum = t[0] + t[1];
-        } else {
-          const uint32_t w = rec[l >> 2];
-          sum = *reinterpret_cast<const float *>(tb + ((rotr(w, ksel[0]) & 0x3FC0u) | kcon[0]));
-        }
-        if (KQJL) {
-          const uint32_t *srec = reinterpret_cast<const uint32_t *>(st + Gm::off_ks + lt * 16);
-          const uint32_t w = srec[l >> 2];
-          const float ts = *reinterpret_cast<const float *>(reinterpret_cast<const unsigned char *>(s_stab) +
-                                                            ((rotr(w, ssel) & 0x3FC0u) | (4u * l)));
-          sum = fmaf(kr[lt], ts, kn[lt] * sum);
-        }
-        part[step] = sum;
-      }
-      // reduce-scatter 8 values over the 16 lanes of each half
-      float sc;
-      {
-        float r4[4], r2[2];
-        const bool hb = (l & 8) != 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float send = hb ? part[k] : part[k + 4];
-          const float keep = hb ? part[k + 4] : part[k];
-          r4[k] = keep + __shfl_xor_sync(kFull, send, 8);
-        }
-        const bool hb2 = (l & 4) != 0;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float send = hb2 ? r4[k] : r4[k + 2];
-          const float keep = hb2 ? r4[k + 2] : r4[k];
-          r2[k] = keep + __shfl_xor_sync(kFull, send, 4);
-        }
-        const bool hb1 = (l & 2) != 0;
-        sc = (hb1 ? r2[1] : r2[0]) + __shfl_xor_sync(kFull, hb1 ? r2[0] : r2[1], 2);
-        sc += __shfl_xor_sync(kFull, sc, 1);
-      }
-      const int tok = wbase + my_j;
-      const bool valid = t0 + tok < t_end;
-      if (!KQJL) sc *= kn[tok];
-      sc = valid ? sc : -INFINITY;
-
-      // ---- online softmax over the warp's 16 tokens (base 2)
-      float tmax = sc;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
-      const float m_new = fmaxf(m_run, tmax);
-      const float p = valid ? ex2_approx(sc - m_new) : 0.f;
-      if (m_new != m_run) {  // warp-uniform: the running max moved (m_run = -inf scales zeros)
-        const float scale = ex2_approx(m_run - m_new);
-        l_run *= scale;
-        w_run *= scale;
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[mb][j] *= scale;
-        m_run = m_new;
-      }
-      l_run += p;  // every token sits on two lanes: halved at the merge
-
-      // ---- B operands: this lane's token weight (p nu on even lanes, p rho on odd ones)
-      // as an fp16 hi/lo pair, gathered into column g of the MMA's B fragment
-      uint32_t bv0, bv1, bs0 = 0, bs1 = 0;
-      {
-        const bool odd = VQJL && (lane & 1);
-        const float *wsrc = reinterpret_cast<const float *>(st + (odd ? Gm::off_vr : Gm::off_vn));
-        const float wv = valid ? p * wsrc[tok] : 0.f;
-        w_run += wv;  // sum of p rho over the odd lanes (the even ones are ignored)
-        const __half hh = __float2half_rn(wv);
-        const float rem = wv - __half2float(hh);
-        const uint32_t hl = (uint32_t)__half_as_ushort(hh) | ((uint32_t)__half_as_ushort(__float2half_rn(rem)) << 16);
-        const uint32_t x0 = __shfl_sync(kFull, hl, bsrc[0]);
-        const uint32_t x1 = __shfl_sync(kFull, hl, bsrc[1]);
-        const uint32_t x2 = __shfl_sync(kFull, hl, bsrc[2]);
-        const uint32_t x3 = __shfl_sync(kFull, hl, bsrc[3]);
-        const uint32_t b0 = __byte_perm(x0, x1, bsel), b1 = __byte_perm(x2, x3, bsel);
-        bv0 = bv_live ? b0 : 0u;
-        bv1 = bv_live ? b1 : 0u;
-        if (VQJL) {
-          bs0 = bs_live ? b0 : 0u;
-          bs1 = bs_live ? b1 : 0u;
-        }
-      }
-
-      // ---- values: decode (token, coordinate-pair) fp16 pairs, transpose, MMA
-      {
-        uint32_t w0[VB], w1[VB];
-        const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + g) * Gm::vc);
-        const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + 8 + g) * Gm::vc);
-#pragma unroll
-        for (int k = 0; k < VB; ++k) {
-          w0[k] = r0[VB * t4 + k];
-          w1[k] = r1[VB * t4 + k];
-        }
-        // field n of a span -> byte offset (field << 7) | (lane << 2) of the value table
-        auto lut = [&](const uint32_t(&w)[VB], int n) -> uint32_t {
-          constexpr int F = 2 * VB;
-          constexpr uint32_t mask = ((1u << F) - 1u) << 7;
-          const int bit = F * n, wi = bit >> 5, off = bit & 31;
-          uint32_t x;
-          if (off < 7) x = w[wi] << (7 - off);
-          else x = __funnelshift_r(w[wi], w[(wi + 1 < VB) ? wi + 1 : wi], off - 7);
-          return *reinterpret_cast<const uint32_t *>(s_vlut + ((x & mask) | lane4));
-        };
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          const uint32_t x00 = movmatrix_t(lut(w0, 2 * mb));
-          const uint32_t x01 = movmatrix_t(lut(w0, 2 * mb + 1));
-          const uint32_t x10 = movmatrix_t(lut(w1, 2 * mb));
-          const uint32_t x11 = movmatrix_t(lut(w1, 2 * mb + 1));
-          mma_16816(acc[mb], x00, x01, x10, x11, bv0, bv1);
-        }
-      }
-
-      // ---- QJL signs: rows of this thread = bits of half (g & 1) of sign word (g >> 1)
-      if (VQJL) {
-        const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + Gm::off_vs);
-        const int wsel = g >> 1;
-        const uint32_t wa0 = sw[(wbase + 2 * t4) * 4 + wsel], wb0 = sw[(wbase + 2 * t4 + 1) * 4 + wsel];
-        const uint32_t wa1 = sw[(wbase + 2 * t4 + 8) * 4 + wsel], wb1 = sw[(wbase + 2 * t4 + 9) * 4 + wsel];
-        // token 2t (8 + 2t) in bits 0..15, token 2t + 1 (9 + 2t) in bits 16..31
-        const uint32_t s0 = __byte_perm(wa0, wb0, swsel), s1 = __byte_perm(wa1, wb1, swsel);
-        const uint32_t s0r10 = rotr(s0, 22), s0r5 = rotr(s0, 27), s0r27 = rotr(s0, 5);
-        const uint32_t s1r10 = rotr(s1, 22), s1r5 = rotr(s1, 27), s1r27 = rotr(s1, 5);
-        auto pick = [&](int k, uint32_t r0, uint32_t r5, uint32_t r10, uint32_t r27) -> uint32_t {
-          const uint32_t src = sign_rot(k) == 10 ? r10 : (sign_rot(k) == 5 ? r5 : (sign_rot(k) == 0 ? r0 : r27));
-          return src & (0x00010001u << sign_land(k));
-        };
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          const uint32_t a0 = pick(2 * mb, s0, s0r5, s0r10, s0r27);
-          const uint32_t a1 = pick(2 * mb + 1, s0, s0r5, s0r10, s0r27);
-          const uint32_t a2 = pick(2 * mb, s1, s1r5, s1r10, s1r27);
-          const uint32_t a3 = pick(2 * mb + 1, s1, s1r5, s1r10, s1r27);
-          mma_16816(acc[mb], a0, a1, a2, a3, bs0, bs1);
-        }
-      }
-    }
-
+    if (!bad)
+      tile_body<Gm, KB, VB, KQJL, VQJL>(s_stage + stage * Gm::stage, smem, warp * 16, t_begin + tile * kTT, t_end,
+                                        lane, lc, ws);
     // release the stage: the last of the four warps refills it
     __syncwarp();
     if (lane == 0) {
       __threadfence_block();
       const unsigned old = atomicAdd(&s_cnt[stage], 1u);
-      if ((old & (kWarps2 - 1)) == kWarps2 - 1 && tile + kStages < ntiles) {
+      if ((old & 3u) == 3u && tile + S < ntiles) {
         __threadfence_block();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue_tile(tile + kStages);
+        issue(tile + S);
       }
     }
   }
 
-  // ---------------- merge the warps and write this chunk's partial record
-  {
-    float lw = l_run, ww = (lane & 1) ? w_run : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lw += __shfl_xor_sync(kFull, lw, o);
-      ww += __shfl_xor_sync(kFull, ww, o);
+  // merge the warps (parked in the key-table area) into this chunk's partial record
+  __syncthreads();
+  float *park = reinterpret_cast<float *>(smem + Gm::sm_ktab);
+  park_warp<VQJL>(park + warp * kPartialFloats, lane, ws);
+  __syncthreads();
+  merge_parked<4, VQJL>(park, tid,
+                        a.partials + (((size_t)b * a.heads_q + hq) * a.splits + split) * kPartialFloats);
+}
+
+// ============================================================================
+// persistent kernel: two CTAs of 8 warps per SM; warp group grp (4 warps)
+// takes the CTA's tiles of local parity grp
+// ============================================================================
+template <int KB, int VB, bool KQJL, bool VQJL>
+__global__ void __launch_bounds__(256, 2) decode_persist_kernel(Decode2Args a) {
+  using Gm = Geo<KB, VB, KQJL, VQJL, 8, 4>;
+  constexpr int S = Gm::kStages;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char *s_stage = smem + Gm::sm_stage;
+  uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Gm::sm_bar);
+  unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + Gm::sm_cnt);
+  float *s_q = reinterpret_cast<float *>(smem + Gm::sm_q);
+  int *s_pre = reinterpret_cast<int *>(smem + Gm::sm_misc);  // [batch + 1] tile prefix
+  int *s_len = s_pre + kMaxPersistBatch + 1;                  // [batch] clamped lengths
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, grp = warp >> 2;
+  const int B = a.batch, H = a.heads_kv;
+  for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
+  for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&s_full[s], 1);
+      s_cnt[s] = 0;
     }
-    if (lane == 0) {
-      s_m[warp] = m_run;
-      s_m[kWarps2 + warp] = 0.5f * lw;
-      s_m[2 * kWarps2 + warp] = ww;
-    }
-  }
-  if (t4 == 0) {  // columns 0/1: value sums of coordinates 16mb + g and 16mb + 8 + g
-#pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-      s_acc[warp * kD + 16 * mb + g] = acc[mb][0] + acc[mb][1];
-      s_acc[warp * kD + 16 * mb + 8 + g] = acc[mb][2] + acc[mb][3];
-    }
-  } else if (VQJL && t4 == 1) {  // columns 2/3: sign sums; row (mb, r) is bit 2mb + r of half g&1 of word g>>1
-#pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-      const int c0 = 64 * (g & 1) + 8 * mb + 2 * (g >> 1);
-      s_sacc[warp * kD + c0] = (acc[mb][0] + acc[mb][1]) * sign_unscale(sign_land(2 * mb));
-      s_sacc[warp * kD + c0 + 1] = (acc[mb][2] + acc[mb][3]) * sign_unscale(sign_land(2 * mb + 1));
-    }
+    mbar_fence_init();
   }
   __syncthreads();
-  const int i = tid;
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kWarps2; ++w) M = fmaxf(M, s_m[w]);
-  float L = 0.f, A = 0.f, Sg = 0.f;
-#pragma unroll
-  for (int w = 0; w < kWarps2; ++w) {
-    const float e = (s_m[w] == -INFINITY) ? 0.f : ex2_approx(s_m[w] - M);
-    L += s_m[kWarps2 + w] * e;
-    A += s_acc[w * kD + i] * e;
-    // the sign MMA summed p rho b over bits b; sum p rho sigma = 2 sum p rho b - sum p rho
-    if (VQJL) Sg += (2.f * s_sacc[w * kD + i] - s_m[2 * kWarps2 + w]) * e;
+  const long long T = (long long)H * s_pre[B];
+  const long long C = gridDim.x, c = blockIdx.x;
+  const long long g0 = T * c / C, g1 = T * (c + 1) / C;
+  if (g0 >= g1) return;  // whole CTA: nothing to do (no record is read for it)
+
+  // batch of global tile g: the largest b with H * pre[b] <= g
+  auto batch_of = [&](long long g) -> int {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((long long)H * s_pre[mid] <= g) lo = mid;
+      else hi = mid;
+    }
+    return lo;
+  };
+  auto issue = [&](long long i) {  // local tile i -> stage i % S
+    const long long g = g0 + i;
+    const int bb = batch_of(g);
+    const int nb = s_pre[bb + 1] - s_pre[bb];
+    const long long r = g - (long long)H * s_pre[bb];
+    const int h = (int)(r / nb), tt = (int)(r % nb);
+    const int t0 = tt * kTT;
+    issue_tile_to<Gm, KQJL, VQJL>(s_stage + (i % S) * Gm::stage, &s_full[i % S], a,
+                                  ((size_t)bb * H + h) * a.capacity + t0, min(kTT, s_len[bb] - t0));
+  };
+  if (tid == 0)
+    for (long long i = 0; i < S && g0 + i < g1; ++i) issue(i);
+
+  const LaneConsts<KB> lc(lane);
+  WarpState ws;
+  bool bad = false;
+  float *park = reinterpret_cast<float *>(smem + Gm::sm_ktab);
+  long long g = g0;
+  while (g < g1) {  // one segment per (batch, kv head) the slice touches
+    const int bb = batch_of(g);
+    const int nb = s_pre[bb + 1] - s_pre[bb];
+    const long long ubase = (long long)H * s_pre[bb];
+    const int h = (int)((g - ubase) / nb);
+    const long long us = ubase + (long long)h * nb;
+    const long long se = min(us + nb, g1);
+    const int len = s_len[bb];
+    const int u = bb * H + h;
+
+    // query and tables for this head (the previous segment's readers are done)
+    const float *qp = a.qprep + (size_t)u * 2 * kD;  // one query head per KV head: row u
+    s_q[tid] = __ldg(qp + tid);
+    __syncthreads();
+    build_tables<KB, VB, KQJL, 256>(smem, Gm::sm_ktab, Gm::sm_stab, Gm::vlut, s_q, a.k_centroids, a.v_centroids,
+                                    tid);
+    __syncthreads();
+
+    ws.reset();
+    // this group's tiles: local index i = t - g0 with i % 2 == grp
+    long long t = g + (((g - g0) & 1) != grp ? 1 : 0);
+    for (; t < se; t += 2) {
+      const long long i = t - g0;
+      const int stage = (int)(i % S);
+      if (!bad && !mbar_wait_bounded(&s_full[stage], (uint32_t)((i / S) & 1), a.error)) bad = true;
+      bad = __any_sync(kFull, bad);
+      if (!bad)
+        tile_body<Gm, KB, VB, KQJL, VQJL>(s_stage + stage * Gm::stage, smem, (warp & 3) * 16,
+                                          (int)((t - us) * kTT), len, lane, lc, ws);
+      // release the stage: the last of the group's four warps refills it
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        const unsigned old = atomicAdd(&s_cnt[stage], 1u);
+        if ((old & 3u) == 3u && g0 + i + S < g1) {
+          __threadfence_block();
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(i + S);
+        }
+      }
+    }
+
+    // flush: both groups are done with this head; park the warps in the table area
+    __syncthreads();
+    park_warp<VQJL>(park + warp * kPartialFloats, lane, ws);
+    __syncthreads();
+    merge_parked<4, VQJL>(park + grp * 4 * kPartialFloats, tid & 127,
+                          a.partials + ((size_t)(c + u) * 2 + grp) * kPartialFloats);
+    __syncthreads();  // the table area is rebuilt next
+    g = se;
   }
-  float *rec = a.partials + (((size_t)b * a.heads_q + hq) * a.splits + split) * kPartialFloats;
-  if (i == 0) {
-    rec[0] = M * kLn2;  // natural-log units for the combine step
-    rec[1] = L;
-  }
-  rec[2 + i] = A;
-  rec[2 + kD + i] = Sg;
 }
 
 template <int KB, int VB, bool KQJL, bool VQJL>
-size_t smem_bytes() {
-  return (size_t)Geo<KB, VB, KQJL, VQJL>::total;
-}
-
-template <int KB, int VB, bool KQJL, bool VQJL>
-int launch2(const Decode2Args &k, dim3 grid, cudaStream_t st) {
-  const size_t smem = smem_bytes<KB, VB, KQJL, VQJL>();
+int launch_split(const Decode2Args &k, dim3 grid, cudaStream_t st) {
+  using Gm = Geo<KB, VB, KQJL, VQJL, 4, 3>;
+  const size_t smem = Gm::sm_misc;
   auto fn = decode2_g1_kernel<KB, VB, KQJL, VQJL>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -544,52 +711,86 @@ int launch2(const Decode2Args &k, dim3 grid, cudaStream_t st) {
       return TQ_ERR_CUDA;
     attr_done = true;
   }
-  fn<<<grid, kWarps2 * 32, smem, st>>>(k);
+  fn<<<grid, 128, smem, st>>>(k);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+// persistent launch: as many CTAs as fit on the device at once (at most two per
+// SM, which the workspace's record count assumes); *ctas receives the grid size
+template <int KB, int VB, bool KQJL, bool VQJL>
+int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st) {
+  using Gm = Geo<KB, VB, KQJL, VQJL, 8, 4>;
+  const size_t smem = Gm::sm_misc + sizeof(int) * (2 * kMaxPersistBatch + 1);
+  auto fn = decode_persist_kernel<KB, VB, KQJL, VQJL>;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, smem) != cudaSuccess) return TQ_ERR_CUDA;
+    per_sm = std::max(1, std::min(2, n));
+  }
+  *ctas = per_sm * num_sms;
+  fn<<<*ctas, 256, smem, st>>>(k);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+template <int KB, int VB, bool KQJL, bool VQJL>
+int launch_variant(const Decode2Args &k, bool persist, int num_sms, int *ctas, cudaStream_t st) {
+  if (persist) return launch_persist<KB, VB, KQJL, VQJL>(k, num_sms, ctas, st);
+  *ctas = 0;
+  return launch_split<KB, VB, KQJL, VQJL>(k, dim3(k.splits, k.heads_kv, k.batch), st);
 }
 
 }  // namespace
 
 // Returns TQ_ERR_UNSUPPORTED when this path does not cover the request (the
-// caller then uses the general kernel).
-int launch_decode2_g1(const DecodeArgs &a, const float *qprep, float *partials, void *stream) {
+// caller then uses the general kernel). *persist_ctas receives the persistent
+// grid size, or 0 when the split-K kernel ran (partials laid out per split).
+int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
   const tq_ctx *ctx = a.ctx;
+  *persist_ctas = 0;
   if (a.heads_q != a.heads_kv) return TQ_ERR_UNSUPPORTED;
-  if (a.cache->capacity % 16) return TQ_ERR_UNSUPPORTED;  // TMA sources need 16-byte aligned rows
-  if (a.chunk % 4) return TQ_ERR_UNSUPPORTED;              // tile starts stay 16-byte aligned
+  // persistent: tiles start at multiples of 64 tokens, so 4-token aligned rows keep
+  // every TMA source 16-byte aligned; split-K: chunk starts as well
+  const bool persist = a.tile_prefix != nullptr && a.batch <= kMaxPersistBatch && a.cache->capacity % 4 == 0 &&
+                       ctx->num_sms > 0;
+  if (!persist && (a.cache->capacity % 16 || a.chunk % 4)) return TQ_ERR_UNSUPPORTED;
   const tq_cache *c = a.cache;
   Decode2Args k{};
   k.k_codes = c->k_codes; k.k_norm = c->k_norm; k.k_signs = c->k_signs; k.k_rnorm = c->k_rnorm;
   k.v_codes = c->v_codes; k.v_norm = c->v_norm; k.v_signs = c->v_signs; k.v_rnorm = c->v_rnorm;
   k.capacity = c->capacity;
+  k.batch = a.batch;
   k.heads_kv = a.heads_kv;
   k.heads_q = a.heads_q;
   k.chunk = a.chunk;
   k.splits = a.splits;
   k.seq_lens = a.seq_lens;
-  k.qprep = qprep;
-  k.partials = partials;
+  k.tile_prefix = a.tile_prefix;
+  k.qprep = a.qprep;
+  k.partials = a.partials;
   k.k_centroids = ctx->dparams->k_centroids;
   k.v_centroids = ctx->dparams->v_centroids;
   k.error = &ctx->dparams->error;
-  dim3 grid(a.splits, a.heads_kv, a.batch);
   cudaStream_t st = (cudaStream_t)stream;
-  const int kb = ctx->k.bits;
+  const int kb = ctx->k.bits, ns = ctx->num_sms;
+  int *pc = persist_ctas;
   switch (ctx->scheme) {
     case TQ_SCHEME_KV:
-      if (kb == 2) return launch2<2, 2, false, false>(k, grid, st);
-      if (kb == 3) return launch2<3, 3, false, false>(k, grid, st);
-      if (kb == 4) return launch2<4, 4, false, false>(k, grid, st);
+      if (kb == 2) return launch_variant<2, 2, false, false>(k, persist, ns, pc, st);
+      if (kb == 3) return launch_variant<3, 3, false, false>(k, persist, ns, pc, st);
+      if (kb == 4) return launch_variant<4, 4, false, false>(k, persist, ns, pc, st);
       break;
     case TQ_SCHEME_KQV:
-      if (kb == 2) return launch2<2, 1, false, true>(k, grid, st);
-      if (kb == 3) return launch2<3, 2, false, true>(k, grid, st);
-      if (kb == 4) return launch2<4, 3, false, true>(k, grid, st);
+      if (kb == 2) return launch_variant<2, 1, false, true>(k, persist, ns, pc, st);
+      if (kb == 3) return launch_variant<3, 2, false, true>(k, persist, ns, pc, st);
+      if (kb == 4) return launch_variant<4, 3, false, true>(k, persist, ns, pc, st);
       break;
     case TQ_SCHEME_QKQV:
-      if (kb == 1) return launch2<1, 1, true, true>(k, grid, st);
-      if (kb == 2) return launch2<2, 2, true, true>(k, grid, st);
-      if (kb == 3) return launch2<3, 3, true, true>(k, grid, st);
+      if (kb == 1) return launch_variant<1, 1, true, true>(k, persist, ns, pc, st);
+      if (kb == 2) return launch_variant<2, 2, true, true>(k, persist, ns, pc, st);
+      if (kb == 3) return launch_variant<3, 3, true, true>(k, persist, ns, pc, st);
       break;
     default: break;
   }

@@ -301,6 +301,7 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
   hp->error = 0;
 
   cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (e == cudaSuccess) e = cudaMalloc((void **)&c->dparams, sizeof(tq::DevParams));
   if (e == cudaSuccess) e = cudaMemcpy(c->dparams, hp, sizeof(tq::DevParams), cudaMemcpyHostToDevice);
   std::free(hp);
@@ -461,9 +462,14 @@ tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads
     return TQ_ERR_ARG;
   int s, chunk;
   tq::choose_splits(batch, heads_kv, max_len, splits, &s, &chunk);
+  // prepared queries | decode-tile prefix over batches | partial records (split-K
+  // per (row, split), or the persistent kernel's 2 per (CTA + head) slot)
   size_t qprep = (size_t)batch * heads_q * 2 * ctx->d * sizeof(float);
-  size_t parts = (size_t)batch * heads_q * s * tq::kPartialFloats * sizeof(float);
-  *out = qprep + parts;
+  size_t prefix = ((size_t)(batch + 1) * sizeof(int32_t) + 15) / 16 * 16;
+  size_t split_parts = (size_t)batch * heads_q * s * tq::kPartialFloats * sizeof(float);
+  size_t persist_parts = (size_t)2 * (2 * (size_t)ctx->num_sms + (size_t)batch * heads_kv) * tq::kPartialFloats *
+                         sizeof(float);
+  *out = qprep + prefix + std::max(split_parts, persist_parts);
   return TQ_OK;
 }
 
@@ -494,7 +500,8 @@ tq_status tq_decode_attention(const tq_ctx *ctx, const tq_cache *cache, const vo
   tq::choose_splits(batch, heads_kv, max_len, splits, &a.splits, &a.chunk);
   a.seq_lens = d_seq_lens;
   a.qprep = (float *)d_workspace;
-  a.partials = a.qprep + (size_t)batch * heads_q * 2 * ctx->d;
+  a.tile_prefix = (int32_t *)(a.qprep + (size_t)batch * heads_q * 2 * ctx->d);
+  a.partials = (float *)((char *)a.tile_prefix + ((size_t)(batch + 1) * sizeof(int32_t) + 15) / 16 * 16);
   a.out = d_out;
   if (ctx->scheme == TQ_SCHEME_KIVI) return (tq_status)tq::launch_decode_kivi(a, stream);
   return (tq_status)tq::launch_decode_tq(a, stream);

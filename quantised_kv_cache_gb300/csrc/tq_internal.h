@@ -13,6 +13,7 @@ constexpr int kD = 128;          // the head dimension this build implements
 constexpr int kMaxLevels = 16;   // 4-bit codebooks at most
 constexpr int kMaxGroup = 8;     // query heads per KV head handled by one CTA
 constexpr int kPartialFloats = 260;  // m, l, acc[128], sign_acc[128], 2 pad
+constexpr int kDecodeTile = 64;      // tokens per tile of the TMA decode kernels
 
 // Device-resident parameter block of a context (one cudaMalloc).
 struct DevParams {
@@ -40,6 +41,7 @@ struct tq_ctx {
   int scheme = 0;
   uint64_t seed = 0;
   int device = 0;
+  int num_sms = 0;  // of `device`
   tq::Role k, v;
   // KIVI options
   int kivi_group = 32;
@@ -90,13 +92,15 @@ struct DecodeArgs {
   int batch, heads_q, heads_kv, max_len, splits, chunk;
   const int32_t *seq_lens;
   float *qprep;     // [batch][heads_q][2][d]
-  float *partials;  // [batch][heads_q][splits][kPartialFloats]
+  int32_t *tile_prefix;  // [batch + 1] decode tiles before each batch (computed by the query prep)
+  float *partials;  // split-K: [batch][heads_q][splits][kPartialFloats]; persistent: [ctas + units][2][...]
   float *out;
 };
 int launch_decode_tq(const DecodeArgs &a, void *stream);
 // TMA-staged, tensor-core decode for one query head per KV head; returns
 // TQ_ERR_UNSUPPORTED when the request falls outside what it covers.
-int launch_decode2_g1(const DecodeArgs &a, const float *qprep, float *partials, void *stream);
+// *persist_ctas receives the persistent grid size, or 0 when the split-K kernel ran.
+int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream);
 int launch_decode_kivi(const DecodeArgs &a, void *stream);
 
 struct DequantArgs {

@@ -197,3 +197,55 @@ def test_decode_argument_errors():
     with pytest.raises(tq.TQError) as e:
         tq.tq_decode_attention(ctx.handle, cache, q, seq, max_len=4, workspace=ws)
     assert e.value.status == tq.TQ_ERR_WORKSPACE
+
+
+def _decode_case(scheme, n, B, H, lens, seed, cap=None):
+    N = max(max(lens), 1)
+    w = wl.Workload(97, "test", B, H, H, N, torch.bfloat16, scheme, n, key_scale_sigma=1.0)
+    q, k, v = wl.generate(w, "cpu", seed=seed)
+    ctx = tq.Context(128, n, scheme, 1000 + seed)
+    cache = tq.Cache(ctx, B, H, cap or N)
+    _append(ctx, cache, k, v, 0)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    out = tq.tq_decode_attention(ctx.handle, cache, q.to(DEV), seq, max_len=N)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    return ctx, cache, q, out.cpu().numpy()
+
+
+@pytest.mark.parametrize("scheme,n", [("KQV", 4), ("QKQV", 3), ("KV", 2)])
+def test_decode_ragged_lengths_with_empty_sequences(scheme, n):
+    # lengths around the 64-token tile: most of the persistent grid's slices are empty
+    lens = [0, 1, 64, 65, 700]
+    B, H = len(lens), 3
+    ctx, cache, q, got = _decode_case(scheme, n, B, H, lens, seed=41)
+    params = otq.make_params(128, n, scheme, 1041)
+    full = P.oracle_decode_from_cache(cache, params, q.float().numpy(), [max(x, 1) for x in lens], B, H, H)
+    for b in range(B):
+        for h in range(H):
+            if lens[b] == 0:
+                assert np.all(got[b, h] == 0.0)
+            else:
+                assert P.rel_l2(got[b, h], full[b, h]) < 1e-3, (b, h)
+
+
+def test_decode_heads_spanning_several_slices():
+    # 2 x 2 heads x 79 tiles: more tiles than persistent CTAs, so slices cross heads and
+    # heads cross slices
+    lens = [5000, 4999]
+    ctx, cache, q, got = _decode_case("KQV", 4, 2, 2, lens, seed=43)
+    want = P.oracle_decode_from_cache(cache, otq.make_params(128, 4, "KQV", 1043), q.float().numpy(), lens, 2, 2, 2)
+    for b in range(2):
+        for h in range(2):
+            assert P.rel_l2(got[b, h], want[b, h]) < 1e-3, (b, h)
+
+
+def test_decode_large_batch_uses_split_kernel():
+    # batches above the persistent kernel's prefix-table size take the split-K kernel
+    B, H, N = 260, 1, 48
+    lens = [N - (b % 7) for b in range(B)]
+    ctx, cache, q, got = _decode_case("KQV", 4, B, H, lens, seed=47, cap=64)
+    params = otq.make_params(128, 4, "KQV", 1047)
+    want = P.oracle_decode_from_cache(cache, params, q.float().numpy(), lens, B, H, H)
+    for b in [0, 1, 100, 259]:
+        assert P.rel_l2(got[b, 0], want[b, 0]) < 1e-3, b
