@@ -208,7 +208,7 @@ tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const voi
 
 /* Workspace bytes tq_decode_attention needs for these sizes: the prepared
  * queries, a per-batch tile prefix, and the partial softmax records (per
- * split for the split-K kernels, or two per (CTA + head) slot for the
+ * split for the split-K kernels, or four per (CTA + head) slot for the
  * persistent kernel, whichever is larger). splits = 0 asks for the library's
  * choice for max_len. */
 tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len,

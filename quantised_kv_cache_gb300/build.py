@@ -35,7 +35,7 @@ def nvcc_path() -> str:
 
 
 def _flags():
-    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
+    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr", "-diag-suppress=177",
                    "-I", os.path.join(ROOT, "include")]
 
 

@@ -333,10 +333,10 @@ struct CombineArgs {
   const float *diag;
   const float *sketch;
   float *out;
-  // persistent layout (tile_prefix != nullptr): records [(cta + unit) * 2 + group],
+  // persistent layout (tile_prefix != nullptr): records [(cta + unit) * groups + group],
   // one query head per KV head
   const int32_t *tile_prefix;
-  int persist_ctas, heads_kv;
+  int persist_ctas, heads_kv, persist_groups;
 };
 
 // one CTA (128 threads, thread = coordinate) per (batch, query head)
@@ -347,26 +347,31 @@ __global__ void __launch_bounds__(128) combine_tq_kernel(CombineArgs a) {
   // the partial records of this row: split-K ones in a row, or the persistent
   // kernel's (cta, group) records of every CTA whose slice touched this head
   const float *base = a.partials + (size_t)row * a.splits * kPartialFloats;
-  long long T = 0, C = 1, c_lo = 0, c_hi = -1;
+  // persistent slices: CTA c holds tiles [bnd(c), bnd(c + 1)), bnd(c) = min(T, 4 floor(T4 c / C))
+  long long T = 0, T4 = 1, C = 1, c_lo = 0, c_hi = -1;
   int unit = 0;
+  auto bnd = [&](long long c) -> long long { return min(T, 4 * (T4 * c / C)); };
   if (a.tile_prefix) {
     const int b = row / a.heads_q, h = row % a.heads_q;
     const int p0 = __ldg(a.tile_prefix + b), nb = __ldg(a.tile_prefix + b + 1) - p0;
     T = (long long)a.heads_kv * __ldg(a.tile_prefix + a.batch);
+    T4 = (T + 3) / 4;
     C = a.persist_ctas;
     unit = b * a.heads_kv + h;
     if (nb > 0) {
       const long long us = (long long)a.heads_kv * p0 + (long long)h * nb, ue = us + nb;
-      c_lo = ((us + 1) * C - 1) / T;  // the CTA whose slice [T c / C, T (c+1) / C) holds tile us
-      c_hi = (ue * C - 1) / T;
+      // the CTA holding tile g: the largest c with bnd(c) <= g
+      c_lo = ((us / 4 + 1) * C - 1) / T4;
+      c_hi = (((ue - 1) / 4 + 1) * C - 1) / T4;
     }
   }
-  const int nrec = a.tile_prefix ? (int)(2 * (c_hi - c_lo + 1)) : a.splits;
+  const int ng = a.persist_groups;
+  const int nrec = a.tile_prefix ? (int)(ng * (c_hi - c_lo + 1)) : a.splits;
   auto record = [&](int k) -> const float * {
     if (!a.tile_prefix) return base + (size_t)k * kPartialFloats;
-    const long long c = c_lo + k / 2;
-    if (T * c / C == T * (c + 1) / C) return nullptr;  // an empty slice wrote nothing
-    return a.partials + ((size_t)(c + unit) * 2 + (k & 1)) * kPartialFloats;
+    const long long c = c_lo + k / ng;
+    if (bnd(c) == bnd(c + 1)) return nullptr;  // an empty slice wrote nothing
+    return a.partials + ((size_t)(c + unit) * ng + (k % ng)) * kPartialFloats;
   };
   float M = -INFINITY;
   for (int k = 0; k < nrec; ++k) {
@@ -635,7 +640,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
     if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
     CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                     ctx->dparams->diag, ctx->dparams->sketch, a.out,
-                    persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv};
+                    persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv, kPersistGroups};
     combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
   }
@@ -682,7 +687,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   if (r != TQ_OK) return r;
 
   CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
-                  ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv};
+                  ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv, 1};
   combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
@@ -722,7 +727,7 @@ int launch_decode_kivi(const DecodeArgs &a, void *stream) {
   if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
   if (r != TQ_OK) return r;
   CombineArgs cmb{a.batch, a.heads_q, a.splits, 0, 0, a.partials, ctx->dparams->diag, ctx->dparams->sketch, a.out,
-                  nullptr, 0, a.heads_kv};
+                  nullptr, 0, a.heads_kv, 1};
   combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

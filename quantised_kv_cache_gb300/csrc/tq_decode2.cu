@@ -1,12 +1,13 @@
 // Decode attention over the packed cache, one query head per KV head, as two
 // kernels that share one tile body:
 //
-// * decode_persist_kernel -- persistent: two CTAs of 8 warps per SM walk
+// * decode_persist_kernel -- persistent: one CTA of 16 warps per SM walks
 //   contiguous slices of the flattened (batch, kv head, 64-token tile) space,
 //   so every SM gets the same number of tiles whatever the sequence lengths;
 //   key tables are rebuilt only where a slice crosses into the next head, and
-//   the TMA ring keeps streaming across that boundary. Each 4-warp group
-//   writes one partial softmax record per (CTA, head) segment.
+//   the TMA ring (up to 16 stages, ~140 KB in flight) keeps streaming across
+//   that boundary. Each 4-warp group writes one partial softmax record per
+//   (CTA, head) segment.
 // * decode2_g1_kernel -- split-K over a fixed (batch, head, chunk) grid, for
 //   batches too large for the persistent kernel's shared-memory prefix table.
 //
@@ -73,16 +74,26 @@ struct Geo {
   static constexpr int vval = 1 << (2 * VB);               // values of one value pair field
   static constexpr int vlut = vval * 32;                   // half2 words, replicated per lane
   // shared-memory offsets (bytes from the dynamic base): value table first
+  static constexpr int ktab_region = (ktab > NW * kPartialFloats) ? ktab : NW * kPartialFloats;
   static constexpr int sm_ktab = vlut * 4;
-  static constexpr int sm_stab = sm_ktab + ktab * 4;
+  static constexpr int sm_stab = sm_ktab + ktab_region * 4;
   static constexpr int sm_stage = sm_stab + stab * 4;
   static constexpr int sm_bar = sm_stage + S * stage;
   static constexpr int sm_cnt = sm_bar + S * 8;
   static constexpr int sm_q = sm_cnt + 16 * ((S * 4 + 15) / 16);   // [2][128] floats
   static constexpr int sm_misc = sm_q + 2 * kD * 4;
   // per-warp partial states are parked in the key-table area at a flush
-  static_assert(NW * kPartialFloats <= ktab, "flush area must fit in the key table");
 };
+
+// stages of the persistent kernel's ring: as many as fit next to the tables in
+// 227 KB, a multiple of the 4 warp groups, at most 16
+template <int KB, int VB, bool KQJL, bool VQJL>
+constexpr int persist_stages() {
+  using G1 = Geo<KB, VB, KQJL, VQJL, 16, 1>;
+  constexpr int fixed = G1::sm_stage + 16 * 8 + 16 * 4 + 2 * kD * 4 + 4 * (2 * 256 + 1) + 4 * kMaxLevels + 64;
+  constexpr int n = (227 * 1024 - fixed) / G1::stage;
+  return (n >= 16) ? 16 : (n / 4) * 4;
+}
 
 struct Decode2Args {
   const uint8_t *k_codes;
@@ -126,16 +137,18 @@ __device__ __forceinline__ void build_lookup(float *T, const float *q, const flo
   constexpr int CPP = VBITS / CB;
   constexpr int LOB = (VBITS >= 8) ? 4 : 3;  // low-part bits (a whole number of codes)
   constexpr int HIB = VBITS - LOB;
-  constexpr int NLO = 1 << LOB, PARTS = NT / KPOS, NH = (1 << HIB) / PARTS;
-  static_assert(NH >= 1 && PARTS * KPOS == NT, "table build split");
+  constexpr int NLO = 1 << LOB;
+  constexpr int PARTS = (NT / KPOS < (1 << HIB)) ? NT / KPOS : (1 << HIB), NH = (1 << HIB) / PARTS;
+  static_assert(NH * PARTS == (1 << HIB) && PARTS * KPOS <= NT, "table build split");
   constexpr int M = (1 << CB) - 1;
+  if (tid >= PARTS * KPOS) return;
   const int pos = tid % KPOS, part = tid / KPOS;
   float qv[CPP];
 #pragma unroll
   for (int j = 0; j < CPP; ++j) qv[j] = q[slot_coord(pos * CPP + j)] * scale;
   float cb[M + 1];
 #pragma unroll
-  for (int c = 0; c <= M; ++c) cb[c] = SIGN ? (c ? 1.f : -1.f) : __ldg(cb_g + c);
+  for (int c = 0; c <= M; ++c) cb[c] = SIGN ? (c ? 1.f : -1.f) : cb_g[c];
   float lo[NLO];
 #pragma unroll
   for (int x = 0; x < NLO; ++x) {
@@ -151,7 +164,7 @@ __device__ __forceinline__ void build_lookup(float *T, const float *q, const flo
 #pragma unroll
     for (int j = 0; j < HIB / CB; ++j) {
       const int c = (y >> (CB * j)) & M;
-      hi = fmaf(qv[LOB / CB + j], SIGN ? (c ? 1.f : -1.f) : __ldg(cb_g + c), hi);
+      hi = fmaf(qv[LOB / CB + j], SIGN ? (c ? 1.f : -1.f) : cb_g[c], hi);
     }
 #pragma unroll
     for (int x = 0; x < NLO; ++x) T[((y << LOB) | x) * KPOS + pos] = lo[x] + hi;
@@ -166,17 +179,22 @@ __device__ __forceinline__ float sign_unscale(int L) {
   return L == 10 ? 16384.f : (L == 11 ? 8192.f : (L == 12 ? 2048.f : (L == 13 ? 128.f : 0.5f)));
 }
 
-// Key tables (with log2(e)) and the value pair table for one query head.
-template <int KB, int VB, bool KQJL, int NT>
-__device__ __forceinline__ void build_tables(unsigned char *smem, int sm_ktab, int sm_stab, int vlut_words,
-                                             const float *s_q, const float *k_centroids, const float *v_centroids,
-                                             int tid) {
+// Key tables (with log2(e)) for one query head; `kc` may point to shared memory.
+template <int KB, bool KQJL, int NT>
+__device__ __forceinline__ void build_key_tables(unsigned char *smem, int sm_ktab, int sm_stab, const float *s_q,
+                                                 const float *kc, int tid) {
   float *s_ktab = reinterpret_cast<float *>(smem + sm_ktab);
-  if constexpr (KB == 3) build_lookup<3, 64, 6, false, NT>(s_ktab, s_q, k_centroids, kLog2e, tid);
-  else build_lookup<KB, 16 * KB, 8, false, NT>(s_ktab, s_q, k_centroids, kLog2e, tid);
+  if constexpr (KB == 3) build_lookup<3, 64, 6, false, NT>(s_ktab, s_q, kc, kLog2e, tid);
+  else build_lookup<KB, 16 * KB, 8, false, NT>(s_ktab, s_q, kc, kLog2e, tid);
   if constexpr (KQJL)
     build_lookup<1, 16, 8, true, NT>(reinterpret_cast<float *>(smem + sm_stab), s_q + kD, nullptr, kLog2e, tid);
-  // value pair table: field f -> half2(c[f & mask], c[f >> VB]), replicated for every lane
+}
+
+// Value pair table (head-independent): field f -> half2(c[f & mask], c[f >> VB]),
+// replicated for every lane, at offset 0 of shared memory.
+template <int VB, int NT>
+__device__ __forceinline__ void build_value_table(unsigned char *smem, int vlut_words, const float *v_centroids,
+                                                  int tid) {
   uint32_t *vl = reinterpret_cast<uint32_t *>(smem);
   for (int e = tid; e < vlut_words; e += NT) {
     const int f = e >> 5;
@@ -545,8 +563,8 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
   s_q[tid] = __ldg(qp + tid);
   if (KQJL) s_q[kD + tid] = __ldg(qp + kD + tid);
   __syncthreads();
-  build_tables<KB, VB, KQJL, 128>(smem, Gm::sm_ktab, Gm::sm_stab, Gm::vlut, s_q, a.k_centroids, a.v_centroids,
-                                  tid);
+  build_key_tables<KB, KQJL, 128>(smem, Gm::sm_ktab, Gm::sm_stab, s_q, a.k_centroids, tid);
+  build_value_table<VB, 128>(smem, Gm::vlut, a.v_centroids, tid);
   __syncthreads();
 
   const LaneConsts<KB> lc(lane);
@@ -587,13 +605,17 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
 }
 
 // ============================================================================
-// persistent kernel: two CTAs of 8 warps per SM; warp group grp (4 warps)
-// takes the CTA's tiles of local parity grp
+// persistent kernel: one CTA of 16 warps per SM; warp group grp (4 warps)
+// takes the CTA's tiles of local index = grp (mod 4), and owns the ring stages
+// s = grp (mod 4), so each group has its next three tiles in flight
 // ============================================================================
+constexpr int kPersistWarps = 16;  // four groups of four (kPersistGroups)
+
 template <int KB, int VB, bool KQJL, bool VQJL>
-__global__ void __launch_bounds__(256, 2) decode_persist_kernel(Decode2Args a) {
-  using Gm = Geo<KB, VB, KQJL, VQJL, 8, 4>;
-  constexpr int S = Gm::kStages;
+__global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(Decode2Args a) {
+  constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
+  static_assert(S >= 8 && S % kPersistGroups == 0, "ring stages");
+  using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *s_stage = smem + Gm::sm_stage;
   uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Gm::sm_bar);
@@ -601,9 +623,12 @@ __global__ void __launch_bounds__(256, 2) decode_persist_kernel(Decode2Args a) {
   float *s_q = reinterpret_cast<float *>(smem + Gm::sm_q);
   int *s_pre = reinterpret_cast<int *>(smem + Gm::sm_misc);  // [batch + 1] tile prefix
   int *s_len = s_pre + kMaxPersistBatch + 1;                  // [batch] clamped lengths
+  float *s_kc = reinterpret_cast<float *>(s_len + kMaxPersistBatch);  // [16] key centroids
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, grp = warp >> 2;
   const int B = a.batch, H = a.heads_kv;
+  if (tid < kMaxLevels) s_kc[tid] = __ldg(a.k_centroids + tid);
+  build_value_table<VB, kPersistWarps * 32>(smem, Gm::vlut, a.v_centroids, tid);
   for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
   for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
   if (tid == 0) {
@@ -614,9 +639,12 @@ __global__ void __launch_bounds__(256, 2) decode_persist_kernel(Decode2Args a) {
     mbar_fence_init();
   }
   __syncthreads();
+  // slice of CTA c: [b(c), b(c + 1)) with b(c) = min(T, 4 floor(ceil(T / 4) c / C)), so
+  // slices (and, when heads hold multiples of 4 tiles, head segments) split evenly
+  // over the four warp groups
   const long long T = (long long)H * s_pre[B];
-  const long long C = gridDim.x, c = blockIdx.x;
-  const long long g0 = T * c / C, g1 = T * (c + 1) / C;
+  const long long C = gridDim.x, c = blockIdx.x, T4 = (T + 3) / 4;
+  const long long g0 = min(T, 4 * (T4 * c / C)), g1 = min(T, 4 * (T4 * (c + 1) / C));
   if (g0 >= g1) return;  // whole CTA: nothing to do (no record is read for it)
 
   // batch of global tile g: the largest b with H * pre[b] <= g
@@ -646,6 +674,14 @@ __global__ void __launch_bounds__(256, 2) decode_persist_kernel(Decode2Args a) {
   WarpState ws;
   bool bad = false;
   float *park = reinterpret_cast<float *>(smem + Gm::sm_ktab);
+  // query row (= unit: one query head per KV head) of the segment starting at tile g
+  auto unit_of = [&](long long g) -> int {
+    const int bb = batch_of(g);
+    const int nb = s_pre[bb + 1] - s_pre[bb];
+    return bb * H + (int)((g - (long long)H * s_pre[bb]) / nb);
+  };
+  if (tid < 2 * kD) s_q[tid] = __ldg(a.qprep + (size_t)unit_of(g0) * 2 * kD + tid);
+  __syncthreads();
   long long g = g0;
   while (g < g1) {  // one segment per (batch, kv head) the slice touches
     const int bb = batch_of(g);
@@ -657,18 +693,18 @@ __global__ void __launch_bounds__(256, 2) decode_persist_kernel(Decode2Args a) {
     const int len = s_len[bb];
     const int u = bb * H + h;
 
-    // query and tables for this head (the previous segment's readers are done)
-    const float *qp = a.qprep + (size_t)u * 2 * kD;  // one query head per KV head: row u
-    s_q[tid] = __ldg(qp + tid);
+    // key tables for this head (s_q holds its query; the previous segment's
+    // readers of the table area passed the barrier that closed its flush)
+    build_key_tables<KB, KQJL, kPersistWarps * 32>(smem, Gm::sm_ktab, Gm::sm_stab, s_q, s_kc, tid);
     __syncthreads();
-    build_tables<KB, VB, KQJL, 256>(smem, Gm::sm_ktab, Gm::sm_stab, Gm::vlut, s_q, a.k_centroids, a.v_centroids,
-                                    tid);
-    __syncthreads();
+    // the next segment's query, fetched while this one streams
+    float q_next = 0.f;
+    if (se < g1 && tid < 2 * kD) q_next = __ldg(a.qprep + (size_t)unit_of(se) * 2 * kD + tid);
 
     ws.reset();
-    // this group's tiles: local index i = t - g0 with i % 2 == grp
-    long long t = g + (((g - g0) & 1) != grp ? 1 : 0);
-    for (; t < se; t += 2) {
+    // this group's tiles: local index i = t - g0 with i % 4 == grp
+    long long t = g + ((grp - (int)((g - g0) & 3)) & 3);
+    for (; t < se; t += kPersistGroups) {
       const long long i = t - g0;
       const int stage = (int)(i % S);
       if (!bad && !mbar_wait_bounded(&s_full[stage], (uint32_t)((i / S) & 1), a.error)) bad = true;
@@ -689,12 +725,13 @@ __global__ void __launch_bounds__(256, 2) decode_persist_kernel(Decode2Args a) {
       }
     }
 
-    // flush: both groups are done with this head; park the warps in the table area
+    // flush: every group is done with this head; park the warps in the table area
     __syncthreads();
     park_warp<VQJL>(park + warp * kPartialFloats, lane, ws);
     __syncthreads();
+    if (tid < 2 * kD) s_q[tid] = q_next;
     merge_parked<4, VQJL>(park + grp * 4 * kPartialFloats, tid & 127,
-                          a.partials + ((size_t)(c + u) * 2 + grp) * kPartialFloats);
+                          a.partials + ((size_t)(c + u) * kPersistGroups + grp) * kPartialFloats);
     __syncthreads();  // the table area is rebuilt next
     g = se;
   }
@@ -715,23 +752,21 @@ int launch_split(const Decode2Args &k, dim3 grid, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
-// persistent launch: as many CTAs as fit on the device at once (at most two per
-// SM, which the workspace's record count assumes); *ctas receives the grid size
+// persistent launch: one CTA per SM (the workspace's record count assumes no more)
 template <int KB, int VB, bool KQJL, bool VQJL>
 int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st) {
-  using Gm = Geo<KB, VB, KQJL, VQJL, 8, 4>;
-  const size_t smem = Gm::sm_misc + sizeof(int) * (2 * kMaxPersistBatch + 1);
+  constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
+  using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
+  const size_t smem = Gm::sm_misc + sizeof(int) * (2 * kMaxPersistBatch + 1) + sizeof(float) * kMaxLevels;
   auto fn = decode_persist_kernel<KB, VB, KQJL, VQJL>;
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static bool attr_done = false;
+  if (!attr_done) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, smem) != cudaSuccess) return TQ_ERR_CUDA;
-    per_sm = std::max(1, std::min(2, n));
+    attr_done = true;
   }
-  *ctas = per_sm * num_sms;
-  fn<<<*ctas, 256, smem, st>>>(k);
+  *ctas = num_sms;
+  fn<<<*ctas, kPersistWarps * 32, smem, st>>>(k);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

@@ -14,6 +14,7 @@ constexpr int kMaxLevels = 16;   // 4-bit codebooks at most
 constexpr int kMaxGroup = 8;     // query heads per KV head handled by one CTA
 constexpr int kPartialFloats = 260;  // m, l, acc[128], sign_acc[128], 2 pad
 constexpr int kDecodeTile = 64;      // tokens per tile of the TMA decode kernels
+constexpr int kPersistGroups = 4;    // partial records per (CTA, head) of the persistent decode (one CTA per SM)
 
 // Device-resident parameter block of a context (one cudaMalloc).
 struct DevParams {
@@ -93,7 +94,7 @@ struct DecodeArgs {
   const int32_t *seq_lens;
   float *qprep;     // [batch][heads_q][2][d]
   int32_t *tile_prefix;  // [batch + 1] decode tiles before each batch (computed by the query prep)
-  float *partials;  // split-K: [batch][heads_q][splits][kPartialFloats]; persistent: [ctas + units][2][...]
+  float *partials;  // split-K: [batch][heads_q][splits][kPartialFloats]; persistent: [ctas + units][kPersistGroups][...]
   float *out;
 };
 int launch_decode_tq(const DecodeArgs &a, void *stream);
