@@ -6,7 +6,8 @@
 //   so every SM gets the same number of tiles whatever the sequence lengths;
 //   key tables are rebuilt only where a slice crosses into the next head, and
 //   the TMA ring (up to 16 stages, ~140 KB in flight) keeps streaming across
-//   that boundary. Each 4-warp group writes one partial softmax record per
+//   that boundary: each warp streams and refills its own quarter of a stage on
+//   its own mbarrier. Each 4-warp group writes one partial softmax record per
 //   (CTA, head) segment.
 // * decode2_g1_kernel -- split-K over a fixed (batch, head, chunk) grid, for
 //   batches too large for the persistent kernel's shared-memory prefix table.
@@ -79,7 +80,7 @@ struct Geo {
   static constexpr int sm_stab = sm_ktab + ktab_region * 4;
   static constexpr int sm_stage = sm_stab + stab * 4;
   static constexpr int sm_bar = sm_stage + S * stage;
-  static constexpr int sm_cnt = sm_bar + S * 8;
+  static constexpr int sm_cnt = sm_bar + S * 4 * 8;                 // (persistent: 4 barriers per stage)
   static constexpr int sm_q = sm_cnt + 16 * ((S * 4 + 15) / 16);   // [2][128] floats
   static constexpr int sm_misc = sm_q + 2 * kD * 4;
   // per-warp partial states are parked in the key-table area at a flush
@@ -90,7 +91,7 @@ struct Geo {
 template <int KB, int VB, bool KQJL, bool VQJL>
 constexpr int persist_stages() {
   using G1 = Geo<KB, VB, KQJL, VQJL, 16, 1>;
-  constexpr int fixed = G1::sm_stage + 16 * 8 + 16 * 4 + 2 * kD * 4 + 4 * (2 * 256 + 1) + 4 * kMaxLevels + 64;
+  constexpr int fixed = G1::sm_stage + 16 * 4 * 8 + 16 * 4 + 2 * kD * 4 + 4 * (2 * 256 + 1) + 4 * kMaxLevels + 64;
   constexpr int n = (227 * 1024 - fixed) / G1::stage;
   return (n >= 16) ? 16 : (n / 4) * 4;
 }
@@ -606,10 +607,41 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
 
 // ============================================================================
 // persistent kernel: one CTA of 16 warps per SM; warp group grp (4 warps)
-// takes the CTA's tiles of local index = grp (mod 4), and owns the ring stages
-// s = grp (mod 4), so each group has its next three tiles in flight
+// takes the CTA's tiles of local index = grp (mod 4), which live in the ring
+// stages s = grp (mod 4). Each warp streams only its own 16-token quarter of
+// a tile, on its own mbarrier, and refills that quarter as soon as it is done
+// with it -- no warp ever waits for another inside a head.
 // ============================================================================
 constexpr int kPersistWarps = 16;  // four groups of four (kPersistGroups)
+
+// TMA of one warp's quarter (tokens t0 .. t0 + n - 1, n <= 16, of slot row s0) into
+// stage `st`, quarter q; n <= 0 completes the barrier phase with no copy
+template <typename Gm, bool KQJL, bool VQJL>
+__device__ __forceinline__ void issue_quarter(unsigned char *st, uint64_t *bar, const Decode2Args &a, size_t s0,
+                                              int q, int n) {
+  if (n <= 0) {
+    mbar_arrive_expect_tx(bar, 0);
+    return;
+  }
+  const int n4 = (n + 3) & ~3;  // norms in 16-byte units
+  uint32_t bytes = n * Gm::kc + n4 * 4 + n * Gm::vc + n4 * 4;
+  if (KQJL) bytes += n * 16 + n4 * 4;
+  if (VQJL) bytes += n * 16 + n4 * 4;
+  mbar_arrive_expect_tx(bar, bytes);
+  const int o = 16 * q;  // first token of the quarter within the tile
+  tma_load_1d(st + Gm::off_kc + o * Gm::kc, a.k_codes + s0 * Gm::kc, n * Gm::kc, bar);
+  tma_load_1d(st + Gm::off_kn + o * 4, a.k_norm + s0, n4 * 4, bar);
+  if (KQJL) {
+    tma_load_1d(st + Gm::off_ks + o * 16, a.k_signs + s0 * 16, n * 16, bar);
+    tma_load_1d(st + Gm::off_kr + o * 4, a.k_rnorm + s0, n4 * 4, bar);
+  }
+  tma_load_1d(st + Gm::off_vc + o * Gm::vc, a.v_codes + s0 * Gm::vc, n * Gm::vc, bar);
+  tma_load_1d(st + Gm::off_vn + o * 4, a.v_norm + s0, n4 * 4, bar);
+  if (VQJL) {
+    tma_load_1d(st + Gm::off_vs + o * 16, a.v_signs + s0 * 16, n * 16, bar);
+    tma_load_1d(st + Gm::off_vr + o * 4, a.v_rnorm + s0, n4 * 4, bar);
+  }
+}
 
 template <int KB, int VB, bool KQJL, bool VQJL>
 __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(Decode2Args a) {
@@ -618,78 +650,90 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
   using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *s_stage = smem + Gm::sm_stage;
-  uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Gm::sm_bar);
-  unsigned *s_cnt = reinterpret_cast<unsigned *>(smem + Gm::sm_cnt);
+  uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Gm::sm_bar);  // [S][4 quarters]
   float *s_q = reinterpret_cast<float *>(smem + Gm::sm_q);
   int *s_pre = reinterpret_cast<int *>(smem + Gm::sm_misc);  // [batch + 1] tile prefix
   int *s_len = s_pre + kMaxPersistBatch + 1;                  // [batch] clamped lengths
   float *s_kc = reinterpret_cast<float *>(s_len + kMaxPersistBatch);  // [16] key centroids
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, grp = warp >> 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, grp = warp >> 2, qtr = warp & 3;
   const int B = a.batch, H = a.heads_kv;
   if (tid < kMaxLevels) s_kc[tid] = __ldg(a.k_centroids + tid);
   build_value_table<VB, kPersistWarps * 32>(smem, Gm::vlut, a.v_centroids, tid);
   for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
   for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&s_full[s], 1);
-      s_cnt[s] = 0;
-    }
-    mbar_fence_init();
-  }
+  if (tid < S * 4) mbar_init(&s_full[tid], 1);
+  mbar_fence_init();
   __syncthreads();
   // slice of CTA c: [b(c), b(c + 1)) with b(c) = min(T, 4 floor(ceil(T / 4) c / C)), so
   // slices (and, when heads hold multiples of 4 tiles, head segments) split evenly
   // over the four warp groups
   const long long T = (long long)H * s_pre[B];
   const long long C = gridDim.x, c = blockIdx.x, T4 = (T + 3) / 4;
-  const long long g0 = min(T, 4 * (T4 * c / C)), g1 = min(T, 4 * (T4 * (c + 1) / C));
+  const int g0 = (int)min(T, 4 * (T4 * c / C)), g1 = (int)min(T, 4 * (T4 * (c + 1) / C));
   if (g0 >= g1) return;  // whole CTA: nothing to do (no record is read for it)
+  const int nloc = g1 - g0;
 
   // batch of global tile g: the largest b with H * pre[b] <= g
-  auto batch_of = [&](long long g) -> int {
+  auto batch_of = [&](int g) -> int {
     int lo = 0, hi = B;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if ((long long)H * s_pre[mid] <= g) lo = mid;
+      if (H * s_pre[mid] <= g) lo = mid;
       else hi = mid;
     }
     return lo;
   };
-  auto issue = [&](long long i) {  // local tile i -> stage i % S
-    const long long g = g0 + i;
-    const int bb = batch_of(g);
-    const int nb = s_pre[bb + 1] - s_pre[bb];
-    const long long r = g - (long long)H * s_pre[bb];
-    const int h = (int)(r / nb), tt = (int)(r % nb);
-    const int t0 = tt * kTT;
-    issue_tile_to<Gm, KQJL, VQJL>(s_stage + (i % S) * Gm::stage, &s_full[i % S], a,
-                                  ((size_t)bb * H + h) * a.capacity + t0, min(kTT, s_len[bb] - t0));
+
+  // refill cursor of this warp (lane 0): the (batch, head, tile) of local tile i_next
+  int cur_i = grp, cur_b = 0, cur_h = 0, cur_t = 0;
+  if (cur_i < nloc) {
+    const int g = g0 + cur_i;
+    cur_b = batch_of(g);
+    const int nb = s_pre[cur_b + 1] - s_pre[cur_b], r = g - H * s_pre[cur_b];
+    cur_h = r / nb;
+    cur_t = r - cur_h * nb;
+  }
+  auto issue_next = [&]() {  // issue this warp's quarter of local tile cur_i, then step the cursor by 4
+    const int st = cur_i % S;
+    const int t0 = cur_t * kTT + 16 * qtr;
+    issue_quarter<Gm, KQJL, VQJL>(s_stage + st * Gm::stage, &s_full[st * 4 + qtr], a,
+                                  ((size_t)cur_b * H + cur_h) * a.capacity + t0, qtr, min(16, s_len[cur_b] - t0));
+    cur_i += kPersistGroups;
+    cur_t += kPersistGroups;
+    while (cur_i < nloc) {
+      const int nb = s_pre[cur_b + 1] - s_pre[cur_b];
+      if (cur_t < nb) break;
+      cur_t -= nb;
+      if (++cur_h == H) {
+        cur_h = 0;
+        do ++cur_b; while (s_pre[cur_b + 1] == s_pre[cur_b]);  // skip empty sequences
+      }
+    }
   };
-  if (tid == 0)
-    for (long long i = 0; i < S && g0 + i < g1; ++i) issue(i);
+  if (lane == 0)
+    for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
 
   const LaneConsts<KB> lc(lane);
   WarpState ws;
   bool bad = false;
   float *park = reinterpret_cast<float *>(smem + Gm::sm_ktab);
   // query row (= unit: one query head per KV head) of the segment starting at tile g
-  auto unit_of = [&](long long g) -> int {
+  auto unit_of = [&](int g) -> int {
     const int bb = batch_of(g);
     const int nb = s_pre[bb + 1] - s_pre[bb];
-    return bb * H + (int)((g - (long long)H * s_pre[bb]) / nb);
+    return bb * H + (g - H * s_pre[bb]) / nb;
   };
   if (tid < 2 * kD) s_q[tid] = __ldg(a.qprep + (size_t)unit_of(g0) * 2 * kD + tid);
   __syncthreads();
-  long long g = g0;
+  int g = g0;
   while (g < g1) {  // one segment per (batch, kv head) the slice touches
     const int bb = batch_of(g);
     const int nb = s_pre[bb + 1] - s_pre[bb];
-    const long long ubase = (long long)H * s_pre[bb];
-    const int h = (int)((g - ubase) / nb);
-    const long long us = ubase + (long long)h * nb;
-    const long long se = min(us + nb, g1);
+    const int ubase = H * s_pre[bb];
+    const int h = (g - ubase) / nb;
+    const int us = ubase + h * nb;
+    const int se = min(us + nb, g1);
     const int len = s_len[bb];
     const int u = bb * H + h;
 
@@ -703,25 +747,19 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
 
     ws.reset();
     // this group's tiles: local index i = t - g0 with i % 4 == grp
-    long long t = g + ((grp - (int)((g - g0) & 3)) & 3);
-    for (; t < se; t += kPersistGroups) {
-      const long long i = t - g0;
-      const int stage = (int)(i % S);
-      if (!bad && !mbar_wait_bounded(&s_full[stage], (uint32_t)((i / S) & 1), a.error)) bad = true;
+    for (int t = g + ((grp - ((g - g0) & 3)) & 3); t < se; t += kPersistGroups) {
+      const int i = t - g0;
+      const int stage = i % S;
+      if (!bad && !mbar_wait_bounded(&s_full[stage * 4 + qtr], (uint32_t)((i / S) & 1), a.error)) bad = true;
       bad = __any_sync(kFull, bad);
       if (!bad)
-        tile_body<Gm, KB, VB, KQJL, VQJL>(s_stage + stage * Gm::stage, smem, (warp & 3) * 16,
-                                          (int)((t - us) * kTT), len, lane, lc, ws);
-      // release the stage: the last of the group's four warps refills it
+        tile_body<Gm, KB, VB, KQJL, VQJL>(s_stage + stage * Gm::stage, smem, qtr * 16, (t - us) * kTT, len, lane,
+                                          lc, ws);
+      // this warp is done with its quarter of the stage: refill it
       __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        const unsigned old = atomicAdd(&s_cnt[stage], 1u);
-        if ((old & 3u) == 3u && g0 + i + S < g1) {
-          __threadfence_block();
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue(i + S);
-        }
+      if (lane == 0 && cur_i < nloc) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_next();
       }
     }
 
