@@ -614,34 +614,45 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
 // ============================================================================
 constexpr int kPersistWarps = 16;  // four groups of four (kPersistGroups)
 
-// TMA of one warp's quarter (tokens t0 .. t0 + n - 1, n <= 16, of slot row s0) into
-// stage `st`, quarter q; n <= 0 completes the barrier phase with no copy
+// One plane of the cache per lane (lanes 0 .. kPlanes - 1): the lanes of a warp
+// issue the TMA copies of its quarter tile in parallel.
 template <typename Gm, bool KQJL, bool VQJL>
-__device__ __forceinline__ void issue_quarter(unsigned char *st, uint64_t *bar, const Decode2Args &a, size_t s0,
-                                              int q, int n) {
-  if (n <= 0) {
-    mbar_arrive_expect_tx(bar, 0);
-    return;
+struct PlaneLane {
+  static constexpr int kPlanes = 4 + (KQJL ? 2 : 0) + (VQJL ? 2 : 0);
+  const unsigned char *base = nullptr;  // global plane
+  int tok = 0;                          // bytes per token
+  int off = 0;                          // stage offset of the plane
+  bool norm = false;                    // 4-byte plane: copied in whole 16-byte units
+  __device__ __forceinline__ PlaneLane(const Decode2Args &a, int lane) {
+    int k = 0;
+    auto set = [&](const void *b, int t, int o, bool nm) {
+      if (lane == k) {
+        base = static_cast<const unsigned char *>(b);
+        tok = t;
+        off = o;
+        norm = nm;
+      }
+      ++k;
+    };
+    set(a.k_codes, Gm::kc, Gm::off_kc, false);
+    set(a.k_norm, 4, Gm::off_kn, true);
+    if (KQJL) {
+      set(a.k_signs, 16, Gm::off_ks, false);
+      set(a.k_rnorm, 4, Gm::off_kr, true);
+    }
+    set(a.v_codes, Gm::vc, Gm::off_vc, false);
+    set(a.v_norm, 4, Gm::off_vn, true);
+    if (VQJL) {
+      set(a.v_signs, 16, Gm::off_vs, false);
+      set(a.v_rnorm, 4, Gm::off_vr, true);
+    }
   }
-  const int n4 = (n + 3) & ~3;  // norms in 16-byte units
-  uint32_t bytes = n * Gm::kc + n4 * 4 + n * Gm::vc + n4 * 4;
-  if (KQJL) bytes += n * 16 + n4 * 4;
-  if (VQJL) bytes += n * 16 + n4 * 4;
-  mbar_arrive_expect_tx(bar, bytes);
-  const int o = 16 * q;  // first token of the quarter within the tile
-  tma_load_1d(st + Gm::off_kc + o * Gm::kc, a.k_codes + s0 * Gm::kc, n * Gm::kc, bar);
-  tma_load_1d(st + Gm::off_kn + o * 4, a.k_norm + s0, n4 * 4, bar);
-  if (KQJL) {
-    tma_load_1d(st + Gm::off_ks + o * 16, a.k_signs + s0 * 16, n * 16, bar);
-    tma_load_1d(st + Gm::off_kr + o * 4, a.k_rnorm + s0, n4 * 4, bar);
+  // bytes of a quarter of n tokens (n >= 1)
+  static __device__ __forceinline__ uint32_t bytes(int n) {
+    const int n4 = (n + 3) & ~3;
+    return n * (Gm::kc + Gm::vc + 16 * ((KQJL ? 1 : 0) + (VQJL ? 1 : 0))) + n4 * 4 * (2 + (KQJL ? 1 : 0) + (VQJL ? 1 : 0));
   }
-  tma_load_1d(st + Gm::off_vc + o * Gm::vc, a.v_codes + s0 * Gm::vc, n * Gm::vc, bar);
-  tma_load_1d(st + Gm::off_vn + o * 4, a.v_norm + s0, n4 * 4, bar);
-  if (VQJL) {
-    tma_load_1d(st + Gm::off_vs + o * 16, a.v_signs + s0 * 16, n * 16, bar);
-    tma_load_1d(st + Gm::off_vr + o * 4, a.v_rnorm + s0, n4 * 4, bar);
-  }
-}
+};
 
 template <int KB, int VB, bool KQJL, bool VQJL>
 __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(Decode2Args a) {
@@ -685,34 +696,51 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     return lo;
   };
 
-  // refill cursor of this warp (lane 0): the (batch, head, tile) of local tile i_next
-  int cur_i = grp, cur_b = 0, cur_h = 0, cur_t = 0;
-  if (cur_i < nloc) {
-    const int g = g0 + cur_i;
-    cur_b = batch_of(g);
-    const int nb = s_pre[cur_b + 1] - s_pre[cur_b], r = g - H * s_pre[cur_b];
-    cur_h = r / nb;
-    cur_t = r - cur_h * nb;
-  }
-  auto issue_next = [&]() {  // issue this warp's quarter of local tile cur_i, then step the cursor by 4
-    const int st = cur_i % S;
-    const int t0 = cur_t * kTT + 16 * qtr;
-    issue_quarter<Gm, KQJL, VQJL>(s_stage + st * Gm::stage, &s_full[st * 4 + qtr], a,
-                                  ((size_t)cur_b * H + cur_h) * a.capacity + t0, qtr, min(16, s_len[cur_b] - t0));
-    cur_i += kPersistGroups;
-    cur_t += kPersistGroups;
-    while (cur_i < nloc) {
-      const int nb = s_pre[cur_b + 1] - s_pre[cur_b];
-      if (cur_t < nb) break;
-      cur_t -= nb;
+  // refill cursor of this warp (all lanes): local tile cur_i, its tile index cur_t
+  // within its head, that head's tile count, sequence length and slot row
+  const PlaneLane<Gm, KQJL, VQJL> pl(a, lane);
+  int cur_i = grp, cur_b = 0, cur_t = 0, cur_nb = 1, cur_len = 0, cur_h = 0;
+  size_t cur_row = 0;
+  auto seek = [&]() {  // normalise cur_t into its head (heads hold >= 1 tile)
+    while (cur_t >= cur_nb) {
+      cur_t -= cur_nb;
       if (++cur_h == H) {
         cur_h = 0;
         do ++cur_b; while (s_pre[cur_b + 1] == s_pre[cur_b]);  // skip empty sequences
+        cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
+        cur_len = s_len[cur_b];
       }
+      cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
     }
   };
-  if (lane == 0)
-    for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
+  if (cur_i < nloc) {
+    const int g = g0 + cur_i;
+    cur_b = batch_of(g);
+    cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
+    cur_len = s_len[cur_b];
+    const int r = g - H * s_pre[cur_b];
+    cur_h = r / cur_nb;
+    cur_t = r - cur_h * cur_nb;
+    cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
+  }
+  // issue this warp's quarter of local tile cur_i (whole warp), then step the cursor by 4 tiles
+  auto issue_next = [&]() {
+    const int st = cur_i % S;
+    uint64_t *bar = &s_full[st * 4 + qtr];
+    const int t0 = cur_t * kTT + 16 * qtr;
+    const int n = min(16, cur_len - t0);
+    if (lane == 0) mbar_arrive_expect_tx(bar, n > 0 ? PlaneLane<Gm, KQJL, VQJL>::bytes(n) : 0u);
+    __syncwarp();
+    if (n > 0 && lane < PlaneLane<Gm, KQJL, VQJL>::kPlanes) {
+      const int cnt = pl.norm ? ((n + 3) & ~3) : n;
+      tma_load_1d(s_stage + st * Gm::stage + pl.off + 16 * qtr * pl.tok, pl.base + (cur_row + t0) * pl.tok,
+                  (uint32_t)(cnt * pl.tok), bar);
+    }
+    cur_i += kPersistGroups;
+    cur_t += kPersistGroups;
+    if (cur_i < nloc) seek();
+  };
+  for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
 
   const LaneConsts<KB> lc(lane);
   WarpState ws;
@@ -757,7 +785,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
                                           lc, ws);
       // this warp is done with its quarter of the stage: refill it
       __syncwarp();
-      if (lane == 0 && cur_i < nloc) {
+      if (cur_i < nloc) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue_next();
       }

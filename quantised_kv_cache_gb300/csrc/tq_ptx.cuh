@@ -45,6 +45,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the thread sleep for up to `hint_ns` while the phase is
+// incomplete (it wakes as soon as the phase completes)
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -52,13 +66,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for phase `parity` of `bar` to complete; false (and *err set) after
-// `budget_ns` of wall time.
+// `budget_ns` of wall time. Between checks the thread sleeps in the try_wait
+// (up to 20 us per call), so a waiting warp issues almost nothing.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *err,
                                                   uint64_t budget_ns = kWaitBudgetNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
     if (global_ns() - t0 > budget_ns) {
       set_error(err, TQ_ERR_TIMEOUT);
       return false;
