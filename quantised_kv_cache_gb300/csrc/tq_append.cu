@@ -233,7 +233,9 @@ int dispatch_bits(int bits, const AppendKernelArgs &k, long long total, cudaStre
 
 int launch_append_tq(const AppendArgs &a, void *stream) {
   if (a.ctx) {
-    const int r = launch_append2(a, a.ctx, stream);
+    int r = launch_append2(a, a.ctx, stream);
+    if (r != TQ_ERR_UNSUPPORTED) return r;
+    r = launch_append_qjl(a, a.ctx, stream);
     if (r != TQ_ERR_UNSUPPORTED) return r;
   }
   AppendKernelArgs k{};

@@ -285,6 +285,15 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
     return TQ_ERR_ARG;
   }
   make_sketch(seed, d, c->sketch);
+  {  // an upper bound of the largest row norm of S (certifies the tensor-core signs)
+    double m = 0.0;
+    for (int j = 0; j < d; ++j) {
+      double ss = 0.0;
+      for (int k = 0; k < d; ++k) ss += (double)c->sketch[j * d + k] * c->sketch[j * d + k];
+      m = std::max(m, std::sqrt(ss));
+    }
+    c->sketch_rowmax = (float)(m * (1.0 + 1e-6));
+  }
 
   tq::DevParams *hp = (tq::DevParams *)std::calloc(1, sizeof(tq::DevParams));
   if (!hp) {
@@ -304,6 +313,8 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (e == cudaSuccess) e = cudaMalloc((void **)&c->dparams, sizeof(tq::DevParams));
   if (e == cudaSuccess) e = cudaMemcpy(c->dparams, hp, sizeof(tq::DevParams), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && tq::launch_sketch_prep(c->dparams, nullptr) != TQ_OK) e = cudaErrorUnknown;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
   std::free(hp);
   if (e != cudaSuccess) {
     if (c->dparams) cudaFree(c->dparams);

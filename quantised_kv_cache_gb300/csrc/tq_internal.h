@@ -26,7 +26,13 @@ struct DevParams {
   float sketch[kD * kD];       // S, row-major [row][col]
   int error;                   // sticky device error word (a tq_status)
   int pad[3];
+  // S as fp16 hi + lo parts (hi = fp16(S), lo = fp16(S - hi)), rows in sign-record
+  // order, in the tensor-core K-major core-matrix layout (set on the device at
+  // context creation): [2][128 x 128] halves, 16-byte aligned
+  uint16_t sketch_hl[2 * kD * kD];
 };
+// fills DevParams::sketch_hl from DevParams::sketch (stream order)
+int launch_sketch_prep(DevParams *dp, void *stream);
 
 struct Role {
   int bits = 0;
@@ -56,6 +62,7 @@ struct tq_ctx {
   float v_bounds[tq::kMaxLevels] = {};
   int8_t diag[tq::kD] = {};
   float *sketch = nullptr;  // host, d*d
+  float sketch_rowmax = 0.f;  // an upper bound of max_j ||S_j||
   tq::DevParams *dparams = nullptr;
   // optional CUDA events recorded around the decode / append kernels
   void *prof_decode_start = nullptr, *prof_decode_stop = nullptr;
@@ -84,6 +91,8 @@ struct AppendArgs {
 int launch_append_tq(const AppendArgs &a, void *stream);
 // thread-per-vector append for vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise
 int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream);
+// thread-per-vector append with the QJL sketch on tcgen05 tensor cores; TQ_ERR_UNSUPPORTED otherwise
+int launch_append_qjl(const AppendArgs &a, const tq_ctx *ctx, void *stream);
 
 struct DecodeArgs {
   const tq_ctx *ctx;
