@@ -221,6 +221,76 @@ def run_small_case(args, dev):
     print(json.dumps({"case": args.case, "ok": True}), flush=True)
 
 
+def run_configs(args, dev):
+    """Decode throughput on the other workloads (one JSON line each): config 1 (single head),
+    config 3 (three schemes at 4 bits), config 4 (GQA 32q/8kv, N=131072, KQV n=3), config 5
+    (KIVI, two layouts). Caches smaller than 3x L2 are replicated and rotated so that every
+    call reads HBM. Times are CUDA events around the library's decode kernel (profile events)
+    and around the whole call (query prep + decode + combine)."""
+    import torch
+    from quantised_kv_cache_gb300 import tq
+    from quantised_kv_cache_gb300 import workloads as wl
+    hbm_peak, peak_kind = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cases = [(1, "KQV", 4, None), (3, "KV", 4, None), (3, "KQV", 4, None), (3, "QKQV", 4, None),
+             (4, "KQV", 3, None), (5, "KIVI", 2, (True, True)), (5, "KIVI", 2, (False, False))]
+    for wid, scheme, n, kivi in cases:
+        w = wl.WORKLOADS[wid]
+        B, Hq, H, N = w.batch, w.heads_q, w.heads_kv, w.seq
+        if kivi is not None:
+            ctx = tq.Context(128, n, scheme, 42, k_per_channel=kivi[0], v_per_token=kivi[1])
+        else:
+            ctx = tq.Context(128, n, scheme, 42)
+        q, k, v = wl.generate(w, dev)
+        one = tq.Cache(ctx, B, H, N, device=dev)
+        rec = one.record_bytes if scheme != "KIVI" else 96
+        bytes_call = B * H * N * rec if scheme != "KIVI" else B * H * ((N - 128) * 96 + 128 * 512)
+        reps = max(1, min(16, int(math.ceil(3 * l2 / max(bytes_call, 1)))))
+        caches = [one] + [tq.Cache(ctx, B, H, N, device=dev) for _ in range(reps - 1)]
+        zeros = torch.zeros((B,), dtype=torch.int32, device=dev)
+        for c in caches:
+            if scheme == "KIVI":
+                for t0 in range(0, N, 512):
+                    t1 = min(N, t0 + 512)
+                    lens = torch.full((B,), t0, dtype=torch.int32, device=dev)
+                    tq.tq_append_quantize(ctx.handle, c, k[:, :, t0:t1].contiguous(), v[:, :, t0:t1].contiguous(), lens)
+            else:
+                tq.tq_append_quantize(ctx.handle, c, k, v, zeros)
+        lens = torch.full((B,), N, dtype=torch.int32, device=dev)
+        splits = w.splits
+        ws = torch.empty(tq.tq_workspace_size(ctx.handle, B, Hq, H, N, splits), dtype=torch.uint8, device=dev)
+        out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+        iters = max(20, 8 * reps)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for i in range(3 * reps):
+            tq.tq_decode_attention(ctx.handle, caches[i % reps], q, lens, N, splits, ws, out)
+        torch.cuda.synchronize()
+        for a_, b_ in evs:
+            a_.record()
+            b_.record()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for i in range(iters):
+            tq.tq_set_profile_events(ctx.handle, evs[i][0], evs[i][1])
+            tq.tq_decode_attention(ctx.handle, caches[i % reps], q, lens, N, splits, ws, out)
+        c1.record()
+        torch.cuda.synchronize()
+        tq.tq_set_profile_events(ctx.handle)
+        assert tq.tq_get_device_error(ctx.handle) == 0
+        ms_kernel = sum(a_.elapsed_time(b_) for a_, b_ in evs) / iters
+        ms_call = c0.elapsed_time(c1) / iters
+        gbs_k, gbs_c = bytes_call / ms_kernel / 1e6, bytes_call / ms_call / 1e6
+        print(json.dumps({"case": "configs", "config": wid, "scheme": scheme, "bits": n,
+                          "kivi_layout": None if kivi is None else {"k_per_channel": kivi[0], "v_per_token": kivi[1]},
+                          "shape": {"batch": B, "heads_q": Hq, "heads_kv": H, "context": N},
+                          "bytes_per_call": bytes_call, "replicas": reps,
+                          "ms_kernel": ms_kernel, "GBps_kernel": gbs_k, "frac_kernel": gbs_k / hbm_peak,
+                          "ms_call": ms_call, "GBps_call": gbs_c, "frac_call": gbs_c / hbm_peak,
+                          "peak": hbm_peak, "peak_kind": peak_kind}), flush=True)
+        del caches, one
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -228,7 +298,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["step", "decode-small", "append-small"], default="step",
+    ap.add_argument("--case", choices=["step", "decode-small", "append-small", "configs"], default="step",
                     help="step: the benchmark; *-small: one kernel family on B16 H32 N4096 (294 MB of records, "
                          "above L2) for profiler captures")
     args = ap.parse_args()
@@ -256,6 +326,9 @@ def main():
     if dist is not None:
         dist.barrier()
 
+    if args.case == "configs":
+        run_configs(args, dev)
+        return
     if args.case != "step":
         run_small_case(args, dev)
         return

@@ -337,6 +337,7 @@ struct CombineArgs {
   // one query head per KV head
   const int32_t *tile_prefix;
   int persist_ctas, heads_kv, persist_groups;
+  int group = 1;  // query heads per KV head (persistent records hold `group` heads per slot)
 };
 
 // one CTA (128 threads, thread = coordinate) per (batch, query head)
@@ -351,8 +352,10 @@ __global__ void __launch_bounds__(128) combine_tq_kernel(CombineArgs a) {
   long long T = 0, T4 = 1, C = 1, c_lo = 0, c_hi = -1;
   int unit = 0;
   auto bnd = [&](long long c) -> long long { return min(T, 4 * (T4 * c / C)); };
+  int hh = 0;
   if (a.tile_prefix) {
-    const int b = row / a.heads_q, h = row % a.heads_q;
+    const int b = row / a.heads_q, h = (row % a.heads_q) / a.group;
+    hh = (row % a.heads_q) % a.group;
     const int p0 = __ldg(a.tile_prefix + b), nb = __ldg(a.tile_prefix + b + 1) - p0;
     T = (long long)a.heads_kv * __ldg(a.tile_prefix + a.batch);
     T4 = (T + 3) / 4;
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(128) combine_tq_kernel(CombineArgs a) {
     if (!a.tile_prefix) return base + (size_t)k * kPartialFloats;
     const long long c = c_lo + k / ng;
     if (bnd(c) == bnd(c + 1)) return nullptr;  // an empty slice wrote nothing
-    return a.partials + ((size_t)(c + unit) * ng + (k % ng)) * kPartialFloats;
+    return a.partials + (((size_t)(c + unit) * ng + (k % ng)) * a.group + hh) * kPartialFloats;
   };
   float M = -INFINITY;
   for (int k = 0; k < nrec; ++k) {
@@ -623,10 +626,12 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   const int G = a.heads_q / a.heads_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return TQ_ERR_UNSUPPORTED;
 
-  const bool g1 = a.heads_q == a.heads_kv;
+  // the persistent kernels (one query head per KV head, or GQA groups of 2 / 4 without
+  // key sketches) take the per-batch tile prefix the query prep computes
+  const bool persist_ok = G == 1 || ((G == 2 || G == 4) && ctx->scheme != TQ_SCHEME_QKQV);
   PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, ctx->k.rotate, ctx->k.qjl,
              ctx->dparams->diag, ctx->dparams->sketch, a.qprep,
-             a.seq_lens, a.cache->capacity, g1 ? a.tile_prefix : nullptr};
+             a.seq_lens, a.cache->capacity, persist_ok ? a.tile_prefix : nullptr};
   const int rows = a.batch * a.heads_q;
   qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
 
@@ -634,13 +639,14 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   if (ctx->prof_decode_start) cudaEventRecord((cudaEvent_t)ctx->prof_decode_start, st);
   int persist_ctas = 0;
   DecodeArgs a2 = a;
-  if (!g1) a2.tile_prefix = nullptr;
+  if (!persist_ok) a2.tile_prefix = nullptr;
   int r2 = launch_decode2_g1(a2, &persist_ctas, stream);
   if (r2 == TQ_OK) {
     if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
     CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                     ctx->dparams->diag, ctx->dparams->sketch, a.out,
                     persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv, kPersistGroups};
+    cmb.group = G;
     combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
   }

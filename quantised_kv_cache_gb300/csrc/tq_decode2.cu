@@ -803,6 +803,396 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
   }
 }
 
+// ============================================================================
+// GQA: G query heads per KV head (G = 2 or 4), persistent like the kernel
+// above. Keys become the MMA's A operand: a lane-replicated table maps each
+// pair field of a key record to (hi, lo) fp16 pairs of the two centroids, and
+// the pair-slot layout makes the MMA's K index natural coordinate order, so B
+// holds the G rotated queries' fp16 hi / lo parts as columns 2h, 2h + 1. Two
+// MMAs per 16 coordinates (A hi, A lo) score 16 tokens for all G heads with
+// all four hi / lo products. A lane (g, t) then owns head t: the scores of
+// tokens g and g + 8, that head's softmax state and accumulator columns.
+// ============================================================================
+template <int KB, int VB, bool VQJL, int G>
+struct GeoQ {
+  using Gs = Geo<KB, VB, false, VQJL, kPersistWarps, 1>;  // stage layout
+  static constexpr int kval = 1 << (2 * KB);
+  static constexpr int vlut = Gs::vlut;                  // words
+  static constexpr int sm_klut = vlut * 4;               // [kval][32 lanes] x (hi, lo) half2 pairs
+  static constexpr int sm_park = sm_klut + kval * 256;   // [4 warps][G][kPartialFloats]
+  static constexpr int sm_stage0 = sm_park + 4 * G * kPartialFloats * 4;
+  static constexpr int fixed = sm_stage0 + 16 * 4 * 8 + G * kD * 4 + 4 * (2 * kMaxPersistBatch + 1) + 64;
+  static constexpr int S = ((227 * 1024 - fixed) / Gs::stage >= 16) ? 16 : (((227 * 1024 - fixed) / Gs::stage) / 4) * 4;
+  static constexpr int stage = Gs::stage;
+  static constexpr int off_kc = Gs::off_kc, off_kn = Gs::off_kn, off_vc = Gs::off_vc, off_vn = Gs::off_vn;
+  static constexpr int off_vs = Gs::off_vs, off_vr = Gs::off_vr, kc = Gs::kc, vc = Gs::vc;
+  static constexpr int sm_bar = sm_stage0 + S * stage;
+  static constexpr int sm_q = sm_bar + S * 4 * 8;                  // [G][128]
+  static constexpr int sm_misc = sm_q + G * kD * 4;
+  static constexpr int total = sm_misc + 4 * (2 * kMaxPersistBatch + 1);
+};
+
+// one warp's 16 tokens for all G heads of its KV head
+template <typename Q, int KB, int VB, bool VQJL, int G>
+__device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const unsigned char *smem, int wbase, int t0,
+                                              int t_end, int lane, const uint32_t (&bk)[8][2], float &m_run,
+                                              float &l_run, float &w_run, float (&acc_v)[8][4],
+                                              float (&acc_s)[8][4]) {
+  const int g = lane >> 2, t4 = lane & 3, h = g >> 1;
+  const uint32_t lane8 = (uint32_t)lane << 3, lane4 = (uint32_t)lane << 2;
+  const float *kn = reinterpret_cast<const float *>(st + Q::off_kn);
+  // ---- scores of tokens g and g + 8 for head t4: S = K_hat (A) x [q_hi, q_lo] (B)
+  float sk[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    uint32_t w0[KB], w1[KB];
+    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Q::off_kc + (wbase + g) * Q::kc);
+    const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Q::off_kc + (wbase + 8 + g) * Q::kc);
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      w0[k] = r0[KB * t4 + k];
+      w1[k] = r1[KB * t4 + k];
+    }
+    // field n of a span -> (hi, lo) pair of the key table at (field << 8) | (lane << 3)
+    auto klut = [&](const uint32_t(&w)[KB], int n) -> uint2 {
+      constexpr int F = 2 * KB;
+      constexpr uint32_t mask = ((1u << F) - 1u) << 8;
+      const int bit = F * n, wi = bit >> 5, off = bit & 31;
+      uint32_t x;
+      if (off < 8) x = w[wi] << (8 - off);
+      else x = __funnelshift_r(w[wi], w[(wi + 1 < KB) ? wi + 1 : wi], off - 8);
+      return *reinterpret_cast<const uint2 *>(smem + Q::sm_klut + ((x & mask) | lane8));
+    };
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      const uint2 a0 = klut(w0, 2 * kb), a1 = klut(w1, 2 * kb), a2 = klut(w0, 2 * kb + 1), a3 = klut(w1, 2 * kb + 1);
+      mma_16816(sk, a0.x, a1.x, a2.x, a3.x, bk[kb][0], bk[kb][1]);
+      mma_16816(sk, a0.y, a1.y, a2.y, a3.y, bk[kb][0], bk[kb][1]);
+    }
+  }
+  const int tok0 = wbase + g, tok1 = wbase + 8 + g;
+  const bool v0 = t0 + tok0 < t_end, v1 = t0 + tok1 < t_end;
+  float s0 = v0 ? (sk[0] + sk[1]) * kn[tok0] : -INFINITY;
+  float s1 = v1 ? (sk[2] + sk[3]) * kn[tok1] : -INFINITY;
+  // ---- online softmax of head t4 over the warp's 16 tokens (the 8 lanes g share t4)
+  float tmax = fmaxf(s0, s1);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+  const float m_new = fmaxf(m_run, tmax);
+  const float p0 = v0 ? ex2_approx(s0 - m_new) : 0.f, p1 = v1 ? ex2_approx(s1 - m_new) : 0.f;
+  if (m_new != m_run) {  // per head (lane-divergent; no shuffles inside)
+    const float scale = ex2_approx(m_run - m_new);
+    l_run *= scale;
+    w_run *= scale;
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc_v[mb][j] *= scale;
+        if (VQJL) acc_s[mb][j] *= scale;
+      }
+    m_run = m_new;
+  }
+  l_run += p0 + p1;
+  // ---- B operands: column 2h + part of lane (g, t) = hi / lo of head h's weights of tokens
+  // 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1); token j of head h sits on lane 4 (j % 8) + h
+  auto hl2 = [](float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
+    hi = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+    lo = (uint32_t)__half_as_ushort(__float2half_rn(a - __half2float(ha))) |
+         ((uint32_t)__half_as_ushort(__float2half_rn(b - __half2float(hb))) << 16);
+  };
+  const int src0 = 4 * (2 * t4) + h, src1 = 4 * (2 * t4 + 1) + h;
+  const bool live = g < 2 * G, lo_part = (g & 1) != 0;
+  auto gather = [&](uint32_t xh, uint32_t xl, uint32_t &b0, uint32_t &b1) {
+    const uint32_t a_h = __shfl_sync(kFull, xh, src0), a_l = __shfl_sync(kFull, xl, src0);
+    const uint32_t c_h = __shfl_sync(kFull, xh, src1), c_l = __shfl_sync(kFull, xl, src1);
+    const uint32_t a = lo_part ? a_l : a_h, c = lo_part ? c_l : c_h;
+    b0 = live ? __byte_perm(a, c, 0x5410u) : 0u;  // tokens 2t, 2t+1
+    b1 = live ? __byte_perm(a, c, 0x7632u) : 0u;  // tokens 2t+8, 2t+9
+  };
+  uint32_t bv0, bv1, bs0 = 0, bs1 = 0;
+  {
+    const float *vn = reinterpret_cast<const float *>(st + Q::off_vn);
+    uint32_t xh, xl;
+    hl2(v0 ? p0 * vn[tok0] : 0.f, v1 ? p1 * vn[tok1] : 0.f, xh, xl);
+    gather(xh, xl, bv0, bv1);
+    if (VQJL) {
+      const float *vr = reinterpret_cast<const float *>(st + Q::off_vr);
+      const float r0 = v0 ? p0 * vr[tok0] : 0.f, r1 = v1 ? p1 * vr[tok1] : 0.f;
+      w_run += r0 + r1;
+      hl2(r0, r1, xh, xl);
+      gather(xh, xl, bs0, bs1);
+    }
+  }
+  // ---- values: as in the one-head body (pair table + movmatrix), G heads in the columns
+  {
+    uint32_t w0[VB], w1[VB];
+    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Q::off_vc + (wbase + g) * Q::vc);
+    const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Q::off_vc + (wbase + 8 + g) * Q::vc);
+#pragma unroll
+    for (int k = 0; k < VB; ++k) {
+      w0[k] = r0[VB * t4 + k];
+      w1[k] = r1[VB * t4 + k];
+    }
+    auto lut = [&](const uint32_t(&w)[VB], int n) -> uint32_t {
+      constexpr int F = 2 * VB;
+      constexpr uint32_t mask = ((1u << F) - 1u) << 7;
+      const int bit = F * n, wi = bit >> 5, off = bit & 31;
+      uint32_t x;
+      if (off < 7) x = w[wi] << (7 - off);
+      else x = __funnelshift_r(w[wi], w[(wi + 1 < VB) ? wi + 1 : wi], off - 7);
+      return *reinterpret_cast<const uint32_t *>(smem + ((x & mask) | lane4));
+    };
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const uint32_t x00 = movmatrix_t(lut(w0, 2 * mb));
+      const uint32_t x01 = movmatrix_t(lut(w0, 2 * mb + 1));
+      const uint32_t x10 = movmatrix_t(lut(w1, 2 * mb));
+      const uint32_t x11 = movmatrix_t(lut(w1, 2 * mb + 1));
+      mma_16816(acc_v[mb], x00, x01, x10, x11, bv0, bv1);
+    }
+  }
+  // ---- QJL signs (same operands as the one-head body), separate accumulator
+  if (VQJL) {
+    const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + Q::off_vs);
+    const int wsel = g >> 1;
+    const uint32_t swsel = (g & 1) ? 0x7632u : 0x5410u;
+    const uint32_t wa0 = sw[(wbase + 2 * t4) * 4 + wsel], wb0 = sw[(wbase + 2 * t4 + 1) * 4 + wsel];
+    const uint32_t wa1 = sw[(wbase + 2 * t4 + 8) * 4 + wsel], wb1 = sw[(wbase + 2 * t4 + 9) * 4 + wsel];
+    const uint32_t sa = __byte_perm(wa0, wb0, swsel), sb = __byte_perm(wa1, wb1, swsel);
+    const uint32_t sar10 = rotr(sa, 22), sar5 = rotr(sa, 27), sar27 = rotr(sa, 5);
+    const uint32_t sbr10 = rotr(sb, 22), sbr5 = rotr(sb, 27), sbr27 = rotr(sb, 5);
+    auto pick = [&](int k, uint32_t r0, uint32_t r5, uint32_t r10, uint32_t r27) -> uint32_t {
+      const uint32_t src = sign_rot(k) == 10 ? r10 : (sign_rot(k) == 5 ? r5 : (sign_rot(k) == 0 ? r0 : r27));
+      return src & (0x00010001u << sign_land(k));
+    };
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const uint32_t a0 = pick(2 * mb, sa, sar5, sar10, sar27);
+      const uint32_t a1 = pick(2 * mb + 1, sa, sar5, sar10, sar27);
+      const uint32_t a2 = pick(2 * mb, sb, sbr5, sbr10, sbr27);
+      const uint32_t a3 = pick(2 * mb + 1, sb, sbr5, sbr10, sbr27);
+      mma_16816(acc_s[mb], a0, a1, a2, a3, bs0, bs1);
+    }
+  }
+}
+
+template <int KB, int VB, bool VQJL, int G>
+__global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kernel(Decode2Args a) {
+  using Q = GeoQ<KB, VB, VQJL, G>;
+  constexpr int S = Q::S;
+  static_assert(S >= 4 && S % kPersistGroups == 0, "ring stages");
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char *s_stage = smem + Q::sm_stage0;
+  uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Q::sm_bar);  // [S][4 quarters]
+  float *s_q = reinterpret_cast<float *>(smem + Q::sm_q);              // [G][128]
+  int *s_pre = reinterpret_cast<int *>(smem + Q::sm_misc);
+  int *s_len = s_pre + kMaxPersistBatch + 1;
+  float *park = reinterpret_cast<float *>(smem + Q::sm_park);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, grp = warp >> 2, qtr = warp & 3;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int B = a.batch, H = a.heads_kv;
+  // head-independent tables: value pairs, and key pairs as (hi, lo) fp16 of the centroids
+  build_value_table<VB, kPersistWarps * 32>(smem, Q::vlut, a.v_centroids, tid);
+  {
+    uint2 *kl = reinterpret_cast<uint2 *>(smem + Q::sm_klut);
+    constexpr int M = (1 << KB) - 1;
+    for (int e = tid; e < Q::kval * 32; e += blockDim.x) {
+      const int f = e >> 5;
+      const float c0 = __ldg(a.k_centroids + (f & M)), c1 = __ldg(a.k_centroids + (f >> KB));
+      const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
+      const __half l0 = __float2half_rn(c0 - __half2float(h0)), l1 = __float2half_rn(c1 - __half2float(h1));
+      kl[e] = make_uint2((uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16),
+                         (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16));
+    }
+  }
+  for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
+  for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
+  if (tid < S * 4) mbar_init(&s_full[tid], 1);
+  mbar_fence_init();
+  __syncthreads();
+  const long long T = (long long)H * s_pre[B];
+  const long long C = gridDim.x, c = blockIdx.x, T4 = (T + 3) / 4;
+  const int g0 = (int)min(T, 4 * (T4 * c / C)), g1 = (int)min(T, 4 * (T4 * (c + 1) / C));
+  if (g0 >= g1) return;
+  const int nloc = g1 - g0;
+  auto batch_of = [&](int gg) -> int {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (H * s_pre[mid] <= gg) lo = mid;
+      else hi = mid;
+    }
+    return lo;
+  };
+  using Gs = typename Q::Gs;
+  const PlaneLane<Gs, false, VQJL> pl(a, lane);
+  // per-warp refill cursor, as in the one-head kernel
+  int cur_i = grp, cur_b = 0, cur_t = 0, cur_nb = 1, cur_len = 0, cur_h = 0;
+  size_t cur_row = 0;
+  auto seek = [&]() {
+    while (cur_t >= cur_nb) {
+      cur_t -= cur_nb;
+      if (++cur_h == H) {
+        cur_h = 0;
+        do ++cur_b; while (s_pre[cur_b + 1] == s_pre[cur_b]);
+        cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
+        cur_len = s_len[cur_b];
+      }
+      cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
+    }
+  };
+  if (cur_i < nloc) {
+    const int gg = g0 + cur_i;
+    cur_b = batch_of(gg);
+    cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
+    cur_len = s_len[cur_b];
+    const int r = gg - H * s_pre[cur_b];
+    cur_h = r / cur_nb;
+    cur_t = r - cur_h * cur_nb;
+    cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
+  }
+  auto issue_next = [&]() {
+    const int stn = cur_i % S;
+    uint64_t *bar = &s_full[stn * 4 + qtr];
+    const int tt0 = cur_t * kTT + 16 * qtr;
+    const int n = min(16, cur_len - tt0);
+    if (lane == 0) mbar_arrive_expect_tx(bar, n > 0 ? PlaneLane<Gs, false, VQJL>::bytes(n) : 0u);
+    __syncwarp();
+    if (n > 0 && lane < PlaneLane<Gs, false, VQJL>::kPlanes) {
+      const int cnt = pl.norm ? ((n + 3) & ~3) : n;
+      tma_load_1d(s_stage + stn * Q::stage + pl.off + 16 * qtr * pl.tok, pl.base + (cur_row + tt0) * pl.tok,
+                  (uint32_t)(cnt * pl.tok), bar);
+    }
+    cur_i += kPersistGroups;
+    cur_t += kPersistGroups;
+    if (cur_i < nloc) seek();
+  };
+  for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
+
+  // queries of unit u (= batch b, kv head hk): query rows (b, hk G + h), h < G
+  auto unit_of = [&](int gg) -> int {
+    const int bb = batch_of(gg);
+    const int nb = s_pre[bb + 1] - s_pre[bb];
+    return bb * H + (gg - H * s_pre[bb]) / nb;
+  };
+  for (int e = tid; e < G * kD; e += blockDim.x) s_q[e] = __ldg(a.qprep + (size_t)unit_of(g0) * G * 2 * kD +
+                                                              (size_t)(e / kD) * 2 * kD + (e % kD));
+  __syncthreads();
+  bool bad = false;
+  int gseg = g0;
+  while (gseg < g1) {
+    const int bb = batch_of(gseg);
+    const int nb = s_pre[bb + 1] - s_pre[bb];
+    const int ubase = H * s_pre[bb];
+    const int hk = (gseg - ubase) / nb;
+    const int us = ubase + hk * nb;
+    const int se = min(us + nb, g1);
+    const int len = s_len[bb];
+    const int u = bb * H + hk;
+    // B fragments of the key MMA: column 2h + part = hi / lo of query h (log2 e folded in);
+    // rows k = 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1) of block kb are coordinates 16 kb + k
+    uint32_t bk[8][2];
+    {
+      const int hh = g >> 1;
+      const bool lop = (g & 1) != 0, live = g < 2 * G;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int k0 = 16 * kb + 2 * t4 + 8 * r;
+          const float q0 = live ? s_q[hh * kD + k0] * kLog2e : 0.f, q1 = live ? s_q[hh * kD + k0 + 1] * kLog2e : 0.f;
+          const __half h0 = __float2half_rn(q0), h1 = __float2half_rn(q1);
+          const __half e0 = lop ? __float2half_rn(q0 - __half2float(h0)) : h0;
+          const __half e1 = lop ? __float2half_rn(q1 - __half2float(h1)) : h1;
+          bk[kb][r] = (uint32_t)__half_as_ushort(e0) | ((uint32_t)__half_as_ushort(e1) << 16);
+        }
+    }
+    __syncthreads();  // every warp has its fragments: s_q may take the next head's queries
+    if (se < g1)
+      for (int e = tid; e < G * kD; e += blockDim.x)
+        s_q[e] = __ldg(a.qprep + (size_t)unit_of(se) * G * 2 * kD + (size_t)(e / kD) * 2 * kD + (e % kD));
+
+    float m_run = -INFINITY, l_run = 0.f, w_run = 0.f;
+    float acc_v[8][4], acc_s[8][4];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc_v[mb][j] = acc_s[mb][j] = 0.f;
+    for (int t = gseg + ((grp - ((gseg - g0) & 3)) & 3); t < se; t += kPersistGroups) {
+      const int i = t - g0;
+      const int stage = i % S;
+      if (!bad && !mbar_wait_bounded(&s_full[stage * 4 + qtr], (uint32_t)((i / S) & 1), a.error)) bad = true;
+      bad = __any_sync(kFull, bad);
+      if (!bad)
+        tile_body_gqa<Q, KB, VB, VQJL, G>(s_stage + stage * Q::stage, smem, qtr * 16, (t - us) * kTT, len, lane,
+                                          bk, m_run, l_run, w_run, acc_v, acc_s);
+      __syncwarp();
+      if (cur_i < nloc) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_next();
+      }
+    }
+
+    // flush, one warp group at a time through the park area [4 warps][G][260]:
+    // lane (g, t) parks head t of its warp (value rows 16mb + g, 16mb + 8 + g)
+    float lsum = l_run, wsum = w_run;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      lsum += __shfl_xor_sync(kFull, lsum, o);
+      wsum += __shfl_xor_sync(kFull, wsum, o);
+    }
+    for (int gr = 0; gr < kPersistGroups; ++gr) {
+      __syncthreads();
+      if (grp == gr && t4 < G) {
+        float *dst = park + (qtr * G + t4) * kPartialFloats;
+        if (g == 0) {
+          dst[0] = m_run;
+          dst[1] = lsum;
+          dst[2] = wsum;
+        }
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          dst[4 + 16 * mb + g] = acc_v[mb][0] + acc_v[mb][1];
+          dst[4 + 16 * mb + 8 + g] = acc_v[mb][2] + acc_v[mb][3];
+          if (VQJL) {
+            const int c0 = 64 * (g & 1) + 8 * mb + 2 * (g >> 1);
+            dst[4 + kD + c0] = (acc_s[mb][0] + acc_s[mb][1]) * sign_unscale(sign_land(2 * mb));
+            dst[4 + kD + c0 + 1] = (acc_s[mb][2] + acc_s[mb][3]) * sign_unscale(sign_land(2 * mb + 1));
+          }
+        }
+      }
+      __syncthreads();
+      if (tid < G * kD) {
+        const int hh = tid / kD, i = tid % kD;
+        // the four warps' records of head hh sit at stride G records
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, park[(w * G + hh) * kPartialFloats]);
+        float L = 0.f, A = 0.f, Sg = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float *p = park + (w * G + hh) * kPartialFloats;
+          const float e = (p[0] == -INFINITY) ? 0.f : ex2_approx(p[0] - M);
+          L += p[1] * e;
+          A += p[4 + i] * e;
+          if (VQJL) Sg += (2.f * p[4 + kD + i] - p[2]) * e;
+        }
+        float *rec = a.partials + (((size_t)(c + u) * kPersistGroups + gr) * G + hh) * kPartialFloats;
+        if (i == 0) {
+          rec[0] = M * kLn2;
+          rec[1] = L;
+        }
+        rec[2 + i] = A;
+        rec[2 + kD + i] = Sg;
+      }
+    }
+    __syncthreads();
+    gseg = se;
+  }
+}
+
 template <int KB, int VB, bool KQJL, bool VQJL>
 int launch_split(const Decode2Args &k, dim3 grid, cudaStream_t st) {
   using Gm = Geo<KB, VB, KQJL, VQJL, 4, 3>;
@@ -836,6 +1226,29 @@ int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
+template <int KB, int VB, bool VQJL, int G>
+int launch_persist_gqa(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st) {
+  using Q = GeoQ<KB, VB, VQJL, G>;
+  const size_t smem = Q::total;
+  auto fn = decode_persist_gqa_kernel<KB, VB, VQJL, G>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    attr_done = true;
+  }
+  *ctas = num_sms;
+  fn<<<*ctas, kPersistWarps * 32, smem, st>>>(k);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+template <int KB, int VB, bool VQJL>
+int launch_gqa_g(const Decode2Args &k, int G, int num_sms, int *ctas, cudaStream_t st) {
+  if (G == 2) return launch_persist_gqa<KB, VB, VQJL, 2>(k, num_sms, ctas, st);
+  if (G == 4) return launch_persist_gqa<KB, VB, VQJL, 4>(k, num_sms, ctas, st);
+  return TQ_ERR_UNSUPPORTED;
+}
+
 template <int KB, int VB, bool KQJL, bool VQJL>
 int launch_variant(const Decode2Args &k, bool persist, int num_sms, int *ctas, cudaStream_t st) {
   if (persist) return launch_persist<KB, VB, KQJL, VQJL>(k, num_sms, ctas, st);
@@ -851,7 +1264,40 @@ int launch_variant(const Decode2Args &k, bool persist, int num_sms, int *ctas, c
 int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
   const tq_ctx *ctx = a.ctx;
   *persist_ctas = 0;
-  if (a.heads_q != a.heads_kv) return TQ_ERR_UNSUPPORTED;
+  const int G = a.heads_q / a.heads_kv;
+  if (G != 1) {
+    // GQA groups of 2 or 4 query heads, keys without a sketch, on the persistent tensor-core kernel
+    if ((G != 2 && G != 4) || ctx->scheme == TQ_SCHEME_QKQV || !a.tile_prefix || a.batch > kMaxPersistBatch ||
+        a.cache->capacity % 4 || ctx->num_sms <= 0)
+      return TQ_ERR_UNSUPPORTED;
+    const tq_cache *c = a.cache;
+    Decode2Args k{};
+    k.k_codes = c->k_codes; k.k_norm = c->k_norm; k.v_codes = c->v_codes; k.v_norm = c->v_norm;
+    k.v_signs = c->v_signs; k.v_rnorm = c->v_rnorm;
+    k.capacity = c->capacity;
+    k.batch = a.batch;
+    k.heads_kv = a.heads_kv;
+    k.heads_q = a.heads_q;
+    k.seq_lens = a.seq_lens;
+    k.tile_prefix = a.tile_prefix;
+    k.qprep = a.qprep;
+    k.partials = a.partials;
+    k.k_centroids = ctx->dparams->k_centroids;
+    k.v_centroids = ctx->dparams->v_centroids;
+    k.error = &ctx->dparams->error;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int kb = ctx->k.bits, ns = ctx->num_sms;
+    if (ctx->scheme == TQ_SCHEME_KV) {
+      if (kb == 2) return launch_gqa_g<2, 2, false>(k, G, ns, persist_ctas, st);
+      if (kb == 3) return launch_gqa_g<3, 3, false>(k, G, ns, persist_ctas, st);
+      if (kb == 4) return launch_gqa_g<4, 4, false>(k, G, ns, persist_ctas, st);
+    } else if (ctx->scheme == TQ_SCHEME_KQV) {
+      if (kb == 2) return launch_gqa_g<2, 1, true>(k, G, ns, persist_ctas, st);
+      if (kb == 3) return launch_gqa_g<3, 2, true>(k, G, ns, persist_ctas, st);
+      if (kb == 4) return launch_gqa_g<4, 3, true>(k, G, ns, persist_ctas, st);
+    }
+    return TQ_ERR_UNSUPPORTED;
+  }
   // persistent: tiles start at multiples of 64 tokens, so 4-token aligned rows keep
   // every TMA source 16-byte aligned; split-K: chunk starts as well
   const bool persist = a.tile_prefix != nullptr && a.batch <= kMaxPersistBatch && a.cache->capacity % 4 == 0 &&

@@ -474,12 +474,12 @@ tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads
   int s, chunk;
   tq::choose_splits(batch, heads_kv, max_len, splits, &s, &chunk);
   // prepared queries | decode-tile prefix over batches | partial records (split-K
-  // per (row, split), or the persistent kernel's kPersistGroups per (CTA + head) slot)
+  // per (row, split), or the persistent kernel's kPersistGroups x G per (CTA + KV head) slot)
   size_t qprep = (size_t)batch * heads_q * 2 * ctx->d * sizeof(float);
   size_t prefix = ((size_t)(batch + 1) * sizeof(int32_t) + 15) / 16 * 16;
   size_t split_parts = (size_t)batch * heads_q * s * tq::kPartialFloats * sizeof(float);
-  size_t persist_parts = (size_t)tq::kPersistGroups * ((size_t)ctx->num_sms + (size_t)batch * heads_kv) *
-                         tq::kPartialFloats * sizeof(float);
+  size_t persist_parts = (size_t)tq::kPersistGroups * (size_t)(heads_q / heads_kv) *
+                         ((size_t)ctx->num_sms + (size_t)batch * heads_kv) * tq::kPartialFloats * sizeof(float);
   *out = qprep + prefix + std::max(split_parts, persist_parts);
   return TQ_OK;
 }

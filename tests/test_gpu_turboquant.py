@@ -140,7 +140,7 @@ def test_dequantize_matches_oracle_reconstruction(scheme, n):
 
 @pytest.mark.parametrize("scheme,n", [("KQV", 4), ("KQV", 3), ("KQV", 2), ("QKQV", 4), ("QKQV", 2),
                                       ("KV", 4), ("KV", 2)])
-@pytest.mark.parametrize("G", [1, 4])
+@pytest.mark.parametrize("G", [1, 2, 4])
 @pytest.mark.parametrize("splits", [0, 1, 5])
 def test_decode_attention_matches_oracle(scheme, n, G, splits):
     B, Hkv = 2, 2
