@@ -313,7 +313,7 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (e == cudaSuccess) e = cudaMalloc((void **)&c->dparams, sizeof(tq::DevParams));
   if (e == cudaSuccess) e = cudaMemcpy(c->dparams, hp, sizeof(tq::DevParams), cudaMemcpyHostToDevice);
-  if (e == cudaSuccess && tq::launch_sketch_prep(c->dparams, nullptr) != TQ_OK) e = cudaErrorUnknown;
+  if (e == cudaSuccess && tq::launch_operand_prep(c->dparams, nullptr) != TQ_OK) e = cudaErrorUnknown;
   if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
   std::free(hp);
   if (e != cudaSuccess) {

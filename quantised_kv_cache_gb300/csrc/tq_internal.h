@@ -26,13 +26,15 @@ struct DevParams {
   float sketch[kD * kD];       // S, row-major [row][col]
   int error;                   // sticky device error word (a tq_status)
   int pad[3];
-  // S as fp16 hi + lo parts (hi = fp16(S), lo = fp16(S - hi)), rows in sign-record
-  // order, in the tensor-core K-major core-matrix layout (set on the device at
-  // context creation): [2][128 x 128] halves, 16-byte aligned
+  // tensor-core B operands in the K-major core-matrix layout, set on the device at
+  // context creation (16-byte aligned): the unnormalised Hadamard matrix times the
+  // seeded diagonal, H D, with its rows in code-storage order, and S as fp16 hi + lo parts (hi = fp16(S),
+  // lo = fp16(S - hi)) with rows and columns in storage order
+  uint16_t hadamard_b[kD * kD];
   uint16_t sketch_hl[2 * kD * kD];
 };
-// fills DevParams::sketch_hl from DevParams::sketch (stream order)
-int launch_sketch_prep(DevParams *dp, void *stream);
+// fills DevParams::hadamard_b and DevParams::sketch_hl (stream order)
+int launch_operand_prep(DevParams *dp, void *stream);
 
 struct Role {
   int bits = 0;
@@ -91,8 +93,9 @@ struct AppendArgs {
 int launch_append_tq(const AppendArgs &a, void *stream);
 // thread-per-vector append for vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise
 int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream);
-// thread-per-vector append with the QJL sketch on tcgen05 tensor cores; TQ_ERR_UNSUPPORTED otherwise
-int launch_append_qjl(const AppendArgs &a, const tq_ctx *ctx, void *stream);
+// thread-per-vector append of rotated vectors with the rotation and the QJL sketch on
+// tcgen05 tensor cores; TQ_ERR_UNSUPPORTED otherwise
+int launch_append_tc(const AppendArgs &a, const tq_ctx *ctx, void *stream);
 
 struct DecodeArgs {
   const tq_ctx *ctx;
