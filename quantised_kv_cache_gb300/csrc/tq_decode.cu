@@ -340,11 +340,10 @@ struct CombineArgs {
   int group = 1;  // query heads per KV head (persistent records hold `group` heads per slot)
 };
 
-// one CTA (128 threads, thread = coordinate) per (batch, query head)
-__global__ void __launch_bounds__(128) combine_tq_kernel(CombineArgs a) {
-  __shared__ float s_sig[kD];
-  __shared__ float s_o[kD];
-  const int row = blockIdx.x, i = threadIdx.x;
+// Merge the partial records of one query row: thread i (of 128) gets coordinate i
+// of the weighted value sum A and sign sum Sg, and every thread the weight L.
+__device__ __forceinline__ void merge_row(const CombineArgs &a, int row, int i, float &L_out, float &A_out,
+                                          float &Sg_out) {
   // the partial records of this row: split-K ones in a row, or the persistent
   // kernel's (cta, group) records of every CTA whose slice touched this head
   const float *base = a.partials + (size_t)row * a.splits * kPartialFloats;
@@ -376,48 +375,96 @@ __global__ void __launch_bounds__(128) combine_tq_kernel(CombineArgs a) {
     if (bnd(c) == bnd(c + 1)) return nullptr;  // an empty slice wrote nothing
     return a.partials + (((size_t)(c + unit) * ng + (k % ng)) * a.group + hh) * kPartialFloats;
   };
-  float M = -INFINITY;
-  for (int k = 0; k < nrec; ++k) {
-    const float *rec = record(k);
-    if (rec) M = fmaxf(M, __ldg(rec));
-  }
-  float L = 0.f, A = 0.f, Sg = 0.f;
+  // one pass with a running maximum (records are few; unrolled so their loads overlap)
+  float M = -INFINITY, L = 0.f, A = 0.f, Sg = 0.f;
+#pragma unroll 4
   for (int k = 0; k < nrec; ++k) {
     const float *rec = record(k);
     if (!rec) continue;
     const float ms = __ldg(rec);
-    const float e = (ms == -INFINITY) ? 0.f : __expf(ms - M);
-    L += __ldg(rec + 1) * e;
-    A += __ldg(rec + 2 + i) * e;
-    if (a.sketch_v) Sg += __ldg(rec + 2 + kD + i) * e;
+    const float l = __ldg(rec + 1), av = __ldg(rec + 2 + i), sv = a.sketch_v ? __ldg(rec + 2 + kD + i) : 0.f;
+    if (ms == -INFINITY) continue;
+    if (ms > M) {
+      const float sc = (M == -INFINITY) ? 0.f : __expf(M - ms);
+      L *= sc;
+      A *= sc;
+      Sg *= sc;
+      M = ms;
+    }
+    const float e = __expf(ms - M);
+    L += l * e;
+    A += av * e;
+    Sg += sv * e;
   }
+  L_out = L;
+  A_out = A;
+  Sg_out = Sg;
+}
+
+// Finish kCombineRows query rows per CTA (128 threads per row): merge each row's
+// partial records, add the sketch term (sqrt(pi/2)/m) S^T Sg with S staged in
+// shared memory, divide by L, and undo the rotation (inverse WHT, then D).
+constexpr int kCombineRows = 4;
+
+__global__ void __launch_bounds__(kCombineRows * 128) combine_tq_kernel(CombineArgs a) {
+  extern __shared__ float s_comb[];
+  float *s_sk = s_comb;                             // [128][128] S (sketch_v only)
+  float *s_sg = s_sk + (a.sketch_v ? kD * kD : 0);  // [rows][128]
+  float *s_o = s_sg + kCombineRows * kD;            // [rows][128]
+  const int tid = threadIdx.x, i = tid & (kD - 1), rr = tid >> 7;
+  const int nrows = a.batch * a.heads_q;
+  const int row = blockIdx.x * kCombineRows + rr;
+  if (a.sketch_v)
+    for (int e = tid; e < kD * kD / 4; e += blockDim.x)
+      reinterpret_cast<float4 *>(s_sk)[e] = __ldg(reinterpret_cast<const float4 *>(a.sketch) + e);
+  float L = 0.f, A = 0.f, Sg = 0.f;
+  if (row < nrows) merge_row(a, row, i, L, A, Sg);
+  s_sg[rr * kD + i] = Sg;
+  __syncthreads();
   float o = A;
   if (a.sketch_v) {
-    s_sig[i] = Sg;
-    __syncthreads();
-    float t = 0.f;
-    for (int k = 0; k < kD; ++k) t = fmaf(__ldg(a.sketch + k * kD + i), s_sig[k], t);
-    o += (kSqrtHalfPi / kD) * t;
+    const float *sg = s_sg + rr * kD;
+    float t0 = 0.f, t1 = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < kD; k += 2) {
+      t0 = fmaf(s_sk[k * kD + i], sg[k], t0);
+      t1 = fmaf(s_sk[(k + 1) * kD + i], sg[k + 1], t1);
+    }
+    o += (kSqrtHalfPi / kD) * (t0 + t1);
   }
   o = (L > 0.f) ? o / L : 0.f;
-  if (!a.rotate) {
-    a.out[(size_t)row * kD + i] = o;
-    return;
-  }
-  s_o[i] = o;
+  s_o[rr * kD + i] = o;
   __syncthreads();
-  if (i < 32) {
+  // rotate back: warp w of the row's four warps
+  const int warp = tid >> 5, lane = tid & 31;
+  if ((warp & 3) == 0 && row < nrows) {
     float v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = s_o[4 * i + j];
-    wht128(v, i);
-    float4 r;
-    r.x = v[0] * __ldg(a.diag + 4 * i + 0);
-    r.y = v[1] * __ldg(a.diag + 4 * i + 1);
-    r.z = v[2] * __ldg(a.diag + 4 * i + 2);
-    r.w = v[3] * __ldg(a.diag + 4 * i + 3);
-    reinterpret_cast<float4 *>(a.out + (size_t)row * kD)[i] = r;
+    for (int j = 0; j < 4; ++j) v[j] = s_o[rr * kD + 4 * lane + j];
+    if (a.rotate) {
+      wht128(v, lane);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] *= __ldg(a.diag + 4 * lane + j);
+    }
+    reinterpret_cast<float4 *>(a.out + (size_t)row * kD)[lane] = make_float4(v[0], v[1], v[2], v[3]);
   }
+}
+
+size_t combine_smem(const CombineArgs &a) {
+  return sizeof(float) * ((a.sketch_v ? kD * kD : 0) + 2 * kCombineRows * kD);
+}
+
+int launch_combine(const CombineArgs &a, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(combine_tq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(float) * (kD * kD + 2 * kCombineRows * kD))) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    attr_done = true;
+  }
+  const int rows = a.batch * a.heads_q;
+  combine_tq_kernel<<<(rows + kCombineRows - 1) / kCombineRows, kCombineRows * 128, combine_smem(a), st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- KIVI decode
@@ -645,10 +692,9 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
     if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
     CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                     ctx->dparams->diag, ctx->dparams->sketch, a.out,
-                    persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv, kPersistGroups};
+                    persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv, G == 1 ? 1 : kPersistGroups};
     cmb.group = G;
-    combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
-    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    return launch_combine(cmb, st);
   }
   if (r2 != TQ_ERR_UNSUPPORTED) return r2;
 
@@ -694,8 +740,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
 
   CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                   ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv, 1};
-  combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_combine(cmb, st);
 }
 
 int launch_decode_kivi(const DecodeArgs &a, void *stream) {
@@ -734,8 +779,7 @@ int launch_decode_kivi(const DecodeArgs &a, void *stream) {
   if (r != TQ_OK) return r;
   CombineArgs cmb{a.batch, a.heads_q, a.splits, 0, 0, a.partials, ctx->dparams->diag, ctx->dparams->sketch, a.out,
                   nullptr, 0, a.heads_kv, 1};
-  combine_tq_kernel<<<rows, 128, 0, st>>>(cmb);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_combine(cmb, st);
 }
 
 }  // namespace tq

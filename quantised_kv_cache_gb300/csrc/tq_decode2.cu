@@ -7,8 +7,7 @@
 //   key tables are rebuilt only where a slice crosses into the next head, and
 //   the TMA ring (up to 16 stages, ~140 KB in flight) keeps streaming across
 //   that boundary: each warp streams and refills its own quarter of a stage on
-//   its own mbarrier. Each 4-warp group writes one partial softmax record per
-//   (CTA, head) segment.
+//   its own mbarrier. Each (CTA, head) segment ends in one partial softmax record.
 // * decode2_g1_kernel -- split-K over a fixed (batch, head, chunk) grid, for
 //   batches too large for the persistent kernel's shared-memory prefix table.
 //
@@ -796,8 +795,8 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     park_warp<VQJL>(park + warp * kPartialFloats, lane, ws);
     __syncthreads();
     if (tid < 2 * kD) s_q[tid] = q_next;
-    merge_parked<4, VQJL>(park + grp * 4 * kPartialFloats, tid & 127,
-                          a.partials + ((size_t)(c + u) * kPersistGroups + grp) * kPartialFloats);
+    // one record per (CTA, head): all 16 warps merged
+    if (tid < kD) merge_parked<kPersistWarps, VQJL>(park, tid, a.partials + (size_t)(c + u) * kPartialFloats);
     __syncthreads();  // the table area is rebuilt next
     g = se;
   }
