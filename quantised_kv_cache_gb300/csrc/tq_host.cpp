@@ -315,8 +315,14 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
   if (e == cudaSuccess) e = cudaMemcpy(c->dparams, hp, sizeof(tq::DevParams), cudaMemcpyHostToDevice);
   if (e == cudaSuccess && tq::launch_operand_prep(c->dparams, nullptr) != TQ_OK) e = cudaErrorUnknown;
   if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags((cudaStream_t *)&c->side_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags((cudaEvent_t *)&c->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags((cudaEvent_t *)&c->ev_join, cudaEventDisableTiming);
   std::free(hp);
   if (e != cudaSuccess) {
+    if (c->ev_join) cudaEventDestroy((cudaEvent_t)c->ev_join);
+    if (c->ev_fork) cudaEventDestroy((cudaEvent_t)c->ev_fork);
+    if (c->side_stream) cudaStreamDestroy((cudaStream_t)c->side_stream);
     if (c->dparams) cudaFree(c->dparams);
     std::free(c->sketch);
     delete c;
@@ -328,6 +334,9 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
 
 void tq_destroy(tq_ctx *ctx) {
   if (!ctx) return;
+  if (ctx->ev_join) cudaEventDestroy((cudaEvent_t)ctx->ev_join);
+  if (ctx->ev_fork) cudaEventDestroy((cudaEvent_t)ctx->ev_fork);
+  if (ctx->side_stream) cudaStreamDestroy((cudaStream_t)ctx->side_stream);
   if (ctx->dparams) cudaFree(ctx->dparams);
   std::free(ctx->sketch);
   delete ctx;
@@ -453,9 +462,18 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.role = ctx->k;
   a.centroids = ctx->dparams->k_centroids;
   a.bounds = ctx->dparams->k_bounds;
-  s = (tq_status)tq::launch_append_tq(a, stream);
-  if (s != TQ_OK) return s;
-  // V
+  // K on the library's side stream, V on the caller's, joined before returning
+  cudaStream_t st = (cudaStream_t)stream, side = (cudaStream_t)ctx->side_stream;
+  const bool fork = side && cudaEventRecord((cudaEvent_t)ctx->ev_fork, st) == cudaSuccess &&
+                    cudaStreamWaitEvent(side, (cudaEvent_t)ctx->ev_fork, 0) == cudaSuccess;
+  s = (tq_status)tq::launch_append_tq(a, fork ? (void *)side : stream);
+  const bool recorded = fork && cudaEventRecord((cudaEvent_t)ctx->ev_join, side) == cudaSuccess;
+  if (fork && !recorded && s == TQ_OK) s = TQ_ERR_CUDA;
+  if (s != TQ_OK) {
+    if (recorded) cudaStreamWaitEvent(st, (cudaEvent_t)ctx->ev_join, 0);
+    return s;
+  }
+  // V on the caller's stream, then the caller's stream waits for K
   a.x = d_v;
   a.codes = cache->v_codes;
   a.norms = cache->v_norm;
@@ -464,7 +482,10 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.role = ctx->v;
   a.centroids = ctx->dparams->v_centroids;
   a.bounds = ctx->dparams->v_bounds;
-  return (tq_status)tq::launch_append_tq(a, stream);
+  s = (tq_status)tq::launch_append_tq(a, stream);
+  if (recorded && cudaStreamWaitEvent(st, (cudaEvent_t)ctx->ev_join, 0) != cudaSuccess && s == TQ_OK)
+    s = TQ_ERR_CUDA;
+  return s;
 }
 
 tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len, int splits,

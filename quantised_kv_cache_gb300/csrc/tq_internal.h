@@ -66,6 +66,9 @@ struct tq_ctx {
   float *sketch = nullptr;  // host, d*d
   float sketch_rowmax = 0.f;  // an upper bound of max_j ||S_j||
   tq::DevParams *dparams = nullptr;
+  // a library-owned stream and two events: the key and value appends of one call
+  // run concurrently (fork / join on the caller's stream)
+  void *side_stream = nullptr, *ev_fork = nullptr, *ev_join = nullptr;
   // optional CUDA events recorded around the decode / append kernels
   void *prof_decode_start = nullptr, *prof_decode_stop = nullptr;
   void *prof_append_start = nullptr, *prof_append_stop = nullptr;
