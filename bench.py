@@ -32,6 +32,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "compressed-KV decode attention GB/s and % of HBM peak; append-quantise tokens/s"
 CAP = 8192
+# kernels of one decode step: the append of the step's keys and values (one launch for
+# this few vectors), query prep, decode attention, combine
+LAUNCHES_PER_STEP = 4
 
 
 def peaks():
@@ -384,23 +387,30 @@ def main():
     if dist is not None:
         dist.barrier()
     K = args.steps
+    # the steps as a user runs them: the library's kernels follow one another with
+    # programmatic overlap, so no event sits between them here
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        step(i)
+    t_stop.record()
+    torch.cuda.synchronize()
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_stop), dist, dev)
+    ms_step = elapsed_ms / K
+    value = job_throughput(step_bytes * K, world, elapsed_ms / 1e3) / 1e9
+    # the same K steps again with events around every decode kernel launch (on the
+    # library's stream) for the kernel's own duration
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for a, b in dec_ev:  # torch creates the CUDA event on first record; the library needs the handle
         a.record()
         b.record()
     torch.cuda.synchronize()
-    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record()
     for i in range(K):
         tq.tq_set_profile_events(ctx.handle, dec_ev[i][0], dec_ev[i][1])
         step(i)
-    t_stop.record()
     torch.cuda.synchronize()
     tq.tq_set_profile_events(ctx.handle)
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_stop), dist, dev)
-    ms_step = elapsed_ms / K
     dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
-    value = job_throughput(step_bytes * K, world, elapsed_ms / 1e3) / 1e9
     assert tq.tq_get_device_error(ctx.handle) == 0
 
     # ---------------- end to end through the ABI with host buffers
@@ -454,7 +464,7 @@ def main():
                                 "what": "bulk re-quantise of all 8192 tokens x 512 heads from bf16 K/V"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": 1e3 * e2e_s / K},
-            "gpu_launches": 5 * K,
+            "gpu_launches": LAUNCHES_PER_STEP * K,
             "clocks": clk,
         }
         if not args.no_cpu_baseline:

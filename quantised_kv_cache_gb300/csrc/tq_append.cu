@@ -233,7 +233,9 @@ int dispatch_bits(int bits, const AppendKernelArgs &k, long long total, cudaStre
 
 int launch_append_tq(const AppendArgs &a, void *stream) {
   if (a.ctx) {
-    int r = launch_append_tc(a, a.ctx, stream);  // rotated roles
+    int r = launch_append_bulk(a, a.ctx, stream);  // rotated roles, bf16 input
+    if (r != TQ_ERR_UNSUPPORTED) return r;
+    r = launch_append_tc(a, a.ctx, stream);  // rotated roles
     if (r != TQ_ERR_UNSUPPORTED) return r;
     r = launch_append2(a, a.ctx, stream);  // unrotated roles
     if (r != TQ_ERR_UNSUPPORTED) return r;

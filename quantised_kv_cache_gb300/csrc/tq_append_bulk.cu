@@ -1,0 +1,641 @@
+// Bulk append-quantise of bf16 vectors on the rotated roles (keys and values of
+// KQV and QKQV): a warp-specialised persistent kernel, one CTA per SM.
+//
+// "Statistical Inference and Quality Measures of KV Cache Quantisations
+// Inspired by TurboQuant", technical summary, "Quantisation schemes" (norm,
+// randomised Walsh-Hadamard rotation, scalar Lloyd-Max codes; the (n-1)-bit
+// vectors keep a 1-bit QJL sketch of their residual) and "Main contribution 1"
+// (sign(S r) and rho = ||x|| ||r||). "KVQuant++", "Fast codebook lookup": a
+// code is the count of boundaries at or below the coordinate.
+//
+// Per tile of 128 vectors:
+// * one control thread (warp 0) loads the tile with 16 tensor-map copies of
+//   8 x 128 bf16 boxes, which land exactly as the K-major core-matrix layout of
+//   the MMA's A operand (rows past the end read as zeros), into a ring of
+//   stages, and issues y = x (H D)^T on the tensor cores (bf16 inputs are
+//   exact, the Hadamard-times-diagonal operand is +-1; fp32 accumulate in
+//   tensor memory, accumulator column n = the coordinate stored at code offset
+//   n); for sketched vectors, once the residuals are in tensor memory, it
+//   issues z = S r in three fp16 passes (hi x hi, lo x hi, hi x lo) into the
+//   columns y used;
+// * two groups of four epilogue warps take alternate tiles (one thread per
+//   vector = tensor-memory lane), so one group computes while the other's MMAs
+//   run: ||y|| = sqrt(d) ||x|| gives the norm and the boundary scale, codes are
+//   counted against the boundaries times ||y|| (no division), the residual
+//   r = y / ||y|| - c[code], scaled by 2^10 and split into fp16 hi + lo, is
+//   stored to tensor memory as the sketch MMA's A operand, and signs come out
+//   of z 32 at a time. Signs within a bound on the dropped terms and the
+//   accumulation error are recomputed in fp32 from the residual rebuilt from
+//   its hi + lo parts, so a sign can differ from exact arithmetic only where
+//   |z| is about 1e-6 or less.
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "tq_ptx.cuh"
+#include "tq_tcgen05.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kTV = 128;                      // vectors per tile = MMA M
+constexpr int kTileBytes = kTV * kD * 2;      // one bf16 tile (32 KB)
+constexpr int kOpB = kD * kD * 2;             // one 16-bit 128 x 128 operand
+constexpr int kEpiWarps = 8;                  // two groups of four
+constexpr int kBulkThreads = 32 * (1 + kEpiWarps);
+constexpr float kRScaleB = 1024.f;            // residual scale for the fp16 split (|r| < 2)
+
+template <bool QJL>
+struct BulkGeo {
+  static constexpr int NS = QJL ? 3 : 4;                      // x stages
+  static constexpr int x0 = 0;
+  static constexpr int hd = NS * kTileBytes;                  // H D, bf16
+  static constexpr int sk = hd + kOpB;                        // S hi, S lo (fp16)
+  static constexpr int bar = sk + (QJL ? 2 * kOpB : 0);       // barriers
+  static constexpr int nbar = 2 * NS + 10;
+  static constexpr int total = bar + nbar * 8 + 16;
+  static constexpr uint32_t tcols = QJL ? 512u : 256u;        // two slots
+  static constexpr uint32_t slot_cols = QJL ? 256u : 128u;    // Y / Z | R hi | R lo
+};
+
+struct BulkArgs {
+  int batch, heads, n_new, capacity;
+  long long total;
+  const int32_t *seq_lens;
+  uint8_t *codes;
+  float *norms;
+  uint8_t *signs;
+  float *rnorms;
+  const float *sketch_perm;  // S in storage order, fp32 (rare-path exact signs)
+  const uint16_t *hd_bf;   // DevParams::hadamard_bf
+  const uint16_t *s_hl;    // DevParams::sketch_hl
+  float sketch_rowmax;
+  int *error;
+  float bounds[kMaxLevels];
+  float centroids[kMaxLevels];
+};
+
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// D (TMEM) (+)= A (shared, descriptor) x B (shared, descriptor); one thread.
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// tcgen05.st of 16 columns without its wait, and the wait, which names the stored
+// registers so that none of them is overwritten before the stores have read them
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile("tcgen05.wait::st.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                 "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]),
+                 "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]),
+                 "+r"(b[14]), "+r"(b[15])
+               :
+               : "memory");
+}
+
+// Code of one coordinate y (0 .. 2^BITS - 1): with P the positive boundaries
+// times ||y|| (P[k] = b[L/2 + k] ||y||), the magnitude index counts the P[k] <=
+// |y| by binary search, then code = (L/2 + magnitude) for y >= 0 and its
+// mirror L - 1 - that for y < 0 (one XOR). For the residual, cneg gets
+// -c[code] 2^10 from C[q] = c[L/2 + q] 2^10 (the codebook is symmetric).
+template <int BITS, bool QJL>
+__device__ __forceinline__ uint32_t encode1(float y, const float (&P)[(1 << (BITS - 1)) > 1 ? (1 << (BITS - 1)) - 1 : 1],
+                                            const float (&C)[1 << (BITS - 1)], float &cneg) {
+  constexpr uint32_t L = 1u << BITS;
+  const float a = fabsf(y);
+  const uint32_t s = (uint32_t)(__float_as_int(y + 0.f) >> 31);  // all ones when y < 0 (y + 0 maps -0 to +0)
+  uint32_t m;
+  float cm = 0.f;
+  if constexpr (BITS == 1) {
+    m = 1u;
+    cm = C[0];
+  } else if constexpr (BITS == 2) {
+    const bool p1 = a >= P[0];
+    m = p1 ? 3u : 2u;
+    if (QJL) cm = p1 ? C[1] : C[0];
+  } else if constexpr (BITS == 3) {
+    const bool p2 = a >= P[1];
+    const bool p1 = a >= (p2 ? P[2] : P[0]);
+    m = (p2 ? 6u : 4u) + (p1 ? 1u : 0u);
+    if (QJL) cm = p2 ? (p1 ? C[3] : C[2]) : (p1 ? C[1] : C[0]);
+  } else {
+    const bool p4 = a >= P[3];
+    const bool p2 = a >= (p4 ? P[5] : P[1]);
+    const bool p1 = a >= (p4 ? (p2 ? P[6] : P[4]) : (p2 ? P[2] : P[0]));
+    m = (p4 ? 12u : 8u) + (p2 ? 2u : 0u) + (p1 ? 1u : 0u);
+    if (QJL) cm = C[(p4 ? 4 : 0) + (p2 ? 2 : 0) + (p1 ? 1 : 0)];
+  }
+  if (QJL) cneg = __int_as_float(__float_as_int(cm) ^ (int)(~s & 0x80000000u));
+  return m ^ (s & (L - 1u));
+}
+
+// tcgen05.ld without its wait, and the wait, which names the loaded registers so
+// that no use of them can be scheduled before it
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                 "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                 "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                 "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void split_pair_b(float a, float b, uint32_t &hi, uint32_t &lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 f = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];\n\ttcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
+__device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
+// Rare path, run by whole warps until no lane has a flagged sign left: each
+// round every flagged lane recomputes one sign in fp32 from its residual,
+// rebuilt from the hi + lo parts at r_hi / r_hi + 64 (storage order), against
+// S in storage order (sperm[n][k] = S[coordinate of n][coordinate of k]).
+// flag / sw hold the four sign words.
+__device__ __forceinline__ void certify_rounds(uint32_t r_hi, const float *sperm, uint32_t (&flag)[4],
+                                               uint32_t (&sw)[4]) {
+  while (__any_sync(kFull, (flag[0] | flag[1] | flag[2] | flag[3]) != 0u)) {
+    const bool has = (flag[0] | flag[1] | flag[2] | flag[3]) != 0u;
+    const int c = flag[0] ? 0 : flag[1] ? 1 : flag[2] ? 2 : 3;
+    const uint32_t fw = c == 0 ? flag[0] : c == 1 ? flag[1] : c == 2 ? flag[2] : flag[3];
+    const int bit = has ? __ffs(fw) - 1 : 0;
+    const float4 *row = reinterpret_cast<const float4 *>(sperm + (size_t)(32 * c + bit) * kD);
+    // four partial sums: a short dependency chain (the rounding order is immaterial
+    // at this precision)
+    float z4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int chunk = 0; chunk < 4; ++chunk) {
+      uint32_t hi[16], lo[16];
+      tmem_ld16(r_hi + 16 * chunk, hi);  // warp-collective: every lane takes part
+      tmem_ld16(r_hi + 64 + 16 * chunk, lo);
+      if (has) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 sv = __ldg(row + 8 * chunk + q);
+          const uint32_t h0 = hi[2 * q], l0 = lo[2 * q], h1 = hi[2 * q + 1], l1 = lo[2 * q + 1];
+          z4[0] = fmaf(sv.x, (half_lo(h0) + half_lo(l0)) * (1.f / kRScaleB), z4[0]);
+          z4[1] = fmaf(sv.y, (half_hi(h0) + half_hi(l0)) * (1.f / kRScaleB), z4[1]);
+          z4[2] = fmaf(sv.z, (half_lo(h1) + half_lo(l1)) * (1.f / kRScaleB), z4[2]);
+          z4[3] = fmaf(sv.w, (half_hi(h1) + half_hi(l1)) * (1.f / kRScaleB), z4[3]);
+        }
+      }
+    }
+    const float zz = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+    if (has) {
+      const uint32_t m = 1u << bit;
+      const uint32_t v = (zz >= 0.f) ? m : 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q == c) {
+          flag[q] &= ~m;
+          sw[q] = (sw[q] & ~m) | v;
+        }
+      }
+    }
+  }
+}
+
+template <int BITS, bool QJL>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    append_bulk_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ BulkArgs a) {
+  using G = BulkGeo<QJL>;
+  constexpr int NS = G::NS;
+  constexpr int L = 1 << BITS, H = L / 2 - 1;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + G::bar);
+  uint64_t *x_full = bars, *x_empty = bars + NS;
+  uint64_t *y_full = bars + 2 * NS, *r_full = y_full + 2, *z_full = r_full + 2, *s_empty = z_full + 2;
+  uint64_t *op_bar = s_empty + 2, *drain = op_bar + 1;
+  uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + G::nbar);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(s_taddr + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long ntiles = (a.total + kTV - 1) / kTV;
+  // this CTA's tiles: blockIdx.x + k gridDim.x, k = 0 .. nloc - 1
+  const long long nloc = ntiles > blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&x_full[s], 1);
+      mbar_init(&x_empty[s], 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&y_full[g], 1);
+      mbar_init(&r_full[g], 4);
+      mbar_init(&z_full[g], 1);
+      mbar_init(&s_empty[g], 4);
+    }
+    mbar_init(op_bar, 1);
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    mbar_fence_init();
+    mbar_arrive_expect_tx(op_bar, (QJL ? 3 : 1) * kOpB);
+    tma_load_1d(smem + G::hd, a.hd_bf, kOpB, op_bar);
+    if (QJL) {
+      tma_load_1d(smem + G::sk, a.s_hl, kOpB, op_bar);
+      tma_load_1d(smem + G::sk + kOpB, a.s_hl + kD * kD, kOpB, op_bar);
+    }
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(s_taddr), G::tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = *s_taddr;
+
+  if (warp == 0) {
+    // ---------------- control thread: tile loads (tensor-map TMA) and MMA issue
+    if (lane == 0) {
+      auto load = [&](long long j) {  // local tile j into stage j % NS (the stage is free)
+        const int s = (int)(j % NS);
+        mbar_arrive_expect_tx(&x_full[s], kTileBytes);
+        const int row0 = (int)((blockIdx.x + j * gridDim.x) * kTV);
+#pragma unroll 1
+        for (int kb = 0; kb < kD / 8; ++kb)
+          tma_load_2d(smem + G::x0 + s * kTileBytes + kb * 2048, &xmap, 8 * kb, row0, &x_full[s]);
+      };
+      long long loaded = 0;
+      for (; loaded < NS && loaded < nloc; ++loaded) load(loaded);
+      bool ok = mbar_wait_bounded(op_bar, 0, a.error);
+      tc_fence_after_sync();
+      constexpr uint32_t id_rot = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
+                                  ((uint32_t)(128 >> 4) << 24);  // bf16 x bf16 -> f32, M = N = 128
+      constexpr uint32_t id_sk = tc_idesc_f16_f32(128, 128);     // fp16 x fp16 -> f32
+      const uint32_t sa_x = smem_u32(smem + G::x0), sa_h = smem_u32(smem + G::hd), sa_s = smem_u32(smem + G::sk);
+      auto sketch = [&](long long k) -> bool {
+        const int g = (int)(k & 1);
+        if (!mbar_wait_bounded(&r_full[g], (uint32_t)((k >> 1) & 1), a.error)) return false;
+        tc_fence_after_sync();
+        const uint32_t d = tbase + G::slot_cols * g;
+#pragma unroll 1
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint64_t dh = tc_sdesc_kmajor(sa_s + 256 * ks, 128, 2048);
+          const uint64_t dl = tc_sdesc_kmajor(sa_s + kOpB + 256 * ks, 128, 2048);
+          tc_mma_f16_ts(d, d + 128 + 8 * ks, dh, id_sk, ks > 0);
+          tc_mma_f16_ts(d, d + 192 + 8 * ks, dh, id_sk, true);
+          tc_mma_f16_ts(d, d + 128 + 8 * ks, dl, id_sk, true);
+        }
+        tc_commit(smem_u32(&z_full[g]));
+        return true;
+      };
+      long long k = 0;
+      for (; ok && k < nloc && !*s_abort; ++k) {
+        const int g = (int)(k & 1), s = (int)(k % NS);
+        if (k >= 2 && !mbar_wait_bounded(&s_empty[g], (uint32_t)(((k >> 1) - 1) & 1), a.error)) ok = false;
+        if (ok && !mbar_wait_bounded(&x_full[s], (uint32_t)((k / NS) & 1), a.error)) ok = false;
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t d = tbase + G::slot_cols * g;
+#pragma unroll 1
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint64_t da = tc_sdesc_kmajor(sa_x + s * kTileBytes + 4096 * ks, 2048, 128);
+          const uint64_t db = tc_sdesc_kmajor(sa_h + 256 * ks, 128, 2048);
+          tc_mma_ss(d, da, db, id_rot, ks > 0);
+        }
+        tc_commit(smem_u32(&x_empty[s]));
+        tc_commit(smem_u32(&y_full[g]));
+        // refill the stage tile k - 1 used (its rotation was issued one round ago)
+        if (k >= 1 && loaded < nloc) {
+          const int sp = (int)((k - 1) % NS);
+          if (!mbar_wait_bounded(&x_empty[sp], (uint32_t)(((k - 1) / NS) & 1), a.error)) {
+            ok = false;
+            break;
+          }
+          load(loaded++);
+        }
+        if (QJL && k >= 1 && !sketch(k - 1)) ok = false;
+      }
+      if (ok && QJL && k >= 1 && !*s_abort) ok = sketch(k - 1);
+      if (!ok) *s_abort = 1;
+      // copies that landed for nobody (an abort) must not outlive the CTA
+      for (long long j = k; j < loaded; ++j) mbar_wait_bounded(&x_full[j % NS], (uint32_t)((j / NS) & 1), a.error);
+    }
+  } else {
+    // ---------------- epilogue: group g (four warps, one thread per vector) takes local tiles k = g (mod 2)
+    const int g = (warp - 1) >> 2, qd = warp & 3;
+    const int row = 32 * qd + lane;  // vector within the tile = TMEM lane
+    const uint32_t tslot = tbase + G::slot_cols * g + ((uint32_t)(32 * qd) << 16);
+    float P[H > 0 ? H : 1], CP[H + 1];
+#pragma unroll
+    for (int q = 0; q <= H; ++q) CP[q] = a.centroids[L / 2 + q] * kRScaleB;
+    const float smax = a.sketch_rowmax;
+    for (long long k = g; k < nloc; k += 2) {
+      const int par = (int)((k >> 1) & 1);
+      const long long tile = blockIdx.x + k * gridDim.x;
+      const long long vec = tile * kTV + row;
+      long long slot = -1;
+      if (vec < a.total) {
+        const int t = (int)(vec % a.n_new);
+        const long long bh = vec / a.n_new;
+        const int b = (int)(bh / a.heads);
+        const int len = __ldg(a.seq_lens + b);
+        if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.capacity + len + t;
+        else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
+      }
+      if (*s_abort || !__all_sync(kFull, mbar_wait_bounded(&y_full[g], (uint32_t)par, a.error))) {
+        *s_abort = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      // pass 1: ||y||^2 = d ||x||^2 (each chunk's load overlaps the previous chunk's sums)
+      float ss = 0.f;
+      {
+        uint32_t ya[32], yb[32];
+        __syncwarp();
+        tmem_ld32_async(tslot, ya);
+        tmem_ld_wait(ya);
+#pragma unroll 1
+        for (int c = 0; c < 4; c += 2) {
+          tmem_ld32_async(tslot + 32 * (c + 1), yb);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(ya[j]), __uint_as_float(ya[j]), ss);
+          tmem_ld_wait(yb);
+          if (c + 2 < 4) tmem_ld32_async(tslot + 32 * (c + 2), ya);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ss = fmaf(__uint_as_float(yb[j]), __uint_as_float(yb[j]), ss);
+          if (c + 2 < 4) tmem_ld_wait(ya);
+        }
+      }
+      const float sv = ss > 0.f ? sqrtf(ss) : 1.f;  // sqrt(d) ||x||, the boundary scale
+      const float inv = ss > 0.f ? kRScaleB / sv : 0.f;
+#pragma unroll
+      for (int j = 0; j < H; ++j) P[j] = a.bounds[L / 2 + j] * sv;
+      // pass 2: codes and residuals of chunk c (32 storage offsets)
+      float rr = 0.f;
+      uint32_t *crec = reinterpret_cast<uint32_t *>(a.codes + (slot >= 0 ? slot : 0) * (BITS * kD / 8));
+      auto chunk_codes = [&](uint32_t (&yz)[32], int c) {
+        uint32_t word[BITS];
+#pragma unroll
+        for (int w = 0; w < BITS; ++w) word[w] = 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float cneg;
+          const uint32_t code = encode1<BITS, QJL>(__uint_as_float(yz[j]), P, CP, cneg);
+          const int off = BITS * j;
+          word[off >> 5] |= code << (off & 31);
+          if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= code >> (32 - (off & 31));
+          if (QJL) {
+            const float r = fmaf(__uint_as_float(yz[j]), inv, cneg);  // r 2^10
+            rr = fmaf(r, r, rr);
+            yz[j] = __float_as_uint(r);
+          }
+        }
+        if (slot >= 0) {
+#pragma unroll
+          for (int w = 0; w < BITS; ++w) crec[BITS * c + w] = word[w];
+        }
+        if (QJL) {
+          uint32_t rh[16], rl[16];
+#pragma unroll
+          for (int p = 0; p < 16; ++p)
+            split_pair_b(__uint_as_float(yz[2 * p]), __uint_as_float(yz[2 * p + 1]), rh[p], rl[p]);
+          __syncwarp();
+          tmem_st16_async(tslot + 128 + 16 * c, rh);
+          tmem_st16_async(tslot + 192 + 16 * c, rl);
+          tmem_st_wait(rh, rl);
+        }
+      };
+      {
+        uint32_t ya[32], yb[32];
+        __syncwarp();
+        tmem_ld32_async(tslot, ya);
+        tmem_ld_wait(ya);
+#pragma unroll 1
+        for (int c = 0; c < 4; c += 2) {
+          tmem_ld32_async(tslot + 32 * (c + 1), yb);
+          chunk_codes(ya, c);
+          tmem_ld_wait(yb);
+          if (c + 2 < 4) tmem_ld32_async(tslot + 32 * (c + 2), ya);
+          chunk_codes(yb, c + 1);
+          if (c + 2 < 4) tmem_ld_wait(ya);
+        }
+      }
+      const float nu = (ss > 0.f) ? sv * 0.08838834764831845f : 0.f;  // ||y|| / sqrt(d)
+      if (slot >= 0) a.norms[slot] = nu;
+      if constexpr (QJL) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r_full[g]);
+        if (!__all_sync(kFull, mbar_wait_bounded(&z_full[g], (uint32_t)par, a.error))) {
+          *s_abort = 1;
+          break;
+        }
+        tc_fence_after_sync();
+        // dropped terms + accumulation error of z' = 2^10 S r
+        const float E = 0x1p-16f * smax * sqrtf(rr) + 0x1p-20f * smax;
+        uint32_t sw[4], flag[4];
+        // sign bits by funnel shifts (bit j of a word <- the sign bit of z[j]; inverted at
+        // the end, so z = -0 reads as negative, but |z| = 0 is flagged and recomputed)
+        auto chunk_signs = [&](const uint32_t (&z)[32], uint32_t &wv, uint32_t &fv) {
+          uint32_t ns = 0u, nf = 0u;
+#pragma unroll
+          for (int bit = 31; bit >= 0; --bit) {
+            ns = __funnelshift_l(z[bit], ns, 1);
+            nf = __funnelshift_l(__float_as_uint(E - fabsf(__uint_as_float(z[bit]))), nf, 1);
+          }
+          wv = ~ns;  // z >= 0
+          fv = ~nf;  // |z| <= E
+        };
+        {
+          uint32_t za[32], zb[32];
+          __syncwarp();
+          tmem_ld32_async(tslot, za);
+          tmem_ld_wait(za);
+          tmem_ld32_async(tslot + 32, zb);
+          chunk_signs(za, sw[0], flag[0]);
+          tmem_ld_wait(zb);
+          tmem_ld32_async(tslot + 64, za);
+          chunk_signs(zb, sw[1], flag[1]);
+          tmem_ld_wait(za);
+          tmem_ld32_async(tslot + 96, zb);
+          chunk_signs(za, sw[2], flag[2]);
+          tmem_ld_wait(zb);
+          chunk_signs(zb, sw[3], flag[3]);
+        }
+        certify_rounds(tslot + 128, a.sketch_perm, flag, sw);
+        if (slot >= 0) {
+          if (ss == 0.f) sw[0] = sw[1] = sw[2] = sw[3] = 0xffffffffu;  // a zero vector: every sign set, rho = 0
+          *reinterpret_cast<uint4 *>(a.signs + slot * (kD / 8)) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+          a.rnorms[slot] = (ss > 0.f) ? nu * sqrtf(rr) * (1.f / kRScaleB) : 0.f;
+        }
+      }
+      // this warp is done with the slot's tensor memory
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[g]);
+    }
+  }
+
+  // ---------------- teardown: no tensor-core work in flight, then free TMEM
+  __syncthreads();
+  if (warp == 0) {
+    if (*s_abort && lane == 0) {  // a last, bounded chance for MMAs still running
+      tc_commit(smem_u32(drain));
+      mbar_wait_bounded(drain, 0, a.error);
+    }
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, G::tcols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+int g_sms_bulk = 0;
+
+template <int BITS, bool QJL>
+int go_bulk(const CUtensorMap &map, const BulkArgs &k, long long ntiles, cudaStream_t st) {
+  if (g_sms_bulk == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms_bulk, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms_bulk <= 0) g_sms_bulk = 152;
+  }
+  using G = BulkGeo<QJL>;
+  auto fn = append_bulk_kernel<BITS, QJL>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, G::total) != cudaSuccess)
+      return TQ_ERR_CUDA;
+    attr_done = true;
+  }
+  long long blocks = ntiles < g_sms_bulk ? ntiles : g_sms_bulk;
+  if (blocks < 1) blocks = 1;
+  fn<<<(unsigned)blocks, kBulkThreads, G::total, st>>>(map, k);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+}  // namespace
+
+// Bulk append of bf16 vectors on rotated roles; TQ_ERR_UNSUPPORTED when it does not apply.
+int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
+  if (!a.role.rotate || a.dtype != TQ_BF16 || a.role.bits < 1 || a.role.bits > 4 || (a.role.qjl && a.role.bits > 3))
+    return TQ_ERR_UNSUPPORTED;
+  const long long total = (long long)a.batch * a.heads * a.n_new;
+  if (total < 2LL * kTV || total > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return TQ_ERR_UNSUPPORTED;
+  // x as a [total][128] bf16 matrix; a box of 8 elements x 128 rows is one column
+  // of 16 core matrices of the MMA's K-major A operand
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)total};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {8, (cuuint32_t)kTV};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.x), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return TQ_ERR_UNSUPPORTED;
+  BulkArgs k{};
+  k.batch = a.batch;
+  k.heads = a.heads;
+  k.n_new = a.n_new;
+  k.capacity = a.capacity;
+  k.total = total;
+  k.seq_lens = a.seq_lens;
+  k.codes = a.codes;
+  k.norms = a.norms;
+  k.signs = a.signs;
+  k.rnorms = a.rnorms;
+  k.sketch_perm = ctx->dparams->sketch_perm;
+  k.hd_bf = ctx->dparams->hadamard_bf;
+  k.s_hl = ctx->dparams->sketch_hl;
+  k.sketch_rowmax = ctx->sketch_rowmax;
+  k.error = a.error;
+  const bool is_k = a.centroids == ctx->dparams->k_centroids;
+  const float *bsrc = is_k ? ctx->k_bounds : ctx->v_bounds;
+  const float *csrc = is_k ? ctx->k_centroids : ctx->v_centroids;
+  for (int i = 0; i < (1 << a.role.bits) - 1; ++i) k.bounds[i] = bsrc[i];
+  for (int i = 0; i < (1 << a.role.bits); ++i) k.centroids[i] = csrc[i];
+  const long long ntiles = (total + kTV - 1) / kTV;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (a.role.qjl) {
+    switch (a.role.bits) {
+      case 1: return go_bulk<1, true>(map, k, ntiles, st);
+      case 2: return go_bulk<2, true>(map, k, ntiles, st);
+      case 3: return go_bulk<3, true>(map, k, ntiles, st);
+      default: return TQ_ERR_UNSUPPORTED;
+    }
+  }
+  switch (a.role.bits) {
+    case 1: return go_bulk<1, false>(map, k, ntiles, st);
+    case 2: return go_bulk<2, false>(map, k, ntiles, st);
+    case 3: return go_bulk<3, false>(map, k, ntiles, st);
+    case 4: return go_bulk<4, false>(map, k, ntiles, st);
+    default: return TQ_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace tq

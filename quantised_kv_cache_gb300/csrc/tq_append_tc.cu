@@ -32,6 +32,7 @@
 //    its hi + lo parts (2^-22 relative), so a sign can differ from exact
 //    arithmetic only where |z| is about 1e-6 or less.
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "tq_ptx.cuh"
@@ -409,7 +410,10 @@ __global__ void __launch_bounds__(128) operand_prep_kernel(DevParams *dp) {
   for (int k = 0; k < kD; ++k) {
     const float h = ((__popc(i & k) & 1) ? -1.f : 1.f) * dp->diag[k];  // (H D)[i][k]
     *reinterpret_cast<__half *>(bh + core_off(n, k)) = __float2half_rn(h);
+    *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<unsigned char *>(dp->hadamard_bf) + core_off(n, k)) =
+        __float2bfloat16_rn(h);
     const float s = dp->sketch[i * kD + slot_coord_tc(k)];
+    dp->sketch_perm[n * kD + k] = s;
     const __half sh = __float2half_rn(s);
     *reinterpret_cast<__half *>(shi + core_off(n, k)) = sh;
     *reinterpret_cast<__half *>(slo + core_off(n, k)) = __float2half_rn(s - __half2float(sh));

@@ -21,6 +21,7 @@
 #include <cuda_fp16.h>
 
 #include "tq_device.cuh"
+#include "tq_ptx.cuh"
 
 namespace tq {
 namespace {
@@ -72,6 +73,7 @@ __device__ void tile_prefix_block(const PrepArgs &a) {
 // one warp per (batch, query head)
 __global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
   __shared__ float s_q[4][kD];
+  pdl_trigger();  // the decode kernel may start its prologue now
   if (a.tile_prefix && blockIdx.x == 0) tile_prefix_block(a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
@@ -338,6 +340,7 @@ struct CombineArgs {
   const int32_t *tile_prefix;
   int persist_ctas, heads_kv, persist_groups;
   int group = 1;  // query heads per KV head (persistent records hold `group` heads per slot)
+  int *error = nullptr;
 };
 
 // Merge the partial records of one query row: thread i (of 128) gets coordinate i
@@ -407,22 +410,28 @@ __device__ __forceinline__ void merge_row(const CombineArgs &a, int row, int i, 
 constexpr int kCombineRows = 4;
 
 __global__ void __launch_bounds__(kCombineRows * 128) combine_tq_kernel(CombineArgs a) {
-  extern __shared__ float s_comb[];
+  extern __shared__ __align__(16) float s_comb[];
+  __shared__ uint64_t s_bar;
   float *s_sk = s_comb;                             // [128][128] S (sketch_v only)
   float *s_sg = s_sk + (a.sketch_v ? kD * kD : 0);  // [rows][128]
   float *s_o = s_sg + kCombineRows * kD;            // [rows][128]
   const int tid = threadIdx.x, i = tid & (kD - 1), rr = tid >> 7;
   const int nrows = a.batch * a.heads_q;
   const int row = blockIdx.x * kCombineRows + rr;
-  if (a.sketch_v)
-    for (int e = tid; e < kD * kD / 4; e += blockDim.x)
-      reinterpret_cast<float4 *>(s_sk)[e] = __ldg(reinterpret_cast<const float4 *>(a.sketch) + e);
+  // S (a context constant) streams into shared memory while the records are merged
+  if (a.sketch_v && tid == 0) {
+    mbar_init(&s_bar, 1);
+    mbar_fence_init();
+    mbar_arrive_expect_tx(&s_bar, kD * kD * sizeof(float));
+    tma_load_1d(s_sk, a.sketch, kD * kD * sizeof(float), &s_bar);
+  }
+  pdl_wait();  // the partial records come from the decode kernel before
   float L = 0.f, A = 0.f, Sg = 0.f;
   if (row < nrows) merge_row(a, row, i, L, A, Sg);
   s_sg[rr * kD + i] = Sg;
   __syncthreads();
   float o = A;
-  if (a.sketch_v) {
+  if (a.sketch_v && mbar_wait_bounded(&s_bar, 0, a.error)) {
     const float *sg = s_sg + rr * kD;
     float t0 = 0.f, t1 = 0.f;
 #pragma unroll 8
@@ -463,8 +472,10 @@ int launch_combine(const CombineArgs &a, cudaStream_t st) {
     attr_done = true;
   }
   const int rows = a.batch * a.heads_q;
-  combine_tq_kernel<<<(rows + kCombineRows - 1) / kCombineRows, kCombineRows * 128, combine_smem(a), st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_overlapped(true, combine_tq_kernel, dim3((rows + kCombineRows - 1) / kCombineRows),
+                           dim3(kCombineRows * 128), combine_smem(a), st, a) == cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- KIVI decode
@@ -694,6 +705,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
                     ctx->dparams->diag, ctx->dparams->sketch, a.out,
                     persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv, G == 1 ? 1 : kPersistGroups};
     cmb.group = G;
+    cmb.error = &ctx->dparams->error;
     return launch_combine(cmb, st);
   }
   if (r2 != TQ_ERR_UNSUPPORTED) return r2;
@@ -740,6 +752,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
 
   CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                   ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv, 1};
+  cmb.error = &ctx->dparams->error;
   return launch_combine(cmb, st);
 }
 
@@ -779,6 +792,7 @@ int launch_decode_kivi(const DecodeArgs &a, void *stream) {
   if (r != TQ_OK) return r;
   CombineArgs cmb{a.batch, a.heads_q, a.splits, 0, 0, a.partials, ctx->dparams->diag, ctx->dparams->sketch, a.out,
                   nullptr, 0, a.heads_kv, 1};
+  cmb.error = &ctx->dparams->error;
   return launch_combine(cmb, st);
 }
 

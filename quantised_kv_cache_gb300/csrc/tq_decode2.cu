@@ -535,6 +535,8 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
 
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();  // the prepared queries come from the kernel before
   const int len = min(max(__ldg(a.seq_lens + b), 0), a.capacity);
   const int t_begin = split * a.chunk;
   const int t_end = min(t_begin + a.chunk, len);
@@ -670,6 +672,10 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
   const int B = a.batch, H = a.heads_kv;
   if (tid < kMaxLevels) s_kc[tid] = __ldg(a.k_centroids + tid);
   build_value_table<VB, kPersistWarps * 32>(smem, Gm::vlut, a.v_centroids, tid);
+  // everything above reads context constants only; the query prep (tile prefix,
+  // prepared queries) and the cache come from earlier kernels of the stream
+  pdl_trigger();
+  pdl_wait();
   for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
   for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
   if (tid < S * 4) mbar_init(&s_full[tid], 1);
@@ -1006,6 +1012,8 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
                          (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16));
     }
   }
+  pdl_trigger();  // the tables above read context constants only
+  pdl_wait();
   for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
   for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
   if (tid < S * 4) mbar_init(&s_full[tid], 1);
@@ -1203,8 +1211,7 @@ int launch_split(const Decode2Args &k, dim3 grid, cudaStream_t st) {
       return TQ_ERR_CUDA;
     attr_done = true;
   }
-  fn<<<grid, 128, smem, st>>>(k);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_overlapped(true, fn, grid, dim3(128), smem, st, k) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 // persistent launch: one CTA per SM (the workspace's record count assumes no more)
@@ -1221,8 +1228,9 @@ int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st
     attr_done = true;
   }
   *ctas = num_sms;
-  fn<<<*ctas, kPersistWarps * 32, smem, st>>>(k);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_overlapped(true, fn, dim3(*ctas), dim3(kPersistWarps * 32), smem, st, k) == cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
 }
 
 template <int KB, int VB, bool VQJL, int G>
@@ -1237,8 +1245,9 @@ int launch_persist_gqa(const Decode2Args &k, int num_sms, int *ctas, cudaStream_
     attr_done = true;
   }
   *ctas = num_sms;
-  fn<<<*ctas, kPersistWarps * 32, smem, st>>>(k);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_overlapped(true, fn, dim3(*ctas), dim3(kPersistWarps * 32), smem, st, k) == cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
 }
 
 template <int KB, int VB, bool VQJL>

@@ -314,6 +314,7 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
   if (e == cudaSuccess) e = cudaMalloc((void **)&c->dparams, sizeof(tq::DevParams));
   if (e == cudaSuccess) e = cudaMemcpy(c->dparams, hp, sizeof(tq::DevParams), cudaMemcpyHostToDevice);
   if (e == cudaSuccess && tq::launch_operand_prep(c->dparams, nullptr) != TQ_OK) e = cudaErrorUnknown;
+  if (e == cudaSuccess && tq::launch_sketch_transpose(c->dparams, nullptr) != TQ_OK) e = cudaErrorUnknown;
   if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags((cudaStream_t *)&c->side_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags((cudaEvent_t *)&c->ev_fork, cudaEventDisableTiming);
@@ -462,6 +463,19 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.role = ctx->k;
   a.centroids = ctx->dparams->k_centroids;
   a.bounds = ctx->dparams->k_bounds;
+  if (tq::append_small_fits(ctx, (long long)batch * heads_kv * n_new)) {
+    // few vectors (a decode step): keys and values in one warp-per-vector launch
+    tq::AppendArgs v = a;
+    v.x = d_v;
+    v.codes = cache->v_codes;
+    v.norms = cache->v_norm;
+    v.signs = cache->v_signs;
+    v.rnorms = cache->v_rnorm;
+    v.role = ctx->v;
+    v.centroids = ctx->dparams->v_centroids;
+    v.bounds = ctx->dparams->v_bounds;
+    return (tq_status)tq::launch_append_small(a, v, ctx, stream);
+  }
   // K on the library's side stream, V on the caller's, joined before returning
   cudaStream_t st = (cudaStream_t)stream, side = (cudaStream_t)ctx->side_stream;
   const bool fork = side && cudaEventRecord((cudaEvent_t)ctx->ev_fork, st) == cudaSuccess &&

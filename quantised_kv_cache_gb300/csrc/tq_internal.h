@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_runtime.h>
+
 #include "../../include/tq.h"
 
 namespace tq {
@@ -32,9 +34,17 @@ struct DevParams {
   // lo = fp16(S - hi)) with rows and columns in storage order
   uint16_t hadamard_b[kD * kD];
   uint16_t sketch_hl[2 * kD * kD];
+  // H D again, as bf16 (+-1 is exact in both formats), for bf16 inputs
+  uint16_t hadamard_bf[kD * kD];
+  // S with rows and columns in storage order, fp32: sketch_perm[n][k] = S[coord(n)][coord(k)]
+  float sketch_perm[kD * kD];
+  // S transposed for the warp-per-vector append: entry (i, 4L + m) = S[8(L/2) + 2m + (L&1)][i]
+  float sketch_tp[kD * kD];
 };
 // fills DevParams::hadamard_b and DevParams::sketch_hl (stream order)
 int launch_operand_prep(DevParams *dp, void *stream);
+// fills DevParams::sketch_tp (stream order)
+int launch_sketch_transpose(DevParams *dp, void *stream);
 
 struct Role {
   int bits = 0;
@@ -94,11 +104,38 @@ struct AppendArgs {
   const tq_ctx *ctx;
 };
 int launch_append_tq(const AppendArgs &a, void *stream);
+
+// Launch `fn` so that it may overlap the tail of the previous kernel in the stream
+// (programmatic stream serialization); `fn` must call pdl_wait() before it reads
+// anything earlier work writes. Plain stream order when `overlap` is false.
+template <typename... P, typename... A>
+inline cudaError_t launch_overlapped(bool overlap, void (*fn)(P...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t st, A &&...args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fn, static_cast<A &&>(args)...);
+}
 // thread-per-vector append for vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise
 int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream);
 // thread-per-vector append of rotated vectors with the rotation and the QJL sketch on
 // tcgen05 tensor cores; TQ_ERR_UNSUPPORTED otherwise
 int launch_append_tc(const AppendArgs &a, const tq_ctx *ctx, void *stream);
+// warp-specialised persistent append of bf16 vectors on rotated roles (tensor-map loads,
+// bf16 MMA rotation); TQ_ERR_UNSUPPORTED otherwise
+int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream);
+// warp-per-vector append of the keys and values of one call in a single launch, for calls
+// of at most kSmallAppendMax vectors per tensor (TQ schemes)
+constexpr long long kSmallAppendMax = 8192;
+bool append_small_fits(const tq_ctx *ctx, long long vectors);
+int launch_append_small(const AppendArgs &k, const AppendArgs &v, const tq_ctx *ctx, void *stream);
 
 struct DecodeArgs {
   const tq_ctx *ctx;

@@ -15,6 +15,15 @@ namespace tq {
 
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // give up on a wait after 2 s of wall time
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream still runs:
+// pdl_wait() returns once that kernel has completed and its writes are visible
+// (at once when there is no such dependency); nothing written by earlier work
+// may be read, and nothing it reads may be written, before it. pdl_trigger()
+// lets the next kernel of the stream be scheduled before this one finishes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

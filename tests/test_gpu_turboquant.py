@@ -55,8 +55,11 @@ def test_context_parameters_match_the_oracle(scheme, n):
 @pytest.mark.parametrize("scheme,n", [("KQV", 4), ("KQV", 3), ("KQV", 2), ("QKQV", 4), ("QKQV", 3),
                                       ("QKQV", 2), ("KV", 4), ("KV", 2)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_append_codes_bit_exact(scheme, n, dtype):
-    B, H, N = 2, 3, 77  # ragged: not a multiple of the 8-vector groups
+@pytest.mark.parametrize("shape", [(2, 3, 77), (2, 4, 1111)], ids=["few", "bulk"])
+def test_append_codes_bit_exact(scheme, n, dtype, shape):
+    # "few": 462 vectors per tensor, the warp-per-vector single-launch path; "bulk": 8888,
+    # above that path's limit (the thread-per-vector kernels), with a ragged last pass
+    B, H, N = shape
     q, k, v = _inputs(B, H, N, dtype, seed=7 + n, scale_sigma=1.0, outliers=2)
     k[0, 1, 5] = 0  # a zero vector
     v[1, 2, 9] = 0
