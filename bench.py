@@ -35,6 +35,11 @@ CAP = 8192
 # kernels of one decode step: the append of the step's keys and values (one launch for
 # this few vectors), query prep, decode attention, combine
 LAUNCHES_PER_STEP = 4
+# DRAM bytes (read + written) of one decode-kernel launch of this workload: an ncu capture of
+# the decode-small case (context 4096: 297.87 MB) scaled to context 8192 (the kernel reads every
+# token once, so traffic grows with the tokens); to be set to None whenever the kernel changes,
+# until it is captured again
+DECODE_TRAFFIC_BYTES = 2 * 297_868_032
 
 
 def peaks():
@@ -454,7 +459,7 @@ def main():
             "pct_of_hbm_peak": 100.0 * (value / world) / hbm_peak,
             "roofline": {"bound": "hbm", "kernel": "decode_persist_kernel (persistent decode attention)",
                          "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "ms_per_launch": dec_ms,
+                         "frac": achieved / hbm_peak, "traffic": DECODE_TRAFFIC_BYTES, "ms_per_launch": dec_ms,
                          "bytes_per_launch": decode_kernel_bytes},
             "append_quantize": {"tokens_per_s": B * CAP / (append_ms / 1e3),
                                 "token_heads_per_s": token_heads / (append_ms / 1e3),

@@ -26,9 +26,11 @@
  *  - "d_" pointers are device pointers on the device that was current when
  *    the context was created; "h_" pointers are host pointers.
  *  - The caller owns every buffer it passes (cache planes, inputs, outputs,
- *    workspace). The library allocates only the context's small parameter
- *    block (codebooks, D, S, the device error word) in tq_init and frees it
- *    in tq_destroy. The library never frees caller memory.
+ *    workspace). The library allocates only the context's parameter block
+ *    (codebooks, D, S, the device error word, S and H D prepared as
+ *    tensor-core operands; about 320 KB), one non-blocking stream and two
+ *    events in tq_init, and frees them in tq_destroy. The library never
+ *    frees caller memory.
  *  - Launches are asynchronous on the given stream (a cudaStream_t passed as
  *    void*; NULL = the legacy default stream). No call synchronises except
  *    tq_get_device_error.
@@ -201,7 +203,13 @@ tq_status tq_cache_sizes_get(const tq_ctx *ctx, int batch, int heads_kv, int cap
  *                stream order.
  * A sequence whose slots would exceed the capacity is skipped and the
  * device error word is set to TQ_ERR_CAPACITY. KIVI: keeps the window rule
- * stated above (groups leave the window when it reaches window + group). */
+ * stated above (groups leave the window when it reaches window + group).
+ * Calls of at most 8192 vectors per tensor quantise keys and values in one
+ * launch; larger ones run the key kernel on the context's own stream,
+ * forked from and joined back into `stream` with events, so all of the
+ * call's work is still ordered before anything later enqueued on `stream`.
+ * (The context's stream and events are shared state: do not call this on one
+ * context from two host threads at once.) */
 tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const void *d_k,
                              const void *d_v, int dtype, int batch, int heads_kv, int n_new,
                              const int32_t *d_seq_lens, void *stream);

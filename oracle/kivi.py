@@ -11,7 +11,7 @@ the ablation flips either axis. "The systems tax": keep the most recent tokens
 (up to 128) in full precision and quantise them in groups once enough have
 accumulated.
 
-Readings where the page is silent (listed in the design doc):
+Readings where the page is silent:
 
 * B = 2, group G = 32, window W = 128 (the page's setting).
 * zero point and step are stored as float16: z = fp16(min), s = fp16((max-min)/3)

@@ -22,7 +22,7 @@ What each step follows:
   KQV  -- WHT on both; K n-bit; V (n-1)-bit + 1-bit QJL;
   QKQV -- WHT on both; K and V (n-1)-bit + 1-bit QJL.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * n bits are per coordinate; norms are float32 side data.
 * KV uses the same sphere-marginal codebook on unrotated unit coordinates.
