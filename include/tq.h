@@ -44,8 +44,16 @@
  * Storage format (both the library and the independent CPU checker implement
  * this text)
  * ---------------------------------------------------------------------------
- *  Cache geometry: each plane is an array over [batch][heads_kv][capacity]
- *  token slots (row-major); a token's slot holds one fixed-size record.
+ *  Cache geometry (TQ schemes): one records array of 16-token blocks,
+ *  [batch][heads_kv][ceil(capacity / 16)] blocks (row-major). A block holds
+ *  the records of its 16 token slots plane by plane, in tq_plane order: the
+ *  K code records [16][d*b_K/8], the K norms [16] (float32), for sketched
+ *  keys the K sign records [16][d/8] and the K residual norms [16], then the
+ *  same four planes for V; unused planes take no bytes. Every plane starts at
+ *  a multiple of 16 bytes, so token slot t of sequence-head (b, h) is at
+ *  block (b * heads_kv + h) * ceil(capacity / 16) + t / 16, entry t % 16 of
+ *  each plane, and the 16 tokens of a block are one contiguous copy
+ *  (tq_cache_sizes gives the block size and the plane offsets).
  *
  *  Code records: a vector's d coordinates each get a b-bit index into the
  *  Lloyd-Max codebook (index 0 = the most negative centroid). The d/2
@@ -66,7 +74,7 @@
  *                   V: (n-1)-bit codes of the rotated unit vector + norm
  *                      + d sign bits + residual norm.
  *    TQ_SCHEME_QKQV K and V: (n-1)-bit codes + norm + signs + residual norm.
- *  Unused planes are NULL with size 0.
+ *  Unused planes have 0 bytes per token.
  *
  *  Quantisation of one vector x (fp32 arithmetic on the device; the CPU
  *  checker repeats it in fp64 and codes must agree except where the exact
@@ -94,7 +102,8 @@
  *    (+ rho sqrt(pi/2)/d D H S^T sigma, sigma_i = +/-1, for sketched vectors;
  *     D and H dropped for TQ_SCHEME_KV).
  *
- *  KIVI records (TQ_SCHEME_KIVI, [KIVI-geom]): 2-bit codes per element in
+ *  KIVI records (TQ_SCHEME_KIVI, [KIVI-geom]): separate planes, each an array
+ *  over [batch][heads_kv][capacity] token slots. 2-bit codes per element in
  *  plain channel order, channel i at bits [2i, 2i+2) (d/4 bytes per token),
  *  for both K and V; float16
  *  (zero, step) pairs per group, zero = fp16(group min), step =
@@ -120,7 +129,7 @@
 extern "C" {
 #endif
 
-#define TQ_ABI_VERSION 1
+#define TQ_ABI_VERSION 2
 
 typedef struct tq_ctx tq_ctx; /* opaque, host-owned */
 
@@ -145,21 +154,30 @@ typedef enum {
 
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
 
-/* Device pointers to the planes of one cache. Sizes come from
- * tq_cache_sizes; a plane whose size is 0 is unused and may be NULL. Every
- * non-NULL plane must be 16-byte aligned. */
+/* The planes of a block of the records array (TQ schemes), in storage order. */
+typedef enum {
+  TQ_PLANE_K_CODES = 0, TQ_PLANE_K_NORM = 1, TQ_PLANE_K_SIGNS = 2, TQ_PLANE_K_RNORM = 3,
+  TQ_PLANE_V_CODES = 4, TQ_PLANE_V_NORM = 5, TQ_PLANE_V_SIGNS = 6, TQ_PLANE_V_RNORM = 7,
+  TQ_NUM_PLANES = 8
+} tq_plane;
+
+/* Device pointers of one cache. Sizes come from tq_cache_sizes; a pointer
+ * whose size is 0 is unused and may be NULL. Every non-NULL pointer must be
+ * 16-byte aligned. */
 typedef struct tq_cache {
   int batch, heads_kv, capacity;
-  uint8_t *k_codes;  float *k_norm;  uint8_t *k_signs;  float *k_rnorm;
-  uint8_t *v_codes;  float *v_norm;  uint8_t *v_signs;  float *v_rnorm;
+  uint8_t *records;                          /* TQ schemes: the blocked records */
+  uint8_t *k_codes;  uint8_t *v_codes;       /* KIVI: 2-bit codes */
   uint16_t *k_stats; uint16_t *v_stats;      /* KIVI: fp16 (zero, step) */
   uint16_t *k_window; uint16_t *v_window;    /* KIVI: bf16 ring buffers */
 } tq_cache;
 
 typedef struct tq_cache_sizes {
-  size_t k_codes, k_norm, k_signs, k_rnorm;
-  size_t v_codes, v_norm, v_signs, v_rnorm;
-  size_t k_stats, v_stats, k_window, v_window;
+  size_t records;                    /* TQ schemes: bytes of the records array */
+  size_t block_bytes;                /* TQ schemes: bytes of one 16-token block */
+  size_t plane_offset[TQ_NUM_PLANES]; /* TQ schemes: byte offset of each plane in a block */
+  size_t plane_bytes[TQ_NUM_PLANES];  /* TQ schemes: bytes per token of each plane (0: unused) */
+  size_t k_codes, v_codes, k_stats, v_stats, k_window, v_window; /* KIVI plane bytes */
   size_t record_bytes; /* algorithmic bytes of one token-head (K + V records) */
 } tq_cache_sizes;
 
@@ -188,9 +206,10 @@ void tq_destroy(tq_ctx *ctx);
  * before sizing or using a cache; TQ_ERR_STATE for other schemes. */
 tq_status tq_set_kivi(tq_ctx *ctx, int group, int window, int k_per_channel, int v_per_token);
 
-/* Byte sizes of every plane of a cache of `capacity` token slots for
- * [batch][heads_kv] sequences-heads. KIVI: capacity must be a multiple of
- * the group. */
+/* Byte sizes of a cache of `capacity` token slots for [batch][heads_kv]
+ * sequences-heads: TQ schemes the records array (whole 16-token blocks per
+ * sequence-head), its block size and plane offsets; KIVI the sizes of its
+ * planes (capacity must be a multiple of the group). */
 tq_status tq_cache_sizes_get(const tq_ctx *ctx, int batch, int heads_kv, int capacity,
                              tq_cache_sizes *out);
 

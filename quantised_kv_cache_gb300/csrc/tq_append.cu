@@ -24,7 +24,7 @@ constexpr int kVecPerWarp = 8;
 
 struct AppendKernelArgs {
   const void *x;
-  int batch, heads, n_new, capacity;
+  int batch, heads, n_new, capacity, cap16, bb;
   const int32_t *seq_lens;
   uint8_t *codes;
   float *norms;
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) append_tq_kernel(AppendKernelA
       // a sequence whose new tokens would not all fit is skipped whole
       const bool ok = len >= 0 && len + a.n_new <= a.capacity;
       if (!ok && lane == 0) set_error(a.error, TQ_ERR_CAPACITY);
-      const long long slot = bh * a.capacity + pos;
+      const long long slot = bh * a.cap16 + pos;
 
       float x[4];
       load4(a.x, (size_t)vec * kD + 4 * lane, BF16, x);
@@ -119,8 +119,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) append_tq_kernel(AppendKernelA
       const uint32_t fb = (uint32_t)idx[2] | ((uint32_t)idx[3] << BITS);
       const uint32_t word = pack_slot_word<BITS>(fa, fb, lane);
       if (ok) {
-        if (lane < 4 * BITS) reinterpret_cast<uint32_t *>(a.codes + slot * (BITS * kD / 8))[lane] = word;
-        if (!QJL && lane == 0) a.norms[slot] = nu;
+        if (lane < 4 * BITS) reinterpret_cast<uint32_t *>(rec_at(a.codes, slot, a.bb, BITS * kD / 8))[lane] = word;
+        if (!QJL && lane == 0) *rec_at(a.norms, slot, a.bb, 4) = nu;
       }
       if (QJL) {
         float r[4], rr = 0.f;
@@ -173,12 +173,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) append_tq_kernel(AppendKernelA
         const long long slot = slot_v[v];
         if (slot >= 0) {
           if (nu_v[v] == 0.f) w0 = w1 = w2 = w3 = 0xffffffffu;
-          uint32_t *srec = reinterpret_cast<uint32_t *>(a.signs + slot * (kD / 8));
+          uint32_t *srec = reinterpret_cast<uint32_t *>(rec_at(a.signs, slot, a.bb, kD / 8));
           const uint32_t wsel = (lane == 0) ? w0 : (lane == 1) ? w1 : (lane == 2) ? w2 : w3;
           if (lane < 4) srec[lane] = wsel;
           if (lane == 0) {
-            a.norms[slot] = nu_v[v];
-            a.rnorms[slot] = rho_v[v];
+            *rec_at(a.norms, slot, a.bb, 4) = nu_v[v];
+            *rec_at(a.rnorms, slot, a.bb, 4) = rho_v[v];
           }
         }
       }
@@ -246,6 +246,8 @@ int launch_append_tq(const AppendArgs &a, void *stream) {
   k.heads = a.heads;
   k.n_new = a.n_new;
   k.capacity = a.capacity;
+  k.cap16 = a.cap16;
+  k.bb = a.bb;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;
   k.norms = a.norms;

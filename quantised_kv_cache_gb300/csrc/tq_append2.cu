@@ -23,7 +23,7 @@ namespace {
 
 struct Append2Args {
   const void *x;
-  int batch, heads, n_new, capacity;
+  int batch, heads, n_new, capacity, cap16, bb;
   const int32_t *seq_lens;
   uint8_t *codes;
   float *norms;
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
       if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);
       continue;
     }
-    const long long slot = bh * a.capacity + len + t;
+    const long long slot = bh * a.cap16 + len + t;
 
     float x[kD];
     if (BF16) {
@@ -138,10 +138,10 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
       word[off >> 5] |= (uint32_t)code << (off & 31);
       if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= (uint32_t)code >> (32 - (off & 31));
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(a.codes + slot * (BITS * kD / 8));
+    uint4 *dst = reinterpret_cast<uint4 *>(rec_at(a.codes, slot, a.bb, BITS * kD / 8));
 #pragma unroll
     for (int k = 0; k < BITS; ++k) dst[k] = make_uint4(word[4 * k], word[4 * k + 1], word[4 * k + 2], word[4 * k + 3]);
-    a.norms[slot] = nu;
+    *rec_at(a.norms, slot, a.bb, 4) = nu;
   }
 }
 
@@ -184,6 +184,8 @@ int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.heads = a.heads;
   k.n_new = a.n_new;
   k.capacity = a.capacity;
+  k.cap16 = a.cap16;
+  k.bb = a.bb;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;
   k.norms = a.norms;

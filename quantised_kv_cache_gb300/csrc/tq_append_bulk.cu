@@ -59,7 +59,7 @@ struct BulkGeo {
 };
 
 struct BulkArgs {
-  int batch, heads, n_new, capacity;
+  int batch, heads, n_new, capacity, cap16, bb;
   long long total;
   const int32_t *seq_lens;
   uint8_t *codes;
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         const long long bh = vec / a.n_new;
         const int b = (int)(bh / a.heads);
         const int len = __ldg(a.seq_lens + b);
-        if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.capacity + len + t;
+        if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.cap16 + len + t;
         else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
       }
       if (*s_abort || !__all_sync(kFull, mbar_wait_bounded(&y_full[g], (uint32_t)par, a.error))) {
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       for (int j = 0; j < H; ++j) P[j] = a.bounds[L / 2 + j] * sv;
       // pass 2: codes and residuals of chunk c (32 storage offsets)
       float rr = 0.f;
-      uint32_t *crec = reinterpret_cast<uint32_t *>(a.codes + (slot >= 0 ? slot : 0) * (BITS * kD / 8));
+      uint32_t *crec = reinterpret_cast<uint32_t *>(rec_at(a.codes, slot >= 0 ? slot : 0, a.bb, BITS * kD / 8));
       auto chunk_codes = [&](uint32_t (&yz)[32], int c) {
         uint32_t word[BITS];
 #pragma unroll
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         }
       }
       const float nu = (ss > 0.f) ? sv * 0.08838834764831845f : 0.f;  // ||y|| / sqrt(d)
-      if (slot >= 0) a.norms[slot] = nu;
+      if (slot >= 0) *rec_at(a.norms, slot, a.bb, 4) = nu;
       if constexpr (QJL) {
         tc_fence_before_sync();
         __syncwarp();
@@ -510,8 +510,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         certify_rounds(tslot + 128, a.sketch_perm, flag, sw);
         if (slot >= 0) {
           if (ss == 0.f) sw[0] = sw[1] = sw[2] = sw[3] = 0xffffffffu;  // a zero vector: every sign set, rho = 0
-          *reinterpret_cast<uint4 *>(a.signs + slot * (kD / 8)) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
-          a.rnorms[slot] = (ss > 0.f) ? nu * sqrtf(rr) * (1.f / kRScaleB) : 0.f;
+          *reinterpret_cast<uint4 *>(rec_at(a.signs, slot, a.bb, kD / 8)) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+          *rec_at(a.rnorms, slot, a.bb, 4) = (ss > 0.f) ? nu * sqrtf(rr) * (1.f / kRScaleB) : 0.f;
         }
       }
       // this warp is done with the slot's tensor memory
@@ -603,6 +603,8 @@ int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.heads = a.heads;
   k.n_new = a.n_new;
   k.capacity = a.capacity;
+  k.cap16 = a.cap16;
+  k.bb = a.bb;
   k.total = total;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;

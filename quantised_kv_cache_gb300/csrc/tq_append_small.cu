@@ -41,8 +41,8 @@ struct SmallRole {
 };
 
 struct SmallArgs {
-  SmallRole role[2];  // keys, values
-  int batch, heads, n_new, capacity;
+  SmallRole role[2];  // keys, values (plane bases in the blocked records)
+  int batch, heads, n_new, capacity, cap16, bb;
   const int32_t *seq_lens;
   const float *diag;       // D as +/-1.0f
   const float *sketch_tp;  // entry (i, 4L + m) = S[8(L/2) + 2m + (L&1)][i]
@@ -50,11 +50,12 @@ struct SmallArgs {
 };
 
 template <int BITS>
-__device__ __forceinline__ void store_codes(uint8_t *codes, long long slot, const int (&idx)[4], int lane) {
+__device__ __forceinline__ void store_codes(uint8_t *codes, long long slot, int bb, const int (&idx)[4], int lane) {
   const uint32_t fa = (uint32_t)idx[0] | ((uint32_t)idx[1] << BITS);
   const uint32_t fb = (uint32_t)idx[2] | ((uint32_t)idx[3] << BITS);
   const uint32_t word = pack_slot_word<BITS>(fa, fb, lane);  // every lane takes part
-  if (slot >= 0 && lane < 4 * BITS) reinterpret_cast<uint32_t *>(codes + slot * (BITS * kD / 8))[lane] = word;
+  if (slot >= 0 && lane < 4 * BITS)
+    reinterpret_cast<uint32_t *>(rec_at(codes, slot, bb, BITS * kD / 8))[lane] = word;
 }
 
 template <bool BF16>
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
     // a sequence whose new tokens would not all fit is skipped whole
     const bool ok = len >= 0 && len + a.n_new <= a.capacity;
     if (!ok && t == 0 && lane == 0 && blockIdx.y == 0) set_error(a.error, TQ_ERR_CAPACITY);
-    slot = ok ? bh * a.capacity + len + t : -1;
+    slot = ok ? bh * a.cap16 + len + t : -1;
 
     float x[4];
     load4(ro.x, (size_t)vec * kD + 4 * lane, BF16, x);
@@ -112,12 +113,12 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
       idx[j] = c;
     }
     switch (ro.bits) {
-      case 1: store_codes<1>(ro.codes, slot, idx, lane); break;
-      case 2: store_codes<2>(ro.codes, slot, idx, lane); break;
-      case 3: store_codes<3>(ro.codes, slot, idx, lane); break;
-      default: store_codes<4>(ro.codes, slot, idx, lane); break;
+      case 1: store_codes<1>(ro.codes, slot, a.bb, idx, lane); break;
+      case 2: store_codes<2>(ro.codes, slot, a.bb, idx, lane); break;
+      case 3: store_codes<3>(ro.codes, slot, a.bb, idx, lane); break;
+      default: store_codes<4>(ro.codes, slot, a.bb, idx, lane); break;
     }
-    if (!qjl && slot >= 0 && lane == 0) ro.norms[slot] = nu;
+    if (!qjl && slot >= 0 && lane == 0) *rec_at(ro.norms, slot, a.bb, 4) = nu;
     if (qjl) {
       // unit-domain residual r = y - c[code]
       float r[4];
@@ -178,10 +179,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
     w = 0xffffffffu;
     rho = 0.f;
   }
-  if (lane < 4) reinterpret_cast<uint32_t *>(ro.signs + slot * (kD / 8))[lane] = w;
+  if (lane < 4) reinterpret_cast<uint32_t *>(rec_at(ro.signs, slot, a.bb, kD / 8))[lane] = w;
   if (lane == 0) {
-    ro.norms[slot] = nu;
-    ro.rnorms[slot] = rho;
+    *rec_at(ro.norms, slot, a.bb, 4) = nu;
+    *rec_at(ro.rnorms, slot, a.bb, 4) = rho;
   }
 }
 
@@ -232,6 +233,8 @@ int launch_append_small(const AppendArgs &k, const AppendArgs &v, const tq_ctx *
   s.heads = k.heads;
   s.n_new = k.n_new;
   s.capacity = k.capacity;
+  s.cap16 = k.cap16;
+  s.bb = k.bb;
   s.seq_lens = k.seq_lens;
   s.diag = ctx->dparams->diag;
   s.sketch_tp = ctx->dparams->sketch_tp;

@@ -43,7 +43,7 @@ namespace {
 
 struct TcArgs {
   const void *x;
-  int batch, heads, n_new, capacity;
+  int batch, heads, n_new, capacity, cap16, bb;
   const int32_t *seq_lens;
   uint8_t *codes;
   float *norms;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
       const long long bh = vec / a.n_new;
       const int b = (int)(bh / a.heads);
       const int len = __ldg(a.seq_lens + b);
-      if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.capacity + len + t;
+      if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.cap16 + len + t;
       else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
     }
     float nu, xs;
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
 #pragma unroll
     for (int k = 0; k < H; ++k) P[k] = a.bounds[L / 2 + k] * sv;
     float rr = 0.f;
-    uint32_t *crec = reinterpret_cast<uint32_t *>(a.codes + (slot >= 0 ? slot : 0) * (BITS * kD / 8));
+    uint32_t *crec = reinterpret_cast<uint32_t *>(rec_at(a.codes, slot >= 0 ? slot : 0, a.bb, BITS * kD / 8));
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       uint32_t yz[32];
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
         tmem_st_x16(tlane + 192 + 16 * q, rl);
       }
     }
-    if (slot >= 0) a.norms[slot] = nu;
+    if (slot >= 0) *rec_at(a.norms, slot, a.bb, 4) = nu;
 
     if constexpr (QJL) {
       tc_fence_before_sync();
@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
           sw[0] = sw[1] = sw[2] = sw[3] = 0xffffffffu;
           rho = 0.f;
         }
-        *reinterpret_cast<uint4 *>(a.signs + slot * (kD / 8)) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
-        a.rnorms[slot] = rho;
+        *reinterpret_cast<uint4 *>(rec_at(a.signs, slot, a.bb, kD / 8)) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+        *rec_at(a.rnorms, slot, a.bb, 4) = rho;
       }
     }
     // the next pass overwrites A and D only after every thread passed its barrier
@@ -475,6 +475,8 @@ int launch_append_tc(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.heads = a.heads;
   k.n_new = a.n_new;
   k.capacity = a.capacity;
+  k.cap16 = a.cap16;
+  k.bb = a.bb;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;
   k.norms = a.norms;

@@ -116,6 +116,7 @@ struct DecodeKernelArgs {
   const float *v_norm;
   const uint8_t *v_signs;
   const float *v_rnorm;
+  int bb, cap16;  // blocked records (plane pointers are the block-0 bases)
   int capacity, heads_kv, heads_q, chunk, splits;
   const int32_t *seq_lens;
   const float *qprep;
@@ -195,14 +196,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
     for (int j = 0; j < 4; ++j) acc[g][j] = sacc[g][j] = 0.f;
   }
 
-  const size_t slot0 = ((size_t)b * a.heads_kv + hk) * a.capacity;
-  const uint32_t *kc = reinterpret_cast<const uint32_t *>(a.k_codes) + slot0 * (KB * 4);
-  const uint32_t *vc = reinterpret_cast<const uint32_t *>(a.v_codes) + slot0 * (VB * 4);
-  const uint32_t *ks = KQJL ? reinterpret_cast<const uint32_t *>(a.k_signs) + slot0 * 4 : nullptr;
-  const uint32_t *vs = VQJL ? reinterpret_cast<const uint32_t *>(a.v_signs) + slot0 * 4 : nullptr;
-  const float *kn = a.k_norm + slot0, *vn = a.v_norm + slot0;
-  const float *kr = KQJL ? a.k_rnorm + slot0 : nullptr;
-  const float *vr = VQJL ? a.v_rnorm + slot0 : nullptr;
+  const long long slot0 = ((long long)b * a.heads_kv + hk) * a.cap16;
+  auto rec32 = [&](const uint8_t *plane, int t, int tok) {
+    return reinterpret_cast<const uint32_t *>(rec_at(plane, slot0 + t, a.bb, tok));
+  };
+  auto recf = [&](const float *plane, int t) { return __ldg(rec_at(plane, slot0 + t, a.bb, 4)); };
   const int my_tok = tile_token_of_lane(lane);
 
   for (int tile = t_begin + warp * kTile; tile < t_end; tile += kDecodeWarps * kTile) {
@@ -212,19 +210,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
     for (int jj = 0; jj < kTile; ++jj) {
       const int t = min(tile + jj, t_end - 1);
       uint32_t code[4];
-      lane_codes<KB>(kc + (size_t)t * (KB * 4), lane, code);
+      lane_codes<KB>(rec32(a.k_codes, t, KB * 16), lane, code);
       float c[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) c[j] = s_cb[code[j]];
-      const float nu = __ldg(kn + t);
+      const float nu = recf(a.k_norm, t);
       float sg[4];
       float rk = 0.f;
       if (KQJL) {
         uint32_t sb[4];
-        lane_signs(ks + (size_t)t * 4, lane, sb);
+        lane_signs(rec32(a.k_signs, t, 16), lane, sb);
 #pragma unroll
         for (int j = 0; j < 4; ++j) sg[j] = sb[j] ? 1.f : -1.f;
-        rk = __ldg(kr + t);
+        rk = recf(a.k_rnorm, t);
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -265,16 +263,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
       if (t >= t_end) break;
       const int src = lane_of_tile_token(jj);
       uint32_t code[4];
-      lane_codes<VB>(vc + (size_t)t * (VB * 4), lane, code);
+      lane_codes<VB>(rec32(a.v_codes, t, VB * 16), lane, code);
       float c[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) c[j] = s_cb[16 + code[j]];
-      const float nu = __ldg(vn + t);
+      const float nu = recf(a.v_norm, t);
       uint32_t sb[4] = {0u, 0u, 0u, 0u};
       float rv = 0.f;
       if (VQJL) {
-        lane_signs(vs + (size_t)t * 4, lane, sb);
-        rv = __ldg(vr + t);
+        lane_signs(rec32(a.v_signs, t, 16), lane, sb);
+        rv = recf(a.v_rnorm, t);
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -712,8 +710,14 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
 
   DecodeKernelArgs k{};
   const tq_cache *c = a.cache;
-  k.k_codes = c->k_codes; k.k_norm = c->k_norm; k.k_signs = c->k_signs; k.k_rnorm = c->k_rnorm;
-  k.v_codes = c->v_codes; k.v_norm = c->v_norm; k.v_signs = c->v_signs; k.v_rnorm = c->v_rnorm;
+  const RecLayout &L = ctx->lay;
+  auto plane = [&](int p) -> const uint8_t * { return L.tok[p] ? c->records + L.off[p] : nullptr; };
+  k.k_codes = plane(TQ_PLANE_K_CODES); k.k_norm = reinterpret_cast<const float *>(plane(TQ_PLANE_K_NORM));
+  k.k_signs = plane(TQ_PLANE_K_SIGNS); k.k_rnorm = reinterpret_cast<const float *>(plane(TQ_PLANE_K_RNORM));
+  k.v_codes = plane(TQ_PLANE_V_CODES); k.v_norm = reinterpret_cast<const float *>(plane(TQ_PLANE_V_NORM));
+  k.v_signs = plane(TQ_PLANE_V_SIGNS); k.v_rnorm = reinterpret_cast<const float *>(plane(TQ_PLANE_V_RNORM));
+  k.bb = L.bb;
+  k.cap16 = cap16_of(c->capacity);
   k.capacity = c->capacity;
   k.heads_kv = a.heads_kv;
   k.heads_q = a.heads_q;

@@ -56,16 +56,18 @@ struct Geo {
   static constexpr int kStages = S;
   // per-token record bytes of each plane
   static constexpr int kc = 16 * KB, vc = 16 * VB;
-  // stage layout (bytes), every plane 16-byte aligned
+  // a stage is four 16-token blocks of the blocked record layout, copied as they are
+  // stored; plane offsets inside a block (bytes, every plane 16-byte aligned)
   static constexpr int off_kc = 0;
-  static constexpr int off_kn = off_kc + kTT * kc;
-  static constexpr int off_ks = off_kn + kTT * 4;
-  static constexpr int off_kr = off_ks + (KQJL ? kTT * 16 : 0);
-  static constexpr int off_vc = off_kr + (KQJL ? kTT * 4 : 0);
-  static constexpr int off_vn = off_vc + kTT * vc;
-  static constexpr int off_vs = off_vn + kTT * 4;
-  static constexpr int off_vr = off_vs + (VQJL ? kTT * 16 : 0);
-  static constexpr int stage = off_vr + (VQJL ? kTT * 4 : 0);
+  static constexpr int off_kn = off_kc + 16 * kc;
+  static constexpr int off_ks = off_kn + 16 * 4;
+  static constexpr int off_kr = off_ks + (KQJL ? 16 * 16 : 0);
+  static constexpr int off_vc = off_kr + (KQJL ? 16 * 4 : 0);
+  static constexpr int off_vn = off_vc + 16 * vc;
+  static constexpr int off_vs = off_vn + 16 * 4;
+  static constexpr int off_vr = off_vs + (VQJL ? 16 * 16 : 0);
+  static constexpr int block = off_vr + (VQJL ? 16 * 4 : 0);
+  static constexpr int stage = 4 * block;
   // key table: positions per record (bytes, or 6-bit pair slots) and values per position
   static constexpr int kpos = (KB == 3) ? 64 : 16 * KB;
   static constexpr int kval = (KB == 3) ? 64 : 256;
@@ -96,14 +98,8 @@ constexpr int persist_stages() {
 }
 
 struct Decode2Args {
-  const uint8_t *k_codes;
-  const float *k_norm;
-  const uint8_t *k_signs;
-  const float *k_rnorm;
-  const uint8_t *v_codes;
-  const float *v_norm;
-  const uint8_t *v_signs;
-  const float *v_rnorm;
+  const uint8_t *records;  // blocked records: [sequence-head][cap16 / 16] blocks of `bb` bytes
+  int bb, cap16;
   int capacity, batch, heads_kv, heads_q, chunk, splits;
   const int32_t *seq_lens;
   const int32_t *tile_prefix;  // persistent kernel: [batch + 1] tiles before each batch
@@ -266,9 +262,13 @@ struct WarpState {
 // One warp's 16 tokens (wbase .. wbase + 15 of the tile at `st`, tile start t0,
 // sequence end t_end): scores, online-softmax step, value and sign MMAs.
 template <typename Gm, int KB, int VB, bool KQJL, bool VQJL>
-__device__ __forceinline__ void tile_body(const unsigned char *st, const unsigned char *smem, int wbase, int t0,
+__device__ __forceinline__ void tile_body(const unsigned char *st, const unsigned char *smem, int wtile, int t0,
                                           int t_end, int lane, const LaneConsts<KB> &lc, WarpState &ws) {
   const int half = lane >> 4, l = lane & 15, g = lane >> 2, t4 = lane & 3;
+  // the warp's 16 tokens (wtile .. wtile + 15 of the tile) are one block of the stage:
+  // addresses are taken inside that block, validity against the tile position
+  st += (wtile >> 4) * Gm::block;
+  constexpr int wbase = 0;
   const float *kn = reinterpret_cast<const float *>(st + Gm::off_kn);
   const float *kr = reinterpret_cast<const float *>(st + Gm::off_kr);
   const unsigned char *tb = smem + Gm::sm_ktab;
@@ -339,7 +339,7 @@ __device__ __forceinline__ void tile_body(const unsigned char *st, const unsigne
     sc += __shfl_xor_sync(kFull, sc, 1);
   }
   const int tok = wbase + lc.my_j;
-  const bool valid = t0 + tok < t_end;
+  const bool valid = t0 + wtile + tok < t_end;
   if (!KQJL) sc *= kn[tok];
   sc = valid ? sc : -INFINITY;
 
@@ -499,25 +499,12 @@ __device__ __forceinline__ void merge_parked(const float *src, int i, float *rec
   rec[2 + kD + i] = Sg;
 }
 
-template <typename Gm, bool KQJL, bool VQJL>
-__device__ __forceinline__ void issue_tile_to(unsigned char *st, uint64_t *bar, const Decode2Args &a, size_t s0, int n) {
-  const int n4 = (n + 3) & ~3;  // norms in 16-byte units
-  uint32_t bytes = n * Gm::kc + n4 * 4 + n * Gm::vc + n4 * 4;
-  if (KQJL) bytes += n * 16 + n4 * 4;
-  if (VQJL) bytes += n * 16 + n4 * 4;
+// Copy the blocks holding tokens s0 .. s0 + n - 1 (s0 a multiple of 16) into a stage.
+template <typename Gm>
+__device__ __forceinline__ void issue_tile_to(unsigned char *st, uint64_t *bar, const Decode2Args &a, long long s0, int n) {
+  const uint32_t bytes = (uint32_t)(((n + 15) >> 4) * Gm::block);
   mbar_arrive_expect_tx(bar, bytes);
-  tma_load_1d(st + Gm::off_kc, a.k_codes + s0 * Gm::kc, n * Gm::kc, bar);
-  tma_load_1d(st + Gm::off_kn, a.k_norm + s0, n4 * 4, bar);
-  if (KQJL) {
-    tma_load_1d(st + Gm::off_ks, a.k_signs + s0 * 16, n * 16, bar);
-    tma_load_1d(st + Gm::off_kr, a.k_rnorm + s0, n4 * 4, bar);
-  }
-  tma_load_1d(st + Gm::off_vc, a.v_codes + s0 * Gm::vc, n * Gm::vc, bar);
-  tma_load_1d(st + Gm::off_vn, a.v_norm + s0, n4 * 4, bar);
-  if (VQJL) {
-    tma_load_1d(st + Gm::off_vs, a.v_signs + s0 * 16, n * 16, bar);
-    tma_load_1d(st + Gm::off_vr, a.v_rnorm + s0, n4 * 4, bar);
-  }
+  tma_load_1d(st, a.records + (s0 >> 4) * Gm::block, bytes, bar);
 }
 
 // ============================================================================
@@ -541,7 +528,7 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
   const int t_begin = split * a.chunk;
   const int t_end = min(t_begin + a.chunk, len);
   const int ntiles = (t_end > t_begin) ? (t_end - t_begin + kTT - 1) / kTT : 0;
-  const size_t slot0 = ((size_t)b * a.heads_kv + hk) * a.capacity;
+  const long long slot0 = ((long long)b * a.heads_kv + hk) * a.cap16;
   const int hq = hk;  // one query head per KV head
 
   if (tid == 0) {
@@ -554,7 +541,7 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
   __syncthreads();
   auto issue = [&](int tile) {
     const int t0 = t_begin + tile * kTT;
-    issue_tile_to<Gm, KQJL, VQJL>(s_stage + (tile % S) * Gm::stage, &s_full[tile % S], a, slot0 + t0,
+    issue_tile_to<Gm>(s_stage + (tile % S) * Gm::stage, &s_full[tile % S], a, slot0 + t0,
                                   min(kTT, t_end - t0));
   };
   if (tid == 0)
@@ -615,46 +602,6 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
 // ============================================================================
 constexpr int kPersistWarps = 16;  // four groups of four (kPersistGroups)
 
-// One plane of the cache per lane (lanes 0 .. kPlanes - 1): the lanes of a warp
-// issue the TMA copies of its quarter tile in parallel.
-template <typename Gm, bool KQJL, bool VQJL>
-struct PlaneLane {
-  static constexpr int kPlanes = 4 + (KQJL ? 2 : 0) + (VQJL ? 2 : 0);
-  const unsigned char *base = nullptr;  // global plane
-  int tok = 0;                          // bytes per token
-  int off = 0;                          // stage offset of the plane
-  bool norm = false;                    // 4-byte plane: copied in whole 16-byte units
-  __device__ __forceinline__ PlaneLane(const Decode2Args &a, int lane) {
-    int k = 0;
-    auto set = [&](const void *b, int t, int o, bool nm) {
-      if (lane == k) {
-        base = static_cast<const unsigned char *>(b);
-        tok = t;
-        off = o;
-        norm = nm;
-      }
-      ++k;
-    };
-    set(a.k_codes, Gm::kc, Gm::off_kc, false);
-    set(a.k_norm, 4, Gm::off_kn, true);
-    if (KQJL) {
-      set(a.k_signs, 16, Gm::off_ks, false);
-      set(a.k_rnorm, 4, Gm::off_kr, true);
-    }
-    set(a.v_codes, Gm::vc, Gm::off_vc, false);
-    set(a.v_norm, 4, Gm::off_vn, true);
-    if (VQJL) {
-      set(a.v_signs, 16, Gm::off_vs, false);
-      set(a.v_rnorm, 4, Gm::off_vr, true);
-    }
-  }
-  // bytes of a quarter of n tokens (n >= 1)
-  static __device__ __forceinline__ uint32_t bytes(int n) {
-    const int n4 = (n + 3) & ~3;
-    return n * (Gm::kc + Gm::vc + 16 * ((KQJL ? 1 : 0) + (VQJL ? 1 : 0))) + n4 * 4 * (2 + (KQJL ? 1 : 0) + (VQJL ? 1 : 0));
-  }
-};
-
 template <int KB, int VB, bool KQJL, bool VQJL>
 __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(Decode2Args a) {
   constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
@@ -703,9 +650,8 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
 
   // refill cursor of this warp (all lanes): local tile cur_i, its tile index cur_t
   // within its head, that head's tile count, sequence length and slot row
-  const PlaneLane<Gm, KQJL, VQJL> pl(a, lane);
   int cur_i = grp, cur_b = 0, cur_t = 0, cur_nb = 1, cur_len = 0, cur_h = 0;
-  size_t cur_row = 0;
+  long long cur_row = 0;
   auto seek = [&]() {  // normalise cur_t into its head (heads hold >= 1 tile)
     while (cur_t >= cur_nb) {
       cur_t -= cur_nb;
@@ -715,7 +661,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
         cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
         cur_len = s_len[cur_b];
       }
-      cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
+      cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
     }
   };
   if (cur_i < nloc) {
@@ -726,7 +672,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     const int r = g - H * s_pre[cur_b];
     cur_h = r / cur_nb;
     cur_t = r - cur_h * cur_nb;
-    cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
+    cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
   }
   // issue this warp's quarter of local tile cur_i (whole warp), then step the cursor by 4 tiles
   auto issue_next = [&]() {
@@ -734,12 +680,11 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     uint64_t *bar = &s_full[st * 4 + qtr];
     const int t0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - t0);
-    if (lane == 0) mbar_arrive_expect_tx(bar, n > 0 ? PlaneLane<Gm, KQJL, VQJL>::bytes(n) : 0u);
-    __syncwarp();
-    if (n > 0 && lane < PlaneLane<Gm, KQJL, VQJL>::kPlanes) {
-      const int cnt = pl.norm ? ((n + 3) & ~3) : n;
-      tma_load_1d(s_stage + st * Gm::stage + pl.off + 16 * qtr * pl.tok, pl.base + (cur_row + t0) * pl.tok,
-                  (uint32_t)(cnt * pl.tok), bar);
+    if (lane == 0) {  // the quarter is one stored block: one bulk copy
+      mbar_arrive_expect_tx(bar, n > 0 ? (uint32_t)Gm::block : 0u);
+      if (n > 0)
+        tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, a.records + ((cur_row + t0) >> 4) * Gm::block,
+                    (uint32_t)Gm::block, bar);
     }
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
@@ -831,6 +776,7 @@ struct GeoQ {
   static constexpr int stage = Gs::stage;
   static constexpr int off_kc = Gs::off_kc, off_kn = Gs::off_kn, off_vc = Gs::off_vc, off_vn = Gs::off_vn;
   static constexpr int off_vs = Gs::off_vs, off_vr = Gs::off_vr, kc = Gs::kc, vc = Gs::vc;
+  static constexpr int block = Gs::block;
   static constexpr int sm_bar = sm_stage0 + S * stage;
   static constexpr int sm_q = sm_bar + S * 4 * 8;                  // [G][128]
   static constexpr int sm_misc = sm_q + G * kD * 4;
@@ -839,11 +785,13 @@ struct GeoQ {
 
 // one warp's 16 tokens for all G heads of its KV head
 template <typename Q, int KB, int VB, bool VQJL, int G>
-__device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const unsigned char *smem, int wbase, int t0,
+__device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const unsigned char *smem, int wtile, int t0,
                                               int t_end, int lane, const uint32_t (&bk)[8][2], float &m_run,
                                               float &l_run, float &w_run, float (&acc_v)[8][4],
                                               float (&acc_s)[8][4]) {
   const int g = lane >> 2, t4 = lane & 3, h = g >> 1;
+  st += (wtile >> 4) * Q::block;  // the warp's block of the stage (see tile_body)
+  constexpr int wbase = 0;
   const uint32_t lane8 = (uint32_t)lane << 3, lane4 = (uint32_t)lane << 2;
   const float *kn = reinterpret_cast<const float *>(st + Q::off_kn);
   // ---- scores of tokens g and g + 8 for head t4: S = K_hat (A) x [q_hi, q_lo] (B)
@@ -875,7 +823,7 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
     }
   }
   const int tok0 = wbase + g, tok1 = wbase + 8 + g;
-  const bool v0 = t0 + tok0 < t_end, v1 = t0 + tok1 < t_end;
+  const bool v0 = t0 + wtile + tok0 < t_end, v1 = t0 + wtile + tok1 < t_end;
   float s0 = v0 ? (sk[0] + sk[1]) * kn[tok0] : -INFINITY;
   float s1 = v1 ? (sk[2] + sk[3]) * kn[tok1] : -INFINITY;
   // ---- online softmax of head t4 over the warp's 16 tokens (the 8 lanes g share t4)
@@ -1034,10 +982,9 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
     return lo;
   };
   using Gs = typename Q::Gs;
-  const PlaneLane<Gs, false, VQJL> pl(a, lane);
   // per-warp refill cursor, as in the one-head kernel
   int cur_i = grp, cur_b = 0, cur_t = 0, cur_nb = 1, cur_len = 0, cur_h = 0;
-  size_t cur_row = 0;
+  long long cur_row = 0;
   auto seek = [&]() {
     while (cur_t >= cur_nb) {
       cur_t -= cur_nb;
@@ -1047,7 +994,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
         cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
         cur_len = s_len[cur_b];
       }
-      cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
+      cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
     }
   };
   if (cur_i < nloc) {
@@ -1058,19 +1005,18 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
     const int r = gg - H * s_pre[cur_b];
     cur_h = r / cur_nb;
     cur_t = r - cur_h * cur_nb;
-    cur_row = ((size_t)cur_b * H + cur_h) * a.capacity;
+    cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
   }
   auto issue_next = [&]() {
     const int stn = cur_i % S;
     uint64_t *bar = &s_full[stn * 4 + qtr];
     const int tt0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - tt0);
-    if (lane == 0) mbar_arrive_expect_tx(bar, n > 0 ? PlaneLane<Gs, false, VQJL>::bytes(n) : 0u);
-    __syncwarp();
-    if (n > 0 && lane < PlaneLane<Gs, false, VQJL>::kPlanes) {
-      const int cnt = pl.norm ? ((n + 3) & ~3) : n;
-      tma_load_1d(s_stage + stn * Q::stage + pl.off + 16 * qtr * pl.tok, pl.base + (cur_row + tt0) * pl.tok,
-                  (uint32_t)(cnt * pl.tok), bar);
+    if (lane == 0) {  // the quarter is one stored block: one bulk copy
+      mbar_arrive_expect_tx(bar, n > 0 ? (uint32_t)Q::block : 0u);
+      if (n > 0)
+        tma_load_1d(s_stage + stn * Q::stage + qtr * Q::block, a.records + ((cur_row + tt0) >> 4) * Q::block,
+                    (uint32_t)Q::block, bar);
     }
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
@@ -1203,6 +1149,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
 template <int KB, int VB, bool KQJL, bool VQJL>
 int launch_split(const Decode2Args &k, dim3 grid, cudaStream_t st) {
   using Gm = Geo<KB, VB, KQJL, VQJL, 4, 3>;
+  if (k.bb != Gm::block) return TQ_ERR_UNSUPPORTED;  // the context's record layout is this stage layout
   const size_t smem = Gm::sm_misc;
   auto fn = decode2_g1_kernel<KB, VB, KQJL, VQJL>;
   static bool attr_done = false;
@@ -1219,6 +1166,7 @@ template <int KB, int VB, bool KQJL, bool VQJL>
 int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st) {
   constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
   using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
+  if (k.bb != Gm::block) return TQ_ERR_UNSUPPORTED;
   const size_t smem = Gm::sm_misc + sizeof(int) * (2 * kMaxPersistBatch + 1) + sizeof(float) * kMaxLevels;
   auto fn = decode_persist_kernel<KB, VB, KQJL, VQJL>;
   static bool attr_done = false;
@@ -1236,6 +1184,7 @@ int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st
 template <int KB, int VB, bool VQJL, int G>
 int launch_persist_gqa(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st) {
   using Q = GeoQ<KB, VB, VQJL, G>;
+  if (k.bb != Q::block) return TQ_ERR_UNSUPPORTED;
   const size_t smem = Q::total;
   auto fn = decode_persist_gqa_kernel<KB, VB, VQJL, G>;
   static bool attr_done = false;
@@ -1276,12 +1225,13 @@ int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
   if (G != 1) {
     // GQA groups of 2 or 4 query heads, keys without a sketch, on the persistent tensor-core kernel
     if ((G != 2 && G != 4) || ctx->scheme == TQ_SCHEME_QKQV || !a.tile_prefix || a.batch > kMaxPersistBatch ||
-        a.cache->capacity % 4 || ctx->num_sms <= 0)
+        ctx->num_sms <= 0)
       return TQ_ERR_UNSUPPORTED;
     const tq_cache *c = a.cache;
     Decode2Args k{};
-    k.k_codes = c->k_codes; k.k_norm = c->k_norm; k.v_codes = c->v_codes; k.v_norm = c->v_norm;
-    k.v_signs = c->v_signs; k.v_rnorm = c->v_rnorm;
+    k.records = c->records;
+    k.bb = ctx->lay.bb;
+    k.cap16 = cap16_of(c->capacity);
     k.capacity = c->capacity;
     k.batch = a.batch;
     k.heads_kv = a.heads_kv;
@@ -1306,15 +1256,15 @@ int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
     }
     return TQ_ERR_UNSUPPORTED;
   }
-  // persistent: tiles start at multiples of 64 tokens, so 4-token aligned rows keep
-  // every TMA source 16-byte aligned; split-K: chunk starts as well
-  const bool persist = a.tile_prefix != nullptr && a.batch <= kMaxPersistBatch && a.cache->capacity % 4 == 0 &&
-                       ctx->num_sms > 0;
-  if (!persist && (a.cache->capacity % 16 || a.chunk % 4)) return TQ_ERR_UNSUPPORTED;
+  // tiles (persistent) and chunks (split-K) start at multiples of 16 tokens, i.e. at
+  // whole blocks of the records, which are 16-byte aligned
+  const bool persist = a.tile_prefix != nullptr && a.batch <= kMaxPersistBatch && ctx->num_sms > 0;
+  if (!persist && a.chunk % kBlockTokens) return TQ_ERR_UNSUPPORTED;
   const tq_cache *c = a.cache;
   Decode2Args k{};
-  k.k_codes = c->k_codes; k.k_norm = c->k_norm; k.k_signs = c->k_signs; k.k_rnorm = c->k_rnorm;
-  k.v_codes = c->v_codes; k.v_norm = c->v_norm; k.v_signs = c->v_signs; k.v_rnorm = c->v_rnorm;
+  k.records = c->records;
+  k.bb = ctx->lay.bb;
+  k.cap16 = cap16_of(c->capacity);
   k.capacity = c->capacity;
   k.batch = a.batch;
   k.heads_kv = a.heads_kv;

@@ -15,6 +15,7 @@ struct DequantKernelArgs {
   const float *norms;
   const uint8_t *signs;
   const float *rnorms;
+  int bb, cap16;
   int batch, heads, capacity, t0, t1;
   const float *centroids;
   const float *diag;
@@ -34,15 +35,15 @@ __global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
   if (vec >= total) return;
   const long long bh = vec / n;
   const int t = a.t0 + (int)(vec % n);
-  const size_t slot = (size_t)bh * a.capacity + t;
+  const long long slot = (long long)bh * a.cap16 + t;
   uint32_t code[4];
-  lane_codes<BITS>(reinterpret_cast<const uint32_t *>(a.codes) + slot * (BITS * 4), lane, code);
-  const float nu = __ldg(a.norms + slot);
+  lane_codes<BITS>(reinterpret_cast<const uint32_t *>(rec_at(a.codes, slot, a.bb, BITS * 16)), lane, code);
+  const float nu = __ldg(rec_at(a.norms, slot, a.bb, 4));
   float y[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) y[j] = nu * s_c[code[j]];
   if (QJL) {
-    const uint32_t *srec = reinterpret_cast<const uint32_t *>(a.signs) + slot * 4;
+    const uint32_t *srec = reinterpret_cast<const uint32_t *>(rec_at(a.signs, slot, a.bb, 16));
     uint32_t sw[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) sw[w] = __ldg(srec + w);
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
       r[2] = fmaf(s.z, sg, r[2]);
       r[3] = fmaf(s.w, sg, r[3]);
     }
-    const float rho = __ldg(a.rnorms + slot) * (kSqrtHalfPi / kD);
+    const float rho = __ldg(rec_at(a.rnorms, slot, a.bb, 4)) * (kSqrtHalfPi / kD);
 #pragma unroll
     for (int j = 0; j < 4; ++j) y[j] = fmaf(rho, r[j], y[j]);
   }
@@ -84,7 +85,7 @@ int go(int bits, const DequantKernelArgs &k, unsigned blocks, cudaStream_t st) {
 }  // namespace
 
 int launch_dequant_tq(const DequantArgs &a, void *stream) {
-  DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.batch, a.heads, a.capacity, a.t0, a.t1,
+  DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.bb, a.cap16, a.batch, a.heads, a.capacity, a.t0, a.t1,
                       a.centroids, a.params->diag, a.params->sketch, a.out};
   const long long total = (long long)a.batch * a.heads * (a.t1 - a.t0);
   const unsigned blocks = (unsigned)((total + 7) / 8);

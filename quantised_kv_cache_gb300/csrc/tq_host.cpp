@@ -294,6 +294,17 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
     }
     c->sketch_rowmax = (float)(m * (1.0 + 1e-6));
   }
+  if (scheme != TQ_SCHEME_KIVI) {  // blocked record layout: planes in tq_plane order
+    const int tok[TQ_NUM_PLANES] = {(int)code_bytes(c->k.bits, d), 4, c->k.qjl ? d / 8 : 0, c->k.qjl ? 4 : 0,
+                                    (int)code_bytes(c->v.bits, d), 4, c->v.qjl ? d / 8 : 0, c->v.qjl ? 4 : 0};
+    int off = 0;
+    for (int p = 0; p < TQ_NUM_PLANES; ++p) {
+      c->lay.off[p] = off;
+      c->lay.tok[p] = tok[p];
+      off += tq::kBlockTokens * tok[p];
+    }
+    c->lay.bb = off;
+  }
 
   tq::DevParams *hp = (tq::DevParams *)std::calloc(1, sizeof(tq::DevParams));
   if (!hp) {
@@ -375,20 +386,14 @@ tq_status tq_cache_sizes_get(const tq_ctx *ctx, int batch, int heads_kv, int cap
     out->record_bytes = 2 * (d / 4 + (size_t)(d / G) * 4);
     return TQ_OK;
   }
-  out->k_codes = slots * code_bytes(ctx->k.bits, d);
-  out->k_norm = slots * sizeof(float);
-  out->v_codes = slots * code_bytes(ctx->v.bits, d);
-  out->v_norm = slots * sizeof(float);
-  size_t rec = code_bytes(ctx->k.bits, d) + 4 + code_bytes(ctx->v.bits, d) + 4;
-  if (ctx->k.qjl) {
-    out->k_signs = slots * (d / 8);
-    out->k_rnorm = slots * sizeof(float);
-    rec += d / 8 + 4;
-  }
-  if (ctx->v.qjl) {
-    out->v_signs = slots * (d / 8);
-    out->v_rnorm = slots * sizeof(float);
-    rec += d / 8 + 4;
+  const size_t blocks = (size_t)batch * heads_kv * (tq::cap16_of(capacity) / tq::kBlockTokens);
+  out->block_bytes = (size_t)ctx->lay.bb;
+  out->records = blocks * ctx->lay.bb;
+  size_t rec = 0;
+  for (int p = 0; p < TQ_NUM_PLANES; ++p) {
+    out->plane_offset[p] = (size_t)ctx->lay.off[p];
+    out->plane_bytes[p] = (size_t)ctx->lay.tok[p];
+    rec += (size_t)ctx->lay.tok[p];
   }
   out->record_bytes = rec;
   return TQ_OK;
@@ -398,11 +403,22 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
                                 int dtype, int batch, int heads_kv, int n_new, const int32_t *d_seq_lens,
                                 void *stream);
 
+// Block-0 bases of the four planes of role `which` (0 keys, 1 values) in the blocked
+// records (nullptr for a plane the role does not use).
+static void set_role_planes(const tq_ctx *ctx, const tq_cache *c, int which, uint8_t *&codes, float *&norms,
+                            uint8_t *&signs, float *&rnorms) {
+  const int p0 = which ? TQ_PLANE_V_CODES : TQ_PLANE_K_CODES;
+  auto at = [&](int p) -> uint8_t * { return ctx->lay.tok[p] ? c->records + ctx->lay.off[p] : nullptr; };
+  codes = at(p0);
+  norms = reinterpret_cast<float *>(at(p0 + 1));
+  signs = at(p0 + 2);
+  rnorms = reinterpret_cast<float *>(at(p0 + 3));
+}
+
 static tq_status check_cache(const tq_ctx *ctx, const tq_cache *c, int batch, int heads_kv) {
   if (!c) return TQ_ERR_ARG;
   if (c->batch != batch || c->heads_kv != heads_kv || c->capacity <= 0) return TQ_ERR_ARG;
-  const void *planes[] = {c->k_codes, c->k_norm, c->k_signs, c->k_rnorm, c->v_codes, c->v_norm,
-                          c->v_signs, c->v_rnorm, c->k_stats, c->v_stats, c->k_window, c->v_window};
+  const void *planes[] = {c->records, c->k_codes, c->v_codes, c->k_stats, c->v_stats, c->k_window, c->v_window};
   for (const void *p : planes)
     if (!aligned16(p)) return TQ_ERR_ALIGN;
   if (ctx->scheme == TQ_SCHEME_KIVI) {
@@ -411,9 +427,7 @@ static tq_status check_cache(const tq_ctx *ctx, const tq_cache *c, int batch, in
     if (c->capacity % ctx->kivi_group) return TQ_ERR_ARG;
     return TQ_OK;
   }
-  if (!c->k_codes || !c->k_norm || !c->v_codes || !c->v_norm) return TQ_ERR_ARG;
-  if (ctx->k.qjl && (!c->k_signs || !c->k_rnorm)) return TQ_ERR_ARG;
-  if (ctx->v.qjl && (!c->v_signs || !c->v_rnorm)) return TQ_ERR_ARG;
+  if (!c->records) return TQ_ERR_ARG;
   return TQ_OK;
 }
 
@@ -456,10 +470,9 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.ctx = ctx;
   // K
   a.x = d_k;
-  a.codes = cache->k_codes;
-  a.norms = cache->k_norm;
-  a.signs = cache->k_signs;
-  a.rnorms = cache->k_rnorm;
+  a.bb = ctx->lay.bb;
+  a.cap16 = tq::cap16_of(cache->capacity);
+  set_role_planes(ctx, cache, 0, a.codes, a.norms, a.signs, a.rnorms);
   a.role = ctx->k;
   a.centroids = ctx->dparams->k_centroids;
   a.bounds = ctx->dparams->k_bounds;
@@ -467,10 +480,7 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
     // few vectors (a decode step): keys and values in one warp-per-vector launch
     tq::AppendArgs v = a;
     v.x = d_v;
-    v.codes = cache->v_codes;
-    v.norms = cache->v_norm;
-    v.signs = cache->v_signs;
-    v.rnorms = cache->v_rnorm;
+    set_role_planes(ctx, cache, 1, v.codes, v.norms, v.signs, v.rnorms);
     v.role = ctx->v;
     v.centroids = ctx->dparams->v_centroids;
     v.bounds = ctx->dparams->v_bounds;
@@ -489,10 +499,7 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   }
   // V on the caller's stream, then the caller's stream waits for K
   a.x = d_v;
-  a.codes = cache->v_codes;
-  a.norms = cache->v_norm;
-  a.signs = cache->v_signs;
-  a.rnorms = cache->v_rnorm;
+  set_role_planes(ctx, cache, 1, a.codes, a.norms, a.signs, a.rnorms);
   a.role = ctx->v;
   a.centroids = ctx->dparams->v_centroids;
   a.bounds = ctx->dparams->v_bounds;
@@ -576,11 +583,15 @@ tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int
     a.t1 = t1;
     a.params = ctx->dparams;
     a.out = out;
+    a.bb = ctx->lay.bb;
+    a.cap16 = tq::cap16_of(cache->capacity);
+    uint8_t *codes, *signs;
+    float *norms, *rnorms;
+    set_role_planes(ctx, cache, which, codes, norms, signs, rnorms);
+    a.codes = codes; a.norms = norms; a.signs = signs; a.rnorms = rnorms;
     if (which == 0) {
-      a.codes = cache->k_codes; a.norms = cache->k_norm; a.signs = cache->k_signs; a.rnorms = cache->k_rnorm;
       a.role = ctx->k; a.centroids = ctx->dparams->k_centroids;
     } else {
-      a.codes = cache->v_codes; a.norms = cache->v_norm; a.signs = cache->v_signs; a.rnorms = cache->v_rnorm;
       a.role = ctx->v; a.centroids = ctx->dparams->v_centroids;
     }
     s = (tq_status)tq::launch_dequant_tq(a, stream);

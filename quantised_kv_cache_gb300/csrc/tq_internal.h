@@ -52,6 +52,26 @@ struct Role {
   bool qjl = false;
 };
 
+// Blocked record layout of the TQ schemes: 16-token blocks of `bb` bytes; plane p holds
+// tok[p] bytes per token at byte offset off[p] of its block (tq_plane order).
+constexpr int kBlockTokens = 16;
+struct RecLayout {
+  int bb = 0;
+  int off[TQ_NUM_PLANES] = {};
+  int tok[TQ_NUM_PLANES] = {};
+};
+
+// Byte offset of token slot `slot` = sequence-head * cap16 + t (cap16 = the capacity rounded up
+// to whole blocks) in a plane of the blocked layout, from that plane's offset in block 0.
+__host__ __device__ __forceinline__ long long rec_off(long long slot, int bb, int tok) {
+  return (slot >> 4) * (long long)bb + (long long)(slot & 15) * tok;
+}
+template <typename T>
+__host__ __device__ __forceinline__ T *rec_at(T *plane, long long slot, int bb, int tok) {
+  return reinterpret_cast<T *>(reinterpret_cast<uintptr_t>(plane) + rec_off(slot, bb, tok));
+}
+__host__ __device__ __forceinline__ int cap16_of(int capacity) { return (capacity + 15) & ~15; }
+
 }  // namespace tq
 
 struct tq_ctx {
@@ -62,6 +82,7 @@ struct tq_ctx {
   int device = 0;
   int num_sms = 0;  // of `device`
   tq::Role k, v;
+  tq::RecLayout lay;  // TQ schemes
   // KIVI options
   int kivi_group = 32;
   int kivi_window = 128;
@@ -92,10 +113,12 @@ struct AppendArgs {
   int dtype;             // TQ_F32 / TQ_BF16
   int batch, heads, n_new, capacity;
   const int32_t *seq_lens;
+  // plane bases (block 0) of this role in the blocked records; slot = sequence-head * cap16 + t
   uint8_t *codes;
   float *norms;
   uint8_t *signs;
   float *rnorms;
+  int bb, cap16;
   Role role;
   const float *centroids;  // device pointers into DevParams
   const float *bounds;
@@ -157,10 +180,11 @@ int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream);
 int launch_decode_kivi(const DecodeArgs &a, void *stream);
 
 struct DequantArgs {
-  const uint8_t *codes;
+  const uint8_t *codes;  // plane bases in the blocked records (see AppendArgs)
   const float *norms;
   const uint8_t *signs;
   const float *rnorms;
+  int bb, cap16;
   int batch, heads, capacity, t0, t1;
   Role role;
   const float *centroids;

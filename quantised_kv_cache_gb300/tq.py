@@ -41,18 +41,22 @@ _sz = ctypes.c_size_t
 
 
 class tq_cache(ctypes.Structure):
-    _fields_ = [("batch", _i), ("heads_kv", _i), ("capacity", _i),
-                ("k_codes", _vp), ("k_norm", _vp), ("k_signs", _vp), ("k_rnorm", _vp),
-                ("v_codes", _vp), ("v_norm", _vp), ("v_signs", _vp), ("v_rnorm", _vp),
+    _fields_ = [("batch", _i), ("heads_kv", _i), ("capacity", _i), ("records", _vp),
+                ("k_codes", _vp), ("v_codes", _vp),
                 ("k_stats", _vp), ("v_stats", _vp), ("k_window", _vp), ("v_window", _vp)]
 
 
-PLANES = ["k_codes", "k_norm", "k_signs", "k_rnorm", "v_codes", "v_norm", "v_signs", "v_rnorm",
-          "k_stats", "v_stats", "k_window", "v_window"]
+# the planes of a block of the records array (TQ schemes), in storage order (tq_plane)
+RECORD_PLANES = ["k_codes", "k_norm", "k_signs", "k_rnorm", "v_codes", "v_norm", "v_signs", "v_rnorm"]
+# separately allocated arrays (records for TQ schemes; the KIVI planes)
+ARRAYS = ["records", "k_codes", "v_codes", "k_stats", "v_stats", "k_window", "v_window"]
+BLOCK_TOKENS = 16
 
 
 class tq_cache_sizes(ctypes.Structure):
-    _fields_ = [(p, _sz) for p in PLANES] + [("record_bytes", _sz)]
+    _fields_ = [("records", _sz), ("block_bytes", _sz), ("plane_offset", _sz * 8), ("plane_bytes", _sz * 8),
+                ("k_codes", _sz), ("v_codes", _sz), ("k_stats", _sz), ("v_stats", _sz), ("k_window", _sz),
+                ("v_window", _sz), ("record_bytes", _sz)]
 
 
 _SIGNATURES = {
@@ -318,15 +322,17 @@ class Context:
 
 
 class Cache:
-    """Cache planes allocated as torch uint8 tensors on `device` (16-byte aligned)."""
+    """A cache's arrays as torch uint8 tensors on `device` (16-byte aligned): for the TQ
+    schemes one blocked records array, for KIVI its planes."""
 
     def __init__(self, ctx: Context, batch: int, heads_kv: int, capacity: int, device="cuda"):
         self.sizes = tq_cache_sizes_get(ctx.handle, batch, heads_kv, capacity)
         self.device = torch.device(device)
+        self.batch, self.heads_kv, self.capacity = batch, heads_kv, capacity
         self.tensors = {}
         self.struct = tq_cache()
         self.struct.batch, self.struct.heads_kv, self.struct.capacity = batch, heads_kv, capacity
-        for p in PLANES:
+        for p in ARRAYS:
             n = getattr(self.sizes, p)
             if n:
                 t = torch.zeros(n, dtype=torch.uint8, device=self.device)
@@ -337,7 +343,19 @@ class Cache:
                 setattr(self.struct, p, None)
 
     def plane(self, name: str) -> torch.Tensor:
-        return self.tensors[name]
+        """One plane as a contiguous uint8 tensor over [batch][heads_kv][capacity] token
+        slots (a copy gathered out of the blocks for the TQ schemes' record planes)."""
+        if "records" not in self.tensors or name not in RECORD_PLANES:
+            return self.tensors[name]
+        p = RECORD_PLANES.index(name)
+        tok = self.sizes.plane_bytes[p]
+        if tok == 0:
+            raise KeyError(name)
+        bb, off = self.sizes.block_bytes, self.sizes.plane_offset[p]
+        nblk = (self.capacity + BLOCK_TOKENS - 1) // BLOCK_TOKENS
+        blocks = self.tensors["records"].view(self.batch * self.heads_kv, nblk, bb)
+        planes = blocks[:, :, off:off + BLOCK_TOKENS * tok].reshape(self.batch * self.heads_kv, nblk * BLOCK_TOKENS * tok)
+        return planes[:, :self.capacity * tok].contiguous().view(-1)
 
     @property
     def record_bytes(self) -> int:

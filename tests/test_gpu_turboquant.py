@@ -87,6 +87,48 @@ def test_append_codes_bit_exact(scheme, n, dtype, shape):
             np.testing.assert_allclose(gpu.rnorm, ora.rnorm, rtol=1e-5, atol=1e-7)
 
 
+@pytest.mark.parametrize("scheme,n", [("KQV", 4), ("QKQV", 3), ("KV", 2)])
+def test_cache_sizes_describe_the_blocked_layout(scheme, n):
+    ctx = tq.Context(128, n, scheme, 1)
+    s = tq.tq_cache_sizes_get(ctx.handle, 3, 2, 50)
+    rk, rv = otq.scheme_roles(scheme, n)
+    tok = [rk.bits * 16, 4, 16 if rk.qjl else 0, 4 if rk.qjl else 0,
+           rv.bits * 16, 4, 16 if rv.qjl else 0, 4 if rv.qjl else 0]
+    assert list(s.plane_bytes) == tok
+    assert list(s.plane_offset) == [16 * sum(tok[:p]) for p in range(8)]
+    assert s.block_bytes == 16 * sum(tok) == 16 * s.record_bytes
+    assert s.records == 3 * 2 * 4 * s.block_bytes  # ceil(50 / 16) = 4 blocks per sequence-head
+
+
+def test_a_token_lands_where_the_layout_says():
+    # one token of sequence-head (b=1, h=0) at slot 37 of a capacity-50 cache: block
+    # (1 * 2 + 0) * 4 + 37 // 16 = 10, entry 37 % 16 = 5 of each plane
+    B, H, cap, t = 2, 2, 50, 37
+    ctx = tq.Context(128, 4, "KQV", 3)
+    cache = tq.Cache(ctx, B, H, cap)
+    g = torch.Generator().manual_seed(4)
+    k = torch.randn(B, H, 1, 128, generator=g)
+    v = torch.randn(B, H, 1, 128, generator=g)
+    tq.tq_append_quantize(ctx.handle, cache, k.to(DEV), v.to(DEV), torch.full((B,), t, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    s = cache.sizes
+    raw = cache.tensors["records"].cpu().numpy()
+    blk = raw[10 * s.block_bytes:11 * s.block_bytes]
+    knorm = blk[s.plane_offset[1] + 5 * 4:s.plane_offset[1] + 6 * 4].view(np.float32)[0]
+    vnorm = blk[s.plane_offset[5] + 5 * 4:s.plane_offset[5] + 6 * 4].view(np.float32)[0]
+    np.testing.assert_allclose(knorm, float(k[1, 0, 0].double().norm()), rtol=1e-6)
+    np.testing.assert_allclose(vnorm, float(v[1, 0, 0].double().norm()), rtol=1e-6)
+    # every other entry of the cache is still zero
+    raw_other = raw.copy()
+    raw_other[10 * s.block_bytes:11 * s.block_bytes] = 0
+    for b in range(B):
+        for h in range(H):
+            if (b, h) != (1, 0):
+                blk2 = (b * H + h) * 4 + 2
+                raw_other[blk2 * s.block_bytes:(blk2 + 1) * s.block_bytes] = 0
+    assert not raw_other.any()
+
+
 def test_append_writes_only_its_slots_and_reports_capacity():
     B, H = 2, 2
     _, k, v = _inputs(B, H, 10, torch.float32, seed=3)
