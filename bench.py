@@ -420,28 +420,54 @@ def main():
 
     # ---------------- end to end through the ABI with host buffers
     pin = [(q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()) for q, kn, vn in pool]
-    dq = torch.empty_like(pool[0][0])
-    dk = torch.empty_like(pool[0][1])
-    dv = torch.empty_like(pool[0][2])
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = dq.numel() * dq.element_size() + dk.numel() * dk.element_size() + dv.numel() * dv.element_size()
-    d2h = host_out.numel() * host_out.element_size()
+    # two sets of device inputs / outputs: step i + 1's inputs are copied in on a copy stream
+    # while step i computes, and step i's output is copied out while step i + 1 computes
+    # (every step still moves its own inputs in and its own output out)
+    dev_in = [tuple(torch.empty_like(x) for x in pool[0]) for _ in range(2)]
+    dev_out = [torch.empty_like(out) for _ in range(2)]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(x.numel() * x.element_size() for x in dev_in[0])
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    compute = torch.cuda.current_stream()
+    copy_s = torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+    for e in in_free + out_free:
+        e.record(compute)
+
+    def stage_in(i):
+        j = i % 2
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(in_free[j])
+            for dst, src in zip(dev_in[j], pin[i % len(pin)]):
+                dst.copy_(src, non_blocking=True)
+            in_ready[j].record(copy_s)
 
     def e2e_step(i):
-        hq, hk, hv = pin[i % len(pin)]
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
+        j = i % 2
+        dq, dk, dv = dev_in[j]
+        compute.wait_event(in_ready[j])
+        compute.wait_event(out_free[j])
         tq.tq_append_quantize(ctx.handle, cache, dk, dv, lens_append)
-        tq.tq_decode_attention(ctx.handle, cache, dq, lens_decode, CAP, 0, ws, out)
-        host_out.copy_(out, non_blocking=True)
+        tq.tq_decode_attention(ctx.handle, cache, dq, lens_decode, CAP, 0, ws, dev_out[j])
+        in_free[j].record(compute)
+        out_ready[j].record(compute)
+        stage_in(i + 1)
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(out_ready[j])
+            host_out[j].copy_(dev_out[j], non_blocking=True)
+            out_free[j].record(copy_s)
 
+    stage_in(0)
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()
+    stage_in(0)  # the first step's inputs, inside the timed region
     for i in range(K):
         e2e_step(i)
     torch.cuda.synchronize()
