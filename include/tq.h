@@ -54,6 +54,12 @@
  *  block (b * heads_kv + h) * ceil(capacity / 16) + t / 16, entry t % 16 of
  *  each plane, and the 16 tokens of a block are one contiguous copy
  *  (tq_cache_sizes gives the block size and the plane offsets).
+ *  Exception: the V code plane of a block is not [16][record] but eight pair
+ *  rows of d*b_V/4 bytes: row j holds tokens 2j and 2j+1, coordinate i in
+ *  field 16 (i mod 8) + i / 8 (d = 128) of 2*b_V bits at bit 2*b_V*field of
+ *  the row's little-endian bit string, token 2j's index in the low b_V bits and
+ *  token 2j+1's in the high ones (two tokens' codes of one coordinate side by
+ *  side, the operand order of the decode's tensor-core value sums).
  *
  *  Code records: a vector's d coordinates each get a b-bit index into the
  *  Lloyd-Max codebook (index 0 = the most negative centroid). The d/2

@@ -25,6 +25,7 @@ constexpr int kVecPerWarp = 8;
 struct AppendKernelArgs {
   const void *x;
   int batch, heads, n_new, capacity, cap16, bb;
+  int vt;  // value role: codes in the pair-interleaved layout (merged atomically)
   const int32_t *seq_lens;
   uint8_t *codes;
   float *norms;
@@ -119,7 +120,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) append_tq_kernel(AppendKernelA
       const uint32_t fb = (uint32_t)idx[2] | ((uint32_t)idx[3] << BITS);
       const uint32_t word = pack_slot_word<BITS>(fa, fb, lane);
       if (ok) {
-        if (lane < 4 * BITS) reinterpret_cast<uint32_t *>(rec_at(a.codes, slot, a.bb, BITS * kD / 8))[lane] = word;
+        if (a.vt) {
+          uint32_t *row = vt_row<BITS>(a.codes, slot, a.bb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) store_code_vt<BITS>(row, 4 * lane + j, (int)(slot & 1), (uint32_t)idx[j]);
+        } else if (lane < 4 * BITS) {
+          reinterpret_cast<uint32_t *>(rec_at(a.codes, slot, a.bb, BITS * kD / 8))[lane] = word;
+        }
         if (!QJL && lane == 0) *rec_at(a.norms, slot, a.bb, 4) = nu;
       }
       if (QJL) {
@@ -248,6 +255,7 @@ int launch_append_tq(const AppendArgs &a, void *stream) {
   k.capacity = a.capacity;
   k.cap16 = a.cap16;
   k.bb = a.bb;
+  k.vt = a.vt;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;
   k.norms = a.norms;

@@ -24,6 +24,7 @@ namespace {
 struct Append2Args {
   const void *x;
   int batch, heads, n_new, capacity, cap16, bb;
+  int vt;  // value role: codes in the pair-interleaved layout (merged atomically)
   const int32_t *seq_lens;
   uint8_t *codes;
   float *norms;
@@ -138,9 +139,35 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
       word[off >> 5] |= (uint32_t)code << (off & 31);
       if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= (uint32_t)code >> (32 - (off & 31));
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(rec_at(a.codes, slot, a.bb, BITS * kD / 8));
+    if (a.vt) {
+      // this token's half of every field of its pair row: code offset n = 32 q + 2 m + e
+      // holds coordinate 8 m + 2 q + e, whose field is vt_field() = 32 q + 16 e + m
+      uint32_t *row = vt_row<BITS>(a.codes, slot, a.bb);
+      const int half = (int)(slot & 1);
 #pragma unroll
-    for (int k = 0; k < BITS; ++k) dst[k] = make_uint4(word[4 * k], word[4 * k + 1], word[4 * k + 2], word[4 * k + 3]);
+      for (int q = 0; q < 4; ++q) {
+        uint32_t cw[32], w[2 * BITS], ones[32], own[2 * BITS];
+#pragma unroll
+        for (int n = 0; n < 32; ++n) {
+          const int off = BITS * (32 * q + n);
+          uint32_t v = word[off >> 5] >> (off & 31);
+          if ((off & 31) + BITS > 32) v |= word[(off >> 5) + 1] << (32 - (off & 31));
+          cw[n] = v & ((1u << BITS) - 1u);
+          ones[n] = (1u << BITS) - 1u;
+        }
+        vt_spread<BITS>(cw, half, w);
+        vt_spread<BITS>(ones, half, own);
+#pragma unroll
+        for (int i = 0; i < 2 * BITS; ++i) {
+          atomicAnd(row + 2 * BITS * q + i, ~own[i]);
+          atomicOr(row + 2 * BITS * q + i, w[i]);
+        }
+      }
+    } else {
+      uint4 *dst = reinterpret_cast<uint4 *>(rec_at(a.codes, slot, a.bb, BITS * kD / 8));
+#pragma unroll
+      for (int k = 0; k < BITS; ++k) dst[k] = make_uint4(word[4 * k], word[4 * k + 1], word[4 * k + 2], word[4 * k + 3]);
+    }
     *rec_at(a.norms, slot, a.bb, 4) = nu;
   }
 }
@@ -186,6 +213,7 @@ int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.capacity = a.capacity;
   k.cap16 = a.cap16;
   k.bb = a.bb;
+  k.vt = a.vt;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;
   k.norms = a.norms;

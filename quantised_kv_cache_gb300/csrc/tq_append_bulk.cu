@@ -248,7 +248,7 @@ __device__ __forceinline__ void certify_rounds(uint32_t r_hi, const float *sperm
   }
 }
 
-template <int BITS, bool QJL>
+template <int BITS, bool QJL, bool VT>
 __global__ void __launch_bounds__(kBulkThreads, 1)
     append_bulk_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ BulkArgs a) {
   using G = BulkGeo<QJL>;
@@ -387,6 +387,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.cap16 + len + t;
         else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
       }
+      // value codes: is the other token of this token's pair (slot ^ 1) the neighbouring lane's?
+      bool paired = false;
+      if (VT) {
+        const long long ps = ((long long)__shfl_xor_sync(kFull, (int)(slot >> 32), 1) << 32) |
+                             (uint32_t)__shfl_xor_sync(kFull, (int)(uint32_t)slot, 1);
+        paired = slot >= 0 && ps >= 0 && ps == (slot ^ 1);
+      }
       if (*s_abort || !__all_sync(kFull, mbar_wait_bounded(&y_full[g], (uint32_t)par, a.error))) {
         *s_abort = 1;
         break;
@@ -419,14 +426,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       float rr = 0.f;
       uint32_t *crec = reinterpret_cast<uint32_t *>(rec_at(a.codes, slot >= 0 ? slot : 0, a.bb, BITS * kD / 8));
       auto chunk_codes = [&](uint32_t (&yz)[32], int c) {
-        uint32_t word[BITS];
+        // key records: BITS words per chunk in code-offset order; value codes: the chunk's
+        // 32 fields of the pair row (2 BITS words), this token's half only
+        constexpr int NW = VT ? 2 * BITS : BITS;
+        uint32_t word[NW];
 #pragma unroll
-        for (int w = 0; w < BITS; ++w) word[w] = 0u;
+        for (int w = 0; w < NW; ++w) word[w] = 0u;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           float cneg;
           const uint32_t code = encode1<BITS, QJL>(__uint_as_float(yz[j]), P, CP, cneg);
-          const int off = BITS * j;
+          const int off = VT ? 2 * BITS * (16 * (j & 1) + (j >> 1)) : BITS * j;
           word[off >> 5] |= code << (off & 31);
           if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= code >> (32 - (off & 31));
           if (QJL) {
@@ -435,7 +445,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             yz[j] = __float_as_uint(r);
           }
         }
-        if (slot >= 0) {
+        if constexpr (VT) {
+          const int half = (int)(slot & 1);
+          if (half) {  // this token's codes go to the high half of each field
+#pragma unroll
+            for (int i = NW - 1; i > 0; --i) word[i] = (word[i] << BITS) | (word[i - 1] >> (32 - BITS));
+            word[0] <<= BITS;
+          }
+          vt_store_chunk<BITS>(vt_row<BITS>(a.codes, slot >= 0 ? slot : 0, a.bb), c, word, half, paired,
+                               slot >= 0);
+        } else if (slot >= 0) {
 #pragma unroll
           for (int w = 0; w < BITS; ++w) crec[BITS * c + w] = word[w];
         }
@@ -555,7 +574,7 @@ EncodeTiledFn encode_fn() {
 
 int g_sms_bulk = 0;
 
-template <int BITS, bool QJL>
+template <int BITS, bool QJL, bool VT>
 int go_bulk(const CUtensorMap &map, const BulkArgs &k, long long ntiles, cudaStream_t st) {
   if (g_sms_bulk == 0) {
     int dev = 0;
@@ -564,7 +583,7 @@ int go_bulk(const CUtensorMap &map, const BulkArgs &k, long long ntiles, cudaStr
     if (g_sms_bulk <= 0) g_sms_bulk = 152;
   }
   using G = BulkGeo<QJL>;
-  auto fn = append_bulk_kernel<BITS, QJL>;
+  auto fn = append_bulk_kernel<BITS, QJL, VT>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, G::total) != cudaSuccess)
@@ -623,19 +642,36 @@ int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   for (int i = 0; i < (1 << a.role.bits); ++i) k.centroids[i] = csrc[i];
   const long long ntiles = (total + kTV - 1) / kTV;
   cudaStream_t st = (cudaStream_t)stream;
+  if (a.role.qjl && a.vt) {
+    switch (a.role.bits) {
+      case 1: return go_bulk<1, true, true>(map, k, ntiles, st);
+      case 2: return go_bulk<2, true, true>(map, k, ntiles, st);
+      case 3: return go_bulk<3, true, true>(map, k, ntiles, st);
+      default: return TQ_ERR_UNSUPPORTED;
+    }
+  }
   if (a.role.qjl) {
     switch (a.role.bits) {
-      case 1: return go_bulk<1, true>(map, k, ntiles, st);
-      case 2: return go_bulk<2, true>(map, k, ntiles, st);
-      case 3: return go_bulk<3, true>(map, k, ntiles, st);
+      case 1: return go_bulk<1, true, false>(map, k, ntiles, st);
+      case 2: return go_bulk<2, true, false>(map, k, ntiles, st);
+      case 3: return go_bulk<3, true, false>(map, k, ntiles, st);
+      default: return TQ_ERR_UNSUPPORTED;
+    }
+  }
+  if (a.vt) {
+    switch (a.role.bits) {
+      case 1: return go_bulk<1, false, true>(map, k, ntiles, st);
+      case 2: return go_bulk<2, false, true>(map, k, ntiles, st);
+      case 3: return go_bulk<3, false, true>(map, k, ntiles, st);
+      case 4: return go_bulk<4, false, true>(map, k, ntiles, st);
       default: return TQ_ERR_UNSUPPORTED;
     }
   }
   switch (a.role.bits) {
-    case 1: return go_bulk<1, false>(map, k, ntiles, st);
-    case 2: return go_bulk<2, false>(map, k, ntiles, st);
-    case 3: return go_bulk<3, false>(map, k, ntiles, st);
-    case 4: return go_bulk<4, false>(map, k, ntiles, st);
+    case 1: return go_bulk<1, false, false>(map, k, ntiles, st);
+    case 2: return go_bulk<2, false, false>(map, k, ntiles, st);
+    case 3: return go_bulk<3, false, false>(map, k, ntiles, st);
+    case 4: return go_bulk<4, false, false>(map, k, ntiles, st);
     default: return TQ_ERR_UNSUPPORTED;
   }
 }

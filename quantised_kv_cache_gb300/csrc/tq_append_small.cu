@@ -35,7 +35,7 @@ struct SmallRole {
   float *norms;
   uint8_t *signs;
   float *rnorms;
-  int bits, rotate, qjl;
+  int bits, rotate, qjl, vt;
   float bounds[kMaxLevels];  // 2^bits - 1 used, +inf after
   float centroids[kMaxLevels];
 };
@@ -56,6 +56,17 @@ __device__ __forceinline__ void store_codes(uint8_t *codes, long long slot, int 
   const uint32_t word = pack_slot_word<BITS>(fa, fb, lane);  // every lane takes part
   if (slot >= 0 && lane < 4 * BITS)
     reinterpret_cast<uint32_t *>(rec_at(codes, slot, bb, BITS * kD / 8))[lane] = word;
+}
+
+// value codes (pair-interleaved layout): each lane merges its four codes into the
+// token pair's row atomically (the partner token's bits are left alone)
+template <int VB>
+__device__ __forceinline__ void store_codes_vt(uint8_t *vplane, long long slot, int bb, const int (&idx)[4],
+                                               int lane) {
+  if (slot < 0) return;
+  uint32_t *row = vt_row<VB>(vplane, slot, bb);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) store_code_vt<VB>(row, 4 * lane + k, (int)(slot & 1), (uint32_t)idx[k]);
 }
 
 template <bool BF16>
@@ -112,11 +123,20 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
       for (int k = 0; k < kMaxLevels - 1; ++k) c += (y[j] >= ro.bounds[k]) ? 1 : 0;
       idx[j] = c;
     }
-    switch (ro.bits) {
-      case 1: store_codes<1>(ro.codes, slot, a.bb, idx, lane); break;
-      case 2: store_codes<2>(ro.codes, slot, a.bb, idx, lane); break;
-      case 3: store_codes<3>(ro.codes, slot, a.bb, idx, lane); break;
-      default: store_codes<4>(ro.codes, slot, a.bb, idx, lane); break;
+    if (ro.vt) {
+      switch (ro.bits) {
+        case 1: store_codes_vt<1>(ro.codes, slot, a.bb, idx, lane); break;
+        case 2: store_codes_vt<2>(ro.codes, slot, a.bb, idx, lane); break;
+        case 3: store_codes_vt<3>(ro.codes, slot, a.bb, idx, lane); break;
+        default: store_codes_vt<4>(ro.codes, slot, a.bb, idx, lane); break;
+      }
+    } else {
+      switch (ro.bits) {
+        case 1: store_codes<1>(ro.codes, slot, a.bb, idx, lane); break;
+        case 2: store_codes<2>(ro.codes, slot, a.bb, idx, lane); break;
+        case 3: store_codes<3>(ro.codes, slot, a.bb, idx, lane); break;
+        default: store_codes<4>(ro.codes, slot, a.bb, idx, lane); break;
+      }
     }
     if (!qjl && slot >= 0 && lane == 0) *rec_at(ro.norms, slot, a.bb, 4) = nu;
     if (qjl) {
@@ -227,6 +247,7 @@ int launch_append_small(const AppendArgs &k, const AppendArgs &v, const tq_ctx *
     o.norms = x.norms;
     o.signs = x.signs;
     o.rnorms = x.rnorms;
+    o.vt = x.vt;
     fill_role(o, x.role, r == 0 ? ctx->k_bounds : ctx->v_bounds, r == 0 ? ctx->k_centroids : ctx->v_centroids);
   }
   s.batch = k.batch;

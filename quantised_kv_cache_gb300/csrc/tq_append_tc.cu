@@ -44,6 +44,7 @@ namespace {
 struct TcArgs {
   const void *x;
   int batch, heads, n_new, capacity, cap16, bb;
+  int vt;  // value role: codes in the pair-interleaved layout
   const int32_t *seq_lens;
   uint8_t *codes;
   float *norms;
@@ -282,14 +283,21 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
     for (int k = 0; k < H; ++k) P[k] = a.bounds[L / 2 + k] * sv;
     float rr = 0.f;
     uint32_t *crec = reinterpret_cast<uint32_t *>(rec_at(a.codes, slot >= 0 ? slot : 0, a.bb, BITS * kD / 8));
+    // value codes: is the other token of this token's pair (slot ^ 1) the neighbouring lane's?
+    const long long pslot = ((long long)__shfl_xor_sync(kFull, (int)(slot >> 32), 1) << 32) |
+                            (uint32_t)__shfl_xor_sync(kFull, (int)(uint32_t)slot, 1);
+    const bool paired = slot >= 0 && pslot >= 0 && pslot == (slot ^ 1);
+    const int half = (int)(slot & 1);
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       uint32_t yz[32];
       __syncwarp();  // tcgen05.ld / st are warp-collective
       tmem_ld_x32(tlane + 32 * q, yz);
-      uint32_t word[BITS];
+      // key records: BITS words per chunk in code-offset order; value codes: the chunk's 32
+      // fields of the pair row (2 BITS words), this token's half
+      uint32_t word[2 * BITS], vw[2 * BITS];
 #pragma unroll
-      for (int w = 0; w < BITS; ++w) word[w] = 0u;
+      for (int w = 0; w < 2 * BITS; ++w) word[w] = vw[w] = 0u;
       uint32_t rh[16], rl[16];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -299,6 +307,9 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
         const int off = BITS * j;
         word[off >> 5] |= (uint32_t)code << (off & 31);
         if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= (uint32_t)code >> (32 - (off & 31));
+        const int voff = 2 * BITS * (16 * (j & 1) + (j >> 1));
+        vw[voff >> 5] |= (uint32_t)code << (voff & 31);
+        if ((voff & 31) + BITS > 32) vw[(voff >> 5) + 1] |= (uint32_t)code >> (32 - (voff & 31));
         if (QJL) {
           float cm = CP[0];
 #pragma unroll
@@ -309,7 +320,14 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
           yz[j] = __float_as_uint(r);
         }
       }
-      if (slot >= 0) {
+      if (a.vt) {  // warp-uniform
+        if (half) {
+#pragma unroll
+          for (int i = 2 * BITS - 1; i > 0; --i) vw[i] = (vw[i] << BITS) | (vw[i - 1] >> (32 - BITS));
+          vw[0] <<= BITS;
+        }
+        vt_store_chunk<BITS>(vt_row<BITS>(a.codes, slot >= 0 ? slot : 0, a.bb), q, vw, half, paired, slot >= 0);
+      } else if (slot >= 0) {
 #pragma unroll
         for (int w = 0; w < BITS; ++w) crec[BITS * q + w] = word[w];
       }
@@ -477,6 +495,7 @@ int launch_append_tc(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.capacity = a.capacity;
   k.cap16 = a.cap16;
   k.bb = a.bb;
+  k.vt = a.vt;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;
   k.norms = a.norms;

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
       if (t >= t_end) break;
       const int src = lane_of_tile_token(jj);
       uint32_t code[4];
-      lane_codes<VB>(rec32(a.v_codes, t, VB * 16), lane, code);
+      lane_codes_vt<VB>(a.v_codes, slot0 + t, a.bb, lane, code);  // pair-interleaved value codes
       float c[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) c[j] = s_cb[16 + code[j]];

@@ -28,8 +28,9 @@
 // * values and QJL signs: the p-weighted sums over a warp's 16 tokens run on
 //   the tensor cores (mma.sync m16n8k16, fp32 accumulate) into ONE accumulator:
 //   B column 0/1 carry the fp16 hi/lo parts of p nu (values), columns 2/3 the
-//   hi/lo parts of p rho (signs). Value codes are decoded to fp16 pairs through
-//   a per-lane replicated table and transposed with movmatrix; a sign bit
+//   hi/lo parts of p rho (signs). Value codes are stored pair-interleaved (two
+//   tokens' codes of one coordinate side by side), so one lookup in a per-lane
+//   replicated table gives an A-fragment register directly; a sign bit
 //   becomes a power of two (its bit moved into the fp16 exponent field by one
 //   rotate, isolated by one AND), undone per accumulator row at the merge.
 //
@@ -386,15 +387,16 @@ __device__ __forceinline__ void tile_body(const unsigned char *st, const unsigne
     }
   }
 
-  // ---- values: decode (token, coordinate-pair) fp16 pairs, transpose, MMA
+  // ---- values: pair-table lookups give the A fragments (coordinates x token pairs), MMA
   {
+    // pair-interleaved value codes: rows t4 and t4 + 4 (tokens 2t4, 2t4 + 1 and
+    // 2t4 + 8, 2t4 + 9), the 16 fields of coordinates g (mod 8) at words VB g ..
     uint32_t w0[VB], w1[VB];
-    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + g) * Gm::vc);
-    const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Gm::off_vc + (wbase + 8 + g) * Gm::vc);
+    const uint32_t *vrow = reinterpret_cast<const uint32_t *>(st + Gm::off_vc);
 #pragma unroll
     for (int k = 0; k < VB; ++k) {
-      w0[k] = r0[VB * t4 + k];
-      w1[k] = r1[VB * t4 + k];
+      w0[k] = vrow[VB * (8 * t4 + g) + k];
+      w1[k] = vrow[VB * (8 * (t4 + 4) + g) + k];
     }
     // field n of a span -> byte offset (field << 7) | (lane << 2) of the value table
     auto lut = [&](const uint32_t(&w)[VB], int n) -> uint32_t {
@@ -408,11 +410,8 @@ __device__ __forceinline__ void tile_body(const unsigned char *st, const unsigne
     };
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
-      const uint32_t x00 = movmatrix_t(lut(w0, 2 * mb));
-      const uint32_t x01 = movmatrix_t(lut(w0, 2 * mb + 1));
-      const uint32_t x10 = movmatrix_t(lut(w1, 2 * mb));
-      const uint32_t x11 = movmatrix_t(lut(w1, 2 * mb + 1));
-      mma_16816(ws.acc[mb], x00, x01, x10, x11, bv0, bv1);
+      // A fragment: rows coordinates 16 mb + g, 16 mb + 8 + g; columns the token pairs
+      mma_16816(ws.acc[mb], lut(w0, 2 * mb), lut(w0, 2 * mb + 1), lut(w1, 2 * mb), lut(w1, 2 * mb + 1), bv0, bv1);
     }
   }
 
@@ -877,15 +876,16 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
       gather(xh, xl, bs0, bs1);
     }
   }
-  // ---- values: as in the one-head body (pair table + movmatrix), G heads in the columns
+  // ---- values: as in the one-head body (pair-table A fragments), G heads in the columns
   {
+    // pair-interleaved value codes: rows t4 and t4 + 4 (tokens 2t4, 2t4 + 1 and
+    // 2t4 + 8, 2t4 + 9), the 16 fields of coordinates g (mod 8) at words VB g ..
     uint32_t w0[VB], w1[VB];
-    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(st + Q::off_vc + (wbase + g) * Q::vc);
-    const uint32_t *r1 = reinterpret_cast<const uint32_t *>(st + Q::off_vc + (wbase + 8 + g) * Q::vc);
+    const uint32_t *vrow = reinterpret_cast<const uint32_t *>(st + Q::off_vc);
 #pragma unroll
     for (int k = 0; k < VB; ++k) {
-      w0[k] = r0[VB * t4 + k];
-      w1[k] = r1[VB * t4 + k];
+      w0[k] = vrow[VB * (8 * t4 + g) + k];
+      w1[k] = vrow[VB * (8 * (t4 + 4) + g) + k];
     }
     auto lut = [&](const uint32_t(&w)[VB], int n) -> uint32_t {
       constexpr int F = 2 * VB;
@@ -898,11 +898,8 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
     };
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
-      const uint32_t x00 = movmatrix_t(lut(w0, 2 * mb));
-      const uint32_t x01 = movmatrix_t(lut(w0, 2 * mb + 1));
-      const uint32_t x10 = movmatrix_t(lut(w1, 2 * mb));
-      const uint32_t x11 = movmatrix_t(lut(w1, 2 * mb + 1));
-      mma_16816(acc_v[mb], x00, x01, x10, x11, bv0, bv1);
+      // A fragment: rows coordinates 16 mb + g, 16 mb + 8 + g; columns the token pairs
+      mma_16816(acc_v[mb], lut(w0, 2 * mb), lut(w0, 2 * mb + 1), lut(w1, 2 * mb), lut(w1, 2 * mb + 1), bv0, bv1);
     }
   }
   // ---- QJL signs (same operands as the one-head body), separate accumulator

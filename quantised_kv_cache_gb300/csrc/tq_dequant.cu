@@ -16,6 +16,7 @@ struct DequantKernelArgs {
   const uint8_t *signs;
   const float *rnorms;
   int bb, cap16;
+  int vt;  // value codes: pair-interleaved layout
   int batch, heads, capacity, t0, t1;
   const float *centroids;
   const float *diag;
@@ -37,7 +38,8 @@ __global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
   const int t = a.t0 + (int)(vec % n);
   const long long slot = (long long)bh * a.cap16 + t;
   uint32_t code[4];
-  lane_codes<BITS>(reinterpret_cast<const uint32_t *>(rec_at(a.codes, slot, a.bb, BITS * 16)), lane, code);
+  if (a.vt) lane_codes_vt<BITS>(a.codes, slot, a.bb, lane, code);
+  else lane_codes<BITS>(reinterpret_cast<const uint32_t *>(rec_at(a.codes, slot, a.bb, BITS * 16)), lane, code);
   const float nu = __ldg(rec_at(a.norms, slot, a.bb, 4));
   float y[4];
 #pragma unroll
@@ -85,7 +87,7 @@ int go(int bits, const DequantKernelArgs &k, unsigned blocks, cudaStream_t st) {
 }  // namespace
 
 int launch_dequant_tq(const DequantArgs &a, void *stream) {
-  DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.bb, a.cap16, a.batch, a.heads, a.capacity, a.t0, a.t1,
+  DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.bb, a.cap16, a.vt, a.batch, a.heads, a.capacity, a.t0, a.t1,
                       a.centroids, a.params->diag, a.params->sketch, a.out};
   const long long total = (long long)a.batch * a.heads * (a.t1 - a.t0);
   const unsigned blocks = (unsigned)((total + 7) / 8);

@@ -139,6 +139,108 @@ __device__ __forceinline__ uint32_t pack_slot_word(uint32_t field_a, uint32_t fi
   return word;
 }
 
+// ---------------------------------------------------------------------------
+// Value codes of the TQ schemes are stored pair-interleaved inside each
+// 16-token block: row j (j = 0..7) holds tokens 2j and 2j+1; coordinate c sits
+// in field o(c) = 16 (c mod 8) + c / 8 of the row, 2*VB bits at bit 2*VB*o, token
+// 2j's code in the low VB bits and token 2j+1's in the high VB bits. A row is
+// 32*VB bytes (8*VB words); the 16 fields of coordinates c = g (mod 8) are
+// contiguous (words VB*g .. VB*g + VB - 1), which is what a tensor-core thread of
+// group g reads as its A fragments (coordinate rows, token pairs).
+__host__ __device__ __forceinline__ int vt_field(int c) { return 16 * (c & 7) + (c >> 3); }
+
+// bit offset of (token slot's half, coordinate c) inside its row
+template <int VB>
+__device__ __forceinline__ int vt_bit(int c, int half) { return 2 * VB * vt_field(c) + VB * half; }
+
+// word pointer of the row holding token `slot` (block-0 base of the value-code plane)
+template <int VB>
+__device__ __forceinline__ uint32_t *vt_row(const uint8_t *vplane, long long slot, int bb) {
+  return reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(vplane) + (slot >> 4) * (long long)bb +
+                                      ((slot & 15) >> 1) * (32 * VB));
+}
+
+// Codes of coordinates 4L..4L+3 of token `slot` (warp-per-vector readers).
+template <int VB>
+__device__ __forceinline__ void lane_codes_vt(const uint8_t *vplane, long long slot, int bb, int lane,
+                                              uint32_t (&c)[4]) {
+  const uint32_t *row = vt_row<VB>(vplane, slot, bb);
+  const int h = (int)(slot & 1);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int bit = vt_bit<VB>(4 * lane + k, h), wi = bit >> 5, off = bit & 31;
+    uint32_t v = __ldg(row + wi) >> off;
+    if (off + VB > 32) v |= __ldg(row + wi + 1) << (32 - off);
+    c[k] = v & ((1u << VB) - 1u);
+  }
+}
+
+// Write one code (its VB bits only, the pair partner's bits untouched), atomically.
+template <int VB>
+__device__ __forceinline__ void store_code_vt(uint32_t *row, int c, int half, uint32_t code) {
+  const int bit = vt_bit<VB>(c, half), wi = bit >> 5, off = bit & 31;
+  constexpr uint32_t M = (1u << VB) - 1u;
+  atomicAnd(row + wi, ~(M << off));
+  atomicOr(row + wi, code << off);
+  if (off + VB > 32) {
+    atomicAnd(row + wi + 1, ~(M >> (32 - off)));
+    atomicOr(row + wi + 1, code >> (32 - off));
+  }
+}
+
+// Thread-per-vector writers: the codes of one chunk of 32 code offsets in the
+// key-record order (offset n = 32 t' + 2 m + e holds coordinate 8 m + 2 t' + e)
+// land in fields o = 32 t' + 16 e + m, i.e. words 2*VB*t' .. 2*VB*t' + 2*VB - 1 of
+// the row. vt_spread builds those words with this token's bits only (half h);
+// vt_store_chunk writes them: when the partner token (slot ^ 1) is the vector of
+// the neighbouring lane (lane ^ 1), the two lanes merge their words and each
+// stores half of them; otherwise each lane merges its bits atomically.
+template <int VB>
+__device__ __forceinline__ void vt_spread(const uint32_t (&code)[32], int half, uint32_t (&w)[2 * VB]) {
+#pragma unroll
+  for (int i = 0; i < 2 * VB; ++i) w[i] = 0u;
+#pragma unroll
+  for (int n = 0; n < 32; ++n) {
+    const int o = 16 * (n & 1) + (n >> 1);  // field within the chunk
+    const int bit = 2 * VB * o;
+    w[bit >> 5] |= code[n] << (bit & 31);
+    if ((bit & 31) + VB > 32) w[(bit >> 5) + 1] |= code[n] >> (32 - (bit & 31));
+  }
+  if (half) {  // move every code to the high half of its field (shift the 64*VB-bit span by VB)
+#pragma unroll
+    for (int i = 2 * VB - 1; i > 0; --i) w[i] = (w[i] << VB) | (w[i - 1] >> (32 - VB));
+    w[0] <<= VB;
+  }
+}
+
+template <int VB>
+__device__ __forceinline__ void vt_store_chunk(uint32_t *row, int chunk, const uint32_t (&w)[2 * VB], int half,
+                                               bool paired, bool valid) {
+  uint32_t *dst = row + 2 * VB * chunk;
+  uint32_t merged[2 * VB];
+#pragma unroll
+  for (int i = 0; i < 2 * VB; ++i) merged[i] = w[i] | __shfl_xor_sync(kFull, w[i], 1);
+  if (!valid) return;
+  if (paired) {
+#pragma unroll
+    for (int i = 0; i < VB; ++i) dst[VB * half + i] = merged[VB * half + i];
+  } else {
+    // this token's bits of every field of the chunk: VB ones at 2*VB*o + VB*half
+    uint32_t own[2 * VB];
+    {
+      uint32_t ones[32];
+#pragma unroll
+      for (int n = 0; n < 32; ++n) ones[n] = (1u << VB) - 1u;
+      vt_spread<VB>(ones, half, own);
+    }
+#pragma unroll
+    for (int i = 0; i < 2 * VB; ++i) {
+      atomicAnd(dst + i, ~own[i]);
+      atomicOr(dst + i, w[i]);
+    }
+  }
+}
+
 // KIVI records keep the plain order: channel i's 2-bit code at bits [2i, 2i+2).
 __device__ __forceinline__ uint32_t kivi_lane_field(const uint32_t *rec, int lane) {
   return __ldg(rec + (lane >> 2)) >> (8 * (lane & 3));  // 8 bits: channels 4L..4L+3

@@ -473,6 +473,7 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.bb = ctx->lay.bb;
   a.cap16 = tq::cap16_of(cache->capacity);
   set_role_planes(ctx, cache, 0, a.codes, a.norms, a.signs, a.rnorms);
+  a.vt = 0;
   a.role = ctx->k;
   a.centroids = ctx->dparams->k_centroids;
   a.bounds = ctx->dparams->k_bounds;
@@ -481,6 +482,7 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
     tq::AppendArgs v = a;
     v.x = d_v;
     set_role_planes(ctx, cache, 1, v.codes, v.norms, v.signs, v.rnorms);
+    v.vt = 1;
     v.role = ctx->v;
     v.centroids = ctx->dparams->v_centroids;
     v.bounds = ctx->dparams->v_bounds;
@@ -500,6 +502,7 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   // V on the caller's stream, then the caller's stream waits for K
   a.x = d_v;
   set_role_planes(ctx, cache, 1, a.codes, a.norms, a.signs, a.rnorms);
+  a.vt = 1;
   a.role = ctx->v;
   a.centroids = ctx->dparams->v_centroids;
   a.bounds = ctx->dparams->v_bounds;
@@ -585,6 +588,7 @@ tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int
     a.out = out;
     a.bb = ctx->lay.bb;
     a.cap16 = tq::cap16_of(cache->capacity);
+    a.vt = which;
     uint8_t *codes, *signs;
     float *norms, *rnorms;
     set_role_planes(ctx, cache, which, codes, norms, signs, rnorms);

@@ -119,6 +119,7 @@ struct AppendArgs {
   uint8_t *signs;
   float *rnorms;
   int bb, cap16;
+  int vt;  // 1: the value role (codes in the pair-interleaved layout)
   Role role;
   const float *centroids;  // device pointers into DevParams
   const float *bounds;
@@ -185,6 +186,7 @@ struct DequantArgs {
   const uint8_t *signs;
   const float *rnorms;
   int bb, cap16;
+  int vt;  // 1: value codes (pair-interleaved layout)
   int batch, heads, capacity, t0, t1;
   Role role;
   const float *centroids;

@@ -11,6 +11,7 @@ import os
 from dataclasses import dataclass
 from typing import Optional
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -321,6 +322,39 @@ class Context:
         return self.handle
 
 
+def _pair_rows_to_records(planes: torch.Tensor, vb: int) -> torch.Tensor:
+    """Value codes of [bh][block] planes (8 pair rows of 32*vb bytes each: row j holds
+    tokens 2j, 2j+1; coordinate c in field 16 (c mod 8) + c // 8 of 2*vb bits, token 2j in
+    the low vb bits) -> per-token code records in the key-record order (code offset n
+    holds coordinate 8 ((n >> 1) & 15) + 2 (n >> 5) + (n & 1), vb bits at bit vb n).
+    Runs with torch on the planes' device, a few blocks of sequence-heads at a time."""
+    dev = planes.device
+    bh, nblk = planes.shape[0], planes.shape[1]
+    # bit position, inside the block's plane, of (token t, the coordinate at code offset n)
+    t = torch.arange(16).view(16, 1)
+    n = torch.arange(128).view(1, 128)
+    coord = 8 * ((n >> 1) & 15) + 2 * (n >> 5) + (n & 1)
+    field = 16 * (coord % 8) + coord // 8
+    pos = (t // 2) * (256 * vb) + 2 * vb * field + vb * (t % 2)          # [16, 128]
+    byte0, shift = (pos // 8).to(dev), (pos % 8).to(dev)
+    byte1 = torch.clamp(byte0 + 1, max=256 * vb - 1)
+    # output record bit q (0 .. 128 vb - 1) = bit q % vb of the code at offset q // vb
+    q = torch.arange(128 * vb)
+    qn, qs = (q // vb).to(dev), (q % vb).to(dev)
+    weights = (1 << torch.arange(8, device=dev)).view(1, 1, 1, 8)
+    out = torch.empty((bh, nblk * 16, 16 * vb), dtype=torch.uint8, device=dev)
+    step = max(1, (1 << 15) // max(1, nblk))  # about 32K blocks (~1 GB of temporaries) per pass
+    for r0 in range(0, bh, step):
+        a = planes[r0:r0 + step].reshape(-1, 256 * vb).to(torch.int32)    # [rows, plane bytes]
+        word = a[:, byte0.view(-1)] | (a[:, byte1.view(-1)] << 8)          # [rows, 16 * 128]
+        codes = (word >> shift.view(1, -1)) & ((1 << vb) - 1)
+        codes = codes.view(-1, 16, 128)                                    # [rows, token, offset]
+        bits = (codes[:, :, qn] >> qs.view(1, 1, -1)) & 1                  # [rows, token, 128 vb]
+        packed = (bits.view(-1, 16, 16 * vb, 8) * weights).sum(-1).to(torch.uint8)
+        out[r0:r0 + step] = packed.view(-1, nblk * 16, 16 * vb)
+    return out
+
+
 class Cache:
     """A cache's arrays as torch uint8 tensors on `device` (16-byte aligned): for the TQ
     schemes one blocked records array, for KIVI its planes."""
@@ -353,8 +387,12 @@ class Cache:
             raise KeyError(name)
         bb, off = self.sizes.block_bytes, self.sizes.plane_offset[p]
         nblk = (self.capacity + BLOCK_TOKENS - 1) // BLOCK_TOKENS
-        blocks = self.tensors["records"].view(self.batch * self.heads_kv, nblk, bb)
-        planes = blocks[:, :, off:off + BLOCK_TOKENS * tok].reshape(self.batch * self.heads_kv, nblk * BLOCK_TOKENS * tok)
+        bh = self.batch * self.heads_kv
+        blocks = self.tensors["records"].view(bh, nblk, bb)
+        planes = blocks[:, :, off:off + BLOCK_TOKENS * tok]
+        if name == "v_codes":
+            return _pair_rows_to_records(planes, tok // 16)[:, :self.capacity].contiguous().view(-1)
+        planes = planes.reshape(bh, nblk * BLOCK_TOKENS * tok)
         return planes[:, :self.capacity * tok].contiguous().view(-1)
 
     @property
