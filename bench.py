@@ -36,10 +36,10 @@ CAP = 8192
 # this few vectors), query prep, decode attention, combine
 LAUNCHES_PER_STEP = 4
 # DRAM bytes (read + written) of one decode-kernel launch of this workload: an ncu capture of
-# the decode-small case (context 4096: 297.93 MB) scaled to context 8192 (the kernel reads every
+# the decode-small case (context 4096: 297.77 MB) scaled to context 8192 (the kernel reads every
 # token once, so traffic grows with the tokens); to be set to None whenever the kernel changes,
 # until it is captured again
-DECODE_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = 2 * 297_774_592
 
 
 def peaks():
