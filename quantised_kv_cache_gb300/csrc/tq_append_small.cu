@@ -89,6 +89,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
     }
     if (tid < kSmallWarps * 4) s_sw[tid] = 0u;
   }
+  // the inputs and the cache may be written by the kernel before (a launch with programmatic
+  // serialization starts before it ends); everything above reads context constants only
+  pdl_trigger();
+  pdl_wait();
   const long long total = (long long)a.batch * a.heads * a.n_new;
   const long long vec = (long long)blockIdx.x * kSmallWarps + warp;
   const bool live = vec < total;  // warp-uniform
@@ -272,8 +276,8 @@ int launch_append_small(const AppendArgs &k, const AppendArgs &v, const tq_ctx *
       return TQ_ERR_CUDA;
     done = true;
   }
-  fn<<<grid, kSmallWarps * 32, kSmallSmem, st>>>(s);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return launch_overlapped(true, fn, grid, dim3(kSmallWarps * 32), kSmallSmem, st, s) == cudaSuccess ? TQ_OK
+                                                                                                 : TQ_ERR_CUDA;
 }
 
 }  // namespace tq

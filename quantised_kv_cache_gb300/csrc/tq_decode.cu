@@ -74,6 +74,7 @@ __device__ void tile_prefix_block(const PrepArgs &a) {
 __global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
   __shared__ float s_q[4][kD];
   pdl_trigger();  // the decode kernel may start its prologue now
+  pdl_wait();     // the queries and lengths may come from the kernel before (e.g. the step's append)
   if (a.tile_prefix && blockIdx.x == 0) tile_prefix_block(a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
@@ -424,6 +425,7 @@ __global__ void __launch_bounds__(kCombineRows * 128) combine_tq_kernel(CombineA
     tma_load_1d(s_sk, a.sketch, kD * kD * sizeof(float), &s_bar);
   }
   pdl_wait();  // the partial records come from the decode kernel before
+  pdl_trigger();  // the next kernel of the stream (e.g. the next step's append) may be scheduled
   float L = 0.f, A = 0.f, Sg = 0.f;
   if (row < nrows) merge_row(a, row, i, L, A, Sg);
   s_sg[rr * kD + i] = Sg;
@@ -689,7 +691,8 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
              ctx->dparams->diag, ctx->dparams->sketch, a.qprep,
              a.seq_lens, a.cache->capacity, persist_ok ? a.tile_prefix : nullptr};
   const int rows = a.batch * a.heads_q;
-  qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
+  if (launch_overlapped(true, qprep_kernel, dim3((rows + 3) / 4), dim3(128), 0, st, p) != cudaSuccess)
+    return TQ_ERR_CUDA;
 
   // the TMA / tensor-core kernels cover one query head per KV head
   if (ctx->prof_decode_start) cudaEventRecord((cudaEvent_t)ctx->prof_decode_start, st);
@@ -769,7 +772,8 @@ int launch_decode_kivi(const DecodeArgs &a, void *stream) {
   PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, 0, 0, ctx->dparams->diag, ctx->dparams->sketch, a.qprep,
              a.seq_lens, a.cache->capacity, nullptr};
   const int rows = a.batch * a.heads_q;
-  qprep_kernel<<<(rows + 3) / 4, 128, 0, st>>>(p);
+  if (launch_overlapped(true, qprep_kernel, dim3((rows + 3) / 4), dim3(128), 0, st, p) != cudaSuccess)
+    return TQ_ERR_CUDA;
   const tq_cache *c = a.cache;
   KiviDecodeKernelArgs k{};
   k.k_codes = c->k_codes; k.v_codes = c->v_codes;
