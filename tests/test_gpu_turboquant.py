@@ -129,6 +129,24 @@ def test_a_token_lands_where_the_layout_says():
     assert not raw_other.any()
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_appends_that_split_a_token_pair_keep_both_halves(dtype):
+    # value codes of tokens 2j and 2j+1 share one field per coordinate: an append starting at
+    # an odd slot (here 601) must merge its half without touching the earlier token's half.
+    # Both calls are above the few-vector limit (the bulk kernels), as is the one-call reference.
+    B, H, N, cut = 2, 8, 1200, 601
+    _, k, v = _inputs(B, H, N, dtype, seed=21)
+    ctx = tq.Context(128, 4, "KQV", 17)
+    one = tq.Cache(ctx, B, H, N)
+    _append(ctx, one, k, v, 0)
+    two = tq.Cache(ctx, B, H, N)
+    _append(ctx, two, k[:, :, :cut].contiguous(), v[:, :, :cut].contiguous(), 0)
+    _append(ctx, two, k[:, :, cut:].contiguous(), v[:, :, cut:].contiguous(), cut)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    assert torch.equal(one.tensors["records"], two.tensors["records"])
+
+
 def test_append_writes_only_its_slots_and_reports_capacity():
     B, H = 2, 2
     _, k, v = _inputs(B, H, 10, torch.float32, seed=3)
