@@ -32,14 +32,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "compressed-KV decode attention GB/s and % of HBM peak; append-quantise tokens/s"
 CAP = 8192
-# kernels of one decode step: the append of the step's keys and values (one launch for
-# this few vectors), query prep, decode attention, combine
-LAUNCHES_PER_STEP = 4
+# kernels of one decode step (tq_decode_step): the persistent decode kernel, which also
+# appends the step's keys and values and prepares the queries, and the combine
+LAUNCHES_PER_STEP = 2
 # DRAM bytes (read + written) of one decode-kernel launch of this workload: an ncu capture of
-# the decode-small case (context 4096: 297.77 MB) scaled to context 8192 (the kernel reads every
-# token once, so traffic grows with the tokens); to be set to None whenever the kernel changes,
-# until it is captured again
-DECODE_TRAFFIC_BYTES = 2 * 297_774_592
+# the decode-small case (context 4096) scaled to context 8192 (the kernel reads every token
+# once, so traffic grows with the tokens); None whenever the kernel has changed since the
+# capture, until it is captured again
+DECODE_TRAFFIC_BYTES = None
 
 
 def peaks():
@@ -218,12 +218,13 @@ def run_small_case(args, dev):
     q, k, v = wl.generate(w, dev, seq=N)
     zeros = torch.zeros((B,), dtype=torch.int32, device=dev)
     tq.tq_append_quantize(ctx.handle, cache, k, v, zeros)
-    lens = torch.full((B,), N, dtype=torch.int32, device=dev)
+    lens = torch.full((B,), N - 1, dtype=torch.int32, device=dev)
+    kn, vn = k[:, :, -1:].contiguous(), v[:, :, -1:].contiguous()
     for _ in range(args.warmup + args.steps):
         if args.case == "append-small":
             tq.tq_append_quantize(ctx.handle, cache, k, v, zeros)
-        else:
-            tq.tq_decode_attention(ctx.handle, cache, q, lens, N)
+        else:  # decode steps re-appending the last token
+            tq.tq_decode_step(ctx.handle, cache, q, kn, vn, lens, N)
     torch.cuda.synchronize()
     assert tq.tq_get_device_error(ctx.handle) == 0
     print(json.dumps({"case": args.case, "ok": True}), flush=True)
@@ -375,6 +376,10 @@ def main():
 
     def step(i):
         q, kn, vn = pool[i % len(pool)]
+        tq.tq_decode_step(ctx.handle, cache, q, kn, vn, lens_append, CAP, ws, out)
+
+    def step_two_calls(i):  # the same step as an append call and a decode call (context only)
+        q, kn, vn = pool[i % len(pool)]
         tq.tq_append_quantize(ctx.handle, cache, kn, vn, lens_append)
         tq.tq_decode_attention(ctx.handle, cache, q, lens_decode, CAP, 0, ws, out)
 
@@ -382,7 +387,9 @@ def main():
                   + B * H * (2 * d * 2 + rec)  # new K/V token read, new records written
                   + B * w.heads_q * d * 2      # q (bf16)
                   + B * w.heads_q * d * 4)     # output (fp32)
-    decode_kernel_bytes = B * H * CAP * rec + B * w.heads_q * d * (2 + 4)
+    # the decode-step kernel: the cache, the queries, the new tokens read and their records
+    # written, the output (written by the combine, counted here as in the step)
+    decode_kernel_bytes = B * H * CAP * rec + B * w.heads_q * d * (2 + 4) + B * H * (2 * d * 2 + rec)
 
     clocks = Clocks(local)
     clocks.start()
@@ -417,6 +424,15 @@ def main():
     tq.tq_set_profile_events(ctx.handle)
     dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
     assert tq.tq_get_device_error(ctx.handle) == 0
+    for i in range(args.warmup):
+        step_two_calls(i)
+    t_start.record()
+    for i in range(K):
+        step_two_calls(i)
+    t_stop.record()
+    torch.cuda.synchronize()
+    two_calls_ms = t_start.elapsed_time(t_stop) / K
+    assert tq.tq_get_device_error(ctx.handle) == 0
 
     # ---------------- end to end through the ABI with host buffers
     pin = [(q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()) for q, kn, vn in pool]
@@ -450,8 +466,7 @@ def main():
         dq, dk, dv = dev_in[j]
         compute.wait_event(in_ready[j])
         compute.wait_event(out_free[j])
-        tq.tq_append_quantize(ctx.handle, cache, dk, dv, lens_append)
-        tq.tq_decode_attention(ctx.handle, cache, dq, lens_decode, CAP, 0, ws, dev_out[j])
+        tq.tq_decode_step(ctx.handle, cache, dq, dk, dv, lens_append, CAP, ws, dev_out[j])
         in_free[j].record(compute)
         out_ready[j].record(compute)
         stage_in(i + 1)
@@ -483,7 +498,9 @@ def main():
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": workload_config(),
             "pct_of_hbm_peak": 100.0 * (value / world) / hbm_peak,
-            "roofline": {"bound": "hbm", "kernel": "decode_persist_kernel (persistent decode attention)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "decode_persist_kernel<4,3,0,1,1> (persistent decode attention with the "
+                                   "step's append and query preparation fused in)",
                          "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": DECODE_TRAFFIC_BYTES, "ms_per_launch": dec_ms,
                          "bytes_per_launch": decode_kernel_bytes},
@@ -495,6 +512,8 @@ def main():
                                 "what": "bulk re-quantise of all 8192 tokens x 512 heads from bf16 K/V"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": 1e3 * e2e_s / K},
+            "two_calls": {"ms_per_step": two_calls_ms,
+                          "what": "the same step as tq_append_quantize + tq_decode_attention (4 launches)"},
             "gpu_launches": LAUNCHES_PER_STEP * K,
             "clocks": clk,
         }

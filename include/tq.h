@@ -239,11 +239,11 @@ tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const voi
                              const void *d_v, int dtype, int batch, int heads_kv, int n_new,
                              const int32_t *d_seq_lens, void *stream);
 
-/* Workspace bytes tq_decode_attention needs for these sizes: the prepared
- * queries, a per-batch tile prefix, and the partial softmax records (per
- * split for the split-K kernels, or four per (CTA + head) slot for the
- * persistent kernel, whichever is larger). splits = 0 asks for the library's
- * choice for max_len. */
+/* Workspace bytes tq_decode_attention and tq_decode_step need for these
+ * sizes: the prepared queries, a per-batch tile prefix, per-batch step
+ * lengths, and the partial softmax records (per split for the split-K
+ * kernels, or four per (CTA + head) slot for the persistent kernel, whichever
+ * is larger). splits = 0 asks for the library's choice for max_len. */
 tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len,
                             int splits, size_t *out);
 
@@ -267,6 +267,38 @@ tq_status tq_decode_attention(const tq_ctx *ctx, const tq_cache *cache, const vo
                               int batch, int heads_q, int heads_kv, const int32_t *d_seq_lens,
                               int max_len, int splits, void *d_workspace, size_t workspace_bytes,
                               float *d_out, void *stream);
+
+/* One decode step: append one new token per sequence, then attend over the
+ * sequence including it. The same results as tq_append_quantize(n_new = 1,
+ * d_seq_lens) followed by tq_decode_attention over d_seq_lens[b] + 1 tokens
+ * (bit for bit when batch * heads_kv <= 8192, where that append runs the
+ * same warp-per-vector arithmetic), in fewer launches: the new
+ * token is quantised where its keys and values are consumed ([HeadQ] 3,
+ * "cache write" then "decode"; [KIVI-geom] "The systems tax": decoding
+ * appends one token at a time and then reads the whole cache).
+ *   d_q : [batch][heads_q][d], dtype q_dtype (TQ_F32 or TQ_BF16)
+ *   d_k_new, d_v_new : [batch][heads_kv][d], dtype kv_dtype (TQ_F32 or TQ_BF16)
+ *   d_seq_lens : int32 [batch], lengths BEFORE the step; the new token of
+ *                sequence b goes to slot d_seq_lens[b]. Not modified: the
+ *                caller adds 1 afterwards, in stream order.
+ *   max_len : >= every d_seq_lens[b] + 1, <= capacity
+ *   d_workspace : >= tq_workspace_size(ctx, batch, heads_q, heads_kv,
+ *                 max_len, 0) bytes, 16-byte aligned
+ *   d_out : float32 [batch][heads_q][d]
+ * A sequence whose new token would not fit (d_seq_lens[b] < 0 or >=
+ * capacity) is not appended, the device error word is set to
+ * TQ_ERR_CAPACITY, and it is attended over min(d_seq_lens[b] + 1, capacity)
+ * tokens (none when negative). With one query head per KV head, the KV or
+ * KQV scheme and batch <= 256, the step is one persistent decode kernel
+ * (the CTA that reads a head's last tile quantises the new token before
+ * copying that tile, and rotates the queries itself) plus the combine;
+ * every other configuration runs a small length kernel, the append and the
+ * decode in stream order. The context's stream and events are used as by
+ * tq_append_quantize. */
+tq_status tq_decode_step(const tq_ctx *ctx, const tq_cache *cache, const void *d_q, int q_dtype,
+                         const void *d_k_new, const void *d_v_new, int kv_dtype, int batch,
+                         int heads_q, int heads_kv, const int32_t *d_seq_lens, int max_len,
+                         void *d_workspace, size_t workspace_bytes, float *d_out, void *stream);
 
 /* Reconstruct tokens [t0, t1) of every (batch, kv head) into fp32
  * ([KVQuant++] "Deployment and use": decompress). d_k_hat / d_v_hat:

@@ -49,26 +49,6 @@ struct SmallArgs {
   int *error;
 };
 
-template <int BITS>
-__device__ __forceinline__ void store_codes(uint8_t *codes, long long slot, int bb, const int (&idx)[4], int lane) {
-  const uint32_t fa = (uint32_t)idx[0] | ((uint32_t)idx[1] << BITS);
-  const uint32_t fb = (uint32_t)idx[2] | ((uint32_t)idx[3] << BITS);
-  const uint32_t word = pack_slot_word<BITS>(fa, fb, lane);  // every lane takes part
-  if (slot >= 0 && lane < 4 * BITS)
-    reinterpret_cast<uint32_t *>(rec_at(codes, slot, bb, BITS * kD / 8))[lane] = word;
-}
-
-// value codes (pair-interleaved layout): each lane merges its four codes into the
-// token pair's row atomically (the partner token's bits are left alone)
-template <int VB>
-__device__ __forceinline__ void store_codes_vt(uint8_t *vplane, long long slot, int bb, const int (&idx)[4],
-                                               int lane) {
-  if (slot < 0) return;
-  uint32_t *row = vt_row<VB>(vplane, slot, bb);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) store_code_vt<VB>(row, 4 * lane + k, (int)(slot & 1), (uint32_t)idx[k]);
-}
-
 template <bool BF16>
 __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const __grid_constant__ SmallArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -111,50 +91,9 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
 
     float x[4];
     load4(ro.x, (size_t)vec * kD + 4 * lane, BF16, x);
-    nu = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
-    float y[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float dg = ro.rotate ? __ldg(a.diag + 4 * lane + j) : 1.f;
-      y[j] = (nu > 0.f) ? (x[j] / nu) * dg : 0.f;
-    }
-    if (ro.rotate) wht128(y, lane);
-    int idx[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      int c = 0;
-#pragma unroll
-      for (int k = 0; k < kMaxLevels - 1; ++k) c += (y[j] >= ro.bounds[k]) ? 1 : 0;
-      idx[j] = c;
-    }
-    if (ro.vt) {
-      switch (ro.bits) {
-        case 1: store_codes_vt<1>(ro.codes, slot, a.bb, idx, lane); break;
-        case 2: store_codes_vt<2>(ro.codes, slot, a.bb, idx, lane); break;
-        case 3: store_codes_vt<3>(ro.codes, slot, a.bb, idx, lane); break;
-        default: store_codes_vt<4>(ro.codes, slot, a.bb, idx, lane); break;
-      }
-    } else {
-      switch (ro.bits) {
-        case 1: store_codes<1>(ro.codes, slot, a.bb, idx, lane); break;
-        case 2: store_codes<2>(ro.codes, slot, a.bb, idx, lane); break;
-        case 3: store_codes<3>(ro.codes, slot, a.bb, idx, lane); break;
-        default: store_codes<4>(ro.codes, slot, a.bb, idx, lane); break;
-      }
-    }
-    if (!qjl && slot >= 0 && lane == 0) *rec_at(ro.norms, slot, a.bb, 4) = nu;
-    if (qjl) {
-      // unit-domain residual r = y - c[code]
-      float r[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        r[j] = y[j] - ro.centroids[idx[j]];
-        rr += r[j] * r[j];
-      }
-      rr = warp_sum(rr);
-      reinterpret_cast<float4 *>(s_r + warp * kRS)[lane] =
-          (nu > 0.f) ? make_float4(r[0], r[1], r[2], r[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    float r[4];
+    encode_vector_warp(ro, x, slot, a.bb, a.diag, lane, nu, r, rr);
+    if (qjl) reinterpret_cast<float4 *>(s_r + warp * kRS)[lane] = make_float4(r[0], r[1], r[2], r[3]);
   } else if (qjl) {
     reinterpret_cast<float4 *>(s_r + warp * kRS)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   }

@@ -478,6 +478,16 @@ int launch_combine(const CombineArgs &a, cudaStream_t st) {
              : TQ_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- decode step
+
+__global__ void step_lengths_kernel(const int32_t *seq_lens, int batch, int capacity, int32_t *out) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch) {
+    const int len = __ldg(seq_lens + b);
+    out[b] = (len < 0) ? 0 : min(len, capacity - 1) + 1;
+  }
+}
+
 // ---------------------------------------------------------------- KIVI decode
 // Scores and values from 2-bit grouped codes ("Your KV cache is not a bit
 // problem but a geometry problem", "What quantisation error is made of":
@@ -759,6 +769,26 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
 
   CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                   ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv, 1};
+  cmb.error = &ctx->dparams->error;
+  return launch_combine(cmb, st);
+}
+
+int launch_step_lengths(const int32_t *seq_lens, int batch, int capacity, int32_t *lens_out, void *stream) {
+  step_lengths_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(seq_lens, batch, capacity, lens_out);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+int launch_decode_step_tq(const DecodeArgs &a, const StepArgs &s, void *stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const tq_ctx *ctx = a.ctx;
+  if (ctx->prof_decode_start) cudaEventRecord((cudaEvent_t)ctx->prof_decode_start, st);
+  int persist_ctas = 0;
+  const int r = launch_decode2_step(a, s, &persist_ctas, stream);
+  if (r != TQ_OK) return r;
+  if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
+  CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
+                  ctx->dparams->diag, ctx->dparams->sketch, a.out, a.tile_prefix, persist_ctas, a.heads_kv, 1};
+  cmb.group = 1;
   cmb.error = &ctx->dparams->error;
   return launch_combine(cmb, st);
 }

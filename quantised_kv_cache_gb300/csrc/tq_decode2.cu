@@ -109,6 +109,16 @@ struct Decode2Args {
   const float *k_centroids;
   const float *v_centroids;
   int *error;
+  // decode step (decode_persist_kernel<..., true>): the kernel appends one token per
+  // sequence at slot seq_lens[b], attends over seq_lens[b] + 1 tokens and prepares
+  // the queries itself
+  const void *q_raw;          // [batch][heads_q][128]
+  const void *k_new, *v_new;  // [batch][heads_kv][128]
+  int q_bf16, kv_bf16, q_rotate;
+  const float *diag;         // D as +/-1.0f
+  const float *sketch_tp;    // permuted S^T (sketch_signs_warp)
+  int32_t *tile_prefix_out;  // [batch + 1] tiles before each batch, for the combine
+  WarpRole role[2];          // keys, values
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -601,11 +611,126 @@ __global__ void __launch_bounds__(128, 2) decode2_g1_kernel(Decode2Args a) {
 // ============================================================================
 constexpr int kPersistWarps = 16;  // four groups of four (kPersistGroups)
 
-template <int KB, int VB, bool KQJL, bool VQJL>
+// Decode step: the lengths before the step (s_raw) and after the append (seq_lens + 1,
+// clamped to [0, capacity]), the
+// exclusive prefix over batches of their 64-token tile counts (batch <= 256: eight warp
+// scans), and, by CTA 0, that prefix for the combine and the append's capacity errors.
+__device__ __forceinline__ void step_lengths(const Decode2Args &a, int *s_pre, int *s_len, int *s_raw, int *s_scan,
+                                             int tid) {
+  const int B = a.batch, lane = tid & 31, warp = tid >> 5;
+  int n = 0;
+  if (tid < B) {
+    const int len = __ldg(a.seq_lens + tid);
+    const int dl = (len < 0) ? 0 : min(len, a.capacity - 1) + 1;
+    s_len[tid] = dl;
+    s_raw[tid] = len;
+    n = (dl + kTT - 1) / kTT;
+    if (blockIdx.x == 0 && (len < 0 || len >= a.capacity)) set_error(a.error, TQ_ERR_CAPACITY);
+  }
+  int v = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31 && warp < kMaxPersistBatch / 32) s_scan[warp] = v;
+  __syncthreads();
+  if (tid < B) {
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_scan[w];
+    s_pre[tid + 1] = base + v;
+  }
+  if (tid == 0) s_pre[0] = 0;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= B; i += blockDim.x) a.tile_prefix_out[i] = s_pre[i];
+}
+
+// Raw query of row `row` (lane L: coordinates 4L..4L+3), copied asynchronously into 512
+// bytes of shared memory by one warp and read back after cp_async_wait_all(), and its
+// preparation as the query prep kernel does it: q_rot = H D q / sqrt(d) (orthonormal H),
+// or q / sqrt(d) for unrotated keys.
+__device__ __forceinline__ void stage_query(const Decode2Args &a, int row, int lane, float *raw) {
+  if (a.q_bf16)
+    cp_async_8(reinterpret_cast<uint16_t *>(raw) + 4 * lane, static_cast<const uint16_t *>(a.q_raw) + (size_t)row * kD + 4 * lane);
+  else
+    cp_async_16(raw + 4 * lane, static_cast<const float *>(a.q_raw) + (size_t)row * kD + 4 * lane);
+  cp_async_commit();
+}
+__device__ __forceinline__ void staged_query(const Decode2Args &a, const float *raw, int lane, float (&v)[4]) {
+  if (a.q_bf16) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(raw) + 4 * lane);
+    v[0] = bf16_bits_to_float(w.x & 0xffffu);
+    v[1] = bf16_bits_to_float(w.x >> 16);
+    v[2] = bf16_bits_to_float(w.y & 0xffffu);
+    v[3] = bf16_bits_to_float(w.y >> 16);
+  } else {
+    const float4 f = reinterpret_cast<const float4 *>(raw)[lane];
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
+  }
+}
+__device__ __forceinline__ void prep_query(const Decode2Args &a, int lane, float (&v)[4]) {
+  if (a.q_rotate) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] *= __ldg(a.diag + 4 * lane + j);
+    wht128(v, lane);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] *= kInvSqrtD;
+}
+
+// Append the new token (one role) of unit u = b * H + h at slot len (the sequence's
+// length before the step, 0 <= len < capacity) by one warp. s_sk: the permuted S^T in
+// shared memory.
+__device__ __forceinline__ void step_append(const Decode2Args &a, int u, int role, int len, int lane,
+                                            const float *s_sk) {
+  const long long slot = (long long)u * a.cap16 + len;
+  float x[4];
+  load4(role ? a.v_new : a.k_new, (size_t)u * kD + 4 * lane, a.kv_bf16 != 0, x);
+  const WarpRole &ro = a.role[role];
+  float nu, rr, r[4];
+  encode_vector_warp(ro, x, slot, a.bb, a.diag, lane, nu, r, rr);
+  if (!ro.qjl) return;
+  uint32_t w[4];
+  sketch_signs_warp(s_sk, r, lane, w);
+  float rho = nu * sqrtf(rr);
+  if (nu == 0.f) {  // a zero vector: every sign set, rho = 0
+    w[0] = w[1] = w[2] = w[3] = 0xffffffffu;
+    rho = 0.f;
+  }
+  const uint32_t mine = lane == 0 ? w[0] : (lane == 1 ? w[1] : (lane == 2 ? w[2] : w[3]));
+  if (lane < 4) reinterpret_cast<uint32_t *>(rec_at(ro.signs, slot, a.bb, kD / 8))[lane] = mine;
+  if (lane == 0) {
+    *rec_at(ro.norms, slot, a.bb, 4) = nu;
+    *rec_at(ro.rnorms, slot, a.bb, 4) = rho;
+  }
+}
+
+// shared-memory bytes of the persistent kernel: the layout of Geo, the batch prefix and
+// lengths, the key centroids, one mbarrier (8-byte aligned) for the decode step's copy of
+// the permuted S^T, and the decode step's lengths before the step
+template <typename Gm>
+constexpr int persist_sbar_offset() {
+  return (Gm::sm_misc + 4 * (2 * kMaxPersistBatch + 1) + 4 * kMaxLevels + 7) & ~7;
+}
+template <typename Gm>
+constexpr int persist_smem_bytes() {
+  return persist_sbar_offset<Gm>() + 8 + 4 * kMaxPersistBatch;  // + the decode step's raw lengths
+}
+
+template <int KB, int VB, bool KQJL, bool VQJL, bool FUSED>
 __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(Decode2Args a) {
+  static_assert(!(FUSED && KQJL), "the decode step prepares queries without a key sketch");
   constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
   static_assert(S >= 8 && S % kPersistGroups == 0, "ring stages");
   using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
+  // the decode step's sketched values read S^T from the key-table area and, past it, the
+  // first ring stages (contiguous when keys have no sketch table), until the ring starts
+  constexpr bool kStepSketch = FUSED && VQJL;
+  static_assert(!kStepSketch || Gm::sm_ktab + kD * kD * 4 <= Gm::sm_stage + S * Gm::stage, "S^T copy area");
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *s_stage = smem + Gm::sm_stage;
   uint64_t *s_full = reinterpret_cast<uint64_t *>(smem + Gm::sm_bar);  // [S][4 quarters]
@@ -613,17 +738,34 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
   int *s_pre = reinterpret_cast<int *>(smem + Gm::sm_misc);  // [batch + 1] tile prefix
   int *s_len = s_pre + kMaxPersistBatch + 1;                  // [batch] clamped lengths
   float *s_kc = reinterpret_cast<float *>(s_len + kMaxPersistBatch);  // [16] key centroids
+  uint64_t *s_sbar = reinterpret_cast<uint64_t *>(smem + persist_sbar_offset<Gm>());
+  int *s_raw = reinterpret_cast<int *>(smem + persist_sbar_offset<Gm>() + 8);  // [batch]
+  const float *s_sk = reinterpret_cast<const float *>(smem + Gm::sm_ktab);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, grp = warp >> 2, qtr = warp & 3;
   const int B = a.batch, H = a.heads_kv;
+  if constexpr (kStepSketch) {
+    // S^T is a context constant: its copy overlaps the wait for the kernel before
+    if (tid == 0) {
+      mbar_init(s_sbar, 1);
+      mbar_fence_init();
+      mbar_arrive_expect_tx(s_sbar, kD * kD * sizeof(float));
+      tma_load_1d(smem + Gm::sm_ktab, a.sketch_tp, kD * kD * sizeof(float), s_sbar);
+    }
+  }
   if (tid < kMaxLevels) s_kc[tid] = __ldg(a.k_centroids + tid);
   build_value_table<VB, kPersistWarps * 32>(smem, Gm::vlut, a.v_centroids, tid);
   // everything above reads context constants only; the query prep (tile prefix,
   // prepared queries) and the cache come from earlier kernels of the stream
   pdl_trigger();
   pdl_wait();
-  for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
-  for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
+  if constexpr (FUSED) {
+    // s_q is free until the first head's query is prepared
+    step_lengths(a, s_pre, s_len, s_raw, reinterpret_cast<int *>(s_q), tid);
+  } else {
+    for (int i = tid; i <= B; i += blockDim.x) s_pre[i] = __ldg(a.tile_prefix + i);
+    for (int i = tid; i < B; i += blockDim.x) s_len[i] = min(max(__ldg(a.seq_lens + i), 0), a.capacity);
+  }
   if (tid < S * 4) mbar_init(&s_full[tid], 1);
   mbar_fence_init();
   __syncthreads();
@@ -633,7 +775,10 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
   const long long T = (long long)H * s_pre[B];
   const long long C = gridDim.x, c = blockIdx.x, T4 = (T + 3) / 4;
   const int g0 = (int)min(T, 4 * (T4 * c / C)), g1 = (int)min(T, 4 * (T4 * (c + 1) / C));
-  if (g0 >= g1) return;  // whole CTA: nothing to do (no record is read for it)
+  if (g0 >= g1) {  // whole CTA: nothing to do (no record is read for it)
+    if constexpr (kStepSketch) mbar_wait_bounded(s_sbar, 0, a.error);  // no copy outlives the CTA
+    return;
+  }
   const int nloc = g1 - g0;
 
   // batch of global tile g: the largest b with H * pre[b] <= g
@@ -689,19 +834,52 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     cur_t += kPersistGroups;
     if (cur_i < nloc) seek();
   };
-  for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
-
-  const LaneConsts<KB> lc(lane);
-  WarpState ws;
-  bool bad = false;
-  float *park = reinterpret_cast<float *>(smem + Gm::sm_ktab);
   // query row (= unit: one query head per KV head) of the segment starting at tile g
   auto unit_of = [&](int g) -> int {
     const int bb = batch_of(g);
     const int nb = s_pre[bb + 1] - s_pre[bb];
     return bb * H + (g - H * s_pre[bb]) / nb;
   };
-  if (tid < 2 * kD) s_q[tid] = __ldg(a.qprep + (size_t)unit_of(g0) * 2 * kD + tid);
+  // decode step: the CTA holding a head's last tile appends that head's new token (keys
+  // and values, one warp each) before any tile is copied (appends issued while the ring's
+  // copies stream would queue their loads and stores behind them); meanwhile the first
+  // head's query is copied into the upper half of s_q
+  if constexpr (FUSED) {
+    if (warp == kPersistWarps - 1) stage_query(a, unit_of(g0), lane, s_q + kD);
+    if constexpr (kStepSketch) mbar_wait_bounded(s_sbar, 0, a.error);
+    const int ua = unit_of(g0), ub = unit_of(g1 - 1);
+    for (int j = warp; j < 2 * (ub - ua + 1); j += kPersistWarps) {
+      const int u = ua + (j >> 1);
+      const int bq = u / H, hq = u - bq * H;
+      const int nb = s_pre[bq + 1] - s_pre[bq];
+      const int gl = H * s_pre[bq] + (hq + 1) * nb - 1;  // the head's last tile
+      const int len = s_raw[bq];
+      if (nb == 0 || gl < g0 || gl >= g1 || len < 0 || len >= a.capacity) continue;
+      step_append(a, u, j & 1, len, lane, s_sk);
+      fence_proxy_async_global();  // the records written above, before their bulk copies
+    }
+    if constexpr (kStepSketch) fence_proxy_async_shared();  // S^T read above, before the ring overwrites it
+    __syncthreads();
+  }
+  for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
+
+  const LaneConsts<KB> lc(lane);
+  WarpState ws;
+  bool bad = false;
+  float *park = reinterpret_cast<float *>(smem + Gm::sm_ktab);
+  if constexpr (FUSED) {
+    if (warp == kPersistWarps - 1) {
+      cp_async_wait_all();
+      __syncwarp();
+      float v[4];
+      staged_query(a, s_q + kD, lane, v);
+      prep_query(a, lane, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_q[4 * lane + j] = v[j];
+    }
+  } else {
+    if (tid < 2 * kD) s_q[tid] = __ldg(a.qprep + (size_t)unit_of(g0) * 2 * kD + tid);
+  }
   __syncthreads();
   int g = g0;
   while (g < g1) {  // one segment per (batch, kv head) the slice touches
@@ -718,9 +896,15 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     // readers of the table area passed the barrier that closed its flush)
     build_key_tables<KB, KQJL, kPersistWarps * 32>(smem, Gm::sm_ktab, Gm::sm_stab, s_q, s_kc, tid);
     __syncthreads();
-    // the next segment's query, fetched while this one streams
+    // the next segment's query, fetched while this one streams (decode step: its raw
+    // values copied into the upper half of s_q, which keys without a sketch leave unused,
+    // by the last warp, which takes no part in the merge below)
     float q_next = 0.f;
-    if (se < g1 && tid < 2 * kD) q_next = __ldg(a.qprep + (size_t)unit_of(se) * 2 * kD + tid);
+    if constexpr (FUSED) {
+      if (se < g1 && warp == kPersistWarps - 1) stage_query(a, unit_of(se), lane, s_q + kD);
+    } else {
+      if (se < g1 && tid < 2 * kD) q_next = __ldg(a.qprep + (size_t)unit_of(se) * 2 * kD + tid);
+    }
 
     ws.reset();
     // this group's tiles: local index i = t - g0 with i % 4 == grp
@@ -744,7 +928,19 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     __syncthreads();
     park_warp<VQJL>(park + warp * kPartialFloats, lane, ws);
     __syncthreads();
-    if (tid < 2 * kD) s_q[tid] = q_next;
+    if constexpr (FUSED) {
+      if (warp == kPersistWarps - 1 && se < g1) {
+        cp_async_wait_all();
+        __syncwarp();
+        float qn4[4];
+        staged_query(a, s_q + kD, lane, qn4);
+        prep_query(a, lane, qn4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s_q[4 * lane + j] = qn4[j];
+      }
+    } else {
+      if (tid < 2 * kD) s_q[tid] = q_next;
+    }
     // one record per (CTA, head): all 16 warps merged
     if (tid < kD) merge_parked<kPersistWarps, VQJL>(park, tid, a.partials + (size_t)(c + u) * kPartialFloats);
     __syncthreads();  // the table area is rebuilt next
@@ -1159,13 +1355,13 @@ int launch_split(const Decode2Args &k, dim3 grid, cudaStream_t st) {
 }
 
 // persistent launch: one CTA per SM (the workspace's record count assumes no more)
-template <int KB, int VB, bool KQJL, bool VQJL>
+template <int KB, int VB, bool KQJL, bool VQJL, bool FUSED = false>
 int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st) {
   constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
   using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
   if (k.bb != Gm::block) return TQ_ERR_UNSUPPORTED;
-  const size_t smem = Gm::sm_misc + sizeof(int) * (2 * kMaxPersistBatch + 1) + sizeof(float) * kMaxLevels;
-  auto fn = decode_persist_kernel<KB, VB, KQJL, VQJL>;
+  const size_t smem = persist_smem_bytes<Gm>();
+  auto fn = decode_persist_kernel<KB, VB, KQJL, VQJL, FUSED>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -1210,7 +1406,86 @@ int launch_variant(const Decode2Args &k, bool persist, int num_sms, int *ctas, c
   return launch_split<KB, VB, KQJL, VQJL>(k, dim3(k.splits, k.heads_kv, k.batch), st);
 }
 
+// Common arguments of the persistent and split-K launches.
+Decode2Args decode2_args(const DecodeArgs &a) {
+  const tq_ctx *ctx = a.ctx;
+  const tq_cache *c = a.cache;
+  Decode2Args k{};
+  k.records = c->records;
+  k.bb = ctx->lay.bb;
+  k.cap16 = cap16_of(c->capacity);
+  k.capacity = c->capacity;
+  k.batch = a.batch;
+  k.heads_kv = a.heads_kv;
+  k.heads_q = a.heads_q;
+  k.chunk = a.chunk;
+  k.splits = a.splits;
+  k.seq_lens = a.seq_lens;
+  k.tile_prefix = a.tile_prefix;
+  k.qprep = a.qprep;
+  k.partials = a.partials;
+  k.k_centroids = ctx->dparams->k_centroids;
+  k.v_centroids = ctx->dparams->v_centroids;
+  k.error = &ctx->dparams->error;
+  return k;
+}
+
 }  // namespace
+
+// The decode step on the persistent kernel (one query head per KV head, keys without a
+// sketch, batch <= 256); TQ_ERR_UNSUPPORTED otherwise. The kernel writes the tile prefix
+// to a.tile_prefix for the combine.
+int launch_decode2_step(const DecodeArgs &a, const StepArgs &s, int *persist_ctas, void *stream) {
+  const tq_ctx *ctx = a.ctx;
+  *persist_ctas = 0;
+  if (a.heads_q != a.heads_kv || a.batch > kMaxPersistBatch || ctx->num_sms <= 0 || !a.tile_prefix)
+    return TQ_ERR_UNSUPPORTED;
+  if (ctx->scheme != TQ_SCHEME_KV && ctx->scheme != TQ_SCHEME_KQV) return TQ_ERR_UNSUPPORTED;
+  Decode2Args k = decode2_args(a);
+  k.tile_prefix = nullptr;
+  k.tile_prefix_out = a.tile_prefix;
+  k.q_raw = a.q;
+  k.q_bf16 = a.q_dtype == TQ_BF16;
+  k.q_rotate = ctx->k.rotate ? 1 : 0;
+  k.k_new = s.k_new;
+  k.v_new = s.v_new;
+  k.kv_bf16 = s.kv_dtype == TQ_BF16;
+  k.diag = ctx->dparams->diag;
+  k.sketch_tp = ctx->dparams->sketch_tp;
+  for (int r = 0; r < 2; ++r) {
+    WarpRole &o = k.role[r];
+    const Role &role = r ? ctx->v : ctx->k;
+    const int p0 = r ? TQ_PLANE_V_CODES : TQ_PLANE_K_CODES;
+    auto at = [&](int p) -> uint8_t * { return ctx->lay.tok[p] ? a.cache->records + ctx->lay.off[p] : nullptr; };
+    o.codes = at(p0);
+    o.norms = reinterpret_cast<float *>(at(p0 + 1));
+    o.signs = at(p0 + 2);
+    o.rnorms = reinterpret_cast<float *>(at(p0 + 3));
+    o.bits = role.bits;
+    o.rotate = role.rotate ? 1 : 0;
+    o.qjl = role.qjl ? 1 : 0;
+    o.vt = r;  // value codes are stored pair-interleaved
+    const float *bounds = r ? ctx->v_bounds : ctx->k_bounds;
+    const float *cents = r ? ctx->v_centroids : ctx->k_centroids;
+    const int L = 1 << role.bits;
+    for (int i = 0; i < kMaxLevels; ++i) {
+      o.bounds[i] = (i < L - 1) ? bounds[i] : __builtin_huge_valf();
+      o.centroids[i] = (i < L) ? cents[i] : 0.f;
+    }
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  const int kb = ctx->k.bits, ns = ctx->num_sms;
+  if (ctx->scheme == TQ_SCHEME_KV) {
+    if (kb == 2) return launch_persist<2, 2, false, false, true>(k, ns, persist_ctas, st);
+    if (kb == 3) return launch_persist<3, 3, false, false, true>(k, ns, persist_ctas, st);
+    if (kb == 4) return launch_persist<4, 4, false, false, true>(k, ns, persist_ctas, st);
+  } else {
+    if (kb == 2) return launch_persist<2, 1, false, true, true>(k, ns, persist_ctas, st);
+    if (kb == 3) return launch_persist<3, 2, false, true, true>(k, ns, persist_ctas, st);
+    if (kb == 4) return launch_persist<4, 3, false, true, true>(k, ns, persist_ctas, st);
+  }
+  return TQ_ERR_UNSUPPORTED;
+}
 
 // Returns TQ_ERR_UNSUPPORTED when this path does not cover the request (the
 // caller then uses the general kernel). *persist_ctas receives the persistent

@@ -241,6 +241,126 @@ __device__ __forceinline__ void vt_store_chunk(uint32_t *row, int chunk, const u
   }
 }
 
+// ---------------------------------------------------------------------------
+// One vector per warp (lane L holding coordinates 4L..4L+3), as a decode step
+// appends its new token: "Statistical Inference and Quality Measures of KV
+// Cache Quantisations Inspired by TurboQuant", technical summary,
+// "Quantisation schemes" (norm, seeded +/-1 diagonal and Walsh-Hadamard
+// rotation, scalar Lloyd-Max codes; the (n-1)-bit role keeps a 1-bit QJL
+// sketch of its residual) and "KVQuant++", "Fast codebook lookup" (a code is
+// the count of boundaries at or below the coordinate).
+
+// What a warp needs to write one role's record planes (block-0 bases of the blocked records).
+struct WarpRole {
+  uint8_t *codes;
+  float *norms;
+  uint8_t *signs;
+  float *rnorms;
+  int bits, rotate, qjl, vt;
+  float bounds[kMaxLevels];  // 2^bits - 1 used, +inf after
+  float centroids[kMaxLevels];
+};
+
+template <int BITS>
+__device__ __forceinline__ void warp_store_codes(uint8_t *codes, long long slot, int bb, const int (&idx)[4],
+                                                 int lane) {
+  const uint32_t fa = (uint32_t)idx[0] | ((uint32_t)idx[1] << BITS);
+  const uint32_t fb = (uint32_t)idx[2] | ((uint32_t)idx[3] << BITS);
+  const uint32_t word = pack_slot_word<BITS>(fa, fb, lane);  // every lane takes part
+  if (slot >= 0 && lane < 4 * BITS)
+    reinterpret_cast<uint32_t *>(rec_at(codes, slot, bb, BITS * kD / 8))[lane] = word;
+}
+
+// value codes (pair-interleaved layout): each lane merges its four codes into the
+// token pair's row atomically (the partner token's bits are left alone)
+template <int VB>
+__device__ __forceinline__ void warp_store_codes_vt(uint8_t *vplane, long long slot, int bb, const int (&idx)[4],
+                                                    int lane) {
+  if (slot < 0) return;
+  uint32_t *row = vt_row<VB>(vplane, slot, bb);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) store_code_vt<VB>(row, 4 * lane + k, (int)(slot & 1), (uint32_t)idx[k]);
+}
+
+// Norm nu, unit rotated coordinates, codes; writes the code plane (and, for roles
+// without a sketch, the norm) of token `slot` (nothing when slot < 0). For sketched
+// roles returns the unit-domain residual r = y - c[code] (zero for a zero vector) and
+// sum r^2 over the warp.
+template <typename R>
+__device__ __forceinline__ void encode_vector_warp(const R &ro, const float (&x)[4], long long slot, int bb,
+                                                   const float *diag, int lane, float &nu, float (&r)[4],
+                                                   float &rr) {
+  nu = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
+  float y[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float dg = ro.rotate ? __ldg(diag + 4 * lane + j) : 1.f;
+    y[j] = (nu > 0.f) ? (x[j] / nu) * dg : 0.f;
+  }
+  if (ro.rotate) wht128(y, lane);
+  int idx[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxLevels - 1; ++k) c += (y[j] >= ro.bounds[k]) ? 1 : 0;
+    idx[j] = c;
+  }
+  if (ro.vt) {
+    switch (ro.bits) {
+      case 1: warp_store_codes_vt<1>(ro.codes, slot, bb, idx, lane); break;
+      case 2: warp_store_codes_vt<2>(ro.codes, slot, bb, idx, lane); break;
+      case 3: warp_store_codes_vt<3>(ro.codes, slot, bb, idx, lane); break;
+      default: warp_store_codes_vt<4>(ro.codes, slot, bb, idx, lane); break;
+    }
+  } else {
+    switch (ro.bits) {
+      case 1: warp_store_codes<1>(ro.codes, slot, bb, idx, lane); break;
+      case 2: warp_store_codes<2>(ro.codes, slot, bb, idx, lane); break;
+      case 3: warp_store_codes<3>(ro.codes, slot, bb, idx, lane); break;
+      default: warp_store_codes<4>(ro.codes, slot, bb, idx, lane); break;
+    }
+  }
+  if (!ro.qjl && slot >= 0 && lane == 0) *rec_at(ro.norms, slot, bb, 4) = nu;
+  rr = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r[j] = 0.f;
+  if (ro.qjl) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float rj = y[j] - ro.centroids[idx[j]];
+      s += rj * rj;
+      r[j] = (nu > 0.f) ? rj : 0.f;
+    }
+    rr = warp_sum(s);
+  }
+}
+
+// The four QJL sign words of one vector (all lanes): word m, bit L = [ (S r)_row >= 0 ] for
+// the sketch row whose sign sits there, read from the permuted transpose of S
+// (entry (i, 4L + m) = that row's column i; a copy in shared memory); lane L forms its
+// four rows, summing over i in ascending order.
+__device__ __forceinline__ void sketch_signs_warp(const float *sketch_tp, const float (&r)[4], int lane,
+                                                  uint32_t (&w)[4]) {
+  float z[4] = {0.f, 0.f, 0.f, 0.f};
+  const float4 *col = reinterpret_cast<const float4 *>(sketch_tp) + lane;
+#pragma unroll 4
+  for (int i4 = 0; i4 < kD / 4; ++i4) {
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      const float ri = __shfl_sync(kFull, r[ii], i4);
+      const float4 sv = col[(4 * i4 + ii) * (kD / 4)];
+      z[0] = fmaf(sv.x, ri, z[0]);
+      z[1] = fmaf(sv.y, ri, z[1]);
+      z[2] = fmaf(sv.z, ri, z[2]);
+      z[3] = fmaf(sv.w, ri, z[3]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) w[m] = __ballot_sync(kFull, z[m] >= 0.f);
+}
+
 // KIVI records keep the plain order: channel i's 2-bit code at bits [2i, 2i+2).
 __device__ __forceinline__ uint32_t kivi_lane_field(const uint32_t *rec, int lane) {
   return __ldg(rec + (lane >> 2)) >> (8 * (lane & 3));  // 8 bits: channels 4L..4L+3

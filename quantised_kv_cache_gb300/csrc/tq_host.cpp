@@ -518,15 +518,27 @@ tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads
     return TQ_ERR_ARG;
   int s, chunk;
   tq::choose_splits(batch, heads_kv, max_len, splits, &s, &chunk);
-  // prepared queries | decode-tile prefix over batches | partial records (split-K
-  // per (row, split), or the persistent kernel's kPersistGroups x G per (CTA + KV head) slot)
+  // prepared queries | decode-tile prefix over batches | decode-step lengths | partial
+  // records (split-K per (row, split), or the persistent kernel's kPersistGroups x G per
+  // (CTA + KV head) slot)
   size_t qprep = (size_t)batch * heads_q * 2 * ctx->d * sizeof(float);
   size_t prefix = ((size_t)(batch + 1) * sizeof(int32_t) + 15) / 16 * 16;
+  size_t lens = ((size_t)batch * sizeof(int32_t) + 15) / 16 * 16;
   size_t split_parts = (size_t)batch * heads_q * s * tq::kPartialFloats * sizeof(float);
   size_t persist_parts = (size_t)tq::kPersistGroups * (size_t)(heads_q / heads_kv) *
                          ((size_t)ctx->num_sms + (size_t)batch * heads_kv) * tq::kPartialFloats * sizeof(float);
-  *out = qprep + prefix + std::max(split_parts, persist_parts);
+  *out = qprep + prefix + lens + std::max(split_parts, persist_parts);
   return TQ_OK;
+}
+
+// Carve a workspace of tq_workspace_size bytes (layout above).
+static void workspace_layout(const tq_ctx *ctx, void *ws, int batch, int heads_q, tq::DecodeArgs &a,
+                             int32_t **step_lens) {
+  a.qprep = (float *)ws;
+  a.tile_prefix = (int32_t *)(a.qprep + (size_t)batch * heads_q * 2 * ctx->d);
+  int32_t *lens = (int32_t *)((char *)a.tile_prefix + ((size_t)(batch + 1) * sizeof(int32_t) + 15) / 16 * 16);
+  if (step_lens) *step_lens = lens;
+  a.partials = (float *)((char *)lens + ((size_t)batch * sizeof(int32_t) + 15) / 16 * 16);
 }
 
 tq_status tq_decode_attention(const tq_ctx *ctx, const tq_cache *cache, const void *d_q, int q_dtype, int batch,
@@ -555,12 +567,60 @@ tq_status tq_decode_attention(const tq_ctx *ctx, const tq_cache *cache, const vo
   a.max_len = max_len;
   tq::choose_splits(batch, heads_kv, max_len, splits, &a.splits, &a.chunk);
   a.seq_lens = d_seq_lens;
-  a.qprep = (float *)d_workspace;
-  a.tile_prefix = (int32_t *)(a.qprep + (size_t)batch * heads_q * 2 * ctx->d);
-  a.partials = (float *)((char *)a.tile_prefix + ((size_t)(batch + 1) * sizeof(int32_t) + 15) / 16 * 16);
+  workspace_layout(ctx, d_workspace, batch, heads_q, a, nullptr);
   a.out = d_out;
   if (ctx->scheme == TQ_SCHEME_KIVI) return (tq_status)tq::launch_decode_kivi(a, stream);
   return (tq_status)tq::launch_decode_tq(a, stream);
+}
+
+tq_status tq_decode_step(const tq_ctx *ctx, const tq_cache *cache, const void *d_q, int q_dtype,
+                         const void *d_k_new, const void *d_v_new, int kv_dtype, int batch, int heads_q,
+                         int heads_kv, const int32_t *d_seq_lens, int max_len, void *d_workspace, size_t ws_bytes,
+                         float *d_out, void *stream) {
+  if (!ctx || !d_q || !d_k_new || !d_v_new || !d_seq_lens || !d_workspace || !d_out) return TQ_ERR_ARG;
+  if (q_dtype != TQ_F32 && q_dtype != TQ_BF16) return TQ_ERR_ARG;
+  if (kv_dtype != TQ_F32 && kv_dtype != TQ_BF16) return TQ_ERR_ARG;
+  if (batch <= 0 || heads_q <= 0 || heads_kv <= 0 || max_len <= 0) return TQ_ERR_ARG;
+  if (heads_q % heads_kv) return TQ_ERR_ARG;
+  if (heads_q / heads_kv > tq::kMaxGroup) return TQ_ERR_UNSUPPORTED;
+  tq_status s = check_cache(ctx, cache, batch, heads_kv);
+  if (s != TQ_OK) return s;
+  if (max_len > cache->capacity) return TQ_ERR_ARG;
+  if (!aligned16(d_q) || !aligned16(d_k_new) || !aligned16(d_v_new) || !aligned16(d_workspace) ||
+      !aligned16(d_out))
+    return TQ_ERR_ALIGN;
+  size_t need = 0;
+  tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, 0, &need);
+  if (ws_bytes < need) return TQ_ERR_WORKSPACE;
+  if (ctx->scheme != TQ_SCHEME_KIVI) {
+    // one decode kernel that also appends the new tokens and prepares the queries
+    tq::DecodeArgs a{};
+    a.ctx = ctx;
+    a.cache = cache;
+    a.q = d_q;
+    a.q_dtype = q_dtype;
+    a.batch = batch;
+    a.heads_q = heads_q;
+    a.heads_kv = heads_kv;
+    a.max_len = max_len;
+    tq::choose_splits(batch, heads_kv, max_len, 0, &a.splits, &a.chunk);
+    a.seq_lens = d_seq_lens;
+    workspace_layout(ctx, d_workspace, batch, heads_q, a, nullptr);
+    a.out = d_out;
+    const tq::StepArgs st{d_k_new, d_v_new, kv_dtype};
+    const int r = tq::launch_decode_step_tq(a, st, stream);
+    if (r != TQ_ERR_UNSUPPORTED) return (tq_status)r;
+  }
+  // otherwise: the append, then the decode over the lengths plus one
+  tq::DecodeArgs lay{};
+  int32_t *lens = nullptr;
+  workspace_layout(ctx, d_workspace, batch, heads_q, lay, &lens);
+  s = (tq_status)tq::launch_step_lengths(d_seq_lens, batch, cache->capacity, lens, stream);
+  if (s != TQ_OK) return s;
+  s = tq_append_quantize(ctx, cache, d_k_new, d_v_new, kv_dtype, batch, heads_kv, 1, d_seq_lens, stream);
+  if (s != TQ_OK) return s;
+  return tq_decode_attention(ctx, cache, d_q, q_dtype, batch, heads_q, heads_kv, lens, max_len, 0, d_workspace,
+                             ws_bytes, d_out, stream);
 }
 
 tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int heads_kv, int t0, int t1,

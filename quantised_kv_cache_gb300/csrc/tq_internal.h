@@ -180,6 +180,20 @@ int launch_decode_tq(const DecodeArgs &a, void *stream);
 int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream);
 int launch_decode_kivi(const DecodeArgs &a, void *stream);
 
+// A decode step: one new token per sequence appended at slot seq_lens[b], then decode
+// attention over seq_lens[b] + 1 tokens (DecodeArgs::seq_lens are the lengths before it).
+struct StepArgs {
+  const void *k_new, *v_new;  // [batch][heads_kv][d]
+  int kv_dtype;               // TQ_F32 / TQ_BF16
+};
+// the step on the persistent decode kernel with the append and the query preparation
+// fused in (TQ_ERR_UNSUPPORTED, with nothing launched, outside what it covers)
+int launch_decode2_step(const DecodeArgs &a, const StepArgs &s, int *persist_ctas, void *stream);
+// that kernel followed by the combine
+int launch_decode_step_tq(const DecodeArgs &a, const StepArgs &s, void *stream);
+// lens_out[b] = seq_lens[b] + 1 clamped to [0, capacity]
+int launch_step_lengths(const int32_t *seq_lens, int batch, int capacity, int32_t *lens_out, void *stream);
+
 struct DequantArgs {
   const uint8_t *codes;  // plane bases in the blocked records (see AppendArgs)
   const float *norms;

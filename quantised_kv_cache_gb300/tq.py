@@ -71,6 +71,8 @@ _SIGNATURES = {
     "tq_workspace_size": (_i, [_vp, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tq_decode_attention": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _i, _i, _i, _i, _vp, _i, _i, _vp, _sz,
                                  _vp, _vp]),
+    "tq_decode_step": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _sz,
+                            _vp, _vp]),
     "tq_dequantize": (_i, [_vp, ctypes.POINTER(tq_cache), _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "tq_export_params": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tq_codebook_f64": (_i, [_i, _i, _vp, _vp]),
@@ -194,6 +196,27 @@ def tq_decode_attention(ctx, cache: "Cache", q: torch.Tensor, seq_lens: torch.Te
     check(lib().tq_decode_attention(ctx, ctypes.byref(cache.struct), _ptr(q), _dtype_code(q), B, Hq, Hkv,
                                     _ptr(seq_lens), max_len, splits, _ptr(workspace), workspace.numel(),
                                     _ptr(out), _stream(stream)), "tq_decode_attention")
+    return out
+
+
+def tq_decode_step(ctx, cache: "Cache", q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   seq_lens: torch.Tensor, max_len: int, workspace: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Append k_new / v_new ([batch][heads_kv][d], or [batch][heads_kv][1][d]) at slot
+    seq_lens[b], then attend over seq_lens[b] + 1 tokens; seq_lens is not modified."""
+    B, Hq, d = q.shape
+    assert q.is_contiguous() and k_new.is_contiguous() and v_new.is_contiguous()
+    Hkv = cache.struct.heads_kv
+    assert k_new.shape == v_new.shape and k_new.dtype == v_new.dtype and k_new.numel() == B * Hkv * d
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_cuda
+    need = tq_workspace_size(ctx, B, Hq, Hkv, max_len, 0)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    check(lib().tq_decode_step(ctx, ctypes.byref(cache.struct), _ptr(q), _dtype_code(q), _ptr(k_new), _ptr(v_new),
+                               _dtype_code(k_new), B, Hq, Hkv, _ptr(seq_lens), max_len, _ptr(workspace),
+                               workspace.numel(), _ptr(out), _stream(stream)), "tq_decode_step")
     return out
 
 

@@ -83,4 +83,6 @@ def test_host_argument_errors(tqmod):
     assert L.tq_cache_sizes_get(None, 1, 1, 1, None) == tqmod.TQ_ERR_ARG
     assert L.tq_append_quantize(None, None, None, None, 0, 1, 1, 1, None, None) == tqmod.TQ_ERR_ARG
     assert L.tq_decode_attention(None, None, None, 0, 1, 1, 1, None, 1, 0, None, 0, None, None) == tqmod.TQ_ERR_ARG
+    assert L.tq_decode_step(None, None, None, 0, None, None, 0, 1, 1, 1, None, 1, None, 0, None,
+                            None) == tqmod.TQ_ERR_ARG
     L.tq_destroy(None)  # no-op
