@@ -35,11 +35,11 @@ CAP = 8192
 # kernels of one decode step (tq_decode_step): the persistent decode kernel, which also
 # appends the step's keys and values and prepares the queries, and the combine
 LAUNCHES_PER_STEP = 2
-# DRAM bytes (read + written) of one decode-kernel launch of this workload: an ncu capture of
-# the decode-small case (context 4096) scaled to context 8192 (the kernel reads every token
-# once, so traffic grows with the tokens); None whenever the kernel has changed since the
+# DRAM bytes (read + written) of one launch of the decode-step kernel on this workload, the
+# median over the launches of an ncu launch list of this bench (dram__bytes_read.sum +
+# dram__bytes_write.sum, context 8192); None whenever the kernel has changed since that
 # capture, until it is captured again
-DECODE_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = 588_555_264
 
 
 def peaks():
