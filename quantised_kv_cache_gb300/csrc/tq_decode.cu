@@ -352,7 +352,11 @@ __device__ __forceinline__ void merge_row(const CombineArgs &a, int row, int i, 
   // persistent slices: CTA c holds tiles [bnd(c), bnd(c + 1)), bnd(c) = min(T, 4 floor(T4 c / C))
   long long T = 0, T4 = 1, C = 1, c_lo = 0, c_hi = -1;
   int unit = 0;
-  auto bnd = [&](long long c) -> long long { return min(T, 4 * (T4 * c / C)); };
+  bool narrow = true;  // every quotient below fits 32-bit division
+  auto qdiv = [&](long long n, long long d) -> long long {
+    return narrow ? (long long)((uint32_t)n / (uint32_t)d) : n / d;
+  };
+  auto bnd = [&](long long c) -> long long { return min(T, 4 * qdiv(T4 * c, C)); };
   int hh = 0;
   if (a.tile_prefix) {
     const int b = row / a.heads_q, h = (row % a.heads_q) / a.group;
@@ -361,12 +365,13 @@ __device__ __forceinline__ void merge_row(const CombineArgs &a, int row, int i, 
     T = (long long)a.heads_kv * __ldg(a.tile_prefix + a.batch);
     T4 = (T + 3) / 4;
     C = a.persist_ctas;
+    narrow = (T4 + 1) * (C + 1) < (1LL << 32);
     unit = b * a.heads_kv + h;
     if (nb > 0) {
       const long long us = (long long)a.heads_kv * p0 + (long long)h * nb, ue = us + nb;
       // the CTA holding tile g: the largest c with bnd(c) <= g
-      c_lo = ((us / 4 + 1) * C - 1) / T4;
-      c_hi = (((ue - 1) / 4 + 1) * C - 1) / T4;
+      c_lo = qdiv((us / 4 + 1) * C - 1, T4);
+      c_hi = qdiv(((ue - 1) / 4 + 1) * C - 1, T4);
     }
   }
   const int ng = a.persist_groups;
