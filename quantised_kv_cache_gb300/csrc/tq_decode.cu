@@ -518,25 +518,17 @@ __device__ __forceinline__ void half2_pair(uint32_t st, float &z, float &s) {
   s = __half2float(__ushort_as_half((unsigned short)(st >> 16)));
 }
 
-// four channels 4L..4L+3 of token t: per-channel stats preloaded in (pz, ps)
-template <bool PER_CHANNEL>
-__device__ __forceinline__ void kivi_token(const uint32_t *codes, const uint32_t *stats_tok, const uint16_t *ring,
-                                           bool quantised, int t, int R, int lane, const float (&pz)[4],
-                                           const float (&ps)[4], float (&x)[4]) {
-  if (quantised) {
-    const uint32_t f = kivi_lane_field(codes + (size_t)t * 8, lane);
-    if (PER_CHANNEL) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) x[c] = fmaf(ps[c], (float)((f >> (2 * c)) & 3u), pz[c]);
-    } else {
-      float z, s;
-      half2_pair(__ldg(stats_tok + (size_t)t * 4 + (lane >> 3)), z, s);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) x[c] = fmaf(s, (float)((f >> (2 * c)) & 3u), z);
-    }
-  } else {
-    load4(ring + (size_t)(t % R) * kD, 4 * lane, true, x);
-  }
+// Code j (0..3) of a lane's 8-bit field f (bits 2j, 2j + 1) as the float 1 + c/4, exactly:
+// its two bits placed in the top of the mantissa of 1.0. A dequantised value z + s c is then
+// 4 s (1 + c/4) + (z - 4 s), so the two stats fold into per-group (or per-token) constants
+// and each code costs a shift, a logic op and one FMA, without an int-to-float conversion.
+__device__ __forceinline__ float kivi_code_f(uint32_t f, int j) {
+  return __uint_as_float(0x3F800000u | ((f << (21 - 2 * j)) & 0x600000u));
+}
+
+// four channels 4L..4L+3 of window token t (bfloat16 ring)
+__device__ __forceinline__ void kivi_window(const uint16_t *ring, int t, int R, int lane, float (&x)[4]) {
+  load4(ring + (size_t)(t % R) * kD, 4 * lane, true, x);
 }
 
 template <bool KPC, bool VPT, int G>
@@ -577,8 +569,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
   const uint16_t *vring = a.v_ring + bh * R * kD;
   const int my_tok = tile_token_of_lane(lane);
 
+  // per lane: the sum of its query coordinates (per-token key stats)
+  float qsum[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) qsum[g] = (qv[g][0] + qv[g][1]) + (qv[g][2] + qv[g][3]);
+
   for (int tile = t_begin + warp * kTile; tile < t_end; tile += kDecodeWarps * kTile) {
-    const bool quant = tile < nq;
+    const bool quant = tile < nq;  // tiles lie wholly in the quantised part or the window
     float kz[4] = {0.f, 0.f, 0.f, 0.f}, kscl[4] = {0.f, 0.f, 0.f, 0.f};
     float vz[4] = {0.f, 0.f, 0.f, 0.f}, vscl[4] = {0.f, 0.f, 0.f, 0.f};
     if (quant && KPC) {
@@ -591,14 +588,46 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
       half2_pair(s4.x, vz[0], vscl[0]); half2_pair(s4.y, vz[1], vscl[1]);
       half2_pair(s4.z, vz[2], vscl[2]); half2_pair(s4.w, vz[3], vscl[3]);
     }
+    // per-channel key stats: this lane's part of q . k_hat = cst + sum_j (4 q_j s_j) (1 + c_j / 4)
+    float q4s[G][4], cst[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      cst[g] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        q4s[g][j] = 4.f * qv[g][j] * kscl[j];
+        cst[g] = fmaf(qv[g][j], fmaf(-4.f, kscl[j], kz[j]), cst[g]);
+      }
+    }
     float part[G][kTile];
 #pragma unroll
     for (int jj = 0; jj < kTile; ++jj) {
       const int t = min(tile + jj, t_end - 1);
-      float x[4];
-      kivi_token<KPC>(kc, ks_tok, kring, quant, t, R, lane, kz, kscl, x);
+      if (quant) {
+        const uint32_t f = kivi_lane_field(kc + (size_t)t * 8, lane);
+        float fc[4];
 #pragma unroll
-      for (int g = 0; g < G; ++g) part[g][jj] = qv[g][0] * x[0] + qv[g][1] * x[1] + qv[g][2] * x[2] + qv[g][3] * x[3];
+        for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
+        if (KPC) {
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            part[g][jj] = fmaf(q4s[g][3], fc[3], fmaf(q4s[g][2], fc[2], fmaf(q4s[g][1], fc[1], fmaf(q4s[g][0], fc[0], cst[g]))));
+        } else {
+          // per-token key stats of this lane's channel group: z q_sum + 4 s (sum_j q_j f_j - q_sum)
+          float z, sc;
+          half2_pair(__ldg(ks_tok + (size_t)t * 4 + (lane >> 3)), z, sc);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float d = fmaf(qv[g][3], fc[3], fmaf(qv[g][2], fc[2], fmaf(qv[g][1], fc[1], qv[g][0] * fc[0])));
+            part[g][jj] = fmaf(4.f * sc, d - qsum[g], z * qsum[g]);
+          }
+        }
+      } else {
+        float x[4];
+        kivi_window(kring, t, R, lane, x);
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g][jj] = qv[g][0] * x[0] + qv[g][1] * x[1] + qv[g][2] * x[2] + qv[g][3] * x[3];
+      }
     }
     const bool valid = tile + my_tok < t_end;
     float p[G];
@@ -620,18 +649,61 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[g][j] *= scale;
     }
+    // values: p (z + s c) = (4 p s) (1 + c/4) + p (z - 4 s); per-token stats fold into the
+    // token's weight, per-channel ones into the tile's sums u_j = sum p (1 + c_j / 4), P = sum p
+    float u[G][4], pz[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      pz[g] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) u[g][j] = 0.f;
+    }
 #pragma unroll
     for (int jj = 0; jj < kTile; ++jj) {
       const int t = tile + jj;
       if (t >= t_end) break;
-      float x[4];
-      kivi_token<!VPT>(vc, vs_tok, vring, quant, t, R, lane, vz, vscl, x);
+      float w[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float w = __shfl_sync(kFull, p[g], lane_of_tile_token(jj));
+      for (int g = 0; g < G; ++g) w[g] = __shfl_sync(kFull, p[g], lane_of_tile_token(jj));
+      if (quant) {
+        const uint32_t f = kivi_lane_field(vc + (size_t)t * 8, lane);
+        float fc[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w, x[j], acc[g][j]);
+        for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
+        if (VPT) {
+          float z, sc;
+          half2_pair(__ldg(vs_tok + (size_t)t * 4 + (lane >> 3)), z, sc);
+          const float s4 = 4.f * sc, z4 = fmaf(-4.f, sc, z);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float w1 = w[g] * s4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w1, fc[j], acc[g][j]);
+            pz[g] = fmaf(w[g], z4, pz[g]);
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) u[g][j] = fmaf(w[g], fc[j], u[g][j]);
+            pz[g] += w[g];
+          }
+        }
+      } else {
+        float x[4];
+        kivi_window(vring, t, R, lane, x);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w[g], x[j], acc[g][j]);
       }
+    }
+    if (quant) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          acc[g][j] += VPT ? pz[g] : fmaf(4.f * vscl[j], u[g][j], fmaf(-4.f, vscl[j], vz[j]) * pz[g]);
     }
   }
 #pragma unroll
