@@ -574,17 +574,50 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
 #pragma unroll
   for (int g = 0; g < G; ++g) qsum[g] = (qv[g][0] + qv[g][1]) + (qv[g][2] + qv[g][3]);
 
-  for (int tile = t_begin + warp * kTile; tile < t_end; tile += kDecodeWarps * kTile) {
-    const bool quant = tile < nq;  // tiles lie wholly in the quantised part or the window
+  // Quantised tokens stream through a per-warp double buffer in shared memory, one 32-token
+  // group per stage (cp.async, 16 bytes per lane and copy): the K and V codes (1 KB each) and
+  // the group's K and V statistics (512 B each: per-channel [128] or per-token [32][4]
+  // (zero, step) pairs). A warp takes whole groups; window tokens are read directly.
+  __shared__ __align__(16) uint32_t s_buf[kDecodeWarps][2][768];  // kc 256 | vc 256 | ks 128 | vs 128 words
+  auto prefetch = [&](int tile0, int bi) {
+    uint32_t *sb = s_buf[warp][bi];
+    const uint32_t *k0 = kc + (size_t)tile0 * 8, *v0 = vc + (size_t)tile0 * 8;
+    cp_async_16(sb + 8 * lane, k0 + 8 * lane);
+    cp_async_16(sb + 8 * lane + 4, k0 + 8 * lane + 4);
+    cp_async_16(sb + 256 + 8 * lane, v0 + 8 * lane);
+    cp_async_16(sb + 256 + 8 * lane + 4, v0 + 8 * lane + 4);
+    const uint32_t *ks0 = KPC ? ks_ch + (size_t)(tile0 / 32) * kD : ks_tok + (size_t)tile0 * 4;
+    const uint32_t *vs0 = VPT ? vs_tok + (size_t)tile0 * 4 : vs_ch + (size_t)(tile0 / 32) * kD;
+    cp_async_16(sb + 512 + 4 * lane, ks0 + 4 * lane);
+    cp_async_16(sb + 640 + 4 * lane, vs0 + 4 * lane);
+    cp_async_commit();
+  };
+  constexpr int kGroupTok = 32;
+  const int qend = min(t_end, nq);  // this chunk's quantised tokens end here
+  int it = 0;
+  if (t_begin + warp * kGroupTok < qend) prefetch(t_begin + warp * kGroupTok, 0);
+  for (int tile0 = t_begin + warp * kGroupTok; tile0 < t_end; tile0 += kDecodeWarps * kGroupTok, ++it) {
+    const bool quant = tile0 < nq;  // groups lie wholly in the quantised part or the window
+    const uint32_t *sb = s_buf[warp][it & 1];
+    if (quant) {
+      const int nxt = tile0 + kDecodeWarps * kGroupTok;
+      if (nxt < qend) {
+        prefetch(nxt, (it + 1) & 1);
+        cp_async_wait_one();
+      } else {
+        cp_async_wait_all();
+      }
+      __syncwarp();
+    }
     float kz[4] = {0.f, 0.f, 0.f, 0.f}, kscl[4] = {0.f, 0.f, 0.f, 0.f};
     float vz[4] = {0.f, 0.f, 0.f, 0.f}, vscl[4] = {0.f, 0.f, 0.f, 0.f};
     if (quant && KPC) {
-      const uint4 s4 = __ldg(reinterpret_cast<const uint4 *>(ks_ch + (size_t)(tile / 32) * kD) + lane);
+      const uint4 s4 = reinterpret_cast<const uint4 *>(sb + 512)[lane];
       half2_pair(s4.x, kz[0], kscl[0]); half2_pair(s4.y, kz[1], kscl[1]);
       half2_pair(s4.z, kz[2], kscl[2]); half2_pair(s4.w, kz[3], kscl[3]);
     }
     if (quant && !VPT) {
-      const uint4 s4 = __ldg(reinterpret_cast<const uint4 *>(vs_ch + (size_t)(tile / 32) * kD) + lane);
+      const uint4 s4 = reinterpret_cast<const uint4 *>(sb + 640)[lane];
       half2_pair(s4.x, vz[0], vscl[0]); half2_pair(s4.y, vz[1], vscl[1]);
       half2_pair(s4.z, vz[2], vscl[2]); half2_pair(s4.w, vz[3], vscl[3]);
     }
@@ -599,112 +632,115 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
         cst[g] = fmaf(qv[g][j], fmaf(-4.f, kscl[j], kz[j]), cst[g]);
       }
     }
-    float part[G][kTile];
+    for (int tile = tile0; tile < tile0 + kGroupTok && tile < t_end; tile += kTile) {
+      float part[G][kTile];
 #pragma unroll
-    for (int jj = 0; jj < kTile; ++jj) {
-      const int t = min(tile + jj, t_end - 1);
-      if (quant) {
-        const uint32_t f = kivi_lane_field(kc + (size_t)t * 8, lane);
-        float fc[4];
+      for (int jj = 0; jj < kTile; ++jj) {
+        const int t = min(tile + jj, t_end - 1);
+        if (quant) {
+          const uint32_t f = sb[(t - tile0) * 8 + (lane >> 2)] >> (8 * (lane & 3));
+          float fc[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
-        if (KPC) {
+          for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
+          if (KPC) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              part[g][jj] = fmaf(q4s[g][3], fc[3], fmaf(q4s[g][2], fc[2], fmaf(q4s[g][1], fc[1], fmaf(q4s[g][0], fc[0], cst[g]))));
+          } else {
+            // per-token key stats of this lane's channel group: z q_sum + 4 s (sum_j q_j f_j - q_sum)
+            float z, sc;
+            half2_pair(sb[512 + (t - tile0) * 4 + (lane >> 3)], z, sc);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float d = fmaf(qv[g][3], fc[3], fmaf(qv[g][2], fc[2], fmaf(qv[g][1], fc[1], qv[g][0] * fc[0])));
+              part[g][jj] = fmaf(4.f * sc, d - qsum[g], z * qsum[g]);
+            }
+          }
+        } else {
+          float x[4];
+          kivi_window(kring, t, R, lane, x);
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g][jj] = qv[g][0] * x[0] + qv[g][1] * x[1] + qv[g][2] * x[2] + qv[g][3] * x[3];
+        }
+      }
+      const bool valid = tile + my_tok < t_end;
+      float p[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float s = reduce8(part[g], lane);
+        s = valid ? s : -INFINITY;
+        float tmax = fmaxf(s, __shfl_xor_sync(kFull, s, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+        const float mnew = fmaxf(m[g], tmax);
+        const float scale = __expf(m[g] - mnew);
+        p[g] = valid ? __expf(s - mnew) : 0.f;
+        float psum = p[g] + __shfl_xor_sync(kFull, p[g], 4);
+        psum += __shfl_xor_sync(kFull, psum, 8);
+        psum += __shfl_xor_sync(kFull, psum, 16);
+        l[g] = l[g] * scale + psum;
+        m[g] = mnew;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[g][j] *= scale;
+      }
+      // values: p (z + s c) = (4 p s) (1 + c/4) + p (z - 4 s); per-token stats fold into the
+      // token's weight, per-channel ones into the tile's sums u_j = sum p (1 + c_j / 4), P = sum p
+      float u[G][4], pz[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        pz[g] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) u[g][j] = 0.f;
+      }
+#pragma unroll
+      for (int jj = 0; jj < kTile; ++jj) {
+        const int t = tile + jj;
+        if (t >= t_end) break;
+        float w[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) w[g] = __shfl_sync(kFull, p[g], lane_of_tile_token(jj));
+        if (quant) {
+          const uint32_t f = sb[256 + (t - tile0) * 8 + (lane >> 2)] >> (8 * (lane & 3));
+          float fc[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
+          if (VPT) {
+            float z, sc;
+            half2_pair(sb[640 + (t - tile0) * 4 + (lane >> 3)], z, sc);
+            const float s4 = 4.f * sc, z4 = fmaf(-4.f, sc, z);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float w1 = w[g] * s4;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w1, fc[j], acc[g][j]);
+              pz[g] = fmaf(w[g], z4, pz[g]);
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) u[g][j] = fmaf(w[g], fc[j], u[g][j]);
+              pz[g] += w[g];
+            }
+          }
+        } else {
+          float x[4];
+          kivi_window(vring, t, R, lane, x);
 #pragma unroll
           for (int g = 0; g < G; ++g)
-            part[g][jj] = fmaf(q4s[g][3], fc[3], fmaf(q4s[g][2], fc[2], fmaf(q4s[g][1], fc[1], fmaf(q4s[g][0], fc[0], cst[g]))));
-        } else {
-          // per-token key stats of this lane's channel group: z q_sum + 4 s (sum_j q_j f_j - q_sum)
-          float z, sc;
-          half2_pair(__ldg(ks_tok + (size_t)t * 4 + (lane >> 3)), z, sc);
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float d = fmaf(qv[g][3], fc[3], fmaf(qv[g][2], fc[2], fmaf(qv[g][1], fc[1], qv[g][0] * fc[0])));
-            part[g][jj] = fmaf(4.f * sc, d - qsum[g], z * qsum[g]);
-          }
+            for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w[g], x[j], acc[g][j]);
         }
-      } else {
-        float x[4];
-        kivi_window(kring, t, R, lane, x);
-#pragma unroll
-        for (int g = 0; g < G; ++g) part[g][jj] = qv[g][0] * x[0] + qv[g][1] * x[1] + qv[g][2] * x[2] + qv[g][3] * x[3];
       }
-    }
-    const bool valid = tile + my_tok < t_end;
-    float p[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float s = reduce8(part[g], lane);
-      s = valid ? s : -INFINITY;
-      float tmax = fmaxf(s, __shfl_xor_sync(kFull, s, 4));
-      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
-      tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-      const float mnew = fmaxf(m[g], tmax);
-      const float scale = __expf(m[g] - mnew);
-      p[g] = valid ? __expf(s - mnew) : 0.f;
-      float psum = p[g] + __shfl_xor_sync(kFull, p[g], 4);
-      psum += __shfl_xor_sync(kFull, psum, 8);
-      psum += __shfl_xor_sync(kFull, psum, 16);
-      l[g] = l[g] * scale + psum;
-      m[g] = mnew;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[g][j] *= scale;
-    }
-    // values: p (z + s c) = (4 p s) (1 + c/4) + p (z - 4 s); per-token stats fold into the
-    // token's weight, per-channel ones into the tile's sums u_j = sum p (1 + c_j / 4), P = sum p
-    float u[G][4], pz[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      pz[g] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) u[g][j] = 0.f;
-    }
-#pragma unroll
-    for (int jj = 0; jj < kTile; ++jj) {
-      const int t = tile + jj;
-      if (t >= t_end) break;
-      float w[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) w[g] = __shfl_sync(kFull, p[g], lane_of_tile_token(jj));
       if (quant) {
-        const uint32_t f = kivi_lane_field(vc + (size_t)t * 8, lane);
-        float fc[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
-        if (VPT) {
-          float z, sc;
-          half2_pair(__ldg(vs_tok + (size_t)t * 4 + (lane >> 3)), z, sc);
-          const float s4 = 4.f * sc, z4 = fmaf(-4.f, sc, z);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float w1 = w[g] * s4;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w1, fc[j], acc[g][j]);
-            pz[g] = fmaf(w[g], z4, pz[g]);
-          }
-        } else {
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) u[g][j] = fmaf(w[g], fc[j], u[g][j]);
-            pz[g] += w[g];
-          }
-        }
-      } else {
-        float x[4];
-        kivi_window(vring, t, R, lane, x);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w[g], x[j], acc[g][j]);
+          for (int j = 0; j < 4; ++j)
+            acc[g][j] += VPT ? pz[g] : fmaf(4.f * vscl[j], u[g][j], fmaf(-4.f, vscl[j], vz[j]) * pz[g]);
       }
     }
-    if (quant) {
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          acc[g][j] += VPT ? pz[g] : fmaf(4.f * vscl[j], u[g][j], fmaf(-4.f, vscl[j], vz[j]) * pz[g]);
-    }
+    __syncwarp();  // every lane is done with this stage before it is refilled
   }
 #pragma unroll
   for (int g = 0; g < G; ++g) {

@@ -43,6 +43,7 @@ __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
