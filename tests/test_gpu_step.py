@@ -179,3 +179,29 @@ def test_step_argument_errors():
     with pytest.raises(tq.TQError) as e:
         tq.tq_decode_step(ctx.handle, cache, q, kv, kv, seq, max_len=8, workspace=ws)
     assert e.value.status == tq.TQ_ERR_WORKSPACE
+
+
+
+@pytest.mark.parametrize("k_per_channel,v_per_token", [(True, True), (False, False)])
+@pytest.mark.parametrize("L", [100, 159, 191])
+def test_step_kivi_equals_append_then_decode(k_per_channel, v_per_token, L):
+    # KIVI takes the general path (a length kernel, the append, the decode). At L = 159 the
+    # step's token brings the window to 160 tokens, so the append also quantises a group out
+    # of the window
+    B, H = 3, 2
+    w = wl.WORKLOADS[5]
+    q, k, v = wl.generate(w, "cpu", seed=41, batch=B, heads_kv=H, seq=L + 1)
+    ctx = tq.Context(128, 2, "KIVI", 9, k_per_channel=k_per_channel, v_per_token=v_per_token)
+    ref = tq.Cache(ctx, B, H, 192)
+    tq.tq_append_quantize(ctx.handle, ref, k[:, :, :L].contiguous().to(DEV), v[:, :, :L].contiguous().to(DEV),
+                          torch.zeros(B, dtype=torch.int32, device=DEV))
+    kn, vn = k[:, :, L:].contiguous(), v[:, :, L:].contiguous()
+    fused = _clone(ctx, ref)
+    want = _two_calls(ctx, ref, q, kn, vn, [L] * B)
+    seq = torch.full((B,), L, dtype=torch.int32, device=DEV)
+    got = tq.tq_decode_step(ctx.handle, fused, q.to(DEV), kn.to(DEV), vn.to(DEV), seq, max_len=192)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    for name, t in ref.tensors.items():
+        assert torch.equal(t, fused.tensors[name]), name
+    assert torch.equal(got, want)
