@@ -51,6 +51,77 @@ def peaks():
     return 6800.0, "fallback"
 
 
+class NvmlClocks:
+    """SM clock, power and clock-event reasons of one GPU read through NVML (the driver's
+    libnvidia-ml, read-only queries) every 10 ms on a host thread, each sample with its host
+    time, so that the samples taken inside the timed loop can be picked out."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid, index):
+        import ctypes
+        self.ct = ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.L, self.h = L, ctypes.c_void_p()
+        found = uuid is not None and L.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(self.h)) == 0
+        if not found and L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        v = ctypes.c_uint()
+        self.max_mhz = float(v.value) if L.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(v)) == 0 else None
+        self.samples, self.stop_flag, self.thread = [], False, None
+
+    def _one(self):
+        ct, L = self.ct, self.L
+        clk, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if L.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) != 0:
+            return None
+        power = mw.value / 1e3 if L.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) == 0 else float("nan")
+        reasons = rs.value if self.reasons_fn(self.h, ct.byref(rs)) == 0 else 0
+        return (time.perf_counter(), float(clk.value), power, reasons)
+
+    def start(self):
+        import threading
+
+        def loop():
+            while not self.stop_flag:
+                smp = self._one()
+                if smp is not None:
+                    self.samples.append(smp)
+                time.sleep(0.01)
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+
+    def stop(self, window=None):
+        self.stop_flag = True
+        self.thread.join(timeout=5)
+        rows = self.samples
+        inside = [r for r in rows if window is None or window[0] <= r[0] <= window[1]]
+        scope = "timed loop" if inside and window is not None else "whole run"
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "nvml"}
+        sm = sorted(r[1] for r in use)
+        reasons = sorted({name for r in use for bit, name in self.REASONS.items() if r[3] & bit})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(use), "scope": scope, "power_w_max": max(r[2] for r in use), "source": "nvml"}
+
+
+def clock_sampler(device_index):
+    """NVML where the driver's library loads, else nvidia-smi."""
+    try:
+        import torch
+        props = torch.cuda.get_device_properties(device_index)
+        uuid = str(getattr(props, "uuid", "")) or None
+        return NvmlClocks(uuid, device_index)
+    except Exception:
+        return Clocks(device_index)
+
+
 class Clocks:
     """nvidia-smi sampled every 100 ms from the warm-up through the timed loops."""
 
@@ -72,7 +143,7 @@ class Clocks:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.send_signal(signal.SIGTERM)
@@ -391,7 +462,7 @@ def main():
     # written, the output (written by the combine, counted here as in the step)
     decode_kernel_bytes = B * H * CAP * rec + B * w.heads_q * d * (2 + 4) + B * H * (2 * d * 2 + rec)
 
-    clocks = Clocks(local)
+    clocks = clock_sampler(local)
     clocks.start()
     for i in range(args.warmup):
         step(i)
@@ -402,11 +473,13 @@ def main():
     # the steps as a user runs them: the library's kernels follow one another with
     # programmatic overlap, so no event sits between them here
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host0 = time.perf_counter()
     t_start.record()
     for i in range(K):
         step(i)
     t_stop.record()
     torch.cuda.synchronize()
+    timed_window = (host0, time.perf_counter())
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_stop), dist, dev)
     ms_step = elapsed_ms / K
     value = job_throughput(step_bytes * K, world, elapsed_ms / 1e3) / 1e9
@@ -487,7 +560,7 @@ def main():
         e2e_step(i)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
-    clk = clocks.stop()
+    clk = clocks.stop(timed_window)
     e2e_value = job_throughput(step_bytes * K, world, e2e_s) / 1e9
 
     line = None
