@@ -10,6 +10,11 @@
 //   its own mbarrier. Each (CTA, head) segment ends in one partial softmax record.
 // * decode2_g1_kernel -- split-K over a fixed (batch, head, chunk) grid, for
 //   batches too large for the persistent kernel's shared-memory prefix table.
+// * decode_persist_kernel<..., true> -- the persistent kernel as one decode step:
+//   it also computes the lengths after the step's append and the tile prefix,
+//   appends the new key and value of every head whose last tile its slice holds
+//   (before its ring's first copy, with S^T bulk-copied into the key-table area),
+//   and rotates its own queries.
 //
 // Both compute softmax(q K_hat^T / sqrt(d)) V_hat with keys read through
 // logits and values through the p-weighted sum in the rotated domain
@@ -652,7 +657,8 @@ __device__ __forceinline__ void step_lengths(const Decode2Args &a, int *s_pre, i
 // or q / sqrt(d) for unrotated keys.
 __device__ __forceinline__ void stage_query(const Decode2Args &a, int row, int lane, float *raw) {
   if (a.q_bf16)
-    cp_async_8(reinterpret_cast<uint16_t *>(raw) + 4 * lane, static_cast<const uint16_t *>(a.q_raw) + (size_t)row * kD + 4 * lane);
+    cp_async_8(reinterpret_cast<uint16_t *>(raw) + 4 * lane,
+               static_cast<const uint16_t *>(a.q_raw) + (size_t)row * kD + 4 * lane);
   else
     cp_async_16(raw + 4 * lane, static_cast<const float *>(a.q_raw) + (size_t)row * kD + 4 * lane);
   cp_async_commit();
