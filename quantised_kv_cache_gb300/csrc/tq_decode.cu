@@ -20,6 +20,8 @@
 
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "tq_device.cuh"
 #include "tq_ptx.cuh"
 
@@ -632,12 +634,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
         cst[g] = fmaf(qv[g][j], fmaf(-4.f, kscl[j], kz[j]), cst[g]);
       }
     }
-    for (int tile = tile0; tile < tile0 + kGroupTok && tile < t_end; tile += kTile) {
+    // one 8-token sub-tile; QUANT: of a quantised group (always whole: chunks and groups are
+    // 32-token aligned), so no token is masked and every record offset is a constant
+    auto sub8 = [&](const int tile, auto quant_c) {
+      constexpr bool QUANT = decltype(quant_c)::value;
       float part[G][kTile];
 #pragma unroll
       for (int jj = 0; jj < kTile; ++jj) {
-        const int t = min(tile + jj, t_end - 1);
-        if (quant) {
+        const int t = QUANT ? tile + jj : min(tile + jj, t_end - 1);
+        if constexpr (QUANT) {
           const uint32_t f = sb[(t - tile0) * 8 + (lane >> 2)] >> (8 * (lane & 3));
           float fc[4];
 #pragma unroll
@@ -663,7 +668,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
           for (int g = 0; g < G; ++g) part[g][jj] = qv[g][0] * x[0] + qv[g][1] * x[1] + qv[g][2] * x[2] + qv[g][3] * x[3];
         }
       }
-      const bool valid = tile + my_tok < t_end;
+      const bool valid = QUANT || tile + my_tok < t_end;
       float p[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -695,11 +700,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
 #pragma unroll
       for (int jj = 0; jj < kTile; ++jj) {
         const int t = tile + jj;
-        if (t >= t_end) break;
+        if (!QUANT && t >= t_end) break;
         float w[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) w[g] = __shfl_sync(kFull, p[g], lane_of_tile_token(jj));
-        if (quant) {
+        if constexpr (QUANT) {
           const uint32_t f = sb[256 + (t - tile0) * 8 + (lane >> 2)] >> (8 * (lane & 3));
           float fc[4];
 #pragma unroll
@@ -732,13 +737,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
             for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w[g], x[j], acc[g][j]);
         }
       }
-      if (quant) {
+      if constexpr (QUANT) {
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             acc[g][j] += VPT ? pz[g] : fmaf(4.f * vscl[j], u[g][j], fmaf(-4.f, vscl[j], vz[j]) * pz[g]);
       }
+    };
+    if (quant) {
+#pragma unroll
+      for (int sub = 0; sub < kGroupTok / kTile; ++sub) sub8(tile0 + kTile * sub, std::true_type{});
+    } else {
+      for (int tile = tile0; tile < tile0 + kGroupTok && tile < t_end; tile += kTile) sub8(tile, std::false_type{});
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
   }
