@@ -1,6 +1,6 @@
-// Inline-PTX helpers for sm_103a: mbarriers, 1-D TMA bulk copies (global ->
-// shared, completion counted in bytes on an mbarrier), warp-level matrix moves
-// and the legacy tensor-core MMA used for small contractions.
+// Inline-PTX helpers for sm_103a: programmatic dependent launch, mbarriers, 1-D TMA
+// bulk copies (global -> shared, completion counted in bytes on an mbarrier), cp.async,
+// proxy fences, and the legacy tensor-core MMA used for small contractions.
 //
 // Every wait is bounded: a wait that exceeds its iteration budget records
 // TQ_ERR_TIMEOUT in the device error word and returns false, so a kernel can
@@ -122,13 +122,6 @@ __device__ __forceinline__ void tma_load_1d(void *smem_dst, const void *gmem_src
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// 8x8 b16 matrix transpose across the warp (fragment layout: lane (g,t) holds row g, cols 2t, 2t+1)
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t y;
-  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 
