@@ -528,9 +528,13 @@ __device__ __forceinline__ float kivi_code_f(uint32_t f, int j) {
   return __uint_as_float(0x3F800000u | ((f << (21 - 2 * j)) & 0x600000u));
 }
 
-// four channels 4L..4L+3 of window token t (bfloat16 ring)
-__device__ __forceinline__ void kivi_window(const uint16_t *ring, int t, int R, int lane, float (&x)[4]) {
-  load4(ring + (size_t)(t % R) * kD, 4 * lane, true, x);
+// four channels 4L..4L+3 of a window token's bfloat16 row staged in shared memory (64 words)
+__device__ __forceinline__ void kivi_window_row(const uint32_t *row, int lane, float (&x)[4]) {
+  const uint2 w = reinterpret_cast<const uint2 *>(row)[lane];
+  x[0] = bf16_bits_to_float(w.x & 0xffffu);
+  x[1] = bf16_bits_to_float(w.x >> 16);
+  x[2] = bf16_bits_to_float(w.y & 0xffffu);
+  x[3] = bf16_bits_to_float(w.y >> 16);
 }
 
 template <bool KPC, bool VPT, int G>
@@ -638,6 +642,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
     // 32-token aligned), so no token is masked and every record offset is a constant
     auto sub8 = [&](const int tile, auto quant_c) {
       constexpr bool QUANT = decltype(quant_c)::value;
+      // window tokens: the sub-tile's K and V rows (8 x 256 B each) staged in this warp's
+      // buffer in one round of copies (no quantised group is in flight once the window starts)
+      const uint32_t *wb = &s_buf[warp][0][0];
+      if constexpr (!QUANT) {
+#pragma unroll
+        for (int c = lane; c < 256; c += 32) {
+          const int tensor = c >> 7, jj = (c >> 4) & 7, part = c & 15;
+          const int t = min(tile + jj, t_end - 1);
+          cp_async_16(&s_buf[warp][0][0] + tensor * 512 + jj * 64 + 4 * part,
+                      (tensor ? vring : kring) + (size_t)(t % R) * kD + 8 * part);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncwarp();
+      }
       float part[G][kTile];
 #pragma unroll
       for (int jj = 0; jj < kTile; ++jj) {
@@ -663,7 +682,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
           }
         } else {
           float x[4];
-          kivi_window(kring, t, R, lane, x);
+          kivi_window_row(wb + jj * 64, lane, x);
 #pragma unroll
           for (int g = 0; g < G; ++g) part[g][jj] = qv[g][0] * x[0] + qv[g][1] * x[1] + qv[g][2] * x[2] + qv[g][3] * x[3];
         }
@@ -730,7 +749,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
           }
         } else {
           float x[4];
-          kivi_window(vring, t, R, lane, x);
+          kivi_window_row(wb + 512 + jj * 64, lane, x);
 #pragma unroll
           for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -743,6 +762,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             acc[g][j] += VPT ? pz[g] : fmaf(4.f * vscl[j], u[g][j], fmaf(-4.f, vscl[j], vz[j]) * pz[g]);
+      } else {
+        __syncwarp();  // every lane is done with the staged rows before the next copies
       }
     };
     if (quant) {
