@@ -182,13 +182,13 @@ class OracleDecode:
     stored-record format. Timed: unpack the records, reconstruct K and V in
     fp64, dense softmax attention of one query."""
 
-    def __init__(self, N, bits, seed):
+    def __init__(self, N, bits, seed, data_seed=None):
         import numpy as np
         from oracle import turboquant as otq
         self.otq = otq
         self.params = otq.make_params(128, bits, "KQV", seed)
         self.rk, self.rv = self.params.roles()
-        g = np.random.default_rng(seed)
+        g = np.random.default_rng(seed if data_seed is None else data_seed)
         K = g.standard_normal((N, 128)) * np.exp(g.standard_normal(128))[None, :]
         V = g.standard_normal((N, 128))
         self.ek = otq.encode(K, self.rk, self.params)
@@ -215,39 +215,179 @@ class OracleDecode:
                 return heads, el
 
 
-def host_threads():
-    threads = os.cpu_count()
+def cpu_model() -> str:
+    """The host CPU's model string (lscpu, else /proc/cpuinfo, else the machine type)."""
     try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [threads])
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name"):
+                return line.split(":", 1)[1].strip()
     except Exception:
         pass
-    return threads
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+_ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def _oracle_worker(job):
+    """One single-threaded oracle process (spawned; BLAS limited to one thread by the
+    environment it inherits): set up one unit of the workload untimed, then repeat the
+    timed operation for `seconds`. Returns (units done, seconds)."""
+    kind, seconds, seed = job
+    import numpy as np
+    if kind == "decode":
+        od = OracleDecode(CAP, 4, 42, data_seed=seed)
+        units, t0 = 0, time.perf_counter()
+        while True:
+            od.one_head()
+            units += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return units, el
+    from oracle import turboquant as otq
+    params = otq.make_params(128, 4, "KQV", 42)
+    rk, rv = params.roles()
+    K, V = config2_like_vectors(QUANTISE_BATCH, seed)
+    units, t0 = 0, time.perf_counter()
+    while True:
+        otq.encode(K, rk, params)
+        otq.encode(V, rv, params)
+        units += QUANTISE_BATCH
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return units, el
+
+
+QUANTISE_BATCH = 2048  # token-heads (one K and one V vector each) per timed oracle encode
+
+
+def config2_like_vectors(n, seed):
+    """n keys shaped like the decode workload's (N(0, 1) times per-channel log-normal(0, 1)
+    scales with four x10 outlier channels) and n N(0, 1) values, rounded to bf16 values, as
+    float64 for the oracle."""
+    import numpy as np
+    g = np.random.default_rng(seed)
+    scale = np.exp(g.standard_normal(128))
+    scale[g.choice(128, 4, replace=False)] *= 10.0
+    K = g.standard_normal((n, 128)) * scale[None, :]
+    V = g.standard_normal((n, 128))
+
+    def bf16(x):
+        u = x.astype(np.float32).view(np.uint32)
+        u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+        return u.view(np.float32).astype(np.float64)
+    return bf16(K), bf16(V)
+
+
+def oracle_rates(kind: str, procs: int, seconds: float):
+    """Units per second of the oracle's `kind` ("decode": (batch, head) units of 8192 tokens;
+    "quantise": token-heads) over `procs` single-threaded spawned processes, each working
+    on its own unit of the workload for `seconds`."""
+    import multiprocessing as mp
+    saved = {k: os.environ.get(k) for k in _ONE_THREAD_ENV}
+    for k in _ONE_THREAD_ENV:
+        os.environ[k] = "1"
+    try:
+        with mp.get_context("spawn").Pool(procs) as pool:
+            res = pool.map(_oracle_worker, [(kind, seconds, 4242 + i) for i in range(procs)])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    units = sum(u for u, _ in res)
+    rate = sum(u / el for u, el in res)
+    return rate, units, max(el for _, el in res)
+
+
+def cpu_baseline(seconds_each: float = 3.0):
+    """The oracle timed on this host: decode attention and quantise, on one thread and on
+    every core (one single-threaded process per core, each on its own unit)."""
+    cores = os.cpu_count() or 1
+    rec = 140
+    out = {"kind": "oracle", "cores": cores, "cpu_model": cpu_model(), "unit": "GB/s"}
+    for kind in ("decode", "quantise"):
+        out[kind] = {}
+        for label, procs in (("1_thread", 1), ("all_cores", cores)):
+            rate, units, el = oracle_rates(kind, procs, seconds_each)
+            if kind == "decode":
+                row = {"heads_per_s": rate, "token_heads_per_s": rate * CAP,
+                       "GB_per_s": rate * CAP * rec / 1e9, "units": units}
+            else:
+                row = {"token_heads_per_s": rate,
+                       "GB_per_s": rate * (2 * 128 * 2 + rec) / 1e9, "units": units}
+            row.update({"threads": procs, "seconds": el})
+            out[kind][label] = row
+    out["value"] = out["decode"]["all_cores"]["GB_per_s"]
+    out["threads"] = cores
+    out["sample"] = (f"decode: (batch, head) units of the decode workload (8192 tokens, KQV n=4) decoded "
+                     f"from their records for {seconds_each:.0f} s per process; quantise: batches of "
+                     f"{QUANTISE_BATCH} K and V vectors shaped like the workload's; each on 1 process and "
+                     f"on {cores} single-threaded processes (one per core)")
+    return out
+
+
+_WORKER_OD = None
+
+
+def _ref_init(seed):
+    global _WORKER_OD
+    _WORKER_OD = OracleDecode(CAP, 4, 42, data_seed=seed)
+
+
+def _ref_decode_one(_):
+    _WORKER_OD.one_head()
+    return 1
 
 
 def run_reference(args, rank):
-    """The oracle as the reference arm, on this host's cores (rank 0 only)."""
+    """The oracle as the reference arm, on this host's cores (rank 0 only): one
+    single-threaded process per core, each holding one (batch, head) unit of the decode
+    workload in the stored-record format (set up untimed). A step decodes one unit in
+    every process at once; K steps are timed after W warm-up steps."""
     if rank != 0:
         return
-    N, bits = CAP, 4
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
     rec = 140  # bytes per token-head, KQV n=4
-    per_head_bytes = N * rec
-    od = OracleDecode(N, bits, 42)
-    for _ in range(args.warmup):
-        od.one_head()
-    total_heads, total_s = 0, 0.0
-    threads = host_threads()
-    for _ in range(args.steps):
-        h, s = od.run(0.0)
-        total_heads += h
-        total_s += s
-    gbs = total_heads * per_head_bytes / total_s / 1e9
-    sample = f"{total_heads} of the 512 (batch, head) decode units over {N} tokens, one per step"
+    saved = {k: os.environ.get(k) for k in _ONE_THREAD_ENV}
+    for k in _ONE_THREAD_ENV:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(cores, initializer=_ref_init, initargs=(0,)) as pool:
+            for _ in range(args.warmup):
+                pool.map(_ref_decode_one, range(cores), chunksize=1)
+            t0 = time.perf_counter()
+            heads = 0
+            for _ in range(args.steps):
+                heads += sum(pool.map(_ref_decode_one, range(cores), chunksize=1))
+            total_s = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    gbs = heads * CAP * rec / total_s / 1e9
+    sample = (f"{heads} (batch, head) decode units of the workload ({CAP} tokens each, from their stored "
+              f"records), {cores} per step, one per single-threaded process")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(),
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "threads": cores,
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -301,19 +441,26 @@ def run_small_case(args, dev):
     print(json.dumps({"case": args.case, "ok": True}), flush=True)
 
 
-def run_configs(args, dev):
-    """Decode throughput on the other workloads (one JSON line each): config 1 (single head),
-    config 3 (three schemes at 4 bits), config 4 (GQA 32q/8kv, N=131072, KQV n=3), config 5
-    (KIVI, two layouts). Caches smaller than 3x L2 are replicated and rotated so that every
-    call reads HBM. Times are CUDA events around the library's decode kernel (profile events)
-    and around the whole call (query prep + decode + combine)."""
+CONFIG_CASES = ([(1, "KQV", 4, None)]
+                + [(3, sch, n, None) for sch in ("KV", "KQV", "QKQV") for n in (2, 3, 4)]
+                + [(4, "KQV", 3, None)]
+                + [(5, "KIVI", 2, lay) for lay in ((True, True), (False, False), (False, True), (True, False))])
+
+
+def measure_configs(dev, cases=CONFIG_CASES):
+    """Decode and bulk append-quantise throughput on every workload (one row per case):
+    config 1 (single head), config 3 (three schemes x three budgets), config 4 (GQA 32q/8kv,
+    N=131072, KQV n=3, 64 chunks), config 5 (KIVI, four layouts). Caches smaller than 3x L2
+    are replicated and rotated so that every decode call reads HBM. Decode times are CUDA
+    events around the library's decode kernel (its profile events, on the call's stream)
+    and around the whole call (query prep + decode + combine); append times are events
+    around a bulk append of the whole context into one cache."""
     import torch
     from quantised_kv_cache_gb300 import tq
     from quantised_kv_cache_gb300 import workloads as wl
     hbm_peak, peak_kind = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    cases = [(1, "KQV", 4, None), (3, "KV", 4, None), (3, "KQV", 4, None), (3, "QKQV", 4, None),
-             (4, "KQV", 3, None), (5, "KIVI", 2, (True, True)), (5, "KIVI", 2, (False, False))]
+    rows = []
     for wid, scheme, n, kivi in cases:
         w = wl.WORKLOADS[wid]
         B, Hq, H, N = w.batch, w.heads_q, w.heads_kv, w.seq
@@ -329,13 +476,19 @@ def run_configs(args, dev):
         caches = [one] + [tq.Cache(ctx, B, H, N, device=dev) for _ in range(reps - 1)]
         zeros = torch.zeros((B,), dtype=torch.int32, device=dev)
         for c in caches:
-            if scheme == "KIVI":
-                for t0 in range(0, N, 512):
-                    t1 = min(N, t0 + 512)
-                    lens = torch.full((B,), t0, dtype=torch.int32, device=dev)
-                    tq.tq_append_quantize(ctx.handle, c, k[:, :, t0:t1].contiguous(), v[:, :, t0:t1].contiguous(), lens)
-            else:
-                tq.tq_append_quantize(ctx.handle, c, k, v, zeros)
+            tq.tq_append_quantize(ctx.handle, c, k, v, zeros)
+        # bulk append of the whole context (the first fill above was its warm-up)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        arep = 3
+        torch.cuda.synchronize()
+        a0.record()
+        for _ in range(arep):
+            tq.tq_append_quantize(ctx.handle, one, k, v, zeros)
+        a1.record()
+        torch.cuda.synchronize()
+        append_ms = a0.elapsed_time(a1) / arep
+        in_bytes = B * H * N * 128 * k.element_size() * 2
+        append_bytes = in_bytes + (B * H * N * rec if scheme != "KIVI" else bytes_call)
         lens = torch.full((B,), N, dtype=torch.int32, device=dev)
         splits = w.splits
         ws = torch.empty(tq.tq_workspace_size(ctx.handle, B, Hq, H, N, splits), dtype=torch.uint8, device=dev)
@@ -361,14 +514,27 @@ def run_configs(args, dev):
         ms_kernel = sum(a_.elapsed_time(b_) for a_, b_ in evs) / iters
         ms_call = c0.elapsed_time(c1) / iters
         gbs_k, gbs_c = bytes_call / ms_kernel / 1e6, bytes_call / ms_call / 1e6
-        print(json.dumps({"case": "configs", "config": wid, "scheme": scheme, "bits": n,
-                          "kivi_layout": None if kivi is None else {"k_per_channel": kivi[0], "v_per_token": kivi[1]},
-                          "shape": {"batch": B, "heads_q": Hq, "heads_kv": H, "context": N},
-                          "bytes_per_call": bytes_call, "replicas": reps,
-                          "ms_kernel": ms_kernel, "GBps_kernel": gbs_k, "frac_kernel": gbs_k / hbm_peak,
-                          "ms_call": ms_call, "GBps_call": gbs_c, "frac_call": gbs_c / hbm_peak,
-                          "peak": hbm_peak, "peak_kind": peak_kind}), flush=True)
-        del caches, one
+        append_gbs = append_bytes / append_ms / 1e6
+        rows.append({"config": wid, "scheme": scheme, "bits": n,
+                     "kivi_layout": None if kivi is None else {"k_per_channel": kivi[0], "v_per_token": kivi[1]},
+                     "shape": {"batch": B, "heads_q": Hq, "heads_kv": H, "context": N,
+                               "input_dtype": str(k.dtype).replace("torch.", "")},
+                     "decode": {"bytes_per_call": bytes_call, "replicas": reps, "ms_kernel": ms_kernel,
+                                "GB_per_s_kernel": gbs_k, "frac_kernel": gbs_k / hbm_peak, "ms_call": ms_call,
+                                "GB_per_s_call": gbs_c, "frac_call": gbs_c / hbm_peak},
+                     "append": {"ms": append_ms, "tokens_per_s": B * N / (append_ms / 1e3),
+                                "token_heads_per_s": B * H * N / (append_ms / 1e3), "bytes": append_bytes,
+                                "GB_per_s": append_gbs, "frac": append_gbs / hbm_peak},
+                     "peak": hbm_peak, "peak_kind": peak_kind})
+        del caches, one, q, k, v, ws, out
+        ctx.close()
+        torch.cuda.empty_cache()
+    return rows
+
+
+def run_configs(args, dev):
+    for row in measure_configs(dev):
+        print(json.dumps(dict(case="configs", **row)), flush=True)
 
 
 def main():
@@ -378,6 +544,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table of the N=1 line")
     ap.add_argument("--case", choices=["step", "decode-small", "append-small", "configs"], default="step",
                     help="step: the benchmark; *-small: one kernel family on B16 H32 N4096 (294 MB of records, "
                          "above L2) for profiler captures")
@@ -439,7 +606,7 @@ def main():
     hbm_peak, peak_kind = peaks()
 
     # ---------------- decode step
-    pool = [wl.step_token(w, s, dev) for s in range(8)]
+    pool = [wl.step_token(w, s, dev, data_seed=1002 + rank) for s in range(8)]
     lens_append = torch.full((B,), CAP - 1, dtype=torch.int32, device=dev)
     lens_decode = torch.full((B,), CAP, dtype=torch.int32, device=dev)
     ws = torch.empty(tq.tq_workspace_size(ctx.handle, B, w.heads_q, H, CAP, 0), dtype=torch.uint8, device=dev)
@@ -506,6 +673,29 @@ def main():
     torch.cuda.synchronize()
     two_calls_ms = t_start.elapsed_time(t_stop) / K
     assert tq.tq_get_device_error(ctx.handle) == 0
+
+    # ---------------- the same step on a paged cache: every sequence-head's blocks scattered
+    # over a pool by a shuffled block table (the records copied there untimed)
+    nblk = cache.blocks_per_seq
+    perm = torch.randperm(B * H * nblk, generator=torch.Generator().manual_seed(77)).to(torch.int32)
+    paged = tq.PagedCache(ctx, B, H, CAP, B * H * nblk, perm.view(B, H, nblk).contiguous(), device=dev)
+    paged.tensors["records"].view(B * H * nblk, -1)[perm.long().to(dev)] = cache.blocks().view(B * H * nblk, -1)
+
+    def step_paged(i):
+        q, kn, vn = pool[i % len(pool)]
+        tq.tq_decode_step(ctx.handle, paged, q, kn, vn, lens_append, CAP, ws, out)
+
+    for i in range(args.warmup):
+        step_paged(i)
+    torch.cuda.synchronize()
+    t_start.record()
+    for i in range(K):
+        step_paged(i)
+    t_stop.record()
+    torch.cuda.synchronize()
+    paged_ms = t_start.elapsed_time(t_stop) / K
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    del paged
 
     # ---------------- end to end through the ABI with host buffers
     pin = [(q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()) for q, kn, vn in pool]
@@ -587,16 +777,17 @@ def main():
                     "ms_per_step": 1e3 * e2e_s / K},
             "two_calls": {"ms_per_step": two_calls_ms,
                           "what": "the same step as tq_append_quantize + tq_decode_attention (4 launches)"},
+            "paged": {"ms_per_step": paged_ms, "GB_per_s": step_bytes / (paged_ms / 1e3) / 1e9,
+                      "frac": step_bytes / (paged_ms / 1e3) / 1e9 / hbm_peak,
+                      "what": "the same step on a paged cache: each sequence-head's 16-token blocks at "
+                              "shuffled pool positions through a block table"},
             "gpu_launches": LAUNCHES_PER_STEP * K,
             "clocks": clk,
         }
+        if world == 1 and not args.no_configs:
+            line["configs"] = measure_configs(dev)
         if not args.no_cpu_baseline:
-            heads, secs = OracleDecode(CAP, w.bits, 42).run(15.0)
-            threads = host_threads()
-            line["cpu_baseline"] = {"value": heads * CAP * rec / secs / 1e9, "unit": "GB/s", "cores": threads,
-                                    "kind": "oracle",
-                                    "sample": f"{heads} (batch, head) decode units of this workload "
-                                              f"(8192 tokens each) in {secs:.1f} s"}
+            line["cpu_baseline"] = cpu_baseline()
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

@@ -135,7 +135,7 @@
 extern "C" {
 #endif
 
-#define TQ_ABI_VERSION 2
+#define TQ_ABI_VERSION 3
 
 typedef struct tq_ctx tq_ctx; /* opaque, host-owned */
 
@@ -169,13 +169,33 @@ typedef enum {
 
 /* Device pointers of one cache. Sizes come from tq_cache_sizes; a pointer
  * whose size is 0 is unused and may be NULL. Every non-NULL pointer must be
- * 16-byte aligned. */
+ * 16-byte aligned.
+ *
+ * Paged layout (TQ schemes only; [KIVI-geom] "The systems tax": decoding appends
+ * one token at a time, so a serving cache grows block by block). With
+ * block_table == NULL the records array is the contiguous
+ * [batch][heads_kv][ceil(capacity / 16)] block grid described above. With a
+ * block table, `records` is a pool of `pool_blocks` 16-token blocks (each
+ * tq_cache_sizes.block_bytes, same plane layout) and
+ *   block_table : int32 [batch][heads_kv][ceil(capacity / 16)], device memory,
+ * maps block j of sequence-head (b, h) -- its token slots 16 j .. 16 j + 15 --
+ * to pool block block_table[(b * heads_kv + h) * ceil(capacity / 16) + j].
+ * Entries a call reaches (the blocks holding the slots it writes or reads) must
+ * lie in [0, pool_blocks) and distinct sequence-heads must not share a block;
+ * entries no call reaches are ignored (-1 is a conventional "unmapped"). A
+ * reached entry outside [0, pool_blocks) is skipped (no access through it) and
+ * sets the device error word to TQ_ERR_ARG. The table is read, never written,
+ * by the library; the caller owns it and may change entries between calls (in
+ * stream order). Results are the contiguous layout's, bit for bit, whatever the
+ * mapping. */
 typedef struct tq_cache {
   int batch, heads_kv, capacity;
-  uint8_t *records;                          /* TQ schemes: the blocked records */
+  uint8_t *records;                          /* TQ schemes: the blocked records (or the pool) */
   uint8_t *k_codes;  uint8_t *v_codes;       /* KIVI: 2-bit codes */
   uint16_t *k_stats; uint16_t *v_stats;      /* KIVI: fp16 (zero, step) */
   uint16_t *k_window; uint16_t *v_window;    /* KIVI: bf16 ring buffers */
+  const int32_t *block_table;                /* TQ schemes: NULL (contiguous) or the block table */
+  int pool_blocks;                           /* blocks in the pool when block_table != NULL */
 } tq_cache;
 
 typedef struct tq_cache_sizes {
@@ -219,6 +239,10 @@ tq_status tq_set_kivi(tq_ctx *ctx, int group, int window, int k_per_channel, int
 tq_status tq_cache_sizes_get(const tq_ctx *ctx, int batch, int heads_kv, int capacity,
                              tq_cache_sizes *out);
 
+/* The same call under the name the cache-sizing step was first specified with
+ * (tq_cache_bytes): identical arguments, results and errors. */
+tq_status tq_cache_bytes(const tq_ctx *ctx, int batch, int heads_kv, int capacity, tq_cache_sizes *out);
+
 /* Quantise and write n_new tokens per sequence ([HeadQ] 3, "cache write";
  * [KIVI-geom] "The systems tax": per-token append).
  *   d_k, d_v : [batch][heads_kv][n_new][d] contiguous, dtype TQ_F32 or TQ_BF16
@@ -246,6 +270,11 @@ tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const voi
  * is larger). splits = 0 asks for the library's choice for max_len. */
 tq_status tq_workspace_size(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len,
                             int splits, size_t *out);
+
+/* The same call as tq_workspace_size under the name the workspace-sizing step was
+ * first specified with (tq_workspace_bytes): identical arguments, results, errors. */
+tq_status tq_workspace_bytes(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len, int splits,
+                             size_t *out);
 
 /* Decode attention read straight from the compressed cache ([HeadQ] 2.1-2.2;
  * [TQ-stats] "Theoretical framework": keys through the logits, values
@@ -347,8 +376,10 @@ tq_status tq_set_profile_events(tq_ctx *ctx, void *start, void *stop, void *appe
  *  - The call allocates nothing: no cudaMalloc, cudaFree or allocating
  *    library routine.
  *  - The first call on a device looks up the array's device address (with
- *    that device current, which must be the context's device) and caches it;
- *    make that first call before any stream capture begins.
+ *    that device current) and caches it; make that first call before any
+ *    stream capture begins. The current device must be the context's device
+ *    (TQ_ERR_ARG otherwise). After cudaDeviceReset on a device the cached
+ *    address is stale: do not call this entry point on that device again.
  *  - Requests whose workspace (tq_workspace_size) exceeds the array return
  *    TQ_ERR_WORKSPACE before any launch.
  *  - Every call shares the one array and the array keeps the last call's

@@ -24,6 +24,8 @@ namespace {
 struct Append2Args {
   const void *x;
   int batch, heads, n_new, capacity, cap16, bb;
+  const int32_t *btab;  // paged caches (NULL: contiguous)
+  int pool_blocks;
   int vt;  // value role: codes in the pair-interleaved layout (merged atomically)
   const int32_t *seq_lens;
   uint8_t *codes;
@@ -68,7 +70,8 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
       if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);
       continue;
     }
-    const long long slot = bh * a.cap16 + len + t;
+    const long long slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
+    if (slot < 0) continue;
 
     float x[kD];
     if (BF16) {
@@ -213,6 +216,8 @@ int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.capacity = a.capacity;
   k.cap16 = a.cap16;
   k.bb = a.bb;
+  k.btab = a.btab;
+  k.pool_blocks = a.pool_blocks;
   k.vt = a.vt;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;

@@ -60,6 +60,8 @@ struct BulkGeo {
 
 struct BulkArgs {
   int batch, heads, n_new, capacity, cap16, bb;
+  const int32_t *btab;  // paged caches (NULL: contiguous)
+  int pool_blocks;
   long long total;
   const int32_t *seq_lens;
   uint8_t *codes;
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         const long long bh = vec / a.n_new;
         const int b = (int)(bh / a.heads);
         const int len = __ldg(a.seq_lens + b);
-        if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.cap16 + len + t;
+        if (len >= 0 && len + a.n_new <= a.capacity) slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
         else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
       }
       // value codes: is the other token of this token's pair (slot ^ 1) the neighbouring lane's?
@@ -624,6 +626,8 @@ int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.capacity = a.capacity;
   k.cap16 = a.cap16;
   k.bb = a.bb;
+  k.btab = a.btab;
+  k.pool_blocks = a.pool_blocks;
   k.total = total;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;

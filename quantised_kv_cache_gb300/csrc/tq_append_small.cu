@@ -43,6 +43,8 @@ struct SmallRole {
 struct SmallArgs {
   SmallRole role[2];  // keys, values (plane bases in the blocked records)
   int batch, heads, n_new, capacity, cap16, bb;
+  const int32_t *btab;  // paged caches (NULL: contiguous)
+  int pool_blocks;
   const int32_t *seq_lens;
   const float *diag;       // D as +/-1.0f
   const float *sketch_tp;  // entry (i, 4L + m) = S[8(L/2) + 2m + (L&1)][i]
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
     // a sequence whose new tokens would not all fit is skipped whole
     const bool ok = len >= 0 && len + a.n_new <= a.capacity;
     if (!ok && t == 0 && lane == 0 && blockIdx.y == 0) set_error(a.error, TQ_ERR_CAPACITY);
-    slot = ok ? bh * a.cap16 + len + t : -1;
+    slot = ok ? phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error) : -1;
 
     float x[4];
     load4(ro.x, (size_t)vec * kD + 4 * lane, BF16, x);
@@ -199,6 +201,8 @@ int launch_append_small(const AppendArgs &k, const AppendArgs &v, const tq_ctx *
   s.capacity = k.capacity;
   s.cap16 = k.cap16;
   s.bb = k.bb;
+  s.btab = k.btab;
+  s.pool_blocks = k.pool_blocks;
   s.seq_lens = k.seq_lens;
   s.diag = ctx->dparams->diag;
   s.sketch_tp = ctx->dparams->sketch_tp;

@@ -44,6 +44,8 @@ namespace {
 struct TcArgs {
   const void *x;
   int batch, heads, n_new, capacity, cap16, bb;
+  const int32_t *btab;  // paged caches (NULL: contiguous)
+  int pool_blocks;
   int vt;  // value role: codes in the pair-interleaved layout
   const int32_t *seq_lens;
   uint8_t *codes;
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
       const long long bh = vec / a.n_new;
       const int b = (int)(bh / a.heads);
       const int len = __ldg(a.seq_lens + b);
-      if (len >= 0 && len + a.n_new <= a.capacity) slot = bh * a.cap16 + len + t;
+      if (len >= 0 && len + a.n_new <= a.capacity) slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
       else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
     }
     float nu, xs;
@@ -495,6 +497,8 @@ int launch_append_tc(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.capacity = a.capacity;
   k.cap16 = a.cap16;
   k.bb = a.bb;
+  k.btab = a.btab;
+  k.pool_blocks = a.pool_blocks;
   k.vt = a.vt;
   k.seq_lens = a.seq_lens;
   k.codes = a.codes;

@@ -120,6 +120,9 @@ struct DecodeKernelArgs {
   const uint8_t *v_signs;
   const float *v_rnorm;
   int bb, cap16;  // blocked records (plane pointers are the block-0 bases)
+  const int32_t *btab;  // paged caches (NULL: contiguous)
+  int pool_blocks;
+  int *error;
   int capacity, heads_kv, heads_q, chunk, splits;
   const int32_t *seq_lens;
   const float *qprep;
@@ -200,10 +203,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
   }
 
   const long long slot0 = ((long long)b * a.heads_kv + hk) * a.cap16;
-  auto rec32 = [&](const uint8_t *plane, int t, int tok) {
-    return reinterpret_cast<const uint32_t *>(rec_at(plane, slot0 + t, a.bb, tok));
+  // token t's physical slot (an unmapped block of a paged cache reads block 0; the error
+  // word reports it)
+  auto ps = [&](int t) -> long long {
+    const long long p = phys_slot(a.btab, a.pool_blocks, slot0 + t, a.error);
+    return p < 0 ? 0 : p;
   };
-  auto recf = [&](const float *plane, int t) { return __ldg(rec_at(plane, slot0 + t, a.bb, 4)); };
+  auto rec32 = [&](const uint8_t *plane, long long slot, int tok) {
+    return reinterpret_cast<const uint32_t *>(rec_at(plane, slot, a.bb, tok));
+  };
+  auto recf = [&](const float *plane, long long slot) { return __ldg(rec_at(plane, slot, a.bb, 4)); };
   const int my_tok = tile_token_of_lane(lane);
 
   for (int tile = t_begin + warp * kTile; tile < t_end; tile += kDecodeWarps * kTile) {
@@ -211,21 +220,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
     float part[G][kTile];
 #pragma unroll
     for (int jj = 0; jj < kTile; ++jj) {
-      const int t = min(tile + jj, t_end - 1);
+      const long long sl = ps(min(tile + jj, t_end - 1));
       uint32_t code[4];
-      lane_codes<KB>(rec32(a.k_codes, t, KB * 16), lane, code);
+      lane_codes<KB>(rec32(a.k_codes, sl, KB * 16), lane, code);
       float c[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) c[j] = s_cb[code[j]];
-      const float nu = recf(a.k_norm, t);
+      const float nu = recf(a.k_norm, sl);
       float sg[4];
       float rk = 0.f;
       if (KQJL) {
         uint32_t sb[4];
-        lane_signs(rec32(a.k_signs, t, 16), lane, sb);
+        lane_signs(rec32(a.k_signs, sl, 16), lane, sb);
 #pragma unroll
         for (int j = 0; j < 4; ++j) sg[j] = sb[j] ? 1.f : -1.f;
-        rk = recf(a.k_rnorm, t);
+        rk = recf(a.k_rnorm, sl);
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -265,17 +274,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
       const int t = tile + jj;
       if (t >= t_end) break;
       const int src = lane_of_tile_token(jj);
+      const long long sl = ps(t);
       uint32_t code[4];
-      lane_codes_vt<VB>(a.v_codes, slot0 + t, a.bb, lane, code);  // pair-interleaved value codes
+      lane_codes_vt<VB>(a.v_codes, sl, a.bb, lane, code);  // pair-interleaved value codes
       float c[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) c[j] = s_cb[16 + code[j]];
-      const float nu = recf(a.v_norm, t);
+      const float nu = recf(a.v_norm, sl);
       uint32_t sb[4] = {0u, 0u, 0u, 0u};
       float rv = 0.f;
       if (VQJL) {
-        lane_signs(rec32(a.v_signs, t, 16), lane, sb);
-        rv = recf(a.v_rnorm, t);
+        lane_signs(rec32(a.v_signs, sl, 16), lane, sb);
+        rv = recf(a.v_rnorm, sl);
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -876,6 +886,9 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   k.v_signs = plane(TQ_PLANE_V_SIGNS); k.v_rnorm = reinterpret_cast<const float *>(plane(TQ_PLANE_V_RNORM));
   k.bb = L.bb;
   k.cap16 = cap16_of(c->capacity);
+  k.btab = c->block_table;
+  k.pool_blocks = c->pool_blocks;
+  k.error = &ctx->dparams->error;
   k.capacity = c->capacity;
   k.heads_kv = a.heads_kv;
   k.heads_q = a.heads_q;

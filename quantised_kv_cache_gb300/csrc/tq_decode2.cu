@@ -104,8 +104,10 @@ constexpr int persist_stages() {
 }
 
 struct Decode2Args {
-  const uint8_t *records;  // blocked records: [sequence-head][cap16 / 16] blocks of `bb` bytes
+  const uint8_t *records;  // blocked records: [sequence-head][cap16 / 16] blocks of `bb` bytes (or a pool)
   int bb, cap16;
+  const int32_t *btab;     // paged caches: virtual block -> pool block (NULL: contiguous)
+  int pool_blocks;
   int capacity, batch, heads_kv, heads_q, chunk, splits;
   const int32_t *seq_lens;
   const int32_t *tile_prefix;  // persistent kernel: [batch + 1] tiles before each batch
@@ -513,12 +515,36 @@ __device__ __forceinline__ void merge_parked(const float *src, int i, float *rec
   rec[2 + kD + i] = Sg;
 }
 
-// Copy the blocks holding tokens s0 .. s0 + n - 1 (s0 a multiple of 16) into a stage.
+// The stored block holding virtual slot vslot (a multiple of 16): contiguous caches keep
+// block vslot / 16 in place, paged ones at the pool block the table names; nullptr for an
+// unmapped entry (recorded as TQ_ERR_ARG; the stage then keeps stale data and the output of
+// that head is meaningless, which the error word reports).
+template <int BLOCK>
+__device__ __forceinline__ const uint8_t *block_src(const Decode2Args &a, long long vslot) {
+  const long long p = phys_slot(a.btab, a.pool_blocks, vslot, a.error);
+  return p < 0 ? nullptr : a.records + (p >> 4) * BLOCK;
+}
+
+// Copy the blocks holding tokens s0 .. s0 + n - 1 (s0 a multiple of 16) into a stage: one
+// copy for contiguous blocks, one per block for a paged cache.
 template <typename Gm>
 __device__ __forceinline__ void issue_tile_to(unsigned char *st, uint64_t *bar, const Decode2Args &a, long long s0, int n) {
-  const uint32_t bytes = (uint32_t)(((n + 15) >> 4) * Gm::block);
+  const int nb = (n + 15) >> 4;
+  if (a.btab == nullptr) {
+    const uint32_t bytes = (uint32_t)(nb * Gm::block);
+    mbar_arrive_expect_tx(bar, bytes);
+    tma_load_1d(st, a.records + (s0 >> 4) * Gm::block, bytes, bar);
+    return;
+  }
+  const uint8_t *src[4];
+  uint32_t bytes = 0;
+  for (int j = 0; j < nb; ++j) {
+    src[j] = block_src<Gm::block>(a, s0 + 16 * j);
+    if (src[j]) bytes += Gm::block;
+  }
   mbar_arrive_expect_tx(bar, bytes);
-  tma_load_1d(st, a.records + (s0 >> 4) * Gm::block, bytes, bar);
+  for (int j = 0; j < nb; ++j)
+    if (src[j]) tma_load_1d(st + j * Gm::block, src[j], (uint32_t)Gm::block, bar);
 }
 
 // ============================================================================
@@ -693,7 +719,8 @@ __device__ __forceinline__ void prep_query(const Decode2Args &a, int lane, float
 // shared memory.
 __device__ __forceinline__ void step_append(const Decode2Args &a, int u, int role, int len, int lane,
                                             const float *s_sk) {
-  const long long slot = (long long)u * a.cap16 + len;
+  const long long slot = phys_slot(a.btab, a.pool_blocks, (long long)u * a.cap16 + len, a.error);
+  if (slot < 0) return;  // an unmapped block: nothing appended (the error word says so)
   float x[4];
   load4(role ? a.v_new : a.k_new, (size_t)u * kD + 4 * lane, a.kv_bf16 != 0, x);
   const WarpRole &ro = a.role[role];
@@ -831,10 +858,9 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     const int t0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - t0);
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
-      mbar_arrive_expect_tx(bar, n > 0 ? (uint32_t)Gm::block : 0u);
-      if (n > 0)
-        tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, a.records + ((cur_row + t0) >> 4) * Gm::block,
-                    (uint32_t)Gm::block, bar);
+      const uint8_t *src = n > 0 ? block_src<Gm::block>(a, cur_row + t0) : nullptr;
+      mbar_arrive_expect_tx(bar, src ? (uint32_t)Gm::block : 0u);
+      if (src) tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, src, (uint32_t)Gm::block, bar);
     }
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
@@ -1212,10 +1238,9 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
     const int tt0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - tt0);
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
-      mbar_arrive_expect_tx(bar, n > 0 ? (uint32_t)Q::block : 0u);
-      if (n > 0)
-        tma_load_1d(s_stage + stn * Q::stage + qtr * Q::block, a.records + ((cur_row + tt0) >> 4) * Q::block,
-                    (uint32_t)Q::block, bar);
+      const uint8_t *src = n > 0 ? block_src<Q::block>(a, cur_row + tt0) : nullptr;
+      mbar_arrive_expect_tx(bar, src ? (uint32_t)Q::block : 0u);
+      if (src) tma_load_1d(s_stage + stn * Q::stage + qtr * Q::block, src, (uint32_t)Q::block, bar);
     }
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
@@ -1420,6 +1445,8 @@ Decode2Args decode2_args(const DecodeArgs &a) {
   k.records = c->records;
   k.bb = ctx->lay.bb;
   k.cap16 = cap16_of(c->capacity);
+  k.btab = c->block_table;
+  k.pool_blocks = c->pool_blocks;
   k.capacity = c->capacity;
   k.batch = a.batch;
   k.heads_kv = a.heads_kv;
@@ -1510,6 +1537,8 @@ int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
     k.records = c->records;
     k.bb = ctx->lay.bb;
     k.cap16 = cap16_of(c->capacity);
+    k.btab = c->block_table;
+    k.pool_blocks = c->pool_blocks;
     k.capacity = c->capacity;
     k.batch = a.batch;
     k.heads_kv = a.heads_kv;
@@ -1543,6 +1572,8 @@ int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
   k.records = c->records;
   k.bb = ctx->lay.bb;
   k.cap16 = cap16_of(c->capacity);
+  k.btab = c->block_table;
+  k.pool_blocks = c->pool_blocks;
   k.capacity = c->capacity;
   k.batch = a.batch;
   k.heads_kv = a.heads_kv;

@@ -16,6 +16,9 @@ struct DequantKernelArgs {
   const uint8_t *signs;
   const float *rnorms;
   int bb, cap16;
+  const int32_t *btab;  // paged caches (NULL: contiguous)
+  int pool_blocks;
+  int *error;
   int vt;  // value codes: pair-interleaved layout
   int batch, heads, capacity, t0, t1;
   const float *centroids;
@@ -36,7 +39,11 @@ __global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
   if (vec >= total) return;
   const long long bh = vec / n;
   const int t = a.t0 + (int)(vec % n);
-  const long long slot = (long long)bh * a.cap16 + t;
+  const long long slot = phys_slot(a.btab, a.pool_blocks, (long long)bh * a.cap16 + t, a.error);
+  if (slot < 0) {  // an unmapped block (the error word says so): zeros
+    reinterpret_cast<float4 *>(a.out + (size_t)vec * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
   uint32_t code[4];
   if (a.vt) lane_codes_vt<BITS>(a.codes, slot, a.bb, lane, code);
   else lane_codes<BITS>(reinterpret_cast<const uint32_t *>(rec_at(a.codes, slot, a.bb, BITS * 16)), lane, code);
@@ -87,8 +94,9 @@ int go(int bits, const DequantKernelArgs &k, unsigned blocks, cudaStream_t st) {
 }  // namespace
 
 int launch_dequant_tq(const DequantArgs &a, void *stream) {
-  DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.bb, a.cap16, a.vt, a.batch, a.heads, a.capacity, a.t0, a.t1,
-                      a.centroids, a.params->diag, a.params->sketch, a.out};
+  DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.bb, a.cap16, a.btab, a.pool_blocks, a.error, a.vt,
+                      a.batch, a.heads, a.capacity, a.t0, a.t1, a.centroids, a.params->diag, a.params->sketch,
+                      a.out};
   const long long total = (long long)a.batch * a.heads * (a.t1 - a.t0);
   const unsigned blocks = (unsigned)((total + 7) / 8);
   cudaStream_t st = (cudaStream_t)stream;

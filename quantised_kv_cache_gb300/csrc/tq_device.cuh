@@ -14,6 +14,20 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kInvSqrtD = 0.08838834764831845f;   // 1 / sqrt(128)
 constexpr float kSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi / 2)
 
+// Paged caches: the physical slot of virtual slot `vslot` (= sequence-head * cap16 + t).
+// Without a block table the two coincide; with one, block vslot >> 4 of the virtual
+// grid lives at pool block bt[vslot >> 4]. Returns -1 for an entry outside
+// [0, pool_blocks) and records TQ_ERR_ARG in the error word (the caller skips the access).
+__device__ __forceinline__ long long phys_slot(const int32_t *bt, int pool_blocks, long long vslot, int *error) {
+  if (bt == nullptr || vslot < 0) return vslot;
+  const int pb = __ldg(bt + (vslot >> 4));
+  if (pb < 0 || pb >= pool_blocks) {
+    if (error) atomicCAS(error, 0, (int)TQ_ERR_ARG);
+    return -1;
+  }
+  return ((long long)pb << 4) | (vslot & 15);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);

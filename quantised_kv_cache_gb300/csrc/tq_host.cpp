@@ -425,10 +425,16 @@ static tq_status check_cache(const tq_ctx *ctx, const tq_cache *c, int batch, in
     if (!c->k_codes || !c->v_codes || !c->k_stats || !c->v_stats || !c->k_window || !c->v_window)
       return TQ_ERR_ARG;
     if (c->capacity % ctx->kivi_group) return TQ_ERR_ARG;
+    if (c->block_table) return TQ_ERR_UNSUPPORTED;  // paging covers the blocked TQ records only
     return TQ_OK;
   }
   if (!c->records) return TQ_ERR_ARG;
+  if (c->block_table && c->pool_blocks <= 0) return TQ_ERR_ARG;
   return TQ_OK;
+}
+
+tq_status tq_cache_bytes(const tq_ctx *ctx, int batch, int heads_kv, int capacity, tq_cache_sizes *out) {
+  return tq_cache_sizes_get(ctx, batch, heads_kv, capacity, out);
 }
 
 tq_status tq_append_quantize(const tq_ctx *ctx, const tq_cache *cache, const void *d_k, const void *d_v,
@@ -472,6 +478,8 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.x = d_k;
   a.bb = ctx->lay.bb;
   a.cap16 = tq::cap16_of(cache->capacity);
+  a.btab = cache->block_table;
+  a.pool_blocks = cache->pool_blocks;
   set_role_planes(ctx, cache, 0, a.codes, a.norms, a.signs, a.rnorms);
   a.vt = 0;
   a.role = ctx->k;
@@ -539,6 +547,11 @@ static void workspace_layout(const tq_ctx *ctx, void *ws, int batch, int heads_q
   int32_t *lens = (int32_t *)((char *)a.tile_prefix + ((size_t)(batch + 1) * sizeof(int32_t) + 15) / 16 * 16);
   if (step_lens) *step_lens = lens;
   a.partials = (float *)((char *)lens + ((size_t)batch * sizeof(int32_t) + 15) / 16 * 16);
+}
+
+tq_status tq_workspace_bytes(const tq_ctx *ctx, int batch, int heads_q, int heads_kv, int max_len, int splits,
+                             size_t *out) {
+  return tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, splits, out);
 }
 
 tq_status tq_decode_attention(const tq_ctx *ctx, const tq_cache *cache, const void *d_q, int q_dtype, int batch,
@@ -648,6 +661,9 @@ tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int
     a.out = out;
     a.bb = ctx->lay.bb;
     a.cap16 = tq::cap16_of(cache->capacity);
+    a.btab = cache->block_table;
+    a.pool_blocks = cache->pool_blocks;
+    a.error = &ctx->dparams->error;
     a.vt = which;
     uint8_t *codes, *signs;
     float *norms, *rnorms;

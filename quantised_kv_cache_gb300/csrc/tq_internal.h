@@ -119,6 +119,8 @@ struct AppendArgs {
   uint8_t *signs;
   float *rnorms;
   int bb, cap16;
+  const int32_t *btab;  // paged caches: the block table (NULL: contiguous)
+  int pool_blocks;
   int vt;  // 1: the value role (codes in the pair-interleaved layout)
   Role role;
   const float *centroids;  // device pointers into DevParams
@@ -200,6 +202,9 @@ struct DequantArgs {
   const uint8_t *signs;
   const float *rnorms;
   int bb, cap16;
+  const int32_t *btab;  // paged caches: the block table (NULL: contiguous)
+  int pool_blocks;
+  int *error;
   int vt;  // 1: value codes (pair-interleaved layout)
   int batch, heads, capacity, t0, t1;
   Role role;

@@ -12,7 +12,10 @@
 // Every GPU that loads this library holds it until the process exits. Host
 // code cannot use the array's name as a device address, so the first call on
 // each device looks the address up with cudaGetSymbolAddress (with that device
-// current) and caches it; every later call reuses the cached address.
+// current) and caches it; every later call reuses the cached address. A
+// cudaDeviceReset unloads the library's device code and frees the array, so the
+// cached address is then stale: this entry point must not be called on a device
+// after that device has been reset.
 
 #include <cuda_runtime.h>
 
@@ -55,6 +58,11 @@ tq_status tq_decode_attention_static(const tq_ctx *ctx, const tq_cache *cache, c
                                      int batch, int heads_q, int heads_kv, const int32_t *d_seq_lens, int max_len,
                                      int splits, float *d_out, void *stream) {
   if (!ctx) return TQ_ERR_ARG;
+  // the array is looked up on the current device, which must be the one holding the
+  // context's parameters and the caller's buffers
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return TQ_ERR_CUDA;
+  if (cur != ctx->device) return TQ_ERR_ARG;
   size_t need = 0;
   tq_status s = tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, splits, &need);
   if (s != TQ_OK) return s;

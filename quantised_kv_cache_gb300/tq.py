@@ -44,7 +44,8 @@ _sz = ctypes.c_size_t
 class tq_cache(ctypes.Structure):
     _fields_ = [("batch", _i), ("heads_kv", _i), ("capacity", _i), ("records", _vp),
                 ("k_codes", _vp), ("v_codes", _vp),
-                ("k_stats", _vp), ("v_stats", _vp), ("k_window", _vp), ("v_window", _vp)]
+                ("k_stats", _vp), ("v_stats", _vp), ("k_window", _vp), ("v_window", _vp),
+                ("block_table", _vp), ("pool_blocks", _i)]
 
 
 # the planes of a block of the records array (TQ schemes), in storage order (tq_plane)
@@ -67,6 +68,8 @@ _SIGNATURES = {
     "tq_destroy": (None, [_vp]),
     "tq_set_kivi": (_i, [_vp, _i, _i, _i, _i]),
     "tq_cache_sizes_get": (_i, [_vp, _i, _i, _i, ctypes.POINTER(tq_cache_sizes)]),
+    "tq_cache_bytes": (_i, [_vp, _i, _i, _i, ctypes.POINTER(tq_cache_sizes)]),
+    "tq_workspace_bytes": (_i, [_vp, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tq_append_quantize": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "tq_workspace_size": (_i, [_vp, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "tq_decode_attention": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _i, _i, _i, _i, _vp, _i, _i, _vp, _sz,
@@ -166,6 +169,12 @@ def tq_cache_sizes_get(ctx, batch: int, heads_kv: int, capacity: int) -> tq_cach
     return out
 
 
+def tq_cache_bytes(ctx, batch: int, heads_kv: int, capacity: int) -> tq_cache_sizes:
+    out = tq_cache_sizes()
+    check(lib().tq_cache_bytes(ctx, batch, heads_kv, capacity, ctypes.byref(out)), "tq_cache_bytes")
+    return out
+
+
 def tq_append_quantize(ctx, cache: "Cache", k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
                        stream=None) -> None:
     B, H, n, d = k.shape
@@ -179,6 +188,13 @@ def tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, splits=0) -> int:
     out = _sz()
     check(lib().tq_workspace_size(ctx, batch, heads_q, heads_kv, max_len, splits, ctypes.byref(out)),
           "tq_workspace_size")
+    return out.value
+
+
+def tq_workspace_bytes(ctx, batch, heads_q, heads_kv, max_len, splits=0) -> int:
+    out = _sz()
+    check(lib().tq_workspace_bytes(ctx, batch, heads_q, heads_kv, max_len, splits, ctypes.byref(out)),
+          "tq_workspace_bytes")
     return out.value
 
 
@@ -389,8 +405,9 @@ class Cache:
         self.tensors = {}
         self.struct = tq_cache()
         self.struct.batch, self.struct.heads_kv, self.struct.capacity = batch, heads_kv, capacity
+        self.struct.block_table, self.struct.pool_blocks = None, 0
         for p in ARRAYS:
-            n = getattr(self.sizes, p)
+            n = self._array_bytes(p)
             if n:
                 t = torch.zeros(n, dtype=torch.uint8, device=self.device)
                 assert t.data_ptr() % 16 == 0
@@ -398,6 +415,17 @@ class Cache:
                 setattr(self.struct, p, t.data_ptr())
             else:
                 setattr(self.struct, p, None)
+
+    def _array_bytes(self, name: str) -> int:
+        return getattr(self.sizes, name)
+
+    @property
+    def blocks_per_seq(self) -> int:
+        return (self.capacity + BLOCK_TOKENS - 1) // BLOCK_TOKENS
+
+    def blocks(self) -> torch.Tensor:
+        """The records as [batch * heads_kv][blocks_per_seq][block_bytes] (TQ schemes)."""
+        return self.tensors["records"].view(self.batch * self.heads_kv, self.blocks_per_seq, self.sizes.block_bytes)
 
     def plane(self, name: str) -> torch.Tensor:
         """One plane as a contiguous uint8 tensor over [batch][heads_kv][capacity] token
@@ -408,10 +436,10 @@ class Cache:
         tok = self.sizes.plane_bytes[p]
         if tok == 0:
             raise KeyError(name)
-        bb, off = self.sizes.block_bytes, self.sizes.plane_offset[p]
-        nblk = (self.capacity + BLOCK_TOKENS - 1) // BLOCK_TOKENS
+        off = self.sizes.plane_offset[p]
+        nblk = self.blocks_per_seq
         bh = self.batch * self.heads_kv
-        blocks = self.tensors["records"].view(bh, nblk, bb)
+        blocks = self.blocks()
         planes = blocks[:, :, off:off + BLOCK_TOKENS * tok]
         if name == "v_codes":
             return _pair_rows_to_records(planes, tok // 16)[:, :self.capacity].contiguous().view(-1)
@@ -424,3 +452,36 @@ class Cache:
 
     def nbytes(self) -> int:
         return sum(t.numel() for t in self.tensors.values())
+
+
+class PagedCache(Cache):
+    """A TQ-scheme cache in the paged layout (include/tq.h, "Paged layout"): `records` is a
+    pool of `pool_blocks` 16-token blocks and `block_table` (int32, on the device,
+    [batch][heads_kv][ceil(capacity / 16)]) maps each sequence-head's blocks into it; -1
+    marks an entry no call may reach. The table is the caller's: change it in place (in
+    stream order) to remap blocks."""
+
+    def __init__(self, ctx: Context, batch: int, heads_kv: int, capacity: int, pool_blocks: int,
+                 block_table: torch.Tensor, device="cuda"):
+        self.pool_blocks = int(pool_blocks)
+        super().__init__(ctx, batch, heads_kv, capacity, device)
+        nblk = self.blocks_per_seq
+        assert block_table.dtype == torch.int32 and block_table.is_contiguous()
+        assert tuple(block_table.shape) == (batch, heads_kv, nblk)
+        self.block_table = block_table.to(self.device)
+        self.struct.block_table = self.block_table.data_ptr()
+        self.struct.pool_blocks = self.pool_blocks
+
+    def _array_bytes(self, name: str) -> int:
+        if name == "records":
+            return self.pool_blocks * self.sizes.block_bytes
+        return getattr(self.sizes, name)
+
+    def blocks(self) -> torch.Tensor:
+        """The sequence-heads' blocks gathered out of the pool through the table (a copy;
+        unmapped entries read as zero blocks)."""
+        pool = self.tensors["records"].view(self.pool_blocks, self.sizes.block_bytes)
+        idx = self.block_table.view(-1).long()
+        out = pool[idx.clamp(min=0)]
+        out[idx < 0] = 0
+        return out.view(self.batch * self.heads_kv, self.blocks_per_seq, self.sizes.block_bytes)

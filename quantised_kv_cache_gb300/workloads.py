@@ -107,19 +107,37 @@ def generate(w: Workload, device="cpu", *, seed: Optional[int] = None, key_dist:
     else:
         raise ValueError(dist)
 
-    if w.key_scale_sigma > 0:
-        scale = torch.exp(w.key_scale_sigma * torch.randn((1, Hkv, 1, d), generator=g, device=device, dtype=f32))
-        if w.outlier_channels:
-            for h in range(Hkv):
-                ch = torch.randperm(d, generator=g, device=device)[: w.outlier_channels]
-                scale[0, h, 0, ch] *= w.outlier_factor
+    scale = key_channel_scales(w, Hkv, device, 1000 + w.wid if seed is None else seed)
+    if scale is not None:
         k = k * scale
     return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
 
 
-def step_token(w: Workload, step: int, device="cpu", *, batch=None, heads_kv=None, heads_q=None,
-               dtype=None):
-    """One decode step's new K/V token per sequence and its query (seeded by step)."""
+def key_channel_scales(w: Workload, heads_kv: int, device, seed: int):
+    """Per-(head, channel) key scales [1, heads_kv, 1, d]: exp(sigma N(0, 1)), with
+    `outlier_channels` seeded channels per head multiplied by `outlier_factor`; None when
+    the workload has no channel scales. Drawn from a generator of their own (seeded by the
+    data seed), so the cache's keys and every decode step's new key share them."""
+    if w.key_scale_sigma <= 0:
+        return None
+    g = _gen(device, seed + 7_919)
+    d = w.d
+    scale = torch.exp(w.key_scale_sigma * torch.randn((1, heads_kv, 1, d), generator=g, device=device,
+                                                      dtype=torch.float32))
+    if w.outlier_channels:
+        for h in range(heads_kv):
+            ch = torch.randperm(d, generator=g, device=device)[: w.outlier_channels]
+            scale[0, h, 0, ch] *= w.outlier_factor
+    return scale
+
+
+def step_token(w: Workload, step: int, device="cpu", *, data_seed: Optional[int] = None, batch=None,
+               heads_kv=None, heads_q=None, dtype=None):
+    """One decode step's new K/V token per sequence and its query (seeded by step).
+
+    The new keys follow the cache's key distribution: N(0, 1) times the per-channel
+    scales (and outlier channels) that `generate` drew with the same data seed
+    (default 1000 + workload id)."""
     B = batch or w.batch
     Hkv = heads_kv or w.heads_kv
     Hq = heads_q or (w.heads_q if heads_kv is None else Hkv * (w.heads_q // w.heads_kv))
@@ -128,4 +146,7 @@ def step_token(w: Workload, step: int, device="cpu", *, batch=None, heads_kv=Non
     k = torch.randn((B, Hkv, 1, w.d), generator=g, device=device)
     v = torch.randn((B, Hkv, 1, w.d), generator=g, device=device)
     q = torch.randn((B, Hq, w.d), generator=g, device=device)
+    scale = key_channel_scales(w, Hkv, device, 1000 + w.wid if data_seed is None else data_seed)
+    if scale is not None:
+        k = k * scale
     return q.to(dt), k.to(dt), v.to(dt)

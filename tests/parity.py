@@ -20,6 +20,48 @@ from oracle import turboquant as otq
 BAND = 1e-6
 MISMATCH_FRACTION = 1e-5
 
+D = 128
+U24 = 2.0 ** -24  # unit roundoff of float32 (round to nearest)
+U23 = 2.0 ** -23  # one ulp: a bound for any faithful rounding (e.g. truncating accumulation)
+
+
+def norm_rtol(through_rotation_mma: bool) -> float:
+    """Largest relative difference allowed between the stored float32 norm and the
+    oracle's fp64 ||x||, from a rounding-error bound of the library's arithmetic (not
+    from observed errors).
+
+    Direct paths compute s = sum_i x_i^2 with float32 FMAs in some order, then
+    sqrt(s). For an inner product evaluated in any order, |fl(x.x) - x.x| <= gamma_d
+    x.x with gamma_d = d u / (1 - d u) (Higham, "Accuracy and Stability of Numerical
+    Algorithms", 2nd ed., Lemma 3.1 and eq. (3.5)); the square root halves that relative
+    error and adds one rounding, so |nu_hat / nu - 1| <= d u / 2 + u + O(u^2). The inputs
+    reach the kernels exactly (bf16 and fp32 are exact in float32), so with
+    u = 2^-24, d = 128: (d/2 + 2) u = 3.93e-6.
+
+    The bf16 bulk path reads the norm off the rotation instead: the tensor cores form
+    y' = H' D x (H' the +/-1 Hadamard matrix, so ||y'|| = sqrt(d) ||x||) with exact
+    products and float32 accumulation, then nu = ||y'|| / sqrt(d). Each y'_n is a sum
+    of d terms of magnitude |x_j|, so |y'_n_hat - y'_n| <= gamma_{d-1} ||x||_1 with the
+    accumulation's rounding taken as merely faithful (u = 2^-23); hence
+    ||y'_hat - y'|| <= sqrt(d) gamma_{d-1} ||x||_1 <= d gamma_{d-1} ||x||_2, a relative
+    error of at most sqrt(d) gamma_{d-1} in ||y'||, plus the sum of squares, the square
+    root and the 1/sqrt(d) factor as above: sqrt(d) (d - 1) 2^-23 + (d/2 + 3) 2^-24 =
+    1.72e-4. Any plausible mistake (a dropped coordinate moves the norm by ~1/d of its
+    square) is orders of magnitude above either bound."""
+    direct = (D / 2 + 2) * U24
+    if not through_rotation_mma:
+        return direct
+    g = (D - 1) * U23 / (1 - (D - 1) * U23)
+    return math.sqrt(D) * g + (D / 2 + 3) * U24
+
+
+def bulk_bf16_path(dtype, vectors_per_tensor: int, role) -> bool:
+    """True when an append of this many bf16 vectors on this role takes the bulk
+    tensor-map kernel, whose norm comes through the rotation (norm_rtol). Appends of at
+    most 8192 vectors per tensor take the warp-per-vector launch; unrotated roles and
+    fp32 inputs compute the norm directly."""
+    return dtype == torch.bfloat16 and role.rotate and vectors_per_tensor > 8192
+
 
 def plane(cache, name, dtype, shape):
     return cache.plane(name).cpu().numpy().view(dtype).reshape(shape)

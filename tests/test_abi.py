@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(tqmod):
 
 
 def test_abi_version_and_status_strings(tqmod):
-    assert tqmod.tq_abi_version() == 2
+    assert tqmod.tq_abi_version() == 3
     assert tqmod.tq_status_str(0) == "ok"
     assert "capacity" in tqmod.tq_status_str(3)
     assert tqmod.tq_status_str(12345) == "unknown status"

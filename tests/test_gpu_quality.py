@@ -9,11 +9,8 @@ contribution 2" (at a 4-bit budget the asymmetric KQV split beats QKQV).
 Everything quantised here is produced by the CUDA path (append through the C
 ABI, tq_dequantize for K_hat / V_hat, tq_decode_attention for the output); the
 full-precision reference is fp64 attention over the raw inputs. The table is
-printed (pytest -s) and, when a gpurun_out/ folder exists, written to
-gpurun_out/quality_report.md.
+printed (visible with pytest -s).
 """
-
-import os
 
 import numpy as np
 import pytest
@@ -84,9 +81,6 @@ def _write_report():
                      f"{r['T']['snr_db']:.1f} | {r['T']['dir_err']:.2e} |")
     text = "\n".join(lines)
     print("\n" + text)
-    if os.path.isdir("gpurun_out"):
-        with open(os.path.join("gpurun_out", "quality_report.md"), "w") as f:
-            f.write(text + "\n")
 
 
 @pytest.mark.parametrize("dist", ["gauss", "lowrank", "student3"])

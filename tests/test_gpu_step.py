@@ -34,7 +34,7 @@ def _prefilled(scheme, n, B, Hkv, G, fill, cap, dtype, seed):
     ctx = tq.Context(128, n, scheme, 300 + seed)
     cache = tq.Cache(ctx, B, Hkv, cap)
     tq.tq_append_quantize(ctx.handle, cache, k.to(DEV), v.to(DEV), torch.zeros(B, dtype=torch.int32, device=DEV))
-    qs, ks, vs = wl.step_token(w, seed, "cpu")
+    qs, ks, vs = wl.step_token(w, seed, "cpu", data_seed=seed)
     ks[0, 0, 0] = 0  # a zero vector among the new tokens
     return ctx, cache, qs, ks, vs
 
@@ -97,7 +97,8 @@ def test_step_matches_the_oracle(scheme, n):
         rep = P.BandReport()
         mism = P.compare_codes(gidx, ora, ocb.lloyd_max(128, role.bits).bounds32, rep)
         assert rep.ok_out_of_band(), f"{which} codes: {rep}"
-        np.testing.assert_allclose(enc.norm[rows], ora.norm, rtol=1e-6, atol=0)
+        # the step appends through the warp-per-vector encoder: a direct sum of squares
+        np.testing.assert_allclose(enc.norm[rows], ora.norm, rtol=P.norm_rtol(False), atol=0)
         if role.qjl:
             srep = P.BandReport()
             P.compare_signs(enc.signs[rows], ora, srep, skip_rows=mism.any(axis=1))

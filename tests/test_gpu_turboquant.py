@@ -55,10 +55,13 @@ def test_context_parameters_match_the_oracle(scheme, n):
 @pytest.mark.parametrize("scheme,n", [("KQV", 4), ("KQV", 3), ("KQV", 2), ("QKQV", 4), ("QKQV", 3),
                                       ("QKQV", 2), ("KV", 4), ("KV", 2)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(2, 3, 77), (2, 4, 1111)], ids=["few", "bulk"])
+@pytest.mark.parametrize("shape", [(2, 3, 1300), (2, 4, 1111)], ids=["few", "bulk"])
 def test_append_codes_bit_exact(scheme, n, dtype, shape):
-    # "few": 462 vectors per tensor, the warp-per-vector single-launch path; "bulk": 8888,
-    # above that path's limit (the thread-per-vector kernels), with a ragged last pass
+    # "few": 7800 vectors per tensor, the warp-per-vector single-launch path (at most 8192);
+    # "bulk": 8888, above that path's limit, with a ragged last tile. Each call compares about
+    # 10^6 codes per tensor, so that the in-band mismatch fraction (bounded by 1e-5 of the
+    # codes compared) is a property of a population large enough for one legitimate in-band
+    # flip (expected ~2e-6 per code) not to exceed it by itself
     B, H, N = shape
     q, k, v = _inputs(B, H, N, dtype, seed=7 + n, scale_sigma=1.0, outliers=2)
     k[0, 1, 5] = 0  # a zero vector
@@ -79,7 +82,8 @@ def test_append_codes_bit_exact(scheme, n, dtype, shape):
         # bytes identical wherever the codes are
         same = ~code_mism.any(axis=1)
         np.testing.assert_array_equal(packed[same], otq.pack_codes(ora.idx[same], role.bits))
-        np.testing.assert_allclose(gpu.norm, ora.norm, rtol=1e-6, atol=0)
+        rtol = P.norm_rtol(P.bulk_bf16_path(dtype, B * H * N, role))
+        np.testing.assert_allclose(gpu.norm, ora.norm, rtol=rtol, atol=0)
         if role.qjl:
             srep = P.BandReport()
             P.compare_signs(gpu.signs, ora, srep, skip_rows=code_mism.any(axis=1))
@@ -98,6 +102,11 @@ def test_cache_sizes_describe_the_blocked_layout(scheme, n):
     assert list(s.plane_offset) == [16 * sum(tok[:p]) for p in range(8)]
     assert s.block_bytes == 16 * sum(tok) == 16 * s.record_bytes
     assert s.records == 3 * 2 * 4 * s.block_bytes  # ceil(50 / 16) = 4 blocks per sequence-head
+    # the sizing calls under their first-specified names give the same answers
+    a = tq.tq_cache_bytes(ctx.handle, 3, 2, 50)
+    assert bytes(a) == bytes(s)
+    for args in [(3, 2, 2, 50, 0), (3, 4, 2, 50, 5), (300, 2, 2, 40, 0)]:
+        assert tq.tq_workspace_bytes(ctx.handle, *args) == tq.tq_workspace_size(ctx.handle, *args)
 
 
 def test_a_token_lands_where_the_layout_says():
@@ -116,8 +125,8 @@ def test_a_token_lands_where_the_layout_says():
     blk = raw[10 * s.block_bytes:11 * s.block_bytes]
     knorm = blk[s.plane_offset[1] + 5 * 4:s.plane_offset[1] + 6 * 4].view(np.float32)[0]
     vnorm = blk[s.plane_offset[5] + 5 * 4:s.plane_offset[5] + 6 * 4].view(np.float32)[0]
-    np.testing.assert_allclose(knorm, float(k[1, 0, 0].double().norm()), rtol=1e-6)
-    np.testing.assert_allclose(vnorm, float(v[1, 0, 0].double().norm()), rtol=1e-6)
+    np.testing.assert_allclose(knorm, float(k[1, 0, 0].double().norm()), rtol=P.norm_rtol(False))
+    np.testing.assert_allclose(vnorm, float(v[1, 0, 0].double().norm()), rtol=P.norm_rtol(False))
     # every other entry of the cache is still zero
     raw_other = raw.copy()
     raw_other[10 * s.block_bytes:11 * s.block_bytes] = 0
@@ -203,7 +212,7 @@ def test_dequantize_matches_oracle_reconstruction(scheme, n):
 
 @pytest.mark.parametrize("scheme,n", [("KQV", 4), ("KQV", 3), ("KQV", 2), ("QKQV", 4), ("QKQV", 2),
                                       ("KV", 4), ("KV", 2)])
-@pytest.mark.parametrize("G", [1, 2, 4])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("splits", [0, 1, 5])
 def test_decode_attention_matches_oracle(scheme, n, G, splits):
     B, Hkv = 2, 2

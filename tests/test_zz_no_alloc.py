@@ -73,8 +73,7 @@ def test_static_scratch_rejects_requests_beyond_its_size():
     buf = torch.zeros(1024, dtype=torch.uint8, device=DEV)
     c = tq.tq_cache()
     c.batch, c.heads_kv, c.capacity = B, H, cap
-    for name in ("k_codes", "k_norm", "v_codes", "v_norm", "v_signs", "v_rnorm"):
-        setattr(c, name, buf.data_ptr())
+    c.records = buf.data_ptr()
     q = torch.zeros((B, H, 128), dtype=torch.float32, device=DEV)
     lens = torch.full((B,), cap, dtype=torch.int32, device=DEV)
     out = torch.zeros((B, H, 128), dtype=torch.float32, device=DEV)
