@@ -24,10 +24,10 @@ Sources (cited by title and section throughout):
   "The systems tax".
 * [KVQuant++] "KVQuant++: attention-aware KV cache quantisation" forum post:
   "Codebook design", "Fast codebook lookup", "Rate-distortion performance",
-  "Core innovation 5".
+  "Rotation-invariance guarantee", "Core innovation 5".
 
 Functions whose parity has no independent pin say "parity unpinned" in their
 docstring; at present that is only the 6D error frame in ``metrics.py``.
 """
 
-from . import rng, codebook, turboquant, attention, kivi, metrics  # noqa: F401
+from . import rng, codebook, rotation, turboquant, attention, kivi, metrics  # noqa: F401

@@ -56,9 +56,8 @@ def attend_gqa(Q: np.ndarray, K: np.ndarray, V: np.ndarray, lengths=None):
 def qkqv_scores(q: np.ndarray, enc_k: "tq.Encoded", params: "tq.Params") -> np.ndarray:
     """Scores of one query against sketched, rotated keys, in the rotated domain."""
     d = params.d
-    H = tq.hadamard(d)
     q = np.asarray(q, dtype=np.float64)
-    q_rot = H @ (params.D.astype(np.float64) * q)
+    q_rot = params.rotate(q[None, :])[0]
     c = params.codebook(enc_k.role.bits).centroids32.astype(np.float64)
     base = enc_k.norm.astype(np.float64) * (c[enc_k.idx] @ q_rot)
     s_q = params.S.astype(np.float64) @ q_rot

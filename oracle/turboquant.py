@@ -52,6 +52,7 @@ from scipy.linalg import hadamard as _scipy_hadamard
 
 from . import codebook as _cb
 from . import rng as _rng
+from . import rotation as _rot
 
 SCHEMES = ("KV", "KQV", "QKQV")
 SQRT_HALF_PI = math.sqrt(math.pi / 2.0)
@@ -85,13 +86,15 @@ def scheme_roles(scheme: str, n: int):
 
 @dataclass(frozen=True)
 class Params:
-    """The quantiser state a context holds: D, S and the codebooks it needs."""
+    """The quantiser state a context holds: D, S, the rotation and the codebooks it needs."""
     d: int
     n: int
     scheme: str
     seed: int
     D: np.ndarray   # int8 +/-1, length d
     S: np.ndarray   # float32, d x d
+    rotation: str = "wht"             # "wht": y = H D u; "dense": y = M u, M in SO(d)
+    M: Optional[np.ndarray] = None    # the dense rotation (fp64), rotation == "dense"
 
     def codebook(self, bits: int) -> _cb.Codebook:
         return _cb.lloyd_max(self.d, bits)
@@ -99,16 +102,33 @@ class Params:
     def roles(self):
         return scheme_roles(self.scheme, self.n)
 
+    def rotate(self, u: np.ndarray) -> np.ndarray:
+        """Rows u -> rows y of the rotated roles."""
+        if self.rotation == "dense":
+            return u @ self.M.T
+        H = hadamard(self.d)
+        return (u * self.D.astype(np.float64)[None, :]) @ H.T
 
-def make_params(d: int, n: int, scheme: str, seed: int) -> Params:
+    def unrotate(self, y: np.ndarray) -> np.ndarray:
+        """Rows y -> rows of the original domain (the transpose of `rotate`)."""
+        if self.rotation == "dense":
+            return y @ self.M
+        H = hadamard(self.d)
+        return (y @ H.T) * self.D.astype(np.float64)[None, :]
+
+
+def make_params(d: int, n: int, scheme: str, seed: int, rotation: str = "wht") -> Params:
     if scheme not in SCHEMES:
         raise ValueError(scheme)
     if d & (d - 1) or d < 4:
         raise ValueError("d must be a power of two")
     if not 2 <= n <= 4:
         raise ValueError("budget n must be 2..4 (the sketched schemes need n-1 >= 1)")
+    if rotation not in ("wht", "dense"):
+        raise ValueError(rotation)
+    M = _rot.dense_rotation(seed, d) if rotation == "dense" else None
     return Params(d=d, n=n, scheme=scheme, seed=seed,
-                  D=_rng.rademacher_diagonal(seed, d), S=_rng.gaussian_sketch(seed, d))
+                  D=_rng.rademacher_diagonal(seed, d), S=_rng.gaussian_sketch(seed, d), rotation=rotation, M=M)
 
 
 @dataclass
@@ -135,8 +155,7 @@ def encode(x: np.ndarray, role: Role, params: Params) -> Encoded:
     u = np.zeros_like(x)
     u[~zero] = x[~zero] / nu[~zero, None]
     if role.rotate:
-        H = hadamard(d)
-        y = (u * params.D.astype(np.float64)[None, :]) @ H.T
+        y = params.rotate(u)
     else:
         y = u
     bounds = cb.bounds32.astype(np.float64)
@@ -168,8 +187,7 @@ def decode(enc: Encoded, params: Params) -> np.ndarray:
         m = params.S.shape[0]
         yhat = yhat + (SQRT_HALF_PI / m) * enc.rnorm.astype(np.float64)[:, None] * (sig @ params.S.astype(np.float64))
     if role.rotate:
-        H = hadamard(d)
-        yhat = (yhat @ H.T) * params.D.astype(np.float64)[None, :]
+        yhat = params.unrotate(yhat)
     return yhat
 
 
