@@ -8,13 +8,19 @@ decode attention of one query per head over the 8192 compressed tokens
 (query prep, decode, combine). `value` is the step's algorithmic bytes
 (packed records + norms + signs read, new records written, q, output) per
 second of device time; `append_quantize` reports the bulk append-quantise
-throughput of refilling the whole cache. Inputs are synthetic, drawn on the
-device from a seeded generator; the 587 MB cache is larger than the 129 MB L2.
+throughput of refilling the whole cache; `paged` the same step on a paged
+cache; `configs` (N = 1) the decode kernel, the decode call and the bulk
+append on every other workload (single head; the scheme x budget sweep; GQA
+over 131072 tokens; the four KIVI layouts); `cpu_baseline` the CPU oracle's
+decode and quantise on one thread and on one single-threaded process per
+core. Inputs are synthetic, drawn on the device from a seeded generator; the
+587 MB cache is larger than the 129 MB L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun each rank runs an independent replica (the path has no
-exchange step); rank 0 prints one JSON line.
+exchange step); rank 0 prints one JSON line. `--impl reference` times the CPU
+oracle as the reference arm on the host's cores.
 """
 
 import argparse

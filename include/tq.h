@@ -160,11 +160,18 @@ typedef enum {
 
 typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
 
+/* The rotation of the rotated roles (KQV and QKQV keys and values). */
+typedef enum {
+  TQ_ROTATION_WHT = 0,   /* y = H_d D u: the randomised Walsh-Hadamard transform (default) */
+  TQ_ROTATION_DENSE = 1  /* y = M u, M a seeded random rotation in SO(d) (see tq_set_rotation) */
+} tq_rotation;
+
 /* The planes of a block of the records array (TQ schemes), in storage order. */
 typedef enum {
   TQ_PLANE_K_CODES = 0, TQ_PLANE_K_NORM = 1, TQ_PLANE_K_SIGNS = 2, TQ_PLANE_K_RNORM = 3,
   TQ_PLANE_V_CODES = 4, TQ_PLANE_V_NORM = 5, TQ_PLANE_V_SIGNS = 6, TQ_PLANE_V_RNORM = 7,
-  TQ_NUM_PLANES = 8
+  TQ_PLANE_K_SIDE = 8, /* keys' rank-r side codes (tq_set_side_basis): r float16 per token */
+  TQ_NUM_PLANES = 9
 } tq_plane;
 
 /* Device pointers of one cache. Sizes come from tq_cache_sizes; a pointer
@@ -231,6 +238,53 @@ void tq_destroy(tq_ctx *ctx);
  * groups values along channels per token, 0 along tokens per channel. Call
  * before sizing or using a cache; TQ_ERR_STATE for other schemes. */
 tq_status tq_set_kivi(tq_ctx *ctx, int group, int window, int k_per_channel, int v_per_token);
+
+/* Choose the rotation of the rotated roles ([KVQuant++] "Rotation-invariance
+ * guarantee" and "Rate-distortion performance": a random QR rotation or a
+ * Hadamard transform, the rotation kept in SO(d), determinant +1).
+ * TQ_ROTATION_DENSE: G is the d x d Gaussian matrix of the method's counter
+ * generator in stream 3 (entry k = row * d + col; the Box-Muller recipe of S,
+ * kept in double), G = Q R with diag(R) > 0, the last column of Q negated when
+ * det Q = -1, and M = Q^T (rounded to float32); y = M u on the cache write and
+ * the query, x_hat = M^T y_hat on reconstruction and on the attention output.
+ * Call before any cache is written with the context (the codes of the two
+ * rotations differ). With the dense rotation the bulk append of bf16 vectors
+ * runs on the tensor-core kernel of fp32 inputs and the decode step runs its
+ * append and query preparation as separate kernels. TQ_ERR_STATE for KIVI, and
+ * after tq_set_side_basis (choose the rotation first). */
+tq_status tq_set_rotation(tq_ctx *ctx, int rotation);
+
+/* Host utility: the dense rotation M (d*d floats, row-major, y = M u) a context
+ * created with `seed` uses under TQ_ROTATION_DENSE. */
+tq_status tq_draw_rotation(uint64_t seed, int d, float *h_rotation);
+
+/* Rank-r key side codes ([HeadQ] section 3: a score-space correction in a basis
+ * learned from calibration queries; [KVQuant++] "Core innovation 4": a low-rank
+ * correction of the key quantisation residual). Each key j of KV head h stores,
+ * besides its base code, z_j = fp16(U_h^T (k_j - k_hat_j)) (plane TQ_PLANE_K_SIDE,
+ * rank float16 values), k_hat_j being the base reconstruction; decoding uses the
+ * corrected key k_hat_j + U_h z_j, i.e. adds q^T U_h z_j / sqrt(d) to each logit,
+ * and tq_dequantize returns the corrected keys.
+ *   rank    : 1..8, or 0 to switch side codes off
+ *   heads_kv: the KV heads every cache used with this context has
+ *   h_basis : float [heads_kv][d][rank] (host), head h's basis U_h with orthonormal
+ *             columns (TQ_ERR_ARG when U_h^T U_h is not the identity to 1e-3)
+ * Applies to the unsketched key roles (TQ_SCHEME_KV, TQ_SCHEME_KQV); TQ_ERR_STATE
+ * otherwise. Call before any cache is sized or written: the record layout gains
+ * the side plane. The context copies the bases to the device (heads_kv * d *
+ * rank floats, twice: as given and in the rotated coordinates) and frees them in
+ * tq_destroy. Appends and decodes of a context with side codes take the general
+ * tensor-core / warp append kernels and the split-K decode kernel. */
+tq_status tq_set_side_basis(tq_ctx *ctx, int rank, int heads_kv, const float *h_basis);
+
+/* Host utility for calibrating side-code bases: the `rank` leading principal
+ * directions (about the origin) of the n rows of h_x (float [n][d]): the
+ * eigenvectors of sum_j x_j x_j^T for its largest eigenvalues, in decreasing
+ * order, each signed so that its largest-magnitude component is positive,
+ * written to h_basis (float [d][rank]). Rows of calibration queries give HeadQ's
+ * basis; rows of key residuals k - k_hat (tq_dequantize) give the low-rank
+ * correction's basis (their top right singular vectors). */
+tq_status tq_principal_basis(const float *h_x, int n, int d, int rank, float *h_basis);
 
 /* Byte sizes of a cache of `capacity` token slots for [batch][heads_kv]
  * sequences-heads: TQ schemes the records array (whole 16-token blocks per

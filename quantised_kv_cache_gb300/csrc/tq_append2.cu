@@ -31,8 +31,13 @@ struct Append2Args {
   uint8_t *codes;
   float *norms;
   int *error;
+  // key side codes (side_rank > 0): plane base and bases [heads][d][rank] (natural order)
+  int side_rank;
+  uint16_t *side;
+  const float *side_ur;
   float diag[kD];
-  float bounds[kMaxLevels];  // 2^BITS - 1 used
+  float bounds[kMaxLevels];     // 2^BITS - 1 used
+  float centroids[kMaxLevels];  // 2^BITS used (side codes)
 };
 
 constexpr float kSqrtD = 11.313708498984761f;  // sqrt(128)
@@ -72,6 +77,7 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
     }
     const long long slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
     if (slot < 0) continue;
+    const int head = (int)(bh % a.heads);
 
     float x[kD];
     if (BF16) {
@@ -132,10 +138,22 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
 #pragma unroll
     for (int w = 0; w < 4 * BITS; ++w) word[w] = 0u;
 #pragma unroll
+    // side code of an unsketched key: z_k = nu sum_i U[i][k] (x_i / nu - c[code_i])
+    const int srank = a.side_rank;
+    const float *su = srank ? a.side_ur + (size_t)head * kD * srank : nullptr;
+    const float inv_nu = (nu > 0.f) ? 1.f / (ROT ? nu * kSqrtD : nu) : 0.f;
+    float zs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
     for (int i = 0; i < kD; ++i) {
       const float y = x[i];
       const int m = count_pos<H>(fabsf(y), P);
       const int code = (y >= 0.f) ? (L / 2 + m) : (L / 2 - 1 - m);
+      if (srank) {
+        const float r = fmaf(y, inv_nu, -a.centroids[code]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < srank) zs[k] = fmaf(__ldg(su + i * srank + k), r, zs[k]);
+      }
       // slot order: coordinate i = 8n + 2t + e at code offset 32t + 2n + e
       const int n = i >> 3, tt = (i >> 1) & 3, e = i & 1;
       const int off = BITS * (32 * tt + 2 * n + e);
@@ -172,6 +190,12 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
       for (int k = 0; k < BITS; ++k) dst[k] = make_uint4(word[4 * k], word[4 * k + 1], word[4 * k + 2], word[4 * k + 3]);
     }
     *rec_at(a.norms, slot, a.bb, 4) = nu;
+    if (srank) {
+      uint16_t *zp = rec_at(a.side, slot, a.bb, 2 * srank);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < srank) zp[k] = __half_as_ushort(__float2half_rn(zs[k] * nu));
+    }
   }
 }
 
@@ -224,8 +248,14 @@ int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.norms = a.norms;
   k.error = a.error;
   for (int i = 0; i < kD; ++i) k.diag[i] = (float)ctx->diag[i];
-  const float *src = (a.centroids == ctx->dparams->k_centroids) ? ctx->k_bounds : ctx->v_bounds;
+  const bool is_k = a.centroids == ctx->dparams->k_centroids;
+  const float *src = is_k ? ctx->k_bounds : ctx->v_bounds;
+  const float *csrc = is_k ? ctx->k_centroids : ctx->v_centroids;
   for (int i = 0; i < (1 << a.role.bits) - 1; ++i) k.bounds[i] = src[i];
+  for (int i = 0; i < (1 << a.role.bits); ++i) k.centroids[i] = csrc[i];
+  k.side_rank = a.side_rank;
+  k.side = a.side;
+  k.side_ur = a.side_ur;
   const long long total = (long long)a.batch * a.heads * a.n_new;
   cudaStream_t st = (cudaStream_t)stream;
   const bool bf16 = a.dtype == TQ_BF16;

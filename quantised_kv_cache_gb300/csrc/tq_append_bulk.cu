@@ -18,9 +18,9 @@
 //   n); for sketched vectors, once the residuals are in tensor memory, it
 //   issues z = S r in three fp16 passes (hi x hi, lo x hi, hi x lo) into the
 //   columns y used;
-// * two groups of four epilogue warps take alternate tiles (one thread per
-//   vector = tensor-memory lane), so one group computes while the other's MMAs
-//   run: ||y|| = sqrt(d) ||x|| gives the norm and the boundary scale, codes are
+// * two (sketched roles) or three groups of four epilogue warps take the tiles
+//   in turn (one thread per vector = tensor-memory lane), so groups compute
+//   while the others' MMAs run: ||y|| = sqrt(d) ||x|| gives the norm and the boundary scale, codes are
 //   counted against the boundaries times ||y|| (no division), the residual
 //   r = y / ||y|| - c[code], scaled by 2^10 and split into fp16 hi + lo, is
 //   stored to tensor memory as the sketch MMA's A operand, and signs come out
@@ -41,20 +41,30 @@ namespace {
 constexpr int kTV = 128;                      // vectors per tile = MMA M
 constexpr int kTileBytes = kTV * kD * 2;      // one bf16 tile (32 KB)
 constexpr int kOpB = kD * kD * 2;             // one 16-bit 128 x 128 operand
-constexpr int kEpiWarps = 8;                  // two groups of four
-constexpr int kBulkThreads = 32 * (1 + kEpiWarps);
 constexpr float kRScaleB = 1024.f;            // residual scale for the fp16 split (|r| < 2)
+
+// Epilogue groups of four warps (one tensor-memory slot each): sketched roles need 256
+// columns a slot (y / z, residual hi, residual lo), so two fit in the 512 columns; the
+// others need 128, so three groups share the SM -- three warps per scheduler to hide the
+// tensor-memory and shared-memory latencies of the code search.
+template <bool QJL>
+constexpr int bulk_groups() { return QJL ? 2 : 3; }
+template <bool QJL>
+constexpr int bulk_threads() { return 32 * (1 + 4 * bulk_groups<QJL>()); }
 
 template <bool QJL>
 struct BulkGeo {
+  static constexpr int NG = bulk_groups<QJL>();
   static constexpr int NS = QJL ? 3 : 4;                      // x stages
   static constexpr int x0 = 0;
   static constexpr int hd = NS * kTileBytes;                  // H D, bf16
   static constexpr int sk = hd + kOpB;                        // S hi, S lo (fp16)
-  static constexpr int bar = sk + (QJL ? 2 * kOpB : 0);       // barriers
-  static constexpr int nbar = 2 * NS + 10;
+  static constexpr int ent = QJL ? 16 : 8;                    // bytes of one cell-table entry
+  static constexpr int ct = sk + (QJL ? 2 * kOpB : 0);        // cell table, [kCells][32 lanes] entries
+  static constexpr int bar = ct + kCells * 32 * ent;          // barriers
+  static constexpr int nbar = 2 * NS + 4 * NG + 2;
   static constexpr int total = bar + nbar * 8 + 16;
-  static constexpr uint32_t tcols = QJL ? 512u : 256u;        // two slots
+  static constexpr uint32_t tcols = 512u;                     // NG slots (a power of two >= NG slots)
   static constexpr uint32_t slot_cols = QJL ? 256u : 128u;    // Y / Z | R hi | R lo
 };
 
@@ -73,8 +83,7 @@ struct BulkArgs {
   const uint16_t *s_hl;    // DevParams::sketch_hl
   float sketch_rowmax;
   int *error;
-  float bounds[kMaxLevels];
-  float centroids[kMaxLevels];
+  CellTable cells;  // the role's code-search table
 };
 
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
@@ -119,42 +128,6 @@ __device__ __forceinline__ void tmem_st_wait(uint32_t (&a)[16], uint32_t (&b)[16
                  "+r"(b[14]), "+r"(b[15])
                :
                : "memory");
-}
-
-// Code of one coordinate y (0 .. 2^BITS - 1): with P the positive boundaries
-// times ||y|| (P[k] = b[L/2 + k] ||y||), the magnitude index counts the P[k] <=
-// |y| by binary search, then code = (L/2 + magnitude) for y >= 0 and its
-// mirror L - 1 - that for y < 0 (one XOR). For the residual, cneg gets
-// -c[code] 2^10 from C[q] = c[L/2 + q] 2^10 (the codebook is symmetric).
-template <int BITS, bool QJL>
-__device__ __forceinline__ uint32_t encode1(float y, const float (&P)[(1 << (BITS - 1)) > 1 ? (1 << (BITS - 1)) - 1 : 1],
-                                            const float (&C)[1 << (BITS - 1)], float &cneg) {
-  constexpr uint32_t L = 1u << BITS;
-  const float a = fabsf(y);
-  const uint32_t s = (uint32_t)(__float_as_int(y + 0.f) >> 31);  // all ones when y < 0 (y + 0 maps -0 to +0)
-  uint32_t m;
-  float cm = 0.f;
-  if constexpr (BITS == 1) {
-    m = 1u;
-    cm = C[0];
-  } else if constexpr (BITS == 2) {
-    const bool p1 = a >= P[0];
-    m = p1 ? 3u : 2u;
-    if (QJL) cm = p1 ? C[1] : C[0];
-  } else if constexpr (BITS == 3) {
-    const bool p2 = a >= P[1];
-    const bool p1 = a >= (p2 ? P[2] : P[0]);
-    m = (p2 ? 6u : 4u) + (p1 ? 1u : 0u);
-    if (QJL) cm = p2 ? (p1 ? C[3] : C[2]) : (p1 ? C[1] : C[0]);
-  } else {
-    const bool p4 = a >= P[3];
-    const bool p2 = a >= (p4 ? P[5] : P[1]);
-    const bool p1 = a >= (p4 ? (p2 ? P[6] : P[4]) : (p2 ? P[2] : P[0]));
-    m = (p4 ? 12u : 8u) + (p2 ? 2u : 0u) + (p1 ? 1u : 0u);
-    if (QJL) cm = C[(p4 ? 4 : 0) + (p2 ? 2 : 0) + (p1 ? 1 : 0)];
-  }
-  if (QJL) cneg = __int_as_float(__float_as_int(cm) ^ (int)(~s & 0x80000000u));
-  return m ^ (s & (L - 1u));
 }
 
 // tcgen05.ld without its wait, and the wait, which names the loaded registers so
@@ -251,7 +224,7 @@ __device__ __forceinline__ void certify_rounds(uint32_t r_hi, const float *sperm
 }
 
 template <int BITS, bool QJL, bool VT>
-__global__ void __launch_bounds__(kBulkThreads, 1)
+__global__ void __launch_bounds__(bulk_threads<QJL>(), 1)
     append_bulk_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ BulkArgs a) {
   using G = BulkGeo<QJL>;
   constexpr int NS = G::NS;
@@ -259,8 +232,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + G::bar);
   uint64_t *x_full = bars, *x_empty = bars + NS;
-  uint64_t *y_full = bars + 2 * NS, *r_full = y_full + 2, *z_full = r_full + 2, *s_empty = z_full + 2;
-  uint64_t *op_bar = s_empty + 2, *drain = op_bar + 1;
+  constexpr int NG = G::NG;
+  uint64_t *y_full = bars + 2 * NS, *r_full = y_full + NG, *z_full = r_full + NG, *s_empty = z_full + NG;
+  uint64_t *op_bar = s_empty + NG, *drain = op_bar + 1;
   uint32_t *s_taddr = reinterpret_cast<uint32_t *>(bars + G::nbar);
   volatile int *s_abort = reinterpret_cast<volatile int *>(s_taddr + 1);
 
@@ -274,7 +248,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       mbar_init(&x_full[s], 1);
       mbar_init(&x_empty[s], 1);
     }
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < NG; ++g) {
       mbar_init(&y_full[g], 1);
       mbar_init(&r_full[g], 4);
       mbar_init(&z_full[g], 1);
@@ -289,6 +263,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     if (QJL) {
       tma_load_1d(smem + G::sk, a.s_hl, kOpB, op_bar);
       tma_load_1d(smem + G::sk + kOpB, a.s_hl + kD * kD, kOpB, op_bar);
+    }
+  }
+  {  // the role's cell table, replicated per lane ([cell][lane]): a warp's lookups of one
+     // coordinate hit 32 consecutive entries, whatever the cells
+    unsigned char *tab = smem + G::ct;
+    for (int i = tid; i < kCells * 32; i += bulk_threads<QJL>()) {
+      const CellEntry &e = a.cells.e[i >> 5];
+      if constexpr (QJL)
+        *reinterpret_cast<float4 *>(tab + i * 16) = make_float4(__int_as_float(e.below), e.thr, e.c_lo, e.c_hi);
+      else
+        *reinterpret_cast<float2 *>(tab + i * 8) = make_float2(__int_as_float(e.below), e.thr);
     }
   }
   if (warp == 0) {
@@ -320,8 +305,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       constexpr uint32_t id_sk = tc_idesc_f16_f32(128, 128);     // fp16 x fp16 -> f32
       const uint32_t sa_x = smem_u32(smem + G::x0), sa_h = smem_u32(smem + G::hd), sa_s = smem_u32(smem + G::sk);
       auto sketch = [&](long long k) -> bool {
-        const int g = (int)(k & 1);
-        if (!mbar_wait_bounded(&r_full[g], (uint32_t)((k >> 1) & 1), a.error)) return false;
+        const int g = (int)(k % NG);
+        if (!mbar_wait_bounded(&r_full[g], (uint32_t)((k / NG) & 1), a.error)) return false;
         tc_fence_after_sync();
         const uint32_t d = tbase + G::slot_cols * g;
 #pragma unroll 1
@@ -337,8 +322,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       };
       long long k = 0;
       for (; ok && k < nloc && !*s_abort; ++k) {
-        const int g = (int)(k & 1), s = (int)(k % NS);
-        if (k >= 2 && !mbar_wait_bounded(&s_empty[g], (uint32_t)(((k >> 1) - 1) & 1), a.error)) ok = false;
+        const int g = (int)(k % NG), s = (int)(k % NS);
+        if (k >= NG && !mbar_wait_bounded(&s_empty[g], (uint32_t)(((k / NG) - 1) & 1), a.error)) ok = false;
         if (ok && !mbar_wait_bounded(&x_full[s], (uint32_t)((k / NS) & 1), a.error)) ok = false;
         if (!ok) break;
         tc_fence_after_sync();
@@ -368,24 +353,29 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       for (long long j = k; j < loaded; ++j) mbar_wait_bounded(&x_full[j % NS], (uint32_t)((j / NS) & 1), a.error);
     }
   } else {
-    // ---------------- epilogue: group g (four warps, one thread per vector) takes local tiles k = g (mod 2)
+    // ---------------- epilogue: group g (four warps, one thread per vector) takes local tiles k = g (mod NG)
     const int g = (warp - 1) >> 2, qd = warp & 3;
     const int row = 32 * qd + lane;  // vector within the tile = TMEM lane
     const uint32_t tslot = tbase + G::slot_cols * g + ((uint32_t)(32 * qd) << 16);
-    float P[H > 0 ? H : 1], CP[H + 1];
-#pragma unroll
-    for (int q = 0; q <= H; ++q) CP[q] = a.centroids[L / 2 + q] * kRScaleB;
+    const unsigned char *tab = smem + G::ct + lane * G::ent;  // this lane's copy of the cell table
     const float smax = a.sketch_rowmax;
-    for (long long k = g; k < nloc; k += 2) {
-      const int par = (int)((k >> 1) & 1);
+    // sequence lengths are loaded a tile ahead: the L2 round trip of the current tile's length
+    // would otherwise stall the warp at the top of every tile
+    auto len_of = [&](long long kk) -> int {
+      const long long v = (blockIdx.x + kk * gridDim.x) * kTV + row;
+      return v < a.total ? __ldg(a.seq_lens + (int)((v / a.n_new) / a.heads)) : 0;
+    };
+    int len_next = (g < nloc) ? len_of(g) : 0;
+    for (long long k = g; k < nloc; k += NG) {
+      const int par = (int)((k / NG) & 1);
       const long long tile = blockIdx.x + k * gridDim.x;
       const long long vec = tile * kTV + row;
+      const int len = len_next;
+      if (k + NG < nloc) len_next = len_of(k + NG);
       long long slot = -1;
       if (vec < a.total) {
         const int t = (int)(vec % a.n_new);
         const long long bh = vec / a.n_new;
-        const int b = (int)(bh / a.heads);
-        const int len = __ldg(a.seq_lens + b);
         if (len >= 0 && len + a.n_new <= a.capacity) slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
         else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
       }
@@ -422,8 +412,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       }
       const float sv = ss > 0.f ? sqrtf(ss) : 1.f;  // sqrt(d) ||x||, the boundary scale
       const float inv = ss > 0.f ? kRScaleB / sv : 0.f;
-#pragma unroll
-      for (int j = 0; j < H; ++j) P[j] = a.bounds[L / 2 + j] * sv;
+      const float A = a.cells.inv2u / sv;  // t = sat(y A + 1/2) places y on the cell grid
       // pass 2: codes and residuals of chunk c (32 storage offsets)
       float rr = 0.f;
       uint32_t *crec = reinterpret_cast<uint32_t *>(rec_at(a.codes, slot >= 0 ? slot : 0, a.bb, BITS * kD / 8));
@@ -436,8 +425,25 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         for (int w = 0; w < NW; ++w) word[w] = 0u;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          float cneg;
-          const uint32_t code = encode1<BITS, QJL>(__uint_as_float(yz[j]), P, CP, cneg);
+          // the code: the cell of y (one fused multiply-add, saturated; the cell index lands
+          // in the low mantissa bits of t 63 stride + 1.5 2^23, already times the entry
+          // stride), then the one boundary the cell may hold
+          const float yv = __uint_as_float(yz[j]);
+          const float t = __saturatef(fmaf(yv, A, 0.5f));
+          constexpr float kMul = 63.f * (QJL ? 512.f : 256.f);
+          constexpr uint32_t kMask = QJL ? 0x7E00u : 0x3F00u;
+          const uint32_t key = __float_as_uint(fmaf(t, kMul, 12582912.f)) & kMask;
+          uint32_t code;
+          float cneg = 0.f;
+          if constexpr (QJL) {
+            const float4 e = *reinterpret_cast<const float4 *>(tab + key);
+            const bool up = yv >= e.y * sv;
+            code = (uint32_t)__float_as_int(e.x) + (up ? 1u : 0u);
+            cneg = -(up ? e.w : e.z);
+          } else {
+            const float2 e = *reinterpret_cast<const float2 *>(tab + key);
+            code = (uint32_t)__float_as_int(e.x) + (yv >= e.y * sv ? 1u : 0u);
+          }
           const int off = VT ? 2 * BITS * (16 * (j & 1) + (j >> 1)) : BITS * j;
           word[off >> 5] |= code << (off & 31);
           if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= code >> (32 - (off & 31));
@@ -594,7 +600,7 @@ int go_bulk(const CUtensorMap &map, const BulkArgs &k, long long ntiles, cudaStr
   }
   long long blocks = ntiles < g_sms_bulk ? ntiles : g_sms_bulk;
   if (blocks < 1) blocks = 1;
-  fn<<<(unsigned)blocks, kBulkThreads, G::total, st>>>(map, k);
+  fn<<<(unsigned)blocks, bulk_threads<QJL>(), G::total, st>>>(map, k);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -604,6 +610,10 @@ int go_bulk(const CUtensorMap &map, const BulkArgs &k, long long ntiles, cudaStr
 int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   if (!a.role.rotate || a.dtype != TQ_BF16 || a.role.bits < 1 || a.role.bits > 4 || (a.role.qjl && a.role.bits > 3))
     return TQ_ERR_UNSUPPORTED;
+  // the rotation operand here is the exact +-1 Walsh-Hadamard one; a dense rotation takes the
+  // fp16 hi / lo passes of the tensor-core kernel for fp32 inputs
+  if (ctx->rotation != TQ_ROTATION_WHT) return TQ_ERR_UNSUPPORTED;
+  if (a.side_rank) return TQ_ERR_UNSUPPORTED;  // keys with side codes: the tensor-core kernel below
   const long long total = (long long)a.batch * a.heads * a.n_new;
   if (total < 2LL * kTV || total > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_fn();
@@ -640,10 +650,8 @@ int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.sketch_rowmax = ctx->sketch_rowmax;
   k.error = a.error;
   const bool is_k = a.centroids == ctx->dparams->k_centroids;
-  const float *bsrc = is_k ? ctx->k_bounds : ctx->v_bounds;
-  const float *csrc = is_k ? ctx->k_centroids : ctx->v_centroids;
-  for (int i = 0; i < (1 << a.role.bits) - 1; ++i) k.bounds[i] = bsrc[i];
-  for (int i = 0; i < (1 << a.role.bits); ++i) k.centroids[i] = csrc[i];
+  k.cells = ctx->cells[is_k ? 0 : 1];
+  if (k.cells.stride != (a.role.qjl ? 512 : 256)) return TQ_ERR_UNSUPPORTED;
   const long long ntiles = (total + kTV - 1) / kTV;
   cudaStream_t st = (cudaStream_t)stream;
   if (a.role.qjl && a.vt) {

@@ -47,6 +47,10 @@ struct SmallArgs {
   int pool_blocks;
   const int32_t *seq_lens;
   const float *diag;       // D as +/-1.0f
+  const float *rot_t;      // dense rotation M^T, or nullptr (Walsh-Hadamard)
+  uint16_t *k_side;        // key side codes (side_rank > 0): plane base, bases [heads][d][rank]
+  const float *side_ur;
+  int side_rank;
   const float *sketch_tp;  // entry (i, 4L + m) = S[8(L/2) + 2m + (L&1)][i]
   int *error;
 };
@@ -94,7 +98,11 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
     float x[4];
     load4(ro.x, (size_t)vec * kD + 4 * lane, BF16, x);
     float r[4];
-    encode_vector_warp(ro, x, slot, a.bb, a.diag, lane, nu, r, rr);
+    const bool side = a.side_rank > 0 && blockIdx.y == 0;  // keys with side codes
+    encode_vector_warp(ro, x, slot, a.bb, a.diag, lane, nu, r, rr, a.rot_t, side);
+    if (side)
+      side_code_warp(a.side_ur + (size_t)(bh % a.heads) * kD * a.side_rank, a.side_rank, nu, r, a.k_side, slot,
+                     a.bb, lane);
     if (qjl) reinterpret_cast<float4 *>(s_r + warp * kRS)[lane] = make_float4(r[0], r[1], r[2], r[3]);
   } else if (qjl) {
     reinterpret_cast<float4 *>(s_r + warp * kRS)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -205,6 +213,10 @@ int launch_append_small(const AppendArgs &k, const AppendArgs &v, const tq_ctx *
   s.pool_blocks = k.pool_blocks;
   s.seq_lens = k.seq_lens;
   s.diag = ctx->dparams->diag;
+  s.rot_t = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot_t : nullptr;
+  s.k_side = k.side;
+  s.side_ur = k.side_ur;
+  s.side_rank = k.side_rank;
   s.sketch_tp = ctx->dparams->sketch_tp;
   s.error = k.error;
   const long long total = (long long)k.batch * k.heads * k.n_new;

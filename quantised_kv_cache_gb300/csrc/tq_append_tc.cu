@@ -53,10 +53,15 @@ struct TcArgs {
   uint8_t *signs;
   float *rnorms;
   const float *sketch;          // S, fp32 [128][128] row-major (rare-path exact signs)
-  const uint16_t *bh;           // B operand of the rotation (DevParams::hadamard_b)
+  const uint16_t *bh;           // B operand of the rotation (DevParams::hadamard_b, or the dense hi part)
+  const uint16_t *bm_lo;        // dense rotation: the lo part of sqrt(d) M (nullptr: Walsh-Hadamard)
   const uint16_t *bs;           // B operand of the sketch, hi then lo (DevParams::sketch_hl)
   float sketch_rowmax;
   int *error;
+  // key side codes (side_rank > 0): plane base and the bases in code-storage order
+  int side_rank;
+  uint16_t *side;
+  const float *side_urs;
   float bounds[kMaxLevels];     // 2^BITS - 1 used
   float centroids[kMaxLevels];  // 2^BITS used
 };
@@ -156,19 +161,23 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
   unsigned char *s_bh = smem;                 // rotation B operand
   unsigned char *s_bs = smem + kOpBytes;      // sketch B operand, hi then lo (QJL)
   constexpr int kOps = QJL ? 3 : 1;
-  uint64_t *s_bar = reinterpret_cast<uint64_t *>(smem + kOps * kOpBytes);
-  uint32_t *s_taddr = reinterpret_cast<uint32_t *>(smem + kOps * kOpBytes + 8);
+  const bool dense = a.bm_lo != nullptr;      // dense rotation: a lo part follows the others
+  unsigned char *s_bl = smem + kOps * kOpBytes;
+  const int nops = kOps + (dense ? 1 : 0);
+  uint64_t *s_bar = reinterpret_cast<uint64_t *>(smem + nops * kOpBytes);
+  uint32_t *s_taddr = reinterpret_cast<uint32_t *>(smem + nops * kOpBytes + 8);
   const int tid = threadIdx.x, warp = tid >> 5;
 
   if (tid == 0) {
     mbar_init(s_bar, 1);
     mbar_fence_init();
-    mbar_arrive_expect_tx(s_bar, kOps * kOpBytes);
+    mbar_arrive_expect_tx(s_bar, nops * kOpBytes);
     tma_load_1d(s_bh, a.bh, kOpBytes, s_bar);
     if (QJL) {
       tma_load_1d(s_bs, a.bs, kOpBytes, s_bar);
       tma_load_1d(s_bs + kOpBytes, a.bs + kD * kD, kOpBytes, s_bar);
     }
+    if (dense) tma_load_1d(s_bl, a.bm_lo, kOpBytes, s_bar);
   }
   __syncwarp();
   if (warp == 0) {
@@ -182,7 +191,7 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
   tc_fence_after_sync();
   const uint32_t tbase = *s_taddr;
   const uint32_t tlane = tbase + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
-  const uint32_t sa_h = smem_u32(s_bh), sa_s = smem_u32(s_bs);
+  const uint32_t sa_h = smem_u32(s_bh), sa_s = smem_u32(s_bs), sa_l = smem_u32(s_bl);
   constexpr uint32_t idesc = tc_idesc_f16_f32(128, 128);
   const float smax = a.sketch_rowmax;
   float P[H > 0 ? H : 1], CP[H + 1];
@@ -197,9 +206,11 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
     // ---------------- 1. load, norm, A = D x 2^-e as fp16 hi + lo
     const long long vec = base + tid;
     long long slot = -1;
+    int head = 0;
     if (vec < total) {
       const int t = (int)(vec % a.n_new);
       const long long bh = vec / a.n_new;
+      head = (int)(bh % a.heads);
       const int b = (int)(bh / a.heads);
       const int len = __ldg(a.seq_lens + b);
       if (len >= 0 && len + a.n_new <= a.capacity) slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
@@ -259,7 +270,8 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
     tc_fence_before_sync();
     __syncthreads();
 
-    // ---------------- 2. y' = H x' (columns in code-storage order)
+    // ---------------- 2. y' = H x' (columns in code-storage order); a dense rotation
+    // sqrt(d) M = B_hi + B_lo adds the pass x'_hi B_lo (x'_lo B_lo, about 2^-44, is dropped)
     if (tid == 0) {
       tc_fence_after_sync();
 #pragma unroll
@@ -267,6 +279,7 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
         const uint64_t db = tc_sdesc_kmajor(sa_h + 256 * ks, 128, 2048);
         tc_mma_f16_ts(tbase, tbase + 128 + 8 * ks, db, idesc, ks > 0);
         tc_mma_f16_ts(tbase, tbase + 192 + 8 * ks, db, idesc, true);
+        if (dense) tc_mma_f16_ts(tbase, tbase + 128 + 8 * ks, tc_sdesc_kmajor(sa_l + 256 * ks, 128, 2048), idesc, true);
       }
       tc_commit(smem_u32(s_bar));
     }
@@ -290,6 +303,12 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
                             (uint32_t)__shfl_xor_sync(kFull, (int)(uint32_t)slot, 1);
     const bool paired = slot >= 0 && pslot >= 0 && pslot == (slot ^ 1);
     const int half = (int)(slot & 1);
+    // side code of an unsketched key: z_k = nu sum_n U[n][k] (y_n / ||y|| - c[code_n]) over
+    // the storage offsets n (the basis stored in the same order)
+    const int srank = QJL ? 0 : a.side_rank;
+    const float *su = srank ? a.side_urs + (size_t)head * kD * srank : nullptr;
+    const float inv_unit = (nu > 0.f) ? 1.f / (nu * kSqrtD * xs) : 0.f;
+    float zs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       uint32_t yz[32];
@@ -320,6 +339,15 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
           const float r = fmaf(y, inv, (y >= 0.f) ? -cm * kRScale : cm * kRScale);
           rr = fmaf(r, r, rr);
           yz[j] = __float_as_uint(r);
+        } else if (srank) {
+          float cm = CP[0];
+#pragma unroll
+          for (int k = 1; k <= H; ++k) cm = (m == k) ? CP[k] : cm;
+          const float r = fmaf(y, inv_unit, (y >= 0.f) ? -cm : cm);
+          const float *un = su + (32 * q + j) * srank;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (k < srank) zs[k] = fmaf(__ldg(un + k), r, zs[k]);
         }
       }
       if (a.vt) {  // warp-uniform
@@ -342,6 +370,12 @@ __global__ void __launch_bounds__(kQV, 2) append_tc_kernel(const __grid_constant
       }
     }
     if (slot >= 0) *rec_at(a.norms, slot, a.bb, 4) = nu;
+    if (srank && slot >= 0) {
+      uint16_t *zp = rec_at(a.side, slot, a.bb, 2 * srank);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < srank) zp[k] = __half_as_ushort(__float2half_rn(zs[k] * nu));
+    }
 
     if constexpr (QJL) {
       tc_fence_before_sync();
@@ -440,6 +474,21 @@ __global__ void __launch_bounds__(128) operand_prep_kernel(DevParams *dp) {
   }
 }
 
+// The dense rotation's B operands, once per context: sqrt(d) M (rows in storage order)
+// split into fp16 hi + lo, K-major core matrices as for H D above.
+__global__ void __launch_bounds__(128) rotation_prep_kernel(DevParams *dp) {
+  const int n = threadIdx.x;
+  unsigned char *hi = reinterpret_cast<unsigned char *>(dp->rot_hl);
+  unsigned char *lo = hi + kOpBytes;
+  const int i = slot_coord_tc(n);
+  for (int k = 0; k < kD; ++k) {
+    const float v = dp->rot[i * kD + k] * kSqrtD;
+    const __half h = __float2half_rn(v);
+    *reinterpret_cast<__half *>(hi + core_off(n, k)) = h;
+    *reinterpret_cast<__half *>(lo + core_off(n, k)) = __float2half_rn(v - __half2float(h));
+  }
+}
+
 int g_sms_tc = 0;
 
 template <int BITS, bool QJL, bool BF16>
@@ -450,12 +499,14 @@ int go(const TcArgs &k, long long total, cudaStream_t st) {
     cudaDeviceGetAttribute(&g_sms_tc, cudaDevAttrMultiProcessorCount, dev);
     if (g_sms_tc <= 0) g_sms_tc = 152;
   }
-  // shared memory sized so that at most two CTAs share an SM (their TMEM totals 512 columns)
-  constexpr int smem = QJL ? 3 * kOpBytes + 64 : 80 * 1024;
+  // shared memory sized so that at most two CTAs share an SM (their TMEM totals 512 columns);
+  // a dense rotation's extra operand leaves sketched roles at one CTA per SM
+  constexpr int smem_max = QJL ? 4 * kOpBytes + 64 : 80 * 1024;
+  const int smem = QJL ? (k.bm_lo ? 4 : 3) * kOpBytes + 64 : 80 * 1024;
   auto fn = append_tc_kernel<BITS, QJL, BF16>;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
       return TQ_ERR_CUDA;
     attr_done = true;
   }
@@ -479,6 +530,11 @@ int dispatch(int bits, const TcArgs &k, long long total, cudaStream_t st) {
 }
 
 }  // namespace
+
+int launch_rotation_prep(DevParams *dp, void *stream) {
+  rotation_prep_kernel<<<1, kD, 0, (cudaStream_t)stream>>>(dp);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
 
 int launch_operand_prep(DevParams *dp, void *stream) {
   operand_prep_kernel<<<1, kD, 0, (cudaStream_t)stream>>>(dp);
@@ -506,10 +562,15 @@ int launch_append_tc(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.signs = a.signs;
   k.rnorms = a.rnorms;
   k.sketch = ctx->dparams->sketch;
-  k.bh = ctx->dparams->hadamard_b;
+  const bool dense = ctx->rotation == TQ_ROTATION_DENSE;
+  k.bh = dense ? ctx->dparams->rot_hl : ctx->dparams->hadamard_b;
+  k.bm_lo = dense ? ctx->dparams->rot_hl + kD * kD : nullptr;
   k.bs = ctx->dparams->sketch_hl;
   k.sketch_rowmax = ctx->sketch_rowmax;
   k.error = a.error;
+  k.side_rank = a.side_rank;
+  k.side = a.side;
+  k.side_urs = a.side_urs;
   const bool is_k = a.centroids == ctx->dparams->k_centroids;
   const float *bsrc = is_k ? ctx->k_bounds : ctx->v_bounds;
   const float *csrc = is_k ? ctx->k_centroids : ctx->v_centroids;

@@ -41,6 +41,11 @@ struct PrepArgs {
   const int32_t *seq_lens;
   int capacity;
   int32_t *tile_prefix;
+  const float *rot_t = nullptr;  // dense rotation M^T (q_rot = M q), or nullptr (Walsh-Hadamard)
+  // key side codes: w = U_rot^T q_rot / sqrt(d) for the row's KV head (rows / heads_q / G),
+  // written to the second half of the row's record (unsketched keys leave it free)
+  const float *side_ur = nullptr;
+  int side_rank = 0, group = 1;
 };
 
 // Exclusive prefix over batches of ceil(clamped length / kDecodeTile), by one
@@ -83,7 +88,9 @@ __global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
   const bool live = row < a.batch * a.heads_q;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (live) load4(a.q, (size_t)row * kD + 4 * lane, a.bf16 != 0, v);
-  if (a.rotate) {
+  if (a.rotate && a.rot_t) {
+    matvec_t_warp(a.rot_t, v, lane);
+  } else if (a.rotate) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] *= __ldg(a.diag + 4 * lane + j);
     wht128(v, lane);
@@ -91,6 +98,17 @@ __global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
   if (live) {
     float4 o = make_float4(v[0] * kInvSqrtD, v[1] * kInvSqrtD, v[2] * kInvSqrtD, v[3] * kInvSqrtD);
     reinterpret_cast<float4 *>(a.qprep + (size_t)row * 2 * kD)[lane] = o;
+  }
+  if (a.side_rank && live) {  // warp-uniform
+    const int hk = (row % a.heads_q) / a.group;
+    const float *U = a.side_ur + (size_t)hk * kD * a.side_rank;
+    for (int k = 0; k < a.side_rank; ++k) {
+      float p = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p = fmaf(__ldg(U + (4 * lane + j) * a.side_rank + k), v[j], p);
+      p = warp_sum(p);
+      if (lane == 0) a.qprep[(size_t)row * 2 * kD + kD + k] = p * kInvSqrtD;
+    }
   }
   if (!a.sketch_k) return;
 #pragma unroll
@@ -129,6 +147,8 @@ struct DecodeKernelArgs {
   float *partials;
   const float *k_centroids;
   const float *v_centroids;
+  const uint16_t *k_side;  // key side codes (side_rank > 0): plane base
+  int side_rank;
 };
 
 // lane -> token (0..7) after the 8-way reduce-scatter below, and back
@@ -180,10 +200,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
   const int t_begin = split * a.chunk;
   const int t_end = min(t_begin + a.chunk, len);
 
-  float qv[G][4], sq[G][4];
+  float qv[G][4], sq[G][4], wz[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const float *qp = a.qprep + ((size_t)b * a.heads_q + hk * G + g) * 2 * kD;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) wz[g][k] = (k < a.side_rank) ? __ldg(qp + kD + k) : 0.f;
     const float4 q4 = __ldg(reinterpret_cast<const float4 *>(qp) + lane);
     qv[g][0] = q4.x; qv[g][1] = q4.y; qv[g][2] = q4.z; qv[g][3] = q4.w;
     if (KQJL) {
@@ -236,11 +258,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_tq_kernel(DecodeKern
         for (int j = 0; j < 4; ++j) sg[j] = sb[j] ? 1.f : -1.f;
         rk = recf(a.k_rnorm, sl);
       }
+      // side code (lane 0 adds the key's correction w . z_hat once to the lanes' partial sums)
+      float zt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (a.side_rank && lane == 0) {
+        const uint16_t *zp = rec_at(a.k_side, sl, a.bb, 2 * a.side_rank);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < a.side_rank) zt[k] = __half2float(__ushort_as_half(zp[k]));
+      }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float s = qv[g][0] * c[0] + qv[g][1] * c[1] + qv[g][2] * c[2] + qv[g][3] * c[3];
         s *= nu;
         if (KQJL) s += rk * (sq[g][0] * sg[0] + sq[g][1] * sg[1] + sq[g][2] * sg[2] + sq[g][3] * sg[3]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s = fmaf(wz[g][k], zt[k], s);
         part[g][jj] = s;
       }
     }
@@ -352,6 +384,7 @@ struct CombineArgs {
   int persist_ctas, heads_kv, persist_groups;
   int group = 1;  // query heads per KV head (persistent records hold `group` heads per slot)
   int *error = nullptr;
+  const float *rot = nullptr;  // dense rotation M (o = M^T o_rot), or nullptr (Walsh-Hadamard)
 };
 
 // Merge the partial records of one query row: thread i (of 128) gets coordinate i
@@ -467,7 +500,9 @@ __global__ void __launch_bounds__(kCombineRows * 128) combine_tq_kernel(CombineA
     float v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] = s_o[rr * kD + 4 * lane + j];
-    if (a.rotate) {
+    if (a.rotate && a.rot) {
+      matvec_t_warp(a.rot, v, lane);
+    } else if (a.rotate) {
       wht128(v, lane);
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] *= __ldg(a.diag + 4 * lane + j);
@@ -855,6 +890,10 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   PrepArgs p{a.q, a.q_dtype == TQ_BF16, a.batch, a.heads_q, ctx->k.rotate, ctx->k.qjl,
              ctx->dparams->diag, ctx->dparams->sketch, a.qprep,
              a.seq_lens, a.cache->capacity, persist_ok ? a.tile_prefix : nullptr};
+  p.rot_t = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot_t : nullptr;
+  p.side_ur = ctx->side_ur;
+  p.side_rank = ctx->side_rank;
+  p.group = G;
   const int rows = a.batch * a.heads_q;
   if (launch_overlapped(true, qprep_kernel, dim3((rows + 3) / 4), dim3(128), 0, st, p) != cudaSuccess)
     return TQ_ERR_CUDA;
@@ -864,7 +903,8 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   int persist_ctas = 0;
   DecodeArgs a2 = a;
   if (!persist_ok) a2.tile_prefix = nullptr;
-  int r2 = launch_decode2_g1(a2, &persist_ctas, stream);
+  // keys with side codes: the scalar kernel below adds their logit correction
+  int r2 = ctx->side_rank ? TQ_ERR_UNSUPPORTED : launch_decode2_g1(a2, &persist_ctas, stream);
   if (r2 == TQ_OK) {
     if (ctx->prof_decode_stop) cudaEventRecord((cudaEvent_t)ctx->prof_decode_stop, st);
     CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
@@ -872,6 +912,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
                     persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv, G == 1 ? 1 : kPersistGroups};
     cmb.group = G;
     cmb.error = &ctx->dparams->error;
+    cmb.rot = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot : nullptr;
     return launch_combine(cmb, st);
   }
   if (r2 != TQ_ERR_UNSUPPORTED) return r2;
@@ -889,6 +930,8 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   k.btab = c->block_table;
   k.pool_blocks = c->pool_blocks;
   k.error = &ctx->dparams->error;
+  k.side_rank = ctx->side_rank;
+  k.k_side = ctx->side_rank ? reinterpret_cast<const uint16_t *>(c->records + L.off[TQ_PLANE_K_SIDE]) : nullptr;
   k.capacity = c->capacity;
   k.heads_kv = a.heads_kv;
   k.heads_q = a.heads_q;
@@ -928,6 +971,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                   ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv, 1};
   cmb.error = &ctx->dparams->error;
+  cmb.rot = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot : nullptr;
   return launch_combine(cmb, st);
 }
 
@@ -948,6 +992,7 @@ int launch_decode_step_tq(const DecodeArgs &a, const StepArgs &s, void *stream) 
                   ctx->dparams->diag, ctx->dparams->sketch, a.out, a.tile_prefix, persist_ctas, a.heads_kv, 1};
   cmb.group = 1;
   cmb.error = &ctx->dparams->error;
+  cmb.rot = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot : nullptr;
   return launch_combine(cmb, st);
 }
 

@@ -361,13 +361,15 @@ __device__ __forceinline__ void tile_body(const unsigned char *st, const unsigne
   if (!KQJL) sc *= kn[tok];
   sc = valid ? sc : -INFINITY;
 
-  // ---- online softmax over the warp's 16 tokens (base 2)
-  float tmax = sc;
+  // ---- online softmax over the warp's 16 tokens (base 2). The running maximum moves only
+  // when some token beats it: one vote finds out, and only then does the warp reduce its
+  // maximum and rescale (warp-uniform; m = -inf scales zeros). Otherwise the tile's
+  // maximum would leave the running one unchanged, so the weights are the same.
+  if (__any_sync(kFull, sc > ws.m)) {
+    float tmax = sc;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
-  const float m_new = fmaxf(ws.m, tmax);
-  const float p = valid ? ex2_approx(sc - m_new) : 0.f;
-  if (m_new != ws.m) {  // warp-uniform: the running max moved (m = -inf scales zeros)
+    for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+    const float m_new = fmaxf(ws.m, tmax);
     const float scale = ex2_approx(ws.m - m_new);
     ws.l *= scale;
     ws.w *= scale;
@@ -377,6 +379,7 @@ __device__ __forceinline__ void tile_body(const unsigned char *st, const unsigne
       for (int j = 0; j < 4; ++j) ws.acc[mb][j] *= scale;
     ws.m = m_new;
   }
+  const float p = valid ? ex2_approx(sc - ws.m) : 0.f;
   ws.l += p;  // every token sits on two lanes: halved at the flush
 
   // ---- B operands: this lane's token weight (p nu on even lanes, p rho on odd ones)
@@ -523,6 +526,17 @@ template <int BLOCK>
 __device__ __forceinline__ const uint8_t *block_src(const Decode2Args &a, long long vslot) {
   const long long p = phys_slot(a.btab, a.pool_blocks, vslot, a.error);
   return p < 0 ? nullptr : a.records + (p >> 4) * BLOCK;
+}
+
+// The stored block a prefetched table entry `pb` names (paged caches), or nullptr when it is
+// outside the pool (recorded as TQ_ERR_ARG, as block_src does).
+template <int BLOCK>
+__device__ __forceinline__ const uint8_t *pool_block(const Decode2Args &a, int pb) {
+  if (pb < 0 || pb >= a.pool_blocks) {
+    set_error(a.error, TQ_ERR_ARG);
+    return nullptr;
+  }
+  return a.records + (long long)pb * BLOCK;
 }
 
 // Copy the blocks holding tokens s0 .. s0 + n - 1 (s0 a multiple of 16) into a stage: one
@@ -851,6 +865,14 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     cur_t = r - cur_h * cur_nb;
     cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
   }
+  // paged caches: lane 0 loads the table entry of the cursor's block as soon as the cursor
+  // moves, a tile before its copy is issued, so the copy never waits on the lookup
+  int pf = -1;
+  auto prefetch = [&]() {
+    if (a.btab != nullptr && lane == 0 && cur_i < nloc && cur_t * kTT + 16 * qtr < cur_len)
+      pf = __ldg(a.btab + ((cur_row + cur_t * kTT + 16 * qtr) >> 4));
+  };
+  prefetch();
   // issue this warp's quarter of local tile cur_i (whole warp), then step the cursor by 4 tiles
   auto issue_next = [&]() {
     const int st = cur_i % S;
@@ -858,13 +880,16 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     const int t0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - t0);
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
-      const uint8_t *src = n > 0 ? block_src<Gm::block>(a, cur_row + t0) : nullptr;
+      const uint8_t *src = n <= 0 ? nullptr
+                           : a.btab ? pool_block<Gm::block>(a, pf)
+                                    : a.records + ((cur_row + t0) >> 4) * Gm::block;
       mbar_arrive_expect_tx(bar, src ? (uint32_t)Gm::block : 0u);
       if (src) tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, src, (uint32_t)Gm::block, bar);
     }
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
     if (cur_i < nloc) seek();
+    prefetch();
   };
   // query row (= unit: one query head per KV head) of the segment starting at tile g
   auto unit_of = [&](int g) -> int {
@@ -1054,24 +1079,27 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
   float s0 = v0 ? (sk[0] + sk[1]) * kn[tok0] : -INFINITY;
   float s1 = v1 ? (sk[2] + sk[3]) * kn[tok1] : -INFINITY;
   // ---- online softmax of head t4 over the warp's 16 tokens (the 8 lanes g share t4)
-  float tmax = fmaxf(s0, s1);
+  // (the heads' maxima are reduced only when some token beats its head's running maximum)
+  if (__any_sync(kFull, fmaxf(s0, s1) > m_run)) {
+    float tmax = fmaxf(s0, s1);
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
-  const float m_new = fmaxf(m_run, tmax);
-  const float p0 = v0 ? ex2_approx(s0 - m_new) : 0.f, p1 = v1 ? ex2_approx(s1 - m_new) : 0.f;
-  if (m_new != m_run) {  // per head (lane-divergent; no shuffles inside)
-    const float scale = ex2_approx(m_run - m_new);
-    l_run *= scale;
-    w_run *= scale;
+    for (int o = 4; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+    const float m_new = fmaxf(m_run, tmax);
+    if (m_new != m_run) {  // per head (lane-divergent; no shuffles inside)
+      const float scale = ex2_approx(m_run - m_new);
+      l_run *= scale;
+      w_run *= scale;
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb)
+      for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc_v[mb][j] *= scale;
-        if (VQJL) acc_s[mb][j] *= scale;
-      }
-    m_run = m_new;
+        for (int j = 0; j < 4; ++j) {
+          acc_v[mb][j] *= scale;
+          if (VQJL) acc_s[mb][j] *= scale;
+        }
+      m_run = m_new;
+    }
   }
+  const float p0 = v0 ? ex2_approx(s0 - m_run) : 0.f, p1 = v1 ? ex2_approx(s1 - m_run) : 0.f;
   l_run += p0 + p1;
   // ---- B operands: column 2h + part of lane (g, t) = hi / lo of head h's weights of tokens
   // 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1); token j of head h sits on lane 4 (j % 8) + h
@@ -1232,19 +1260,28 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
     cur_t = r - cur_h * cur_nb;
     cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
   }
+  int pf = -1;  // paged caches: the cursor block's table entry, loaded a tile ahead (see above)
+  auto prefetch = [&]() {
+    if (a.btab != nullptr && lane == 0 && cur_i < nloc && cur_t * kTT + 16 * qtr < cur_len)
+      pf = __ldg(a.btab + ((cur_row + cur_t * kTT + 16 * qtr) >> 4));
+  };
+  prefetch();
   auto issue_next = [&]() {
     const int stn = cur_i % S;
     uint64_t *bar = &s_full[stn * 4 + qtr];
     const int tt0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - tt0);
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
-      const uint8_t *src = n > 0 ? block_src<Q::block>(a, cur_row + tt0) : nullptr;
+      const uint8_t *src = n <= 0 ? nullptr
+                           : a.btab ? pool_block<Q::block>(a, pf)
+                                    : a.records + ((cur_row + tt0) >> 4) * Q::block;
       mbar_arrive_expect_tx(bar, src ? (uint32_t)Q::block : 0u);
       if (src) tma_load_1d(s_stage + stn * Q::stage + qtr * Q::block, src, (uint32_t)Q::block, bar);
     }
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
     if (cur_i < nloc) seek();
+    prefetch();
   };
   for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
 
@@ -1474,6 +1511,9 @@ int launch_decode2_step(const DecodeArgs &a, const StepArgs &s, int *persist_cta
   if (a.heads_q != a.heads_kv || a.batch > kMaxPersistBatch || ctx->num_sms <= 0 || !a.tile_prefix)
     return TQ_ERR_UNSUPPORTED;
   if (ctx->scheme != TQ_SCHEME_KV && ctx->scheme != TQ_SCHEME_KQV) return TQ_ERR_UNSUPPORTED;
+  // the fused kernel rotates queries and new tokens with the Walsh-Hadamard transform
+  if (ctx->scheme == TQ_SCHEME_KQV && ctx->rotation != TQ_ROTATION_WHT) return TQ_ERR_UNSUPPORTED;
+  if (ctx->side_rank) return TQ_ERR_UNSUPPORTED;  // key side codes: the general path
   Decode2Args k = decode2_args(a);
   k.tile_prefix = nullptr;
   k.tile_prefix_out = a.tile_prefix;

@@ -25,6 +25,11 @@ struct DequantKernelArgs {
   const float *diag;
   const float *sketch;
   float *out;
+  const float *rot;  // dense rotation M (x = M^T y), or nullptr (Walsh-Hadamard)
+  // key side codes (side_rank > 0): x_hat += U z_hat, U [heads][d][rank] as given
+  const uint16_t *side;
+  const float *side_u;
+  int side_rank;
 };
 
 template <int BITS, bool ROT, bool QJL>
@@ -71,10 +76,21 @@ __global__ void __launch_bounds__(256) dequant_tq_kernel(DequantKernelArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) y[j] = fmaf(rho, r[j], y[j]);
   }
-  if (ROT) {
+  if (ROT && a.rot) {
+    matvec_t_warp(a.rot, y, lane);
+  } else if (ROT) {
     wht128(y, lane);
 #pragma unroll
     for (int j = 0; j < 4; ++j) y[j] *= __ldg(a.diag + 4 * lane + j);
+  }
+  if (a.side_rank) {
+    const uint16_t *zp = rec_at(a.side, slot, a.bb, 2 * a.side_rank);
+    const float *U = a.side_u + (size_t)(bh % a.heads) * kD * a.side_rank;
+    for (int k = 0; k < a.side_rank; ++k) {
+      const float z = __half2float(__ushort_as_half(zp[k]));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) y[j] = fmaf(__ldg(U + (4 * lane + j) * a.side_rank + k), z, y[j]);
+    }
   }
   reinterpret_cast<float4 *>(a.out + (size_t)vec * kD)[lane] = make_float4(y[0], y[1], y[2], y[3]);
 }
@@ -96,7 +112,7 @@ int go(int bits, const DequantKernelArgs &k, unsigned blocks, cudaStream_t st) {
 int launch_dequant_tq(const DequantArgs &a, void *stream) {
   DequantKernelArgs k{a.codes, a.norms, a.signs, a.rnorms, a.bb, a.cap16, a.btab, a.pool_blocks, a.error, a.vt,
                       a.batch, a.heads, a.capacity, a.t0, a.t1, a.centroids, a.params->diag, a.params->sketch,
-                      a.out};
+                      a.out, a.rot, a.side, a.side_u, a.side_rank};
   const long long total = (long long)a.batch * a.heads * (a.t1 - a.t0);
   const unsigned blocks = (unsigned)((total + 7) / 8);
   cudaStream_t st = (cudaStream_t)stream;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -26,6 +27,47 @@ __device__ __forceinline__ long long phys_slot(const int32_t *bt, int pool_block
     return -1;
   }
   return ((long long)pb << 4) | (vslot & 15);
+}
+
+// v <- A^T v for a d x d row-major matrix A (d = 128) held by one warp, lane L owning
+// coordinates 4L..4L+3: lane L sums A[k][4L..4L+3] v_k over k, each v_k reaching it by a
+// shuffle and each row of A read as one coalesced 512-byte line. With A = M^T this is
+// the dense rotation y = M v; with A = M its inverse x = M^T y.
+__device__ __forceinline__ void matvec_t_warp(const float *A, float (&v)[4], int lane) {
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int k4 = 0; k4 < 32; ++k4) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float vk = __shfl_sync(0xffffffffu, v[j], k4);
+      const float4 a = __ldg(reinterpret_cast<const float4 *>(A + (4 * k4 + j) * 128) + lane);
+      y[0] = fmaf(a.x, vk, y[0]);
+      y[1] = fmaf(a.y, vk, y[1]);
+      y[2] = fmaf(a.z, vk, y[2]);
+      y[3] = fmaf(a.w, vk, y[3]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = y[j];
+}
+
+// Side code of one key held by a warp (lane L: unit-domain residual r[4L..4L+3] in the
+// coordinates the codes live in): z_k = fp16(nu sum_i U[i][k] r_i) for k < rank, with U the
+// key head's basis in those coordinates ([d][rank], natural order); lane k < rank stores z_k
+// at token `slot` of the side plane (nothing when slot < 0).
+__device__ __forceinline__ void side_code_warp(const float *U, int rank, float nu, const float (&r)[4],
+                                               uint16_t *side_plane, long long slot, int bb, int lane) {
+  float mine = 0.f;
+  for (int k = 0; k < rank; ++k) {
+    float p = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p = fmaf(__ldg(U + (4 * lane + j) * rank + k), r[j], p);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+    if (lane == k) mine = p * nu;
+  }
+  if (slot >= 0 && lane < rank)
+    rec_at(side_plane, slot, bb, 2 * rank)[lane] = __half_as_ushort(__float2half_rn(mine));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -236,8 +278,10 @@ __device__ __forceinline__ void vt_store_chunk(uint32_t *row, int chunk, const u
   for (int i = 0; i < 2 * VB; ++i) merged[i] = w[i] | __shfl_xor_sync(kFull, w[i], 1);
   if (!valid) return;
   if (paired) {
+    // (a select rather than merged[VB * half + i]: an index known only at run time would
+    // put the array in local memory)
 #pragma unroll
-    for (int i = 0; i < VB; ++i) dst[VB * half + i] = merged[VB * half + i];
+    for (int i = 0; i < VB; ++i) dst[VB * half + i] = half ? merged[VB + i] : merged[i];
   } else {
     // this token's bits of every field of the chunk: VB ones at 2*VB*o + VB*half
     uint32_t own[2 * VB];
@@ -300,18 +344,23 @@ __device__ __forceinline__ void warp_store_codes_vt(uint8_t *vplane, long long s
 // without a sketch, the norm) of token `slot` (nothing when slot < 0). For sketched
 // roles returns the unit-domain residual r = y - c[code] (zero for a zero vector) and
 // sum r^2 over the warp.
+// rot_t: the dense rotation's M^T (row-major) for contexts set to TQ_ROTATION_DENSE, else
+// nullptr (the randomised Walsh-Hadamard transform with diagonal `diag`). want_res: return
+// the residual of an unsketched role too (for its side code).
 template <typename R>
 __device__ __forceinline__ void encode_vector_warp(const R &ro, const float (&x)[4], long long slot, int bb,
                                                    const float *diag, int lane, float &nu, float (&r)[4],
-                                                   float &rr) {
+                                                   float &rr, const float *rot_t = nullptr, bool want_res = false) {
   nu = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
   float y[4];
+  const bool wht = ro.rotate && rot_t == nullptr;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float dg = ro.rotate ? __ldg(diag + 4 * lane + j) : 1.f;
+    const float dg = wht ? __ldg(diag + 4 * lane + j) : 1.f;
     y[j] = (nu > 0.f) ? (x[j] / nu) * dg : 0.f;
   }
-  if (ro.rotate) wht128(y, lane);
+  if (wht) wht128(y, lane);
+  else if (ro.rotate) matvec_t_warp(rot_t, y, lane);
   int idx[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -339,7 +388,7 @@ __device__ __forceinline__ void encode_vector_warp(const R &ro, const float (&x)
   rr = 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) r[j] = 0.f;
-  if (ro.qjl) {
+  if (ro.qjl || want_res) {
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {

@@ -61,6 +61,99 @@ void make_sketch(uint64_t seed, int d, float *out) {
   }
 }
 
+// The dense rotation's Gaussian matrix: the same Box-Muller recipe on stream 3, kept in double.
+void make_rotation_gaussian(uint64_t seed, int d, double *out) {
+  const double scale = std::ldexp(1.0, -53);
+  const double two_pi = 2.0 * M_PI;
+  for (int k = 0; k < d * d; ++k) {
+    uint64_t w1 = draw(seed, 3, 2 * (uint64_t)k);
+    uint64_t w2 = draw(seed, 3, 2 * (uint64_t)k + 1);
+    double u1 = (double)((w1 >> 11) + 1) * scale;
+    double u2 = (double)(w2 >> 11) * scale;
+    out[k] = std::sqrt(-2.0 * std::log(u1)) * std::cos(two_pi * u2);
+  }
+}
+
+// Blocked record layout of a TQ-scheme context: planes in tq_plane order, each 16 tokens of
+// its per-token bytes (the side plane only with side codes on).
+void build_layout(tq_ctx *c) {
+  const int d = c->d;
+  const int tok[TQ_NUM_PLANES] = {(int)(c->k.bits * d / 8), 4, c->k.qjl ? d / 8 : 0, c->k.qjl ? 4 : 0,
+                                  (int)(c->v.bits * d / 8), 4, c->v.qjl ? d / 8 : 0, c->v.qjl ? 4 : 0,
+                                  2 * c->side_rank};
+  int off = 0;
+  for (int p = 0; p < TQ_NUM_PLANES; ++p) {
+    c->lay.off[p] = off;
+    c->lay.tok[p] = tok[p];
+    off += tq::kBlockTokens * tok[p];
+  }
+  c->lay.bb = off;
+}
+
+// Eigen-decomposition of a symmetric d x d matrix A (row-major, destroyed) by cyclic Jacobi
+// rotations: eigenvalues to w, eigenvectors to the columns of V (row-major).
+void jacobi_eigen(std::vector<double> &A, int d, std::vector<double> &w, std::vector<double> &V) {
+  V.assign((size_t)d * d, 0.0);
+  for (int i = 0; i < d; ++i) V[(size_t)i * d + i] = 1.0;
+  for (int sweep = 0; sweep < 100; ++sweep) {
+    double off = 0.0, tot = 0.0;
+    for (int i = 0; i < d; ++i)
+      for (int j = 0; j < d; ++j) {
+        const double a = A[(size_t)i * d + j] * A[(size_t)i * d + j];
+        tot += a;
+        if (i != j) off += a;
+      }
+    if (off <= 1e-30 * tot) break;
+    for (int p = 0; p < d - 1; ++p)
+      for (int q = p + 1; q < d; ++q) {
+        const double apq = A[(size_t)p * d + q];
+        if (apq == 0.0) continue;
+        const double app = A[(size_t)p * d + p], aqq = A[(size_t)q * d + q];
+        const double theta = (aqq - app) / (2.0 * apq);
+        const double t = (theta >= 0.0 ? 1.0 : -1.0) / (std::fabs(theta) + std::sqrt(theta * theta + 1.0));
+        const double c = 1.0 / std::sqrt(t * t + 1.0), s = t * c;
+        for (int k = 0; k < d; ++k) {  // columns p, q
+          const double akp = A[(size_t)k * d + p], akq = A[(size_t)k * d + q];
+          A[(size_t)k * d + p] = c * akp - s * akq;
+          A[(size_t)k * d + q] = s * akp + c * akq;
+        }
+        for (int k = 0; k < d; ++k) {  // rows p, q
+          const double apk = A[(size_t)p * d + k], aqk = A[(size_t)q * d + k];
+          A[(size_t)p * d + k] = c * apk - s * aqk;
+          A[(size_t)q * d + k] = s * apk + c * aqk;
+        }
+        for (int k = 0; k < d; ++k) {
+          const double vkp = V[(size_t)k * d + p], vkq = V[(size_t)k * d + q];
+          V[(size_t)k * d + p] = c * vkp - s * vkq;
+          V[(size_t)k * d + q] = s * vkp + c * vkq;
+        }
+      }
+  }
+  w.resize(d);
+  for (int i = 0; i < d; ++i) w[i] = A[(size_t)i * d + i];
+}
+
+// Sign of det(A) (A d x d, row-major, copied) by Gaussian elimination with partial pivoting.
+int det_sign(std::vector<double> A, int d) {
+  int sign = 1;
+  for (int c = 0; c < d; ++c) {
+    int p = c;
+    for (int r = c + 1; r < d; ++r)
+      if (std::fabs(A[r * d + c]) > std::fabs(A[p * d + c])) p = r;
+    if (A[p * d + c] == 0.0) return 0;
+    if (p != c) {
+      for (int k = 0; k < d; ++k) std::swap(A[p * d + k], A[c * d + k]);
+      sign = -sign;
+    }
+    if (A[c * d + c] < 0.0) sign = -sign;
+    for (int r = c + 1; r < d; ++r) {
+      const double f = A[r * d + c] / A[c * d + c];
+      for (int k = c; k < d; ++k) A[r * d + k] -= f * A[c * d + k];
+    }
+  }
+  return sign;
+}
+
 // ---------------------------------------------------------------- codebook
 
 struct GaussLegendre {
@@ -218,6 +311,74 @@ void choose_splits(int batch, int heads_kv, int max_len, int requested, int *spl
   *chunk = c;
 }
 
+bool draw_dense_rotation(uint64_t seed, int d, double *M) {
+  // G = Q R with a positive diagonal: Q's columns are G's columns orthonormalised in order
+  // (modified Gram-Schmidt, each column taken through the projections twice); a reflection
+  // (det Q = sign det G = -1) becomes a rotation by negating the last column; M = Q^T
+  std::vector<double> G((size_t)d * d), Q((size_t)d * d);
+  make_rotation_gaussian(seed, d, G.data());
+  for (int j = 0; j < d; ++j) {
+    std::vector<double> v(d);
+    for (int i = 0; i < d; ++i) v[i] = G[(size_t)i * d + j];
+    for (int pass = 0; pass < 2; ++pass)
+      for (int c = 0; c < j; ++c) {
+        double dot = 0.0;
+        for (int i = 0; i < d; ++i) dot += Q[(size_t)i * d + c] * v[i];
+        for (int i = 0; i < d; ++i) v[i] -= dot * Q[(size_t)i * d + c];
+      }
+    double nn = 0.0;
+    for (int i = 0; i < d; ++i) nn += v[i] * v[i];
+    nn = std::sqrt(nn);
+    if (!(nn > 0.0)) return false;
+    for (int i = 0; i < d; ++i) Q[(size_t)i * d + j] = v[i] / nn;
+  }
+  const int s = det_sign(G, d);
+  if (s == 0) return false;
+  if (s < 0)
+    for (int i = 0; i < d; ++i) Q[(size_t)i * d + d - 1] = -Q[(size_t)i * d + d - 1];
+  for (int i = 0; i < d; ++i)
+    for (int k = 0; k < d; ++k) M[(size_t)i * d + k] = Q[(size_t)k * d + i];
+  return true;
+}
+
+bool build_cell_table(const float *bounds, const float *centroids, int bits, int stride, CellTable *out) {
+  const int nb = (1 << bits) - 1;
+  double bmax = 0.0;
+  for (int j = 0; j < nb; ++j) bmax = std::max(bmax, std::fabs((double)bounds[j]));
+  const double eps = 0.5 / stride;  // cell k: t * 63 in [k - eps, k + 1 - eps)
+  const double u0 = std::max(bmax * 1.05, 0.05);
+  for (int step = 0; step < 2000; ++step) {
+    const double U = u0 * std::pow(1.0005, step);
+    const float inv2u = (float)(1.0 / (2.0 * U));
+    int cell[16];
+    bool ok = true;
+    for (int j = 0; j < nb && ok; ++j) {
+      const double t = (double)bounds[j] * (double)inv2u + 0.5;
+      const double s = t * (kCells - 1) + eps;
+      const double fl = std::floor(s);
+      cell[j] = (int)fl;
+      ok = t > 0.0 && t < 1.0 && std::min(s - fl, fl + 1.0 - s) >= kCellMargin && (j == 0 || cell[j] > cell[j - 1]);
+    }
+    if (!ok) continue;
+    out->inv2u = inv2u;
+    out->stride = stride;
+    for (int k = 0; k < kCells; ++k) {
+      int below = 0, inside = -1;
+      for (int j = 0; j < nb; ++j) {
+        if (cell[j] < k) ++below;
+        if (cell[j] == k) inside = j;
+      }
+      CellEntry &e = out->e[k];
+      e.below = below;
+      e.thr = inside >= 0 ? bounds[inside] : __builtin_huge_valf();
+      e.c_lo = centroids[below] * 1024.f;
+      e.c_hi = centroids[inside >= 0 ? below + 1 : below] * 1024.f;
+    }
+    return true;
+  }
+  return false;
+}
+
 }  // namespace tq
 
 extern "C" {
@@ -278,6 +439,15 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
     for (size_t i = 0; i < cv.c.size(); ++i) c->v_centroids[i] = (float)cv.c[i];
     for (size_t i = 0; i < cv.b.size(); ++i) c->v_bounds[i] = (float)cv.b[i];
   }
+  if (is_tq_scheme(scheme)) {
+    // the bulk append's code search: 16-byte entries for sketched roles (they also need the
+    // code's centroid), 8-byte ones otherwise
+    if (!tq::build_cell_table(c->k_bounds, c->k_centroids, c->k.bits, c->k.qjl ? 512 : 256, &c->cells[0]) ||
+        !tq::build_cell_table(c->v_bounds, c->v_centroids, c->v.bits, c->v.qjl ? 512 : 256, &c->cells[1])) {
+      delete c;
+      return TQ_ERR_UNSUPPORTED;
+    }
+  }
   make_diag(seed, d, c->diag);
   c->sketch = (float *)std::malloc(sizeof(float) * d * d);
   if (!c->sketch) {
@@ -294,17 +464,7 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
     }
     c->sketch_rowmax = (float)(m * (1.0 + 1e-6));
   }
-  if (scheme != TQ_SCHEME_KIVI) {  // blocked record layout: planes in tq_plane order
-    const int tok[TQ_NUM_PLANES] = {(int)code_bytes(c->k.bits, d), 4, c->k.qjl ? d / 8 : 0, c->k.qjl ? 4 : 0,
-                                    (int)code_bytes(c->v.bits, d), 4, c->v.qjl ? d / 8 : 0, c->v.qjl ? 4 : 0};
-    int off = 0;
-    for (int p = 0; p < TQ_NUM_PLANES; ++p) {
-      c->lay.off[p] = off;
-      c->lay.tok[p] = tok[p];
-      off += tq::kBlockTokens * tok[p];
-    }
-    c->lay.bb = off;
-  }
+  if (scheme != TQ_SCHEME_KIVI) build_layout(c);
 
   tq::DevParams *hp = (tq::DevParams *)std::calloc(1, sizeof(tq::DevParams));
   if (!hp) {
@@ -346,12 +506,151 @@ tq_status tq_init(int d, int bits, int scheme, uint64_t seed, tq_ctx **out) {
 
 void tq_destroy(tq_ctx *ctx) {
   if (!ctx) return;
+  if (ctx->side_u) cudaFree(ctx->side_u);
+  if (ctx->side_ur) cudaFree(ctx->side_ur);
+  if (ctx->side_urs) cudaFree(ctx->side_urs);
   if (ctx->ev_join) cudaEventDestroy((cudaEvent_t)ctx->ev_join);
   if (ctx->ev_fork) cudaEventDestroy((cudaEvent_t)ctx->ev_fork);
   if (ctx->side_stream) cudaStreamDestroy((cudaStream_t)ctx->side_stream);
   if (ctx->dparams) cudaFree(ctx->dparams);
   std::free(ctx->sketch);
   delete ctx;
+}
+
+tq_status tq_draw_rotation(uint64_t seed, int d, float *h_rotation) {
+  if (!h_rotation || d < 4 || d > 1024 || (d & (d - 1))) return TQ_ERR_ARG;
+  std::vector<double> M((size_t)d * d);
+  if (!tq::draw_dense_rotation(seed, d, M.data())) return TQ_ERR_ARG;
+  for (size_t i = 0; i < M.size(); ++i) h_rotation[i] = (float)M[i];
+  return TQ_OK;
+}
+
+tq_status tq_set_rotation(tq_ctx *ctx, int rotation) {
+  if (!ctx) return TQ_ERR_ARG;
+  if (ctx->scheme == TQ_SCHEME_KIVI) return TQ_ERR_STATE;
+  if (rotation != TQ_ROTATION_WHT && rotation != TQ_ROTATION_DENSE) return TQ_ERR_ARG;
+  if (ctx->side_rank) return TQ_ERR_STATE;  // side-code bases are set in the rotated coordinates
+  if (rotation == TQ_ROTATION_DENSE && ctx->rotation != TQ_ROTATION_DENSE) {
+    const int d = ctx->d;
+    std::vector<float> M((size_t)d * d), MT((size_t)d * d);
+    if (tq_draw_rotation(ctx->seed, d, M.data()) != TQ_OK) return TQ_ERR_ARG;
+    for (int i = 0; i < d; ++i)
+      for (int k = 0; k < d; ++k) MT[(size_t)k * d + i] = M[(size_t)i * d + k];
+    cudaError_t e = cudaMemcpy(ctx->dparams->rot, M.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(ctx->dparams->rot_t, MT.data(), sizeof(float) * d * d, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && tq::launch_rotation_prep(ctx->dparams, nullptr) != TQ_OK) e = cudaErrorUnknown;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
+    if (e != cudaSuccess) return TQ_ERR_CUDA;
+  }
+  ctx->rotation = rotation;
+  return TQ_OK;
+}
+
+tq_status tq_principal_basis(const float *h_x, int n, int d, int rank, float *h_basis) {
+  if (!h_x || !h_basis || n <= 0 || d <= 0 || d > 1024 || rank <= 0 || rank > d) return TQ_ERR_ARG;
+  std::vector<double> C((size_t)d * d, 0.0), w, V;
+  for (int j = 0; j < n; ++j) {
+    const float *x = h_x + (size_t)j * d;
+    for (int a = 0; a < d; ++a)
+      for (int b = a; b < d; ++b) C[(size_t)a * d + b] += (double)x[a] * x[b];
+  }
+  for (int a = 0; a < d; ++a)
+    for (int b = 0; b < a; ++b) C[(size_t)a * d + b] = C[(size_t)b * d + a];
+  jacobi_eigen(C, d, w, V);
+  std::vector<int> order(d);
+  for (int i = 0; i < d; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return w[x] > w[y]; });
+  for (int r = 0; r < rank; ++r) {
+    const int col = order[r];
+    int imax = 0;
+    for (int i = 1; i < d; ++i)
+      if (std::fabs(V[(size_t)i * d + col]) > std::fabs(V[(size_t)imax * d + col])) imax = i;
+    const double sgn = V[(size_t)imax * d + col] < 0.0 ? -1.0 : 1.0;
+    for (int i = 0; i < d; ++i) h_basis[(size_t)i * rank + r] = (float)(sgn * V[(size_t)i * d + col]);
+  }
+  return TQ_OK;
+}
+
+tq_status tq_set_side_basis(tq_ctx *ctx, int rank, int heads_kv, const float *h_basis) {
+  if (!ctx) return TQ_ERR_ARG;
+  if (ctx->scheme == TQ_SCHEME_KIVI || ctx->k.qjl) return TQ_ERR_STATE;
+  if (rank < 0 || rank > 8) return TQ_ERR_ARG;
+  const int d = ctx->d;
+  if (ctx->side_u) cudaFree(ctx->side_u);
+  if (ctx->side_ur) cudaFree(ctx->side_ur);
+  if (ctx->side_urs) cudaFree(ctx->side_urs);
+  ctx->side_u = ctx->side_ur = ctx->side_urs = nullptr;
+  ctx->side_rank = 0;
+  ctx->side_heads = 0;
+  if (rank == 0) {
+    build_layout(ctx);
+    return TQ_OK;
+  }
+  if (heads_kv <= 0 || !h_basis) return TQ_ERR_ARG;
+  // orthonormal columns per head
+  for (int h = 0; h < heads_kv; ++h) {
+    const float *U = h_basis + (size_t)h * d * rank;
+    for (int a = 0; a < rank; ++a)
+      for (int b = 0; b < rank; ++b) {
+        double s = 0.0;
+        for (int i = 0; i < d; ++i) s += (double)U[(size_t)i * rank + a] * U[(size_t)i * rank + b];
+        if (std::fabs(s - (a == b ? 1.0 : 0.0)) > 1e-3) return TQ_ERR_ARG;
+      }
+  }
+  // the bases in the rotated coordinates the codes live in: U_rot = H D U (orthonormal H),
+  // M U (dense rotation) or U (unrotated keys); and in code-storage order
+  const size_t n = (size_t)heads_kv * d * rank;
+  std::vector<float> ur(n), urs(n);
+  std::vector<float> M;
+  if (ctx->k.rotate && ctx->rotation == TQ_ROTATION_DENSE) {
+    M.resize((size_t)d * d);
+    if (tq_draw_rotation(ctx->seed, d, M.data()) != TQ_OK) return TQ_ERR_ARG;
+  }
+  const double inv_sqrt_d = 1.0 / std::sqrt((double)d);
+  for (int h = 0; h < heads_kv; ++h) {
+    const float *U = h_basis + (size_t)h * d * rank;
+    float *R = ur.data() + (size_t)h * d * rank;
+    for (int k = 0; k < rank; ++k)
+      for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        if (!ctx->k.rotate) {
+          acc = U[(size_t)i * rank + k];
+        } else if (!M.empty()) {
+          for (int j = 0; j < d; ++j) acc += (double)M[(size_t)i * d + j] * U[(size_t)j * rank + k];
+        } else {
+          for (int j = 0; j < d; ++j)
+            acc += ((__builtin_popcount(i & j) & 1) ? -1.0 : 1.0) * ctx->diag[j] * U[(size_t)j * rank + k];
+          acc *= inv_sqrt_d;
+        }
+        R[(size_t)i * rank + k] = (float)acc;
+      }
+    // code-storage order: offset o = 32 t + 2 m + e holds coordinate 8 m + 2 t + e
+    float *S = urs.data() + (size_t)h * d * rank;
+    for (int o = 0; o < d; ++o) {
+      const int t = o >> 5, m = (o >> 1) & 15, e = o & 1;
+      const int i = 8 * m + 2 * t + e;
+      for (int k = 0; k < rank; ++k) S[(size_t)o * rank + k] = R[(size_t)i * rank + k];
+    }
+  }
+  cudaError_t e = cudaMalloc((void **)&ctx->side_u, n * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->side_ur, n * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->side_urs, n * sizeof(float));
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->side_u, h_basis, n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->side_ur, ur.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->side_urs, urs.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    if (ctx->side_u) cudaFree(ctx->side_u);
+    if (ctx->side_ur) cudaFree(ctx->side_ur);
+    if (ctx->side_urs) cudaFree(ctx->side_urs);
+    ctx->side_u = ctx->side_ur = ctx->side_urs = nullptr;
+    build_layout(ctx);
+    return TQ_ERR_CUDA;
+  }
+  ctx->side_rank = rank;
+  ctx->side_heads = heads_kv;
+  build_layout(ctx);
+  return TQ_OK;
 }
 
 tq_status tq_set_kivi(tq_ctx *ctx, int group, int window, int k_per_channel, int v_per_token) {
@@ -430,6 +729,7 @@ static tq_status check_cache(const tq_ctx *ctx, const tq_cache *c, int batch, in
   }
   if (!c->records) return TQ_ERR_ARG;
   if (c->block_table && c->pool_blocks <= 0) return TQ_ERR_ARG;
+  if (ctx->side_rank && heads_kv != ctx->side_heads) return TQ_ERR_ARG;  // one basis per KV head
   return TQ_OK;
 }
 
@@ -482,12 +782,18 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
   a.pool_blocks = cache->pool_blocks;
   set_role_planes(ctx, cache, 0, a.codes, a.norms, a.signs, a.rnorms);
   a.vt = 0;
+  a.side_rank = ctx->side_rank;
+  a.side = ctx->side_rank ? reinterpret_cast<uint16_t *>(cache->records + ctx->lay.off[TQ_PLANE_K_SIDE]) : nullptr;
+  a.side_ur = ctx->side_ur;
+  a.side_urs = ctx->side_urs;
   a.role = ctx->k;
   a.centroids = ctx->dparams->k_centroids;
   a.bounds = ctx->dparams->k_bounds;
   if (tq::append_small_fits(ctx, (long long)batch * heads_kv * n_new)) {
     // few vectors (a decode step): keys and values in one warp-per-vector launch
     tq::AppendArgs v = a;
+    v.side_rank = 0;
+    v.side = nullptr;
     v.x = d_v;
     set_role_planes(ctx, cache, 1, v.codes, v.norms, v.signs, v.rnorms);
     v.vt = 1;
@@ -508,6 +814,8 @@ static tq_status append_tq_both(const tq_ctx *ctx, const tq_cache *cache, const 
     return s;
   }
   // V on the caller's stream, then the caller's stream waits for K
+  a.side_rank = 0;
+  a.side = nullptr;
   a.x = d_v;
   set_role_planes(ctx, cache, 1, a.codes, a.norms, a.signs, a.rnorms);
   a.vt = 1;
@@ -659,6 +967,7 @@ tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int
     a.t1 = t1;
     a.params = ctx->dparams;
     a.out = out;
+    a.rot = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot : nullptr;
     a.bb = ctx->lay.bb;
     a.cap16 = tq::cap16_of(cache->capacity);
     a.btab = cache->block_table;
@@ -671,6 +980,11 @@ tq_status tq_dequantize(const tq_ctx *ctx, const tq_cache *cache, int batch, int
     a.codes = codes; a.norms = norms; a.signs = signs; a.rnorms = rnorms;
     if (which == 0) {
       a.role = ctx->k; a.centroids = ctx->dparams->k_centroids;
+      if (ctx->side_rank) {
+        a.side_rank = ctx->side_rank;
+        a.side = reinterpret_cast<const uint16_t *>(cache->records + ctx->lay.off[TQ_PLANE_K_SIDE]);
+        a.side_u = ctx->side_u;
+      }
     } else {
       a.role = ctx->v; a.centroids = ctx->dparams->v_centroids;
     }

@@ -40,11 +40,21 @@ struct DevParams {
   float sketch_perm[kD * kD];
   // S transposed for the warp-per-vector append: entry (i, 4L + m) = S[8(L/2) + 2m + (L&1)][i]
   float sketch_tp[kD * kD];
+  // the dense rotation (contexts set to TQ_ROTATION_DENSE; y = M u): M and M^T row-major, and
+  // sqrt(d) M as fp16 hi + lo tensor-core B operands (rows in code-storage order, K-major core
+  // matrices), like hadamard_b
+  float rot[kD * kD];
+  float rot_t[kD * kD];
+  uint16_t rot_hl[2 * kD * kD];
 };
 // fills DevParams::hadamard_b and DevParams::sketch_hl (stream order)
 int launch_operand_prep(DevParams *dp, void *stream);
 // fills DevParams::sketch_tp (stream order)
 int launch_sketch_transpose(DevParams *dp, void *stream);
+// fills DevParams::rot_hl from DevParams::rot (stream order)
+int launch_rotation_prep(DevParams *dp, void *stream);
+// the dense rotation drawn for `seed` (row-major d x d, y = M u), in double
+bool draw_dense_rotation(uint64_t seed, int d, double *M);
 
 struct Role {
   int bits = 0;
@@ -72,6 +82,30 @@ __host__ __device__ __forceinline__ T *rec_at(T *plane, long long slot, int bb, 
 }
 __host__ __device__ __forceinline__ int cap16_of(int capacity) { return (capacity + 15) & ~15; }
 
+// Code search by cells (the bulk append). A coordinate y of a vector whose boundary scale is
+// s (= ||y||) maps to t = sat(y * inv2u / s + 1/2) in [0, 1] and to cell
+// k = floor(round(t * 63 * stride) / stride) (stride 256 for 8-byte table entries, 512 for
+// 16-byte ones), i.e. t * 63 in [k - 1/(2 stride), k + 1 - 1/(2 stride)). The grid is chosen on
+// the host so that no cell holds two boundaries and every boundary lies at least
+// kCellMargin cells from a cell edge; the code is then below[k] + [y >= fl(thr[k] * s)]
+// -- the count of boundaries b_j with y >= fl(b_j * s), found with one lookup and one compare.
+constexpr int kCells = 64;
+constexpr double kCellMargin = 0.05;
+struct CellEntry {
+  int below;   // boundaries entirely below the cell
+  float thr;   // the boundary inside the cell (unit domain), or +inf
+  float c_lo;  // 2^10 c[below], 2^10 c[below + 1]: the centroids of the two possible codes
+  float c_hi;  //   (sketched roles: the residual y / s - c[code])
+};
+struct CellTable {
+  CellEntry e[kCells];
+  float inv2u;  // 1 / (2U): the cells cover the unit-domain line [-U, U]
+  int stride;   // 256 or 512 (see above)
+};
+// Build the table for sorted float32 boundaries (2^bits - 1 of them); false if no grid of
+// the searched widths satisfies the margin (it always does for the Lloyd-Max boundaries).
+bool build_cell_table(const float *bounds, const float *centroids, int bits, int stride, CellTable *out);
+
 }  // namespace tq
 
 struct tq_ctx {
@@ -96,6 +130,13 @@ struct tq_ctx {
   int8_t diag[tq::kD] = {};
   float *sketch = nullptr;  // host, d*d
   float sketch_rowmax = 0.f;  // an upper bound of max_j ||S_j||
+  tq::CellTable cells[2];     // bulk append code search (keys, values)
+  int rotation = TQ_ROTATION_WHT;  // tq_rotation of the rotated roles
+  // key side codes (tq_set_side_basis): rank, KV heads, device bases [heads][d][rank] as
+  // given (natural coordinates), rotated (natural coordinate order of the rotated domain)
+  // and rotated in code-storage order (row n = the coordinate stored at code offset n)
+  int side_rank = 0, side_heads = 0;
+  float *side_u = nullptr, *side_ur = nullptr, *side_urs = nullptr;
   tq::DevParams *dparams = nullptr;
   // a library-owned stream and two events: the key and value appends of one call
   // run concurrently (fork / join on the caller's stream)
@@ -122,6 +163,11 @@ struct AppendArgs {
   const int32_t *btab;  // paged caches: the block table (NULL: contiguous)
   int pool_blocks;
   int vt;  // 1: the value role (codes in the pair-interleaved layout)
+  // key side codes (keys of a context with tq_set_side_basis; 0 / nullptr otherwise): the
+  // side plane base, the bases in the code coordinates, natural and code-storage order
+  int side_rank;
+  uint16_t *side;
+  const float *side_ur, *side_urs;
   Role role;
   const float *centroids;  // device pointers into DevParams
   const float *bounds;
@@ -211,6 +257,10 @@ struct DequantArgs {
   const float *centroids;
   const DevParams *params;
   float *out;
+  const float *rot;  // dense rotation M, or nullptr (Walsh-Hadamard)
+  const uint16_t *side = nullptr;  // key side codes: plane base, bases as given, rank
+  const float *side_u = nullptr;
+  int side_rank = 0;
 };
 int launch_dequant_tq(const DequantArgs &a, void *stream);
 

@@ -36,6 +36,10 @@ SCHEMES = {"KV": TQ_SCHEME_KV, "KQV": TQ_SCHEME_KQV, "QKQV": TQ_SCHEME_QKQV, "KI
 TQ_F32 = 0
 TQ_BF16 = 1
 
+TQ_ROTATION_WHT = 0
+TQ_ROTATION_DENSE = 1
+ROTATIONS = {"wht": TQ_ROTATION_WHT, "dense": TQ_ROTATION_DENSE}
+
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
 _sz = ctypes.c_size_t
@@ -49,14 +53,14 @@ class tq_cache(ctypes.Structure):
 
 
 # the planes of a block of the records array (TQ schemes), in storage order (tq_plane)
-RECORD_PLANES = ["k_codes", "k_norm", "k_signs", "k_rnorm", "v_codes", "v_norm", "v_signs", "v_rnorm"]
+RECORD_PLANES = ["k_codes", "k_norm", "k_signs", "k_rnorm", "v_codes", "v_norm", "v_signs", "v_rnorm", "k_side"]
 # separately allocated arrays (records for TQ schemes; the KIVI planes)
 ARRAYS = ["records", "k_codes", "v_codes", "k_stats", "v_stats", "k_window", "v_window"]
 BLOCK_TOKENS = 16
 
 
 class tq_cache_sizes(ctypes.Structure):
-    _fields_ = [("records", _sz), ("block_bytes", _sz), ("plane_offset", _sz * 8), ("plane_bytes", _sz * 8),
+    _fields_ = [("records", _sz), ("block_bytes", _sz), ("plane_offset", _sz * 9), ("plane_bytes", _sz * 9),
                 ("k_codes", _sz), ("v_codes", _sz), ("k_stats", _sz), ("v_stats", _sz), ("k_window", _sz),
                 ("v_window", _sz), ("record_bytes", _sz)]
 
@@ -67,6 +71,10 @@ _SIGNATURES = {
     "tq_init": (_i, [_i, _i, _i, ctypes.c_uint64, ctypes.POINTER(_vp)]),
     "tq_destroy": (None, [_vp]),
     "tq_set_kivi": (_i, [_vp, _i, _i, _i, _i]),
+    "tq_set_rotation": (_i, [_vp, _i]),
+    "tq_set_side_basis": (_i, [_vp, _i, _i, _vp]),
+    "tq_principal_basis": (_i, [_vp, _i, _i, _i, _vp]),
+    "tq_draw_rotation": (_i, [ctypes.c_uint64, _i, _vp]),
     "tq_cache_sizes_get": (_i, [_vp, _i, _i, _i, ctypes.POINTER(tq_cache_sizes)]),
     "tq_cache_bytes": (_i, [_vp, _i, _i, _i, ctypes.POINTER(tq_cache_sizes)]),
     "tq_workspace_bytes": (_i, [_vp, _i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
@@ -161,6 +169,37 @@ def tq_destroy(ctx) -> None:
 
 def tq_set_kivi(ctx, group=32, window=128, k_per_channel=True, v_per_token=True) -> None:
     check(lib().tq_set_kivi(ctx, group, window, int(k_per_channel), int(v_per_token)), "tq_set_kivi")
+
+
+def tq_set_rotation(ctx, rotation="wht") -> None:
+    r = ROTATIONS[rotation] if isinstance(rotation, str) else int(rotation)
+    check(lib().tq_set_rotation(ctx, r), "tq_set_rotation")
+
+
+def tq_set_side_basis(ctx, basis: Optional[np.ndarray]) -> None:
+    """basis: float [heads_kv][d][rank] with orthonormal columns per head, or None (off)."""
+    if basis is None:
+        check(lib().tq_set_side_basis(ctx, 0, 0, None), "tq_set_side_basis")
+        return
+    B = np.ascontiguousarray(basis, dtype=np.float32)
+    heads, d, rank = B.shape
+    check(lib().tq_set_side_basis(ctx, rank, heads, B.ctypes.data_as(ctypes.c_void_p)), "tq_set_side_basis")
+
+
+def tq_principal_basis(x: np.ndarray, rank: int) -> np.ndarray:
+    """[d][rank] leading principal directions (about the origin) of the rows of x."""
+    X = np.ascontiguousarray(x, dtype=np.float32)
+    n, d = X.shape
+    U = np.zeros((d, rank), np.float32)
+    check(lib().tq_principal_basis(X.ctypes.data_as(ctypes.c_void_p), n, d, rank, U.ctypes.data_as(ctypes.c_void_p)),
+          "tq_principal_basis")
+    return U
+
+
+def tq_draw_rotation(seed: int, d: int = 128):
+    M = np.zeros((d, d), np.float32)
+    check(lib().tq_draw_rotation(ctypes.c_uint64(seed), d, M.ctypes.data_as(ctypes.c_void_p)), "tq_draw_rotation")
+    return M
 
 
 def tq_cache_sizes_get(ctx, batch: int, heads_kv: int, capacity: int) -> tq_cache_sizes:
@@ -336,10 +375,13 @@ class Context:
     """Owns one tq_ctx (created on the current CUDA device)."""
 
     def __init__(self, d: int = 128, bits: int = 4, scheme="KQV", seed: int = 42, *, kivi_group=32,
-                 kivi_window=128, k_per_channel=True, v_per_token=True):
+                 kivi_window=128, k_per_channel=True, v_per_token=True, rotation="wht"):
         self.d, self.bits, self.seed = d, bits, seed
         self.scheme = scheme if isinstance(scheme, str) else [k for k, v in SCHEMES.items() if v == scheme][0]
         self.handle = tq_init(d, bits, self.scheme, seed)
+        self.rotation = rotation
+        if rotation != "wht":
+            tq_set_rotation(self.handle, rotation)
         if self.scheme == "KIVI":
             tq_set_kivi(self.handle, kivi_group, kivi_window, k_per_channel, v_per_token)
             self.kivi = dict(group=kivi_group, window=kivi_window, k_per_channel=k_per_channel,

@@ -86,3 +86,27 @@ def test_host_argument_errors(tqmod):
     assert L.tq_decode_step(None, None, None, 0, None, None, 0, 1, 1, 1, None, 1, None, 0, None,
                             None) == tqmod.TQ_ERR_ARG
     L.tq_destroy(None)  # no-op
+
+
+@pytest.mark.parametrize("seed", [0, 42, 300])
+def test_library_dense_rotation_matches_oracle(tqmod, seed):
+    """The library's Gram-Schmidt of the stream-3 Gaussian and the oracle's LAPACK QR,
+    both sign-fixed to SO(d), round to the same float32 matrix (a last-place difference is
+    allowed where the two fp64 values straddle a rounding point)."""
+    from oracle import rotation as orot
+    M = tqmod.tq_draw_rotation(seed, 128)
+    want = orot.dense_rotation(seed, 128)
+    assert np.max(np.abs(M.astype(np.float64) - want)) < 1e-7
+    assert np.mean(M == want.astype(np.float32)) > 0.999
+    assert abs(np.linalg.det(M.astype(np.float64)) - 1.0) < 1e-5
+
+
+def test_library_principal_basis_matches_oracle(tqmod):
+    """Jacobi rotations in C++ against LAPACK's symmetric eigensolver in the oracle, with the
+    same sign convention."""
+    from oracle import sidecode as sc
+    g = np.random.default_rng(0)
+    X = (g.standard_normal((300, 128)) @ np.diag(np.linspace(3, 0.1, 128))).astype(np.float32)
+    for r in (1, 4, 8):
+        U = tqmod.tq_principal_basis(X, r)
+        np.testing.assert_allclose(U, sc.principal_basis(X.astype(np.float64), r), atol=1e-6)

@@ -97,9 +97,10 @@ def test_cache_sizes_describe_the_blocked_layout(scheme, n):
     s = tq.tq_cache_sizes_get(ctx.handle, 3, 2, 50)
     rk, rv = otq.scheme_roles(scheme, n)
     tok = [rk.bits * 16, 4, 16 if rk.qjl else 0, 4 if rk.qjl else 0,
-           rv.bits * 16, 4, 16 if rv.qjl else 0, 4 if rv.qjl else 0]
+           rv.bits * 16, 4, 16 if rv.qjl else 0, 4 if rv.qjl else 0,
+           0]  # the keys' side-code plane, empty without tq_set_side_basis
     assert list(s.plane_bytes) == tok
-    assert list(s.plane_offset) == [16 * sum(tok[:p]) for p in range(8)]
+    assert list(s.plane_offset) == [16 * sum(tok[:p]) for p in range(9)]
     assert s.block_bytes == 16 * sum(tok) == 16 * s.record_bytes
     assert s.records == 3 * 2 * 4 * s.block_bytes  # ceil(50 / 16) = 4 blocks per sequence-head
     # the sizing calls under their first-specified names give the same answers
