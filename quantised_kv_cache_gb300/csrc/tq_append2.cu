@@ -1,20 +1,16 @@
-// Append-quantise with one thread per vector (vectors without a QJL sketch:
-// keys of KV / KQV, values of KV).
+// Append-quantise of unrotated vectors (the KV scheme's keys and values) with one
+// thread per vector.
 //
 // "Statistical Inference ... Inspired by TurboQuant", technical summary,
-// "Quantisation schemes": normalise, rotate with the randomised WHT, code each
-// coordinate with the Lloyd-Max codebook; "KVQuant++", "Fast codebook lookup":
-// the code is a boundary count, found by binary search.
+// "Quantisation schemes": the KV scheme codes each coordinate of the normalised
+// vector with the Lloyd-Max codebook, without rotation; "KVQuant++", "Fast
+// codebook lookup": the code is a boundary count, found by binary search.
 //
-// A thread holds its whole 128-coordinate vector in registers, so the seven
-// butterfly stages of the Walsh-Hadamard transform need no shuffles. The
-// transform is left unnormalised (entries +/-1) and the vector is not divided
-// by its norm: instead each vector compares against its own scaled boundaries
-// nu * sqrt(128) * b_j (nu * b_j without rotation), which decides every code
-// exactly as y = H D x / (nu sqrt(128)) against b_j would. The +/-1 diagonal D
-// arrives as kernel parameters, so its multiplications read constant-bank
-// operands. The boundaries are symmetric about 0, so a code is the sign of y
-// plus a binary search of |y| over the positive boundaries.
+// A thread holds its whole 128-coordinate vector in registers and does not divide
+// it by its norm: it compares against its own scaled boundaries nu * b_j, which
+// decides every code exactly as x / nu against b_j would. The boundaries are
+// symmetric about 0, so a code is the sign of x plus a binary search of |x| over
+// the positive boundaries. (Rotated roles take the tensor-core kernels.)
 
 #include "tq_device.cuh"
 
@@ -35,12 +31,10 @@ struct Append2Args {
   int side_rank;
   uint16_t *side;
   const float *side_ur;
-  float diag[kD];
   float bounds[kMaxLevels];     // 2^BITS - 1 used
   float centroids[kMaxLevels];  // 2^BITS used (side codes)
 };
 
-constexpr float kSqrtD = 11.313708498984761f;  // sqrt(128)
 
 // count of positive boundaries P[0..H-1] (ascending) at or below a >= 0
 template <int H>
@@ -60,7 +54,7 @@ __device__ __forceinline__ int count_pos(float a, const float (&P)[H]) {
   }
 }
 
-template <int BITS, bool ROT, bool BF16>
+template <int BITS, bool BF16>
 __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Append2Args a) {
   constexpr int L = 1 << BITS, H = L / 2 - 1;
   const long long total = (long long)a.batch * a.heads * a.n_new;
@@ -113,22 +107,9 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
       for (int i = 0; i < w; ++i) sq[i] = sq[i] + sq[i + w];
     const float nu = sqrtf(sq[0]);
 
-    if (ROT) {
-#pragma unroll
-      for (int i = 0; i < kD; ++i) x[i] *= a.diag[i];
-#pragma unroll
-      for (int hs = 1; hs < kD; hs <<= 1)
-#pragma unroll
-        for (int i = 0; i < kD; ++i)
-          if ((i & hs) == 0) {
-            const float u = x[i], v = x[i + hs];
-            x[i] = u + v;
-            x[i + hs] = u - v;
-          }
-    }
-    // positive boundaries scaled to this vector: b_{L/2 + k} * nu (* sqrt(128)); a zero
-    // vector keeps the unit boundaries so that y = 0 codes to L/2 as the format requires
-    const float s = (nu > 0.f) ? (ROT ? nu * kSqrtD : nu) : 1.f;
+    // positive boundaries scaled to this vector: b_{L/2 + k} * nu; a zero vector keeps the
+    // unit boundaries so that y = 0 codes to L/2 as the format requires
+    const float s = (nu > 0.f) ? nu : 1.f;
     float P[H];
 #pragma unroll
     for (int k = 0; k < H; ++k) P[k] = a.bounds[L / 2 + k] * s;
@@ -137,11 +118,10 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
     uint32_t word[4 * BITS];
 #pragma unroll
     for (int w = 0; w < 4 * BITS; ++w) word[w] = 0u;
-#pragma unroll
     // side code of an unsketched key: z_k = nu sum_i U[i][k] (x_i / nu - c[code_i])
     const int srank = a.side_rank;
     const float *su = srank ? a.side_ur + (size_t)head * kD * srank : nullptr;
-    const float inv_nu = (nu > 0.f) ? 1.f / (ROT ? nu * kSqrtD : nu) : 0.f;
+    const float inv_nu = (nu > 0.f) ? 1.f / nu : 0.f;
     float zs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < kD; ++i) {
@@ -201,7 +181,7 @@ __global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Ap
 
 int g_sms2 = 0;
 
-template <int BITS, bool ROT, bool BF16>
+template <int BITS, bool BF16>
 int go(const Append2Args &k, long long total, cudaStream_t st) {
   if (g_sms2 == 0) {
     int dev = 0;
@@ -213,16 +193,16 @@ int go(const Append2Args &k, long long total, cudaStream_t st) {
   const long long cap = 4LL * g_sms2;  // enough resident threads to cover memory latency
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  append2_kernel<BITS, ROT, BF16><<<(unsigned)blocks, 128, 0, st>>>(k);
+  append2_kernel<BITS, BF16><<<(unsigned)blocks, 128, 0, st>>>(k);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
-template <bool ROT, bool BF16>
+template <bool BF16>
 int dispatch(int bits, const Append2Args &k, long long total, cudaStream_t st) {
   switch (bits) {
-    case 2: return go<2, ROT, BF16>(k, total, st);
-    case 3: return go<3, ROT, BF16>(k, total, st);
-    case 4: return go<4, ROT, BF16>(k, total, st);
+    case 2: return go<2, BF16>(k, total, st);
+    case 3: return go<3, BF16>(k, total, st);
+    case 4: return go<4, BF16>(k, total, st);
     default: return TQ_ERR_UNSUPPORTED;
   }
 }
@@ -231,7 +211,7 @@ int dispatch(int bits, const Append2Args &k, long long total, cudaStream_t st) {
 
 // Thread-per-vector append for vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise.
 int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
-  if (a.role.qjl || a.role.bits < 2) return TQ_ERR_UNSUPPORTED;
+  if (a.role.qjl || a.role.rotate || a.role.bits < 2) return TQ_ERR_UNSUPPORTED;
   Append2Args k{};
   k.x = a.x;
   k.batch = a.batch;
@@ -247,7 +227,6 @@ int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.codes = a.codes;
   k.norms = a.norms;
   k.error = a.error;
-  for (int i = 0; i < kD; ++i) k.diag[i] = (float)ctx->diag[i];
   const bool is_k = a.centroids == ctx->dparams->k_centroids;
   const float *src = is_k ? ctx->k_bounds : ctx->v_bounds;
   const float *csrc = is_k ? ctx->k_centroids : ctx->v_centroids;
@@ -259,9 +238,7 @@ int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   const long long total = (long long)a.batch * a.heads * a.n_new;
   cudaStream_t st = (cudaStream_t)stream;
   const bool bf16 = a.dtype == TQ_BF16;
-  if (a.role.rotate) return bf16 ? dispatch<true, true>(a.role.bits, k, total, st)
-                                 : dispatch<true, false>(a.role.bits, k, total, st);
-  return bf16 ? dispatch<false, true>(a.role.bits, k, total, st) : dispatch<false, false>(a.role.bits, k, total, st);
+  return bf16 ? dispatch<true>(a.role.bits, k, total, st) : dispatch<false>(a.role.bits, k, total, st);
 }
 
 }  // namespace tq

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 1) append_small_kernel(const
     load4(ro.x, (size_t)vec * kD + 4 * lane, BF16, x);
     float r[4];
     const bool side = a.side_rank > 0 && blockIdx.y == 0;  // keys with side codes
-    encode_vector_warp(ro, x, slot, a.bb, a.diag, lane, nu, r, rr, a.rot_t, side);
+    encode_vector_warp_general(ro, x, slot, a.bb, a.diag, lane, nu, r, rr, a.rot_t, side);
     if (side)
       side_code_warp(a.side_ur + (size_t)(bh % a.heads) * kD * a.side_rank, a.side_rank, nu, r, a.k_side, slot,
                      a.bb, lane);

@@ -46,6 +46,9 @@ struct PrepArgs {
   // written to the second half of the row's record (unsketched keys leave it free)
   const float *side_ur = nullptr;
   int side_rank = 0, group = 1;
+  // S transposed and permuted: entry (i, 4L + m) = S[8 (L / 2) + 2 m + (L & 1)][i], so that
+  // lane L reads its four sketch rows' column i as one coalesced float4
+  const float *sketch_tp = nullptr;
 };
 
 // Exclusive prefix over batches of ceil(clamped length / kDecodeTile), by one
@@ -114,17 +117,23 @@ __global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) s_q[warp][4 * lane + j] = v[j];
   __syncwarp();
-  // (S q_rot)_k for k = lane + 32 m
+  // (S q_rot)_k for the four sketch rows k = 8 (lane / 2) + 2 m + (lane & 1), each row's
+  // column i read from the transposed copy in one coalesced 512-byte line per i
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
   for (int i = 0; i < kD; ++i) {
     const float qi = s_q[warp][i];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) acc[m] = fmaf(__ldg(a.sketch + (lane + 32 * m) * kD + i), qi, acc[m]);
+    const float4 s4 = __ldg(reinterpret_cast<const float4 *>(a.sketch_tp + (size_t)i * kD) + lane);
+    acc[0] = fmaf(s4.x, qi, acc[0]);
+    acc[1] = fmaf(s4.y, qi, acc[1]);
+    acc[2] = fmaf(s4.z, qi, acc[2]);
+    acc[3] = fmaf(s4.w, qi, acc[3]);
   }
   if (live) {
     const float c = kSqrtHalfPi / kD * kInvSqrtD;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) a.qprep[(size_t)row * 2 * kD + kD + lane + 32 * m] = acc[m] * c;
+    for (int m = 0; m < 4; ++m)
+      a.qprep[(size_t)row * 2 * kD + kD + 8 * (lane >> 1) + 2 * m + (lane & 1)] = acc[m] * c;
   }
 }
 
@@ -891,6 +900,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
              ctx->dparams->diag, ctx->dparams->sketch, a.qprep,
              a.seq_lens, a.cache->capacity, persist_ok ? a.tile_prefix : nullptr};
   p.rot_t = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot_t : nullptr;
+  p.sketch_tp = ctx->dparams->sketch_tp;
   p.side_ur = ctx->side_ur;
   p.side_rank = ctx->side_rank;
   p.group = G;

@@ -106,8 +106,6 @@ constexpr int persist_stages() {
 struct Decode2Args {
   const uint8_t *records;  // blocked records: [sequence-head][cap16 / 16] blocks of `bb` bytes (or a pool)
   int bb, cap16;
-  const int32_t *btab;     // paged caches: virtual block -> pool block (NULL: contiguous)
-  int pool_blocks;
   int capacity, batch, heads_kv, heads_q, chunk, splits;
   const int32_t *seq_lens;
   const int32_t *tile_prefix;  // persistent kernel: [batch + 1] tiles before each batch
@@ -126,6 +124,10 @@ struct Decode2Args {
   const float *sketch_tp;    // permuted S^T (sketch_signs_warp)
   int32_t *tile_prefix_out;  // [batch + 1] tiles before each batch, for the combine
   WarpRole role[2];          // keys, values
+  // paged caches: virtual block -> pool block (NULL: contiguous). Last in the struct: placed
+  // after `records`, the shifted parameter offsets cost the contiguous token loop 5 %.
+  const int32_t *btab;
+  int pool_blocks;
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -361,15 +363,13 @@ __device__ __forceinline__ void tile_body(const unsigned char *st, const unsigne
   if (!KQJL) sc *= kn[tok];
   sc = valid ? sc : -INFINITY;
 
-  // ---- online softmax over the warp's 16 tokens (base 2). The running maximum moves only
-  // when some token beats it: one vote finds out, and only then does the warp reduce its
-  // maximum and rescale (warp-uniform; m = -inf scales zeros). Otherwise the tile's
-  // maximum would leave the running one unchanged, so the weights are the same.
-  if (__any_sync(kFull, sc > ws.m)) {
-    float tmax = sc;
+  // ---- online softmax over the warp's 16 tokens (base 2)
+  float tmax = sc;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
-    const float m_new = fmaxf(ws.m, tmax);
+  for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+  const float m_new = fmaxf(ws.m, tmax);
+  const float p = valid ? ex2_approx(sc - m_new) : 0.f;
+  if (m_new != ws.m) {  // warp-uniform: the running max moved (m = -inf scales zeros)
     const float scale = ex2_approx(ws.m - m_new);
     ws.l *= scale;
     ws.w *= scale;
@@ -379,7 +379,6 @@ __device__ __forceinline__ void tile_body(const unsigned char *st, const unsigne
       for (int j = 0; j < 4; ++j) ws.acc[mb][j] *= scale;
     ws.m = m_new;
   }
-  const float p = valid ? ex2_approx(sc - ws.m) : 0.f;
   ws.l += p;  // every token sits on two lanes: halved at the flush
 
   // ---- B operands: this lane's token weight (p nu on even lanes, p rho on odd ones)
@@ -730,11 +729,16 @@ __device__ __forceinline__ void prep_query(const Decode2Args &a, int lane, float
 
 // Append the new token (one role) of unit u = b * H + h at slot len (the sequence's
 // length before the step, 0 <= len < capacity) by one warp. s_sk: the permuted S^T in
-// shared memory.
+// shared memory. PAGED: translate the slot through the block table (the contiguous cache's
+// instantiation carries no translation).
+template <bool PAGED>
 __device__ __forceinline__ void step_append(const Decode2Args &a, int u, int role, int len, int lane,
                                             const float *s_sk) {
-  const long long slot = phys_slot(a.btab, a.pool_blocks, (long long)u * a.cap16 + len, a.error);
-  if (slot < 0) return;  // an unmapped block: nothing appended (the error word says so)
+  long long slot = (long long)u * a.cap16 + len;
+  if constexpr (PAGED) {
+    slot = phys_slot(a.btab, a.pool_blocks, slot, a.error);
+    if (slot < 0) return;  // an unmapped block: nothing appended (the error word says so)
+  }
   float x[4];
   load4(role ? a.v_new : a.k_new, (size_t)u * kD + 4 * lane, a.kv_bf16 != 0, x);
   const WarpRole &ro = a.role[role];
@@ -768,7 +772,9 @@ constexpr int persist_smem_bytes() {
   return persist_sbar_offset<Gm>() + 8 + 4 * kMaxPersistBatch;  // + the decode step's raw lengths
 }
 
-template <int KB, int VB, bool KQJL, bool VQJL, bool FUSED>
+// PAGED: the cache has a block table (a separate instantiation, so that the contiguous
+// kernel's copy issue stays as short as it can be).
+template <int KB, int VB, bool KQJL, bool VQJL, bool FUSED, bool PAGED>
 __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(Decode2Args a) {
   static_assert(!(FUSED && KQJL), "the decode step prepares queries without a key sketch");
   constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
@@ -869,7 +875,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
   // moves, a tile before its copy is issued, so the copy never waits on the lookup
   int pf = -1;
   auto prefetch = [&]() {
-    if (a.btab != nullptr && lane == 0 && cur_i < nloc && cur_t * kTT + 16 * qtr < cur_len)
+    if (PAGED && lane == 0 && cur_i < nloc && cur_t * kTT + 16 * qtr < cur_len)
       pf = __ldg(a.btab + ((cur_row + cur_t * kTT + 16 * qtr) >> 4));
   };
   prefetch();
@@ -880,16 +886,21 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     const int t0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - t0);
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
-      const uint8_t *src = n <= 0 ? nullptr
-                           : a.btab ? pool_block<Gm::block>(a, pf)
-                                    : a.records + ((cur_row + t0) >> 4) * Gm::block;
-      mbar_arrive_expect_tx(bar, src ? (uint32_t)Gm::block : 0u);
-      if (src) tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, src, (uint32_t)Gm::block, bar);
+      if constexpr (PAGED) {
+        const uint8_t *src = n > 0 ? pool_block<Gm::block>(a, pf) : nullptr;
+        mbar_arrive_expect_tx(bar, src ? (uint32_t)Gm::block : 0u);
+        if (src) tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, src, (uint32_t)Gm::block, bar);
+      } else {
+        mbar_arrive_expect_tx(bar, n > 0 ? (uint32_t)Gm::block : 0u);
+        if (n > 0)
+          tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, a.records + ((cur_row + t0) >> 4) * Gm::block,
+                      (uint32_t)Gm::block, bar);
+      }
     }
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
     if (cur_i < nloc) seek();
-    prefetch();
+    if constexpr (PAGED) prefetch();
   };
   // query row (= unit: one query head per KV head) of the segment starting at tile g
   auto unit_of = [&](int g) -> int {
@@ -912,7 +923,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
       const int gl = H * s_pre[bq] + (hq + 1) * nb - 1;  // the head's last tile
       const int len = s_raw[bq];
       if (nb == 0 || gl < g0 || gl >= g1 || len < 0 || len >= a.capacity) continue;
-      step_append(a, u, j & 1, len, lane, s_sk);
+      step_append<PAGED>(a, u, j & 1, len, lane, s_sk);
       fence_proxy_async_global();  // the records written above, before their bulk copies
     }
     if constexpr (kStepSketch) fence_proxy_async_shared();  // S^T read above, before the ring overwrites it
@@ -1079,27 +1090,24 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
   float s0 = v0 ? (sk[0] + sk[1]) * kn[tok0] : -INFINITY;
   float s1 = v1 ? (sk[2] + sk[3]) * kn[tok1] : -INFINITY;
   // ---- online softmax of head t4 over the warp's 16 tokens (the 8 lanes g share t4)
-  // (the heads' maxima are reduced only when some token beats its head's running maximum)
-  if (__any_sync(kFull, fmaxf(s0, s1) > m_run)) {
-    float tmax = fmaxf(s0, s1);
+  float tmax = fmaxf(s0, s1);
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
-    const float m_new = fmaxf(m_run, tmax);
-    if (m_new != m_run) {  // per head (lane-divergent; no shuffles inside)
-      const float scale = ex2_approx(m_run - m_new);
-      l_run *= scale;
-      w_run *= scale;
+  for (int o = 4; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o));
+  const float m_new = fmaxf(m_run, tmax);
+  const float p0 = v0 ? ex2_approx(s0 - m_new) : 0.f, p1 = v1 ? ex2_approx(s1 - m_new) : 0.f;
+  if (m_new != m_run) {  // per head (lane-divergent; no shuffles inside)
+    const float scale = ex2_approx(m_run - m_new);
+    l_run *= scale;
+    w_run *= scale;
 #pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
+    for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc_v[mb][j] *= scale;
-          if (VQJL) acc_s[mb][j] *= scale;
-        }
-      m_run = m_new;
-    }
+      for (int j = 0; j < 4; ++j) {
+        acc_v[mb][j] *= scale;
+        if (VQJL) acc_s[mb][j] *= scale;
+      }
+    m_run = m_new;
   }
-  const float p0 = v0 ? ex2_approx(s0 - m_run) : 0.f, p1 = v1 ? ex2_approx(s1 - m_run) : 0.f;
   l_run += p0 + p1;
   // ---- B operands: column 2h + part of lane (g, t) = hi / lo of head h's weights of tokens
   // 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1); token j of head h sits on lane 4 (j % 8) + h
@@ -1429,12 +1437,13 @@ int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st
   using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
   if (k.bb != Gm::block) return TQ_ERR_UNSUPPORTED;
   const size_t smem = persist_smem_bytes<Gm>();
-  auto fn = decode_persist_kernel<KB, VB, KQJL, VQJL, FUSED>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  auto fn = k.btab ? decode_persist_kernel<KB, VB, KQJL, VQJL, FUSED, true>
+                   : decode_persist_kernel<KB, VB, KQJL, VQJL, FUSED, false>;
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[k.btab ? 1 : 0]) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    attr_done = true;
+    attr_done[k.btab ? 1 : 0] = true;
   }
   *ctas = num_sms;
   return launch_overlapped(true, fn, dim3(*ctas), dim3(kPersistWarps * 32), smem, st, k) == cudaSuccess

@@ -344,13 +344,67 @@ __device__ __forceinline__ void warp_store_codes_vt(uint8_t *vplane, long long s
 // without a sketch, the norm) of token `slot` (nothing when slot < 0). For sketched
 // roles returns the unit-domain residual r = y - c[code] (zero for a zero vector) and
 // sum r^2 over the warp.
-// rot_t: the dense rotation's M^T (row-major) for contexts set to TQ_ROTATION_DENSE, else
-// nullptr (the randomised Walsh-Hadamard transform with diagonal `diag`). want_res: return
-// the residual of an unsketched role too (for its side code).
 template <typename R>
 __device__ __forceinline__ void encode_vector_warp(const R &ro, const float (&x)[4], long long slot, int bb,
                                                    const float *diag, int lane, float &nu, float (&r)[4],
-                                                   float &rr, const float *rot_t = nullptr, bool want_res = false) {
+                                                   float &rr) {
+  nu = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
+  float y[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float dg = ro.rotate ? __ldg(diag + 4 * lane + j) : 1.f;
+    y[j] = (nu > 0.f) ? (x[j] / nu) * dg : 0.f;
+  }
+  if (ro.rotate) wht128(y, lane);
+  int idx[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxLevels - 1; ++k) c += (y[j] >= ro.bounds[k]) ? 1 : 0;
+    idx[j] = c;
+  }
+  if (ro.vt) {
+    switch (ro.bits) {
+      case 1: warp_store_codes_vt<1>(ro.codes, slot, bb, idx, lane); break;
+      case 2: warp_store_codes_vt<2>(ro.codes, slot, bb, idx, lane); break;
+      case 3: warp_store_codes_vt<3>(ro.codes, slot, bb, idx, lane); break;
+      default: warp_store_codes_vt<4>(ro.codes, slot, bb, idx, lane); break;
+    }
+  } else {
+    switch (ro.bits) {
+      case 1: warp_store_codes<1>(ro.codes, slot, bb, idx, lane); break;
+      case 2: warp_store_codes<2>(ro.codes, slot, bb, idx, lane); break;
+      case 3: warp_store_codes<3>(ro.codes, slot, bb, idx, lane); break;
+      default: warp_store_codes<4>(ro.codes, slot, bb, idx, lane); break;
+    }
+  }
+  if (!ro.qjl && slot >= 0 && lane == 0) *rec_at(ro.norms, slot, bb, 4) = nu;
+  rr = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r[j] = 0.f;
+  if (ro.qjl) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float rj = y[j] - ro.centroids[idx[j]];
+      s += rj * rj;
+      r[j] = (nu > 0.f) ? rj : 0.f;
+    }
+    rr = warp_sum(s);
+  }
+}
+
+// encode_vector_warp with two run-time options, for the warp-per-vector append: rot_t, the
+// dense rotation's M^T (row-major) for contexts set to TQ_ROTATION_DENSE, else nullptr (the
+// randomised Walsh-Hadamard transform with diagonal `diag`); want_res, return the residual of
+// an unsketched role too (for its side code). A function of its own: the fused decode step,
+// which encodes its new token with encode_vector_warp, ran 5 % slower when that function
+// carried these options.
+template <typename R>
+__device__ __forceinline__ void encode_vector_warp_general(const R &ro, const float (&x)[4], long long slot, int bb,
+                                                           const float *diag, int lane, float &nu, float (&r)[4],
+                                                           float &rr, const float *rot_t, bool want_res) {
   nu = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
   float y[4];
   const bool wht = ro.rotate && rot_t == nullptr;
