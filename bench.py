@@ -458,9 +458,10 @@ def measure_configs(dev, cases=CONFIG_CASES):
     config 1 (single head), config 3 (three schemes x three budgets), config 4 (GQA 32q/8kv,
     N=131072, KQV n=3, 64 chunks), config 5 (KIVI, four layouts). Caches smaller than 3x L2
     are replicated and rotated so that every decode call reads HBM. Decode times are CUDA
-    events around the library's decode kernel (its profile events, on the call's stream)
-    and around the whole call (query prep + decode + combine); append times are events
-    around a bulk append of the whole context into one cache."""
+    events around the library's decode kernel (its profile events, on the call's stream),
+    around the whole call (query prep + decode + combine, issued call by call from Python),
+    and around a CUDA-graph replay of the same calls (the device time of the whole call);
+    append times are events around a bulk append of the whole context into one cache."""
     import torch
     from quantised_kv_cache_gb300 import tq
     from quantised_kv_cache_gb300 import workloads as wl
@@ -517,9 +518,29 @@ def measure_configs(dev, cases=CONFIG_CASES):
         torch.cuda.synchronize()
         tq.tq_set_profile_events(ctx.handle)
         assert tq.tq_get_device_error(ctx.handle) == 0
+        # the same calls captured once as a CUDA graph and replayed: the device time of the
+        # whole call without the host's launch gaps between calls
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(iters):
+                    tq.tq_decode_attention(ctx.handle, caches[i % reps], q, lens, N, splits, ws, out,
+                                           stream=torch.cuda.current_stream())
+        graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        graph.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        assert tq.tq_get_device_error(ctx.handle) == 0
+        del graph
         ms_kernel = sum(a_.elapsed_time(b_) for a_, b_ in evs) / iters
         ms_call = c0.elapsed_time(c1) / iters
-        gbs_k, gbs_c = bytes_call / ms_kernel / 1e6, bytes_call / ms_call / 1e6
+        ms_graph = g0.elapsed_time(g1) / iters
+        gbs_k, gbs_c, gbs_g = bytes_call / ms_kernel / 1e6, bytes_call / ms_call / 1e6, bytes_call / ms_graph / 1e6
         append_gbs = append_bytes / append_ms / 1e6
         rows.append({"config": wid, "scheme": scheme, "bits": n,
                      "kivi_layout": None if kivi is None else {"k_per_channel": kivi[0], "v_per_token": kivi[1]},
@@ -527,7 +548,8 @@ def measure_configs(dev, cases=CONFIG_CASES):
                                "input_dtype": str(k.dtype).replace("torch.", "")},
                      "decode": {"bytes_per_call": bytes_call, "replicas": reps, "ms_kernel": ms_kernel,
                                 "GB_per_s_kernel": gbs_k, "frac_kernel": gbs_k / hbm_peak, "ms_call": ms_call,
-                                "GB_per_s_call": gbs_c, "frac_call": gbs_c / hbm_peak},
+                                "GB_per_s_call": gbs_c, "frac_call": gbs_c / hbm_peak, "ms_graph": ms_graph,
+                                "GB_per_s_graph": gbs_g, "frac_graph": gbs_g / hbm_peak},
                      "append": {"ms": append_ms, "tokens_per_s": B * N / (append_ms / 1e3),
                                 "token_heads_per_s": B * H * N / (append_ms / 1e3), "bytes": append_bytes,
                                 "GB_per_s": append_gbs, "frac": append_gbs / hbm_peak},

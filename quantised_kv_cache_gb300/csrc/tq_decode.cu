@@ -394,25 +394,31 @@ struct CombineArgs {
   int group = 1;  // query heads per KV head (persistent records hold `group` heads per slot)
   int *error = nullptr;
   const float *rot = nullptr;  // dense rotation M (o = M^T o_rot), or nullptr (Walsh-Hadamard)
+  int num_sms = 0;             // the device's SMs (sizes the combine's grid)
 };
 
-// Merge the partial records of one query row: thread i (of 128) gets coordinate i
-// of the weighted value sum A and sign sum Sg, and every thread the weight L.
-__device__ __forceinline__ void merge_row(const CombineArgs &a, int row, int i, float &L_out, float &A_out,
-                                          float &Sg_out) {
-  // the partial records of this row: split-K ones in a row, or the persistent
-  // kernel's (cta, group) records of every CTA whose slice touched this head
-  const float *base = a.partials + (size_t)row * a.splits * kPartialFloats;
+// The partial records of one query row: split-K ones in a row, or the persistent kernel's
+// (cta, group) records of every CTA whose slice touched the row's head. record(k) is the
+// k-th of count() records, or nullptr for a CTA whose slice was empty (it wrote nothing).
+struct RowRecords {
+  const CombineArgs &a;
+  const float *base = nullptr;
   // persistent slices: CTA c holds tiles [bnd(c), bnd(c + 1)), bnd(c) = min(T, 4 floor(T4 c / C))
   long long T = 0, T4 = 1, C = 1, c_lo = 0, c_hi = -1;
-  int unit = 0;
+  int unit = 0, hh = 0, nrec = 0;
   bool narrow = true;  // every quotient below fits 32-bit division
-  auto qdiv = [&](long long n, long long d) -> long long {
+
+  __device__ __forceinline__ long long qdiv(long long n, long long d) const {
     return narrow ? (long long)((uint32_t)n / (uint32_t)d) : n / d;
-  };
-  auto bnd = [&](long long c) -> long long { return min(T, 4 * qdiv(T4 * c, C)); };
-  int hh = 0;
-  if (a.tile_prefix) {
+  }
+  __device__ __forceinline__ long long bnd(long long c) const { return min(T, 4 * qdiv(T4 * c, C)); }
+
+  __device__ __forceinline__ RowRecords(const CombineArgs &args, int row) : a(args) {
+    base = a.partials + (size_t)row * a.splits * kPartialFloats;
+    if (!a.tile_prefix) {
+      nrec = a.splits;
+      return;
+    }
     const int b = row / a.heads_q, h = (row % a.heads_q) / a.group;
     hh = (row % a.heads_q) % a.group;
     const int p0 = __ldg(a.tile_prefix + b), nb = __ldg(a.tile_prefix + b + 1) - p0;
@@ -427,55 +433,38 @@ __device__ __forceinline__ void merge_row(const CombineArgs &a, int row, int i, 
       c_lo = qdiv((us / 4 + 1) * C - 1, T4);
       c_hi = qdiv(((ue - 1) / 4 + 1) * C - 1, T4);
     }
+    nrec = (int)(a.persist_groups * (c_hi - c_lo + 1));
   }
-  const int ng = a.persist_groups;
-  const int nrec = a.tile_prefix ? (int)(ng * (c_hi - c_lo + 1)) : a.splits;
-  auto record = [&](int k) -> const float * {
+  __device__ __forceinline__ const float *record(int k) const {
     if (!a.tile_prefix) return base + (size_t)k * kPartialFloats;
+    const int ng = a.persist_groups;
     const long long c = c_lo + k / ng;
-    if (bnd(c) == bnd(c + 1)) return nullptr;  // an empty slice wrote nothing
+    if (bnd(c) == bnd(c + 1)) return nullptr;
     return a.partials + (((size_t)(c + unit) * ng + (k % ng)) * a.group + hh) * kPartialFloats;
-  };
-  // one pass with a running maximum (records are few; unrolled so their loads overlap)
-  float M = -INFINITY, L = 0.f, A = 0.f, Sg = 0.f;
-#pragma unroll 4
-  for (int k = 0; k < nrec; ++k) {
-    const float *rec = record(k);
-    if (!rec) continue;
-    const float ms = __ldg(rec);
-    const float l = __ldg(rec + 1), av = __ldg(rec + 2 + i), sv = a.sketch_v ? __ldg(rec + 2 + kD + i) : 0.f;
-    if (ms == -INFINITY) continue;
-    if (ms > M) {
-      const float sc = (M == -INFINITY) ? 0.f : __expf(M - ms);
-      L *= sc;
-      A *= sc;
-      Sg *= sc;
-      M = ms;
-    }
-    const float e = __expf(ms - M);
-    L += l * e;
-    A += av * e;
-    Sg += sv * e;
   }
-  L_out = L;
-  A_out = A;
-  Sg_out = Sg;
-}
+};
 
-// Finish kCombineRows query rows per CTA (128 threads per row): merge each row's
-// partial records, add the sketch term (sqrt(pi/2)/m) S^T Sg with S staged in
-// shared memory, divide by L, and undo the rotation (inverse WHT, then D).
-constexpr int kCombineRows = 4;
+// Finish R query rows per CTA of 512 threads: a team of W = 16 / R warps per row merges the
+// row's partial records in parallel -- the records' maximum M first, then warp w sums
+// e^(m_k - M) (l_k, A_k, Sg_k) over records k = w (mod W), and the team adds the W partial
+// sums -- then adds the sketch term (sqrt(pi/2)/m) S^T Sg with S staged in shared memory,
+// divides by L and undoes the rotation (inverse WHT, then D; or M^T).
+constexpr int kCombineThreads = 512;
+constexpr int kPartStride = 2 * kD + 4;  // floats per warp's partial sums: A, Sg, L (16-byte rows)
 
-__global__ void __launch_bounds__(kCombineRows * 128) combine_tq_kernel(CombineArgs a) {
+template <int R>
+__global__ void __launch_bounds__(kCombineThreads) combine_tq_kernel(CombineArgs a) {
+  constexpr int W = 16 / R, TS = 32 * W, NS = TS / kD;  // warps, threads, S^T k-slices per row
   extern __shared__ __align__(16) float s_comb[];
   __shared__ uint64_t s_bar;
-  float *s_sk = s_comb;                             // [128][128] S (sketch_v only)
-  float *s_sg = s_sk + (a.sketch_v ? kD * kD : 0);  // [rows][128]
-  float *s_o = s_sg + kCombineRows * kD;            // [rows][128]
-  const int tid = threadIdx.x, i = tid & (kD - 1), rr = tid >> 7;
+  __shared__ float s_red[16];
+  float *s_sk = s_comb;                              // [128][128] S (sketch_v only)
+  float *s_part = s_sk + (a.sketch_v ? kD * kD : 0);  // [16 warps][kPartStride] partial sums
+  float *s_v = s_part + 16 * kPartStride;            // [R][NS][128] S^T slices, then [R][128] outputs
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rr = warp / W, w = warp % W, t = tid % TS;  // row of the CTA, warp and thread in its team
   const int nrows = a.batch * a.heads_q;
-  const int row = blockIdx.x * kCombineRows + rr;
+  const int row = blockIdx.x * R + rr;
   // S (a context constant) streams into shared memory while the records are merged
   if (a.sketch_v && tid == 0) {
     mbar_init(&s_bar, 1);
@@ -483,29 +472,102 @@ __global__ void __launch_bounds__(kCombineRows * 128) combine_tq_kernel(CombineA
     mbar_arrive_expect_tx(&s_bar, kD * kD * sizeof(float));
     tma_load_1d(s_sk, a.sketch, kD * kD * sizeof(float), &s_bar);
   }
-  pdl_wait();  // the partial records come from the decode kernel before
+  pdl_wait();     // the partial records come from the decode kernel before
   pdl_trigger();  // the next kernel of the stream (e.g. the next step's append) may be scheduled
-  float L = 0.f, A = 0.f, Sg = 0.f;
-  if (row < nrows) merge_row(a, row, i, L, A, Sg);
-  s_sg[rr * kD + i] = Sg;
-  __syncthreads();
-  float o = A;
-  if (a.sketch_v && mbar_wait_bounded(&s_bar, 0, a.error)) {
-    const float *sg = s_sg + rr * kD;
-    float t0 = 0.f, t1 = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < kD; k += 2) {
-      t0 = fmaf(s_sk[k * kD + i], sg[k], t0);
-      t1 = fmaf(s_sk[(k + 1) * kD + i], sg[k + 1], t1);
-    }
-    o += (kSqrtHalfPi / kD) * (t0 + t1);
+  const bool live = row < nrows;
+  const RowRecords rec(a, live ? row : 0);
+  const int nrec = live ? rec.nrec : 0;
+
+  // the records' maximum
+  float m = -INFINITY;
+  for (int k = t; k < nrec; k += TS) {
+    const float *r = rec.record(k);
+    if (r) m = fmaxf(m, __ldg(r));
   }
-  o = (L > 0.f) ? o / L : 0.f;
-  s_o[rr * kD + i] = o;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  if (lane == 0) s_red[warp] = m;
   __syncthreads();
-  // rotate back: warp w of the row's four warps
-  const int warp = tid >> 5, lane = tid & 31;
-  if ((warp & 3) == 0 && row < nrows) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < W; ++j) M = fmaxf(M, s_red[rr * W + j]);
+
+  // this warp's share: lane L holds coordinates 2L, 2L + 1, 64 + 2L, 65 + 2L
+  float L = 0.f, A[4] = {0.f, 0.f, 0.f, 0.f}, G[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int k = w; k < nrec; k += W) {
+    const float *r = rec.record(k);
+    if (!r) continue;
+    const float ms = __ldg(r);
+    if (ms == -INFINITY) continue;
+    const float e = __expf(ms - M);
+    L = fmaf(__ldg(r + 1), e, L);
+    const float2 a0 = __ldg(reinterpret_cast<const float2 *>(r + 2) + lane);
+    const float2 a1 = __ldg(reinterpret_cast<const float2 *>(r + 2 + 64) + lane);
+    A[0] = fmaf(a0.x, e, A[0]);
+    A[1] = fmaf(a0.y, e, A[1]);
+    A[2] = fmaf(a1.x, e, A[2]);
+    A[3] = fmaf(a1.y, e, A[3]);
+    if (a.sketch_v) {
+      const float2 g0 = __ldg(reinterpret_cast<const float2 *>(r + 2 + kD) + lane);
+      const float2 g1 = __ldg(reinterpret_cast<const float2 *>(r + 2 + kD + 64) + lane);
+      G[0] = fmaf(g0.x, e, G[0]);
+      G[1] = fmaf(g0.y, e, G[1]);
+      G[2] = fmaf(g1.x, e, G[2]);
+      G[3] = fmaf(g1.y, e, G[3]);
+    }
+  }
+  float *mine = s_part + warp * kPartStride;
+  reinterpret_cast<float2 *>(mine)[lane] = make_float2(A[0], A[1]);
+  reinterpret_cast<float2 *>(mine + 64)[lane] = make_float2(A[2], A[3]);
+  reinterpret_cast<float2 *>(mine + kD)[lane] = make_float2(G[0], G[1]);
+  reinterpret_cast<float2 *>(mine + kD + 64)[lane] = make_float2(G[2], G[3]);
+  if (lane == 0) mine[2 * kD] = L;
+  __syncthreads();
+  // the team's sums: thread t < 128 of the team takes coordinate t (A, and Sg into slot W)
+  const float *team = s_part + rr * W * kPartStride;
+  float Lr = 0.f;
+#pragma unroll
+  for (int j = 0; j < W; ++j) Lr += team[j * kPartStride + 2 * kD];
+  float Ar = 0.f, Gr = 0.f;
+  if (t < kD) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      Ar += team[j * kPartStride + t];
+      Gr += team[j * kPartStride + kD + t];
+    }
+  }
+  __syncthreads();  // every team read its partial sums
+  float *sg = s_part + rr * kD;  // the team's Sg, over its (now free) partial sums
+  if (t < kD) sg[t] = Gr;
+  __syncthreads();
+  // sketch term: slice j = t / 128 of the team sums k in [j * 128 / NS, (j + 1) * 128 / NS)
+  float *slices = s_v + rr * NS * kD;
+  if (a.sketch_v) {
+    const bool ok = mbar_wait_bounded(&s_bar, 0, a.error);
+    const int i = t % kD, j = t / kD;
+    float acc = 0.f;
+    if (ok) {
+#pragma unroll 8
+      for (int k = j * (kD / NS); k < (j + 1) * (kD / NS); ++k) acc = fmaf(s_sk[k * kD + i], sg[k], acc);
+    }
+    slices[j * kD + i] = acc;
+  }
+  __syncthreads();
+  float *s_o = s_v + R * NS * kD;  // [R][128]
+  if (t < kD) {
+    float o = Ar;
+    if (a.sketch_v) {
+      float x = 0.f;
+#pragma unroll
+      for (int j = 0; j < NS; ++j) x += slices[j * kD + t];
+      o += (kSqrtHalfPi / kD) * x;
+    }
+    s_o[rr * kD + t] = (Lr > 0.f) ? o / Lr : 0.f;
+  }
+  __syncthreads();
+  // rotate back: the team's first warp
+  if (w == 0 && live) {
     float v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] = s_o[rr * kD + 4 * lane + j];
@@ -520,23 +582,41 @@ __global__ void __launch_bounds__(kCombineRows * 128) combine_tq_kernel(CombineA
   }
 }
 
-size_t combine_smem(const CombineArgs &a) {
-  return sizeof(float) * ((a.sketch_v ? kD * kD : 0) + 2 * kCombineRows * kD);
+// rows per CTA: four when the rows fill the GPU three times over, else fewer, so that the
+// records of few rows spread over more warps
+int combine_rows_per_cta(int rows, int num_sms) {
+  if (num_sms <= 0) num_sms = 1;
+  if (rows >= 3 * num_sms) return 4;
+  if (rows >= (3 * num_sms) / 2) return 2;
+  return 1;
 }
 
-int launch_combine(const CombineArgs &a, cudaStream_t st) {
+size_t combine_smem(const CombineArgs &a, int R) {
+  const int NS = (kCombineThreads / R) / kD;
+  return sizeof(float) * ((a.sketch_v ? kD * kD : 0) + 16 * kPartStride + R * NS * kD + R * kD);
+}
+
+template <int R>
+int launch_combine_r(const CombineArgs &a, cudaStream_t st) {
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(combine_tq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(float) * (kD * kD + 2 * kCombineRows * kD))) != cudaSuccess)
+    if (cudaFuncSetAttribute(combine_tq_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(float) * kD * kD + combine_smem(CombineArgs{}, R))) != cudaSuccess)
       return TQ_ERR_CUDA;
     attr_done = true;
   }
   const int rows = a.batch * a.heads_q;
-  return launch_overlapped(true, combine_tq_kernel, dim3((rows + kCombineRows - 1) / kCombineRows),
-                           dim3(kCombineRows * 128), combine_smem(a), st, a) == cudaSuccess
+  return launch_overlapped(true, combine_tq_kernel<R>, dim3((rows + R - 1) / R), dim3(kCombineThreads),
+                           combine_smem(a, R), st, a) == cudaSuccess
              ? TQ_OK
              : TQ_ERR_CUDA;
+}
+
+int launch_combine(const CombineArgs &a, cudaStream_t st) {
+  const int R = combine_rows_per_cta(a.batch * a.heads_q, a.num_sms);
+  if (R == 4) return launch_combine_r<4>(a, st);
+  if (R == 2) return launch_combine_r<2>(a, st);
+  return launch_combine_r<1>(a, st);
 }
 
 // ---------------------------------------------------------------- decode step
@@ -922,6 +1002,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
                     persist_ctas ? a.tile_prefix : nullptr, persist_ctas, a.heads_kv, G == 1 ? 1 : kPersistGroups};
     cmb.group = G;
     cmb.error = &ctx->dparams->error;
+    cmb.num_sms = ctx->num_sms;
     cmb.rot = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot : nullptr;
     return launch_combine(cmb, st);
   }
@@ -981,6 +1062,7 @@ int launch_decode_tq(const DecodeArgs &a, void *stream) {
   CombineArgs cmb{a.batch, a.heads_q, a.splits, ctx->v.rotate, ctx->v.qjl, a.partials,
                   ctx->dparams->diag, ctx->dparams->sketch, a.out, nullptr, 0, a.heads_kv, 1};
   cmb.error = &ctx->dparams->error;
+  cmb.num_sms = ctx->num_sms;
   cmb.rot = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot : nullptr;
   return launch_combine(cmb, st);
 }
@@ -1002,6 +1084,7 @@ int launch_decode_step_tq(const DecodeArgs &a, const StepArgs &s, void *stream) 
                   ctx->dparams->diag, ctx->dparams->sketch, a.out, a.tile_prefix, persist_ctas, a.heads_kv, 1};
   cmb.group = 1;
   cmb.error = &ctx->dparams->error;
+  cmb.num_sms = ctx->num_sms;
   cmb.rot = ctx->rotation == TQ_ROTATION_DENSE ? ctx->dparams->rot : nullptr;
   return launch_combine(cmb, st);
 }
@@ -1044,6 +1127,7 @@ int launch_decode_kivi(const DecodeArgs &a, void *stream) {
   CombineArgs cmb{a.batch, a.heads_q, a.splits, 0, 0, a.partials, ctx->dparams->diag, ctx->dparams->sketch, a.out,
                   nullptr, 0, a.heads_kv, 1};
   cmb.error = &ctx->dparams->error;
+  cmb.num_sms = ctx->num_sms;
   return launch_combine(cmb, st);
 }
 

@@ -128,6 +128,8 @@ struct Decode2Args {
   // after `records`, the shifted parameter offsets cost the contiguous token loop 5 %.
   const int32_t *btab;
   int pool_blocks;
+  // an upper bound of the tiles the call covers (sizes the persistent grid; 0: one CTA per SM)
+  long long tiles_max;
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -1430,7 +1432,14 @@ int launch_split(const Decode2Args &k, dim3 grid, cudaStream_t st) {
   return launch_overlapped(true, fn, grid, dim3(128), smem, st, k) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
-// persistent launch: one CTA per SM (the workspace's record count assumes no more)
+// persistent grid: one CTA per SM, or one per 4 tiles when the call has fewer (slices start
+// at multiples of 4 tiles, so further CTAs would get nothing and only lengthen the combine)
+inline int persist_grid(const Decode2Args &k, int num_sms) {
+  if (k.tiles_max <= 0) return num_sms;
+  return (int)std::max(1LL, std::min((long long)num_sms, (k.tiles_max + 3) / 4));
+}
+
+// persistent launch: at most one CTA per SM (the workspace's record count assumes no more)
 template <int KB, int VB, bool KQJL, bool VQJL, bool FUSED = false>
 int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st) {
   constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
@@ -1445,7 +1454,7 @@ int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st
       return TQ_ERR_CUDA;
     attr_done[k.btab ? 1 : 0] = true;
   }
-  *ctas = num_sms;
+  *ctas = persist_grid(k, num_sms);
   return launch_overlapped(true, fn, dim3(*ctas), dim3(kPersistWarps * 32), smem, st, k) == cudaSuccess
              ? TQ_OK
              : TQ_ERR_CUDA;
@@ -1463,7 +1472,7 @@ int launch_persist_gqa(const Decode2Args &k, int num_sms, int *ctas, cudaStream_
       return TQ_ERR_CUDA;
     attr_done = true;
   }
-  *ctas = num_sms;
+  *ctas = persist_grid(k, num_sms);
   return launch_overlapped(true, fn, dim3(*ctas), dim3(kPersistWarps * 32), smem, st, k) == cudaSuccess
              ? TQ_OK
              : TQ_ERR_CUDA;
@@ -1481,6 +1490,12 @@ int launch_variant(const Decode2Args &k, bool persist, int num_sms, int *ctas, c
   if (persist) return launch_persist<KB, VB, KQJL, VQJL>(k, num_sms, ctas, st);
   *ctas = 0;
   return launch_split<KB, VB, KQJL, VQJL>(k, dim3(k.splits, k.heads_kv, k.batch), st);
+}
+
+// tiles of a call whose lengths are at most max_len (+ 1 for a decode step's append)
+long long tiles_bound(const DecodeArgs &a) {
+  const long long len = std::min<long long>((long long)a.max_len + 1, a.cache->capacity);
+  return (long long)a.batch * a.heads_kv * ((len + kTT - 1) / kTT);
 }
 
 // Common arguments of the persistent and split-K launches.
@@ -1506,6 +1521,7 @@ Decode2Args decode2_args(const DecodeArgs &a) {
   k.k_centroids = ctx->dparams->k_centroids;
   k.v_centroids = ctx->dparams->v_centroids;
   k.error = &ctx->dparams->error;
+  k.tiles_max = tiles_bound(a);
   return k;
 }
 
@@ -1581,24 +1597,7 @@ int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
     if ((G != 2 && G != 4) || ctx->scheme == TQ_SCHEME_QKQV || !a.tile_prefix || a.batch > kMaxPersistBatch ||
         ctx->num_sms <= 0)
       return TQ_ERR_UNSUPPORTED;
-    const tq_cache *c = a.cache;
-    Decode2Args k{};
-    k.records = c->records;
-    k.bb = ctx->lay.bb;
-    k.cap16 = cap16_of(c->capacity);
-    k.btab = c->block_table;
-    k.pool_blocks = c->pool_blocks;
-    k.capacity = c->capacity;
-    k.batch = a.batch;
-    k.heads_kv = a.heads_kv;
-    k.heads_q = a.heads_q;
-    k.seq_lens = a.seq_lens;
-    k.tile_prefix = a.tile_prefix;
-    k.qprep = a.qprep;
-    k.partials = a.partials;
-    k.k_centroids = ctx->dparams->k_centroids;
-    k.v_centroids = ctx->dparams->v_centroids;
-    k.error = &ctx->dparams->error;
+    const Decode2Args k = decode2_args(a);
     cudaStream_t st = (cudaStream_t)stream;
     const int kb = ctx->k.bits, ns = ctx->num_sms;
     if (ctx->scheme == TQ_SCHEME_KV) {
@@ -1616,26 +1615,7 @@ int launch_decode2_g1(const DecodeArgs &a, int *persist_ctas, void *stream) {
   // whole blocks of the records, which are 16-byte aligned
   const bool persist = a.tile_prefix != nullptr && a.batch <= kMaxPersistBatch && ctx->num_sms > 0;
   if (!persist && a.chunk % kBlockTokens) return TQ_ERR_UNSUPPORTED;
-  const tq_cache *c = a.cache;
-  Decode2Args k{};
-  k.records = c->records;
-  k.bb = ctx->lay.bb;
-  k.cap16 = cap16_of(c->capacity);
-  k.btab = c->block_table;
-  k.pool_blocks = c->pool_blocks;
-  k.capacity = c->capacity;
-  k.batch = a.batch;
-  k.heads_kv = a.heads_kv;
-  k.heads_q = a.heads_q;
-  k.chunk = a.chunk;
-  k.splits = a.splits;
-  k.seq_lens = a.seq_lens;
-  k.tile_prefix = a.tile_prefix;
-  k.qprep = a.qprep;
-  k.partials = a.partials;
-  k.k_centroids = ctx->dparams->k_centroids;
-  k.v_centroids = ctx->dparams->v_centroids;
-  k.error = &ctx->dparams->error;
+  const Decode2Args k = decode2_args(a);
   cudaStream_t st = (cudaStream_t)stream;
   const int kb = ctx->k.bits, ns = ctx->num_sms;
   int *pc = persist_ctas;
