@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(bulk_threads<QJL>(), 1)
       const uint32_t sa_x = smem_u32(smem + G::x0), sa_h = smem_u32(smem + G::hd), sa_s = smem_u32(smem + G::sk);
       auto sketch = [&](long long k) -> bool {
         const int g = (int)(k % NG);
-        if (!mbar_wait_bounded(&r_full[g], (uint32_t)((k / NG) & 1), a.error)) return false;
+        if (!mbar_wait_bounded(&r_full[g], (uint32_t)((k / NG) & 1), a.error)) return false;  // (already complete)
         tc_fence_after_sync();
         const uint32_t d = tbase + G::slot_cols * g;
 #pragma unroll 1
@@ -320,13 +320,10 @@ __global__ void __launch_bounds__(bulk_threads<QJL>(), 1)
         tc_commit(smem_u32(&z_full[g]));
         return true;
       };
-      long long k = 0;
-      for (; ok && k < nloc && !*s_abort; ++k) {
+      // the rotation of tile k into slot k % NG (once the slot is free and the tile has landed),
+      // then the refill of the stage tile k - 1 used (its rotation was issued one round ago)
+      auto rotate = [&](long long k) -> bool {
         const int g = (int)(k % NG), s = (int)(k % NS);
-        if (k >= NG && !mbar_wait_bounded(&s_empty[g], (uint32_t)(((k / NG) - 1) & 1), a.error)) ok = false;
-        if (ok && !mbar_wait_bounded(&x_full[s], (uint32_t)((k / NS) & 1), a.error)) ok = false;
-        if (!ok) break;
-        tc_fence_after_sync();
         const uint32_t d = tbase + G::slot_cols * g;
 #pragma unroll 1
         for (int ks = 0; ks < kD / 16; ++ks) {
@@ -336,18 +333,55 @@ __global__ void __launch_bounds__(bulk_threads<QJL>(), 1)
         }
         tc_commit(smem_u32(&x_empty[s]));
         tc_commit(smem_u32(&y_full[g]));
-        // refill the stage tile k - 1 used (its rotation was issued one round ago)
         if (k >= 1 && loaded < nloc) {
           const int sp = (int)((k - 1) % NS);
-          if (!mbar_wait_bounded(&x_empty[sp], (uint32_t)(((k - 1) / NS) & 1), a.error)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait_bounded(&x_empty[sp], (uint32_t)(((k - 1) / NS) & 1), a.error)) return false;
           load(loaded++);
         }
-        if (QJL && k >= 1 && !sketch(k - 1)) ok = false;
+        return true;
+      };
+      long long k = 0;
+      if constexpr (QJL) {
+        // two streams of work, issued in whichever order they become ready: the sketch of
+        // the oldest rotated tile (once its group has stored the residuals) and the rotation
+        // of the next tile (once its slot is free). Issuing a sketch only after the next
+        // rotation's slot came free would make each group wait for the other's signs.
+        long long kz = 0;  // next tile to sketch (kz < k)
+        uint64_t t_idle = global_ns();
+        while (ok && (k < nloc || kz < k) && !*s_abort) {
+          bool moved = false;
+          if (kz < k && mbar_test_wait(&r_full[kz % NG], (uint32_t)((kz / NG) & 1))) {
+            ok = sketch(kz++);
+            moved = true;
+          }
+          if (ok && k < nloc) {
+            const int g = (int)(k % NG), s = (int)(k % NS);
+            if ((k < NG || mbar_test_wait(&s_empty[g], (uint32_t)(((k / NG) - 1) & 1))) &&
+                mbar_test_wait(&x_full[s], (uint32_t)((k / NS) & 1))) {
+              tc_fence_after_sync();
+              ok = rotate(k++);
+              moved = true;
+            }
+          }
+          if (moved) {
+            t_idle = global_ns();
+          } else if (global_ns() - t_idle > kWaitBudgetNs) {
+            set_error(a.error, TQ_ERR_TIMEOUT);
+            ok = false;
+          } else {
+            __nanosleep(32);
+          }
+        }
+      } else {
+        for (; ok && k < nloc && !*s_abort; ++k) {
+          const int g = (int)(k % NG), s = (int)(k % NS);
+          if (k >= NG && !mbar_wait_bounded(&s_empty[g], (uint32_t)(((k / NG) - 1) & 1), a.error)) ok = false;
+          if (ok && !mbar_wait_bounded(&x_full[s], (uint32_t)((k / NS) & 1), a.error)) ok = false;
+          if (!ok) break;
+          tc_fence_after_sync();
+          ok = rotate(k);
+        }
       }
-      if (ok && QJL && k >= 1 && !*s_abort) ok = sketch(k - 1);
       if (!ok) *s_abort = 1;
       // copies that landed for nobody (an abort) must not outlive the CTA
       for (long long j = k; j < loaded; ++j) mbar_wait_bounded(&x_full[j % NS], (uint32_t)((j / NS) & 1), a.error);
