@@ -41,11 +41,12 @@ CAP = 8192
 # kernels of one decode step (tq_decode_step): the persistent decode kernel, which also
 # appends the step's keys and values and prepares the queries, and the combine
 LAUNCHES_PER_STEP = 2
-# DRAM bytes (read + written) of one launch of the decode-step kernel on this workload, the
-# median over the launches of an ncu launch list of this bench (dram__bytes_read.sum +
-# dram__bytes_write.sum, context 8192); None whenever the kernel has changed since that
-# capture, until it is captured again
-DECODE_TRAFFIC_BYTES = 588_555_264
+# DRAM bytes (read + written) of one launch of the decode-step kernel on this workload: the
+# median over three launches (after three warm-up steps) of one ncu capture of this bench
+# restricted to that kernel (dram__bytes_read.sum + dram__bytes_write.sum, context 8192;
+# profiles/step_launches_kqv4_b16_h32_n8192.md); None whenever the kernel has changed since
+# that capture, until it is captured again
+DECODE_TRAFFIC_BYTES = 588_590_336
 
 
 def peaks():
@@ -421,12 +422,43 @@ def workload_config():
             "parallelism": "replicas"}
 
 
+def run_workload_decode(args, dev):
+    """Decode calls on one of the other workloads, for profiler captures: the GQA long context
+    (32 query heads on 8 KV heads, context 131072, KQV n=3; 113 MB of records) or the KIVI
+    layout study (B8 H40 context 4096, per-channel keys and per-token values; 143 MB)."""
+    import torch
+    from quantised_kv_cache_gb300 import tq
+    from quantised_kv_cache_gb300 import workloads as wl
+    wid = 4 if args.case == "gqa-decode" else 5
+    w = wl.WORKLOADS[wid]
+    B, Hq, H, N = w.batch, w.heads_q, w.heads_kv, w.seq
+    if wid == 5:
+        ctx = tq.Context(128, 2, "KIVI", 42, k_per_channel=True, v_per_token=True)
+    else:
+        ctx = tq.Context(128, w.bits, w.scheme, 42)
+    q, k, v = wl.generate(w, dev)
+    cache = tq.Cache(ctx, B, H, N, device=dev)
+    tq.tq_append_quantize(ctx.handle, cache, k, v, torch.zeros((B,), dtype=torch.int32, device=dev))
+    del k, v
+    lens = torch.full((B,), N, dtype=torch.int32, device=dev)
+    ws = torch.empty(tq.tq_workspace_size(ctx.handle, B, Hq, H, N, w.splits), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        tq.tq_decode_attention(ctx.handle, cache, q, lens, N, w.splits, ws, out)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    print(json.dumps({"case": args.case, "ok": True}), flush=True)
+
+
 def run_small_case(args, dev):
     """A smaller instance of the Llama-2-7B-shaped workload for profiler captures:
     B16 H32 context 4096 (294 MB of compressed records, 537 MB of bf16 K/V)."""
     import torch
     from quantised_kv_cache_gb300 import tq
     from quantised_kv_cache_gb300 import workloads as wl
+    if args.case in ("gqa-decode", "kivi-decode"):
+        run_workload_decode(args, dev)
+        return
     w = wl.WORKLOADS[2]
     N = 4096
     B, H = w.batch, w.heads_kv
@@ -573,9 +605,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table of the N=1 line")
-    ap.add_argument("--case", choices=["step", "decode-small", "append-small", "configs"], default="step",
+    ap.add_argument("--case", choices=["step", "decode-small", "append-small", "gqa-decode", "kivi-decode", "configs"],
+                    default="step",
                     help="step: the benchmark; *-small: one kernel family on B16 H32 N4096 (294 MB of records, "
-                         "above L2) for profiler captures")
+                         "above L2) for profiler captures; gqa-decode / kivi-decode: decode calls of the GQA "
+                         "and KIVI workloads, for profiler captures")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

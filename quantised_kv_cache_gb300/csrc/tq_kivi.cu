@@ -16,6 +16,8 @@
 
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "tq_device.cuh"
 
 namespace tq {
@@ -50,17 +52,57 @@ __device__ __forceinline__ void kivi_load(const KiviTensorArgs &a, long long bh,
   }
 }
 
-__device__ __forceinline__ void group_stats(float mn, float mx, __half &z, __half &s) {
-  z = __float2half_rn(mn);
-  s = __double2half(((double)mx - (double)mn) / 3.0);
+// The step fp16((max - min) / 3) with the quotient taken in fp64 and then rounded to fp16
+// (mx >= mn), without fp64 division, which this GPU runs at a small fraction of its fp32
+// rate. D = mx - mn is held exactly as d + e (two-sum). The fp32 quotient d / 3 lies within
+// 2^-23 of D / 3, so its nearest fp16 value c is the answer or one of its neighbours; the
+// exact sign of D - 3m at the midpoints m between c and its neighbours decides (3m has at
+// most 14 significant bits, and d - 3m is exact because d and 3m are within a factor of 2),
+// ties going to the even value as they do from an fp64 quotient that lands on a midpoint.
+// Where D - 3m is nonzero but within the fp64 quotient's own rounding error of zero, that
+// rounding could itself land on the midpoint: those groups, and quotients outside the
+// normal fp16 range, take the fp64 path.
+__device__ __forceinline__ __half kivi_step(float mn, float mx) {
+  const float d = __fsub_rn(mx, mn);
+  const float bv = __fsub_rn(d, mx);
+  const float av = __fsub_rn(d, bv);
+  const float e = __fadd_rn(__fsub_rn(mx, av), __fsub_rn(-mn, bv));
+  const float q = __fdiv_rn(d, 3.f);
+  if (!(q >= 0x1p-13f && q <= 60000.f)) return __double2half(((double)mx - (double)mn) / 3.0);
+  const __half c = __float2half_rn(q);
+  const unsigned short cb = __half_as_ushort(c);
+  const float cf = __half2float(c);
+  const float up = __half2float(__ushort_as_half((unsigned short)(cb + 1)));
+  const float dn = __half2float(__ushort_as_half((unsigned short)(cb - 1)));
+  const float mu = __fmul_rn(__fadd_rn(cf, up), 0.5f), ml = __fmul_rn(__fadd_rn(cf, dn), 0.5f);
+  const float tu = __fadd_rn(__fsub_rn(d, __fmul_rn(3.f, mu)), e);  // sign of D - 3 mu, exactly
+  const float td = __fadd_rn(__fsub_rn(d, __fmul_rn(3.f, ml)), e);  // sign of D - 3 ml, exactly
+  if ((tu != 0.f && fabsf(tu) <= mu * 0x1p-50f) || (td != 0.f && fabsf(td) <= ml * 0x1p-50f))
+    return __double2half(((double)mx - (double)mn) / 3.0);
+  unsigned short r = cb;
+  if (tu > 0.f || (tu == 0.f && (cb & 1u))) r = (unsigned short)(cb + 1);
+  else if (td < 0.f || (td == 0.f && (cb & 1u))) r = (unsigned short)(cb - 1);
+  return __ushort_as_half(r);
 }
 
-__device__ __forceinline__ uint32_t kivi_code(float x, float z, float s) {
-  if (!(s > 0.f)) return 0u;
-  float t = rintf((x - z) / s);
-  t = fminf(fmaxf(t, 0.f), 3.f);
+__device__ __forceinline__ void group_stats(float mn, float mx, __half &z, __half &s) {
+  z = __float2half_rn(mn);
+  s = kivi_step(mn, mx);
+}
+
+// code = clamp(rint((x - z) / s), 0, 3), ties to even, with the division as a product by
+// inv = 1 / s (0 when s = 0, which makes every code 0). The product is within a few fp32 ulps
+// of the quotient, so it decides the code except near a rounding boundary; there, and at
+// exact ties (frequent when x and z carry few significant bits), the correctly rounded
+// quotient decides.
+__device__ __forceinline__ uint32_t kivi_code(float x, float z, float s, float inv) {
+  const float dx = x - z;
+  float t = dx * inv;
+  if (fabsf(t - floorf(t) - 0.5f) < 0x1p-16f) t = __fdiv_rn(dx, s);
+  t = fminf(fmaxf(rintf(t), 0.f), 3.f);
   return (uint32_t)t;
 }
+__device__ __forceinline__ float kivi_inv(float s) { return (s > 0.f) ? 1.f / s : 0.f; }
 
 // one warp per (batch, head, group of 32 tokens); lane owns channels 4L..4L+3
 __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, int units_per_bh) {
@@ -92,7 +134,7 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
       mx[c] = fmaxf(mx[c], x[c]);
     }
   }
-  float zf[4], sf[4];
+  float zf[4], sf[4], inv[4];
   uint32_t st[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -100,6 +142,7 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
     group_stats(mn[c], mx[c], z, s);
     zf[c] = __half2float(z);
     sf[c] = __half2float(s);
+    inv[c] = kivi_inv(sf[c]);
     st[c] = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
   }
   uint4 *srec = reinterpret_cast<uint4 *>(a.stats + (((size_t)bh * (a.capacity / kG) + g) * kD) * 2);
@@ -110,7 +153,7 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
     kivi_load(a, bh, n0, j, lane, x);
     uint32_t field = 0;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf[c], sf[c]) << (2 * c);
+    for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf[c], sf[c], inv[c]) << (2 * c);
     const uint32_t word = kivi_pack_word(field, lane);
     if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + ((size_t)bh * a.capacity + j) * (kD / 4))[lane] = word;
   }
@@ -142,10 +185,10 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, in
   }
   __half z, s;
   group_stats(mn, mx, z, s);
-  const float zf = __half2float(z), sf = __half2float(s);
+  const float zf = __half2float(z), sf = __half2float(s), inv = kivi_inv(sf);
   uint32_t field = 0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf, sf) << (2 * c);
+  for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf, sf, inv) << (2 * c);
   const uint32_t word = kivi_pack_word(field, lane);
   const size_t slot = (size_t)bh * a.capacity + j;
   if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + slot * (kD / 4))[lane] = word;
@@ -155,13 +198,16 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, in
   }
 }
 
-// one warp per (batch, head, new token): window tokens go to the bf16 ring
-__global__ void __launch_bounds__(256) kivi_window_write(KiviTensorArgs a) {
+// one warp per (batch, head, new token t >= t_first): window tokens go to the bf16 ring.
+// Tokens j < nq(n1) are quantised, and nq(n1) > n1 - W - G, so only the last W + G - 1 new
+// tokens can stay in the window: t_first = max(0, n_new - (W + G - 1)).
+__global__ void __launch_bounds__(256) kivi_window_write(KiviTensorArgs a, int t_first) {
   const int lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const long long bh = unit / a.n_new;
+  const int span = a.n_new - t_first;
+  const long long bh = unit / span;
   if (bh >= (long long)a.batch * a.heads) return;
-  const int t = (int)(unit % a.n_new);
+  const int t = t_first + (int)(unit % span);
   const int b = (int)(bh / a.heads);
   const int n0 = __ldg(a.seq_lens + b);
   const int n1 = n0 + a.n_new;
@@ -230,8 +276,9 @@ int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   if (per_channel) kivi_flush_per_channel<<<blocks, 256, 0, st>>>(t, units);
   else kivi_flush_per_token<<<blocks, 256, 0, st>>>(t, units);
-  const long long wwarps = bh * t.n_new;
-  kivi_window_write<<<(unsigned)((wwarps + 7) / 8), 256, 0, st>>>(t);
+  const int t_first = std::max(0, t.n_new - (t.window + kG - 1));
+  const long long wwarps = bh * (t.n_new - t_first);
+  kivi_window_write<<<(unsigned)((wwarps + 7) / 8), 256, 0, st>>>(t, t_first);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

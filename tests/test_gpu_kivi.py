@@ -136,3 +136,57 @@ def test_kivi_capacity_error():
     lens = torch.zeros((B,), dtype=torch.int32, device=DEV)
     tq.tq_append_quantize(ctx.handle, cache, k.to(DEV), v.to(DEV), lens)
     assert tq.tq_get_device_error(ctx.handle) == tq.TQ_ERR_CAPACITY
+
+
+def _tie_groups(n_groups, seed):
+    """fp32 rows of 32 values whose range makes (max - min) / 3 an exact fp16 midpoint (a tie
+    of the step's rounding), lands just beside one, or is tiny / huge, mixed with ordinary
+    groups: the step must come out as fp16 of the fp64 quotient in every case."""
+    g = np.random.default_rng(seed)
+    rows = []
+    for i in range(n_groups):
+        kind = i % 6
+        k, e = int(g.integers(1024, 2048)), int(g.integers(-12, 10))
+        m = (k + 0.5) * 2.0 ** (e - 10)  # an fp16 midpoint
+        lo = np.float32(g.standard_normal() * 2.0 ** e)
+        if kind == 0:
+            rng_ = 3.0 * m
+        elif kind == 1:
+            rng_ = 3.0 * m * (1 + 2.0 ** -21)
+        elif kind == 2:
+            rng_ = 3.0 * m * (1 - 2.0 ** -21)
+        elif kind == 3:
+            rng_ = 3.0 * 2.0 ** -20 * float(g.uniform(1, 2))  # a quotient below the normal fp16 range
+        elif kind == 4:
+            rng_ = 3.0 * 70000.0  # a quotient above the largest fp16
+        else:
+            rng_ = float(np.exp(g.normal()))
+        hi = np.float32(np.float64(lo) + rng_)
+        row = lo + (hi - lo) * g.uniform(0, 1, 32).astype(np.float32)
+        row[0], row[1] = lo, hi
+        rows.append(row.astype(np.float32))
+    return np.stack(rows)
+
+
+def test_kivi_step_rounding_ties_match_the_fp64_quotient():
+    # V per token: each token is four groups of 32 channels; 800 groups in 200 tokens
+    B, H, N = 1, 1, 200 + 128
+    x = _tie_groups(4 * N, seed=4).reshape(1, 1, N, 128)
+    k = torch.from_numpy(np.random.default_rng(1).standard_normal((B, H, N, 128)).astype(np.float32))
+    v = torch.from_numpy(x)
+    ctx = tq.Context(128, 2, "KIVI", 0, k_per_channel=True, v_per_token=True)
+    cache = tq.Cache(ctx, B, H, 352)
+    _fill(ctx, cache, k, v, [N])
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    _check_tensor(cache, "v", v, False, B, H, N)
+    # and per channel: the same values laid along tokens (groups of 32 tokens per channel)
+    xt = _tie_groups(128 * 10, seed=5).reshape(128, 10, 32).transpose(1, 2, 0).reshape(1, 1, 320, 128)
+    N2 = 320 + 128
+    k2 = np.concatenate([xt, np.random.default_rng(2).standard_normal((1, 1, 128, 128)).astype(np.float32)], axis=2)
+    ctx2 = tq.Context(128, 2, "KIVI", 0, k_per_channel=True, v_per_token=True)
+    cache2 = tq.Cache(ctx2, B, H, 480)
+    _fill(ctx2, cache2, torch.from_numpy(np.ascontiguousarray(k2)), torch.from_numpy(np.ascontiguousarray(k2)), [N2])
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx2.handle) == 0
+    _check_tensor(cache2, "k", torch.from_numpy(np.ascontiguousarray(k2)), True, B, H, N2)
