@@ -1052,8 +1052,7 @@ struct GeoQ {
 template <typename Q, int KB, int VB, bool VQJL, int G>
 __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const unsigned char *smem, int wtile, int t0,
                                               int t_end, int lane, const uint32_t (&bk)[8][2], float &m_run,
-                                              float &l_run, float &w_run, float (&acc_v)[8][4],
-                                              float (&acc_s)[8][4]) {
+                                              float &l_run, float &w_run, float (&acc)[8][4]) {
   const int g = lane >> 2, t4 = lane & 3, h = g >> 1;
   st += (wtile >> 4) * Q::block;  // the warp's block of the stage (see tile_body)
   constexpr int wbase = 0;
@@ -1104,15 +1103,15 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc_v[mb][j] *= scale;
-        if (VQJL) acc_s[mb][j] *= scale;
-      }
+      for (int j = 0; j < 4; ++j) acc[mb][j] *= scale;
     m_run = m_new;
   }
   l_run += p0 + p1;
-  // ---- B operands: column 2h + part of lane (g, t) = hi / lo of head h's weights of tokens
-  // 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1); token j of head h sits on lane 4 (j % 8) + h
+  // ---- B operands, column g of lane (g, t), tokens 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1); token j
+  // of head h sits on lane 4 (j % 8) + h. Without signs: column 2h + part = the hi / lo part of
+  // head h's weights p nu, one MMA per 16 coordinates. With signs: column 2h = head h's values,
+  // 2h + 1 its signs, each filled by two MMAs (hi, then lo parts of p nu or p rho) into one
+  // accumulator -- twice the MMAs of two hi / lo accumulators, half their registers.
   auto hl2 = [](float a, float b, uint32_t &hi, uint32_t &lo) {
     const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
     hi = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
@@ -1120,26 +1119,31 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
          ((uint32_t)__half_as_ushort(__float2half_rn(b - __half2float(hb))) << 16);
   };
   const int src0 = 4 * (2 * t4) + h, src1 = 4 * (2 * t4 + 1) + h;
-  const bool live = g < 2 * G, lo_part = (g & 1) != 0;
-  auto gather = [&](uint32_t xh, uint32_t xl, uint32_t &b0, uint32_t &b1) {
+  const bool live = g < 2 * G, odd = (g & 1) != 0;
+  // the hi and lo fragments of one weight kind; `mine`: this lane's column takes that kind
+  auto gather = [&](uint32_t xh, uint32_t xl, bool mine, uint32_t (&bh)[2], uint32_t (&bl)[2]) {
     const uint32_t a_h = __shfl_sync(kFull, xh, src0), a_l = __shfl_sync(kFull, xl, src0);
     const uint32_t c_h = __shfl_sync(kFull, xh, src1), c_l = __shfl_sync(kFull, xl, src1);
-    const uint32_t a = lo_part ? a_l : a_h, c = lo_part ? c_l : c_h;
-    b0 = live ? __byte_perm(a, c, 0x5410u) : 0u;  // tokens 2t, 2t+1
-    b1 = live ? __byte_perm(a, c, 0x7632u) : 0u;  // tokens 2t+8, 2t+9
+    bh[0] = mine ? __byte_perm(a_h, c_h, 0x5410u) : 0u;  // tokens 2t, 2t+1
+    bh[1] = mine ? __byte_perm(a_h, c_h, 0x7632u) : 0u;  // tokens 2t+8, 2t+9
+    bl[0] = mine ? __byte_perm(a_l, c_l, 0x5410u) : 0u;
+    bl[1] = mine ? __byte_perm(a_l, c_l, 0x7632u) : 0u;
   };
-  uint32_t bv0, bv1, bs0 = 0, bs1 = 0;
+  uint32_t bvh[2], bvl[2], bsh[2] = {0u, 0u}, bsl[2] = {0u, 0u};
+  uint32_t bv0, bv1;
   {
     const float *vn = reinterpret_cast<const float *>(st + Q::off_vn);
     uint32_t xh, xl;
     hl2(v0 ? p0 * vn[tok0] : 0.f, v1 ? p1 * vn[tok1] : 0.f, xh, xl);
-    gather(xh, xl, bv0, bv1);
+    gather(xh, xl, live && (VQJL ? !odd : true), bvh, bvl);
+    bv0 = odd ? bvl[0] : bvh[0];  // without signs: hi / lo by column parity
+    bv1 = odd ? bvl[1] : bvh[1];
     if (VQJL) {
       const float *vr = reinterpret_cast<const float *>(st + Q::off_vr);
       const float r0 = v0 ? p0 * vr[tok0] : 0.f, r1 = v1 ? p1 * vr[tok1] : 0.f;
       w_run += r0 + r1;
       hl2(r0, r1, xh, xl);
-      gather(xh, xl, bs0, bs1);
+      gather(xh, xl, live && odd, bsh, bsl);
     }
   }
   // ---- values: as in the one-head body (pair-table A fragments), G heads in the columns
@@ -1165,7 +1169,13 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
       // A fragment: rows coordinates 16 mb + g, 16 mb + 8 + g; columns the token pairs
-      mma_16816(acc_v[mb], lut(w0, 2 * mb), lut(w0, 2 * mb + 1), lut(w1, 2 * mb), lut(w1, 2 * mb + 1), bv0, bv1);
+      const uint32_t a0 = lut(w0, 2 * mb), a1 = lut(w0, 2 * mb + 1), a2 = lut(w1, 2 * mb), a3 = lut(w1, 2 * mb + 1);
+      if (VQJL) {
+        mma_16816(acc[mb], a0, a1, a2, a3, bvh[0], bvh[1]);
+        mma_16816(acc[mb], a0, a1, a2, a3, bvl[0], bvl[1]);
+      } else {
+        mma_16816(acc[mb], a0, a1, a2, a3, bv0, bv1);
+      }
     }
   }
   // ---- QJL signs (same operands as the one-head body), separate accumulator
@@ -1188,7 +1198,8 @@ __device__ __forceinline__ void tile_body_gqa(const unsigned char *st, const uns
       const uint32_t a1 = pick(2 * mb + 1, sa, sar5, sar10, sar27);
       const uint32_t a2 = pick(2 * mb, sb, sbr5, sbr10, sbr27);
       const uint32_t a3 = pick(2 * mb + 1, sb, sbr5, sbr10, sbr27);
-      mma_16816(acc_s[mb], a0, a1, a2, a3, bs0, bs1);
+      mma_16816(acc[mb], a0, a1, a2, a3, bsh[0], bsh[1]);
+      mma_16816(acc[mb], a0, a1, a2, a3, bsl[0], bsl[1]);
     }
   }
 }
@@ -1339,11 +1350,11 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
         s_q[e] = __ldg(a.qprep + (size_t)unit_of(se) * G * 2 * kD + (size_t)(e / kD) * 2 * kD + (e % kD));
 
     float m_run = -INFINITY, l_run = 0.f, w_run = 0.f;
-    float acc_v[8][4], acc_s[8][4];
+    float acc[8][4];
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc_v[mb][j] = acc_s[mb][j] = 0.f;
+      for (int j = 0; j < 4; ++j) acc[mb][j] = 0.f;
     for (int t = gseg + ((grp - ((gseg - g0) & 3)) & 3); t < se; t += kPersistGroups) {
       const int i = t - g0;
       const int stage = i % S;
@@ -1351,7 +1362,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
       bad = __any_sync(kFull, bad);
       if (!bad)
         tile_body_gqa<Q, KB, VB, VQJL, G>(s_stage + stage * Q::stage, smem, qtr * 16, (t - us) * kTT, len, lane,
-                                          bk, m_run, l_run, w_run, acc_v, acc_s);
+                                          bk, m_run, l_run, w_run, acc);
       __syncwarp();
       if (cur_i < nloc) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1378,12 +1389,15 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
         }
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
-          dst[4 + 16 * mb + g] = acc_v[mb][0] + acc_v[mb][1];
-          dst[4 + 16 * mb + 8 + g] = acc_v[mb][2] + acc_v[mb][3];
-          if (VQJL) {
+          if (VQJL) {  // columns 2t (values) and 2t + 1 (signs, rows in the sign MMA's order)
+            dst[4 + 16 * mb + g] = acc[mb][0];
+            dst[4 + 16 * mb + 8 + g] = acc[mb][2];
             const int c0 = 64 * (g & 1) + 8 * mb + 2 * (g >> 1);
-            dst[4 + kD + c0] = (acc_s[mb][0] + acc_s[mb][1]) * sign_unscale(sign_land(2 * mb));
-            dst[4 + kD + c0 + 1] = (acc_s[mb][2] + acc_s[mb][3]) * sign_unscale(sign_land(2 * mb + 1));
+            dst[4 + kD + c0] = acc[mb][1] * sign_unscale(sign_land(2 * mb));
+            dst[4 + kD + c0 + 1] = acc[mb][3] * sign_unscale(sign_land(2 * mb + 1));
+          } else {  // columns 2t, 2t + 1: hi and lo parts of the values
+            dst[4 + 16 * mb + g] = acc[mb][0] + acc[mb][1];
+            dst[4 + 16 * mb + 8 + g] = acc[mb][2] + acc[mb][3];
           }
         }
       }
