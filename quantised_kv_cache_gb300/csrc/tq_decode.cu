@@ -113,27 +113,48 @@ __global__ void __launch_bounds__(128) qprep_kernel(PrepArgs a) {
       if (lane == 0) a.qprep[(size_t)row * 2 * kD + kD + k] = p * kInvSqrtD;
     }
   }
-  if (!a.sketch_k) return;
+  if (!a.sketch_k) return;  // (uniform over the grid)
 #pragma unroll
   for (int j = 0; j < 4; ++j) s_q[warp][4 * lane + j] = v[j];
-  __syncwarp();
-  // (S q_rot)_k for the four sketch rows k = 8 (lane / 2) + 2 m + (lane & 1), each row's
-  // column i read from the transposed copy in one coalesced 512-byte line per i
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int i = 0; i < kD; ++i) {
-    const float qi = s_q[warp][i];
+  __syncthreads();
+  // (S q_rot)_k for the four sketch rows k = 8 (lane / 2) + 2 m + (lane & 1) of the block's four
+  // query rows: warp w sums columns i in [32 w, 32 w + 32), each column read from the transposed
+  // copy in one coalesced 512-byte line, and the four warps' partial sums meet in shared memory
+  // (a warp streaming all 128 lines for one row kept too few loads in flight)
+  __shared__ __align__(16) float s_part[4][4][kD];  // [warp][row][lane-ordered outputs]
+  float acc[4][4] = {};
+#pragma unroll 8
+  for (int ii = 0; ii < 32; ++ii) {
+    const int i = 32 * warp + ii;
     const float4 s4 = __ldg(reinterpret_cast<const float4 *>(a.sketch_tp + (size_t)i * kD) + lane);
-    acc[0] = fmaf(s4.x, qi, acc[0]);
-    acc[1] = fmaf(s4.y, qi, acc[1]);
-    acc[2] = fmaf(s4.z, qi, acc[2]);
-    acc[3] = fmaf(s4.w, qi, acc[3]);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float qi = s_q[r][i];
+      acc[r][0] = fmaf(s4.x, qi, acc[r][0]);
+      acc[r][1] = fmaf(s4.y, qi, acc[r][1]);
+      acc[r][2] = fmaf(s4.z, qi, acc[r][2]);
+      acc[r][3] = fmaf(s4.w, qi, acc[r][3]);
+    }
   }
-  if (live) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    reinterpret_cast<float4 *>(s_part[warp][r])[lane] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  __syncthreads();
+  if (live) {  // warp w finishes row w of the block
     const float c = kSqrtHalfPi / kD * kInvSqrtD;
+    float4 t = reinterpret_cast<const float4 *>(s_part[0][warp])[lane];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      const float4 u = reinterpret_cast<const float4 *>(s_part[w][warp])[lane];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const float o[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
     for (int m = 0; m < 4; ++m)
-      a.qprep[(size_t)row * 2 * kD + kD + 8 * (lane >> 1) + 2 * m + (lane & 1)] = acc[m] * c;
+      a.qprep[(size_t)row * 2 * kD + kD + 8 * (lane >> 1) + 2 * m + (lane & 1)] = o[m] * c;
   }
 }
 
