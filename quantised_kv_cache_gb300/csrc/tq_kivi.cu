@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
     mn[c] = INFINITY;
     mx[c] = -INFINITY;
   }
+  // (unrolled so that eight rows' loads are in flight at a time)
+#pragma unroll 8
   for (int k = 0; k < kG; ++k) {
     float x[4];
     kivi_load(a, bh, n0, g * kG + k, lane, x);
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
   }
   uint4 *srec = reinterpret_cast<uint4 *>(a.stats + (((size_t)bh * (a.capacity / kG) + g) * kD) * 2);
   srec[lane] = make_uint4(st[0], st[1], st[2], st[3]);
+#pragma unroll 8
   for (int k = 0; k < kG; ++k) {
     const int j = g * kG + k;
     float x[4];
@@ -159,7 +162,9 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
   }
 }
 
-// one warp per (batch, head, token); groups are 32 channels = 8 lanes
+// one warp per (batch, head, run of kTokRun consecutive tokens); groups are 32 channels = 8
+// lanes. The run's rows are loaded before any is coded, so a warp has several loads in flight.
+constexpr int kTokRun = 4;
 __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, int units_per_bh) {
   const int lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -172,29 +177,38 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, in
     if (lane == 0 && unit % units_per_bh == 0) set_error(a.error, TQ_ERR_CAPACITY);
     return;
   }
-  const int j = kivi_nq(n0, a.window) + (int)(unit % units_per_bh);
-  if (j >= kivi_nq(n1, a.window)) return;
-  float x[4];
-  kivi_load(a, bh, n0, j, lane, x);
-  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  const int j0 = kivi_nq(n0, a.window) + kTokRun * (int)(unit % units_per_bh);
+  const int jend = kivi_nq(n1, a.window);
+  if (j0 >= jend) return;
+  float x[kTokRun][4];
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  for (int r = 0; r < kTokRun; ++r) {
+    if (j0 + r < jend) kivi_load(a, bh, n0, j0 + r, lane, x[r]);
   }
-  __half z, s;
-  group_stats(mn, mx, z, s);
-  const float zf = __half2float(z), sf = __half2float(s), inv = kivi_inv(sf);
-  uint32_t field = 0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf, sf, inv) << (2 * c);
-  const uint32_t word = kivi_pack_word(field, lane);
-  const size_t slot = (size_t)bh * a.capacity + j;
-  if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + slot * (kD / 4))[lane] = word;
-  if ((lane & 7) == 0) {
-    const uint32_t st = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
-    reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[lane >> 3] = st;
+  for (int r = 0; r < kTokRun; ++r) {
+    const int j = j0 + r;
+    if (j >= jend) break;  // warp-uniform
+    float mn = fminf(fminf(x[r][0], x[r][1]), fminf(x[r][2], x[r][3]));
+    float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    }
+    __half z, s;
+    group_stats(mn, mx, z, s);
+    const float zf = __half2float(z), sf = __half2float(s), inv = kivi_inv(sf);
+    uint32_t field = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) field |= kivi_code(x[r][c], zf, sf, inv) << (2 * c);
+    const uint32_t word = kivi_pack_word(field, lane);
+    const size_t slot = (size_t)bh * a.capacity + j;
+    if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + slot * (kD / 4))[lane] = word;
+    if ((lane & 7) == 0) {
+      const uint32_t st = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
+      reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[lane >> 3] = st;
+    }
   }
 }
 
@@ -271,7 +285,7 @@ int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
   const long long bh = (long long)t.batch * t.heads;
   // groups (or tokens) newly quantised by one append: at most (n_new + G - 1) tokens
   const int max_tokens = t.n_new + kG - 1;
-  const int units = per_channel ? (max_tokens + kG - 1) / kG + 1 : max_tokens;
+  const int units = per_channel ? (max_tokens + kG - 1) / kG + 1 : (max_tokens + kTokRun - 1) / kTokRun;
   const long long warps = bh * units;
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   if (per_channel) kivi_flush_per_channel<<<blocks, 256, 0, st>>>(t, units);
