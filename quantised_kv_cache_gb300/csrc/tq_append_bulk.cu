@@ -9,9 +9,10 @@
 // code is the count of boundaries at or below the coordinate.
 //
 // Per tile of 128 vectors:
-// * one control thread (warp 0) loads the tile with 16 tensor-map copies of
-//   8 x 128 bf16 boxes, which land exactly as the K-major core-matrix layout of
-//   the MMA's A operand (rows past the end read as zeros), into a ring of
+// * one control thread (warp 0) loads the tile with one tensor-map copy of an
+//   8 x 128 x 16 bf16 box (x viewed as [column block][row][8 columns]), which lands
+//   exactly as the K-major core-matrix layout of the MMA's A operand (rows past
+//   the end read as zeros), into a ring of
 //   stages, and issues y = x (H D)^T on the tensor cores (bf16 inputs are
 //   exact, the Hadamard-times-diagonal operand is +-1; fp32 accumulate in
 //   tensor memory, accumulator column n = the coordinate stored at code offset
@@ -86,11 +87,12 @@ struct BulkArgs {
   CellTable cells;  // the role's code-search table
 };
 
-__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -292,9 +294,7 @@ __global__ void __launch_bounds__(bulk_threads<QJL>(), 1)
         const int s = (int)(j % NS);
         mbar_arrive_expect_tx(&x_full[s], kTileBytes);
         const int row0 = (int)((blockIdx.x + j * gridDim.x) * kTV);
-#pragma unroll 1
-        for (int kb = 0; kb < kD / 8; ++kb)
-          tma_load_2d(smem + G::x0 + s * kTileBytes + kb * 2048, &xmap, 8 * kb, row0, &x_full[s]);
+        tma_load_3d(smem + G::x0 + s * kTileBytes, &xmap, 0, row0, 0, &x_full[s]);
       };
       long long loaded = 0;
       for (; loaded < NS && loaded < nloc; ++loaded) load(loaded);
@@ -652,14 +652,15 @@ int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   if (total < 2LL * kTV || total > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return TQ_ERR_UNSUPPORTED;
-  // x as a [total][128] bf16 matrix; a box of 8 elements x 128 rows is one column
-  // of 16 core matrices of the MMA's K-major A operand
+  // x, a [total][128] bf16 matrix, seen as [16 column blocks][total rows][8 columns] (strides 16 B
+  // and 256 B): one box of 8 x 128 x 16 lands a whole 128-vector tile as the MMA's K-major A
+  // operand, 16 column blocks of 16 core matrices each, in a single copy
   CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)total};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {8, (cuuint32_t)kTV};
-  const cuuint32_t estr[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.x), dims, strides, box, estr,
+  const cuuint64_t dims[3] = {8, (cuuint64_t)total, (cuuint64_t)kD / 8};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, 16};
+  const cuuint32_t box[3] = {8, (cuuint32_t)kTV, (cuuint32_t)kD / 8};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.x), dims, strides, box, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return TQ_ERR_UNSUPPORTED;
