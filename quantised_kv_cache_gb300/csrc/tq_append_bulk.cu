@@ -85,6 +85,7 @@ struct BulkArgs {
   float sketch_rowmax;
   int *error;
   CellTable cells;  // the role's code-search table
+  FastDiv div_new, div_heads;  // by n_new and by heads (vector indices are below 2^31)
 };
 
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int x, int y, int z,
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(bulk_threads<QJL>(), 1)
     // would otherwise stall the warp at the top of every tile
     auto len_of = [&](long long kk) -> int {
       const long long v = (blockIdx.x + kk * gridDim.x) * kTV + row;
-      return v < a.total ? __ldg(a.seq_lens + (int)((v / a.n_new) / a.heads)) : 0;
+      return v < a.total ? __ldg(a.seq_lens + fast_div(fast_div((uint32_t)v, a.div_new), a.div_heads)) : 0;
     };
     int len_next = (g < nloc) ? len_of(g) : 0;
     for (long long k = g; k < nloc; k += NG) {
@@ -408,8 +409,9 @@ __global__ void __launch_bounds__(bulk_threads<QJL>(), 1)
       if (k + NG < nloc) len_next = len_of(k + NG);
       long long slot = -1;
       if (vec < a.total) {
-        const int t = (int)(vec % a.n_new);
-        const long long bh = vec / a.n_new;
+        const uint32_t bh32 = fast_div((uint32_t)vec, a.div_new);
+        const int t = (int)((uint32_t)vec - bh32 * (uint32_t)a.n_new);
+        const long long bh = bh32;
         if (len >= 0 && len + a.n_new <= a.capacity) slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
         else if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);  // the sequence is skipped whole
       }
@@ -686,6 +688,8 @@ int launch_append_bulk(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.error = a.error;
   const bool is_k = a.centroids == ctx->dparams->k_centroids;
   k.cells = ctx->cells[is_k ? 0 : 1];
+  k.div_new = make_fastdiv((uint32_t)a.n_new);
+  k.div_heads = make_fastdiv((uint32_t)a.heads);
   if (k.cells.stride != (a.role.qjl ? 512 : 256)) return TQ_ERR_UNSUPPORTED;
   const long long ntiles = (total + kTV - 1) / kTV;
   cudaStream_t st = (cudaStream_t)stream;

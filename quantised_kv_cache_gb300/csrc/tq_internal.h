@@ -56,6 +56,32 @@ int launch_rotation_prep(DevParams *dp, void *stream);
 // the dense rotation drawn for `seed` (row-major d x d, y = M u), in double
 bool draw_dense_rotation(uint64_t seed, int d, double *M);
 
+// Unsigned 32-bit division by a divisor fixed for a launch, as one multiply-high, one
+// subtraction, one add and two shifts (Granlund and Montgomery, "Division by Invariant Integers
+// using Multiplication", 1994, section 4): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0),
+// t = umulhi(m, n), for every 32-bit n.
+struct FastDiv {
+  uint32_t d = 1, m = 1, s1 = 0, s2 = 0;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  if (d == 0) d = 1;
+  int l = 0;
+  while (l < 32 && (1ull << l) < d) ++l;
+  f.d = d;
+  f.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+  f.s1 = l < 1 ? (uint32_t)l : 1u;
+  f.s2 = l > 1 ? (uint32_t)(l - 1) : 0u;
+  return f;
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+#endif
+
 struct Role {
   int bits = 0;
   bool rotate = false;
