@@ -683,6 +683,17 @@ __device__ __forceinline__ float kivi_code_f(uint32_t f, int j) {
   return __uint_as_float(0x3F800000u | ((f << (21 - 2 * j)) & 0x600000u));
 }
 
+// The same floats for a lane's four channels, two per lookup: byte `sel` picks (this lane's byte
+// of a record word, moved to bits 8..15 by one byte permute) indexes a lane-replicated table of
+// the 16 nibble values, T[n][lane] = (1 + (n & 3)/4, 1 + (n >> 2)/4), at byte offset
+// n * 256 + lane * 8 (a warp's 32 lookups of one nibble fill two wavefronts, no conflict).
+__device__ __forceinline__ void kivi_codes4(const unsigned char *tab, uint32_t lane8, uint32_t word, uint32_t sel,
+                                            float2 &c01, float2 &c23) {
+  const uint32_t x = __byte_perm(word, 0u, sel);
+  c01 = *reinterpret_cast<const float2 *>(tab + ((x & 0xF00u) | lane8));
+  c23 = *reinterpret_cast<const float2 *>(tab + (((x >> 4) & 0xF00u) | lane8));
+}
+
 // four channels 4L..4L+3 of a window token's bfloat16 row staged in shared memory (64 words)
 __device__ __forceinline__ void kivi_window_row(const uint32_t *row, int lane, float (&x)[4]) {
   const uint2 w = reinterpret_cast<const uint2 *>(row)[lane];
@@ -696,6 +707,7 @@ template <bool KPC, bool VPT, int G>
 __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDecodeKernelArgs a) {
   __shared__ float s_m[kDecodeWarps][G], s_l[kDecodeWarps][G];
   __shared__ float s_acc[kDecodeWarps][G][kD];
+  __shared__ __align__(16) float2 s_nib[16][32];  // kivi_codes4's table
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int len = min(max(__ldg(a.seq_lens + b), 0), a.capacity);
@@ -710,14 +722,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
     const float4 q4 = __ldg(reinterpret_cast<const float4 *>(a.qprep + ((size_t)b * a.heads_q + hk * G + g) * 2 * kD) + lane);
     qv[g][0] = q4.x; qv[g][1] = q4.y; qv[g][2] = q4.z; qv[g][3] = q4.w;
   }
-  float m[G], l[G], acc[G][4];
+  // accumulators of this lane's channels 4L..4L+3 as two pairs (packed fp32 FMAs)
+  float m[G], l[G];
+  float2 acc[G][2];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m[g] = -INFINITY;
     l[g] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[g][j] = 0.f;
+    for (int j = 0; j < 2; ++j) acc[g][j] = make_float2(0.f, 0.f);
   }
+  for (int e = tid; e < 16 * 32; e += kDecodeWarps * 32) {
+    const int n = e >> 5;
+    s_nib[n][e & 31] = make_float2(1.f + 0.25f * (float)(n & 3), 1.f + 0.25f * (float)(n >> 2));
+  }
+  __syncthreads();
+  const unsigned char *nib = reinterpret_cast<const unsigned char *>(&s_nib[0][0]);
+  const uint32_t lane8 = (uint32_t)lane << 3, bsel = 0x4404u | ((uint32_t)(lane & 3) << 4);
   const size_t bh = (size_t)b * a.heads_kv + hk;
   const uint32_t *kc = reinterpret_cast<const uint32_t *>(a.k_codes) + bh * a.capacity * 8;
   const uint32_t *vc = reinterpret_cast<const uint32_t *>(a.v_codes) + bh * a.capacity * 8;
@@ -817,21 +838,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
       for (int jj = 0; jj < kTile; ++jj) {
         const int t = QUANT ? tile + jj : min(tile + jj, t_end - 1);
         if constexpr (QUANT) {
-          const uint32_t f = sb[(t - tile0) * 8 + (lane >> 2)] >> (8 * (lane & 3));
-          float fc[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
+          float2 c01, c23;
+          kivi_codes4(nib, lane8, sb[(t - tile0) * 8 + (lane >> 2)], bsel, c01, c23);
           if (KPC) {
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-              part[g][jj] = fmaf(q4s[g][3], fc[3], fmaf(q4s[g][2], fc[2], fmaf(q4s[g][1], fc[1], fmaf(q4s[g][0], fc[0], cst[g]))));
+            for (int g = 0; g < G; ++g) {
+              float2 d2 = __ffma2_rn(make_float2(q4s[g][0], q4s[g][1]), c01, make_float2(cst[g], 0.f));
+              d2 = __ffma2_rn(make_float2(q4s[g][2], q4s[g][3]), c23, d2);
+              part[g][jj] = d2.x + d2.y;
+            }
           } else {
             // per-token key stats of this lane's channel group: z q_sum + 4 s (sum_j q_j f_j - q_sum)
             float z, sc;
             half2_pair(sb[512 + (t - tile0) * 4 + (lane >> 3)], z, sc);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              const float d = fmaf(qv[g][3], fc[3], fmaf(qv[g][2], fc[2], fmaf(qv[g][1], fc[1], qv[g][0] * fc[0])));
+              float2 d2 = __fmul2_rn(make_float2(qv[g][0], qv[g][1]), c01);
+              d2 = __ffma2_rn(make_float2(qv[g][2], qv[g][3]), c23, d2);
+              const float d = d2.x + d2.y;
               part[g][jj] = fmaf(4.f * sc, d - qsum[g], z * qsum[g]);
             }
           }
@@ -860,16 +884,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
         l[g] = l[g] * scale + psum;
         m[g] = mnew;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[g][j] *= scale;
+        for (int j = 0; j < 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], make_float2(scale, scale));
       }
       // values: p (z + s c) = (4 p s) (1 + c/4) + p (z - 4 s); per-token stats fold into the
       // token's weight, per-channel ones into the tile's sums u_j = sum p (1 + c_j / 4), P = sum p
-      float u[G][4], pz[G];
+      float2 u[G][2];
+      float pz[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         pz[g] = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) u[g][j] = 0.f;
+        u[g][0] = u[g][1] = make_float2(0.f, 0.f);
       }
 #pragma unroll
       for (int jj = 0; jj < kTile; ++jj) {
@@ -879,26 +903,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
 #pragma unroll
         for (int g = 0; g < G; ++g) w[g] = __shfl_sync(kFull, p[g], lane_of_tile_token(jj));
         if constexpr (QUANT) {
-          const uint32_t f = sb[256 + (t - tile0) * 8 + (lane >> 2)] >> (8 * (lane & 3));
-          float fc[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) fc[j] = kivi_code_f(f, j);
+          float2 c01, c23;
+          kivi_codes4(nib, lane8, sb[256 + (t - tile0) * 8 + (lane >> 2)], bsel, c01, c23);
           if (VPT) {
             float z, sc;
             half2_pair(sb[640 + (t - tile0) * 4 + (lane >> 3)], z, sc);
             const float s4 = 4.f * sc, z4 = fmaf(-4.f, sc, z);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              const float w1 = w[g] * s4;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w1, fc[j], acc[g][j]);
+              const float2 w1 = make_float2(w[g] * s4, w[g] * s4);
+              acc[g][0] = __ffma2_rn(w1, c01, acc[g][0]);
+              acc[g][1] = __ffma2_rn(w1, c23, acc[g][1]);
               pz[g] = fmaf(w[g], z4, pz[g]);
             }
           } else {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) u[g][j] = fmaf(w[g], fc[j], u[g][j]);
+              u[g][0] = __ffma2_rn(make_float2(w[g], w[g]), c01, u[g][0]);
+              u[g][1] = __ffma2_rn(make_float2(w[g], w[g]), c23, u[g][1]);
               pz[g] += w[g];
             }
           }
@@ -907,8 +929,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
           kivi_window_row(wb + 512 + jj * 64, lane, x);
 #pragma unroll
           for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(w[g], x[j], acc[g][j]);
+          {
+            acc[g][0] = __ffma2_rn(make_float2(w[g], w[g]), make_float2(x[0], x[1]), acc[g][0]);
+            acc[g][1] = __ffma2_rn(make_float2(w[g], w[g]), make_float2(x[2], x[3]), acc[g][1]);
+          }
         }
       }
       if constexpr (QUANT) {
@@ -916,7 +940,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
         for (int g = 0; g < G; ++g)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            acc[g][j] += VPT ? pz[g] : fmaf(4.f * vscl[j], u[g][j], fmaf(-4.f, vscl[j], vz[j]) * pz[g]);
+          {
+            const float uj = (j & 1) ? u[g][j >> 1].y : u[g][j >> 1].x;
+            const float add = VPT ? pz[g] : fmaf(4.f * vscl[j], uj, fmaf(-4.f, vscl[j], vz[j]) * pz[g]);
+            if (j & 1) acc[g][j >> 1].y += add;
+            else acc[g][j >> 1].x += add;
+          }
       } else {
         __syncwarp();  // every lane is done with the staged rows before the next copies
       }
@@ -936,7 +965,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
       s_l[warp][g] = l[g];
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) s_acc[warp][g][4 * lane + j] = acc[g][j];
+    for (int j = 0; j < 4; ++j) s_acc[warp][g][4 * lane + j] = (j & 1) ? acc[g][j >> 1].y : acc[g][j >> 1].x;
   }
   __syncthreads();
   const int i = tid;
