@@ -81,3 +81,24 @@ def test_static_scratch_rejects_requests_beyond_its_size():
                                              B, H, H, ctypes.c_void_p(lens.data_ptr()), cap, 1024,
                                              ctypes.c_void_p(out.data_ptr()), None)
     assert st == tq.TQ_ERR_WORKSPACE
+
+
+@pytest.mark.skipif(not torch.cuda.is_available() or torch.cuda.device_count() < 2,
+                    reason="needs a second CUDA device")
+def test_static_scratch_refuses_a_call_from_another_device():
+    # the scratch array is looked up on the current device; a call made while another device
+    # is current than the context's is refused before anything is launched
+    from quantised_kv_cache_gb300 import tq
+
+    ctx = tq.Context(128, 4, "KQV", 1)
+    B, H, cap = 1, 2, 64
+    cache = tq.Cache(ctx, B, H, cap, device=torch.device("cuda", 0))
+    q = torch.zeros((B, H, 128), dtype=torch.float32, device="cuda:0")
+    lens = torch.full((B,), 10, dtype=torch.int32, device="cuda:0")
+    out = torch.zeros((B, H, 128), dtype=torch.float32, device="cuda:0")
+    with torch.cuda.device(1):
+        st = tq.lib().tq_decode_attention_static(ctx.handle, ctypes.byref(cache.struct),
+                                                 ctypes.c_void_p(q.data_ptr()), tq.TQ_F32, B, H, H,
+                                                 ctypes.c_void_p(lens.data_ptr()), cap, 0,
+                                                 ctypes.c_void_p(out.data_ptr()), None)
+    assert st == tq.TQ_ERR_ARG
