@@ -675,18 +675,13 @@ __device__ __forceinline__ void half2_pair(uint32_t st, float &z, float &s) {
   s = __half2float(__ushort_as_half((unsigned short)(st >> 16)));
 }
 
-// Code j (0..3) of a lane's 8-bit field f (bits 2j, 2j + 1) as the float 1 + c/4, exactly:
-// its two bits placed in the top of the mantissa of 1.0. A dequantised value z + s c is then
-// 4 s (1 + c/4) + (z - 4 s), so the two stats fold into per-group (or per-token) constants
-// and each code costs a shift, a logic op and one FMA, without an int-to-float conversion.
-__device__ __forceinline__ float kivi_code_f(uint32_t f, int j) {
-  return __uint_as_float(0x3F800000u | ((f << (21 - 2 * j)) & 0x600000u));
-}
-
-// The same floats for a lane's four channels, two per lookup: byte `sel` picks (this lane's byte
-// of a record word, moved to bits 8..15 by one byte permute) indexes a lane-replicated table of
-// the 16 nibble values, T[n][lane] = (1 + (n & 3)/4, 1 + (n >> 2)/4), at byte offset
-// n * 256 + lane * 8 (a warp's 32 lookups of one nibble fill two wavefronts, no conflict).
+// A code c (0..3) enters the arithmetic as the exact float 1 + c/4. A dequantised value
+// z + s c is then 4 s (1 + c/4) + (z - 4 s), so the two stats fold into per-group (or per-token)
+// constants and a code costs no int-to-float conversion. kivi_codes4 gives those floats for a
+// lane's four channels, two per lookup: byte `sel` picks (this lane's byte of a record word,
+// moved to bits 8..15 by one byte permute) indexes a lane-replicated table of the 16 nibble
+// values, T[n][lane] = (1 + (n & 3)/4, 1 + (n >> 2)/4), at byte offset n * 256 + lane * 8 (a
+// warp's 32 lookups of one nibble fill two wavefronts, no conflict).
 __device__ __forceinline__ void kivi_codes4(const unsigned char *tab, uint32_t lane8, uint32_t word, uint32_t sel,
                                             float2 &c01, float2 &c23) {
   const uint32_t x = __byte_perm(word, 0u, sel);
