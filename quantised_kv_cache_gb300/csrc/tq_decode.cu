@@ -675,7 +675,8 @@ __device__ __forceinline__ void half2_pair(uint32_t st, float &z, float &s) {
   s = __half2float(__ushort_as_half((unsigned short)(st >> 16)));
 }
 
-// A code c (0..3) enters the arithmetic as the exact float 1 + c/4. A dequantised value
+// A code c (0..3) enters the arithmetic as the exact float 1 + c/4 (its two bits placed in the
+// top of the mantissa of 1.0). A dequantised value
 // z + s c is then 4 s (1 + c/4) + (z - 4 s), so the two stats fold into per-group (or per-token)
 // constants and a code costs no int-to-float conversion. kivi_codes4 gives those floats for a
 // lane's four channels, two per lookup: byte `sel` picks (this lane's byte of a record word,
@@ -833,8 +834,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kivi_kernel(KiviDeco
       for (int jj = 0; jj < kTile; ++jj) {
         const int t = QUANT ? tile + jj : min(tile + jj, t_end - 1);
         if constexpr (QUANT) {
+          // keys: the code floats by bit placement (two logic ops each) -- the table lookups
+          // that the values use would put the shared-memory path, already the busier one,
+          // further ahead (measured 2 % slower for keys)
           float2 c01, c23;
-          kivi_codes4(nib, lane8, sb[(t - tile0) * 8 + (lane >> 2)], bsel, c01, c23);
+          {
+            const uint32_t f = sb[(t - tile0) * 8 + (lane >> 2)] >> (8 * (lane & 3));
+            auto cf = [&](int j) { return __uint_as_float(0x3F800000u | ((f << (21 - 2 * j)) & 0x600000u)); };
+            c01 = make_float2(cf(0), cf(1));
+            c23 = make_float2(cf(2), cf(3));
+          }
           if (KPC) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
