@@ -97,10 +97,11 @@ __device__ __forceinline__ void group_stats(float mn, float mx, __half &z, __hal
 // quotient decides.
 __device__ __forceinline__ uint32_t kivi_code(float x, float z, float s, float inv) {
   const float dx = x - z;
-  float t = dx * inv;
-  if (fabsf(t - floorf(t) - 0.5f) < 0x1p-16f) t = __fdiv_rn(dx, s);
-  t = fminf(fmaxf(rintf(t), 0.f), 3.f);
-  return (uint32_t)t;
+  const float t = dx * inv;
+  float r = rintf(t);
+  if (fabsf(t - r) > 0.5f - 0x1p-16f) r = rintf(__fdiv_rn(dx, s));  // within 2^-16 of a half-integer
+  r = fminf(fmaxf(r, 0.f), 3.f);
+  return (uint32_t)r;
 }
 __device__ __forceinline__ float kivi_inv(float s) { return (s > 0.f) ? 1.f / s : 0.f; }
 
@@ -183,32 +184,54 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, in
   float x[kTokRun][4];
 #pragma unroll
   for (int r = 0; r < kTokRun; ++r) {
-    if (j0 + r < jend) kivi_load(a, bh, n0, j0 + r, lane, x[r]);
+    if (j0 + r < jend) {
+      kivi_load(a, bh, n0, j0 + r, lane, x[r]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) x[r][c] = 0.f;
+    }
   }
+  // each token's group minima and maxima (a lane's four channels, then the eight lanes of its
+  // group); then lane L computes the step of token (L >> 2) & 3, group L & 3 only, so the
+  // run's sixteen steps take one evaluation instead of one per token
+  float mn[kTokRun], mx[kTokRun];
+#pragma unroll
+  for (int r = 0; r < kTokRun; ++r) {
+    mn[r] = fminf(fminf(x[r][0], x[r][1]), fminf(x[r][2], x[r][3]));
+    mx[r] = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mn[r] = fminf(mn[r], __shfl_xor_sync(kFull, mn[r], o));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], o));
+    }
+  }
+  const int r_me = (lane >> 2) & (kTokRun - 1), src = 8 * (lane & 3);
+  float mn_me = 0.f, mx_me = 0.f;
+#pragma unroll
+  for (int r = 0; r < kTokRun; ++r) {
+    const float lo = __shfl_sync(kFull, mn[r], src), hi = __shfl_sync(kFull, mx[r], src);
+    if (r == r_me) {
+      mn_me = lo;
+      mx_me = hi;
+    }
+  }
+  __half zm, sm;
+  group_stats(mn_me, mx_me, zm, sm);
+  const uint32_t zs_me = (uint32_t)__half_as_ushort(zm) | ((uint32_t)__half_as_ushort(sm) << 16);
 #pragma unroll
   for (int r = 0; r < kTokRun; ++r) {
     const int j = j0 + r;
     if (j >= jend) break;  // warp-uniform
-    float mn = fminf(fminf(x[r][0], x[r][1]), fminf(x[r][2], x[r][3]));
-    float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-    }
-    __half z, s;
-    group_stats(mn, mx, z, s);
-    const float zf = __half2float(z), sf = __half2float(s), inv = kivi_inv(sf);
+    const uint32_t st = __shfl_sync(kFull, zs_me, 4 * r + (lane >> 3));  // this lane's group's step
+    const float zf = __half2float(__ushort_as_half((unsigned short)(st & 0xffffu)));
+    const float sf = __half2float(__ushort_as_half((unsigned short)(st >> 16))), inv = kivi_inv(sf);
     uint32_t field = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) field |= kivi_code(x[r][c], zf, sf, inv) << (2 * c);
     const uint32_t word = kivi_pack_word(field, lane);
     const size_t slot = (size_t)bh * a.capacity + j;
     if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + slot * (kD / 4))[lane] = word;
-    if ((lane & 7) == 0) {
-      const uint32_t st = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
-      reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[lane >> 3] = st;
-    }
+    if ((lane & 7) == 0) reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[lane >> 3] = st;
   }
 }
 
