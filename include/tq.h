@@ -451,6 +451,16 @@ size_t tq_static_scratch_bytes(void);
  * error word into *code (TQ_OK when nothing was recorded). */
 tq_status tq_get_device_error(const tq_ctx *ctx, void *stream, int *code);
 
+/* Self-test of the failure path every kernel's waits share: enqueues on `stream`
+ * one warp that waits on an mbarrier nothing completes, with a budget of
+ * `budget_ns` nanoseconds of %globaltimer time (at most 2e9, the kernels' own
+ * budget). The wait gives up, records TQ_ERR_TIMEOUT in the context's device
+ * error word (read it with tq_get_device_error) and the kernel returns; no copy
+ * or tensor-core operation is in flight, so the context stays usable. The
+ * context's GPU must be current. Errors: TQ_ERR_ARG (null context, budget
+ * above 2e9, another device current), TQ_ERR_CUDA (launch). */
+tq_status tq_selftest_bounded_wait(const tq_ctx *ctx, unsigned long long budget_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

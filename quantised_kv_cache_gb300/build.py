@@ -22,7 +22,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libtq.so")
 
 SOURCES = ["tq_host.cpp", "tq_append.cu", "tq_decode.cu", "tq_dequant.cu", "tq_kivi.cu", "tq_noalloc.cu", "tq_decode2.cu", "tq_append2.cu",
-           "tq_append_tc.cu", "tq_append_small.cu", "tq_append_bulk.cu"]
+           "tq_append_tc.cu", "tq_append_small.cu", "tq_append_bulk.cu", "tq_selftest.cu"]
 HEADERS = ["tq_internal.h", "tq_device.cuh", "tq_ptx.cuh", "tq_tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

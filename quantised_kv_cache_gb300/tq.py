@@ -93,6 +93,7 @@ _SIGNATURES = {
     "tq_decode_attention_static": (_i, [_vp, ctypes.POINTER(tq_cache), _vp, _i, _i, _i, _i, _vp, _i, _i, _vp,
                                         _vp]),
     "tq_static_scratch_bytes": (_sz, []),
+    "tq_selftest_bounded_wait": (_i, [_vp, ctypes.c_ulonglong, _vp]),
 }
 
 _lib = None
@@ -365,6 +366,11 @@ def tq_get_device_error(ctx, stream=None) -> int:
     code = _i()
     check(lib().tq_get_device_error(ctx, _stream(stream), ctypes.byref(code)), "tq_get_device_error")
     return code.value
+
+
+def tq_selftest_bounded_wait(ctx, budget_ns: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (a wait that can only run out)."""
+    check(lib().tq_selftest_bounded_wait(ctx, budget_ns, _stream(stream)), "tq_selftest_bounded_wait")
 
 
 # ----------------------------------------------------------------------------
