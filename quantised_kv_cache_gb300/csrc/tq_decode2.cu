@@ -873,20 +873,37 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     cur_t = r - cur_h * cur_nb;
     cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
   }
-  // paged caches: lane 0 loads the table entry of the cursor's block as soon as the cursor
-  // moves, a tile before its copy is issued, so the copy never waits on the lookup
-  int pf = -1;
-  auto prefetch = [&]() {
-    if (PAGED && lane == 0 && cur_i < nloc && cur_t * kTT + 16 * qtr < cur_len)
-      pf = __ldg(a.btab + ((cur_row + cur_t * kTT + 16 * qtr) >> 4));
+  // paged caches: the table entries of this warp's next 32 copies, one per lane (lane j: the
+  // copy of local tile cur_i + 4 j, as of the refill), loaded together once every 32 copies and
+  // handed out by a shuffle -- a per-copy lookup cost ~34 instructions of branch, address and
+  // load per copy
+  int pf_lane = -1, pf_next = 32;
+  auto refill_entries = [&]() {
+    const int li = cur_i + kPersistGroups * lane;
+    int e = -1;
+    if (li < nloc) {
+      const int g = g0 + li;
+      const int bq = batch_of(g);
+      const int nb = s_pre[bq + 1] - s_pre[bq];
+      const int r = g - H * s_pre[bq];
+      const int hq = r / nb, tq_ = r - hq * nb;
+      const int t0 = tq_ * kTT + 16 * qtr;
+      if (t0 < s_len[bq]) e = __ldg(a.btab + ((((long long)bq * H + hq) * a.cap16 + t0) >> 4));
+    }
+    pf_lane = e;
+    pf_next = 0;
   };
-  prefetch();
   // issue this warp's quarter of local tile cur_i (whole warp), then step the cursor by 4 tiles
   auto issue_next = [&]() {
     const int st = cur_i % S;
     uint64_t *bar = &s_full[st * 4 + qtr];
     const int t0 = cur_t * kTT + 16 * qtr;
     const int n = min(16, cur_len - t0);
+    int pf = -1;
+    if constexpr (PAGED) {
+      if (pf_next == 32) refill_entries();
+      pf = __shfl_sync(kFull, pf_lane, pf_next++);
+    }
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
       if constexpr (PAGED) {
         const uint8_t *src = n > 0 ? pool_block<Gm::block>(a, pf) : nullptr;
@@ -902,7 +919,6 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     cur_i += kPersistGroups;
     cur_t += kPersistGroups;
     if (cur_i < nloc) seek();
-    if constexpr (PAGED) prefetch();
   };
   // query row (= unit: one query head per KV head) of the segment starting at tile g
   auto unit_of = [&](int g) -> int {
