@@ -847,40 +847,15 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
     return lo;
   };
 
-  // refill cursor of this warp (all lanes): local tile cur_i, its tile index cur_t
-  // within its head, that head's tile count, sequence length and slot row
-  int cur_i = grp, cur_b = 0, cur_t = 0, cur_nb = 1, cur_len = 0, cur_h = 0;
-  long long cur_row = 0;
-  auto seek = [&]() {  // normalise cur_t into its head (heads hold >= 1 tile)
-    while (cur_t >= cur_nb) {
-      cur_t -= cur_nb;
-      if (++cur_h == H) {
-        cur_h = 0;
-        do ++cur_b; while (s_pre[cur_b + 1] == s_pre[cur_b]);  // skip empty sequences
-        cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
-        cur_len = s_len[cur_b];
-      }
-      cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
-    }
-  };
-  if (cur_i < nloc) {
-    const int g = g0 + cur_i;
-    cur_b = batch_of(g);
-    cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
-    cur_len = s_len[cur_b];
-    const int r = g - H * s_pre[cur_b];
-    cur_h = r / cur_nb;
-    cur_t = r - cur_h * cur_nb;
-    cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
-  }
-  // paged caches: the table entries of this warp's next 32 copies, one per lane (lane j: the
-  // copy of local tile cur_i + 4 j, as of the refill), loaded together once every 32 copies and
-  // handed out by a shuffle -- a per-copy lookup cost ~34 instructions of branch, address and
-  // load per copy
-  int pf_lane = -1, pf_next = 32;
-  auto refill_entries = [&]() {
+  // the copies of this warp, in batches of 32 (lane j: the copy of local tile cur_i + 4 j as of
+  // the batch's start): each lane works out its tile's head, token range and source block once
+  // (for a paged cache through the block table), and each copy takes its source by a shuffle
+  int cur_i = grp;
+  const uint8_t *src_lane = nullptr;
+  int src_next = 32;
+  auto refill_sources = [&]() {
     const int li = cur_i + kPersistGroups * lane;
-    int e = -1;
+    const uint8_t *p = nullptr;
     if (li < nloc) {
       const int g = g0 + li;
       const int bq = batch_of(g);
@@ -888,37 +863,27 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
       const int r = g - H * s_pre[bq];
       const int hq = r / nb, tq_ = r - hq * nb;
       const int t0 = tq_ * kTT + 16 * qtr;
-      if (t0 < s_len[bq]) e = __ldg(a.btab + ((((long long)bq * H + hq) * a.cap16 + t0) >> 4));
+      if (t0 < s_len[bq]) {  // this quarter holds tokens: its stored block
+        const long long vslot = ((long long)bq * H + hq) * a.cap16 + t0;
+        if constexpr (PAGED) p = pool_block<Gm::block>(a, __ldg(a.btab + (vslot >> 4)));
+        else p = a.records + (vslot >> 4) * Gm::block;
+      }
     }
-    pf_lane = e;
-    pf_next = 0;
+    src_lane = p;
+    src_next = 0;
   };
-  // issue this warp's quarter of local tile cur_i (whole warp), then step the cursor by 4 tiles
+  // issue this warp's quarter of local tile cur_i (whole warp), then step to the group's next tile
   auto issue_next = [&]() {
     const int st = cur_i % S;
     uint64_t *bar = &s_full[st * 4 + qtr];
-    const int t0 = cur_t * kTT + 16 * qtr;
-    const int n = min(16, cur_len - t0);
-    int pf = -1;
-    if constexpr (PAGED) {
-      if (pf_next == 32) refill_entries();
-      pf = __shfl_sync(kFull, pf_lane, pf_next++);
-    }
+    if (src_next == 32) refill_sources();
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(
+        __shfl_sync(kFull, reinterpret_cast<unsigned long long>(src_lane), src_next++));
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
-      if constexpr (PAGED) {
-        const uint8_t *src = n > 0 ? pool_block<Gm::block>(a, pf) : nullptr;
-        mbar_arrive_expect_tx(bar, src ? (uint32_t)Gm::block : 0u);
-        if (src) tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, src, (uint32_t)Gm::block, bar);
-      } else {
-        mbar_arrive_expect_tx(bar, n > 0 ? (uint32_t)Gm::block : 0u);
-        if (n > 0)
-          tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, a.records + ((cur_row + t0) >> 4) * Gm::block,
-                      (uint32_t)Gm::block, bar);
-      }
+      mbar_arrive_expect_tx(bar, src ? (uint32_t)Gm::block : 0u);
+      if (src) tma_load_1d(s_stage + st * Gm::stage + qtr * Gm::block, src, (uint32_t)Gm::block, bar);
     }
     cur_i += kPersistGroups;
-    cur_t += kPersistGroups;
-    if (cur_i < nloc) seek();
   };
   // query row (= unit: one query head per KV head) of the segment starting at tile g
   auto unit_of = [&](int g) -> int {
