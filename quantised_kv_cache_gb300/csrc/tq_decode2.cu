@@ -731,16 +731,11 @@ __device__ __forceinline__ void prep_query(const Decode2Args &a, int lane, float
 
 // Append the new token (one role) of unit u = b * H + h at slot len (the sequence's
 // length before the step, 0 <= len < capacity) by one warp. s_sk: the permuted S^T in
-// shared memory. PAGED: translate the slot through the block table (the contiguous cache's
-// instantiation carries no translation).
-template <bool PAGED>
+// shared memory. A paged cache's slot goes through the block table.
 __device__ __forceinline__ void step_append(const Decode2Args &a, int u, int role, int len, int lane,
                                             const float *s_sk) {
-  long long slot = (long long)u * a.cap16 + len;
-  if constexpr (PAGED) {
-    slot = phys_slot(a.btab, a.pool_blocks, slot, a.error);
-    if (slot < 0) return;  // an unmapped block: nothing appended (the error word says so)
-  }
+  const long long slot = phys_slot(a.btab, a.pool_blocks, (long long)u * a.cap16 + len, a.error);
+  if (slot < 0) return;  // an unmapped block: nothing appended (the error word says so)
   float x[4];
   load4(role ? a.v_new : a.k_new, (size_t)u * kD + 4 * lane, a.kv_bf16 != 0, x);
   const WarpRole &ro = a.role[role];
@@ -774,9 +769,10 @@ constexpr int persist_smem_bytes() {
   return persist_sbar_offset<Gm>() + 8 + 4 * kMaxPersistBatch;  // + the decode step's raw lengths
 }
 
-// PAGED: the cache has a block table (a separate instantiation, so that the contiguous
-// kernel's copy issue stays as short as it can be).
-template <int KB, int VB, bool KQJL, bool VQJL, bool FUSED, bool PAGED>
+// One instantiation serves contiguous and paged caches: the layout only changes where each
+// batch of copy sources is computed (measured: a separate contiguous instantiation ran its
+// tile loop 3.7 % slower).
+template <int KB, int VB, bool KQJL, bool VQJL, bool FUSED>
 __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(Decode2Args a) {
   static_assert(!(FUSED && KQJL), "the decode step prepares queries without a key sketch");
   constexpr int S = persist_stages<KB, VB, KQJL, VQJL>();
@@ -865,7 +861,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
       const int t0 = tq_ * kTT + 16 * qtr;
       if (t0 < s_len[bq]) {  // this quarter holds tokens: its stored block
         const long long vslot = ((long long)bq * H + hq) * a.cap16 + t0;
-        if constexpr (PAGED) p = pool_block<Gm::block>(a, __ldg(a.btab + (vslot >> 4)));
+        if (a.btab) p = pool_block<Gm::block>(a, __ldg(a.btab + (vslot >> 4)));
         else p = a.records + (vslot >> 4) * Gm::block;
       }
     }
@@ -906,7 +902,7 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_kernel(D
       const int gl = H * s_pre[bq] + (hq + 1) * nb - 1;  // the head's last tile
       const int len = s_raw[bq];
       if (nb == 0 || gl < g0 || gl >= g1 || len < 0 || len >= a.capacity) continue;
-      step_append<PAGED>(a, u, j & 1, len, lane, s_sk);
+      step_append(a, u, j & 1, len, lane, s_sk);
       fence_proxy_async_global();  // the records written above, before their bulk copies
     }
     if constexpr (kStepSketch) fence_proxy_async_shared();  // S^T read above, before the ring overwrites it
@@ -1441,13 +1437,12 @@ int launch_persist(const Decode2Args &k, int num_sms, int *ctas, cudaStream_t st
   using Gm = Geo<KB, VB, KQJL, VQJL, kPersistWarps, S>;
   if (k.bb != Gm::block) return TQ_ERR_UNSUPPORTED;
   const size_t smem = persist_smem_bytes<Gm>();
-  auto fn = k.btab ? decode_persist_kernel<KB, VB, KQJL, VQJL, FUSED, true>
-                   : decode_persist_kernel<KB, VB, KQJL, VQJL, FUSED, false>;
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[k.btab ? 1 : 0]) {
+  auto fn = decode_persist_kernel<KB, VB, KQJL, VQJL, FUSED>;
+  static bool attr_done = false;
+  if (!attr_done) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return TQ_ERR_CUDA;
-    attr_done[k.btab ? 1 : 0] = true;
+    attr_done = true;
   }
   *ctas = persist_grid(k, num_sms);
   return launch_overlapped(true, fn, dim3(*ctas), dim3(kPersistWarps * 32), smem, st, k) == cudaSuccess
