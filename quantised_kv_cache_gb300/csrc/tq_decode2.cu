@@ -1233,53 +1233,40 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1) decode_persist_gqa_kern
     return lo;
   };
   using Gs = typename Q::Gs;
-  // per-warp refill cursor, as in the one-head kernel
-  int cur_i = grp, cur_b = 0, cur_t = 0, cur_nb = 1, cur_len = 0, cur_h = 0;
-  long long cur_row = 0;
-  auto seek = [&]() {
-    while (cur_t >= cur_nb) {
-      cur_t -= cur_nb;
-      if (++cur_h == H) {
-        cur_h = 0;
-        do ++cur_b; while (s_pre[cur_b + 1] == s_pre[cur_b]);
-        cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
-        cur_len = s_len[cur_b];
+  // this warp's copies in batches of 32 sources, one per lane, as in the one-head kernel
+  int cur_i = grp;
+  const uint8_t *src_lane = nullptr;
+  int src_next = 32;
+  auto refill_sources = [&]() {
+    const int li = cur_i + kPersistGroups * lane;
+    const uint8_t *p = nullptr;
+    if (li < nloc) {
+      const int gq = g0 + li;
+      const int bq = batch_of(gq);
+      const int nb = s_pre[bq + 1] - s_pre[bq];
+      const int r = gq - H * s_pre[bq];
+      const int hq = r / nb, tq_ = r - hq * nb;
+      const int t0 = tq_ * kTT + 16 * qtr;
+      if (t0 < s_len[bq]) {
+        const long long vslot = ((long long)bq * H + hq) * a.cap16 + t0;
+        if (a.btab) p = pool_block<Q::block>(a, __ldg(a.btab + (vslot >> 4)));
+        else p = a.records + (vslot >> 4) * Q::block;
       }
-      cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
     }
+    src_lane = p;
+    src_next = 0;
   };
-  if (cur_i < nloc) {
-    const int gg = g0 + cur_i;
-    cur_b = batch_of(gg);
-    cur_nb = s_pre[cur_b + 1] - s_pre[cur_b];
-    cur_len = s_len[cur_b];
-    const int r = gg - H * s_pre[cur_b];
-    cur_h = r / cur_nb;
-    cur_t = r - cur_h * cur_nb;
-    cur_row = ((long long)cur_b * H + cur_h) * a.cap16;
-  }
-  int pf = -1;  // paged caches: the cursor block's table entry, loaded a tile ahead (see above)
-  auto prefetch = [&]() {
-    if (a.btab != nullptr && lane == 0 && cur_i < nloc && cur_t * kTT + 16 * qtr < cur_len)
-      pf = __ldg(a.btab + ((cur_row + cur_t * kTT + 16 * qtr) >> 4));
-  };
-  prefetch();
   auto issue_next = [&]() {
     const int stn = cur_i % S;
     uint64_t *bar = &s_full[stn * 4 + qtr];
-    const int tt0 = cur_t * kTT + 16 * qtr;
-    const int n = min(16, cur_len - tt0);
+    if (src_next == 32) refill_sources();
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(
+        __shfl_sync(kFull, reinterpret_cast<unsigned long long>(src_lane), src_next++));
     if (lane == 0) {  // the quarter is one stored block: one bulk copy
-      const uint8_t *src = n <= 0 ? nullptr
-                           : a.btab ? pool_block<Q::block>(a, pf)
-                                    : a.records + ((cur_row + tt0) >> 4) * Q::block;
       mbar_arrive_expect_tx(bar, src ? (uint32_t)Q::block : 0u);
       if (src) tma_load_1d(s_stage + stn * Q::stage + qtr * Q::block, src, (uint32_t)Q::block, bar);
     }
     cur_i += kPersistGroups;
-    cur_t += kPersistGroups;
-    if (cur_i < nloc) seek();
-    prefetch();
   };
   for (int k = 0; k < S / kPersistGroups && cur_i < nloc; ++k) issue_next();
 
