@@ -55,7 +55,8 @@ def quantize_groups(vals: np.ndarray):
     mn = v.min(axis=-1)
     mx = v.max(axis=-1)
     z16 = mn.astype(np.float16)
-    s16 = ((mx - mn) / LEVELS).astype(np.float16)
+    with np.errstate(over="ignore"):  # a step above fp16's largest finite value rounds to inf
+        s16 = ((mx - mn) / LEVELS).astype(np.float16)
     z = z16.astype(np.float64)[..., None]
     s = s16.astype(np.float64)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
