@@ -105,7 +105,51 @@ __device__ __forceinline__ uint32_t kivi_code(float x, float z, float s, float i
 }
 __device__ __forceinline__ float kivi_inv(float s) { return (s > 0.f) ? 1.f / s : 0.f; }
 
-// one warp per (batch, head, group of 32 tokens); lane owns channels 4L..4L+3
+// Codes of many values at once. For a value x of a group with statistics (z, s) the code is
+// clamp(rint(t), 0, 3), t = (x - z) * inv, exactly as kivi_code computes it; two values go
+// through each packed fp32 operation. Rounding uses the magic constant 1.5 * 2^23: for
+// |u| < 2^22, u + 1.5 * 2^23 rounds u to the nearest integer, ties to even (the constant is
+// even), and leaves it in the low mantissa bits, so the sum's bit pattern minus kMagicBits is
+// the code of the clamped u (clamping to the integers 0 and 3 commutes with rounding). The
+// distance of the clamped t from its rounding is kept: when it is within 2^-16 of 1/2 the
+// product may have decided a rounding that only the exact quotient can (kivi_code's slow
+// path), and the caller recomputes those values with kivi_code itself. Outside [0, 3] the clamp
+// decides and both paths agree.
+constexpr float kMagic = 12582912.f;
+constexpr uint32_t kMagicBits = 0x4B400000u;
+constexpr float kTieBand = 0.5f - 0x1p-16f;
+
+struct CodePair {
+  uint32_t b0, b1;  // kMagicBits + code
+  float dev;        // max |clamped t - its rounding| of the two
+};
+
+__device__ __forceinline__ CodePair kivi_code_pair(float2 x, float2 nz, float2 inv) {
+  const float2 t = __fmul2_rn(__fadd2_rn(x, nz), inv);
+  const float2 tc = make_float2(fminf(fmaxf(t.x, 0.f), 3.f), fminf(fmaxf(t.y, 0.f), 3.f));
+  const float2 m = __fadd2_rn(tc, make_float2(kMagic, kMagic));
+  const float2 r = __fadd2_rn(m, make_float2(-kMagic, -kMagic));
+  const float2 d = __ffma2_rn(r, make_float2(-1.f, -1.f), tc);
+  return CodePair{__float_as_uint(m.x), __float_as_uint(m.y), fmaxf(fabsf(d.x), fabsf(d.y))};
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t w) {
+  __nv_bfloat162 h;
+  memcpy(&h, &w, 4);
+  return h;
+}
+__device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 h) {
+  uint32_t w;
+  memcpy(&w, &h, 4);
+  return w;
+}
+
+// one warp per (batch, head, group of 32 tokens); lane L owns channels 4L..4L+3 and writes
+// byte L of each token's 32-byte code record. bfloat16 rows stay in registers between the
+// statistics and the codes; fp32 rows are read twice (the second time mostly from L2).
+template <bool BF16>
 __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, int units_per_bh) {
   const int lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -120,21 +164,60 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
   }
   const int g = kivi_nq(n0, a.window) / kG + (int)(unit % units_per_bh);
   if (g * kG >= kivi_nq(n1, a.window)) return;
+  const int j0 = g * kG;
+  // a group that starts at or after n0 is read from the input only, at constant row strides
+  const bool from_input = j0 >= n0;
+  const size_t in0 = ((size_t)bh * a.n_new + (size_t)(from_input ? j0 - n0 : 0)) * kD + 4 * lane;
   float mn[4], mx[4];
+  uint2 raw[BF16 ? kG : 1];
+  if constexpr (BF16) {
+    const uint2 *src = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.x) + in0);
+    if (from_input) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    mn[c] = INFINITY;
-    mx[c] = -INFINITY;
-  }
-  // (unrolled so that eight rows' loads are in flight at a time)
-#pragma unroll 8
-  for (int k = 0; k < kG; ++k) {
-    float x[4];
-    kivi_load(a, bh, n0, g * kG + k, lane, x);
+      for (int k = 0; k < kG; ++k) raw[k] = __ldg(src + k * (kD / 4));
+    } else {
+      const int R = a.window + kG;
+#pragma unroll
+      for (int k = 0; k < kG; ++k) {
+        const int j = j0 + k;
+        const uint2 *p = (j < n0) ? reinterpret_cast<const uint2 *>(a.ring + ((size_t)bh * R + (j % R)) * kD + 4 * lane)
+                                  : reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.x) +
+                                                                    ((size_t)bh * a.n_new + (j - n0)) * kD + 4 * lane);
+        raw[k] = __ldg(p);
+      }
+    }
+    // bfloat16 minima and maxima are exact, two channels per instruction
+    __nv_bfloat162 lo01 = as_bf162(raw[0].x), hi01 = lo01, lo23 = as_bf162(raw[0].y), hi23 = lo23;
+#pragma unroll
+    for (int k = 1; k < kG; ++k) {
+      lo01 = __hmin2(lo01, as_bf162(raw[k].x));
+      hi01 = __hmax2(hi01, as_bf162(raw[k].x));
+      lo23 = __hmin2(lo23, as_bf162(raw[k].y));
+      hi23 = __hmax2(hi23, as_bf162(raw[k].y));
+    }
+    mn[0] = bf16_lo(bf162_bits(lo01));
+    mn[1] = bf16_hi(bf162_bits(lo01));
+    mn[2] = bf16_lo(bf162_bits(lo23));
+    mn[3] = bf16_hi(bf162_bits(lo23));
+    mx[0] = bf16_lo(bf162_bits(hi01));
+    mx[1] = bf16_hi(bf162_bits(hi01));
+    mx[2] = bf16_lo(bf162_bits(hi23));
+    mx[3] = bf16_hi(bf162_bits(hi23));
+  } else {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      mn[c] = fminf(mn[c], x[c]);
-      mx[c] = fmaxf(mx[c], x[c]);
+      mn[c] = INFINITY;
+      mx[c] = -INFINITY;
+    }
+#pragma unroll 8
+    for (int k = 0; k < kG; ++k) {
+      float x[4];
+      kivi_load(a, bh, n0, j0 + k, lane, x);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        mn[c] = fminf(mn[c], x[c]);
+        mx[c] = fmaxf(mx[c], x[c]);
+      }
     }
   }
   float zf[4], sf[4], inv[4];
@@ -150,22 +233,37 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
   }
   uint4 *srec = reinterpret_cast<uint4 *>(a.stats + (((size_t)bh * (a.capacity / kG) + g) * kD) * 2);
   srec[lane] = make_uint4(st[0], st[1], st[2], st[3]);
-#pragma unroll 8
+  const float2 nz01 = make_float2(-zf[0], -zf[1]), nz23 = make_float2(-zf[2], -zf[3]);
+  const float2 iv01 = make_float2(inv[0], inv[1]), iv23 = make_float2(inv[2], inv[3]);
+  uint8_t *crow = a.codes + ((size_t)bh * a.capacity + j0) * (kD / 4) + lane;
+#pragma unroll  // (whole: raw[] stays in registers)
   for (int k = 0; k < kG; ++k) {
-    const int j = g * kG + k;
     float x[4];
-    kivi_load(a, bh, n0, j, lane, x);
-    uint32_t field = 0;
+    if constexpr (BF16) {
+      x[0] = bf16_lo(raw[k].x);
+      x[1] = bf16_hi(raw[k].x);
+      x[2] = bf16_lo(raw[k].y);
+      x[3] = bf16_hi(raw[k].y);
+    } else {
+      kivi_load(a, bh, n0, j0 + k, lane, x);
+    }
+    const CodePair p = kivi_code_pair(make_float2(x[0], x[1]), nz01, iv01);
+    const CodePair q = kivi_code_pair(make_float2(x[2], x[3]), nz23, iv23);
+    uint32_t field = p.b0 + 4u * p.b1 + 16u * q.b0 + 64u * q.b1 - 85u * kMagicBits;
+    if (fmaxf(p.dev, q.dev) > kTieBand) {
+      field = 0;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf[c], sf[c], inv[c]) << (2 * c);
-    const uint32_t word = kivi_pack_word(field, lane);
-    if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + ((size_t)bh * a.capacity + j) * (kD / 4))[lane] = word;
+      for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf[c], sf[c], inv[c]) << (2 * c);
+    }
+    crow[k * (kD / 4)] = (uint8_t)field;
   }
 }
 
-// one warp per (batch, head, run of kTokRun consecutive tokens); groups are 32 channels = 8
-// lanes. The run's rows are loaded before any is coded, so a warp has several loads in flight.
-constexpr int kTokRun = 4;
+// one warp per (batch, head, run of kTokRun = 8 consecutive tokens); lane L codes group L mod 4
+// (channels 32 (L mod 4) .. + 31) of token L / 4 by itself: statistics, step and codes, no
+// exchange between lanes. Its 64 code bits are bytes 8 (L mod 4) .. + 7 of the token's record.
+constexpr int kTokRun = 8;
+template <bool BF16>
 __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, int units_per_bh) {
   const int lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -178,61 +276,87 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, in
     if (lane == 0 && unit % units_per_bh == 0) set_error(a.error, TQ_ERR_CAPACITY);
     return;
   }
-  const int j0 = kivi_nq(n0, a.window) + kTokRun * (int)(unit % units_per_bh);
-  const int jend = kivi_nq(n1, a.window);
-  if (j0 >= jend) return;
-  float x[kTokRun][4];
+  const int j = kivi_nq(n0, a.window) + kTokRun * (int)(unit % units_per_bh) + (lane >> 2);
+  if (j >= kivi_nq(n1, a.window)) return;  // lanes work independently from here on
+  const int grp = lane & 3;
+  float x[kG];
+  float mn, mx;
+  const bool from_ring = j < n0;
+  if (BF16 || from_ring) {
+    const uint16_t *row = from_ring ? a.ring + ((size_t)bh * (a.window + kG) + (j % (a.window + kG))) * kD
+                                    : static_cast<const uint16_t *>(a.x) + ((size_t)bh * a.n_new + (j - n0)) * kD;
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + kG * grp);
+    uint32_t w[kG / 2];
 #pragma unroll
-  for (int r = 0; r < kTokRun; ++r) {
-    if (j0 + r < jend) {
-      kivi_load(a, bh, n0, j0 + r, lane, x[r]);
-    } else {
+    for (int i = 0; i < kG / 8; ++i) {
+      const uint4 u = __ldg(src + i);
+      w[4 * i] = u.x;
+      w[4 * i + 1] = u.y;
+      w[4 * i + 2] = u.z;
+      w[4 * i + 3] = u.w;
+    }
+    __nv_bfloat162 lo = as_bf162(w[0]), hi = lo;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) x[r][c] = 0.f;
+    for (int i = 1; i < kG / 2; ++i) {
+      lo = __hmin2(lo, as_bf162(w[i]));
+      hi = __hmax2(hi, as_bf162(w[i]));
+    }
+    mn = fminf(bf16_lo(bf162_bits(lo)), bf16_hi(bf162_bits(lo)));
+    mx = fmaxf(bf16_lo(bf162_bits(hi)), bf16_hi(bf162_bits(hi)));
+#pragma unroll
+    for (int i = 0; i < kG / 2; ++i) {
+      x[2 * i] = bf16_lo(w[i]);
+      x[2 * i + 1] = bf16_hi(w[i]);
+    }
+  } else {
+    const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(a.x) +
+                                                         ((size_t)bh * a.n_new + (j - n0)) * kD + kG * grp);
+#pragma unroll
+    for (int i = 0; i < kG / 4; ++i) {
+      const float4 f = __ldg(src + i);
+      x[4 * i] = f.x;
+      x[4 * i + 1] = f.y;
+      x[4 * i + 2] = f.z;
+      x[4 * i + 3] = f.w;
+    }
+    mn = x[0];
+    mx = x[0];
+#pragma unroll
+    for (int c = 1; c < kG; ++c) {
+      mn = fminf(mn, x[c]);
+      mx = fmaxf(mx, x[c]);
     }
   }
-  // each token's group minima and maxima (a lane's four channels, then the eight lanes of its
-  // group); then lane L computes the step of token (L >> 2) & 3, group L & 3 only, so the
-  // run's sixteen steps take one evaluation instead of one per token
-  float mn[kTokRun], mx[kTokRun];
+  __half z, s;
+  group_stats(mn, mx, z, s);
+  const float zf = __half2float(z), sf = __half2float(s), inv = kivi_inv(sf);
+  const size_t slot = (size_t)bh * a.capacity + j;
+  reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[grp] =
+      (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
+  const float2 nz = make_float2(-zf, -zf), iv = make_float2(inv, inv);
+  uint32_t word[2];
+  float dev = 0.f;
 #pragma unroll
-  for (int r = 0; r < kTokRun; ++r) {
-    mn[r] = fminf(fminf(x[r][0], x[r][1]), fminf(x[r][2], x[r][3]));
-    mx[r] = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+  for (int h = 0; h < 2; ++h) {
+    uint32_t acc = 0u - 0x55555555u * kMagicBits;  // the sum of kMagicBits * 4^i, i < 16, taken off
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      mn[r] = fminf(mn[r], __shfl_xor_sync(kFull, mn[r], o));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], o));
+    for (int i = 0; i < 8; ++i) {
+      const CodePair p = kivi_code_pair(make_float2(x[16 * h + 2 * i], x[16 * h + 2 * i + 1]), nz, iv);
+      acc += p.b0 * (1u << (4 * i)) + p.b1 * (1u << (4 * i + 2));
+      dev = fmaxf(dev, p.dev);
+    }
+    word[h] = acc;
+  }
+  if (dev > kTieBand) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc |= kivi_code(x[16 * h + i], zf, sf, inv) << (2 * i);
+      word[h] = acc;
     }
   }
-  const int r_me = (lane >> 2) & (kTokRun - 1), src = 8 * (lane & 3);
-  float mn_me = 0.f, mx_me = 0.f;
-#pragma unroll
-  for (int r = 0; r < kTokRun; ++r) {
-    const float lo = __shfl_sync(kFull, mn[r], src), hi = __shfl_sync(kFull, mx[r], src);
-    if (r == r_me) {
-      mn_me = lo;
-      mx_me = hi;
-    }
-  }
-  __half zm, sm;
-  group_stats(mn_me, mx_me, zm, sm);
-  const uint32_t zs_me = (uint32_t)__half_as_ushort(zm) | ((uint32_t)__half_as_ushort(sm) << 16);
-#pragma unroll
-  for (int r = 0; r < kTokRun; ++r) {
-    const int j = j0 + r;
-    if (j >= jend) break;  // warp-uniform
-    const uint32_t st = __shfl_sync(kFull, zs_me, 4 * r + (lane >> 3));  // this lane's group's step
-    const float zf = __half2float(__ushort_as_half((unsigned short)(st & 0xffffu)));
-    const float sf = __half2float(__ushort_as_half((unsigned short)(st >> 16))), inv = kivi_inv(sf);
-    uint32_t field = 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) field |= kivi_code(x[r][c], zf, sf, inv) << (2 * c);
-    const uint32_t word = kivi_pack_word(field, lane);
-    const size_t slot = (size_t)bh * a.capacity + j;
-    if (lane < 8) reinterpret_cast<uint32_t *>(a.codes + slot * (kD / 4))[lane] = word;
-    if ((lane & 7) == 0) reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[lane >> 3] = st;
-  }
+  reinterpret_cast<uint2 *>(a.codes + slot * (kD / 4))[grp] = make_uint2(word[0], word[1]);
 }
 
 // one warp per (batch, head, new token t >= t_first): window tokens go to the bf16 ring.
@@ -311,8 +435,13 @@ int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
   const int units = per_channel ? (max_tokens + kG - 1) / kG + 1 : (max_tokens + kTokRun - 1) / kTokRun;
   const long long warps = bh * units;
   const unsigned blocks = (unsigned)((warps + 7) / 8);
-  if (per_channel) kivi_flush_per_channel<<<blocks, 256, 0, st>>>(t, units);
-  else kivi_flush_per_token<<<blocks, 256, 0, st>>>(t, units);
+  if (per_channel) {
+    if (t.bf16) kivi_flush_per_channel<true><<<blocks, 256, 0, st>>>(t, units);
+    else kivi_flush_per_channel<false><<<blocks, 256, 0, st>>>(t, units);
+  } else {
+    if (t.bf16) kivi_flush_per_token<true><<<blocks, 256, 0, st>>>(t, units);
+    else kivi_flush_per_token<false><<<blocks, 256, 0, st>>>(t, units);
+  }
   const int t_first = std::max(0, t.n_new - (t.window + kG - 1));
   const long long wwarps = bh * (t.n_new - t_first);
   kivi_window_write<<<(unsigned)((wwarps + 7) / 8), 256, 0, st>>>(t, t_first);

@@ -84,6 +84,31 @@ def test_kivi_append_matches_oracle(layout, chunks):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
+def test_kivi_append_of_fp32_inputs_matches_oracle(layout):
+    # fp32 inputs take their own load paths (tokens already in the window are bfloat16)
+    kpc, vpt = layout
+    B, H, chunks = 2, 3, [100, 1, 1, 60, 33, 105]
+    N = sum(chunks)
+    q, k, v = _inputs(B, H, N, seed=5 + kpc + 2 * vpt, dtype=torch.float32)
+    ctx = tq.Context(128, 2, "KIVI", 0, k_per_channel=kpc, v_per_token=vpt)
+    cache = tq.Cache(ctx, B, H, 320)
+    _fill(ctx, cache, k, v, chunks)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    # the window holds bfloat16, so a token that ends an append inside the window (at or after
+    # nq of that append's total) is quantised later from its bfloat16 value
+    ke, ve = k.clone(), v.clone()
+    t = 0
+    for c in chunks:
+        lo = max(t, okivi.quantized_length(t + c))
+        ke[:, :, lo:t + c] = k[:, :, lo:t + c].to(torch.bfloat16).float()
+        ve[:, :, lo:t + c] = v[:, :, lo:t + c].to(torch.bfloat16).float()
+        t += c
+    _check_tensor(cache, "k", ke, kpc, B, H, N)
+    _check_tensor(cache, "v", ve, not vpt, B, H, N)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("G", [1, 4])
 def test_kivi_decode_matches_oracle(layout, G):
     kpc, vpt = layout
