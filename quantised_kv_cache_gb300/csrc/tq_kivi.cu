@@ -38,6 +38,7 @@ struct KiviTensorArgs {
   uint16_t *stats;     // fp16 (zero, step) pairs
   uint16_t *ring;      // bf16 [batch][heads][window + G][d]
   int *error;
+  FastDiv div_units, div_heads;  // by the flush kernel's warps per (batch, head), and by heads
 };
 
 // token j's four channels 4L..4L+3 from the ring (j < n0) or the input
@@ -90,47 +91,26 @@ __device__ __forceinline__ void group_stats(float mn, float mx, __half &z, __hal
   s = kivi_step(mn, mx);
 }
 
-// code = clamp(rint((x - z) / s), 0, 3), ties to even, with the division as a product by
-// inv = 1 / s (0 when s = 0, which makes every code 0). The product is within a few fp32 ulps
-// of the quotient, so it decides the code except near a rounding boundary; there, and at
-// exact ties (frequent when x and z carry few significant bits), the correctly rounded
-// quotient decides.
-__device__ __forceinline__ uint32_t kivi_code(float x, float z, float s, float inv) {
-  const float dx = x - z;
-  const float t = dx * inv;
-  float r = rintf(t);
-  if (fabsf(t - r) > 0.5f - 0x1p-16f) r = rintf(__fdiv_rn(dx, s));  // within 2^-16 of a half-integer
-  r = fminf(fmaxf(r, 0.f), 3.f);
-  return (uint32_t)r;
-}
-__device__ __forceinline__ float kivi_inv(float s) { return (s > 0.f) ? 1.f / s : 0.f; }
-
-// Codes of many values at once. For a value x of a group with statistics (z, s) the code is
-// clamp(rint(t), 0, 3), t = (x - z) * inv, exactly as kivi_code computes it; two values go
-// through each packed fp32 operation. Rounding uses the magic constant 1.5 * 2^23: for
-// |u| < 2^22, u + 1.5 * 2^23 rounds u to the nearest integer, ties to even (the constant is
-// even), and leaves it in the low mantissa bits, so the sum's bit pattern minus kMagicBits is
-// the code of the clamped u (clamping to the integers 0 and 3 commutes with rounding). The
-// distance of the clamped t from its rounding is kept: when it is within 2^-16 of 1/2 the
-// product may have decided a rounding that only the exact quotient can (kivi_code's slow
-// path), and the caller recomputes those values with kivi_code itself. Outside [0, 3] the clamp
-// decides and both paths agree.
-constexpr float kMagic = 12582912.f;
-constexpr uint32_t kMagicBits = 0x4B400000u;
-constexpr float kTieBand = 0.5f - 0x1p-16f;
-
-struct CodePair {
-  uint32_t b0, b1;  // kMagicBits + code
-  float dev;        // max |clamped t - its rounding| of the two
+// code = clamp(rint((x - z) / s), 0, 3), ties to even, the quotient taken exactly. With
+// dx = x - z (fp32) the code is the number of the thresholds (k + 1/2) s, k = 0, 1, 2, that dx
+// passes: past s / 2 and 5 s / 2 strictly, past 3 s / 2 from the threshold on, since a quotient
+// of exactly 1/2 or 5/2 rounds down to the even code and 3/2 rounds up. Each threshold is exact
+// in fp32 (s has 11 significant bits, k + 1/2 at most 3), so no division is needed and ties,
+// frequent when x and z carry few significant bits, come out exactly. A zero or infinite step
+// makes every code 0, as a zero quotient would: the thresholds are then NaN, which no
+// comparison passes.
+struct KiviThr {
+  float c0, c1, c2;
 };
-
-__device__ __forceinline__ CodePair kivi_code_pair(float2 x, float2 nz, float2 inv) {
-  const float2 t = __fmul2_rn(__fadd2_rn(x, nz), inv);
-  const float2 tc = make_float2(fminf(fmaxf(t.x, 0.f), 3.f), fminf(fmaxf(t.y, 0.f), 3.f));
-  const float2 m = __fadd2_rn(tc, make_float2(kMagic, kMagic));
-  const float2 r = __fadd2_rn(m, make_float2(-kMagic, -kMagic));
-  const float2 d = __ffma2_rn(r, make_float2(-1.f, -1.f), tc);
-  return CodePair{__float_as_uint(m.x), __float_as_uint(m.y), fmaxf(fabsf(d.x), fabsf(d.y))};
+__device__ __forceinline__ KiviThr kivi_thresholds(float s) {
+  if (!(s > 0.f && s < INFINITY)) {
+    const float nan = __int_as_float(0x7fffffff);
+    return KiviThr{nan, nan, nan};
+  }
+  return KiviThr{0.5f * s, 1.5f * s, 2.5f * s};
+}
+__device__ __forceinline__ uint32_t kivi_code(float dx, const KiviThr &t) {
+  return (uint32_t)(dx > t.c0) + (uint32_t)(dx >= t.c1) + (uint32_t)(dx > t.c2);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -146,54 +126,45 @@ __device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 h) {
   return w;
 }
 
-// one warp per (batch, head, group of 32 tokens); lane L owns channels 4L..4L+3 and writes
-// byte L of each token's 32-byte code record. bfloat16 rows stay in registers between the
-// statistics and the codes; fp32 rows are read twice (the second time mostly from L2).
-template <bool BF16>
-__global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, int units_per_bh) {
-  const int lane = threadIdx.x & 31;
-  const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const long long bh = unit / units_per_bh;
-  if (bh >= (long long)a.batch * a.heads) return;
-  const int b = (int)(bh / a.heads);
-  const int n0 = __ldg(a.seq_lens + b);
-  const int n1 = n0 + a.n_new;
-  if (n1 > a.capacity) {
-    if (lane == 0 && unit % units_per_bh == 0) set_error(a.error, TQ_ERR_CAPACITY);
-    return;
-  }
-  const int g = kivi_nq(n0, a.window) / kG + (int)(unit % units_per_bh);
-  if (g * kG >= kivi_nq(n1, a.window)) return;
-  const int j0 = g * kG;
-  // a group that starts at or after n0 is read from the input only, at constant row strides
-  const bool from_input = j0 >= n0;
-  const size_t in0 = ((size_t)bh * a.n_new + (size_t)(from_input ? j0 - n0 : 0)) * kD + 4 * lane;
-  float mn[4], mx[4];
-  uint2 raw[BF16 ? kG : 1];
-  if constexpr (BF16) {
-    const uint2 *src = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.x) + in0);
-    if (from_input) {
-#pragma unroll
-      for (int k = 0; k < kG; ++k) raw[k] = __ldg(src + k * (kD / 4));
+// Group-per-channel coding of one group, rows j0 .. j0 + 31, lane L: channels 4L..4L+3. The rows
+// are read twice, for the statistics and for the codes (the second time mostly from L2), which
+// keeps registers and so leaves room for more warps to hide the loads. IN: every row comes from
+// the input, at constant strides; otherwise rows before n0 come from the window ring.
+template <bool BF16, bool IN>
+__device__ __forceinline__ void code_channel_group(const KiviTensorArgs &a, long long bh, int n0, int j0, int lane) {
+  const int R = a.window + kG;
+  // input row j0 + k at in0 + k * kD elements (j0 - n0 is negative only when !IN)
+  const long long in0 = ((long long)bh * a.n_new + (j0 - n0)) * kD + 4 * lane;
+  // row k's four channels: raw bfloat16 pairs (BF16), or floats
+  auto row_bf16 = [&](int k) -> uint2 {
+    const int j = j0 + k;
+    if (IN || j >= n0) return __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.x) + in0 + k * kD));
+    return __ldg(reinterpret_cast<const uint2 *>(a.ring + ((size_t)bh * R + (j % R)) * kD + 4 * lane));
+  };
+  auto row_f32 = [&](int k, float (&x)[4]) {
+    const int j = j0 + k;
+    if (IN || j >= n0) {
+      const float4 f = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.x) + in0 + k * kD));
+      x[0] = f.x;
+      x[1] = f.y;
+      x[2] = f.z;
+      x[3] = f.w;
     } else {
-      const int R = a.window + kG;
-#pragma unroll
-      for (int k = 0; k < kG; ++k) {
-        const int j = j0 + k;
-        const uint2 *p = (j < n0) ? reinterpret_cast<const uint2 *>(a.ring + ((size_t)bh * R + (j % R)) * kD + 4 * lane)
-                                  : reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.x) +
-                                                                    ((size_t)bh * a.n_new + (j - n0)) * kD + 4 * lane);
-        raw[k] = __ldg(p);
-      }
+      load4(a.ring + ((size_t)bh * R + (j % R)) * kD + 4 * lane, 0, true, x);
     }
+  };
+  float mn[4], mx[4];
+  if constexpr (BF16) {
     // bfloat16 minima and maxima are exact, two channels per instruction
-    __nv_bfloat162 lo01 = as_bf162(raw[0].x), hi01 = lo01, lo23 = as_bf162(raw[0].y), hi23 = lo23;
-#pragma unroll
+    const uint2 r0 = row_bf16(0);
+    __nv_bfloat162 lo01 = as_bf162(r0.x), hi01 = lo01, lo23 = as_bf162(r0.y), hi23 = lo23;
+#pragma unroll 8
     for (int k = 1; k < kG; ++k) {
-      lo01 = __hmin2(lo01, as_bf162(raw[k].x));
-      hi01 = __hmax2(hi01, as_bf162(raw[k].x));
-      lo23 = __hmin2(lo23, as_bf162(raw[k].y));
-      hi23 = __hmax2(hi23, as_bf162(raw[k].y));
+      const uint2 r = row_bf16(k);
+      lo01 = __hmin2(lo01, as_bf162(r.x));
+      hi01 = __hmax2(hi01, as_bf162(r.x));
+      lo23 = __hmin2(lo23, as_bf162(r.y));
+      hi23 = __hmax2(hi23, as_bf162(r.y));
     }
     mn[0] = bf16_lo(bf162_bits(lo01));
     mn[1] = bf16_hi(bf162_bits(lo01));
@@ -212,7 +183,7 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
 #pragma unroll 8
     for (int k = 0; k < kG; ++k) {
       float x[4];
-      kivi_load(a, bh, n0, j0 + k, lane, x);
+      row_f32(k, x);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         mn[c] = fminf(mn[c], x[c]);
@@ -220,43 +191,60 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
       }
     }
   }
-  float zf[4], sf[4], inv[4];
+  float nz[4];
+  KiviThr thr[4];
   uint32_t st[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     __half z, s;
     group_stats(mn[c], mx[c], z, s);
-    zf[c] = __half2float(z);
-    sf[c] = __half2float(s);
-    inv[c] = kivi_inv(sf[c]);
+    nz[c] = -__half2float(z);
+    thr[c] = kivi_thresholds(__half2float(s));
     st[c] = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
   }
-  uint4 *srec = reinterpret_cast<uint4 *>(a.stats + (((size_t)bh * (a.capacity / kG) + g) * kD) * 2);
+  uint4 *srec = reinterpret_cast<uint4 *>(a.stats + (((size_t)bh * (a.capacity / kG) + j0 / kG) * kD) * 2);
   srec[lane] = make_uint4(st[0], st[1], st[2], st[3]);
-  const float2 nz01 = make_float2(-zf[0], -zf[1]), nz23 = make_float2(-zf[2], -zf[3]);
-  const float2 iv01 = make_float2(inv[0], inv[1]), iv23 = make_float2(inv[2], inv[3]);
+  const float2 nz01 = make_float2(nz[0], nz[1]), nz23 = make_float2(nz[2], nz[3]);
   uint8_t *crow = a.codes + ((size_t)bh * a.capacity + j0) * (kD / 4) + lane;
-#pragma unroll  // (whole: raw[] stays in registers)
+#pragma unroll 8
   for (int k = 0; k < kG; ++k) {
     float x[4];
     if constexpr (BF16) {
-      x[0] = bf16_lo(raw[k].x);
-      x[1] = bf16_hi(raw[k].x);
-      x[2] = bf16_lo(raw[k].y);
-      x[3] = bf16_hi(raw[k].y);
+      const uint2 r = row_bf16(k);
+      x[0] = bf16_lo(r.x);
+      x[1] = bf16_hi(r.x);
+      x[2] = bf16_lo(r.y);
+      x[3] = bf16_hi(r.y);
     } else {
-      kivi_load(a, bh, n0, j0 + k, lane, x);
+      row_f32(k, x);
     }
-    const CodePair p = kivi_code_pair(make_float2(x[0], x[1]), nz01, iv01);
-    const CodePair q = kivi_code_pair(make_float2(x[2], x[3]), nz23, iv23);
-    uint32_t field = p.b0 + 4u * p.b1 + 16u * q.b0 + 64u * q.b1 - 85u * kMagicBits;
-    if (fmaxf(p.dev, q.dev) > kTieBand) {
-      field = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) field |= kivi_code(x[c], zf[c], sf[c], inv[c]) << (2 * c);
-    }
+    const float2 d01 = __fadd2_rn(make_float2(x[0], x[1]), nz01);
+    const float2 d23 = __fadd2_rn(make_float2(x[2], x[3]), nz23);
+    const uint32_t field = kivi_code(d01.x, thr[0]) | (kivi_code(d01.y, thr[1]) << 2) |
+                           (kivi_code(d23.x, thr[2]) << 4) | (kivi_code(d23.y, thr[3]) << 6);
     crow[k * (kD / 4)] = (uint8_t)field;
   }
+}
+
+// one warp per (batch, head, group of 32 tokens); lane L owns channels 4L..4L+3 and writes
+// byte L of each token's 32-byte code record
+template <bool BF16>
+__global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
+  const uint32_t bh = fast_div(unit, a.div_units);
+  if (bh >= (uint32_t)(a.batch * a.heads)) return;
+  const int n0 = __ldg(a.seq_lens + fast_div(bh, a.div_heads));
+  const int n1 = n0 + a.n_new;
+  const int u = (int)(unit - bh * a.div_units.d);
+  if (n1 > a.capacity) {
+    if (lane == 0 && u == 0) set_error(a.error, TQ_ERR_CAPACITY);
+    return;
+  }
+  const int j0 = kivi_nq(n0, a.window) + kG * u;
+  if (j0 >= kivi_nq(n1, a.window)) return;
+  if (j0 >= n0) code_channel_group<BF16, true>(a, bh, n0, j0, lane);
+  else code_channel_group<BF16, false>(a, bh, n0, j0, lane);
 }
 
 // one warp per (batch, head, run of kTokRun = 8 consecutive tokens); lane L codes group L mod 4
@@ -264,19 +252,19 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a, 
 // exchange between lanes. Its 64 code bits are bytes 8 (L mod 4) .. + 7 of the token's record.
 constexpr int kTokRun = 8;
 template <bool BF16>
-__global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, int units_per_bh) {
+__global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a) {
   const int lane = threadIdx.x & 31;
-  const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const long long bh = unit / units_per_bh;
-  if (bh >= (long long)a.batch * a.heads) return;
-  const int b = (int)(bh / a.heads);
-  const int n0 = __ldg(a.seq_lens + b);
+  const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
+  const uint32_t bh = fast_div(unit, a.div_units);
+  if (bh >= (uint32_t)(a.batch * a.heads)) return;
+  const int n0 = __ldg(a.seq_lens + fast_div(bh, a.div_heads));
   const int n1 = n0 + a.n_new;
+  const int u = (int)(unit - bh * a.div_units.d);
   if (n1 > a.capacity) {
-    if (lane == 0 && unit % units_per_bh == 0) set_error(a.error, TQ_ERR_CAPACITY);
+    if (lane == 0 && u == 0) set_error(a.error, TQ_ERR_CAPACITY);
     return;
   }
-  const int j = kivi_nq(n0, a.window) + kTokRun * (int)(unit % units_per_bh) + (lane >> 2);
+  const int j = kivi_nq(n0, a.window) + kTokRun * u + (lane >> 2);
   if (j >= kivi_nq(n1, a.window)) return;  // lanes work independently from here on
   const int grp = lane & 3;
   float x[kG];
@@ -329,32 +317,22 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a, in
   }
   __half z, s;
   group_stats(mn, mx, z, s);
-  const float zf = __half2float(z), sf = __half2float(s), inv = kivi_inv(sf);
+  const float nzf = -__half2float(z);
+  const KiviThr thr = kivi_thresholds(__half2float(s));
   const size_t slot = (size_t)bh * a.capacity + j;
   reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[grp] =
       (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
-  const float2 nz = make_float2(-zf, -zf), iv = make_float2(inv, inv);
+  const float2 nz = make_float2(nzf, nzf);
   uint32_t word[2];
-  float dev = 0.f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    uint32_t acc = 0u - 0x55555555u * kMagicBits;  // the sum of kMagicBits * 4^i, i < 16, taken off
+    uint32_t acc = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const CodePair p = kivi_code_pair(make_float2(x[16 * h + 2 * i], x[16 * h + 2 * i + 1]), nz, iv);
-      acc += p.b0 * (1u << (4 * i)) + p.b1 * (1u << (4 * i + 2));
-      dev = fmaxf(dev, p.dev);
+      const float2 d = __fadd2_rn(make_float2(x[16 * h + 2 * i], x[16 * h + 2 * i + 1]), nz);
+      acc |= (kivi_code(d.x, thr) << (4 * i)) | (kivi_code(d.y, thr) << (4 * i + 2));
     }
     word[h] = acc;
-  }
-  if (dev > kTieBand) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t acc = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) acc |= kivi_code(x[16 * h + i], zf, sf, inv) << (2 * i);
-      word[h] = acc;
-    }
   }
   reinterpret_cast<uint2 *>(a.codes + slot * (kD / 4))[grp] = make_uint2(word[0], word[1]);
 }
@@ -434,13 +412,16 @@ int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
   const int max_tokens = t.n_new + kG - 1;
   const int units = per_channel ? (max_tokens + kG - 1) / kG + 1 : (max_tokens + kTokRun - 1) / kTokRun;
   const long long warps = bh * units;
+  if (warps >= 0xffffffffLL - 8) return TQ_ERR_ARG;  // warp indices are 32-bit
+  t.div_units = make_fastdiv((uint32_t)units);
+  t.div_heads = make_fastdiv((uint32_t)t.heads);
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   if (per_channel) {
-    if (t.bf16) kivi_flush_per_channel<true><<<blocks, 256, 0, st>>>(t, units);
-    else kivi_flush_per_channel<false><<<blocks, 256, 0, st>>>(t, units);
+    if (t.bf16) kivi_flush_per_channel<true><<<blocks, 256, 0, st>>>(t);
+    else kivi_flush_per_channel<false><<<blocks, 256, 0, st>>>(t);
   } else {
-    if (t.bf16) kivi_flush_per_token<true><<<blocks, 256, 0, st>>>(t, units);
-    else kivi_flush_per_token<false><<<blocks, 256, 0, st>>>(t, units);
+    if (t.bf16) kivi_flush_per_token<true><<<blocks, 256, 0, st>>>(t);
+    else kivi_flush_per_token<false><<<blocks, 256, 0, st>>>(t);
   }
   const int t_first = std::max(0, t.n_new - (t.window + kG - 1));
   const long long wwarps = bh * (t.n_new - t_first);
