@@ -55,8 +55,9 @@ __device__ __forceinline__ void kivi_load(const KiviTensorArgs &a, long long bh,
 
 // The step fp16((max - min) / 3) with the quotient taken in fp64 and then rounded to fp16
 // (mx >= mn), without fp64 division, which this GPU runs at a small fraction of its fp32
-// rate. D = mx - mn is held exactly as d + e (two-sum). The fp32 quotient d / 3 lies within
-// 2^-23 of D / 3, so its nearest fp16 value c is the answer or one of its neighbours; the
+// rate. D = mx - mn is held exactly as d + e (two-sum). The product q = d * fp32(1/3) lies
+// within 2^-22 (relative) of D / 3, far inside one fp16 step, so its nearest fp16 value c is
+// the answer or one of its neighbours; the
 // exact sign of D - 3m at the midpoints m between c and its neighbours decides (3m has at
 // most 14 significant bits, and d - 3m is exact because d and 3m are within a factor of 2),
 // ties going to the even value as they do from an fp64 quotient that lands on a midpoint.
@@ -68,7 +69,7 @@ __device__ __forceinline__ __half kivi_step(float mn, float mx) {
   const float bv = __fsub_rn(d, mx);
   const float av = __fsub_rn(d, bv);
   const float e = __fadd_rn(__fsub_rn(mx, av), __fsub_rn(-mn, bv));
-  const float q = __fdiv_rn(d, 3.f);
+  const float q = __fmul_rn(d, 1.f / 3.f);
   if (!(q >= 0x1p-13f && q <= 60000.f)) return __double2half(((double)mx - (double)mn) / 3.0);
   const __half c = __float2half_rn(q);
   const unsigned short cb = __half_as_ushort(c);
@@ -92,25 +93,39 @@ __device__ __forceinline__ void group_stats(float mn, float mx, __half &z, __hal
 }
 
 // code = clamp(rint((x - z) / s), 0, 3), ties to even, the quotient taken exactly. With
-// dx = x - z (fp32) the code is the number of the thresholds (k + 1/2) s, k = 0, 1, 2, that dx
-// passes: past s / 2 and 5 s / 2 strictly, past 3 s / 2 from the threshold on, since a quotient
-// of exactly 1/2 or 5/2 rounds down to the even code and 3/2 rounds up. Each threshold is exact
-// in fp32 (s has 11 significant bits, k + 1/2 at most 3), so no division is needed and ties,
-// frequent when x and z carry few significant bits, come out exactly. A zero or infinite step
-// makes every code 0, as a zero quotient would: the thresholds are then NaN, which no
-// comparison passes.
-struct KiviThr {
-  float c0, c1, c2;
+// dx = x - z (fp32) the code is the number of the thresholds c_k = (k + 1/2) s, k = 0, 1, 2, that
+// dx passes: c_0 and c_2 strictly, c_1 from the threshold on, since a quotient of exactly 1/2
+// or 5/2 rounds down to the even code and 3/2 rounds up. Each threshold is exact in fp32 (s has
+// 11 significant bits, k + 1/2 at most 3), so no division is needed and ties, frequent when x
+// and z carry few significant bits, come out exactly. The three tests are the signs of
+// A = c_0 - dx, B = dx - c_1 and C = c_2 - dx (a difference of equal values is +0): they pass
+// as p_0 = sign A, p_1 = not sign B, p_2 = sign C, and since they pass in order the code's
+// high bit is p_1 and its low bit p_0 ^ p_1 ^ p_2, i.e. the complements of sign B and of the
+// sign of A ^ B ^ C. kivi_push2 shifts these two sign bits into a word from below, so that
+// the complement of the word holds the codes, the value pushed last in the lowest bits. A zero
+// or infinite step makes every code 0, as a zero quotient would: the thresholds are then +inf
+// and x is compared as is (so that an infinite zero point gives no inf - inf).
+struct KiviCoder {
+  float nz, c0, c1, c2;  // -z (0 for a degenerate step) and the thresholds
 };
-__device__ __forceinline__ KiviThr kivi_thresholds(float s) {
-  if (!(s > 0.f && s < INFINITY)) {
-    const float nan = __int_as_float(0x7fffffff);
-    return KiviThr{nan, nan, nan};
-  }
-  return KiviThr{0.5f * s, 1.5f * s, 2.5f * s};
+__device__ __forceinline__ KiviCoder kivi_coder(__half z, __half s) {
+  const float sf = __half2float(s);
+  if (!(sf > 0.f && sf < INFINITY)) return KiviCoder{0.f, INFINITY, INFINITY, INFINITY};
+  return KiviCoder{-__half2float(z), 0.5f * sf, 1.5f * sf, 2.5f * sf};
 }
-__device__ __forceinline__ uint32_t kivi_code(float dx, const KiviThr &t) {
-  return (uint32_t)(dx > t.c0) + (uint32_t)(dx >= t.c1) + (uint32_t)(dx > t.c2);
+// push the codes of x.y, then x.x (coders kx for x.x, ky for x.y)
+__device__ __forceinline__ void kivi_push2(float2 x, const KiviCoder &kx, const KiviCoder &ky, uint32_t &acc) {
+  const float2 dx = __fadd2_rn(x, make_float2(kx.nz, ky.nz));
+  const float2 A = __ffma2_rn(dx, make_float2(-1.f, -1.f), make_float2(kx.c0, ky.c0));
+  const float2 B = __fadd2_rn(dx, make_float2(-kx.c1, -ky.c1));
+  const float2 C = __ffma2_rn(dx, make_float2(-1.f, -1.f), make_float2(kx.c2, ky.c2));
+  const uint32_t bx = __float_as_uint(B.x), by = __float_as_uint(B.y);
+  const uint32_t tx = __float_as_uint(A.x) ^ bx ^ __float_as_uint(C.x);
+  const uint32_t ty = __float_as_uint(A.y) ^ by ^ __float_as_uint(C.y);
+  acc = __funnelshift_l(by, acc, 1);
+  acc = __funnelshift_l(ty, acc, 1);
+  acc = __funnelshift_l(bx, acc, 1);
+  acc = __funnelshift_l(tx, acc, 1);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -191,20 +206,17 @@ __device__ __forceinline__ void code_channel_group(const KiviTensorArgs &a, long
       }
     }
   }
-  float nz[4];
-  KiviThr thr[4];
+  KiviCoder kc[4];
   uint32_t st[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     __half z, s;
     group_stats(mn[c], mx[c], z, s);
-    nz[c] = -__half2float(z);
-    thr[c] = kivi_thresholds(__half2float(s));
+    kc[c] = kivi_coder(z, s);
     st[c] = (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
   }
   uint4 *srec = reinterpret_cast<uint4 *>(a.stats + (((size_t)bh * (a.capacity / kG) + j0 / kG) * kD) * 2);
   srec[lane] = make_uint4(st[0], st[1], st[2], st[3]);
-  const float2 nz01 = make_float2(nz[0], nz[1]), nz23 = make_float2(nz[2], nz[3]);
   uint8_t *crow = a.codes + ((size_t)bh * a.capacity + j0) * (kD / 4) + lane;
 #pragma unroll 8
   for (int k = 0; k < kG; ++k) {
@@ -218,11 +230,10 @@ __device__ __forceinline__ void code_channel_group(const KiviTensorArgs &a, long
     } else {
       row_f32(k, x);
     }
-    const float2 d01 = __fadd2_rn(make_float2(x[0], x[1]), nz01);
-    const float2 d23 = __fadd2_rn(make_float2(x[2], x[3]), nz23);
-    const uint32_t field = kivi_code(d01.x, thr[0]) | (kivi_code(d01.y, thr[1]) << 2) |
-                           (kivi_code(d23.x, thr[2]) << 4) | (kivi_code(d23.y, thr[3]) << 6);
-    crow[k * (kD / 4)] = (uint8_t)field;
+    uint32_t acc = 0;
+    kivi_push2(make_float2(x[2], x[3]), kc[2], kc[3], acc);
+    kivi_push2(make_float2(x[0], x[1]), kc[0], kc[1], acc);
+    crow[k * (kD / 4)] = (uint8_t)~acc;
   }
 }
 
@@ -317,22 +328,17 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a) {
   }
   __half z, s;
   group_stats(mn, mx, z, s);
-  const float nzf = -__half2float(z);
-  const KiviThr thr = kivi_thresholds(__half2float(s));
+  const KiviCoder kc = kivi_coder(z, s);
   const size_t slot = (size_t)bh * a.capacity + j;
   reinterpret_cast<uint32_t *>(a.stats + slot * (kD / kG) * 2)[grp] =
       (uint32_t)__half_as_ushort(z) | ((uint32_t)__half_as_ushort(s) << 16);
-  const float2 nz = make_float2(nzf, nzf);
   uint32_t word[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t acc = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 d = __fadd2_rn(make_float2(x[16 * h + 2 * i], x[16 * h + 2 * i + 1]), nz);
-      acc |= (kivi_code(d.x, thr) << (4 * i)) | (kivi_code(d.y, thr) << (4 * i + 2));
-    }
-    word[h] = acc;
+    for (int i = 7; i >= 0; --i) kivi_push2(make_float2(x[16 * h + 2 * i], x[16 * h + 2 * i + 1]), kc, kc, acc);
+    word[h] = ~acc;
   }
   reinterpret_cast<uint2 *>(a.codes + slot * (kD / 4))[grp] = make_uint2(word[0], word[1]);
 }
