@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a) 
 // exchange between lanes. Its 64 code bits are bytes 8 (L mod 4) .. + 7 of the token's record.
 constexpr int kTokRun = 8;
 template <bool BF16>
-__global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a) {
+// (six blocks of 256 per SM: 40 registers; the loads' latency, not the arithmetic, leads)
+__global__ void __launch_bounds__(256, 6) kivi_flush_per_token(KiviTensorArgs a) {
   const int lane = threadIdx.x & 31;
   const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
   const uint32_t bh = fast_div(unit, a.div_units);
@@ -343,32 +344,40 @@ __global__ void __launch_bounds__(256) kivi_flush_per_token(KiviTensorArgs a) {
   reinterpret_cast<uint2 *>(a.codes + slot * (kD / 4))[grp] = make_uint2(word[0], word[1]);
 }
 
-// one warp per (batch, head, new token t >= t_first): window tokens go to the bf16 ring.
-// Tokens j < nq(n1) are quantised, and nq(n1) > n1 - W - G, so only the last W + G - 1 new
-// tokens can stay in the window: t_first = max(0, n_new - (W + G - 1)).
-__global__ void __launch_bounds__(256) kivi_window_write(KiviTensorArgs a, int t_first) {
+// Window tokens go to the bf16 ring. Tokens j < nq(n1) are quantised, and nq(n1) > n1 - W - G,
+// so only the last W + G - 1 new tokens can stay in the window: t_first = max(0, n_new - (W + G -
+// 1)). One warp per (batch, head, run of kWinRun new tokens from t_first on); a half-warp moves
+// one token row, 16 bytes (8 channels) per lane.
+constexpr int kWinRun = 8;
+__global__ void __launch_bounds__(256) kivi_window_write(KiviTensorArgs a, int t_first, FastDiv div_runs) {
   const int lane = threadIdx.x & 31;
-  const long long unit = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int span = a.n_new - t_first;
-  const long long bh = unit / span;
-  if (bh >= (long long)a.batch * a.heads) return;
-  const int t = t_first + (int)(unit % span);
-  const int b = (int)(bh / a.heads);
-  const int n0 = __ldg(a.seq_lens + b);
+  const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
+  const uint32_t bh = fast_div(unit, div_runs);
+  if (bh >= (uint32_t)(a.batch * a.heads)) return;
+  const int n0 = __ldg(a.seq_lens + fast_div(bh, a.div_heads));
   const int n1 = n0 + a.n_new;
   if (n1 > a.capacity) return;
-  const int j = n0 + t;
-  if (j < kivi_nq(n1, a.window)) return;
-  float x[4];
-  load4(a.x, ((size_t)bh * a.n_new + t) * kD + 4 * lane, a.bf16 != 0, x);
+  const int nq1 = kivi_nq(n1, a.window);
   const int R = a.window + kG;
-  uint16_t h[4];
+  const int t0 = t_first + kWinRun * (int)(unit - bh * div_runs.d);
+  const int piece = lane & 15;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) h[c] = __bfloat16_as_ushort(__float2bfloat16_rn(x[c]));
-  uint2 w;
-  w.x = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
-  w.y = (uint32_t)h[2] | ((uint32_t)h[3] << 16);
-  reinterpret_cast<uint2 *>(a.ring + ((size_t)bh * R + (j % R)) * kD)[lane] = w;
+  for (int i = 0; i < kWinRun / 2; ++i) {
+    const int t = t0 + 2 * i + (lane >> 4);
+    const int j = n0 + t;
+    if (t >= a.n_new || j < nq1) continue;
+    const size_t row = ((size_t)bh * a.n_new + t) * kD;
+    uint4 w;
+    if (a.bf16) {
+      w = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.x) + row) + piece);
+    } else {
+      const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(a.x) + row) + 2 * piece;
+      const float4 f0 = __ldg(src), f1 = __ldg(src + 1);
+      w = make_uint4(bf162_bits(__floats2bfloat162_rn(f0.x, f0.y)), bf162_bits(__floats2bfloat162_rn(f0.z, f0.w)),
+                     bf162_bits(__floats2bfloat162_rn(f1.x, f1.y)), bf162_bits(__floats2bfloat162_rn(f1.z, f1.w)));
+    }
+    reinterpret_cast<uint4 *>(a.ring + ((size_t)bh * R + (j % R)) * kD)[piece] = w;
+  }
 }
 
 struct KiviDequantKernelArgs {
@@ -430,8 +439,9 @@ int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
     else kivi_flush_per_token<false><<<blocks, 256, 0, st>>>(t);
   }
   const int t_first = std::max(0, t.n_new - (t.window + kG - 1));
-  const long long wwarps = bh * (t.n_new - t_first);
-  kivi_window_write<<<(unsigned)((wwarps + 7) / 8), 256, 0, st>>>(t, t_first);
+  const int runs = (t.n_new - t_first + kWinRun - 1) / kWinRun;
+  const long long wwarps = bh * runs;
+  kivi_window_write<<<(unsigned)((wwarps + 7) / 8), 256, 0, st>>>(t, t_first, make_fastdiv((uint32_t)runs));
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
