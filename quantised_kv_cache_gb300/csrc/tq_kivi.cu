@@ -263,8 +263,9 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a) 
 // exchange between lanes. Its 64 code bits are bytes 8 (L mod 4) .. + 7 of the token's record.
 constexpr int kTokRun = 8;
 template <bool BF16>
-// (six blocks of 256 per SM: 40 registers; the loads' latency, not the arithmetic, leads)
-__global__ void __launch_bounds__(256, 6) kivi_flush_per_token(KiviTensorArgs a) {
+// (bfloat16: six blocks of 256 per SM, 40 registers; the loads' latency, not the arithmetic,
+// leads)
+__global__ void __launch_bounds__(256, BF16 ? 6 : 4) kivi_flush_per_token(KiviTensorArgs a) {
   const int lane = threadIdx.x & 31;
   const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
   const uint32_t bh = fast_div(unit, a.div_units);
