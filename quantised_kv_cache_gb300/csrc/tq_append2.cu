@@ -1,16 +1,20 @@
-// Append-quantise of unrotated vectors (the KV scheme's keys and values) with one
-// thread per vector.
+// Append-quantise of unrotated vectors (the KV scheme's keys and values), one warp per
+// token pair.
 //
 // "Statistical Inference ... Inspired by TurboQuant", technical summary,
 // "Quantisation schemes": the KV scheme codes each coordinate of the normalised
 // vector with the Lloyd-Max codebook, without rotation; "KVQuant++", "Fast
 // codebook lookup": the code is a boundary count, found by binary search.
 //
-// A thread holds its whole 128-coordinate vector in registers and does not divide
-// it by its norm: it compares against its own scaled boundaries nu * b_j, which
-// decides every code exactly as x / nu against b_j would. The boundaries are
-// symmetric about 0, so a code is the sign of x plus a binary search of |x| over
-// the positive boundaries. (Rotated roles take the tensor-core kernels.)
+// A warp takes two consecutive stored pairs of a sequence-head (slots 2j and 2j + 1 are the
+// unit the value layout interleaves) and the tokens of them that this append writes; lane L
+// holds coordinates 4L..4L+3 of each, every row loaded (coalesced) before any is coded. The vector is not divided by its
+// norm: each coordinate is compared against the scaled boundaries nu * b_j, which decides
+// every code exactly as x / nu against b_j would. The boundaries are symmetric about 0, so a
+// code is the sign of x plus a binary search of |x| over the positive boundaries. Key records
+// and value rows are assembled from the lanes' codes by shuffles and written as whole words;
+// a value row whose other token is not part of this append keeps that token's bits (the warp
+// is the row's only writer in the launch). (Rotated roles take the tensor-core kernels.)
 
 #include "tq_device.cuh"
 
@@ -33,6 +37,7 @@ struct Append2Args {
   const float *side_ur;
   float bounds[kMaxLevels];     // 2^BITS - 1 used
   float centroids[kMaxLevels];  // 2^BITS used (side codes)
+  FastDiv div_pairs, div_heads;  // by the warps (groups of token pairs) per sequence-head, and by heads
 };
 
 
@@ -54,146 +59,196 @@ __device__ __forceinline__ int count_pos(float a, const float (&P)[H]) {
   }
 }
 
-template <int BITS, bool BF16>
-__global__ void __launch_bounds__(128) append2_kernel(const __grid_constant__ Append2Args a) {
-  constexpr int L = 1 << BITS, H = L / 2 - 1;
-  const long long total = (long long)a.batch * a.heads * a.n_new;
-  for (long long vec = (long long)blockIdx.x * blockDim.x + threadIdx.x; vec < total;
-       vec += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(vec % a.n_new);
-    const long long bh = vec / a.n_new;
-    const int b = (int)(bh / a.heads);
-    const int len = __ldg(a.seq_lens + b);
-    const bool ok = len >= 0 && len + a.n_new <= a.capacity;  // a sequence that would not fit is skipped whole
-    if (!ok) {
-      if (t == 0) set_error(a.error, TQ_ERR_CAPACITY);
-      continue;
-    }
-    const long long slot = phys_slot(a.btab, a.pool_blocks, bh * a.cap16 + len + t, a.error);
-    if (slot < 0) continue;
-    const int head = (int)(bh % a.heads);
+// Word `lane` (lanes < 8 VB) of a pair row of the value layout: coordinate c's field
+// o = vt_field(c) = 16 (c mod 8) + c / 8 holds 2 VB bits, the even token's code low. Lane L
+// contributes the fields of its coordinates 4L + k, packed as `both` (field k at bit 2 VB k):
+// field o comes from lane 2 (o mod 16) + o / 64, position (o / 16) mod 4.
+template <int VB>
+__device__ __forceinline__ uint32_t vt_row_word(uint32_t both, int lane) {
+  constexpr int F = 2 * VB;
+  constexpr int K = (32 + F - 1) / F + 1;  // fields touching one word
+  const int first = (32 * lane) / F;
+  uint32_t word = 0;
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const int o = first + i;
+    const int src = 2 * (o & 15) + ((o >> 6) & 1);
+    const uint32_t v = __shfl_sync(kFull, both, src);
+    const uint32_t f = (v >> (F * ((o >> 4) & 3))) & ((1u << F) - 1u);
+    const int shift = F * o - 32 * lane;
+    if (o < 128 && shift > -F && shift < 32) word |= (shift >= 0) ? (f << shift) : (f >> (-shift));
+  }
+  return word;
+}
+// the bits of word `lane` of a pair row that belong to token half h (VB ones per field)
+template <int VB>
+__device__ __forceinline__ uint32_t vt_row_half_mask(int h, int lane) {
+  constexpr int F = 2 * VB;
+  constexpr int K = (32 + F - 1) / F + 1;
+  const int first = (32 * lane) / F;
+  const uint32_t f = ((1u << VB) - 1u) << (VB * h);
+  uint32_t word = 0;
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const int o = first + i;
+    const int shift = F * o - 32 * lane;
+    if (o < 128 && shift > -F && shift < 32) word |= (shift >= 0) ? (f << shift) : (f >> (-shift));
+  }
+  return word;
+}
 
-    float x[kD];
-    if (BF16) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.x) + vec * kD);
+// kPairs consecutive pairs of one sequence-head per warp, all rows loaded before any is coded
+constexpr int kPairs = 2;
+
+// The same two assemblies when a field's 2 BITS bits divide 32 (BITS = 2, 4): a word holds
+// n = 16 / BITS whole fields, all from one half (key records) or one position (value rows),
+// and its sources are n lanes two apart, so each field costs a shuffle, a shift and an add.
+// Key record word w (lanes < 4 BITS): slots n w + i, i < n, the field (low: pair 2L, high:
+// pair 2L + 1) of lane 2 ((n w + i) mod 16) + (n w) / 32, half ((n w) / 16) mod 2.
+template <int BITS>
+__device__ __forceinline__ uint32_t key_word_even(uint32_t both, int lane) {
+  constexpr int F = 2 * BITS, N = 32 / F;
+  const int s = N * lane;
+  const int src = 2 * (s & 15) + ((s >> 5) & 1);
+  const int sh = F * ((s >> 4) & 1);
+  uint32_t word = 0;
 #pragma unroll
-      for (int k = 0; k < kD / 8; ++k) {
-        const uint4 w = __ldg(src + k);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  for (int i = 0; i < N; ++i) {
+    const uint32_t v = __shfl_sync(kFull, both, (src + 2 * i) & 31);
+    word += ((v >> sh) & ((1u << F) - 1u)) << (F * i);
+  }
+  return word;
+}
+// Value row word w (lanes < 8 BITS): fields o = n w + i, from lane 2 (o mod 16) + o / 64,
+// position (o / 16) mod 4 of that lane's four fields.
+template <int BITS>
+__device__ __forceinline__ uint32_t vt_word_even(uint32_t both, int lane) {
+  constexpr int F = 2 * BITS, N = 32 / F;
+  const int o = N * lane;
+  const int src = 2 * (o & 15) + ((o >> 6) & 1);
+  const int sh = F * ((o >> 4) & 3);
+  uint32_t word = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          x[8 * k + 2 * j] = __uint_as_float(ww[j] << 16);
-          x[8 * k + 2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
-        }
+  for (int i = 0; i < N; ++i) {
+    const uint32_t v = __shfl_sync(kFull, both, (src + 2 * i) & 31);
+    word += ((v >> sh) & ((1u << F) - 1u)) << (F * i);
+  }
+  return word;
+}
+
+template <int BITS, bool BF16>
+__global__ void __launch_bounds__(256) append2_kernel(const __grid_constant__ Append2Args a) {
+  constexpr int L = 1 << BITS, H = L / 2 - 1;
+  const int lane = threadIdx.x & 31;
+  const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
+  const uint32_t bh = fast_div(unit, a.div_pairs);
+  if (bh >= (uint32_t)(a.batch * a.heads)) return;
+  const uint32_t b = fast_div(bh, a.div_heads);
+  const int head = (int)(bh - b * (uint32_t)a.heads);
+  const int group = (int)(unit - bh * a.div_pairs.d);
+  const int len = __ldg(a.seq_lens + b);
+  if (len < 0 || len + a.n_new > a.capacity) {  // a sequence that would not fit is skipped whole
+    if (group == 0 && lane == 0) set_error(a.error, TQ_ERR_CAPACITY);
+    return;
+  }
+  // the group's slots from s0 = (len rounded down to even) + 2 kPairs group; the append
+  // writes slots [len, len + n_new)
+  const int s0 = (len & ~1) + 2 * kPairs * group;
+  const int s_end = len + a.n_new;
+  if (s0 >= s_end) return;
+  float x[2 * kPairs][4];
+#pragma unroll
+  for (int i = 0; i < 2 * kPairs; ++i) {
+    const int s = s0 + i;
+    const long long t = (long long)bh * a.n_new + (s - len);  // input row
+    if (s >= len && s < s_end) {
+      if (BF16) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.x) + t * kD) + lane);
+        x[i][0] = __uint_as_float(w.x << 16);
+        x[i][1] = __uint_as_float(w.x & 0xffff0000u);
+        x[i][2] = __uint_as_float(w.y << 16);
+        x[i][3] = __uint_as_float(w.y & 0xffff0000u);
+      } else {
+        const float4 f = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.x) + t * kD) + lane);
+        x[i][0] = f.x;
+        x[i][1] = f.y;
+        x[i][2] = f.z;
+        x[i][3] = f.w;
       }
     } else {
-      const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(a.x) + vec * kD);
 #pragma unroll
-      for (int k = 0; k < kD / 4; ++k) {
-        const float4 f = __ldg(src + k);
-        x[4 * k] = f.x;
-        x[4 * k + 1] = f.y;
-        x[4 * k + 2] = f.z;
-        x[4 * k + 3] = f.w;
-      }
+      for (int j = 0; j < 4; ++j) x[i][j] = 0.f;
     }
-    // squared norm by a pairwise tree (matches the warp design's rounding order closely)
-    float sq[kD / 2];
+  }
 #pragma unroll
-    for (int i = 0; i < kD / 2; ++i) sq[i] = fmaf(x[2 * i], x[2 * i], x[2 * i + 1] * x[2 * i + 1]);
+  for (int p = 0; p < kPairs; ++p) {
+    const int sp = s0 + 2 * p;
+    if (sp >= s_end) break;  // warp-uniform
+    const long long vs = (long long)bh * a.cap16 + sp;
+    long long slot[2];
+    int code[2][4];
 #pragma unroll
-    for (int w = kD / 4; w >= 1; w >>= 1)
+    for (int h = 0; h < 2; ++h) {
+      const bool has = sp + h >= len && sp + h < s_end;
+      slot[h] = has ? phys_slot(a.btab, a.pool_blocks, vs + h, a.error) : -1;
+      const float (&xv)[4] = x[2 * p + h];
+      const float nu = sqrtf(warp_sum(xv[0] * xv[0] + xv[1] * xv[1] + xv[2] * xv[2] + xv[3] * xv[3]));
+      // positive boundaries scaled to this vector: b_{L/2 + k} * nu; a zero vector keeps the
+      // unit boundaries so that x = 0 codes to L/2 as the format requires
+      const float sc = (nu > 0.f) ? nu : 1.f;
+      float P[H];
 #pragma unroll
-      for (int i = 0; i < w; ++i) sq[i] = sq[i] + sq[i + w];
-    const float nu = sqrtf(sq[0]);
-
-    // positive boundaries scaled to this vector: b_{L/2 + k} * nu; a zero vector keeps the
-    // unit boundaries so that y = 0 codes to L/2 as the format requires
-    const float s = (nu > 0.f) ? nu : 1.f;
-    float P[H];
+      for (int k = 0; k < H; ++k) P[k] = a.bounds[L / 2 + k] * sc;
 #pragma unroll
-    for (int k = 0; k < H; ++k) P[k] = a.bounds[L / 2 + k] * s;
-
-    // code i: sign half plus the count of positive boundaries below |y|; nu = 0 gives y = 0 -> L/2
-    uint32_t word[4 * BITS];
-#pragma unroll
-    for (int w = 0; w < 4 * BITS; ++w) word[w] = 0u;
-    // side code of an unsketched key: z_k = nu sum_i U[i][k] (x_i / nu - c[code_i])
-    const int srank = a.side_rank;
-    const float *su = srank ? a.side_ur + (size_t)head * kD * srank : nullptr;
-    const float inv_nu = (nu > 0.f) ? 1.f / nu : 0.f;
-    float zs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < kD; ++i) {
-      const float y = x[i];
-      const int m = count_pos<H>(fabsf(y), P);
-      const int code = (y >= 0.f) ? (L / 2 + m) : (L / 2 - 1 - m);
-      if (srank) {
-        const float r = fmaf(y, inv_nu, -a.centroids[code]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k < srank) zs[k] = fmaf(__ldg(su + i * srank + k), r, zs[k]);
+      for (int j = 0; j < 4; ++j) {
+        const float y = xv[j];
+        const int m = count_pos<H>(fabsf(y), P);
+        code[h][j] = (y >= 0.f) ? (L / 2 + m) : (L / 2 - 1 - m);
       }
-      // slot order: coordinate i = 8n + 2t + e at code offset 32t + 2n + e
-      const int n = i >> 3, tt = (i >> 1) & 3, e = i & 1;
-      const int off = BITS * (32 * tt + 2 * n + e);
-      word[off >> 5] |= (uint32_t)code << (off & 31);
-      if ((off & 31) + BITS > 32) word[(off >> 5) + 1] |= (uint32_t)code >> (32 - (off & 31));
+      if (!a.vt) {  // key record of this token
+        const uint32_t fa = (uint32_t)code[h][0] | ((uint32_t)code[h][1] << BITS);
+        const uint32_t fb = (uint32_t)code[h][2] | ((uint32_t)code[h][3] << BITS);
+        uint32_t word;  // every lane takes part
+        if constexpr (32 % (2 * BITS) == 0) word = key_word_even<BITS>(fa | (fb << (2 * BITS)), lane);
+        else word = pack_slot_word<BITS>(fa, fb, lane);
+        if (slot[h] >= 0 && lane < 4 * BITS)
+          reinterpret_cast<uint32_t *>(rec_at(a.codes, slot[h], a.bb, BITS * kD / 8))[lane] = word;
+      }
+      if (slot[h] >= 0 && lane == 0) *rec_at(a.norms, slot[h], a.bb, 4) = nu;
+      if (a.side_rank) {  // warp-uniform
+        const float inv_nu = (nu > 0.f) ? 1.f / nu : 0.f;
+        float r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) r[j] = fmaf(xv[j], inv_nu, -a.centroids[code[h][j]]);
+        side_code_warp(a.side_ur + (size_t)head * kD * a.side_rank, a.side_rank, nu, r, a.side, slot[h], a.bb, lane);
+      }
     }
     if (a.vt) {
-      // this token's half of every field of its pair row: code offset n = 32 q + 2 m + e
-      // holds coordinate 8 m + 2 q + e, whose field is vt_field() = 32 q + 16 e + m
-      uint32_t *row = vt_row<BITS>(a.codes, slot, a.bb);
-      const int half = (int)(slot & 1);
+      // the pair row: both tokens' codes, this lane's four fields packed
+      uint32_t both = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t cw[32], w[2 * BITS], ones[32], own[2 * BITS];
-#pragma unroll
-        for (int n = 0; n < 32; ++n) {
-          const int off = BITS * (32 * q + n);
-          uint32_t v = word[off >> 5] >> (off & 31);
-          if ((off & 31) + BITS > 32) v |= word[(off >> 5) + 1] << (32 - (off & 31));
-          cw[n] = v & ((1u << BITS) - 1u);
-          ones[n] = (1u << BITS) - 1u;
-        }
-        vt_spread<BITS>(cw, half, w);
-        vt_spread<BITS>(ones, half, own);
-#pragma unroll
-        for (int i = 0; i < 2 * BITS; ++i) {
-          atomicAnd(row + 2 * BITS * q + i, ~own[i]);
-          atomicOr(row + 2 * BITS * q + i, w[i]);
+      for (int j = 0; j < 4; ++j)
+        both |= ((uint32_t)code[0][j] | ((uint32_t)code[1][j] << BITS)) << (2 * BITS * j);
+      uint32_t word;  // every lane takes part
+      if constexpr (32 % (2 * BITS) == 0) word = vt_word_even<BITS>(both, lane);
+      else word = vt_row_word<BITS>(both, lane);
+      const long long any = slot[0] >= 0 ? slot[0] : slot[1];
+      if (any >= 0 && lane < 8 * BITS) {
+        uint32_t *row = vt_row<BITS>(a.codes, any, a.bb);
+        if (slot[0] >= 0 && slot[1] >= 0) {
+          row[lane] = word;
+        } else {  // one token of the pair: keep the other token's bits
+          const uint32_t mine = vt_row_half_mask<BITS>(slot[0] >= 0 ? 0 : 1, lane);
+          row[lane] = (row[lane] & ~mine) | (word & mine);
         }
       }
-    } else {
-      uint4 *dst = reinterpret_cast<uint4 *>(rec_at(a.codes, slot, a.bb, BITS * kD / 8));
-#pragma unroll
-      for (int k = 0; k < BITS; ++k) dst[k] = make_uint4(word[4 * k], word[4 * k + 1], word[4 * k + 2], word[4 * k + 3]);
-    }
-    *rec_at(a.norms, slot, a.bb, 4) = nu;
-    if (srank) {
-      uint16_t *zp = rec_at(a.side, slot, a.bb, 2 * srank);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (k < srank) zp[k] = __half_as_ushort(__float2half_rn(zs[k] * nu));
     }
   }
 }
 
-int g_sms2 = 0;
-
 template <int BITS, bool BF16>
-int go(const Append2Args &k, long long total, cudaStream_t st) {
-  if (g_sms2 == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms2, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms2 <= 0) g_sms2 = 152;
-  }
-  long long blocks = (total + 127) / 128;
-  const long long cap = 4LL * g_sms2;  // enough resident threads to cover memory latency
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  append2_kernel<BITS, BF16><<<(unsigned)blocks, 128, 0, st>>>(k);
+int go(const Append2Args &k, long long warps, cudaStream_t st) {
+  append2_kernel<BITS, BF16><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(k);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -209,7 +264,7 @@ int dispatch(int bits, const Append2Args &k, long long total, cudaStream_t st) {
 
 }  // namespace
 
-// Thread-per-vector append for vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise.
+// Warp-per-pair append for unrotated vectors without a sketch; TQ_ERR_UNSUPPORTED otherwise.
 int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   if (a.role.qjl || a.role.rotate || a.role.bits < 2) return TQ_ERR_UNSUPPORTED;
   Append2Args k{};
@@ -235,10 +290,17 @@ int launch_append2(const AppendArgs &a, const tq_ctx *ctx, void *stream) {
   k.side_rank = a.side_rank;
   k.side = a.side;
   k.side_ur = a.side_ur;
-  const long long total = (long long)a.batch * a.heads * a.n_new;
+  // pairs of slots touched per sequence-head: [len rounded down to even, len + n_new), in
+  // groups of kPairs per warp
+  const int pairs = a.n_new / 2 + 1;
+  const int groups = (pairs + kPairs - 1) / kPairs;
+  const long long warps = (long long)a.batch * a.heads * groups;
+  if (warps >= 0xffffffffLL - 8) return TQ_ERR_ARG;  // warp indices are 32-bit
+  k.div_pairs = make_fastdiv((uint32_t)groups);
+  k.div_heads = make_fastdiv((uint32_t)a.heads);
   cudaStream_t st = (cudaStream_t)stream;
   const bool bf16 = a.dtype == TQ_BF16;
-  return bf16 ? dispatch<true>(a.role.bits, k, total, st) : dispatch<false>(a.role.bits, k, total, st);
+  return bf16 ? dispatch<true>(a.role.bits, k, warps, st) : dispatch<false>(a.role.bits, k, warps, st);
 }
 
 }  // namespace tq
