@@ -59,27 +59,6 @@ __device__ __forceinline__ int count_pos(float a, const float (&P)[H]) {
   }
 }
 
-// Word `lane` (lanes < 8 VB) of a pair row of the value layout: coordinate c's field
-// o = vt_field(c) = 16 (c mod 8) + c / 8 holds 2 VB bits, the even token's code low. Lane L
-// contributes the fields of its coordinates 4L + k, packed as `both` (field k at bit 2 VB k):
-// field o comes from lane 2 (o mod 16) + o / 64, position (o / 16) mod 4.
-template <int VB>
-__device__ __forceinline__ uint32_t vt_row_word(uint32_t both, int lane) {
-  constexpr int F = 2 * VB;
-  constexpr int K = (32 + F - 1) / F + 1;  // fields touching one word
-  const int first = (32 * lane) / F;
-  uint32_t word = 0;
-#pragma unroll
-  for (int i = 0; i < K; ++i) {
-    const int o = first + i;
-    const int src = 2 * (o & 15) + ((o >> 6) & 1);
-    const uint32_t v = __shfl_sync(kFull, both, src);
-    const uint32_t f = (v >> (F * ((o >> 4) & 3))) & ((1u << F) - 1u);
-    const int shift = F * o - 32 * lane;
-    if (o < 128 && shift > -F && shift < 32) word |= (shift >= 0) ? (f << shift) : (f >> (-shift));
-  }
-  return word;
-}
 // the bits of word `lane` of a pair row that belong to token half h (VB ones per field)
 template <int VB>
 __device__ __forceinline__ uint32_t vt_row_half_mask(int h, int lane) {
@@ -100,11 +79,15 @@ __device__ __forceinline__ uint32_t vt_row_half_mask(int h, int lane) {
 // kPairs consecutive pairs of one sequence-head per warp, all rows loaded before any is coded
 constexpr int kPairs = 2;
 
-// The same two assemblies when a field's 2 BITS bits divide 32 (BITS = 2, 4): a word holds
-// n = 16 / BITS whole fields, all from one half (key records) or one position (value rows),
-// and its sources are n lanes two apart, so each field costs a shuffle, a shift and an add.
-// Key record word w (lanes < 4 BITS): slots n w + i, i < n, the field (low: pair 2L, high:
-// pair 2L + 1) of lane 2 ((n w + i) mod 16) + (n w) / 32, half ((n w) / 16) mod 2.
+// Records and pair rows are assembled from the lanes' codes by shuffles. Every lane packs its
+// two pair fields (key records: pair 2L low, pair 2L + 1 high) or its four coordinate fields
+// (value rows: coordinate 4L + k at field k) into one word, 2 BITS bits a field. Key record
+// slot s (pair p = 4n + t at slot 16t + n) is lane 2 (s mod 16) + (s / 32) mod 2's field
+// (s / 16) mod 2; value row field o = vt_field(c) is lane 2 (o mod 16) + o / 64's field
+// (o / 16) mod 4. When a field's 2 BITS bits divide 32 (BITS = 2, 4), a word holds
+// n = 16 / BITS whole fields, all at one position of their lanes, from n lanes two apart, so
+// each field costs a shuffle, a shift and an add.
+// Key record word w (lanes < 4 BITS): slots n w + i, i < n.
 template <int BITS>
 __device__ __forceinline__ uint32_t key_word_even(uint32_t both, int lane) {
   constexpr int F = 2 * BITS, N = 32 / F;
@@ -134,6 +117,32 @@ __device__ __forceinline__ uint32_t vt_word_even(uint32_t both, int lane) {
     word += ((v >> sh) & ((1u << F) - 1u)) << (F * i);
   }
   return word;
+}
+
+// 3-bit codes (6-bit fields): 16 consecutive fields fill exactly three words, so word j of such
+// a group takes fields i0 = 32 j / 6 .. i0 + 5 (from lanes src0 + 2 i, at shift sh of their
+// packed fields), gathered in 64 bits and shifted right by 32 j - 6 i0.
+__device__ __forceinline__ uint32_t word6(uint32_t both, int src0, int sh, int j) {
+  const int i0 = (32 * j) / 6;
+  uint64_t acc = 0;
+#pragma unroll
+  for (int k = 0; k < 6; ++k) {
+    const uint32_t v = __shfl_sync(kFull, both, (src0 + 2 * (i0 + k)) & 31);
+    acc |= (uint64_t)((v >> sh) & 63u) << (6 * k);
+  }
+  return (uint32_t)(acc >> (32 * j - 6 * i0));
+}
+// key record word w (lanes < 12): group G = w / 3 of 16 slots (a fields of even lanes, b of
+// even, a of odd, b of odd)
+__device__ __forceinline__ uint32_t key_word6(uint32_t both, int lane) {
+  const int G = lane / 3, j = lane - 3 * (lane / 3);
+  return word6(both, (G >> 1) & 1, 6 * (G & 1), j);
+}
+// value row word w (lanes < 24): fields o = 16 m + i, m = w / 3, from lanes 2 i + m / 4,
+// position m mod 4
+__device__ __forceinline__ uint32_t vt_word6(uint32_t both, int lane) {
+  const int m = lane / 3, j = lane - 3 * (lane / 3);
+  return word6(both, (m >> 2) & 1, 6 * (m & 3), j);
 }
 
 template <int BITS, bool BF16>
@@ -210,7 +219,7 @@ __global__ void __launch_bounds__(256) append2_kernel(const __grid_constant__ Ap
         const uint32_t fb = (uint32_t)code[h][2] | ((uint32_t)code[h][3] << BITS);
         uint32_t word;  // every lane takes part
         if constexpr (32 % (2 * BITS) == 0) word = key_word_even<BITS>(fa | (fb << (2 * BITS)), lane);
-        else word = pack_slot_word<BITS>(fa, fb, lane);
+        else word = key_word6(fa | (fb << (2 * BITS)), lane);
         if (slot[h] >= 0 && lane < 4 * BITS)
           reinterpret_cast<uint32_t *>(rec_at(a.codes, slot[h], a.bb, BITS * kD / 8))[lane] = word;
       }
@@ -231,7 +240,7 @@ __global__ void __launch_bounds__(256) append2_kernel(const __grid_constant__ Ap
         both |= ((uint32_t)code[0][j] | ((uint32_t)code[1][j] << BITS)) << (2 * BITS * j);
       uint32_t word;  // every lane takes part
       if constexpr (32 % (2 * BITS) == 0) word = vt_word_even<BITS>(both, lane);
-      else word = vt_row_word<BITS>(both, lane);
+      else word = vt_word6(both, lane);
       const long long any = slot[0] >= 0 ? slot[0] : slot[1];
       if (any >= 0 && lane < 8 * BITS) {
         uint32_t *row = vt_row<BITS>(a.codes, any, a.bb);
