@@ -1,5 +1,5 @@
-// Append-quantise of unrotated vectors (the KV scheme's keys and values), one warp per
-// token pair.
+// Append-quantise of unrotated vectors (the KV scheme's keys and values), one warp per two
+// token pairs.
 //
 // "Statistical Inference ... Inspired by TurboQuant", technical summary,
 // "Quantisation schemes": the KV scheme codes each coordinate of the normalised
@@ -8,13 +8,14 @@
 //
 // A warp takes two consecutive stored pairs of a sequence-head (slots 2j and 2j + 1 are the
 // unit the value layout interleaves) and the tokens of them that this append writes; lane L
-// holds coordinates 4L..4L+3 of each, every row loaded (coalesced) before any is coded. The vector is not divided by its
-// norm: each coordinate is compared against the scaled boundaries nu * b_j, which decides
-// every code exactly as x / nu against b_j would. The boundaries are symmetric about 0, so a
-// code is the sign of x plus a binary search of |x| over the positive boundaries. Key records
-// and value rows are assembled from the lanes' codes by shuffles and written as whole words;
-// a value row whose other token is not part of this append keeps that token's bits (the warp
-// is the row's only writer in the launch). (Rotated roles take the tensor-core kernels.)
+// holds coordinates 4L..4L+3 of each, every row loaded (coalesced) before any is coded. The
+// vector is not divided by its norm: each coordinate is compared against the scaled
+// boundaries nu * b_j, which decides every code exactly as x / nu against b_j would. The
+// boundaries are symmetric about 0, so a code is the sign of x plus a binary search of |x|
+// over the positive boundaries. Key records and value rows are assembled from the lanes'
+// codes by shuffles and written as whole words; a value row whose other token is not part of
+// this append keeps that token's bits (the warp is the row's only writer in the launch).
+// (Rotated roles take the tensor-core kernels.)
 
 #include "tq_device.cuh"
 
@@ -26,7 +27,7 @@ struct Append2Args {
   int batch, heads, n_new, capacity, cap16, bb;
   const int32_t *btab;  // paged caches (NULL: contiguous)
   int pool_blocks;
-  int vt;  // value role: codes in the pair-interleaved layout (merged atomically)
+  int vt;  // value role: codes in the pair-interleaved layout
   const int32_t *seq_lens;
   uint8_t *codes;
   float *norms;

@@ -261,10 +261,10 @@ __global__ void __launch_bounds__(256) kivi_flush_per_channel(KiviTensorArgs a) 
 // one warp per (batch, head, run of kTokRun = 8 consecutive tokens); lane L codes group L mod 4
 // (channels 32 (L mod 4) .. + 31) of token L / 4 by itself: statistics, step and codes, no
 // exchange between lanes. Its 64 code bits are bytes 8 (L mod 4) .. + 7 of the token's record.
+// (bfloat16: six blocks of 256 per SM, 40 registers; the loads' latency, not the arithmetic,
+// leads.)
 constexpr int kTokRun = 8;
 template <bool BF16>
-// (bfloat16: six blocks of 256 per SM, 40 registers; the loads' latency, not the arithmetic,
-// leads)
 __global__ void __launch_bounds__(256, BF16 ? 6 : 4) kivi_flush_per_token(KiviTensorArgs a) {
   const int lane = threadIdx.x & 31;
   const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
@@ -290,11 +290,11 @@ __global__ void __launch_bounds__(256, BF16 ? 6 : 4) kivi_flush_per_token(KiviTe
     uint32_t w[kG / 2];
 #pragma unroll
     for (int i = 0; i < kG / 8; ++i) {
-      const uint4 u = __ldg(src + i);
-      w[4 * i] = u.x;
-      w[4 * i + 1] = u.y;
-      w[4 * i + 2] = u.z;
-      w[4 * i + 3] = u.w;
+      const uint4 q4 = __ldg(src + i);
+      w[4 * i] = q4.x;
+      w[4 * i + 1] = q4.y;
+      w[4 * i + 2] = q4.z;
+      w[4 * i + 3] = q4.w;
     }
     __nv_bfloat162 lo = as_bf162(w[0]), hi = lo;
 #pragma unroll
