@@ -450,6 +450,30 @@ def run_workload_decode(args, dev):
     print(json.dumps({"case": args.case, "ok": True}), flush=True)
 
 
+def run_workload_append(args, dev):
+    """Bulk appends on one of the other workloads, for profiler captures: the KIVI layout study
+    (B8 H40 context 4096, bf16, per-channel keys and per-token values) or the scheme sweep's
+    unrotated KV scheme at 4 bits (B4 H8 context 16384, fp32). Each step re-appends the whole
+    context from sequence length 0."""
+    import torch
+    from quantised_kv_cache_gb300 import tq
+    from quantised_kv_cache_gb300 import workloads as wl
+    wid = 5 if args.case == "kivi-append" else 3
+    w = wl.WORKLOADS[wid]
+    if wid == 5:
+        ctx = tq.Context(128, 2, "KIVI", 42, k_per_channel=True, v_per_token=True)
+    else:
+        ctx = tq.Context(128, 4, "KV", 42)
+    _, k, v = wl.generate(w, dev)
+    cache = tq.Cache(ctx, w.batch, w.heads_kv, w.seq, device=dev)
+    zeros = torch.zeros((w.batch,), dtype=torch.int32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        tq.tq_append_quantize(ctx.handle, cache, k, v, zeros)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ctx.handle) == 0
+    print(json.dumps({"case": args.case, "ok": True}), flush=True)
+
+
 def run_small_case(args, dev):
     """A smaller instance of the Llama-2-7B-shaped workload for profiler captures:
     B16 H32 context 4096 (294 MB of compressed records, 537 MB of bf16 K/V)."""
@@ -458,6 +482,9 @@ def run_small_case(args, dev):
     from quantised_kv_cache_gb300 import workloads as wl
     if args.case in ("gqa-decode", "kivi-decode"):
         run_workload_decode(args, dev)
+        return
+    if args.case in ("kivi-append", "kv-append"):
+        run_workload_append(args, dev)
         return
     w = wl.WORKLOADS[2]
     N = 4096
@@ -605,11 +632,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table of the N=1 line")
-    ap.add_argument("--case", choices=["step", "decode-small", "append-small", "gqa-decode", "kivi-decode", "configs"],
+    ap.add_argument("--case", choices=["step", "decode-small", "append-small", "gqa-decode", "kivi-decode",
+                                       "kivi-append", "kv-append", "configs"],
                     default="step",
                     help="step: the benchmark; *-small: one kernel family on B16 H32 N4096 (294 MB of records, "
                          "above L2) for profiler captures; gqa-decode / kivi-decode: decode calls of the GQA "
-                         "and KIVI workloads, for profiler captures")
+                         "and KIVI workloads, kivi-append / kv-append: bulk appends of the KIVI workload and "
+                         "of the scheme sweep's KV scheme at 4 bits, for profiler captures")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
