@@ -8,11 +8,12 @@
 //
 // Append of n_new tokens to a sequence holding N0 tokens, N = N0 + n_new:
 // the window rule leaves tokens [0, nq(N)) quantised and [nq(N), N) in the
-// window, nq(N) = G floor((N - W) / G) once N >= W + G. Two stream-ordered
-// launches per tensor keep the ring consistent:
-//   flush  -- quantise every group in [nq(N0), nq(N)), reading tokens < N0
-//             from the ring and later ones from the input;
-//   window -- copy tokens [max(nq(N), N0), N) from the input into the ring.
+// window, nq(N) = G floor((N - W) / G) once N >= W + G. Stream-ordered launches
+// keep each ring consistent:
+//   flush  -- (one per tensor) quantise every group in [nq(N0), nq(N)), reading
+//             tokens < N0 from the ring and later ones from the input;
+//   window -- (one for both tensors, after both flushes) copy tokens
+//             [max(nq(N), N0), N) from the input into the ring.
 
 #include <cuda_fp16.h>
 
@@ -350,7 +351,13 @@ __global__ void __launch_bounds__(256, BF16 ? 6 : 4) kivi_flush_per_token(KiviTe
 // 1)). One warp per (batch, head, run of kWinRun new tokens from t_first on); a half-warp moves
 // one token row, 16 bytes (8 channels) per lane.
 constexpr int kWinRun = 8;
-__global__ void __launch_bounds__(256) kivi_window_write(KiviTensorArgs a, int t_first, FastDiv div_runs) {
+// (one launch for both tensors: blockIdx.y = 0 keys, 1 values)
+struct KiviWindowArgs {
+  KiviTensorArgs t[2];
+};
+__global__ void __launch_bounds__(256) kivi_window_write(const __grid_constant__ KiviWindowArgs w, int t_first,
+                                                         FastDiv div_runs) {
+  const KiviTensorArgs &a = w.t[blockIdx.y];
   const int lane = threadIdx.x & 31;
   const uint32_t unit = blockIdx.x * 8u + (threadIdx.x >> 5);
   const uint32_t bh = fast_div(unit, div_runs);
@@ -422,7 +429,7 @@ __global__ void __launch_bounds__(256) kivi_dequant_kernel(KiviDequantKernelArgs
   reinterpret_cast<float4 *>(a.out + (size_t)vec * kD)[lane] = make_float4(y[0], y[1], y[2], y[3]);
 }
 
-int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
+int flush(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
   const long long bh = (long long)t.batch * t.heads;
   // groups (or tokens) newly quantised by one append: at most (n_new + G - 1) tokens
   const int max_tokens = t.n_new + kG - 1;
@@ -430,7 +437,6 @@ int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
   const long long warps = bh * units;
   if (warps >= 0xffffffffLL - 8) return TQ_ERR_ARG;  // warp indices are 32-bit
   t.div_units = make_fastdiv((uint32_t)units);
-  t.div_heads = make_fastdiv((uint32_t)t.heads);
   const unsigned blocks = (unsigned)((warps + 7) / 8);
   if (per_channel) {
     if (t.bf16) kivi_flush_per_channel<true><<<blocks, 256, 0, st>>>(t);
@@ -439,10 +445,17 @@ int flush_and_window(KiviTensorArgs t, bool per_channel, cudaStream_t st) {
     if (t.bf16) kivi_flush_per_token<true><<<blocks, 256, 0, st>>>(t);
     else kivi_flush_per_token<false><<<blocks, 256, 0, st>>>(t);
   }
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+// window tokens of both tensors; after both flushes (each tensor's flush reads its ring first)
+int window(const KiviWindowArgs &w, cudaStream_t st) {
+  const KiviTensorArgs &t = w.t[0];
+  const long long bh = (long long)t.batch * t.heads;
   const int t_first = std::max(0, t.n_new - (t.window + kG - 1));
   const int runs = (t.n_new - t_first + kWinRun - 1) / kWinRun;
   const long long wwarps = bh * runs;
-  kivi_window_write<<<(unsigned)((wwarps + 7) / 8), 256, 0, st>>>(t, t_first, make_fastdiv((uint32_t)runs));
+  kivi_window_write<<<dim3((unsigned)((wwarps + 7) / 8), 2), 256, 0, st>>>(w, t_first, make_fastdiv((uint32_t)runs));
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -462,17 +475,21 @@ int launch_append_kivi(const KiviAppendArgs &a, void *stream) {
   t.window = ctx->kivi_window;
   t.seq_lens = a.seq_lens;
   t.error = a.error;
-  t.x = a.k;
-  t.codes = c->k_codes;
-  t.stats = c->k_stats;
-  t.ring = c->k_window;
-  int r = flush_and_window(t, ctx->kivi_k_per_channel != 0, st);
-  if (r != TQ_OK) return r;
-  t.x = a.v;
-  t.codes = c->v_codes;
-  t.stats = c->v_stats;
-  t.ring = c->v_window;
-  return flush_and_window(t, ctx->kivi_v_per_token == 0, st);
+  t.div_heads = make_fastdiv((uint32_t)a.heads);
+  KiviWindowArgs w{};
+  w.t[0] = w.t[1] = t;
+  w.t[0].x = a.k;
+  w.t[0].codes = c->k_codes;
+  w.t[0].stats = c->k_stats;
+  w.t[0].ring = c->k_window;
+  w.t[1].x = a.v;
+  w.t[1].codes = c->v_codes;
+  w.t[1].stats = c->v_stats;
+  w.t[1].ring = c->v_window;
+  int r = flush(w.t[0], ctx->kivi_k_per_channel != 0, st);
+  if (r == TQ_OK) r = flush(w.t[1], ctx->kivi_v_per_token == 0, st);
+  if (r == TQ_OK) r = window(w, st);
+  return r;
 }
 
 int launch_dequant_kivi(const KiviDequantArgs &a, void *stream) {
